@@ -1,0 +1,92 @@
+"""Plant plausible mistakes in copies of the oracle and check that a pin catches each.
+
+Every mutant is the oracle's C source with one edit (a dropped term, a wrong
+sign, a wrong index, a swapped operand), compiled on the CPU into a temporary
+directory.  The pins of test_oracle.py run against it; at least one of them
+must fail.  The oracle itself is never modified.
+"""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle as pins
+
+MUTANTS = {
+    "rope_sign": ("x[i] = a * c - b * s;", "x[i] = a * c + b * s;"),
+    "rope_freq": ("pow(theta, -2.0 * (double)i / (double)D)",
+                  "pow(theta, -1.0 * (double)i / (double)D)"),
+    "rope_pairing": ("double a = x[i], b = x[i + half];", "double a = x[i], b = x[half - 1 - i];"),
+    "gqa_map": ("const int32_t kvh = h / group;", "const int32_t kvh = h % Hk;"),
+    "causal_off_by_one": ("if (causal && j > qpos)", "if (causal && j >= qpos)"),
+    "query_alignment": ("const int64_t qpos = L - qo_len + (t - qo_indptr[b]);",
+                        "const int64_t qpos = (t - qo_indptr[b]);"),
+    "page_offset": ("const int64_t page = indices[indptr[b] + j / P];\n"
+                    "        const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;\n"
+                    "        for (int32_t d = 0; d < D; ++d) kv[d]",
+                    "const int64_t page = indices[j / P];\n"
+                    "        const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;\n"
+                    "        for (int32_t d = 0; d < D; ++d) kv[d]"),
+    "head_page_layout": ("const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;\n"
+                         "        for (int32_t d = 0; d < D; ++d) kv[d]",
+                         "const int64_t off = ((page * P + j % P) * Hk + kvh) * (int64_t)D;\n"
+                         "        for (int32_t d = 0; d < D; ++d) kv[d]"),
+    "last_page_len": ("return (n - 1) * page_size + last_page_len[b];", "return n * page_size;"),
+    "lse_drops_max": ("const double l = m + log(sum);", "const double l = log(sum);"),
+    "scale_dropped": ("scores[j] = sm_scale * dot;", "scores[j] = dot;"),
+    "v_reads_k": ("o[d] += p * bf16_bits_to_double(v_pages[off + d]);",
+                  "o[d] += p * bf16_bits_to_double(k_pages[off + d]);"),
+    "merge_weight": ("wb * o_b[r * D + d]", "wa * o_b[r * D + d]"),
+    "merge_lse": ("const double l = M + log(exp(a - M) + exp(b - M));",
+                  "const double l = M + log(exp(a - M) + exp(b - M) + 1.0);"),
+    "append_pos": ("const int64_t pos = L - n_new + i;", "const int64_t pos = L - n_new + i - 1;"),
+    "append_head": ("const int64_t src = (src_tok * Hk + h) * (int64_t)D;",
+                    "const int64_t src = (src_tok * Hk + (Hk - 1 - h)) * (int64_t)D;"),
+}
+
+
+def _checks():
+    c = []
+    for kw in ([dict(), dict(rope_theta=10000.0), dict(qo_lens=[1, 3, 5, 2], causal=True),
+                dict(qo_lens=[1, 3, 5, 2], causal=True, rope_theta=500.0),
+                dict(Hq=6, Hk=3, D=6, P=3)]):
+        c.append(lambda kw=kw: pins.test_matches_dense_torch(kw))
+    c += [pins.test_closed_form_single_key, lambda: pins.test_closed_form_zero_query(16),
+          pins.test_closed_form_equal_keys, pins.test_empty_request,
+          lambda: pins.test_page_size_and_contiguous_invariance(dict()),
+          pins.test_dropping_pages_equals_masking, lambda: pins.test_split_merge_equals_unsplit(3),
+          pins.test_merge_with_empty_state_is_identity, pins.test_merge_matches_logsumexp_of_union,
+          pins.test_cascade_equals_flat, pins.test_rope_matches_complex_rotation,
+          pins.test_rope_d2_is_rotation_by_position_radians,
+          pins.test_causal_row_equals_decode_at_shorter_length,
+          pins.test_append_then_attend_equals_concatenation,
+          pins.test_kv_len_and_malformed_tables]
+    return c
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    src = open(oracle._SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) >= 1, f"mutant {name} no longer applies"
+    mutated = src.replace(old, new, 1)
+    c_path = os.path.join(tmp_path, "mutant.c")
+    so_path = os.path.join(tmp_path, "mutant.so")
+    with open(c_path, "w") as f:
+        f.write(mutated)
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", c_path, "-o",
+                    so_path, "-lm"], check=True)
+    caught = 0
+    with oracle._library(so_path):
+        for check in _checks():
+            try:
+                check()
+            except (AssertionError, ValueError):
+                caught += 1
+    assert caught >= 1, f"no pin caught the planted mistake '{name}'"
+
+
+def test_unmutated_oracle_passes_every_check():
+    for check in _checks():
+        check()
