@@ -1,0 +1,275 @@
+"""Python binding of ``libbsrattn.so``: BSR (paged) KV-cache attention on GB300.
+
+Argument marshalling only.  Each function carries the name of the C entry
+point it calls (see ``include/bsr_attn.h`` for layouts, ownership and error
+behaviour); every step of the computation runs in the library's CUDA
+kernels.  PyTorch supplies device memory and streams.  There is no fallback:
+if the library is not built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import _build
+
+__all__ = [
+    "BsrError", "load", "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run",
+    "bsr_merge_states", "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info",
+    "bsr_last_device_error", "bsr_status_string", "Schedule", "EXPORTED_SYMBOLS",
+]
+
+BSR_OK = 0
+BSR_DTYPE_BF16 = 0
+BSR_DTYPE_F32 = 1
+
+EXPORTED_SYMBOLS = (
+    "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run", "bsr_merge_states", "bsr_append_kv",
+    "bsr_schedule_destroy", "bsr_schedule_get_info", "bsr_last_device_error",
+    "bsr_status_string",
+)
+
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_vp = ctypes.c_void_p
+_lib = None
+
+
+class BsrError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {bsr_status_string(code)} ({code})")
+
+
+class _Info(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("num_qo_heads", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("page_size", ctypes.c_int32), ("causal", ctypes.c_int32),
+        ("rope_theta", ctypes.c_float), ("sum_qo", ctypes.c_int64),
+        ("active_tokens", ctypes.c_int64), ("num_decode_items", ctypes.c_int32),
+        ("num_prefill_items", ctypes.c_int32), ("num_split_streams", ctypes.c_int32),
+        ("num_partials", ctypes.c_int32), ("decode_ctas", ctypes.c_int32),
+        ("decode_warps_per_cta", ctypes.c_int32), ("prefill_ctas", ctypes.c_int32),
+        ("num_sms", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+        ("decode_imbalance", ctypes.c_double), ("prefill_imbalance", ctypes.c_double),
+    ]
+
+
+def load(path: str | None = None):
+    """Load the built library (raises if it is missing: there is no fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build() "
+                           "(block_sparse_kv_bsr_gb300._build.build())")
+    lib = ctypes.CDLL(path)
+    lib.bsr_attn_plan.restype = ctypes.c_int
+    lib.bsr_attn_plan.argtypes = [_i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _vp,
+                                  ctypes.POINTER(_vp)]
+    lib.bsr_attn_plan_host.restype = ctypes.c_int
+    lib.bsr_attn_plan_host.argtypes = [_i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                       ctypes.c_int32, ctypes.POINTER(_Info), _i32p,
+                                       ctypes.c_int64]
+    lib.bsr_attn_run.restype = ctypes.c_int
+    lib.bsr_attn_run.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
+                                 ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp]
+    lib.bsr_merge_states.restype = ctypes.c_int
+    lib.bsr_merge_states.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int64, ctypes.c_int32,
+                                     ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp]
+    lib.bsr_append_kv.restype = ctypes.c_int
+    lib.bsr_append_kv.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32, ctypes.c_int64,
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                  _vp, _vp, _vp, _vp]
+    lib.bsr_schedule_destroy.restype = None
+    lib.bsr_schedule_destroy.argtypes = [_vp]
+    lib.bsr_schedule_get_info.restype = ctypes.c_int
+    lib.bsr_schedule_get_info.argtypes = [_vp, ctypes.POINTER(_Info)]
+    lib.bsr_last_device_error.restype = ctypes.c_int
+    lib.bsr_last_device_error.argtypes = [_vp]
+    lib.bsr_status_string.restype = ctypes.c_char_p
+    lib.bsr_status_string.argtypes = [ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+def bsr_status_string(code: int) -> str:
+    return load().bsr_status_string(int(code)).decode()
+
+
+def _check(code: int, where: str):
+    if code != BSR_OK:
+        raise BsrError(code, where)
+
+
+def _host_i32(x) -> np.ndarray:
+    if hasattr(x, "detach"):
+        if x.is_cuda:
+            raise ValueError("plan reads host arrays: pass CPU tensors / numpy arrays")
+        x = x.detach().numpy()
+    return np.ascontiguousarray(x, dtype=np.int32)
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+class Schedule:
+    """Owns a ``bsr_schedule_t``; destroyed with :func:`bsr_schedule_destroy`."""
+
+    def __init__(self, handle: int):
+        self.handle = handle
+
+    def info(self) -> dict:
+        return bsr_schedule_get_info(self)
+
+    def close(self):
+        if self.handle:
+            bsr_schedule_destroy(self)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def _plan_args(indptr, indices, last_page_len, qo_indptr):
+    ip, ix, lp = _host_i32(indptr), _host_i32(indices), _host_i32(last_page_len)
+    qi = None if qo_indptr is None else _host_i32(qo_indptr)
+    keep = (ip, ix, lp, qi)
+    ptrs = (ip.ctypes.data_as(_i32p), ix.ctypes.data_as(_i32p) if ix.size else None,
+            lp.ctypes.data_as(_i32p) if lp.size else None,
+            qi.ctypes.data_as(_i32p) if qi is not None else None)
+    return keep, ptrs, len(ip) - 1
+
+
+def bsr_attn_plan(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_heads: int,
+                  head_dim: int, page_size: int, num_pages: int, qo_indptr=None,
+                  causal: bool = False, rope_theta: float = 0.0, stream=None,
+                  schedule: Schedule | None = None) -> Schedule:
+    """Plan one batch from HOST page-table arrays; returns (or re-plans) a Schedule."""
+    lib = load()
+    keep, (ip, ix, lp, qi), batch = _plan_args(indptr, indices, last_page_len, qo_indptr)
+    handle = _vp(schedule.handle if schedule is not None else None)
+    code = lib.bsr_attn_plan(ip, ix, lp, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                             qi, int(num_pages), int(bool(causal)), float(rope_theta),
+                             _vp(_stream_ptr(stream)), ctypes.byref(handle))
+    del keep
+    _check(code, "bsr_attn_plan")
+    if schedule is not None:
+        schedule.handle = handle.value
+        return schedule
+    return Schedule(handle.value)
+
+
+def bsr_attn_plan_host(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_heads: int,
+                       head_dim: int, page_size: int, num_pages: int, num_sms: int,
+                       qo_indptr=None, causal: bool = False, rope_theta: float = 0.0):
+    """Host-only planning for `num_sms` SMs: returns (info dict, units int32 [n, 8])."""
+    lib = load()
+    keep, (ip, ix, lp, qi), batch = _plan_args(indptr, indices, last_page_len, qo_indptr)
+    args = [ip, ix, lp, batch, num_qo_heads, num_kv_heads, head_dim, page_size, qi,
+            int(num_pages), int(bool(causal)), float(rope_theta), int(num_sms)]
+    info = _Info()
+    n = lib.bsr_attn_plan_host(*args, ctypes.byref(info), None, 0)
+    if n < 0:
+        raise BsrError(n, "bsr_attn_plan_host")
+    units = np.zeros((max(n, 1), 8), dtype=np.int32)
+    n2 = lib.bsr_attn_plan_host(*args, None, units.ctypes.data_as(_i32p), units.shape[0])
+    del keep
+    if n2 < 0:
+        raise BsrError(n2, "bsr_attn_plan_host")
+    return {name: getattr(info, name) for name, _ in _Info._fields_}, units[:n]
+
+
+def bsr_attn_run(schedule: Schedule, q, k_pages, v_pages, *, sm_scale: float,
+                 rope_theta: float = 0.0, causal: bool = False, out=None, lse=None,
+                 out_dtype=None, want_lse: bool = True, stream=None):
+    """Run a schedule; returns (out, lse).  out/lse are allocated here when not given."""
+    import torch
+    lib = load()
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out must be bf16 or fp32")
+    dt = BSR_DTYPE_F32 if out.dtype == torch.float32 else BSR_DTYPE_BF16
+    for t in (q, k_pages, v_pages):
+        if t.dtype != torch.bfloat16:
+            raise ValueError("q, k_pages, v_pages must be bf16")
+    code = lib.bsr_attn_run(_vp(schedule.handle), _dptr(q), _dptr(k_pages), _dptr(v_pages),
+                            float(sm_scale), float(rope_theta), int(bool(causal)), _dptr(out), dt,
+                            _dptr(lse), _vp(_stream_ptr(stream)))
+    _check(code, "bsr_attn_run")
+    return out, lse
+
+
+def bsr_merge_states(o_a, lse_a, o_b, lse_b, *, o_out=None, lse_out=None, stream=None):
+    """LSE-merge two attention states [rows, heads, D] (bf16 or fp32)."""
+    import torch
+    lib = load()
+    if o_out is None:
+        o_out = torch.empty_like(o_a)
+    if lse_out is None:
+        lse_out = torch.empty_like(lse_a)
+    dt = BSR_DTYPE_F32 if o_a.dtype == torch.float32 else BSR_DTYPE_BF16
+    rows, heads, D = o_a.shape
+    code = lib.bsr_merge_states(_dptr(o_a), _dptr(lse_a), _dptr(o_b), _dptr(lse_b), rows, heads, D,
+                                dt, _dptr(o_out), _dptr(lse_out), _vp(_stream_ptr(stream)))
+    _check(code, "bsr_merge_states")
+    return o_out, lse_out
+
+
+def bsr_append_kv(k_new, v_new, append_indptr, indptr, indices, last_page_len, k_pages, v_pages,
+                  *, device_status=None, stream=None):
+    """Write new tokens' k/v into their pages (all arguments are device tensors)."""
+    lib = load()
+    num_pages, Hk, P, D = k_pages.shape
+    code = lib.bsr_append_kv(_dptr(k_new), _dptr(v_new), _dptr(append_indptr), _dptr(indptr),
+                             _dptr(indices), _dptr(last_page_len), len(indptr) - 1,
+                             int(k_new.shape[0]), Hk, D, P, num_pages, _dptr(k_pages),
+                             _dptr(v_pages), _dptr(device_status), _vp(_stream_ptr(stream)))
+    _check(code, "bsr_append_kv")
+
+
+def bsr_schedule_destroy(schedule: Schedule):
+    load().bsr_schedule_destroy(_vp(schedule.handle))
+    schedule.handle = 0
+
+
+def bsr_schedule_get_info(schedule: Schedule) -> dict:
+    info = _Info()
+    _check(load().bsr_schedule_get_info(_vp(schedule.handle), ctypes.byref(info)),
+           "bsr_schedule_get_info")
+    return {name: getattr(info, name) for name, _ in _Info._fields_}
+
+
+def bsr_last_device_error(schedule: Schedule) -> int:
+    code = load().bsr_last_device_error(_vp(schedule.handle))
+    if code < 0:
+        raise BsrError(code, "bsr_last_device_error")
+    return code

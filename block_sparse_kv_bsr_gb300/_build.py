@@ -1,0 +1,91 @@
+"""Build the C-ABI library ``libbsrattn.so`` for sm_103a with nvcc.
+
+Every translation unit under ``csrc/`` is compiled in parallel into
+``_build/`` and linked into one shared library (static CUDA runtime, no
+libcuda link: the driver entry point for tensor-map encoding is fetched at
+run time).  The build is skipped when no source or flag changed.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import hashlib
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+OUT = os.path.join(PKG, "_build")
+LIB_NAME = "libbsrattn.so"
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}"]
+
+
+def _nvcc() -> str:
+    for cand in (shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libbsrattn.so")
+
+
+def sources() -> list[str]:
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cu", ".cpp")))
+
+
+def _digest() -> str:
+    h = hashlib.sha256()
+    files = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
+    files.append(os.path.join(INCLUDE, "bsr_attn.h"))
+    for full in files:
+        with open(full, "rb") as f:
+            h.update(os.path.basename(full).encode())
+            h.update(f.read())
+    h.update(" ".join(ARCH + COMMON).encode())
+    return h.hexdigest()[:16]
+
+
+def lib_path() -> str:
+    return os.path.join(OUT, LIB_NAME)
+
+
+def build(verbose: bool = False, jobs: int | None = None) -> str:
+    """Compile and link if needed; return the path of the shared library."""
+    os.makedirs(OUT, exist_ok=True)
+    tag = _digest()
+    stamp = os.path.join(OUT, "stamp")
+    lib = lib_path()
+    if os.path.exists(lib) and os.path.exists(stamp) and open(stamp).read() == tag:
+        return lib
+    nvcc = _nvcc()
+
+    def compile_one(src: str) -> str:
+        obj = os.path.join(OUT, os.path.basename(src) + ".o")
+        cmd = [nvcc, *ARCH, *COMMON, "-c", src, "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {os.path.basename(src)}:\n{r.stdout}\n{r.stderr}")
+        if verbose:
+            print(r.stdout + r.stderr)
+        return obj
+
+    srcs = sources()
+    with cf.ThreadPoolExecutor(max_workers=jobs or min(len(srcs), os.cpu_count() or 4)) as ex:
+        objs = list(ex.map(compile_one, srcs))
+    tmp = f"{lib}.{os.getpid()}.tmp"
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", *objs, "-o", tmp]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, lib)
+    with open(stamp, "w") as f:
+        f.write(tag)
+    return lib
+
+
+if __name__ == "__main__":
+    print(build(verbose=True))

@@ -1,0 +1,37 @@
+// Instantiations of the decode kernel for head_dim 64 and their launcher.
+#include "bsr_decode.cuh"
+#include "bsr_schedule.h"
+
+namespace bsr {
+
+namespace {
+template <bool ROPE, bool R16, bool SMALLP>
+cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                       int grid, cudaStream_t stream) {
+  auto kern = bsr_decode_kernel<64, ROPE, R16, SMALLP>;
+  constexpr size_t smem = DecodeCfg<64>::kSmemBytes;
+  // The attribute is per device; setting it again is harmless and cheap.
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kDecodeWarps * 32, smem, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_decode_d64(bool rope, bool r16, bool smallp, const CUtensorMap& tk,
+                               const CUtensorMap& tv, const DecodeParams& p, int grid,
+                               cudaStream_t stream) {
+  const int key = (rope ? 4 : 0) | (r16 ? 2 : 0) | (smallp ? 1 : 0);
+  switch (key) {
+    case 0: return launch_one<false, false, false>(tk, tv, p, grid, stream);
+    case 1: return launch_one<false, false, true>(tk, tv, p, grid, stream);
+    case 2: return launch_one<false, true, false>(tk, tv, p, grid, stream);
+    case 3: return launch_one<false, true, true>(tk, tv, p, grid, stream);
+    case 4: return launch_one<true, false, false>(tk, tv, p, grid, stream);
+    case 5: return launch_one<true, false, true>(tk, tv, p, grid, stream);
+    case 6: return launch_one<true, true, false>(tk, tv, p, grid, stream);
+    default: return launch_one<true, true, true>(tk, tv, p, grid, stream);
+  }
+}
+
+}  // namespace bsr

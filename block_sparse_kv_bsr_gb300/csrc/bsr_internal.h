@@ -1,0 +1,62 @@
+// Internal data layout shared by the host planner and the CUDA kernels.
+// The planner (bsr_plan.cpp) writes these records into one device workspace
+// with a single host-to-device copy; the kernels only read them (plus the
+// merge counters and partial states, which they own at run time).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "bsr_attn.h"
+
+namespace bsr {
+
+// Keys per pipeline stage of the decode kernel: one m16n8k16 K-step of the
+// P.V product and two n-tiles of the Q.K^T product.
+constexpr int kStageTokens = 16;
+// Packed (query, head) rows per decode work unit: the M of one mma tile.
+constexpr int kMaxDecodeRows = 16;
+// Warps per decode CTA (each warp is an independent workgroup).
+constexpr int kDecodeWarps = 8;
+
+// One decode work unit: rows [row0, row0 + nrows) of the packed rows of
+// (request req, kv head kvh) against keys [tok0, tok1).  Packed row R is
+// query R / group of the request, qo head kvh * group + R % group.  Every
+// field the kernel needs is stored here so that no pointer is chased.
+struct alignas(16) DecodeItem {
+  int32_t req;
+  int32_t kvh;
+  int32_t row0;
+  int32_t nrows;
+  int32_t tok0;        // first key; a multiple of max(page_size, kStageTokens)
+  int32_t tok1;        // one past the last key
+  int32_t slot;        // -1: the unit covers all keys and writes out/lse; else partial slot
+  int32_t first_slot;  // first partial slot (and merge counter) of a split range
+  int32_t page_base;   // indptr[req]
+  int32_t q_row0;      // qo_indptr[req]
+  int32_t qpos0;       // position of the request's first query: kv_len - qo_len
+  int32_t nchunks;     // units the range was cut into (1 when unsplit)
+};
+
+struct DecodeParams {
+  const DecodeItem* items;
+  const int32_t* warp_ptr;        // [num_warps + 1] item ranges per warp
+  int32_t* counters;              // [num_partials] arrivals per split range (at first_slot)
+  float* part_o;                  // [num_partials, kMaxDecodeRows, D] normalized partial outputs
+  float* part_lse;                // [num_partials, kMaxDecodeRows] partial LSE (log2 domain)
+  const int32_t* indices;         // [nnz] page ids
+  const float2* rope;             // [rope rows, 4, D / 8] (cos, sin) in fragment order, or null
+  const uint16_t* q;              // bf16 [sum_qo, Hq, D]
+  const void* k_pages;            // bf16 [num_pages, Hk, P, D] (read directly when P < 16)
+  const void* v_pages;
+  void* out;                      // bf16 or fp32 [sum_qo, Hq, D]
+  float* lse;                     // fp32 [sum_qo, Hq] or null
+  int32_t* error;                 // device status word
+  float scale_log2;               // sm_scale * log2(e)
+  int32_t Hq, Hk, group, P;
+  int32_t causal, out_f32, num_warps;
+  int32_t rope_max_pos;           // last row of the cos/sin table
+  uint64_t wait_limit_ns;         // bound on every barrier wait
+};
+
+}  // namespace bsr

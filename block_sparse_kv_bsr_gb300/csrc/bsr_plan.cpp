@@ -1,0 +1,552 @@
+// Host planner for BSR (paged) attention: validates the block table, cuts each
+// (request, kv head, packed-row group) key range into page-aligned work units,
+// spreads the units over persistent warps at equal cost, and uploads
+// everything the kernels read in one asynchronous copy.
+//
+// The scheduling idea follows "FlashInfer: Block-Sparse KV 캐시로 어텐션
+// 병목을 해소하다" (visionhong.com), section "벤치마크: FlashInfer는 얼마나
+// 빠른가?": long sequences are split into smaller work units and interleaved
+// with short ones so that every workgroup stays busy on a skewed batch.  The
+// block table follows section "FlashInfer는 KV 캐시를 어떻게 통합하는가?:
+// Block-Sparse 포맷" (active blocks listed per request, inactive ones absent).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <numeric>
+#include <vector>
+
+#include "bsr_attn.h"
+#include "bsr_schedule.h"
+
+namespace {
+
+using bsr::DecodeItem;
+using bsr::kDecodeWarps;
+using bsr::kMaxDecodeRows;
+using bsr::kStageTokens;
+
+constexpr size_t kAlign = 256;
+// Cost of one work unit beyond its keys (q load, epilogue, partial write),
+// in key-equivalents; used only to weigh units against each other.
+constexpr int64_t kUnitOverhead = 48;
+// Shortest piece a key range is cut into (keys): below this the partial
+// write and merge cost more than the balance gains.
+constexpr int64_t kMinPiece = 64;
+// Least work (key-equivalents) worth a warp of its own: small batches use
+// fewer warps instead of many tiny pieces.
+constexpr int64_t kMinWarpWork = 128;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// A (request, kv head, row group) range of keys before chunking.
+struct Unit {
+  int32_t req, kvh, row0, nrows, kend;
+};
+
+struct Piece {
+  int32_t unit, tok0, tok1;
+  int64_t cost;
+};
+
+// cos/sin of every (position, frequency) in the order the decode kernel's
+// fragments consume them: [pos][quad t][k] with k = 4*ks + j and frequency
+// 16*ks + 2t + j (j < 2) or 16*ks + 8 + 2t + (j - 2) (j >= 2).  Angles are
+// computed in fp64 and rounded once to fp32.
+void build_rope_table(float* dst, int32_t rows, int32_t D, double theta) {
+  const int per_quad = D / 8;
+  std::vector<double> omega(D / 2);
+  for (int f = 0; f < D / 2; ++f) omega[f] = std::pow(theta, -2.0 * double(f) / double(D));
+  for (int32_t pos = 0; pos < rows; ++pos)
+    for (int t = 0; t < 4; ++t)
+      for (int k = 0; k < per_quad; ++k) {
+        const int ks = k / 4, j = k % 4;
+        const int f = 16 * ks + (j < 2 ? 2 * t + j : 8 + 2 * t + (j - 2));
+        const double a = double(pos) * omega[f];
+        float* e = dst + ((size_t(pos) * 4 + t) * per_quad + k) * 2;
+        e[0] = float(std::cos(a));
+        e[1] = float(std::sin(a));
+      }
+}
+
+int fail_cuda(cudaError_t e) {
+  cudaGetLastError();
+  return e == cudaErrorMemoryAllocation ? BSR_ERR_OUT_OF_MEMORY : BSR_ERR_CUDA;
+}
+
+// Everything the planner decides without a GPU: validation, units, cuts,
+// per-warp item lists.
+struct HostPlan {
+  int32_t group = 0;
+  int64_t sum_qo = 0, active = 0;
+  int32_t max_len = 0, max_rows = 0;
+  std::vector<DecodeItem> items;
+  std::vector<int32_t> warp_ptr;
+  int32_t n_partials = 0, n_split = 0, warps = 0;
+  double imbalance = 1.0;
+};
+
+int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
+                   int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                   int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
+                   int32_t causal, float rope_theta, int num_sms, HostPlan* hp) {
+  if (indptr == nullptr || batch < 0 || num_pages_in_pool < 0 || num_sms <= 0)
+    return BSR_ERR_INVALID_ARGUMENT;
+  if (batch > 0 && last_page_len == nullptr) return BSR_ERR_INVALID_ARGUMENT;
+  if (num_qo_heads <= 0 || num_kv_heads <= 0) return BSR_ERR_INVALID_ARGUMENT;
+  if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return BSR_ERR_INVALID_ARGUMENT;
+  if (causal != 0 && causal != 1) return BSR_ERR_INVALID_ARGUMENT;
+  if (head_dim != 64 && head_dim != 128) return BSR_ERR_UNSUPPORTED;
+  if (!is_pow2(page_size) || page_size > 256) return BSR_ERR_UNSUPPORTED;
+  if (num_qo_heads % num_kv_heads != 0) return BSR_ERR_UNSUPPORTED;
+  const int32_t group = num_qo_heads / num_kv_heads;
+  if (group > kMaxDecodeRows) return BSR_ERR_UNSUPPORTED;
+  if (int64_t(num_pages_in_pool) * num_kv_heads * page_size > INT32_MAX) return BSR_ERR_UNSUPPORTED;
+  const bool rope = rope_theta > 0.f;
+
+  // ---------------------------------------------------------------- table validation
+  if (indptr[0] != 0) return BSR_ERR_PAGE_TABLE;
+  if (qo_indptr != nullptr && qo_indptr[0] != 0) return BSR_ERR_PAGE_TABLE;
+  std::vector<int32_t> kv_len(batch), qo_len(batch), q_row0(batch);
+  int64_t sum_qo = 0, active = 0;
+  int32_t max_len = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int64_t n = int64_t(indptr[b + 1]) - indptr[b];
+    if (n < 0) return BSR_ERR_PAGE_TABLE;
+    int64_t L = 0;
+    if (n > 0) {
+      if (last_page_len[b] < 1 || last_page_len[b] > page_size) return BSR_ERR_PAGE_TABLE;
+      L = (n - 1) * page_size + last_page_len[b];
+    }
+    if (L > INT32_MAX / 2) return BSR_ERR_UNSUPPORTED;
+    const int64_t nq = qo_indptr ? int64_t(qo_indptr[b + 1]) - qo_indptr[b] : 1;
+    if (nq < 0) return BSR_ERR_PAGE_TABLE;
+    if ((causal || rope) && L > 0 && nq > L) return BSR_ERR_PAGE_TABLE;
+    kv_len[b] = int32_t(L);
+    qo_len[b] = int32_t(nq);
+    q_row0[b] = int32_t(sum_qo);
+    sum_qo += nq;
+    active += L;
+    max_len = std::max<int32_t>(max_len, int32_t(L));
+  }
+  if (sum_qo > INT32_MAX / num_qo_heads) return BSR_ERR_UNSUPPORTED;
+  const int64_t nnz = indptr[batch];
+  if (nnz > 0 && indices == nullptr) return BSR_ERR_INVALID_ARGUMENT;
+  for (int64_t e = 0; e < nnz; ++e)
+    if (indices[e] < 0 || indices[e] >= num_pages_in_pool) return BSR_ERR_PAGE_TABLE;
+
+  // ---------------------------------------------------------------- units
+  const int64_t align = std::max<int64_t>(page_size, kStageTokens);
+  std::vector<Unit> units;
+  int32_t max_rows = 0;
+  for (int32_t b = 0; b < batch; ++b) {
+    const int32_t rows = qo_len[b] * group;
+    const int32_t qpos0 = kv_len[b] - qo_len[b];
+    for (int32_t h = 0; h < num_kv_heads; ++h)
+      for (int32_t r0 = 0; r0 < rows; r0 += kMaxDecodeRows) {
+        const int32_t nr = std::min(kMaxDecodeRows, rows - r0);
+        int64_t kend = kv_len[b];
+        if (causal)
+          kend = std::min<int64_t>(kend, std::max<int64_t>(0, int64_t(qpos0) + (r0 + nr - 1) / group + 1));
+        units.push_back({b, h, r0, nr, int32_t(kend)});
+        max_rows = std::max(max_rows, nr);
+      }
+  }
+
+  // ---------------------------------------------------------------- cut + balance
+  // Ranges are laid end to end, longest first, and the sequence is cut into
+  // consecutive per-warp segments of (almost) equal cost: a range that does
+  // not fit in the current warp's budget is cut at a stage-aligned key and its
+  // remainder continues on the next warp.  Long ranges therefore spread over
+  // many warps while short ones fill the rest (the interleaving of long and
+  // short work).  The budget is the smallest one for which the cut fits the
+  // warps, found by bisection, so the busiest warp carries about one stage
+  // more than the mean.  The cut is a pure function of the table and SM count.
+  std::vector<int32_t> order(units.size());
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t x, int32_t y) { return units[x].kend > units[y].kend; });
+  int64_t total = 0;
+  for (const Unit& u : units) total += u.kend + kUnitOverhead;
+  const int64_t max_warps = int64_t(num_sms) * kDecodeWarps;
+  const int warps_used =
+      units.empty() ? 0
+                    : int(std::max<int64_t>(1, std::min<int64_t>(max_warps, (total + kMinWarpWork - 1) / kMinWarpWork)));
+  std::vector<Piece> pieces;
+  std::vector<int32_t> owner;
+  // Cut with budget T; returns the number of warps the cut needs (anything
+  // above warps_used means "does not fit").
+  auto partition = [&](int64_t T, bool record) -> int64_t {
+    if (record) {
+      pieces.clear();
+      owner.clear();
+    }
+    int64_t w = 0, room = T;
+    for (int32_t u : order) {
+      const int64_t kend = units[u].kend;
+      int64_t pos = 0;
+      bool placed = false;  // the piece ending at kend (an empty range still needs one)
+      while (!placed) {
+        const int64_t rest = kend - pos;
+        if (rest + kUnitOverhead <= room) {
+          if (record) {
+            pieces.push_back({u, int32_t(pos), int32_t(kend), rest + kUnitOverhead});
+            owner.push_back(int32_t(w));
+          }
+          room -= rest + kUnitOverhead;
+          pos = kend;
+          placed = true;
+        } else {
+          int64_t take = (room - kUnitOverhead) / align * align;
+          if (rest - take < kMinPiece) take = (rest - kMinPiece) / align * align;
+          const bool fresh = room == T;
+          if (take >= kMinPiece) {
+            if (record) {
+              pieces.push_back({u, int32_t(pos), int32_t(pos + take), take + kUnitOverhead});
+              owner.push_back(int32_t(w));
+            }
+            pos += take;
+          } else if (fresh) {
+            return max_warps + 2;  // budget below one piece: cannot make progress
+          }
+          ++w;
+          room = T;
+          if (w >= warps_used) return w + 1;
+        }
+      }
+    }
+    return w + 1;
+  };
+  if (!units.empty()) {
+    int64_t lo = std::max<int64_t>((total + warps_used - 1) / warps_used,
+                                   2 * kMinPiece + kUnitOverhead + align);
+    int64_t hi = lo;
+    while (partition(hi, false) > warps_used) hi *= 2;
+    while (lo < hi) {
+      const int64_t mid = lo + (hi - lo) / 2;
+      if (partition(mid, false) <= warps_used) hi = mid; else lo = mid + 1;
+    }
+    partition(lo, true);
+  }
+
+  // ---------------------------------------------------------------- items
+  std::vector<int32_t> pieces_of_unit(units.size(), 0);
+  for (const Piece& pc : pieces) pieces_of_unit[pc.unit]++;
+  std::vector<int32_t> first_slot(units.size(), -1), next_slot(units.size(), 0);
+  int32_t n_partials = 0, n_split = 0;
+  for (size_t u = 0; u < units.size(); ++u)
+    if (pieces_of_unit[u] > 1) {
+      first_slot[u] = n_partials;
+      n_partials += pieces_of_unit[u];
+      ++n_split;
+    }
+  std::vector<std::vector<int32_t>> per_warp(warps_used);
+  for (size_t i = 0; i < pieces.size(); ++i) per_warp[owner[i]].push_back(int32_t(i));
+  std::vector<DecodeItem> items;
+  items.reserve(pieces.size());
+  std::vector<int32_t> warp_ptr(warps_used + 1, 0);
+  std::vector<int64_t> load(warps_used, 0);
+  for (int w = 0; w < warps_used; ++w) {
+    for (int32_t i : per_warp[w]) {
+      const Piece& pc = pieces[i];
+      const Unit& u = units[pc.unit];
+      DecodeItem it{};
+      it.req = u.req;
+      it.kvh = u.kvh;
+      it.row0 = u.row0;
+      it.nrows = u.nrows;
+      it.tok0 = pc.tok0;
+      it.tok1 = pc.tok1;
+      it.nchunks = pieces_of_unit[pc.unit];
+      it.first_slot = first_slot[pc.unit];
+      // pieces of a range are cut in key order, so slot order is key order
+      it.slot = it.nchunks > 1 ? first_slot[pc.unit] + next_slot[pc.unit]++ : -1;
+      it.page_base = indptr[u.req];
+      it.q_row0 = q_row0[u.req];
+      it.qpos0 = kv_len[u.req] - qo_len[u.req];
+      items.push_back(it);
+      load[w] += pc.cost;
+    }
+    warp_ptr[w + 1] = int32_t(items.size());
+  }
+  double imbalance = 1.0;
+  if (warps_used > 0) {
+    const int64_t mx = *std::max_element(load.begin(), load.end());
+    const double mean = double(std::accumulate(load.begin(), load.end(), int64_t(0))) / warps_used;
+    imbalance = mean > 0 ? double(mx) / mean : 1.0;
+  }
+
+  hp->group = group;
+  hp->sum_qo = sum_qo;
+  hp->active = active;
+  hp->max_len = max_len;
+  hp->max_rows = max_rows;
+  hp->items = std::move(items);
+  hp->warp_ptr = std::move(warp_ptr);
+  hp->n_partials = n_partials;
+  hp->n_split = n_split;
+  hp->warps = warps_used;
+  hp->imbalance = imbalance;
+  return BSR_OK;
+}
+
+}  // namespace
+
+extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
+                             const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                             const int32_t* qo_indptr, int32_t num_pages_in_pool, int32_t causal,
+                             float rope_theta, void* stream_v, bsr_schedule_t* schedule) {
+  if (schedule == nullptr) return BSR_ERR_INVALID_ARGUMENT;
+  const cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const bool rope = rope_theta > 0.f;
+  int device = 0, num_sms = 0;
+  cudaError_t ce = cudaGetDevice(&device);
+  if (ce != cudaSuccess) return fail_cuda(ce);
+  ce = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
+  if (ce != cudaSuccess) return fail_cuda(ce);
+  HostPlan hp;
+  const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
+                                head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
+                                rope_theta, num_sms, &hp);
+  if (rc != BSR_OK) return rc;
+  const int64_t nnz = indptr[batch];
+
+  bsr_schedule* s = *schedule;
+  const bool fresh = (s == nullptr);
+  if (fresh) {
+    s = new (std::nothrow) bsr_schedule();
+    if (s == nullptr) return BSR_ERR_OUT_OF_MEMORY;
+  } else if (s->device != device) {
+    return BSR_ERR_SCHEDULE_MISMATCH;
+  }
+  auto bail = [&](int code) {
+    if (fresh) bsr_schedule_destroy(s);
+    return code;
+  };
+
+  // ---------------------------------------------------------------- RoPE table (cached)
+  const int32_t rope_rows =
+      rope ? int32_t(align_up(size_t(hp.max_len), kStageTokens)) + kStageTokens : 0;
+  const size_t rope_bytes = size_t(rope_rows) * head_dim / 2 * sizeof(float) * 2;
+  if (rope) {
+    if (s->h_rope == nullptr || s->rope_cache_theta != rope_theta || s->rope_cache_D != head_dim ||
+        s->rope_cache_rows < rope_rows) {
+      std::free(s->h_rope);
+      s->h_rope = static_cast<uint8_t*>(std::malloc(rope_bytes));
+      if (s->h_rope == nullptr) return bail(BSR_ERR_OUT_OF_MEMORY);
+      build_rope_table(reinterpret_cast<float*>(s->h_rope), rope_rows, head_dim, double(rope_theta));
+      s->rope_cache_theta = rope_theta;
+      s->rope_cache_D = head_dim;
+      s->rope_cache_rows = rope_rows;
+    }
+  }
+
+  // ---------------------------------------------------------------- workspace layout
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + std::max<size_t>(bytes, 1), kAlign);
+    return o;
+  };
+  const size_t off_indices = take(size_t(std::max<int64_t>(nnz, 1)) * 4);
+  const size_t off_items = take(hp.items.size() * sizeof(DecodeItem));
+  const size_t off_warp_ptr = take(hp.warp_ptr.size() * 4);
+  const size_t off_counters = take(size_t(std::max(hp.n_partials, 1)) * 4);
+  const size_t off_error = take(16);
+  const size_t off_rope = take(rope_bytes);
+  const size_t image_bytes = off;  // everything above is uploaded
+  const size_t off_part_o = take(size_t(hp.n_partials) * kMaxDecodeRows * head_dim * 4);
+  const size_t off_part_lse = take(size_t(hp.n_partials) * kMaxDecodeRows * 4);
+  const size_t ws_bytes = off;
+
+  // ---------------------------------------------------------------- staging + upload
+  if (s->upload_pending) {
+    ce = cudaEventSynchronize(s->upload_done);  // the staging buffer is about to be rewritten
+    if (ce != cudaSuccess) return bail(fail_cuda(ce));
+    s->upload_pending = false;
+  }
+  if (s->stage_cap < image_bytes) {
+    if (s->h_stage) cudaFreeHost(s->h_stage);
+    s->h_stage = nullptr;
+    s->stage_cap = 0;
+    ce = cudaMallocHost(reinterpret_cast<void**>(&s->h_stage), image_bytes);
+    if (ce != cudaSuccess) return bail(fail_cuda(ce));
+    s->stage_cap = image_bytes;
+  }
+  if (s->ws_cap < ws_bytes) {
+    if (s->d_ws) {
+      ce = cudaFree(s->d_ws);  // synchronizes: no kernel can still be reading it
+      s->d_ws = nullptr;
+      s->ws_cap = 0;
+      if (ce != cudaSuccess) return bail(fail_cuda(ce));
+    }
+    ce = cudaMalloc(reinterpret_cast<void**>(&s->d_ws), ws_bytes);
+    if (ce != cudaSuccess) return bail(fail_cuda(ce));
+    s->ws_cap = ws_bytes;
+  }
+  if (s->upload_done == nullptr) {
+    ce = cudaEventCreateWithFlags(&s->upload_done, cudaEventDisableTiming);
+    if (ce != cudaSuccess) return bail(fail_cuda(ce));
+  }
+  uint8_t* h = s->h_stage;
+  std::memset(h, 0, image_bytes);
+  if (nnz > 0) std::memcpy(h + off_indices, indices, size_t(nnz) * 4);
+  if (!hp.items.empty())
+    std::memcpy(h + off_items, hp.items.data(), hp.items.size() * sizeof(DecodeItem));
+  std::memcpy(h + off_warp_ptr, hp.warp_ptr.data(), hp.warp_ptr.size() * 4);
+  if (rope) std::memcpy(h + off_rope, s->h_rope, rope_bytes);
+  ce = cudaMemcpyAsync(s->d_ws, h, image_bytes, cudaMemcpyHostToDevice, stream);
+  if (ce != cudaSuccess) return bail(fail_cuda(ce));
+  ce = cudaEventRecord(s->upload_done, stream);
+  if (ce != cudaSuccess) return bail(fail_cuda(ce));
+  s->upload_pending = true;
+
+  // ---------------------------------------------------------------- commit
+  s->device = device;
+  s->num_sms = num_sms;
+  s->batch = batch;
+  s->Hq = num_qo_heads;
+  s->Hk = num_kv_heads;
+  s->D = head_dim;
+  s->P = page_size;
+  s->group = hp.group;
+  s->causal = causal;
+  s->rope_theta = rope_theta;
+  s->num_pages = num_pages_in_pool;
+  s->sum_qo = hp.sum_qo;
+  s->active_tokens = hp.active;
+  s->rope_rows = rope_rows;
+  s->max_rows = hp.max_rows;
+  s->n_items = int32_t(hp.items.size());
+  s->n_partials = hp.n_partials;
+  s->n_split = hp.n_split;
+  s->dec_warps = hp.warps;
+  s->dec_ctas = (hp.warps + kDecodeWarps - 1) / kDecodeWarps;
+  s->dec_imbalance = hp.imbalance;
+  s->ws_used = ws_bytes;
+  s->off_indices = off_indices;
+  s->off_items = off_items;
+  s->off_warp_ptr = off_warp_ptr;
+  s->off_counters = off_counters;
+  s->off_error = off_error;
+  s->off_rope = off_rope;
+  s->off_part_o = off_part_o;
+  s->off_part_lse = off_part_lse;
+  *schedule = s;
+  return BSR_OK;
+}
+
+extern "C" void bsr_schedule_destroy(bsr_schedule_t s) {
+  if (s == nullptr) return;
+  if (s->device >= 0) cudaSetDevice(s->device);
+  if (s->d_ws) {
+    cudaDeviceSynchronize();
+    cudaFree(s->d_ws);
+  }
+  if (s->upload_done) cudaEventDestroy(s->upload_done);
+  if (s->h_stage) cudaFreeHost(s->h_stage);
+  std::free(s->h_rope);
+  cudaGetLastError();
+  delete s;
+}
+
+extern "C" int bsr_schedule_get_info(bsr_schedule_t s, bsr_schedule_info_t* info) {
+  if (s == nullptr || info == nullptr) return BSR_ERR_INVALID_ARGUMENT;
+  std::memset(info, 0, sizeof(*info));
+  info->batch = s->batch;
+  info->num_qo_heads = s->Hq;
+  info->num_kv_heads = s->Hk;
+  info->head_dim = s->D;
+  info->page_size = s->P;
+  info->causal = s->causal;
+  info->rope_theta = s->rope_theta;
+  info->sum_qo = s->sum_qo;
+  info->active_tokens = s->active_tokens;
+  info->num_decode_items = s->n_items;
+  info->num_prefill_items = 0;
+  info->num_split_streams = s->n_split;
+  info->num_partials = s->n_partials;
+  info->decode_ctas = s->dec_ctas;
+  info->decode_warps_per_cta = kDecodeWarps;
+  info->prefill_ctas = 0;
+  info->num_sms = s->num_sms;
+  info->workspace_bytes = int64_t(s->ws_used);
+  info->decode_imbalance = s->dec_imbalance;
+  info->prefill_imbalance = 1.0;
+  return BSR_OK;
+}
+
+extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
+                                  const int32_t* last_page_len, int32_t batch,
+                                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                  int32_t page_size, const int32_t* qo_indptr,
+                                  int32_t num_pages_in_pool, int32_t causal, float rope_theta,
+                                  int32_t num_sms, bsr_schedule_info_t* info, int32_t* units,
+                                  int64_t max_units) {
+  HostPlan hp;
+  const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
+                                head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
+                                rope_theta, num_sms, &hp);
+  if (rc != BSR_OK) return rc;
+  if (info != nullptr) {
+    std::memset(info, 0, sizeof(*info));
+    info->batch = batch;
+    info->num_qo_heads = num_qo_heads;
+    info->num_kv_heads = num_kv_heads;
+    info->head_dim = head_dim;
+    info->page_size = page_size;
+    info->causal = causal;
+    info->rope_theta = rope_theta;
+    info->sum_qo = hp.sum_qo;
+    info->active_tokens = hp.active;
+    info->num_decode_items = int32_t(hp.items.size());
+    info->num_split_streams = hp.n_split;
+    info->num_partials = hp.n_partials;
+    info->decode_ctas = (hp.warps + kDecodeWarps - 1) / kDecodeWarps;
+    info->decode_warps_per_cta = kDecodeWarps;
+    info->num_sms = num_sms;
+    info->decode_imbalance = hp.imbalance;
+    info->prefill_imbalance = 1.0;
+  }
+  const int64_t n = int64_t(hp.items.size());
+  if (units != nullptr) {
+    if (max_units < n) return BSR_ERR_INVALID_ARGUMENT;
+    for (int32_t w = 0; w < hp.warps; ++w)
+      for (int32_t i = hp.warp_ptr[w]; i < hp.warp_ptr[w + 1]; ++i) {
+        const DecodeItem& it = hp.items[i];
+        int32_t* u = units + int64_t(i) * 8;
+        u[0] = it.req; u[1] = it.kvh; u[2] = it.row0; u[3] = it.nrows;
+        u[4] = it.tok0; u[5] = it.tok1; u[6] = it.slot; u[7] = w;
+      }
+  }
+  return int(n);
+}
+
+extern "C" int bsr_last_device_error(bsr_schedule_t s) {
+  if (s == nullptr || s->d_ws == nullptr) return BSR_ERR_INVALID_ARGUMENT;
+  int32_t word = 0;
+  cudaError_t ce = cudaSetDevice(s->device);
+  if (ce == cudaSuccess) ce = cudaDeviceSynchronize();
+  if (ce == cudaSuccess) ce = cudaMemcpy(&word, s->d_ws + s->off_error, 4, cudaMemcpyDeviceToHost);
+  if (ce != cudaSuccess) return fail_cuda(ce);
+  return word;
+}
+
+extern "C" const char* bsr_status_string(int status) {
+  switch (status) {
+    case BSR_OK: return "ok";
+    case BSR_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case BSR_ERR_UNSUPPORTED: return "unsupported head_dim, page_size or head grouping";
+    case BSR_ERR_PAGE_TABLE: return "malformed page table";
+    case BSR_ERR_OUT_OF_MEMORY: return "out of memory";
+    case BSR_ERR_CUDA: return "CUDA error";
+    case BSR_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded wait";
+    case BSR_ERR_SCHEDULE_MISMATCH: return "arguments disagree with the schedule";
+    default: return "unknown status";
+  }
+}

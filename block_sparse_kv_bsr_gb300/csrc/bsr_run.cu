@@ -1,0 +1,135 @@
+// bsr_attn_run: executes a planned schedule on the GPU.
+//
+// Host work here is argument checking, encoding the TMA tensor maps of the
+// caller's K/V page pools (cached per pool pointer), and one kernel launch.
+// Nothing is allocated and the host is never synchronized, so the call can
+// be captured in a CUDA graph.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "bsr_attn.h"
+#include "bsr_schedule.h"
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map over a page pool [num_pages, Hk, P, D] bf16 seen as rows of D
+// elements, loaded 16 rows x 64 columns at a time into 128B-swizzled tiles.
+// D = 128: rank 3 {64 cols, 2 column blocks, rows} so one box is one column
+// block of 16 rows; D = 64: rank 2 {64 cols, rows}.
+bool encode_pool(CUtensorMap* tm, const void* base, int64_t rows, int D, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint32_t rank;
+  if (D == 128) {
+    rank = 3;
+    dims[0] = 64; dims[1] = 2; dims[2] = cuuint64_t(rows);
+    strides[0] = 128; strides[1] = 256;
+    box[0] = 64; box[1] = 1; box[2] = cuuint32_t(box_rows);
+  } else {
+    rank = 2;
+    dims[0] = 64; dims[1] = cuuint64_t(rows);
+    strides[0] = 128;
+    box[0] = 64; box[1] = cuuint32_t(box_rows);
+  }
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages,
+                            const void* v_pages, float sm_scale, float rope_theta, int32_t causal,
+                            void* out, int32_t out_dtype, float* lse, void* stream_v) {
+  if (s == nullptr || s->d_ws == nullptr) return BSR_ERR_INVALID_ARGUMENT;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return BSR_ERR_INVALID_ARGUMENT;
+  if (out_dtype != BSR_DTYPE_BF16 && out_dtype != BSR_DTYPE_F32) return BSR_ERR_INVALID_ARGUMENT;
+  if (rope_theta != s->rope_theta || causal != s->causal) return BSR_ERR_SCHEDULE_MISMATCH;
+  if (s->n_items == 0) return BSR_OK;
+  if (q == nullptr || out == nullptr || k_pages == nullptr || v_pages == nullptr)
+    return BSR_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(q, 4) ||
+      !aligned(out, out_dtype == BSR_DTYPE_F32 ? 8 : 4) || (lse && !aligned(lse, 4)))
+    return BSR_ERR_INVALID_ARGUMENT;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != s->device) return BSR_ERR_SCHEDULE_MISMATCH;
+  const cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+
+  const bool smallp = s->P < bsr::kStageTokens;
+  const int64_t rows = int64_t(s->num_pages) * s->Hk * s->P;
+  if (!smallp && (s->tm_k_ptr != k_pages || s->tm_v_ptr != v_pages)) {
+    if (rows <= 0 || !encode_pool(&s->tm_k, k_pages, rows, s->D, bsr::kStageTokens) ||
+        !encode_pool(&s->tm_v, v_pages, rows, s->D, bsr::kStageTokens)) {
+      s->tm_k_ptr = s->tm_v_ptr = nullptr;
+      return BSR_ERR_CUDA;
+    }
+    s->tm_k_ptr = k_pages;
+    s->tm_v_ptr = v_pages;
+  }
+
+  bsr::DecodeParams p{};
+  p.items = s->dev<const bsr::DecodeItem>(s->off_items);
+  p.warp_ptr = s->dev<const int32_t>(s->off_warp_ptr);
+  p.counters = s->dev<int32_t>(s->off_counters);
+  p.part_o = s->dev<float>(s->off_part_o);
+  p.part_lse = s->dev<float>(s->off_part_lse);
+  p.indices = s->dev<const int32_t>(s->off_indices);
+  p.rope = s->rope_rows > 0 ? s->dev<const float2>(s->off_rope) : nullptr;
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_pages = k_pages;
+  p.v_pages = v_pages;
+  p.out = out;
+  p.lse = lse;
+  p.error = s->dev<int32_t>(s->off_error);
+  p.scale_log2 = float(double(sm_scale) * 1.4426950408889634);
+  p.Hq = s->Hq;
+  p.Hk = s->Hk;
+  p.group = s->group;
+  p.P = s->P;
+  p.causal = s->causal;
+  p.out_f32 = out_dtype == BSR_DTYPE_F32;
+  p.num_warps = s->dec_warps;
+  p.rope_max_pos = s->rope_rows > 0 ? s->rope_rows - 1 : 0;
+  p.wait_limit_ns = 1000000000ull;  // 1 s: orders of magnitude above any healthy wait
+
+  const bool rope = s->rope_rows > 0;
+  const bool r16 = s->max_rows > 8;
+  CUtensorMap dummy{};
+  const CUtensorMap& tk = smallp ? dummy : s->tm_k;
+  const CUtensorMap& tv = smallp ? dummy : s->tm_v;
+  cudaError_t e = s->D == 128
+                      ? bsr::launch_decode_d128(rope, r16, smallp, tk, tv, p, s->dec_ctas, stream)
+                      : bsr::launch_decode_d64(rope, r16, smallp, tk, tv, p, s->dec_ctas, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return BSR_ERR_CUDA;
+  }
+  return BSR_OK;
+}

@@ -1,0 +1,63 @@
+// Host-side state of one schedule (opaque to C callers as bsr_schedule_t).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "bsr_internal.h"
+
+struct bsr_schedule {
+  int device = -1;
+  int num_sms = 0;
+
+  // problem the schedule was planned for
+  int32_t batch = 0, Hq = 0, Hk = 0, D = 0, P = 0, group = 0, causal = 0;
+  float rope_theta = 0.f;
+  int32_t num_pages = 0;
+  int64_t sum_qo = 0, active_tokens = 0;
+  int32_t rope_rows = 0;       // rows of the cos/sin table (0 without RoPE)
+  int32_t max_rows = 0;        // largest packed-row count of one decode unit
+
+  // decode plan
+  int32_t n_items = 0, n_partials = 0, n_split = 0, dec_warps = 0, dec_ctas = 0;
+  double dec_imbalance = 0.0;
+
+  // one device allocation holding everything the kernels read or own
+  uint8_t* d_ws = nullptr;
+  size_t ws_cap = 0, ws_used = 0;
+  size_t off_indices = 0, off_items = 0, off_warp_ptr = 0, off_counters = 0, off_rope = 0,
+         off_error = 0, off_part_o = 0, off_part_lse = 0;
+
+  // pinned staging buffer for the single host-to-device upload
+  uint8_t* h_stage = nullptr;
+  size_t stage_cap = 0;
+  cudaEvent_t upload_done = nullptr;
+  bool upload_pending = false;
+
+  // cos/sin table cache: rebuilt only when theta, head_dim or the length grow
+  float rope_cache_theta = 0.f;
+  int32_t rope_cache_D = 0, rope_cache_rows = 0;
+  uint8_t* h_rope = nullptr;   // host copy in fragment order (malloc)
+
+  // tensor maps of the last k/v pools seen by run (re-encoded when they change)
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  const void* tm_k_ptr = nullptr;
+  const void* tm_v_ptr = nullptr;
+
+  template <typename T>
+  T* dev(size_t off) const { return reinterpret_cast<T*>(d_ws + off); }
+};
+
+namespace bsr {
+// Kernel launchers (one translation unit per head dim).
+cudaError_t launch_decode_d64(bool rope, bool r16, bool smallp, const CUtensorMap& tk,
+                              const CUtensorMap& tv, const DecodeParams& p, int grid,
+                              cudaStream_t stream);
+cudaError_t launch_decode_d128(bool rope, bool r16, bool smallp, const CUtensorMap& tk,
+                               const CUtensorMap& tv, const DecodeParams& p, int grid,
+                               cudaStream_t stream);
+}  // namespace bsr

@@ -1,0 +1,212 @@
+/*
+ * bsr_attn.h — C ABI of a GB300 (sm_103a) attention engine for batched
+ * attention over a KV cache stored in Block-Sparse-Row (paged) form.
+ *
+ * What it computes follows "FlashInfer: Block-Sparse KV 캐시로 어텐션 병목을
+ * 해소하다 (MLSys 2025 Best Paper)" (visionhong.com):
+ *   - section "FlashInfer는 KV 캐시를 어떻게 통합하는가?: Block-Sparse 포맷":
+ *     the KV cache is a block-sparse tensor whose blocks are runs of
+ *     consecutive tokens and whose sparse metadata lists the active blocks;
+ *     paged and contiguous caches are instances of it; inactive blocks are
+ *     skipped; a shared prefix is stored once (at its own block size) and
+ *     composed with per-request suffixes;
+ *   - section "어텐션 연산에서 진짜 병목은 어디인가?": decode is bound by
+ *     memory bandwidth (the whole KV history is read per generated token),
+ *     prefill by compute;
+ *   - section "JIT 컴파일은 어텐션을 어떻게 빠르게 만드는가?": RoPE is fused
+ *     into the attention kernel instead of running as its own pass;
+ *   - section "벤치마크: FlashInfer는 얼마나 빠른가?": a load-balanced scheduler
+ *     cuts long sequences into smaller work units and interleaves them with
+ *     short ones so that no workgroup idles on a skewed batch.
+ * The pages give no signatures; these calls state that problem directly.
+ *
+ * Conventions for every call
+ *   - All tensors are dense, row-major, and live in device memory unless a
+ *     parameter says "host".  bf16 is IEEE bfloat16 (uint16 storage).
+ *   - q, out      : [sum_qo, Hq, D]        (sum_qo = qo_indptr[batch])
+ *   - k/v pages   : [num_pages, Hk, P, D]  (HND: one (page, kv head) block of
+ *                   P*D elements is contiguous)
+ *   - lse         : [sum_qo, Hq] fp32, natural-log log-sum-exp of the scaled
+ *                   logits of the row; -inf (and out = 0) for a row that
+ *                   attends to no key.
+ *   - Page table (indptr, indices, last_page_len) for request b: its pages
+ *     are indices[indptr[b] .. indptr[b+1]); every page is full except the
+ *     last, which holds last_page_len[b] tokens (1..P); a request with no
+ *     page has length 0.  Key j of b is slot j mod P of page j / P of that
+ *     list; dropped (inactive) blocks are simply absent from the list.
+ *   - Query i of request b (qo_indptr[b] <= row < qo_indptr[b+1]) sits at
+ *     position L_b - qo_len_b + i; with causal masking it sees keys at
+ *     positions <= its own.  qo head h reads kv head h / (Hq / Hk).
+ *   - RoPE (rope_theta > 0): rotate-half form, frequency theta^(-2i/D) for
+ *     pair (i, i + D/2); keys are stored un-rotated and rotated on load at
+ *     their position in the request's page list; queries at their position.
+ *   - stream is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Every call returns BSR_OK (0) or a negative BSR_ERR_* code.  No call
+ *     aborts the process and no kernel traps.
+ *   - Supported: head_dim 64 or 128; page_size a power of two in [1, 256];
+ *     Hq a multiple of Hk with Hq / Hk <= 16.
+ */
+#ifndef BSR_ATTN_H_
+#define BSR_ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  BSR_OK = 0,
+  BSR_ERR_INVALID_ARGUMENT = -1, /* null pointer, bad size, bad scale */
+  BSR_ERR_UNSUPPORTED = -2,      /* head_dim / page_size / group size outside the set */
+  BSR_ERR_PAGE_TABLE = -3,       /* malformed indptr / indices / last_page_len / qo_indptr */
+  BSR_ERR_OUT_OF_MEMORY = -4,    /* device or pinned host allocation failed */
+  BSR_ERR_CUDA = -5,             /* a CUDA runtime/driver call or launch failed */
+  BSR_ERR_DEVICE_TIMEOUT = -6,   /* a kernel gave up on a bounded wait (see bsr_last_device_error) */
+  BSR_ERR_SCHEDULE_MISMATCH = -7 /* run arguments disagree with what the schedule was planned for */
+};
+
+enum { BSR_DTYPE_BF16 = 0, BSR_DTYPE_F32 = 1 };
+
+typedef struct bsr_schedule* bsr_schedule_t;
+
+/*
+ * bsr_attn_plan — build the load-balanced work schedule for one batch.
+ * (Scheduler: "벤치마크: FlashInfer는 얼마나 빠른가?"; block table:
+ * "Block-Sparse 포맷".)
+ *
+ * indptr [batch+1], indices [indptr[batch]], last_page_len [batch] and
+ * qo_indptr [batch+1] are HOST arrays; the caller keeps ownership and may
+ * free them on return.  qo_indptr may be NULL, meaning one query per request.
+ * The planner validates the table (indptr and qo_indptr start at 0 and never
+ * decrease, page ids in [0, num_pages_in_pool), 1 <= last_page_len <=
+ * page_size for non-empty requests, qo_len <= kv_len when causal or RoPE),
+ * cuts every (request, kv head) key range into page-aligned chunks, spreads
+ * the chunks over persistent warps at equal cost (long sequences cut and
+ * interleaved with short ones), and uploads the page table, the work lists,
+ * zeroed merge counters and (rope_theta > 0) an fp32 cos/sin table built in
+ * fp64 with ONE asynchronous host-to-device copy on `stream`.
+ *
+ * *schedule must be NULL (a new schedule is created) or a schedule returned
+ * by an earlier plan, which is then re-planned in place: its device workspace
+ * is reused when large enough.  Re-planning is ordered on `stream` after work
+ * already queued there; work on other streams that still reads the old
+ * schedule is the caller's to finish first.
+ * The schedule binds the current CUDA device.
+ */
+int bsr_attn_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
+                  int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
+                  int32_t causal, float rope_theta, void* stream, bsr_schedule_t* schedule);
+
+/*
+ * bsr_attn_run — execute a schedule: out = softmax(sm_scale * q k^T) v and
+ * lse per (query row, qo head).  ("어텐션 연산에서 진짜 병목은 어디인가?",
+ * "Block-Sparse 포맷", "JIT 컴파일은 …" for the fused RoPE.)
+ *
+ * q (bf16), k_pages, v_pages (bf16, num_pages_in_pool pages as planned) are
+ * read; out (out_dtype: BSR_DTYPE_BF16 or BSR_DTYPE_F32) and lse (fp32, may
+ * be NULL) are written.  All are caller-owned device buffers; no buffer may
+ * alias another.  sm_scale must be finite and > 0.  rope_theta and causal
+ * must equal the values given to plan (else BSR_ERR_SCHEDULE_MISMATCH).
+ * k_pages/v_pages must be 16-byte aligned.
+ * The call allocates nothing, never synchronizes the host, and is
+ * stream-ordered; it may be captured in a CUDA graph.  Two runs of one
+ * schedule must not overlap in time (they share its merge workspace).
+ */
+int bsr_attn_run(bsr_schedule_t schedule, const void* q, const void* k_pages, const void* v_pages,
+                 float sm_scale, float rope_theta, int32_t causal, void* out, int32_t out_dtype,
+                 float* lse, void* stream);
+
+/*
+ * bsr_merge_states — combine two attention states over disjoint key sets
+ * (split chunks, or the shared-prefix and suffix levels of a cascade;
+ * "Block-Sparse 포맷", composition of a stored-once prefix with suffixes):
+ *   lse = M + ln(exp(lse_a - M) + exp(lse_b - M)),  M = max(lse_a, lse_b)
+ *   o   = exp(lse_a - lse) o_a + exp(lse_b - lse) o_b
+ * A row whose two states are both empty (lse = -inf) gets o = 0, lse = -inf.
+ * o_a, o_b, o_out: [num_rows, num_heads, head_dim] of `dtype`; lse_*:
+ * [num_rows, num_heads] fp32.  o_out may equal o_a and lse_out may equal
+ * lse_a (in-place); no other aliasing.  Device buffers, caller-owned.
+ */
+int bsr_merge_states(const void* o_a, const float* lse_a, const void* o_b, const float* lse_b,
+                     int64_t num_rows, int32_t num_heads, int32_t head_dim, int32_t dtype,
+                     void* o_out, float* lse_out, void* stream);
+
+/*
+ * bsr_append_kv — write new tokens' (un-rotated) k and v into their pages
+ * (the append step of chunked prefill / decode).
+ *
+ * All arrays are DEVICE arrays.  The page table (indptr, indices,
+ * last_page_len; batch requests) describes the cache AFTER the append:
+ * request b appends n_b = append_indptr[b+1] - append_indptr[b] tokens, which
+ * take positions L_b - n_b .. L_b - 1.  k_new, v_new: bf16
+ * [num_new_tokens, Hk, D]; k_pages, v_pages: bf16 [num_pages_in_pool, Hk, P, D],
+ * written in place; every other slot keeps its bits.  The device-resident
+ * table cannot be checked on the host: a token whose page id falls outside
+ * [0, num_pages_in_pool) or whose request cannot hold it is skipped, and bit
+ * 1 is OR-ed into *device_status (a device int32, may be NULL) for the caller
+ * to read after synchronizing.
+ */
+int bsr_append_kv(const void* k_new, const void* v_new, const int32_t* append_indptr,
+                  const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
+                  int32_t batch, int64_t num_new_tokens, int32_t num_kv_heads, int32_t head_dim,
+                  int32_t page_size, int32_t num_pages_in_pool, void* k_pages, void* v_pages,
+                  int32_t* device_status, void* stream);
+
+/* Free a schedule's device workspace and host buffers after synchronizing
+ * the device.  NULL is ignored. */
+void bsr_schedule_destroy(bsr_schedule_t schedule);
+
+/* What a plan produced (sizes are per schedule). */
+typedef struct bsr_schedule_info {
+  int32_t batch, num_qo_heads, num_kv_heads, head_dim, page_size, causal;
+  float rope_theta;
+  int64_t sum_qo;
+  int64_t active_tokens;      /* sum of attended key counts over requests */
+  int32_t num_decode_items;   /* work units of the split-KV decode kernel */
+  int32_t num_prefill_items;  /* work units of the tensor-core prefill kernel */
+  int32_t num_split_streams;  /* (request, kv head, row group) ranges cut into >1 chunk */
+  int32_t num_partials;       /* partial states written before merging */
+  int32_t decode_ctas, decode_warps_per_cta;
+  int32_t prefill_ctas;
+  int32_t num_sms;
+  int64_t workspace_bytes;
+  double decode_imbalance;    /* max / mean planned cost over decode warps */
+  double prefill_imbalance;   /* max / mean planned cost over prefill CTAs */
+} bsr_schedule_info_t;
+
+int bsr_schedule_get_info(bsr_schedule_t schedule, bsr_schedule_info_t* info);
+
+/*
+ * bsr_attn_plan_host — the host half of bsr_attn_plan, for a given SM count,
+ * touching no GPU: validates the table exactly like bsr_attn_plan and returns
+ * the number of decode work units (or a negative BSR_ERR_* code).  If `info`
+ * is non-NULL it is filled as bsr_schedule_get_info would (without the
+ * workspace size); if `units` is non-NULL (capacity max_units rows) each unit
+ * is written as int32[8]: request, kv head, first packed row, packed rows,
+ * first key, end key, partial slot (-1 = unsplit), warp.  Packed row R of
+ * (request, kv head) is query R / (Hq/Hk), qo head kv_head * (Hq/Hk) +
+ * R % (Hq/Hk).  All arrays are host arrays owned by the caller.  Use it to
+ * inspect or test a schedule (coverage of every key, balance) without a device.
+ */
+int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
+                       const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                       const int32_t* qo_indptr, int32_t num_pages_in_pool, int32_t causal,
+                       float rope_theta, int32_t num_sms, bsr_schedule_info_t* info,
+                       int32_t* units, int64_t max_units);
+
+/* Device-side status word of a schedule (0 = fine; bit 0: a kernel gave up on
+ * a bounded wait).  Synchronizes the schedule's device; returns the word, or
+ * a negative BSR_ERR_* code. */
+int bsr_last_device_error(bsr_schedule_t schedule);
+
+/* Static, human-readable text for a status code. */
+const char* bsr_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSR_ATTN_H_ */

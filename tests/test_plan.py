@@ -1,0 +1,103 @@
+"""Host planner: every key of every (request, kv head, row group) is covered exactly once,
+split ranges are numbered in key order, and the load balances on skewed batches."""
+import numpy as np
+import pytest
+
+import block_sparse_kv_bsr_gb300 as bsr
+import workloads as wl
+from block_sparse_kv_bsr_gb300 import _build
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    _build.build()
+    bsr.load()
+
+
+def plan_of(w: wl.Paged, num_sms=152):
+    return bsr.bsr_attn_plan_host(
+        w.indptr, w.indices, w.last_page_len, num_qo_heads=w.num_qo_heads,
+        num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, page_size=w.page_size,
+        num_pages=w.num_pages, num_sms=num_sms, qo_indptr=w.qo_indptr, causal=w.causal,
+        rope_theta=w.rope_theta)
+
+
+def check_coverage(w: wl.Paged, units: np.ndarray):
+    g = w.num_qo_heads // w.num_kv_heads
+    ranges = {}
+    for req, kvh, row0, nrows, tok0, tok1, slot, warp in units.tolist():
+        assert 1 <= nrows <= 16
+        assert tok0 % max(w.page_size, 16) == 0
+        ranges.setdefault((req, kvh, row0, nrows), []).append((tok0, tok1, slot))
+    for b in range(w.batch):
+        L = w.kv_len[b]
+        nq = int(w.qo_indptr[b + 1] - w.qo_indptr[b])
+        rows = nq * g
+        for kvh in range(w.num_kv_heads):
+            for r0 in range(0, rows, 16):
+                nr = min(16, rows - r0)
+                kend = L
+                if w.causal:
+                    kend = min(L, max(0, (L - nq) + (r0 + nr - 1) // g + 1))
+                pieces = sorted(ranges.pop((b, kvh, r0, nr)))
+                if len(pieces) == 1:
+                    assert pieces[0][2] == -1
+                else:
+                    slots = [p[2] for p in pieces]
+                    assert slots == list(range(slots[0], slots[0] + len(slots)))
+                pos = 0
+                for tok0, tok1, _ in pieces:
+                    assert tok0 == pos and (tok1 > tok0 or kend == 0)
+                    pos = tok1
+                assert pos == kend
+    assert not ranges, "units for ranges that do not exist"
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3, 5])
+def test_small_configs_cover_every_key(cfg):
+    w = wl.by_name(cfg, small=True)
+    info, units = plan_of(w, num_sms=8)
+    check_coverage(w, units)
+    assert info["active_tokens"] == w.active_tokens
+
+
+def test_cascade_levels_cover_every_key():
+    c = wl.config4(small=True)
+    for w in (c.prefix, c.suffix):
+        info, units = plan_of(w, num_sms=8)
+        check_coverage(w, units)
+
+
+@pytest.mark.parametrize("P", [1, 2, 8, 32, 256])
+def test_page_sizes(P):
+    w = wl.make_paged("p", 3, [1, 15, 16, 17, 300, 513], Hq=8, Hk=2, D=64, P=P)
+    info, units = plan_of(w, num_sms=2)
+    check_coverage(w, units)
+
+
+def test_empty_requests_get_a_unit():
+    w = wl.make_paged("e", 4, [0, 40, 0], Hq=4, Hk=2, D=64, P=16)
+    info, units = plan_of(w, num_sms=2)
+    check_coverage(w, units)
+
+
+def test_skewed_batch_is_balanced():
+    w = wl.config3(small=False)
+    info, units = plan_of(w, num_sms=152)
+    check_coverage(w, units)
+    assert info["decode_imbalance"] < 1.05
+    assert info["num_split_streams"] >= 13 * 8     # every long (request, head) range is cut
+
+
+def test_uniform_batch_is_balanced():
+    w = wl.config2(small=False)
+    info, units = plan_of(w, num_sms=152)
+    check_coverage(w, units)
+    assert info["decode_imbalance"] < 1.05
+
+
+def test_plan_is_deterministic():
+    w = wl.config3(small=True)
+    a = plan_of(w, num_sms=16)[1]
+    b = plan_of(w, num_sms=16)[1]
+    assert np.array_equal(a, b)
