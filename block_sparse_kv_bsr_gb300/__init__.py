@@ -53,6 +53,7 @@ class _Info(ctypes.Structure):
         ("num_partials", ctypes.c_int32), ("decode_ctas", ctypes.c_int32),
         ("decode_warps_per_cta", ctypes.c_int32), ("prefill_ctas", ctypes.c_int32),
         ("num_sms", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+        ("upload_bytes", ctypes.c_int64),
         ("decode_imbalance", ctypes.c_double), ("prefill_imbalance", ctypes.c_double),
     ]
 

@@ -429,6 +429,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->dec_ctas = (hp.warps + kDecodeWarps - 1) / kDecodeWarps;
   s->dec_imbalance = hp.imbalance;
   s->ws_used = ws_bytes;
+  s->upload_bytes = image_bytes;
   s->off_indices = off_indices;
   s->off_items = off_items;
   s->off_warp_ptr = off_warp_ptr;
@@ -476,6 +477,7 @@ extern "C" int bsr_schedule_get_info(bsr_schedule_t s, bsr_schedule_info_t* info
   info->prefill_ctas = 0;
   info->num_sms = s->num_sms;
   info->workspace_bytes = int64_t(s->ws_used);
+  info->upload_bytes = int64_t(s->upload_bytes);
   info->decode_imbalance = s->dec_imbalance;
   info->prefill_imbalance = 1.0;
   return BSR_OK;

@@ -27,7 +27,7 @@ struct bsr_schedule {
 
   // one device allocation holding everything the kernels read or own
   uint8_t* d_ws = nullptr;
-  size_t ws_cap = 0, ws_used = 0;
+  size_t ws_cap = 0, ws_used = 0, upload_bytes = 0;
   size_t off_indices = 0, off_items = 0, off_warp_ptr = 0, off_counters = 0, off_rope = 0,
          off_error = 0, off_part_o = 0, off_part_lse = 0;
 

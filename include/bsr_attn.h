@@ -171,7 +171,8 @@ typedef struct bsr_schedule_info {
   int32_t decode_ctas, decode_warps_per_cta;
   int32_t prefill_ctas;
   int32_t num_sms;
-  int64_t workspace_bytes;
+  int64_t workspace_bytes;    /* device workspace of the schedule */
+  int64_t upload_bytes;       /* bytes of the one host-to-device copy a plan makes */
   double decode_imbalance;    /* max / mean planned cost over decode warps */
   double prefill_imbalance;   /* max / mean planned cost over prefill CTAs */
 } bsr_schedule_info_t;

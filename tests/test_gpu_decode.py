@@ -1,0 +1,215 @@
+"""GPU parity of the decode path (plan + run through the C ABI) against the fp64 oracle,
+element by element, on seeded inputs that span several tiles and ragged tails."""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_kv_bsr_gb300 as bsr
+import oracle
+import workloads as wl
+from block_sparse_kv_bsr_gb300 import _build
+from parity import (assert_lse_close, assert_out_close, bits, check_full, device_tensors, plan,
+                    run)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_device):
+    _build.build()
+    bsr.load()
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_tiny_decode(out_dtype):
+    w = wl.config1()
+    out, lse, _ = run(w, out_dtype=out_dtype)
+    check_full(w, out, lse)
+
+
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_small_configs(cfg):
+    w = wl.by_name(cfg, small=True)
+    out, lse, s = run(w)
+    check_full(w, out, lse)
+    out32, lse32, _ = run(w, out_dtype=torch.float32)
+    check_full(w, out32, lse32)
+
+
+@pytest.mark.parametrize("P", [1, 2, 4, 8, 16, 32, 64, 256])
+@pytest.mark.parametrize("D", [64, 128])
+def test_page_sizes(P, D):
+    lens = [1, P, P + 1, 3 * P - 1, 37, 300, 777]
+    w = wl.make_paged(f"p{P}d{D}", 100 + P, lens, Hq=8, Hk=2, D=D, P=P)
+    out, lse, _ = run(w)
+    check_full(w, out, lse)
+
+
+@pytest.mark.parametrize("Hq,Hk", [(8, 8), (8, 2), (16, 2), (32, 8), (16, 1)])
+def test_gqa_groups(Hq, Hk):
+    w = wl.make_paged(f"g{Hq}x{Hk}", 7, [5, 64, 200, 513], Hq=Hq, Hk=Hk, D=128, P=16)
+    out, lse, _ = run(w)
+    check_full(w, out, lse)
+
+
+@pytest.mark.parametrize("rope", [0.0, 5e5])
+@pytest.mark.parametrize("causal", [False, True])
+def test_multi_query_rows(rope, causal):
+    # qo_len * group spans one and several 16-row groups, with ragged row tails
+    w = wl.make_paged("mq", 9, [40, 130, 17, 600], Hq=16, Hk=2, D=128, P=16,
+                      qo_lens=[1, 2, 3, 5], causal=causal, rope_theta=rope)
+    out, lse, _ = run(w)
+    check_full(w, out, lse)
+
+
+def test_rope_long_positions():
+    w = wl.make_paged("ropelong", 11, [5000, 1, 33, 4097], Hq=32, Hk=8, D=128, P=16,
+                      rope_theta=5e5)
+    out, lse, _ = run(w)
+    check_full(w, out, lse)
+
+
+def test_rope_d64():
+    w = wl.make_paged("rope64", 12, [1, 77, 300], Hq=8, Hk=2, D=64, P=16, rope_theta=1e4,
+                      qo_lens=[1, 2, 4], causal=True)
+    out, lse, _ = run(w)
+    check_full(w, out, lse)
+
+
+def test_empty_and_edge_lengths():
+    w = wl.make_paged("edges", 13, [0, 1, 16, 17, 31, 32, 0], Hq=8, Hk=2, D=128, P=16)
+    out, lse, _ = run(w)
+    check_full(w, out, lse)
+    o = out.float().cpu().numpy()
+    assert np.all(o[0] == 0) and np.all(o[6] == 0)
+    assert np.all(np.isneginf(lse.cpu().numpy()[[0, 6]]))
+
+
+def test_dropped_blocks_are_skipped():
+    w = wl.make_paged("drop", 14, [2000, 50, 900, 16], Hq=32, Hk=8, D=128, P=16, drop=0.5)
+    out, lse, _ = run(w)
+    check_full(w, out, lse)
+
+
+def test_long_sequence_split_and_merged():
+    # one long request: the planner must cut it over many warps and merge the pieces
+    w = wl.make_paged("long", 15, [60000], Hq=32, Hk=8, D=128, P=16)
+    out, lse, s = run(w)
+    assert s.info()["num_split_streams"] == 8
+    check_full(w, out, lse)
+
+
+def test_run_is_deterministic_and_replan_in_place():
+    w = wl.config3(small=True)
+    t = device_tensors(w)
+    out1, lse1, s = run(w, t)
+    out2, lse2, s2 = run(w, t, schedule=s)   # re-plan into the same schedule
+    assert s2 is s
+    assert torch.equal(bits_t(out1), bits_t(out2)) and torch.equal(lse1, lse2)
+
+
+def bits_t(x):
+    return x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32)
+
+
+def test_cuda_graph_capture_replays_identically():
+    w = wl.config2(small=True)
+    q, k, v = device_tensors(w)
+    s = plan(w)
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta, out=out,
+                         lse=lse)   # warm-up: tensor maps, function attributes
+    torch.cuda.synchronize()
+    ref_out, ref_lse = out.clone(), lse.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta, out=out,
+                         lse=lse, stream=stream)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(bits_t(out), bits_t(ref_out)) and torch.equal(lse, ref_lse)
+
+
+def test_mismatched_run_arguments_are_rejected():
+    w = wl.config2(small=True)
+    q, k, v = device_tensors(w)
+    s = plan(w)
+    with pytest.raises(bsr.BsrError) as e:
+        bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, rope_theta=0.0)
+    assert e.value.code == -7
+    with pytest.raises(bsr.BsrError) as e:
+        bsr.bsr_attn_run(s, q, k, v, sm_scale=-1.0, rope_theta=w.rope_theta)
+    assert e.value.code == -1
+
+
+# ---------------------------------------------------------------- merge_states
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("D", [64, 128])
+def test_merge_states(dtype, D):
+    g = torch.Generator().manual_seed(5)
+    rows, heads = 37, 6
+    oa = torch.randn(rows, heads, D, generator=g).to(dtype)
+    ob = torch.randn(rows, heads, D, generator=g).to(dtype)
+    la = (torch.randn(rows, heads, generator=g) * 3).float()
+    lb = (torch.randn(rows, heads, generator=g) * 3).float()
+    la[0, 0] = -float("inf")            # one side empty
+    la[1, :] = -float("inf")
+    lb[1, :] = -float("inf")            # both sides empty
+    oa[1] = float("nan")                # an empty state's o must not leak
+    ob[1] = float("nan")
+    ro, rl = oracle.merge_states(oa.double().numpy(), la.double().numpy(),
+                                 ob.double().numpy(), lb.double().numpy())
+    dev = "cuda:0"
+    o, l = bsr.bsr_merge_states(oa.to(dev), la.to(dev), ob.to(dev), lb.to(dev))
+    torch.cuda.synchronize()
+    assert_out_close(o.float().cpu().numpy(), ro, dtype == torch.bfloat16, "merge")
+    assert_lse_close(l.cpu().numpy(), rl, "merge")
+    # in place into o_a / lse_a
+    a, al = oa.to(dev), la.to(dev)
+    bsr.bsr_merge_states(a, al, ob.to(dev), lb.to(dev), o_out=a, lse_out=al)
+    torch.cuda.synchronize()
+    assert torch.equal(bits_t(a), bits_t(o)) and torch.equal(al, l)
+
+
+# ---------------------------------------------------------------- append_kv
+
+@pytest.mark.parametrize("P,D", [(16, 128), (1, 64), (256, 128), (8, 128)])
+def test_append_kv_is_bit_exact(P, D):
+    w = wl.make_paged("app", 21, [40, 9, 300, 1], Hq=8, Hk=2, D=D, P=P, qo_lens=[5, 9, 17, 1],
+                      causal=True, append=True)
+    kp, vp = oracle.append_kv(w.k_new, w.v_new, w.append_indptr, w.indptr, w.indices,
+                              w.last_page_len, w.k_pages, w.v_pages, num_kv_heads=2, head_dim=D,
+                              page_size=P)
+    dev = "cuda:0"
+    k, v = w.k_pages.to(dev), w.v_pages.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    bsr.bsr_append_kv(w.k_new.to(dev), w.v_new.to(dev), w.append_indptr.to(dev),
+                      w.indptr.to(dev), w.indices.to(dev), w.last_page_len.to(dev), k, v,
+                      device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(bits(k).view(np.uint16), kp)
+    assert np.array_equal(bits(v).view(np.uint16), vp)
+
+
+def test_append_rejects_out_of_range_page_on_device():
+    w = wl.make_paged("appbad", 22, [40], Hq=8, Hk=2, D=128, P=16, qo_lens=[3], causal=True,
+                      append=True)
+    dev = "cuda:0"
+    bad = w.indices.clone()
+    bad[-1] = w.num_pages + 5
+    k, v = w.k_pages.to(dev), w.v_pages.to(dev)
+    before = bits(k).copy()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    bsr.bsr_append_kv(w.k_new.to(dev), w.v_new.to(dev), w.append_indptr.to(dev),
+                      w.indptr.to(dev), bad.to(dev), w.last_page_len.to(dev), k, v,
+                      device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    assert np.array_equal(bits(k), before)
