@@ -5,14 +5,25 @@
 namespace bsr {
 
 namespace {
+constexpr int kMaxDevices = 64;
+
 template <bool ROPE, bool R16, bool SMALLP>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                        int grid, cudaStream_t stream) {
   auto kern = bsr_decode_kernel<64, ROPE, R16, SMALLP>;
   constexpr size_t smem = DecodeCfg<64>::kSmemBytes;
-  // The attribute is per device; setting it again is harmless and cheap.
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+  // The shared-memory opt-in is per device; set it on the first launch there so
+  // that later launches (including ones under stream capture) make no extra call.
+  static bool opted_in[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!opted_in[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
+    if (e != cudaSuccess) return e;
+    opted_in[dev] = true;
+  }
   kern<<<grid, kDecodeWarps * 32, smem, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }
