@@ -18,7 +18,8 @@ from . import _build
 __all__ = [
     "BsrError", "load", "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run",
     "bsr_merge_states", "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info",
-    "bsr_last_device_error", "bsr_status_string", "Schedule", "EXPORTED_SYMBOLS",
+    "bsr_last_device_error", "bsr_status_string", "bsr_attn_decode_noalloc", "Schedule",
+    "EXPORTED_SYMBOLS",
 ]
 
 BSR_OK = 0
@@ -28,7 +29,7 @@ BSR_DTYPE_F32 = 1
 EXPORTED_SYMBOLS = (
     "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run", "bsr_merge_states", "bsr_append_kv",
     "bsr_schedule_destroy", "bsr_schedule_get_info", "bsr_last_device_error",
-    "bsr_status_string",
+    "bsr_status_string", "bsr_attn_decode_noalloc",
 )
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -95,6 +96,11 @@ def load(path: str | None = None):
     lib.bsr_schedule_get_info.argtypes = [_vp, ctypes.POINTER(_Info)]
     lib.bsr_last_device_error.restype = ctypes.c_int
     lib.bsr_last_device_error.argtypes = [_vp]
+    lib.bsr_attn_decode_noalloc.restype = ctypes.c_int
+    lib.bsr_attn_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _vp,
+                                            ctypes.c_int32, _vp, _vp, _vp]
     lib.bsr_status_string.restype = ctypes.c_char_p
     lib.bsr_status_string.argtypes = [ctypes.c_int]
     _lib = lib
@@ -274,3 +280,25 @@ def bsr_last_device_error(schedule: Schedule) -> int:
     if code < 0:
         raise BsrError(code, "bsr_last_device_error")
     return code
+
+
+def bsr_attn_decode_noalloc(q, k_pages, v_pages, indptr, indices, last_page_len, *,
+                            sm_scale: float, out, lse=None, device_status=None, stream=None):
+    """Decode (one query per request) without any allocation inside the library.
+
+    For callers that cannot allocate device memory at call time: every buffer,
+    including ``out``, ``lse`` and the device page table, is the caller's; the
+    library's scratch is a fixed static device array shared by all calls on a
+    device (serialize calls on one stream).
+    """
+    import torch
+    lib = load()
+    num_pages, Hk, P, D = k_pages.shape
+    batch, Hq = q.shape[0], q.shape[1]
+    dt = BSR_DTYPE_F32 if out.dtype == torch.float32 else BSR_DTYPE_BF16
+    code = lib.bsr_attn_decode_noalloc(_dptr(q), _dptr(k_pages), _dptr(v_pages), _dptr(indptr),
+                                       _dptr(indices), _dptr(last_page_len), batch, Hq, Hk, D, P,
+                                       num_pages, float(sm_scale), _dptr(out), dt, _dptr(lse),
+                                       _dptr(device_status), _vp(_stream_ptr(stream)))
+    _check(code, "bsr_attn_decode_noalloc")
+    return out, lse

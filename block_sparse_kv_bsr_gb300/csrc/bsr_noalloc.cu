@@ -1,0 +1,284 @@
+// bsr_attn_decode_noalloc: split-KV decode for callers that cannot allocate.
+//
+// Some callers cannot call cudaMalloc at the point where they need attention:
+// an inference runtime whose memory is carved up once at start-up by its own
+// allocator, code that runs where allocating would synchronize the device or
+// break a fixed memory budget, or a plugin host that forbids allocation
+// inside its execute callback.  This entry point serves them.  It runs the
+// same decode kernel as bsr_attn_run, but the kernel's scratch memory (work
+// units, per-warp ranges, merge counters, partial states) lives in one
+// file-scope __device__ array of fixed size instead of a planned workspace,
+// and the split of each request into key chunks is computed on the device
+// from the device-resident page table.  Nothing is allocated: no cudaMalloc,
+// no cudaFree, no pinned or pageable host buffer.
+//
+// Costs of that choice, for the user: the array (kScratchBytes, about 17 MB)
+// is held on every GPU that loads this library until the process exits; all
+// calls on a device share it, so two calls whose kernels overlap on the GPU
+// race (serialize them on one stream); and the chunking is a fixed equal split
+// per (request, kv head) rather than the host planner's balanced cut.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "bsr_attn.h"
+#include "bsr_schedule.h"
+
+namespace {
+
+using bsr::DecodeItem;
+using bsr::kDecodeWarps;
+using bsr::kMaxDecodeRows;
+using bsr::kStageTokens;
+
+// Capacity of the static scratch: work units of (request, kv head, chunk).
+constexpr int kMaxUnits = 2048;
+// Largest number of chunks one (request, kv head) range is cut into.
+constexpr int kMaxSplits = 64;
+constexpr int kMaxHeadDim = 128;
+constexpr int kMaxDevices = 64;
+
+// Layout of the scratch array (byte offsets, each 256-aligned).
+constexpr size_t kOffItems = 0;
+constexpr size_t kOffWarpPtr = kOffItems + size_t(kMaxUnits) * sizeof(DecodeItem);
+constexpr size_t kOffCounters = kOffWarpPtr + size_t(kMaxUnits + 64) * 4;
+constexpr size_t kOffStatus = kOffCounters + size_t(kMaxUnits) * 4;
+constexpr size_t kOffPartLse = kOffStatus + 256;
+constexpr size_t kOffPartO = kOffPartLse + size_t(kMaxUnits) * kMaxDecodeRows * 4;
+constexpr size_t kScratchBytes = kOffPartO + size_t(kMaxUnits) * kMaxDecodeRows * kMaxHeadDim * 4;
+static_assert(kOffWarpPtr % 256 == 0 && kOffCounters % 256 == 0 && kOffStatus % 256 == 0 &&
+                  kOffPartLse % 256 == 0 && kOffPartO % 256 == 0,
+              "scratch regions must stay 256-byte aligned");
+
+// The scratch itself.  In host code `g_scratch` names a host-side stand-in,
+// not device memory: the host only ever passes the address returned by
+// cudaGetSymbolAddress for the current device.
+static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
+
+// Writes one work unit per (request, kv head, chunk) and the per-warp ranges
+// (one unit per warp), and clears the merge counters: every call starts from
+// a known state whatever the previous call left behind.
+__global__ void fill_units_kernel(uint8_t* scratch, const int32_t* __restrict__ indptr,
+                                  const int32_t* __restrict__ indices,
+                                  const int32_t* __restrict__ last_page_len, int32_t batch,
+                                  int32_t Hk, int32_t group, int32_t P, int32_t num_pages,
+                                  int32_t splits, int32_t* status) {
+  DecodeItem* items = reinterpret_cast<DecodeItem*>(scratch + kOffItems);
+  int32_t* warp_ptr = reinterpret_cast<int32_t*>(scratch + kOffWarpPtr);
+  int32_t* counters = reinterpret_cast<int32_t*>(scratch + kOffCounters);
+  const int32_t units = batch * Hk * splits;
+  const int32_t u = blockIdx.x * blockDim.x + threadIdx.x;
+  if (u == 0) warp_ptr[units] = units;
+  if (u >= units) return;
+  const int32_t s = u % splits;
+  const int32_t bh = u / splits;
+  const int32_t b = bh / Hk, kvh = bh % Hk;
+  const int32_t n = indptr[b + 1] - indptr[b];
+  int32_t L = 0;
+  if (n > 0) {
+    const int32_t last = last_page_len[b];
+    if (last >= 1 && last <= P) {
+      L = (n - 1) * P + last;
+    } else if (status != nullptr) {
+      atomicOr(status, 2);
+    }
+  } else if (n < 0 && status != nullptr) {
+    atomicOr(status, 2);
+  }
+  const int32_t align = P > kStageTokens ? P : kStageTokens;
+  int32_t len = (L + splits - 1) / splits;
+  len = (len + align - 1) / align * align;
+  int32_t t0 = s * len, t1 = t0 + len < L ? t0 + len : L;
+  if (t0 >= L) t0 = t1 = 0;  // an empty chunk still reports an empty state to the merge
+  // The device table cannot be checked on the host: a chunk that names a page
+  // outside the pool is dropped (reported in the status word) instead of read.
+  for (int32_t j = t0 / P; t1 > t0 && j < (t1 + P - 1) / P; ++j) {
+    const int32_t page = indices[indptr[b] + j];
+    if (page < 0 || page >= num_pages) {
+      if (status != nullptr) atomicOr(status, 2);
+      t0 = t1 = 0;
+    }
+  }
+  DecodeItem it;
+  it.req = b;
+  it.kvh = kvh;
+  it.row0 = 0;
+  it.nrows = group;
+  it.tok0 = t0;
+  it.tok1 = t1;
+  it.nchunks = splits;
+  it.first_slot = bh * splits;
+  it.slot = splits > 1 ? u : -1;
+  it.page_base = indptr[b];
+  it.q_row0 = b;
+  it.qpos0 = L - 1;
+  items[u] = it;
+  warp_ptr[u] = u;
+  if (s == 0) counters[bh * splits] = 0;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Same tile geometry as the planned path: 16 rows x 64 columns, 128B swizzle.
+bool encode_pool(CUtensorMap* tm, const void* base, int64_t rows, int D) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint32_t rank;
+  if (D == 128) {
+    rank = 3;
+    dims[0] = 64; dims[1] = 2; dims[2] = cuuint64_t(rows);
+    strides[0] = 128; strides[1] = 256;
+    box[0] = 64; box[1] = 1; box[2] = kStageTokens;
+  } else {
+    rank = 2;
+    dims[0] = 64; dims[1] = cuuint64_t(rows);
+    strides[0] = 128;
+    box[0] = 64; box[1] = kStageTokens;
+  }
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array, looked up once per device (with that
+// device current) on the first call made there.
+uint8_t* scratch_on(int dev) {
+  static uint8_t* addr[kMaxDevices] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    addr[dev] = static_cast<uint8_t*>(p);
+  }
+  return addr[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* indptr, const int32_t* indices,
+                                       const int32_t* last_page_len, int32_t batch,
+                                       int32_t num_qo_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t page_size,
+                                       int32_t num_pages_in_pool, float sm_scale, void* out,
+                                       int32_t out_dtype, float* lse, int32_t* device_status,
+                                       void* stream_v) {
+  if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || num_pages_in_pool < 0)
+    return BSR_ERR_INVALID_ARGUMENT;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return BSR_ERR_INVALID_ARGUMENT;
+  if (out_dtype != BSR_DTYPE_BF16 && out_dtype != BSR_DTYPE_F32) return BSR_ERR_INVALID_ARGUMENT;
+  if (head_dim != 64 && head_dim != 128) return BSR_ERR_UNSUPPORTED;
+  if (page_size <= 0 || page_size > 256 || (page_size & (page_size - 1))) return BSR_ERR_UNSUPPORTED;
+  if (num_qo_heads % num_kv_heads != 0 || num_qo_heads / num_kv_heads > kMaxDecodeRows)
+    return BSR_ERR_UNSUPPORTED;
+  if (int64_t(num_pages_in_pool) * num_kv_heads * page_size > INT32_MAX) return BSR_ERR_UNSUPPORTED;
+  // The static scratch holds kMaxUnits (request, kv head, chunk) units: larger batches are
+  // refused here, before anything is launched.
+  if (int64_t(batch) * num_kv_heads > kMaxUnits) return BSR_ERR_UNSUPPORTED;
+  if (batch == 0) return BSR_OK;
+  if (!q || !k_pages || !v_pages || !indptr || !indices || !last_page_len || !out)
+    return BSR_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(q, 4) ||
+      !aligned(out, out_dtype == BSR_DTYPE_F32 ? 8 : 4) || (lse && !aligned(lse, 4)))
+    return BSR_ERR_INVALID_ARGUMENT;
+  const cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return BSR_ERR_CUDA;
+  }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return BSR_ERR_CUDA;
+  }
+  uint8_t* scratch = scratch_on(dev);
+  if (scratch == nullptr) return BSR_ERR_CUDA;
+
+  // Equal split per (request, kv head): enough units to cover every warp slot of the
+  // persistent grid, never more than the scratch holds.
+  const int64_t pairs = int64_t(batch) * num_kv_heads;
+  const int64_t want = int64_t(sms) * kDecodeWarps;
+  int64_t splits = (want + pairs - 1) / pairs;
+  if (splits > kMaxSplits) splits = kMaxSplits;
+  if (splits * pairs > kMaxUnits) splits = kMaxUnits / pairs;
+  if (splits < 1) splits = 1;
+  const int32_t units = int32_t(splits * pairs);
+  const int32_t group = num_qo_heads / num_kv_heads;
+  int32_t* status = device_status != nullptr
+                        ? device_status
+                        : reinterpret_cast<int32_t*>(scratch + kOffStatus);
+
+  fill_units_kernel<<<(units + 255) / 256, 256, 0, stream>>>(
+      scratch, indptr, indices, last_page_len, batch, num_kv_heads, group, page_size,
+      num_pages_in_pool, int32_t(splits), status);
+  if (cudaGetLastError() != cudaSuccess) return BSR_ERR_CUDA;
+
+  const bool smallp = page_size < kStageTokens;
+  CUtensorMap tk{}, tv{};
+  const int64_t rows = int64_t(num_pages_in_pool) * num_kv_heads * page_size;
+  if (!smallp) {
+    if (rows <= 0 || !encode_pool(&tk, k_pages, rows, head_dim) ||
+        !encode_pool(&tv, v_pages, rows, head_dim))
+      return BSR_ERR_CUDA;
+  }
+  bsr::DecodeParams p{};
+  p.items = reinterpret_cast<const DecodeItem*>(scratch + kOffItems);
+  p.warp_ptr = reinterpret_cast<const int32_t*>(scratch + kOffWarpPtr);
+  p.counters = reinterpret_cast<int32_t*>(scratch + kOffCounters);
+  p.part_o = reinterpret_cast<float*>(scratch + kOffPartO);
+  p.part_lse = reinterpret_cast<float*>(scratch + kOffPartLse);
+  p.indices = indices;
+  p.rope = nullptr;
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_pages = k_pages;
+  p.v_pages = v_pages;
+  p.out = out;
+  p.lse = lse;
+  p.error = status;
+  p.scale_log2 = float(double(sm_scale) * 1.4426950408889634);
+  p.Hq = num_qo_heads;
+  p.Hk = num_kv_heads;
+  p.group = group;
+  p.P = page_size;
+  p.causal = 0;
+  p.out_f32 = out_dtype == BSR_DTYPE_F32;
+  p.num_warps = units;
+  p.rope_max_pos = 0;
+  p.wait_limit_ns = 1000000000ull;
+  const int grid = (units + kDecodeWarps - 1) / kDecodeWarps;
+  const bool r16 = group > 8;
+  const cudaError_t e =
+      head_dim == 128 ? bsr::launch_decode_d128(false, r16, smallp, tk, tv, p, grid, stream)
+                      : bsr::launch_decode_d64(false, r16, smallp, tk, tv, p, grid, stream);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return BSR_ERR_CUDA;
+  }
+  return BSR_OK;
+}

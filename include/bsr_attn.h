@@ -198,6 +198,37 @@ int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
                        float rope_theta, int32_t num_sms, bsr_schedule_info_t* info,
                        int32_t* units, int64_t max_units);
 
+/*
+ * bsr_attn_decode_noalloc — decode attention that allocates nothing.
+ * The paper has no counterpart; this is a service to callers that cannot call
+ * cudaMalloc where they need attention (a runtime that carves all device
+ * memory once at start-up with its own allocator, or a host that forbids
+ * allocation inside its execute step).
+ *
+ * Computes what bsr_attn_plan + bsr_attn_run compute for one query per
+ * request, non-causal, without RoPE: q [batch, Hq, D] bf16; k_pages/v_pages
+ * [num_pages_in_pool, Hk, P, D] bf16; indptr [batch+1], indices, last_page_len
+ * [batch] are DEVICE arrays; out [batch, Hq, D] (out_dtype) and lse
+ * [batch, Hq] fp32 (may be NULL) are written.  All buffers are the caller's.
+ * Each (request, kv head) key range is cut into equal chunks on the device.
+ * The kernel's scratch lives in one static device array of about 17 MB that
+ * every GPU loading this library holds until the process exits; it holds at
+ * most 2048 (request, kv head, chunk) units, so batch * num_kv_heads above
+ * 2048 is refused with BSR_ERR_UNSUPPORTED before anything runs.  The first
+ * call on a device looks up the array's device address (make that call before
+ * any stream capture).  All calls on a device share the array and every call
+ * rewrites it: calls whose kernels overlap on the GPU race, so keep them on
+ * one stream.  A request whose table entries are malformed, or whose pages
+ * fall outside the pool, is treated as empty and bit 1 is OR-ed into
+ * *device_status (device int32, may be NULL); bit 0 means a bounded wait gave up.
+ */
+int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                            const int32_t* indptr, const int32_t* indices,
+                            const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
+                            int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                            int32_t num_pages_in_pool, float sm_scale, void* out,
+                            int32_t out_dtype, float* lse, int32_t* device_status, void* stream);
+
 /* Device-side status word of a schedule (0 = fine; bit 0: a kernel gave up on
  * a bounded wait).  Synchronizes the schedule's device; returns the word, or
  * a negative BSR_ERR_* code. */

@@ -1,0 +1,97 @@
+"""bsr_attn_decode_noalloc: decode for callers that cannot allocate device memory.
+
+Such callers (a serving runtime that hands out all device memory from its own
+pool, a host that forbids allocation while it executes a step) pass every
+buffer themselves; the library keeps its scratch in a fixed static device array.
+Here the entry point is called through the C ABI and its output is checked
+against the planned entry point (bsr_attn_plan + bsr_attn_run) on the same
+inputs, with the parity tolerances, on two calls in a row (the second call
+reuses the scratch the first one left behind).  This file is collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_kv_bsr_gb300 as bsr
+import workloads as wl
+from block_sparse_kv_bsr_gb300 import _build
+from parity import assert_lse_close, assert_out_close, check_full, device_tensors, run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_device):
+    _build.build()
+    bsr.load()
+
+
+def call_noalloc(w, tensors, out, lse, status):
+    """Call the C entry point directly (ctypes), every buffer preallocated by the caller."""
+    lib = bsr.load()
+    q, k, v = tensors
+    dev_tab = [w.indptr.to(q.device), w.indices.to(q.device), w.last_page_len.to(q.device)]
+    code = lib.bsr_attn_decode_noalloc(
+        ctypes.c_void_p(q.data_ptr()), ctypes.c_void_p(k.data_ptr()),
+        ctypes.c_void_p(v.data_ptr()), ctypes.c_void_p(dev_tab[0].data_ptr()),
+        ctypes.c_void_p(dev_tab[1].data_ptr()), ctypes.c_void_p(dev_tab[2].data_ptr()),
+        w.batch, w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size, w.num_pages,
+        ctypes.c_float(w.sm_scale), ctypes.c_void_p(out.data_ptr()),
+        1 if out.dtype == torch.float32 else 0, ctypes.c_void_p(lse.data_ptr()),
+        ctypes.c_void_p(status.data_ptr()),
+        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    return code
+
+
+CASES = {
+    "tiny_d64": lambda: wl.config1(),
+    "skewed_small_d128": lambda: wl.config3(small=True),
+    "page1_gqa8": lambda: wl.make_paged("p1", 31, [1, 40, 0, 333], Hq=16, Hk=2, D=128, P=1),
+    "page256": lambda: wl.make_paged("p256", 32, [300, 5, 1000], Hq=8, Hk=8, D=64, P=256),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_noalloc_matches_planned_entry_point_twice(name, out_dtype):
+    w = CASES[name]()
+    tensors = device_tensors(w)
+    ref_out, ref_lse, _ = run(w, tensors, out_dtype=out_dtype)
+    ref_o = ref_out.float().cpu().numpy().astype(np.float64)
+    ref_l = ref_lse.cpu().numpy().astype(np.float64)
+    bf16 = out_dtype == torch.bfloat16
+    for call in range(2):
+        out = torch.full_like(ref_out, float("nan"))
+        lse = torch.full_like(ref_lse, float("nan"))
+        status = torch.zeros(1, dtype=torch.int32, device=ref_out.device)
+        assert call_noalloc(w, tensors, out, lse, status) == 0
+        assert int(status.item()) == 0
+        assert_out_close(out.float().cpu().numpy(), ref_o, bf16, f"{name} call {call}")
+        assert_lse_close(lse.cpu().numpy(), ref_l, f"{name} call {call}")
+        check_full(w, out, lse)      # and against the fp64 oracle
+
+
+def test_noalloc_refuses_batches_beyond_its_scratch():
+    w = wl.make_paged("big", 33, [16] * 257, Hq=8, Hk=8, D=64, P=16)   # 2056 > 2048 units
+    tensors = device_tensors(w)
+    out = torch.empty_like(tensors[0])
+    lse = torch.empty(tensors[0].shape[:2], dtype=torch.float32, device=out.device)
+    status = torch.zeros(1, dtype=torch.int32, device=out.device)
+    assert call_noalloc(w, tensors, out, lse, status) == -2     # BSR_ERR_UNSUPPORTED
+
+
+def test_noalloc_reports_pages_outside_the_pool():
+    w = wl.make_paged("badpage", 34, [40, 20], Hq=8, Hk=2, D=128, P=16)
+    bad = w.indices.clone()
+    bad[0] = w.num_pages + 3
+    w.indices = bad
+    tensors = device_tensors(w)
+    out = torch.empty_like(tensors[0])
+    lse = torch.empty(tensors[0].shape[:2], dtype=torch.float32, device=out.device)
+    status = torch.zeros(1, dtype=torch.int32, device=out.device)
+    assert call_noalloc(w, tensors, out, lse, status) == 0
+    assert int(status.item()) & 2
+    assert torch.isfinite(out.float()).all()
