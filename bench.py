@@ -40,7 +40,7 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "bsr_decode_skewed_b128.md")
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--small", action="store_true", help="small case (profiling, smoke)")
@@ -65,33 +65,59 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples of SM clock and throttle reasons around the timed region.
+
+    The sampler is started (and its first sample awaited) before the timed
+    region; samples that arrive inside the region are summarized.  A region
+    shorter than the sampling period gets the nearest sample, marked as such.
+    """
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 50):
         self.gpu = gpu_index
+        self.period = period_ms
         self.proc = None
-        self.lines = []
+        self.samples = []          # (host time, sm_mhz, max_mhz, reasons)
+        self.t0 = self.t1 = None
 
-    def __enter__(self):
+    def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
         except Exception:
             self.proc = None
+            return self
+        threading.Thread(target=self._read, daemon=True).start()
+        deadline = time.time() + 10.0
+        while not self.samples and time.time() < deadline:
+            time.sleep(0.01)
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm, mx = float(parts[1]), float(parts[2])
+            except ValueError:
+                continue
+            reasons = {n for n, v in zip(self.NAMES, parts[5:9]) if v.lower().startswith("active")}
+            self.samples.append((time.time(), sm, mx, reasons))
 
-    def __exit__(self, *a):
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+        time.sleep(2 * self.period / 1000.0)   # let a sample that straddles the end arrive
+
+    def stop(self):
         if self.proc:
             self.proc.terminate()
             try:
@@ -100,22 +126,20 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [x.strip() for x in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if not self.samples or self.t0 is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        inside = [x for x in self.samples if self.t0 <= x[0] <= self.t1 + self.period / 1000.0]
+        how = "inside timed region"
+        if not inside:
+            mid = 0.5 * (self.t0 + self.t1)
+            inside = [min(self.samples, key=lambda x: abs(x[0] - mid))]
+            how = "nearest sample (timed region shorter than the sampling period)"
+        reasons = set()
+        for x in inside:
+            reasons |= x[3]
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": inside[0][2],
+                "reasons": sorted(reasons), "samples": len(inside), "period_ms": self.period,
+                "window": how}
 
 
 def traffic_from_profile(digest: str):
@@ -130,38 +154,25 @@ def traffic_from_profile(digest: str):
     return float(m.group(1))
 
 
-def cpu_baseline(w, budget_s=12.0):
-    """Time the fp64 oracle on whole requests of the batch (shortest-first sample up to budget)."""
-    import numpy as np
+def cpu_baseline(w, budget_s=10.0, min_passes=1):
+    """Time the fp64 oracle over whole passes of the batch until `budget_s` is spent."""
     import oracle
     import workloads as wl
     threads = oracle.default_threads()
-    # one warm call, then grow the sample until the budget is used
-    order = list(range(w.batch))
-    rng = np.random.default_rng(0)
-    rng.shuffle(order)
-    chosen, done_bytes, spent = [], 0, 0.0
-    for b in order:
-        rows = np.arange(int(w.qo_indptr[b]), int(w.qo_indptr[b + 1]))
-        heads = np.arange(w.num_qo_heads)
-        rr = np.repeat(rows, len(heads))
-        hh = np.tile(heads, len(rows))
+    alg = wl.algorithmic_bytes(w)
+    passes, spent = 0, 0.0
+    while passes < min_passes or spent < budget_s:
         t0 = time.perf_counter()
         oracle.attention(w.q, w.k_pages, w.v_pages, w.indptr, w.indices, w.last_page_len,
                          w.qo_indptr, num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
                          head_dim=w.head_dim, page_size=w.page_size, sm_scale=w.sm_scale,
-                         rope_theta=w.rope_theta, causal=w.causal, rows=rr, heads=hh,
-                         threads=threads)
+                         rope_theta=w.rope_theta, causal=w.causal, threads=threads)
         spent += time.perf_counter() - t0
-        chosen.append(b)
-        done_bytes += w.kv_len[b] * 2 * w.num_kv_heads * w.head_dim * 2 + \
-            len(rows) * w.num_qo_heads * (w.head_dim * 4 + 4)
-        if spent >= budget_s:
-            break
-    return {"value": done_bytes / spent / 1e9, "unit": "GB/s", "cores": threads,
+        passes += 1
+    return {"value": round(alg * passes / spent / 1e9, 3), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
-            "sample": f"{len(chosen)} of {w.batch} requests (all heads), {sum(w.kv_len[b] for b in chosen)} "
-                      f"keys, fp64 C oracle, {spent:.1f} s"}
+            "sample": f"{passes} full pass(es) of the {w.batch}-request batch "
+                      f"({w.active_tokens} keys, all heads), fp64 C oracle, {spent:.1f} s"}
 
 
 def main():
@@ -209,16 +220,19 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for a, b in evs:
-            a.record(stream)
-            step()
-            b.record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize()
+    clocks = ClockSampler(local).start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks.mark_start()
+    t_start.record(stream)
+    for a, b in evs:
+        a.record(stream)
+        step()
+        b.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_end()
+    clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
@@ -310,29 +324,24 @@ def main():
 
 
 def run_reference(args, rank, world):
-    """The oracle as it stands, on this host's cores, on a bounded sample of the workload."""
+    """The oracle as it stands, on this host's cores: one step = one pass over the batch."""
     if rank != 0:
         return
     import workloads as wl
     w = wl.config3(small=args.small)
     for _ in range(args.warmup):
-        cpu_baseline(w, budget_s=0.5)
-    vals, samples = [], []
+        cpu_baseline(w, budget_s=0.0)
     t0 = time.perf_counter()
-    for _ in range(args.steps):
-        r = cpu_baseline(w, budget_s=2.0)
-        vals.append(r["value"])
-        samples.append(r["sample"])
+    r = cpu_baseline(w, budget_s=0.0, min_passes=args.steps)
     elapsed = time.perf_counter() - t0
-    v = statistics.mean(vals)
-    res = {"impl": "reference", "metric": METRIC, "value": round(v, 3), "unit": "GB/s",
+    res = {"impl": "reference", "metric": METRIC, "value": r["value"], "unit": "GB/s",
            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
            "ms_per_step": round(elapsed * 1e3 / args.steps, 2), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": w.name},
-           "cpu_baseline": {"value": round(v, 3), "unit": "GB/s", "cores": r["cores"],
-                            "kind": "oracle", "sample": samples[-1]},
-           "e2e": {"value": round(v, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+           "cpu_baseline": {"value": r["value"], "unit": "GB/s", "cores": r["cores"],
+                            "kind": "oracle", "sample": r["sample"]},
+           "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(res))
 

@@ -46,12 +46,13 @@ struct DecodeCfg {
   static constexpr int kHalves = D / 64;                        // 128-byte column blocks per row
   static constexpr int kStageKBytes = kStageTokens * D * 2;      // one K (or V) tile
   static constexpr int kStageBytes = 2 * kStageKBytes;           // K + V
-  static constexpr int kStages = (D == 128) ? 3 : 6;             // ring depth per warp
+  static constexpr int kStages = (D == 128) ? BSR_DECODE_STAGES_D128 : BSR_DECODE_STAGES_D64;
   static constexpr int kKSteps = D / 16;
   static constexpr int kNTiles = D / 8;
   static constexpr int kRopeK = D / 8;                           // (cos, sin) pairs per (pos, quad)
   static constexpr size_t kSmemBytes =
       size_t(kDecodeWarps) * kStages * kStageBytes + size_t(kDecodeWarps) * kStages * 8 + 1024;
+  static_assert(kSmemBytes <= 232448, "decode stages exceed the shared memory of one SM");
 };
 
 // Byte offset of (token t, column d) in a 16-token tile stored as
@@ -86,6 +87,104 @@ __device__ __forceinline__ void rope_pair(uint32_t xlo, uint32_t xhi, float2 cs0
   y[0] = b0 * cs0.x + a0 * cs0.y;
   x[1] = a1 * cs1.x - b1 * cs1.y;
   y[1] = b1 * cs1.x + a1 * cs1.y;
+}
+
+// Merge the partial states of one split range (the last-arriving warp calls
+// this).  Rows are taken four at a time; the chunk maxima and sums are
+// computed lane-parallel over chunks, and the weighted sum of partial outputs
+// (each lane owns D/32 columns) is accumulated in chunk order, so the result
+// does not depend on which warp merges.  Loads of four chunks are issued
+// together to keep the merge off the kernel's tail.
+template <int D>
+__device__ __forceinline__ void merge_range(const DecodeParams& p, const DecodeItem& ci, int lane) {
+  constexpr int CPL = D / 32;
+  constexpr float kLn2 = 0.69314718055994530942f;
+  const int nck = ci.nchunks, group = p.group;
+  const float* lse_base = p.part_lse + size_t(ci.first_slot) * kMaxDecodeRows;
+  const float* o_base = p.part_o + size_t(ci.first_slot) * kMaxDecodeRows * D;
+#pragma unroll 1
+  for (int r0 = 0; r0 < ci.nrows; r0 += 4) {
+    const int nr = min(4, ci.nrows - r0);
+    float M[4], S[4], L2[4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) { M[rr] = -INFINITY; S[rr] = 0.f; }
+    // chunk maxima (lane k holds chunk k, k + 32, ...)
+#pragma unroll 1
+    for (int k = lane; k < nck; k += 32) {
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr)
+        if (rr < nr) M[rr] = fmaxf(M[rr], __ldcg(lse_base + size_t(k) * kMaxDecodeRows + r0 + rr));
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M[rr] = fmaxf(M[rr], __shfl_xor_sync(0xffffffffu, M[rr], o));
+#pragma unroll 1
+    for (int k = lane; k < nck; k += 32) {
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr)
+        if (rr < nr && M[rr] != -INFINITY)
+          S[rr] += ptx::ex2(__ldcg(lse_base + size_t(k) * kMaxDecodeRows + r0 + rr) - M[rr]);
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) S[rr] += __shfl_xor_sync(0xffffffffu, S[rr], o);
+      L2[rr] = M[rr] == -INFINITY ? -INFINITY : M[rr] + ptx::lg2(S[rr]);
+    }
+    float acc[4][CPL];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[rr][c] = 0.f;
+#pragma unroll 1
+    for (int k0 = 0; k0 < nck; k0 += 4) {
+      float w[4][4], v[4][4][CPL];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const int k = k0 + kk;
+          const bool on = k < nck && rr < nr && L2[rr] != -INFINITY;
+          const size_t sl = size_t(k) * kMaxDecodeRows + r0 + rr;
+          w[kk][rr] = on ? __ldcg(lse_base + sl) : -INFINITY;
+          if constexpr (CPL == 4) {
+            const float4 t = on ? __ldcg(reinterpret_cast<const float4*>(o_base + sl * D) + lane)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[kk][rr][0] = t.x; v[kk][rr][1] = t.y; v[kk][rr][2 % CPL] = t.z; v[kk][rr][3 % CPL] = t.w;
+          } else {
+            const float2 t = on ? __ldcg(reinterpret_cast<const float2*>(o_base + sl * D) + lane)
+                                : make_float2(0.f, 0.f);
+            v[kk][rr][0] = t.x; v[kk][rr][1 % CPL] = t.y;
+          }
+        }
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          const float wt = w[kk][rr] == -INFINITY ? 0.f : ptx::ex2(w[kk][rr] - L2[rr]);
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) acc[rr][c] += wt * v[kk][rr][c];
+        }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      if (rr >= nr) break;
+      const int R = ci.row0 + r0 + rr;
+      const size_t orow = size_t(ci.q_row0 + R / group) * p.Hq + ci.kvh * group + R % group;
+      if (p.out_f32) {
+        float* dst = static_cast<float*>(p.out) + orow * D + CPL * lane;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) dst[c] = acc[rr][c];
+      } else {
+        uint16_t* dst = static_cast<uint16_t*>(p.out) + orow * D + CPL * lane;
+#pragma unroll
+        for (int c = 0; c < CPL; c += 2)
+          *reinterpret_cast<uint32_t*>(dst + c) = ptx::pack_bf16(acc[rr][c], acc[rr][c + 1]);
+      }
+      if (p.lse != nullptr && lane == 0) p.lse[orow] = L2[rr] * kLn2;
+    }
+  }
 }
 
 template <int D, bool ROPE, bool R16, bool SMALLP>
@@ -535,56 +634,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
         __threadfence();
-        // merge the range's partial states in chunk order; each lane owns D/32 columns
-        constexpr int CPL = D / 32;
-#pragma unroll 1
-        for (int r = 0; r < ci.nrows; ++r) {
-          const int R = ci.row0 + r;
-          const size_t orow = size_t(ci.q_row0 + R / group) * p.Hq + ci.kvh * group + R % group;
-          float M = -INFINITY;
-#pragma unroll 1
-          for (int k = 0; k < ci.nchunks; ++k)
-            M = fmaxf(M, __ldcg(p.part_lse + size_t(ci.first_slot + k) * kMaxDecodeRows + r));
-          float acc[CPL];
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-          float lse2 = -INFINITY;
-          if (M != -INFINITY) {
-            float sum = 0.f;
-#pragma unroll 1
-            for (int k = 0; k < ci.nchunks; ++k)
-              sum += ptx::ex2(__ldcg(p.part_lse + size_t(ci.first_slot + k) * kMaxDecodeRows + r) - M);
-            lse2 = M + ptx::lg2(sum);
-#pragma unroll 1
-            for (int k = 0; k < ci.nchunks; ++k) {
-              const size_t sl = size_t(ci.first_slot + k) * kMaxDecodeRows + r;
-              const float w = ptx::ex2(__ldcg(p.part_lse + sl) - lse2);
-              const float* src = p.part_o + sl * D + CPL * lane;
-              if constexpr (CPL == 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-                acc[0] += w * v.x;
-                acc[1] += w * v.y;
-                acc[2] += w * v.z;
-                acc[3] += w * v.w;
-              } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-                acc[0] += w * v.x;
-                acc[1] += w * v.y;
-              }
-            }
-          }
-          if (p.out_f32) {
-            float* dst = static_cast<float*>(p.out) + orow * D + CPL * lane;
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) dst[c] = acc[c];
-          } else {
-            uint16_t* dst = static_cast<uint16_t*>(p.out) + orow * D + CPL * lane;
-#pragma unroll
-            for (int c = 0; c < CPL; c += 2)
-              *reinterpret_cast<uint32_t*>(dst + c) = ptx::pack_bf16(acc[c], acc[c + 1]);
-          }
-          if (p.lse != nullptr && lane == 0) p.lse[orow] = lse2 * kLn2;
-        }
+        merge_range<D>(p, ci, lane);
         if (lane == 0) atomicExch(p.counters + ci.first_slot, 0);
       }
     }

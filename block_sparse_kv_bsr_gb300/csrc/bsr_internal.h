@@ -16,8 +16,19 @@ namespace bsr {
 constexpr int kStageTokens = 16;
 // Packed (query, head) rows per decode work unit: the M of one mma tile.
 constexpr int kMaxDecodeRows = 16;
-// Warps per decode CTA (each warp is an independent workgroup).
-constexpr int kDecodeWarps = 8;
+// Warps per decode CTA (each warp is an independent workgroup) and pipeline
+// stages per warp; one CTA per SM, so warps x stages x stage bytes must fit
+// the 227 KB of shared memory.  Overridable at build time for tuning sweeps.
+#ifndef BSR_DECODE_WARPS
+#define BSR_DECODE_WARPS 8
+#endif
+#ifndef BSR_DECODE_STAGES_D128
+#define BSR_DECODE_STAGES_D128 3
+#endif
+#ifndef BSR_DECODE_STAGES_D64
+#define BSR_DECODE_STAGES_D64 6
+#endif
+constexpr int kDecodeWarps = BSR_DECODE_WARPS;
 
 // One decode work unit: rows [row0, row0 + nrows) of the packed rows of
 // (request req, kv head kvh) against keys [tok0, tok1).  Packed row R is
@@ -57,6 +68,28 @@ struct DecodeParams {
   int32_t causal, out_f32, num_warps;
   int32_t rope_max_pos;           // last row of the cos/sin table
   uint64_t wait_limit_ns;         // bound on every barrier wait
+};
+
+// Work units of the tensor-core prefill kernel use the same record with up to
+// kPrefillRows packed rows; partial states are [slot][kPrefillRows][D].
+constexpr int kPrefillRows = 128;
+
+struct PrefillParams {
+  const DecodeItem* items;
+  const int32_t* cta_ptr;         // [num_ctas + 1] unit ranges per CTA
+  int32_t* counters;              // [num_partials, 4] arrivals per (split range, row-owner warp)
+  float* part_o;                  // [num_partials, kPrefillRows, D]
+  float* part_lse;                // [num_partials, kPrefillRows] (log2 domain)
+  const int32_t* indices;
+  const float2* rope_nat;         // [rope rows, D / 2] (cos, sin) by frequency, or null
+  const uint16_t* q;
+  void* out;
+  float* lse;
+  int32_t* error;
+  float scale_log2;
+  int32_t Hq, Hk, group, P;
+  int32_t causal, out_f32, num_ctas, rope_max_pos;
+  uint64_t wait_limit_ns;
 };
 
 }  // namespace bsr

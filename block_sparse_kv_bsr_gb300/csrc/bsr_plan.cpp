@@ -39,6 +39,13 @@ constexpr int64_t kMinPiece = 64;
 // Least work (key-equivalents) worth a warp of its own: small batches use
 // fewer warps instead of many tiny pieces.
 constexpr int64_t kMinWarpWork = 128;
+// Prefill: packed rows from which a request takes the tensor-core kernel, the
+// per-unit overhead (Q load, pipeline fill, epilogue) in keys, the shortest
+// key piece and the least work per CTA.
+constexpr int32_t kPrefillMinRows = 64;
+constexpr int64_t kPrefillOverhead = 256;
+constexpr int64_t kPrefillMinPiece = 512;
+constexpr int64_t kPrefillMinCtaWork = 1024;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -46,6 +53,7 @@ bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 // A (request, kv head, row group) range of keys before chunking.
 struct Unit {
   int32_t req, kvh, row0, nrows, kend;
+  int32_t page_base, q_row0, qpos0;
 };
 
 struct Piece {
@@ -73,9 +81,156 @@ void build_rope_table(float* dst, int32_t rows, int32_t D, double theta) {
       }
 }
 
+// The same angles in frequency order, [pos][f] with f = 0 .. D/2-1 (prefill kernel).
+void build_rope_table_natural(float* dst, int32_t rows, int32_t D, double theta) {
+  for (int f = 0; f < D / 2; ++f) {
+    const double omega = std::pow(theta, -2.0 * double(f) / double(D));
+    for (int32_t pos = 0; pos < rows; ++pos) {
+      const double a = double(pos) * omega;
+      float* e = dst + (size_t(pos) * (D / 2) + f) * 2;
+      e[0] = float(std::cos(a));
+      e[1] = float(std::sin(a));
+    }
+  }
+}
+
 int fail_cuda(cudaError_t e) {
   cudaGetLastError();
   return e == cudaErrorMemoryAllocation ? BSR_ERR_OUT_OF_MEMORY : BSR_ERR_CUDA;
+}
+
+// One kernel's work list: items grouped by worker (a decode warp or a prefill CTA).
+struct WorkList {
+  std::vector<DecodeItem> items;
+  std::vector<int32_t> ptr;          // [workers + 1]
+  int32_t n_partials = 0, n_split = 0, workers = 0;
+  double imbalance = 1.0;
+};
+
+// Cut key ranges into pieces and spread them over at most `max_workers`
+// workers at equal cost.  Ranges are laid end to end, longest first, and the
+// sequence is cut into consecutive per-worker segments of (almost) equal
+// cost: a range that does not fit the current worker's budget is cut at an
+// `align`-key boundary and its remainder continues on the next worker.  Long
+// ranges therefore spread over many workers while short ones fill the rest
+// (the interleaving of long and short work).  The budget is the smallest one
+// for which the cut fits the workers, found by bisection, so the busiest
+// worker carries about one piece-alignment more than the mean.  The result
+// is a pure function of its inputs.
+void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align, int64_t overhead,
+             int64_t min_piece, int64_t min_worker_work, WorkList* out) {
+  std::vector<int32_t> order(units.size());
+  std::iota(order.begin(), order.end(), 0);
+  std::stable_sort(order.begin(), order.end(),
+                   [&](int32_t x, int32_t y) { return units[x].kend > units[y].kend; });
+  int64_t total = 0;
+  for (const Unit& u : units) total += u.kend + overhead;
+  const int workers =
+      units.empty() ? 0
+                    : int(std::max<int64_t>(1, std::min<int64_t>(max_workers, (total + min_worker_work - 1) / min_worker_work)));
+  std::vector<Piece> pieces;
+  std::vector<int32_t> owner;
+  // Cut with budget T; returns the number of workers the cut needs (anything
+  // above `workers` means "does not fit").
+  auto partition = [&](int64_t T, bool record) -> int64_t {
+    if (record) {
+      pieces.clear();
+      owner.clear();
+    }
+    int64_t w = 0, room = T;
+    for (int32_t u : order) {
+      const int64_t kend = units[u].kend;
+      int64_t pos = 0;
+      bool placed = false;  // the piece ending at kend (an empty range still needs one)
+      while (!placed) {
+        const int64_t rest = kend - pos;
+        if (rest + overhead <= room) {
+          if (record) {
+            pieces.push_back({u, int32_t(pos), int32_t(kend), rest + overhead});
+            owner.push_back(int32_t(w));
+          }
+          room -= rest + overhead;
+          pos = kend;
+          placed = true;
+        } else {
+          int64_t take = (room - overhead) / align * align;
+          if (rest - take < min_piece) take = (rest - min_piece) / align * align;
+          const bool fresh = room == T;
+          if (take >= min_piece) {
+            if (record) {
+              pieces.push_back({u, int32_t(pos), int32_t(pos + take), take + overhead});
+              owner.push_back(int32_t(w));
+            }
+            pos += take;
+          } else if (fresh) {
+            return max_workers + 2;  // budget below one piece: cannot make progress
+          }
+          ++w;
+          room = T;
+          if (w >= workers) return w + 1;
+        }
+      }
+    }
+    return w + 1;
+  };
+  if (!units.empty()) {
+    int64_t lo = std::max<int64_t>((total + workers - 1) / workers, 2 * min_piece + overhead + align);
+    int64_t hi = lo;
+    while (partition(hi, false) > workers) hi *= 2;
+    while (lo < hi) {
+      const int64_t mid = lo + (hi - lo) / 2;
+      if (partition(mid, false) <= workers) hi = mid; else lo = mid + 1;
+    }
+    partition(lo, true);
+  }
+
+  std::vector<int32_t> pieces_of_unit(units.size(), 0);
+  for (const Piece& pc : pieces) pieces_of_unit[pc.unit]++;
+  std::vector<int32_t> first_slot(units.size(), -1), next_slot(units.size(), 0);
+  out->n_partials = 0;
+  out->n_split = 0;
+  for (size_t u = 0; u < units.size(); ++u)
+    if (pieces_of_unit[u] > 1) {
+      first_slot[u] = out->n_partials;
+      out->n_partials += pieces_of_unit[u];
+      ++out->n_split;
+    }
+  std::vector<std::vector<int32_t>> per_worker(workers);
+  for (size_t i = 0; i < pieces.size(); ++i) per_worker[owner[i]].push_back(int32_t(i));
+  out->items.clear();
+  out->items.reserve(pieces.size());
+  out->ptr.assign(workers + 1, 0);
+  std::vector<int64_t> load(workers, 0);
+  for (int w = 0; w < workers; ++w) {
+    for (int32_t i : per_worker[w]) {
+      const Piece& pc = pieces[i];
+      const Unit& u = units[pc.unit];
+      DecodeItem it{};
+      it.req = u.req;
+      it.kvh = u.kvh;
+      it.row0 = u.row0;
+      it.nrows = u.nrows;
+      it.tok0 = pc.tok0;
+      it.tok1 = pc.tok1;
+      it.nchunks = pieces_of_unit[pc.unit];
+      it.first_slot = first_slot[pc.unit];
+      // pieces of a range are cut in key order, so slot order is key order
+      it.slot = it.nchunks > 1 ? first_slot[pc.unit] + next_slot[pc.unit]++ : -1;
+      it.page_base = u.page_base;
+      it.q_row0 = u.q_row0;
+      it.qpos0 = u.qpos0;
+      out->items.push_back(it);
+      load[w] += pc.cost;
+    }
+    out->ptr[w + 1] = int32_t(out->items.size());
+  }
+  out->workers = workers;
+  out->imbalance = 1.0;
+  if (workers > 0) {
+    const int64_t mx = *std::max_element(load.begin(), load.end());
+    const double mean = double(std::accumulate(load.begin(), load.end(), int64_t(0))) / workers;
+    out->imbalance = mean > 0 ? double(mx) / mean : 1.0;
+  }
 }
 
 // Everything the planner decides without a GPU: validation, units, cuts,
@@ -84,10 +239,8 @@ struct HostPlan {
   int32_t group = 0;
   int64_t sum_qo = 0, active = 0;
   int32_t max_len = 0, max_rows = 0;
-  std::vector<DecodeItem> items;
-  std::vector<int32_t> warp_ptr;
-  int32_t n_partials = 0, n_split = 0, warps = 0;
-  double imbalance = 1.0;
+  WorkList dec;   // split-KV decode kernel, workers = warps
+  WorkList pre;   // tensor-core prefill kernel, workers = CTAs
 };
 
 int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
@@ -140,157 +293,41 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
     if (indices[e] < 0 || indices[e] >= num_pages_in_pool) return BSR_ERR_PAGE_TABLE;
 
   // ---------------------------------------------------------------- units
-  const int64_t align = std::max<int64_t>(page_size, kStageTokens);
-  std::vector<Unit> units;
+  // A request goes to the tensor-core prefill kernel when its packed rows fill
+  // at least half of a 128-row tile (and the layout suits it); the others use
+  // the decode kernel's 16-row groups.
+  std::vector<Unit> dunits, punits;
   int32_t max_rows = 0;
   for (int32_t b = 0; b < batch; ++b) {
     const int32_t rows = qo_len[b] * group;
     const int32_t qpos0 = kv_len[b] - qo_len[b];
+    const bool prefill = head_dim == 128 && page_size >= kStageTokens && rows >= kPrefillMinRows;
+    const int32_t step = prefill ? bsr::kPrefillRows : kMaxDecodeRows;
     for (int32_t h = 0; h < num_kv_heads; ++h)
-      for (int32_t r0 = 0; r0 < rows; r0 += kMaxDecodeRows) {
-        const int32_t nr = std::min(kMaxDecodeRows, rows - r0);
+      for (int32_t r0 = 0; r0 < rows; r0 += step) {
+        const int32_t nr = std::min(step, rows - r0);
         int64_t kend = kv_len[b];
         if (causal)
           kend = std::min<int64_t>(kend, std::max<int64_t>(0, int64_t(qpos0) + (r0 + nr - 1) / group + 1));
-        units.push_back({b, h, r0, nr, int32_t(kend)});
-        max_rows = std::max(max_rows, nr);
-      }
-  }
-
-  // ---------------------------------------------------------------- cut + balance
-  // Ranges are laid end to end, longest first, and the sequence is cut into
-  // consecutive per-warp segments of (almost) equal cost: a range that does
-  // not fit in the current warp's budget is cut at a stage-aligned key and its
-  // remainder continues on the next warp.  Long ranges therefore spread over
-  // many warps while short ones fill the rest (the interleaving of long and
-  // short work).  The budget is the smallest one for which the cut fits the
-  // warps, found by bisection, so the busiest warp carries about one stage
-  // more than the mean.  The cut is a pure function of the table and SM count.
-  std::vector<int32_t> order(units.size());
-  std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int32_t x, int32_t y) { return units[x].kend > units[y].kend; });
-  int64_t total = 0;
-  for (const Unit& u : units) total += u.kend + kUnitOverhead;
-  const int64_t max_warps = int64_t(num_sms) * kDecodeWarps;
-  const int warps_used =
-      units.empty() ? 0
-                    : int(std::max<int64_t>(1, std::min<int64_t>(max_warps, (total + kMinWarpWork - 1) / kMinWarpWork)));
-  std::vector<Piece> pieces;
-  std::vector<int32_t> owner;
-  // Cut with budget T; returns the number of warps the cut needs (anything
-  // above warps_used means "does not fit").
-  auto partition = [&](int64_t T, bool record) -> int64_t {
-    if (record) {
-      pieces.clear();
-      owner.clear();
-    }
-    int64_t w = 0, room = T;
-    for (int32_t u : order) {
-      const int64_t kend = units[u].kend;
-      int64_t pos = 0;
-      bool placed = false;  // the piece ending at kend (an empty range still needs one)
-      while (!placed) {
-        const int64_t rest = kend - pos;
-        if (rest + kUnitOverhead <= room) {
-          if (record) {
-            pieces.push_back({u, int32_t(pos), int32_t(kend), rest + kUnitOverhead});
-            owner.push_back(int32_t(w));
-          }
-          room -= rest + kUnitOverhead;
-          pos = kend;
-          placed = true;
+        const Unit unit{b, h, r0, nr, int32_t(kend), indptr[b], q_row0[b], qpos0};
+        if (prefill) {
+          punits.push_back(unit);
         } else {
-          int64_t take = (room - kUnitOverhead) / align * align;
-          if (rest - take < kMinPiece) take = (rest - kMinPiece) / align * align;
-          const bool fresh = room == T;
-          if (take >= kMinPiece) {
-            if (record) {
-              pieces.push_back({u, int32_t(pos), int32_t(pos + take), take + kUnitOverhead});
-              owner.push_back(int32_t(w));
-            }
-            pos += take;
-          } else if (fresh) {
-            return max_warps + 2;  // budget below one piece: cannot make progress
-          }
-          ++w;
-          room = T;
-          if (w >= warps_used) return w + 1;
+          dunits.push_back(unit);
+          max_rows = std::max(max_rows, nr);
         }
       }
-    }
-    return w + 1;
-  };
-  if (!units.empty()) {
-    int64_t lo = std::max<int64_t>((total + warps_used - 1) / warps_used,
-                                   2 * kMinPiece + kUnitOverhead + align);
-    int64_t hi = lo;
-    while (partition(hi, false) > warps_used) hi *= 2;
-    while (lo < hi) {
-      const int64_t mid = lo + (hi - lo) / 2;
-      if (partition(mid, false) <= warps_used) hi = mid; else lo = mid + 1;
-    }
-    partition(lo, true);
   }
-
-  // ---------------------------------------------------------------- items
-  std::vector<int32_t> pieces_of_unit(units.size(), 0);
-  for (const Piece& pc : pieces) pieces_of_unit[pc.unit]++;
-  std::vector<int32_t> first_slot(units.size(), -1), next_slot(units.size(), 0);
-  int32_t n_partials = 0, n_split = 0;
-  for (size_t u = 0; u < units.size(); ++u)
-    if (pieces_of_unit[u] > 1) {
-      first_slot[u] = n_partials;
-      n_partials += pieces_of_unit[u];
-      ++n_split;
-    }
-  std::vector<std::vector<int32_t>> per_warp(warps_used);
-  for (size_t i = 0; i < pieces.size(); ++i) per_warp[owner[i]].push_back(int32_t(i));
-  std::vector<DecodeItem> items;
-  items.reserve(pieces.size());
-  std::vector<int32_t> warp_ptr(warps_used + 1, 0);
-  std::vector<int64_t> load(warps_used, 0);
-  for (int w = 0; w < warps_used; ++w) {
-    for (int32_t i : per_warp[w]) {
-      const Piece& pc = pieces[i];
-      const Unit& u = units[pc.unit];
-      DecodeItem it{};
-      it.req = u.req;
-      it.kvh = u.kvh;
-      it.row0 = u.row0;
-      it.nrows = u.nrows;
-      it.tok0 = pc.tok0;
-      it.tok1 = pc.tok1;
-      it.nchunks = pieces_of_unit[pc.unit];
-      it.first_slot = first_slot[pc.unit];
-      // pieces of a range are cut in key order, so slot order is key order
-      it.slot = it.nchunks > 1 ? first_slot[pc.unit] + next_slot[pc.unit]++ : -1;
-      it.page_base = indptr[u.req];
-      it.q_row0 = q_row0[u.req];
-      it.qpos0 = kv_len[u.req] - qo_len[u.req];
-      items.push_back(it);
-      load[w] += pc.cost;
-    }
-    warp_ptr[w + 1] = int32_t(items.size());
-  }
-  double imbalance = 1.0;
-  if (warps_used > 0) {
-    const int64_t mx = *std::max_element(load.begin(), load.end());
-    const double mean = double(std::accumulate(load.begin(), load.end(), int64_t(0))) / warps_used;
-    imbalance = mean > 0 ? double(mx) / mean : 1.0;
-  }
+  balance(dunits, int64_t(num_sms) * kDecodeWarps, std::max<int64_t>(page_size, kStageTokens),
+          kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec);
+  balance(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillRows), kPrefillOverhead,
+          kPrefillMinPiece, kPrefillMinCtaWork, &hp->pre);
 
   hp->group = group;
   hp->sum_qo = sum_qo;
   hp->active = active;
   hp->max_len = max_len;
   hp->max_rows = max_rows;
-  hp->items = std::move(items);
-  hp->warp_ptr = std::move(warp_ptr);
-  hp->n_partials = n_partials;
-  hp->n_split = n_split;
-  hp->warps = warps_used;
-  hp->imbalance = imbalance;
   return BSR_OK;
 }
 
@@ -337,9 +374,12 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
     if (s->h_rope == nullptr || s->rope_cache_theta != rope_theta || s->rope_cache_D != head_dim ||
         s->rope_cache_rows < rope_rows) {
       std::free(s->h_rope);
-      s->h_rope = static_cast<uint8_t*>(std::malloc(rope_bytes));
+      // two tables of the same angles: fragment order (decode) then frequency order (prefill)
+      s->h_rope = static_cast<uint8_t*>(std::malloc(2 * rope_bytes));
       if (s->h_rope == nullptr) return bail(BSR_ERR_OUT_OF_MEMORY);
       build_rope_table(reinterpret_cast<float*>(s->h_rope), rope_rows, head_dim, double(rope_theta));
+      build_rope_table_natural(reinterpret_cast<float*>(s->h_rope + rope_bytes), rope_rows,
+                               head_dim, double(rope_theta));
       s->rope_cache_theta = rope_theta;
       s->rope_cache_D = head_dim;
       s->rope_cache_rows = rope_rows;
@@ -354,14 +394,19 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
     return o;
   };
   const size_t off_indices = take(size_t(std::max<int64_t>(nnz, 1)) * 4);
-  const size_t off_items = take(hp.items.size() * sizeof(DecodeItem));
-  const size_t off_warp_ptr = take(hp.warp_ptr.size() * 4);
-  const size_t off_counters = take(size_t(std::max(hp.n_partials, 1)) * 4);
+  const size_t off_items = take(hp.dec.items.size() * sizeof(DecodeItem));
+  const size_t off_warp_ptr = take(hp.dec.ptr.size() * 4);
+  const size_t off_counters = take(size_t(std::max(hp.dec.n_partials, 1)) * 4);
+  const size_t off_pitems = take(hp.pre.items.size() * sizeof(DecodeItem));
+  const size_t off_cta_ptr = take(hp.pre.ptr.size() * 4);
+  const size_t off_pcounters = take(size_t(std::max(hp.pre.n_partials, 1)) * 4 * 4);  // per row-owner warp
   const size_t off_error = take(16);
-  const size_t off_rope = take(rope_bytes);
+  const size_t off_rope = take(rope ? 2 * rope_bytes : 0);
   const size_t image_bytes = off;  // everything above is uploaded
-  const size_t off_part_o = take(size_t(hp.n_partials) * kMaxDecodeRows * head_dim * 4);
-  const size_t off_part_lse = take(size_t(hp.n_partials) * kMaxDecodeRows * 4);
+  const size_t off_part_o = take(size_t(hp.dec.n_partials) * kMaxDecodeRows * head_dim * 4);
+  const size_t off_part_lse = take(size_t(hp.dec.n_partials) * kMaxDecodeRows * 4);
+  const size_t off_ppart_o = take(size_t(hp.pre.n_partials) * bsr::kPrefillRows * head_dim * 4);
+  const size_t off_ppart_lse = take(size_t(hp.pre.n_partials) * bsr::kPrefillRows * 4);
   const size_t ws_bytes = off;
 
   // ---------------------------------------------------------------- staging + upload
@@ -396,10 +441,13 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   uint8_t* h = s->h_stage;
   std::memset(h, 0, image_bytes);
   if (nnz > 0) std::memcpy(h + off_indices, indices, size_t(nnz) * 4);
-  if (!hp.items.empty())
-    std::memcpy(h + off_items, hp.items.data(), hp.items.size() * sizeof(DecodeItem));
-  std::memcpy(h + off_warp_ptr, hp.warp_ptr.data(), hp.warp_ptr.size() * 4);
-  if (rope) std::memcpy(h + off_rope, s->h_rope, rope_bytes);
+  if (!hp.dec.items.empty())
+    std::memcpy(h + off_items, hp.dec.items.data(), hp.dec.items.size() * sizeof(DecodeItem));
+  std::memcpy(h + off_warp_ptr, hp.dec.ptr.data(), hp.dec.ptr.size() * 4);
+  if (!hp.pre.items.empty())
+    std::memcpy(h + off_pitems, hp.pre.items.data(), hp.pre.items.size() * sizeof(DecodeItem));
+  std::memcpy(h + off_cta_ptr, hp.pre.ptr.data(), hp.pre.ptr.size() * 4);
+  if (rope) std::memcpy(h + off_rope, s->h_rope, 2 * rope_bytes);
   ce = cudaMemcpyAsync(s->d_ws, h, image_bytes, cudaMemcpyHostToDevice, stream);
   if (ce != cudaSuccess) return bail(fail_cuda(ce));
   ce = cudaEventRecord(s->upload_done, stream);
@@ -422,12 +470,23 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->active_tokens = hp.active;
   s->rope_rows = rope_rows;
   s->max_rows = hp.max_rows;
-  s->n_items = int32_t(hp.items.size());
-  s->n_partials = hp.n_partials;
-  s->n_split = hp.n_split;
-  s->dec_warps = hp.warps;
-  s->dec_ctas = (hp.warps + kDecodeWarps - 1) / kDecodeWarps;
-  s->dec_imbalance = hp.imbalance;
+  s->n_items = int32_t(hp.dec.items.size());
+  s->n_partials = hp.dec.n_partials;
+  s->n_split = hp.dec.n_split;
+  s->dec_warps = hp.dec.workers;
+  s->dec_ctas = (hp.dec.workers + kDecodeWarps - 1) / kDecodeWarps;
+  s->dec_imbalance = hp.dec.imbalance;
+  s->n_pitems = int32_t(hp.pre.items.size());
+  s->n_ppartials = hp.pre.n_partials;
+  s->n_psplit = hp.pre.n_split;
+  s->pre_ctas = hp.pre.workers;
+  s->pre_imbalance = hp.pre.imbalance;
+  s->rope_bytes = rope_bytes;
+  s->off_pitems = off_pitems;
+  s->off_cta_ptr = off_cta_ptr;
+  s->off_pcounters = off_pcounters;
+  s->off_ppart_o = off_ppart_o;
+  s->off_ppart_lse = off_ppart_lse;
   s->ws_used = ws_bytes;
   s->upload_bytes = image_bytes;
   s->off_indices = off_indices;
@@ -469,17 +528,17 @@ extern "C" int bsr_schedule_get_info(bsr_schedule_t s, bsr_schedule_info_t* info
   info->sum_qo = s->sum_qo;
   info->active_tokens = s->active_tokens;
   info->num_decode_items = s->n_items;
-  info->num_prefill_items = 0;
-  info->num_split_streams = s->n_split;
-  info->num_partials = s->n_partials;
+  info->num_prefill_items = s->n_pitems;
+  info->num_split_streams = s->n_split + s->n_psplit;
+  info->num_partials = s->n_partials + s->n_ppartials;
   info->decode_ctas = s->dec_ctas;
   info->decode_warps_per_cta = kDecodeWarps;
-  info->prefill_ctas = 0;
+  info->prefill_ctas = s->pre_ctas;
   info->num_sms = s->num_sms;
   info->workspace_bytes = int64_t(s->ws_used);
   info->upload_bytes = int64_t(s->upload_bytes);
   info->decode_imbalance = s->dec_imbalance;
-  info->prefill_imbalance = 1.0;
+  info->prefill_imbalance = s->pre_imbalance;
   return BSR_OK;
 }
 
@@ -506,25 +565,31 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
     info->rope_theta = rope_theta;
     info->sum_qo = hp.sum_qo;
     info->active_tokens = hp.active;
-    info->num_decode_items = int32_t(hp.items.size());
-    info->num_split_streams = hp.n_split;
-    info->num_partials = hp.n_partials;
-    info->decode_ctas = (hp.warps + kDecodeWarps - 1) / kDecodeWarps;
+    info->num_decode_items = int32_t(hp.dec.items.size());
+    info->num_prefill_items = int32_t(hp.pre.items.size());
+    info->num_split_streams = hp.dec.n_split + hp.pre.n_split;
+    info->num_partials = hp.dec.n_partials + hp.pre.n_partials;
+    info->decode_ctas = (hp.dec.workers + kDecodeWarps - 1) / kDecodeWarps;
     info->decode_warps_per_cta = kDecodeWarps;
+    info->prefill_ctas = hp.pre.workers;
     info->num_sms = num_sms;
-    info->decode_imbalance = hp.imbalance;
-    info->prefill_imbalance = 1.0;
+    info->decode_imbalance = hp.dec.imbalance;
+    info->prefill_imbalance = hp.pre.imbalance;
   }
-  const int64_t n = int64_t(hp.items.size());
+  const int64_t n = int64_t(hp.dec.items.size() + hp.pre.items.size());
   if (units != nullptr) {
     if (max_units < n) return BSR_ERR_INVALID_ARGUMENT;
-    for (int32_t w = 0; w < hp.warps; ++w)
-      for (int32_t i = hp.warp_ptr[w]; i < hp.warp_ptr[w + 1]; ++i) {
-        const DecodeItem& it = hp.items[i];
-        int32_t* u = units + int64_t(i) * 8;
-        u[0] = it.req; u[1] = it.kvh; u[2] = it.row0; u[3] = it.nrows;
-        u[4] = it.tok0; u[5] = it.tok1; u[6] = it.slot; u[7] = w;
-      }
+    int64_t i_out = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+      const WorkList& wl = pass == 0 ? hp.dec : hp.pre;
+      for (int32_t w = 0; w < wl.workers; ++w)
+        for (int32_t i = wl.ptr[w]; i < wl.ptr[w + 1]; ++i, ++i_out) {
+          const DecodeItem& it = wl.items[i];
+          int32_t* u = units + i_out * 8;
+          u[0] = it.req; u[1] = it.kvh; u[2] = it.row0; u[3] = it.nrows;
+          u[4] = it.tok0; u[5] = it.tok1; u[6] = it.slot; u[7] = pass == 0 ? w : -1 - w;
+        }
+    }
   }
   return int(n);
 }

@@ -72,7 +72,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return BSR_ERR_INVALID_ARGUMENT;
   if (out_dtype != BSR_DTYPE_BF16 && out_dtype != BSR_DTYPE_F32) return BSR_ERR_INVALID_ARGUMENT;
   if (rope_theta != s->rope_theta || causal != s->causal) return BSR_ERR_SCHEDULE_MISMATCH;
-  if (s->n_items == 0) return BSR_OK;
+  if (s->n_items == 0 && s->n_pitems == 0) return BSR_OK;
   if (q == nullptr || out == nullptr || k_pages == nullptr || v_pages == nullptr)
     return BSR_ERR_INVALID_ARGUMENT;
   if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(q, 4) ||
@@ -94,42 +94,75 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     s->tm_v_ptr = v_pages;
   }
 
-  bsr::DecodeParams p{};
-  p.items = s->dev<const bsr::DecodeItem>(s->off_items);
-  p.warp_ptr = s->dev<const int32_t>(s->off_warp_ptr);
-  p.counters = s->dev<int32_t>(s->off_counters);
-  p.part_o = s->dev<float>(s->off_part_o);
-  p.part_lse = s->dev<float>(s->off_part_lse);
-  p.indices = s->dev<const int32_t>(s->off_indices);
-  p.rope = s->rope_rows > 0 ? s->dev<const float2>(s->off_rope) : nullptr;
-  p.q = static_cast<const uint16_t*>(q);
-  p.k_pages = k_pages;
-  p.v_pages = v_pages;
-  p.out = out;
-  p.lse = lse;
-  p.error = s->dev<int32_t>(s->off_error);
-  p.scale_log2 = float(double(sm_scale) * 1.4426950408889634);
-  p.Hq = s->Hq;
-  p.Hk = s->Hk;
-  p.group = s->group;
-  p.P = s->P;
-  p.causal = s->causal;
-  p.out_f32 = out_dtype == BSR_DTYPE_F32;
-  p.num_warps = s->dec_warps;
-  p.rope_max_pos = s->rope_rows > 0 ? s->rope_rows - 1 : 0;
-  p.wait_limit_ns = 1000000000ull;  // 1 s: orders of magnitude above any healthy wait
-
   const bool rope = s->rope_rows > 0;
-  const bool r16 = s->max_rows > 8;
+  const float scale_log2 = float(double(sm_scale) * 1.4426950408889634);
+  const uint64_t wait_limit_ns = 1000000000ull;  // 1 s: orders of magnitude above any healthy wait
   CUtensorMap dummy{};
   const CUtensorMap& tk = smallp ? dummy : s->tm_k;
   const CUtensorMap& tv = smallp ? dummy : s->tm_v;
-  cudaError_t e = s->D == 128
-                      ? bsr::launch_decode_d128(rope, r16, smallp, tk, tv, p, s->dec_ctas, stream)
-                      : bsr::launch_decode_d64(rope, r16, smallp, tk, tv, p, s->dec_ctas, stream);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return BSR_ERR_CUDA;
+
+  if (s->n_items > 0) {
+    bsr::DecodeParams p{};
+    p.items = s->dev<const bsr::DecodeItem>(s->off_items);
+    p.warp_ptr = s->dev<const int32_t>(s->off_warp_ptr);
+    p.counters = s->dev<int32_t>(s->off_counters);
+    p.part_o = s->dev<float>(s->off_part_o);
+    p.part_lse = s->dev<float>(s->off_part_lse);
+    p.indices = s->dev<const int32_t>(s->off_indices);
+    p.rope = rope ? s->dev<const float2>(s->off_rope) : nullptr;
+    p.q = static_cast<const uint16_t*>(q);
+    p.k_pages = k_pages;
+    p.v_pages = v_pages;
+    p.out = out;
+    p.lse = lse;
+    p.error = s->dev<int32_t>(s->off_error);
+    p.scale_log2 = scale_log2;
+    p.Hq = s->Hq;
+    p.Hk = s->Hk;
+    p.group = s->group;
+    p.P = s->P;
+    p.causal = s->causal;
+    p.out_f32 = out_dtype == BSR_DTYPE_F32;
+    p.num_warps = s->dec_warps;
+    p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
+    p.wait_limit_ns = wait_limit_ns;
+    const bool r16 = s->max_rows > 8;
+    const cudaError_t e =
+        s->D == 128 ? bsr::launch_decode_d128(rope, r16, smallp, tk, tv, p, s->dec_ctas, stream)
+                    : bsr::launch_decode_d64(rope, r16, smallp, tk, tv, p, s->dec_ctas, stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return BSR_ERR_CUDA;
+    }
+  }
+  if (s->n_pitems > 0) {
+    bsr::PrefillParams p{};
+    p.items = s->dev<const bsr::DecodeItem>(s->off_pitems);
+    p.cta_ptr = s->dev<const int32_t>(s->off_cta_ptr);
+    p.counters = s->dev<int32_t>(s->off_pcounters);
+    p.part_o = s->dev<float>(s->off_ppart_o);
+    p.part_lse = s->dev<float>(s->off_ppart_lse);
+    p.indices = s->dev<const int32_t>(s->off_indices);
+    p.rope_nat = rope ? s->dev<const float2>(s->off_rope + s->rope_bytes) : nullptr;
+    p.q = static_cast<const uint16_t*>(q);
+    p.out = out;
+    p.lse = lse;
+    p.error = s->dev<int32_t>(s->off_error);
+    p.scale_log2 = scale_log2;
+    p.Hq = s->Hq;
+    p.Hk = s->Hk;
+    p.group = s->group;
+    p.P = s->P;
+    p.causal = s->causal;
+    p.out_f32 = out_dtype == BSR_DTYPE_F32;
+    p.num_ctas = s->pre_ctas;
+    p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
+    p.wait_limit_ns = wait_limit_ns;
+    const cudaError_t e = bsr::launch_prefill(rope, tk, tv, p, s->pre_ctas, stream);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return BSR_ERR_CUDA;
+    }
   }
   return BSR_OK;
 }

@@ -24,12 +24,17 @@ struct bsr_schedule {
   // decode plan
   int32_t n_items = 0, n_partials = 0, n_split = 0, dec_warps = 0, dec_ctas = 0;
   double dec_imbalance = 0.0;
+  // prefill plan (tensor-core kernel)
+  int32_t n_pitems = 0, n_ppartials = 0, n_psplit = 0, pre_ctas = 0;
+  double pre_imbalance = 1.0;
+  size_t rope_bytes = 0;     // one of the two cos/sin tables (fragment order, then frequency order)
 
   // one device allocation holding everything the kernels read or own
   uint8_t* d_ws = nullptr;
   size_t ws_cap = 0, ws_used = 0, upload_bytes = 0;
   size_t off_indices = 0, off_items = 0, off_warp_ptr = 0, off_counters = 0, off_rope = 0,
          off_error = 0, off_part_o = 0, off_part_lse = 0;
+  size_t off_pitems = 0, off_cta_ptr = 0, off_pcounters = 0, off_ppart_o = 0, off_ppart_lse = 0;
 
   // pinned staging buffer for the single host-to-device upload
   uint8_t* h_stage = nullptr;
@@ -60,4 +65,6 @@ cudaError_t launch_decode_d64(bool rope, bool r16, bool smallp, const CUtensorMa
 cudaError_t launch_decode_d128(bool rope, bool r16, bool smallp, const CUtensorMap& tk,
                                const CUtensorMap& tv, const DecodeParams& p, int grid,
                                cudaStream_t stream);
+cudaError_t launch_prefill(bool rope, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, int grid, cudaStream_t stream);
 }  // namespace bsr

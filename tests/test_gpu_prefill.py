@@ -1,0 +1,90 @@
+"""GPU parity of the tensor-core (tcgen05/TMEM) prefill kernel against the fp64 oracle.
+
+Requests whose packed (query, head) rows fill at least half of a 128-row tile
+take this kernel; the cases cover causal and non-causal attention, RoPE,
+ragged row tiles, key counts that are not multiples of the 128-key tile,
+page sizes 16/32/256 and key ranges split over several CTAs and merged.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_kv_bsr_gb300 as bsr
+import workloads as wl
+from block_sparse_kv_bsr_gb300 import _build
+from parity import (LSE_ATOL, assert_lse_close, assert_out_close, check_full, oracle_full, run)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_device):
+    _build.build()
+    bsr.load()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("P", [16, 32, 256])
+def test_prefill_no_rope(causal, P):
+    w = wl.make_paged(f"pf{P}", 40 + P, [700, 333, 1300], Hq=32, Hk=8, D=128, P=P,
+                      qo_lens=[37, 16, 300], causal=causal)
+    out, lse, s = run(w)
+    info = s.info()
+    assert info["num_prefill_items"] > 0
+    check_full(w, out, lse)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_prefill_rope_causal(out_dtype):
+    w = wl.make_paged("pfrope", 51, [900, 1500], Hq=32, Hk=8, D=128, P=16,
+                      qo_lens=[100, 257], causal=True, rope_theta=5e5)
+    out, lse, s = run(w, out_dtype=out_dtype)
+    assert s.info()["num_prefill_items"] > 0
+    check_full(w, out, lse)
+
+
+def test_prefill_split_ranges_merge():
+    # few row tiles against many keys: the planner cuts key ranges to fill the SMs
+    w = wl.make_paged("pfsplit", 52, [20000], Hq=32, Hk=8, D=128, P=16, qo_lens=[64])
+    out, lse, s = run(w)
+    info = s.info()
+    assert info["num_prefill_items"] > info["num_split_streams"] > 0
+    check_full(w, out, lse)
+
+
+def test_prefill_rows_at_the_class_boundary():
+    # 16 queries x group 4 = 64 rows (prefill) next to 15 x 4 = 60 rows (decode groups)
+    w = wl.make_paged("pfmix", 53, [400, 401], Hq=32, Hk=8, D=128, P=16, qo_lens=[16, 15],
+                      causal=True)
+    out, lse, s = run(w)
+    info = s.info()
+    assert info["num_prefill_items"] > 0 and info["num_decode_items"] > 0
+    check_full(w, out, lse)
+
+
+def test_prefill_rope_short_keys_within_rounding_bound():
+    """RoPE with very few keys per query: the rotated keys are bf16 MMA operands, so
+    each score can move by up to 2^-9 * sm_scale * sum_d |q_d k_d|; lse and out are
+    checked against that bound (plus the usual bars) instead of the bare 1e-3."""
+    w = wl.make_paged("pfshort", 54, [70, 130], Hq=32, Hk=8, D=128, P=16, qo_lens=[64, 64],
+                      causal=True, rope_theta=1e4)
+    out, lse, _ = run(w)
+    ro, rl = oracle_full(w)
+    q = w.q.double()
+    bound = 0.0
+    for b in range(w.batch):
+        pages = w.indices[w.indptr[b]:w.indptr[b + 1]].long()
+        K = w.k_pages[pages].permute(1, 0, 2, 3).reshape(w.num_kv_heads, -1, 128)[:, :w.kv_len[b]]
+        qb = q[w.qo_indptr[b]:w.qo_indptr[b + 1]]
+        # |q|.|k| products bound the rotated products (rotation keeps pair norms)
+        qa = qb.abs().view(qb.shape[0], qb.shape[1], 2, 64).pow(2).sum(2).sqrt()
+        ka = K.double().abs().view(K.shape[0], K.shape[1], 2, 64).pow(2).sum(2).sqrt()
+        kh = ka.repeat_interleave(w.num_qo_heads // w.num_kv_heads, 0)
+        s_abs = torch.einsum("nhf,hlf->nhl", qa, kh) * w.sm_scale
+        bound = max(bound, float(s_abs.max()) * 2.0 ** -9)
+    err_l = np.abs(lse.cpu().numpy() - rl)
+    assert err_l.max() <= LSE_ATOL + bound, (err_l.max(), bound)
+    err_o = np.abs(out.float().cpu().numpy() - ro)
+    assert err_o.max() <= 5e-3 + 2 * bound * np.abs(w.v_pages.float().nan_to_num()).max()

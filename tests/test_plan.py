@@ -22,20 +22,34 @@ def plan_of(w: wl.Paged, num_sms=152):
         rope_theta=w.rope_theta)
 
 
+def is_prefill(w: wl.Paged, b: int) -> bool:
+    g = w.num_qo_heads // w.num_kv_heads
+    rows = int(w.qo_indptr[b + 1] - w.qo_indptr[b]) * g
+    return w.head_dim == 128 and w.page_size >= 16 and rows >= 64
+
+
 def check_coverage(w: wl.Paged, units: np.ndarray):
+    """Every key of every (request, kv head, row group) in exactly one unit, in key order.
+
+    Decode units (warp >= 0) take 16-row groups; prefill units (warp < 0) 128-row tiles.
+    """
     g = w.num_qo_heads // w.num_kv_heads
     ranges = {}
     for req, kvh, row0, nrows, tok0, tok1, slot, warp in units.tolist():
-        assert 1 <= nrows <= 16
-        assert tok0 % max(w.page_size, 16) == 0
+        step = 128 if warp < 0 else 16
+        assert is_prefill(w, req) == (warp < 0)
+        assert 1 <= nrows <= step
+        align = max(w.page_size, 128 if warp < 0 else 16)
+        assert tok0 % align == 0
         ranges.setdefault((req, kvh, row0, nrows), []).append((tok0, tok1, slot))
     for b in range(w.batch):
         L = w.kv_len[b]
         nq = int(w.qo_indptr[b + 1] - w.qo_indptr[b])
         rows = nq * g
+        step = 128 if is_prefill(w, b) else 16
         for kvh in range(w.num_kv_heads):
-            for r0 in range(0, rows, 16):
-                nr = min(16, rows - r0)
+            for r0 in range(0, rows, step):
+                nr = min(step, rows - r0)
                 kend = L
                 if w.causal:
                     kend = min(L, max(0, (L - nq) + (r0 + nr - 1) // g + 1))
@@ -94,6 +108,19 @@ def test_uniform_batch_is_balanced():
     info, units = plan_of(w, num_sms=152)
     check_coverage(w, units)
     assert info["decode_imbalance"] < 1.05
+
+
+def test_prefill_configs_use_the_tensor_core_kernel():
+    w = wl.config5(small=False)
+    info, units = plan_of(w, num_sms=152)
+    check_coverage(w, units)
+    assert info["num_prefill_items"] > 0 and info["num_decode_items"] == 0
+    assert info["prefill_imbalance"] < 1.10
+    c = wl.config4(small=False)
+    info, units = plan_of(c.prefix, num_sms=152)
+    check_coverage(c.prefix, units)
+    assert info["num_prefill_items"] >= 152          # 64 tiles cut to fill every SM
+    assert info["num_split_streams"] > 0
 
 
 def test_plan_is_deterministic():

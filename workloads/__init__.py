@@ -259,7 +259,7 @@ def config5(small: bool = False) -> Paged:
     """Chunked prefill: append qo tokens after kv_len cached ones, causal, RoPE 5e5."""
     g = torch.Generator().manual_seed(1005)
     if small:
-        B, qo, kv = 3, 150, (40, 700)
+        B, qo, kv = 3, 150, (200, 700)
         name = "chunked_prefill_small"
     else:
         B, qo, kv = 16, 512, (1024, 8192)
