@@ -14,8 +14,11 @@ roofline  = the decode kernel's algorithmic bytes / its mean CUDA-event duration
             against the measured HBM copy bandwidth.
 cpu_baseline = the fp64 oracle on this host's cores (a bounded sample of the batch).
 
---impl reference times the oracle (the only reference this method has here) on the
-same workload.  Under torchrun each rank runs an independent replica (weak scaling).
+--config selects another workload for measurement (2: Llama-3-8B-shaped decode with RoPE,
+4: shared-prefix cascade, 5: chunked prefill with append, reported in TFLOP/s); the
+default is the skewed decode above.  --impl reference times the oracle (the only
+reference this method has here) on the same workload.  Under torchrun each rank runs an
+independent replica (weak scaling).
 """
 from __future__ import annotations
 
@@ -45,6 +48,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--small", action="store_true", help="small case (profiling, smoke)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5],
+                    help="workload; 3 (skewed block-sparse decode) is the headline")
     return ap.parse_args()
 
 
@@ -53,6 +58,14 @@ def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def peaks():
@@ -175,6 +188,140 @@ def cpu_baseline(w, budget_s=10.0, min_passes=1):
                       f"({w.active_tokens} keys, all heads), fp64 C oracle, {spent:.1f} s"}
 
 
+class Part:
+    """One library call of a step, timed with its own CUDA events."""
+
+    def __init__(self, label, fn, kernel, bound, work, work_unit):
+        self.label, self.fn, self.kernel, self.bound = label, fn, kernel, bound
+        self.work, self.work_unit = work, work_unit      # algorithmic bytes or FLOPs per call
+        self.ms = []
+
+
+def attention_flops(w) -> int:
+    """4*D FLOPs (QK^T and PV) per attended (query, qo head, key) pair."""
+    total = 0
+    for b in range(w.batch):
+        n = int(w.qo_indptr[b + 1] - w.qo_indptr[b])
+        L = w.kv_len[b]
+        keys = sum(min(L, L - n + i + 1) for i in range(n)) if w.causal else n * L
+        total += keys
+    return total * w.num_qo_heads * 4 * w.head_dim
+
+
+def build_job(cfg: int, dev, small: bool):
+    """Device tensors, schedules and the per-step calls of one workload."""
+    import torch
+    import block_sparse_kv_bsr_gb300 as bsr
+    import workloads as wl
+
+    def plan(w, schedule=None):
+        return bsr.bsr_attn_plan(w.indptr, w.indices, w.last_page_len,
+                                 num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
+                                 head_dim=w.head_dim, page_size=w.page_size,
+                                 num_pages=w.num_pages, qo_indptr=w.qo_indptr, causal=w.causal,
+                                 rope_theta=w.rope_theta, schedule=schedule)
+
+    job = {"parts": [], "schedules": []}
+    if cfg in (1, 2, 3):
+        w = wl.by_name(cfg, small)
+        q, k, v = w.q.to(dev), w.k_pages.to(dev), w.v_pages.to(dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        s = plan(w)
+        run = lambda: bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+                                       causal=w.causal, out=out, lse=lse)
+        alg = wl.algorithmic_bytes(w)
+        kname = f"bsr_decode_kernel<{w.head_dim},{int(w.rope_theta > 0)},0,0>"
+        job["parts"] = [Part("decode", run, kname, "hbm", alg, "B")]
+        job["schedules"] = [s]
+        job.update(workload=w, metric=METRIC, unit="GB/s", numerator=alg, scale=1e9,
+                   config={"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads,
+                           "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                           "page_size": w.page_size, "active_kv_tokens": w.active_tokens,
+                           "algorithmic_bytes": alg, "rope_theta": w.rope_theta,
+                           "l2": "inputs larger than L2, no flush" if alg > 2e8 else
+                                 "inputs smaller than L2: L2-warm"})
+        if cfg == 3:
+            job["config"]["drop"] = "25% of non-final pages"
+        q_host = w.q.pin_memory()
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        q_dev = torch.empty_like(q)
+
+        def e2e():
+            plan(w, s)
+            q_dev.copy_(q_host, non_blocking=True)
+            bsr.bsr_attn_run(s, q_dev, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+                             causal=w.causal, out=out, lse=lse)
+            out_host.copy_(out, non_blocking=True)
+            lse_host.copy_(lse, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        job["e2e"] = e2e
+        job["e2e_bytes"] = lambda: (q.numel() * 2 + int(s.info()["upload_bytes"]),
+                                    out.numel() * 2 + lse.numel() * 4)
+    elif cfg == 4:
+        c = wl.config4(small)
+        pre, suf = c.prefix, c.suffix
+        q = suf.q.to(dev)
+        pk, pv = pre.k_pages.to(dev), pre.v_pages.to(dev)
+        sk, sv = suf.k_pages.to(dev), suf.v_pages.to(dev)
+        o_p = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        o_s = torch.empty_like(o_p)
+        l_p = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        l_s = torch.empty_like(l_p)
+        o = torch.empty_like(o_p)
+        l = torch.empty_like(l_p)
+        sp, ss = plan(pre), plan(suf)
+        kv_p = pre.active_tokens * 2 * pre.num_kv_heads * pre.head_dim * 2
+        kv_s = suf.active_tokens * 2 * suf.num_kv_heads * suf.head_dim * 2
+        qo = q.numel() * 2
+        st = o.numel() * 4 + l.numel() * 4                  # one fp32 state
+        job["parts"] = [
+            Part("prefix", lambda: bsr.bsr_attn_run(sp, q, pk, pv, sm_scale=pre.sm_scale,
+                                                    out=o_p, lse=l_p),
+                 "bsr_prefill_kernel<0>", "tensor", attention_flops(pre), "FLOP"),
+            Part("suffix", lambda: bsr.bsr_attn_run(ss, q, sk, sv, sm_scale=suf.sm_scale,
+                                                    out=o_s, lse=l_s),
+                 "bsr_decode_kernel<128,0,0,0>", "hbm", kv_s + qo + st, "B"),
+            Part("merge", lambda: bsr.bsr_merge_states(o_p, l_p, o_s, l_s, o_out=o, lse_out=l),
+                 "merge_states_kernel<128,1>", "hbm", 3 * st, "B"),
+        ]
+        job["schedules"] = [sp, ss]
+        alg = kv_p + kv_s + qo + st
+        job.update(workload=suf, metric="BSR shared-prefix cascade decode: achieved GB/s; us/call",
+                   unit="GB/s", numerator=alg, scale=1e9,
+                   config={"workload": c.name, "requests": suf.batch,
+                           "prefix_tokens": pre.kv_len[0], "prefix_page_size": pre.page_size,
+                           "suffix_tokens": suf.active_tokens, "algorithmic_bytes": alg,
+                           "levels": "prefix (tensor cores) + suffix (decode) + LSE merge"})
+    elif cfg == 5:
+        w = wl.config5(small)
+        q, k, v = w.q.to(dev), w.k_pages.to(dev), w.v_pages.to(dev)
+        kn, vn = w.k_new.to(dev), w.v_new.to(dev)
+        tab = [t.to(dev) for t in (w.append_indptr, w.indptr, w.indices, w.last_page_len)]
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        s = plan(w)
+        flops = attention_flops(w)
+        app_bytes = 2 * 2 * kn.numel() * 2
+        job["parts"] = [
+            Part("append", lambda: bsr.bsr_append_kv(kn, vn, *tab, k, v), "append_kv_kernel",
+                 "hbm", app_bytes, "B"),
+            Part("prefill", lambda: bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale,
+                                                     rope_theta=w.rope_theta, causal=True,
+                                                     out=out, lse=lse),
+                 "bsr_prefill_kernel<1>", "tensor", flops, "FLOP"),
+        ]
+        job["schedules"] = [s]
+        job.update(workload=w, metric="BSR chunked-prefill attention (causal, RoPE): TFLOP/s",
+                   unit="TFLOP/s", numerator=flops, scale=1e12,
+                   config={"workload": w.name, "batch": w.batch, "qo_len": 512,
+                           "kv_tokens_after_append": w.active_tokens,
+                           "algorithmic_flops": flops, "rope_theta": w.rope_theta})
+    return job
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -194,29 +341,21 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
 
-    w = wl.config3(small=args.small)
-    alg_bytes = wl.algorithmic_bytes(w)
-    q = w.q.to(dev)
-    k = w.k_pages.to(dev)
-    v = w.v_pages.to(dev)
-    out = torch.empty_like(q)
-    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+    job = build_job(args.config, dev, args.small)
+    parts = job["parts"]
     stream = torch.cuda.current_stream()
-    s = bsr.bsr_attn_plan(w.indptr, w.indices, w.last_page_len, num_qo_heads=w.num_qo_heads,
-                          num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
-                          page_size=w.page_size, num_pages=w.num_pages, qo_indptr=w.qo_indptr)
-    info = s.info()
 
     def step():
-        bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, out=out, lse=lse)
+        for pt in parts:
+            pt.fn()
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
 
-    # ---- device-timed steps: one event pair per launch (kernel duration) + the whole region
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    # ---- device-timed steps: one event pair per call (kernel duration) + the whole region
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in parts] for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -225,10 +364,11 @@ def main():
     t_end = torch.cuda.Event(enable_timing=True)
     clocks.mark_start()
     t_start.record(stream)
-    for a, b in evs:
-        a.record(stream)
-        step()
-        b.record(stream)
+    for row in evs:
+        for pt, (a, b) in zip(parts, row):
+            a.record(stream)
+            pt.fn()
+            b.record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks.mark_end()
@@ -236,50 +376,49 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
-    kernel_ms = [a.elapsed_time(b) for a, b in evs]
+    for row in evs:
+        for pt, (a, b) in zip(parts, row):
+            pt.ms.append(a.elapsed_time(b))
     ms_step = total_ms / args.steps
     if world > 1:
         t = torch.tensor([ms_step], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         ms_step = float(t.item())
-    assert bsr.bsr_last_device_error(s) == 0
+    for s in job["schedules"]:
+        assert bsr.bsr_last_device_error(s) == 0
 
     # ---- end to end through the public API with host buffers
-    q_host = w.q.pin_memory()
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    q_dev = torch.empty_like(q)
+    e2e = None
+    if "e2e" in job:
+        for _ in range(max(1, args.warmup)):
+            job["e2e"]()
+        e2e_steps = max(3, min(args.steps, 20))
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            job["e2e"]()
+        e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
+        h2d, d2h = job["e2e_bytes"]()
+        e2e = {"value": round(job["numerator"] / (e2e_ms * 1e-3) / job["scale"], 1),
+               "unit": job["unit"], "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h,
+               "includes": "re-plan from host page table + H2D q + run + D2H out/lse"}
 
-    def e2e_step():
-        bsr.bsr_attn_plan(w.indptr, w.indices, w.last_page_len, num_qo_heads=w.num_qo_heads,
-                          num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
-                          page_size=w.page_size, num_pages=w.num_pages, qo_indptr=w.qo_indptr,
-                          schedule=s)
-        q_dev.copy_(q_host, non_blocking=True)
-        bsr.bsr_attn_run(s, q_dev, k, v, sm_scale=w.sm_scale, out=out, lse=lse)
-        out_host.copy_(out, non_blocking=True)
-        lse_host.copy_(lse, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
-    e2e_steps = max(3, min(args.steps, 20))
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    e2e_ms = (time.perf_counter() - t0) * 1e3 / e2e_steps
-    info = s.info()
-    h2d = q.numel() * 2 + int(info["upload_bytes"])
-    d2h = out.numel() * 2 + lse.numel() * 4
-
-    peak, peak_kind = peaks()
-    kern_mean_ms = sum(kernel_ms) / len(kernel_ms)
-    achieved = alg_bytes / (kern_mean_ms * 1e-3) / 1e9
-    value = alg_bytes * world / (ms_step * 1e-3) / 1e9
+    peak_hbm, hbm_kind = peaks()
+    peak_tensor, tensor_kind = tensor_peak()
+    # the roofline reports the call that takes the most time in a step
+    dom = max(parts, key=lambda pt: sum(pt.ms))
+    dom_ms = sum(dom.ms) / len(dom.ms)
+    if dom.bound == "hbm":
+        achieved, peak, unit, kind = dom.work / (dom_ms * 1e-3) / 1e9, peak_hbm, "GB/s", hbm_kind
+        kind = f"{kind} hbm_gbs (copy)"
+    else:
+        achieved, peak, unit = dom.work / (dom_ms * 1e-3) / 1e12, peak_tensor, "TFLOP/s"
+        kind = f"{tensor_kind} bf16 dense (cuBLAS GEMM)"
+    value = job["numerator"] * world / (ms_step * 1e-3) / job["scale"]
     res = {
-        "metric": METRIC,
+        "metric": job["metric"],
         "value": round(value, 1),
-        "unit": "GB/s",
+        "unit": job["unit"],
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -290,35 +429,29 @@ def main():
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, page table drawn per workloads/)",
-        "config": {"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads,
-                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                   "page_size": w.page_size, "active_kv_tokens": w.active_tokens,
-                   "algorithmic_bytes": alg_bytes, "drop": "25% of non-final pages",
-                   "l2": "inputs larger than L2 (active KV >> 129 MB), no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_kind": f"{peak_kind} hbm_gbs (copy)",
-                     "traffic": traffic_from_profile(_build._digest()),
-                     "kernel": "bsr_decode_kernel<128,false,false,false>",
-                     "kernel_us_mean": round(kern_mean_ms * 1e3, 2),
-                     "kernel_us_min": round(min(kernel_ms) * 1e3, 2)},
-        "e2e": {"value": round(alg_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "includes": "re-plan from host page table + H2D q + run + D2H out/lse"},
-        "gpu_launches": args.steps,
+        "config": dict(job["config"], parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+        "roofline": {"bound": dom.bound, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": unit, "frac": round(achieved / peak, 4), "peak_kind": kind,
+                     "traffic": traffic_from_profile(_build._digest()) if args.config == 3 else None,
+                     "kernel": dom.kernel, "kernel_us_mean": round(dom_ms * 1e3, 2),
+                     "kernel_us_min": round(min(dom.ms) * 1e3, 2)},
+        "parts_us": {pt.label: round(sum(pt.ms) / len(pt.ms) * 1e3, 2) for pt in parts},
+        "gpu_launches": args.steps * len(parts),
         "clocks": clocks.summary(),
-        "schedule": {"warps": info["decode_ctas"] * info["decode_warps_per_cta"],
-                     "items": info["num_decode_items"],
-                     "split_ranges": info["num_split_streams"],
-                     "imbalance": round(info["decode_imbalance"], 4)},
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(w)
+    if e2e is not None:
+        res["e2e"] = e2e
+    info = job["schedules"][-1].info()
+    res["schedule"] = {"decode_warps": info["decode_ctas"] * info["decode_warps_per_cta"],
+                       "decode_items": info["num_decode_items"],
+                       "prefill_ctas": info["prefill_ctas"],
+                       "prefill_items": info["num_prefill_items"],
+                       "split_ranges": info["num_split_streams"],
+                       "imbalance": round(max(info["decode_imbalance"], info["prefill_imbalance"]), 4)}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.config == 3:
+        res["cpu_baseline"] = cpu_baseline(job["workload"])
     if rank == 0:
         print(json.dumps(res))
-    s.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 
