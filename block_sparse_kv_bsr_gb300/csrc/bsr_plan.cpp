@@ -175,7 +175,8 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
   };
   if (!units.empty()) {
     int64_t lo = std::max<int64_t>((total + workers - 1) / workers, 2 * min_piece + overhead + align);
-    int64_t hi = lo;
+    // the optimum is rarely more than a few pieces' slack above the mean
+    int64_t hi = lo + 2 * (align + overhead + min_piece);
     while (partition(hi, false) > workers) hi *= 2;
     while (lo < hi) {
       const int64_t mid = lo + (hi - lo) / 2;
@@ -195,14 +196,14 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
       out->n_partials += pieces_of_unit[u];
       ++out->n_split;
     }
-  std::vector<std::vector<int32_t>> per_worker(workers);
-  for (size_t i = 0; i < pieces.size(); ++i) per_worker[owner[i]].push_back(int32_t(i));
+  // the cut emits pieces worker by worker, so piece order is already grouped by worker
   out->items.clear();
   out->items.reserve(pieces.size());
   out->ptr.assign(workers + 1, 0);
   std::vector<int64_t> load(workers, 0);
+  size_t i = 0;
   for (int w = 0; w < workers; ++w) {
-    for (int32_t i : per_worker[w]) {
+    for (; i < pieces.size() && owner[i] == w; ++i) {
       const Piece& pc = pieces[i];
       const Unit& u = units[pc.unit];
       DecodeItem it{};
