@@ -156,7 +156,8 @@ class ClockSampler:
 
 
 def traffic_from_profile(digest: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches this build."""
+    """DRAM bytes per launch from the committed ncu summary, if it was captured on the
+    decode kernel built from the current sources (digest of those sources)."""
     try:
         text = open(PROFILE_SUMMARY).read()
     except OSError:
@@ -432,7 +433,7 @@ def main():
         "config": dict(job["config"], parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
         "roofline": {"bound": dom.bound, "achieved": round(achieved, 1), "peak": peak,
                      "unit": unit, "frac": round(achieved / peak, 4), "peak_kind": kind,
-                     "traffic": traffic_from_profile(_build._digest()) if args.config == 3 else None,
+                     "traffic": traffic_from_profile(_build.kernel_digest()) if args.config == 3 else None,
                      "kernel": dom.kernel, "kernel_us_mean": round(dom_ms * 1e3, 2),
                      "kernel_us_min": round(min(dom.ms) * 1e3, 2)},
         "parts_us": {pt.label: round(sum(pt.ms) / len(pt.ms) * 1e3, 2) for pt in parts},

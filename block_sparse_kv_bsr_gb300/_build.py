@@ -47,6 +47,20 @@ def _digest() -> str:
     return h.hexdigest()[:16]
 
 
+# Sources that determine the decode kernel's machine code (for matching a profile to a build).
+DECODE_KERNEL_SOURCES = ("bsr_decode.cuh", "bsr_decode_d128.cu", "bsr_internal.h", "ptx.cuh")
+
+
+def kernel_digest(names=DECODE_KERNEL_SOURCES) -> str:
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    h.update(" ".join(ARCH + COMMON).encode())
+    return h.hexdigest()[:16]
+
+
 def lib_path() -> str:
     return os.path.join(OUT, LIB_NAME)
 

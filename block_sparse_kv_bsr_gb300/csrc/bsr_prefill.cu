@@ -9,7 +9,8 @@
 //
 // Roles:
 //   warps 0-3  row owners: thread t owns packed row t of the tile and TMEM lane
-//              t.  They load (and RoPE-rotate) Q, run the online softmax on S
+//              t.  They load Q (RoPE-rotated and split into bf16 hi + lo, so
+//              QK^T takes two passes), run the online softmax on S
 //              rows read from TMEM (two passes: row max, then exp2 / P), write
 //              P (bf16) to shared memory, rescale O in TMEM when the running
 //              max grows by more than 2^8, and write out / lse.
@@ -50,7 +51,8 @@ template <bool ROPE>
 struct PrefillSmem {
   static constexpr int kThreads = ROPE ? 320 : 192;
   static constexpr int kQ = 0;
-  static constexpr int kStage0 = kQ + kTileBytes;                  // K then V per stage
+  static constexpr int kQlo = kQ + kTileBytes;                     // RoPE: low half of the split q
+  static constexpr int kStage0 = ROPE ? kQlo + kTileBytes : kQlo;  // K then V per stage
   static constexpr int kStageBytes = 2 * kTileBytes;
   static constexpr int kP = kStage0 + 2 * kStageBytes;
   static constexpr int kBars = kP + kTileBytes;
@@ -247,6 +249,13 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
           umma::mma_f16_ss(S_T(g), umma::sdesc_sw128(base + L::kQ + off, 16, 1024),
                            umma::sdesc_sw128(ks + off, 16, 1024), idesc_qk, k > 0);
         }
+        if constexpr (ROPE) {
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
+            umma::mma_f16_ss(S_T(g), umma::sdesc_sw128(base + L::kQlo + off, 16, 1024),
+                             umma::sdesc_sw128(ks + off, 16, 1024), idesc_qk, 1);
+          }
+        }
         umma::commit(BAR(S_FULL + (g & 1)));
         return true;
       };
@@ -314,10 +323,34 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
         const uint4* src = reinterpret_cast<const uint4*>(p.q + orow * D);
 #pragma unroll
         for (int c = 0; c < 16; ++c) qraw[c] = vrow ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+        if constexpr (!ROPE) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c)
-          sts128(base + L::kQ + sw_off(t, c), qraw[c].x, qraw[c].y, qraw[c].z, qraw[c].w);
-        if (ROPE && vrow) rope_row_inplace(base + L::kQ, t, p.rope_nat, min(max(qpos, 0), p.rope_max_pos));
+          for (int c = 0; c < 16; ++c)
+            sts128(base + L::kQ + sw_off(t, c), qraw[c].x, qraw[c].y, qraw[c].z, qraw[c].w);
+        } else {
+          // The rotated query is split into bf16 hi + lo (two QK^T passes): its rounding
+          // error would not average out over keys the way the keys' does.
+          const float4* tab = reinterpret_cast<const float4*>(
+              p.rope_nat + size_t(vrow ? min(max(qpos, 0), p.rope_max_pos) : 0) * (D / 2));
+#pragma unroll 2
+          for (int c = 0; c < 8; ++c) {
+            const uint32_t* a = reinterpret_cast<const uint32_t*>(&qraw[c]);
+            const uint32_t* b = reinterpret_cast<const uint32_t*>(&qraw[c + 8]);
+            uint32_t xh[4], xl[4], yh[4], yl[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float4 cs = __ldg(tab + 4 * c + e);   // frequencies 8c + 2e, 8c + 2e + 1
+              const float a0 = ptx::bf16_lo(a[e]), a1 = ptx::bf16_hi(a[e]);
+              const float b0 = ptx::bf16_lo(b[e]), b1 = ptx::bf16_hi(b[e]);
+              ptx::split_bf16(a0 * cs.x - b0 * cs.y, a1 * cs.z - b1 * cs.w, xh[e], xl[e]);
+              ptx::split_bf16(b0 * cs.x + a0 * cs.y, b1 * cs.z + a1 * cs.w, yh[e], yl[e]);
+            }
+            sts128(base + L::kQ + sw_off(t, c), xh[0], xh[1], xh[2], xh[3]);
+            sts128(base + L::kQ + sw_off(t, c + 8), yh[0], yh[1], yh[2], yh[3]);
+            sts128(base + L::kQlo + sw_off(t, c), xl[0], xl[1], xl[2], xl[3]);
+            sts128(base + L::kQlo + sw_off(t, c + 8), yl[0], yl[1], yl[2], yl[3]);
+          }
+        }
         ptx::fence_proxy_async_smem();
         mbar_arrive(BAR(Q_FULL));
 
