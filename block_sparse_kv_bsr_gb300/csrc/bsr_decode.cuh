@@ -41,6 +41,9 @@
 
 namespace bsr {
 
+// Key count below which the decode kernel also splits rotated keys hi + lo.
+constexpr int kRopeExactKeysBelow = 256;
+
 template <int D>
 struct DecodeCfg {
   static constexpr int kHalves = D / 64;                        // 128-byte column blocks per row
@@ -305,6 +308,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const bool vA = g4 < ci.nrows, vB = R16 && (g4 + 8 < ci.nrows);
     const int qposA = ci.qpos0 + rA / group, qposB = ci.qpos0 + rB / group;
     const int qpos_min = ci.qpos0 + ci.row0 / group;
+    // The rotated keys are bf16 MMA operands.  Their rounding error averages out
+    // over many keys; a unit whose rows see only a few keys also carries the low
+    // bf16 half of each rotated key (a third Q.K^T pass) so that even one key
+    // keeps the score exact to ~16 bits.
+    const bool ksplit = ROPE && qpos_min + 1 < kRopeExactKeysBelow;
 
     // q fragments (A operand): regs [0] and [NR/2] hold row g4 (columns 2t4.. and
     // 8+2t4..); with R16 regs [1] and [3] hold row g4 + 8.
@@ -446,21 +454,22 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
           ptx::ldsm_x4(kh, kt + tile_off(k_tok, 16 * (ks + KH) + 8 * k_hb));
           const float4 a01 = __ldg(tabA + 2 * ks), a23 = __ldg(tabA + 2 * ks + 1);
           const float4 b01 = __ldg(tabB + 2 * ks), b23 = __ldg(tabB + 2 * ks + 1);
-          uint32_t lh[4], ll[4], hh[4], hl[4];
-          float x[2], y[2];
+          uint32_t lh[4], ll[4] = {0u, 0u, 0u, 0u}, hh[4], hl[4] = {0u, 0u, 0u, 0u};
           // kl[0], kl[1]: key g4 (n-tile 0); kl[2], kl[3]: key 8 + g4 (n-tile 1)
-          rope_pair(kl[0], kh[0], make_float2(a01.x, a01.y), make_float2(a01.z, a01.w), x, y);
-          ptx::split_bf16(x[0], x[1], lh[0], ll[0]);
-          ptx::split_bf16(y[0], y[1], hh[0], hl[0]);
-          rope_pair(kl[1], kh[1], make_float2(a23.x, a23.y), make_float2(a23.z, a23.w), x, y);
-          ptx::split_bf16(x[0], x[1], lh[1], ll[1]);
-          ptx::split_bf16(y[0], y[1], hh[1], hl[1]);
-          rope_pair(kl[2], kh[2], make_float2(b01.x, b01.y), make_float2(b01.z, b01.w), x, y);
-          ptx::split_bf16(x[0], x[1], lh[2], ll[2]);
-          ptx::split_bf16(y[0], y[1], hh[2], hl[2]);
-          rope_pair(kl[3], kh[3], make_float2(b23.x, b23.y), make_float2(b23.z, b23.w), x, y);
-          ptx::split_bf16(x[0], x[1], lh[3], ll[3]);
-          ptx::split_bf16(y[0], y[1], hh[3], hl[3]);
+          const float4 cs01[4] = {a01, a23, b01, b23};
+#pragma unroll
+          for (int r = 0; r < 4; ++r) {
+            float x[2], y[2];
+            rope_pair(kl[r], kh[r], make_float2(cs01[r].x, cs01[r].y),
+                      make_float2(cs01[r].z, cs01[r].w), x, y);
+            if (ksplit) {
+              ptx::split_bf16(x[0], x[1], lh[r], ll[r]);
+              ptx::split_bf16(y[0], y[1], hh[r], hl[r]);
+            } else {
+              lh[r] = ptx::pack_bf16(x[0], x[1]);
+              hh[r] = ptx::pack_bf16(y[0], y[1]);
+            }
+          }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int kk = half == 0 ? ks : ks + KH;
@@ -474,8 +483,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             ptx::mma_bf16(s1[0], s1[1], s1[2], s1[3], h0, h1, h2, h3, bh[2], bh[3]);
             ptx::mma_bf16(s0[0], s0[1], s0[2], s0[3], l0, l1, l2, l3, bh[0], bh[1]);
             ptx::mma_bf16(s1[0], s1[1], s1[2], s1[3], l0, l1, l2, l3, bh[2], bh[3]);
-            ptx::mma_bf16(s0[0], s0[1], s0[2], s0[3], h0, h1, h2, h3, bl[0], bl[1]);
-            ptx::mma_bf16(s1[0], s1[1], s1[2], s1[3], h0, h1, h2, h3, bl[2], bl[3]);
+            if (ksplit) {
+              ptx::mma_bf16(s0[0], s0[1], s0[2], s0[3], h0, h1, h2, h3, bl[0], bl[1]);
+              ptx::mma_bf16(s1[0], s1[1], s1[2], s1[3], h0, h1, h2, h3, bl[2], bl[3]);
+            }
           }
         }
       }

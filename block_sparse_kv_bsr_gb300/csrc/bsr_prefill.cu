@@ -22,7 +22,7 @@
 //              O += P V (P K-major from shared memory, V MN-major) into a TMEM
 //              O buffer.  S is double-buffered so that QK^T of the next tile
 //              runs on the tensor cores while the row owners work on this one.
-//   warps 6-9  (RoPE only) rotate each landed K tile in place, ahead of the MMA
+//   warps 6-7  (RoPE only) rotate each landed K tile in place, ahead of the MMA
 //              ("JIT 컴파일은 …": RoPE fused into attention, k stored un-rotated).
 // A unit whose key range was split writes an fp32 partial state; for each
 // 32-row quarter the last arriving warp merges the partials in key order.
@@ -49,7 +49,7 @@ constexpr uint32_t kTmemCols = 512;      // S0 | S1 | O | (unused)
 
 template <bool ROPE>
 struct PrefillSmem {
-  static constexpr int kThreads = ROPE ? 320 : 192;
+  static constexpr int kThreads = ROPE ? 256 : 192;
   static constexpr int kQ = 0;
   static constexpr int kQlo = kQ + kTileBytes;                     // RoPE: low half of the split q
   static constexpr int kStage0 = ROPE ? kQlo + kTileBytes : kQlo;  // K then V per stage
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(BAR(KV_FULL + i), 1);
-      ptx::mbar_init(BAR(KV_READY + i), 128);
+      ptx::mbar_init(BAR(KV_READY + i), 64);
       ptx::mbar_init(BAR(KV_EMPTY + i), 1);
       ptx::mbar_init(BAR(S_FULL + i), 1);
     }
@@ -267,8 +267,8 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
         ++qc;
         umma::fence_after_sync();
         if (!issue_qk(gt)) break;
+        if (nt > 1 && !issue_qk(gt + 1)) break;
         for (int j = 0; j < nt; ++j, ++gt) {
-          if (j + 1 < nt && !issue_qk(gt + 1)) { ok = false; break; }
           if (!wt.wait(BAR(P_FULL), gt & 1)) { ok = false; break; }
           umma::fence_after_sync();
           const uint32_t vs = stage_k(gt) + kTileBytes;
@@ -282,12 +282,14 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
           }
           umma::commit(BAR(KV_EMPTY + (gt & 1)));
           umma::commit(BAR(PV_DONE));
+          // S buffer gt % 2 was read by the row owners before P_FULL: refill it with tile j + 2
+          if (j + 2 < nt && !issue_qk(gt + 2)) { ok = false; break; }
         }
       }
     }
   } else if (warp >= 6) {
     // ------------------------------------------------------------ RoPE on K (ROPE only)
-    const int t = tid - 192;           // key row of the tile
+    const int t = tid - 192;           // this thread rotates key rows t and t + 64 of the tile
     uint32_t gt = 0;
     bool ok = true;
     for (int u = u_begin; u < u_end && ok; ++u) {
@@ -296,8 +298,10 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
       for (int j = 0; j < nt; ++j, ++gt) {
         if (!wt.warp_wait(BAR(KV_FULL + (gt & 1)), (gt >> 1) & 1)) { ok = false; break; }
         const int key0 = it.tok0 + kTileN * j;
-        if (t < min(kTileN, it.tok1 - key0))
-          rope_row_inplace(stage_k(gt), t, p.rope_nat, min(key0 + t, p.rope_max_pos));
+        const int nkeys = min(kTileN, it.tok1 - key0);
+#pragma unroll 1
+        for (int r = t; r < nkeys; r += 64)
+          rope_row_inplace(stage_k(gt), r, p.rope_nat, min(key0 + r, p.rope_max_pos));
         ptx::fence_proxy_async_smem();
         mbar_arrive(BAR(KV_READY + (gt & 1)));
       }
@@ -332,7 +336,7 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
           // error would not average out over keys the way the keys' does.
           const float4* tab = reinterpret_cast<const float4*>(
               p.rope_nat + size_t(vrow ? min(max(qpos, 0), p.rope_max_pos) : 0) * (D / 2));
-#pragma unroll 2
+#pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint32_t* a = reinterpret_cast<const uint32_t*>(&qraw[c]);
             const uint32_t* b = reinterpret_cast<const uint32_t*>(&qraw[c + 8]);
@@ -360,19 +364,15 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
           const uint32_t vs = stage_k(gt) + kTileBytes;
           const int klim = p.causal ? min(nkeys, qpos - key0 + 1) : nkeys;   // keys [0, klim) visible
 
-          // ---- pass 1: row max of S (read from TMEM in 32-column chunks)
+          // ---- S row t: one 128-column TMEM load; mask, online softmax (log2, lazy rescale)
           if (!wt.warp_wait(BAR(S_FULL + (gt & 1)), (gt >> 1) & 1)) { ok = false; break; }
           umma::fence_after_sync();
-          const uint32_t s_addr = S_T(gt) + lane_off;
+          float sv[kTileN];
+          umma::tmem_ld128(S_T(gt) + lane_off, sv);
           float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float v[32];
-            umma::tmem_ld32(s_addr + 32 * c, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (32 * c + i < klim) mx = fmaxf(mx, v[i]);
-          }
+          for (int i = 0; i < kTileN; ++i)
+            if (i < klim) mx = fmaxf(mx, sv[i]);
           mx = mx == -INFINITY ? mx : mx * p.scale_log2;
           float alpha = 1.f;
           if (mx > m_used + 8.f) {          // also true the first time a row sees a key
@@ -380,6 +380,15 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
             m_used = mx;
           }
           const float mu = m_used == -INFINITY ? 0.f : m_used;
+          float rs = 0.f;
+          uint32_t pk[kTileN / 2];
+#pragma unroll
+          for (int i = 0; i < kTileN; i += 2) {
+            const float p0 = i < klim ? ptx::ex2(sv[i] * p.scale_log2 - mu) : 0.f;
+            const float p1 = i + 1 < klim ? ptx::ex2(sv[i + 1] * p.scale_log2 - mu) : 0.f;
+            rs += p0 + p1;
+            pk[i / 2] = ptx::pack_bf16(p0, p1);
+          }
 
           // P buffer and O are free once the previous P.V has completed
           if (j > 0) {
@@ -396,25 +405,9 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
               }
             }
           }
-          // ---- pass 2: p = exp2(s * scale - m), row sum, P (bf16) to shared memory
-          float rs = 0.f;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float v[32];
-            umma::tmem_ld32(s_addr + 32 * c, v);
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const float p0 = 32 * c + i < klim ? ptx::ex2(v[i] * p.scale_log2 - mu) : 0.f;
-              const float p1 = 32 * c + i + 1 < klim ? ptx::ex2(v[i + 1] * p.scale_log2 - mu) : 0.f;
-              rs += p0 + p1;
-              pk[i / 2] = ptx::pack_bf16(p0, p1);
-            }
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-              sts128(base + L::kP + sw_off(t, 4 * c + q4), pk[4 * q4], pk[4 * q4 + 1],
-                     pk[4 * q4 + 2], pk[4 * q4 + 3]);
-          }
+          for (int c = 0; c < 16; ++c)
+            sts128(base + L::kP + sw_off(t, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
           l = l * alpha + rs;
           // V rows past the last valid key of the final 16-key group may hold
           // another page's tail: zero them so that P = 0 contributes exactly 0.
