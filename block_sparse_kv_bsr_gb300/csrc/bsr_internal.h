@@ -86,10 +86,24 @@ struct PrefillParams {
   void* out;
   float* lse;
   int32_t* error;
+  const int32_t* rk_off;          // RoPE: first row of each request in the rotated-K buffer
+  int32_t rk_total;               // RoPE: rows per kv head in the rotated-K buffer
   float scale_log2;
   int32_t Hq, Hk, group, P;
   int32_t causal, out_f32, num_ctas, rope_max_pos;
   uint64_t wait_limit_ns;
+};
+
+// Rotate the keys of the prefill requests once per run into a dense buffer
+// [Hk][rk_total][D] (request rows at rk_start[i] .. rk_start[i + 1]).
+struct RopeKParams {
+  const uint16_t* k_pages;
+  const int32_t* indices;
+  const int32_t* rk_req_pbase;    // [n] indptr[b] of each prefill request
+  const int32_t* rk_start;        // [n + 1]
+  const float2* rope_nat;
+  uint16_t* rotk;
+  int32_t n, rk_total, Hk, P, rope_max_pos;
 };
 
 }  // namespace bsr

@@ -242,6 +242,9 @@ struct HostPlan {
   int32_t max_len = 0, max_rows = 0;
   WorkList dec;   // split-KV decode kernel, workers = warps
   WorkList pre;   // tensor-core prefill kernel, workers = CTAs
+  // requests on the prefill kernel (for the rotated-K pre-pass when RoPE is on)
+  std::vector<int32_t> rk_off, rk_pbase, rk_start;
+  int32_t rk_total = 0;
 };
 
 int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
@@ -319,6 +322,16 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
         }
       }
   }
+  hp->rk_off.assign(batch, -1);
+  hp->rk_pbase.clear();
+  hp->rk_start.assign(1, 0);
+  for (const Unit& u : punits) {
+    if (hp->rk_off[u.req] >= 0 || kv_len[u.req] == 0) continue;
+    hp->rk_off[u.req] = hp->rk_start.back();
+    hp->rk_pbase.push_back(indptr[u.req]);
+    hp->rk_start.push_back(hp->rk_start.back() + kv_len[u.req]);
+  }
+  hp->rk_total = hp->rk_start.back();
   balance(dunits, int64_t(num_sms) * kDecodeWarps, std::max<int64_t>(page_size, kStageTokens),
           kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec);
   balance(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillRows), kPrefillOverhead,
@@ -401,6 +414,10 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const size_t off_pitems = take(hp.pre.items.size() * sizeof(DecodeItem));
   const size_t off_cta_ptr = take(hp.pre.ptr.size() * 4);
   const size_t off_pcounters = take(size_t(std::max(hp.pre.n_partials, 1)) * 4 * 4);  // per row-owner warp
+  const bool rotk = rope && !hp.pre.items.empty() && hp.rk_total > 0;
+  const size_t off_rk_off = take(rotk ? size_t(batch) * 4 : 0);
+  const size_t off_rk_pbase = take(rotk ? hp.rk_pbase.size() * 4 : 0);
+  const size_t off_rk_start = take(rotk ? hp.rk_start.size() * 4 : 0);
   const size_t off_error = take(16);
   const size_t off_rope = take(rope ? 2 * rope_bytes : 0);
   const size_t image_bytes = off;  // everything above is uploaded
@@ -408,6 +425,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const size_t off_part_lse = take(size_t(hp.dec.n_partials) * kMaxDecodeRows * 4);
   const size_t off_ppart_o = take(size_t(hp.pre.n_partials) * bsr::kPrefillRows * head_dim * 4);
   const size_t off_ppart_lse = take(size_t(hp.pre.n_partials) * bsr::kPrefillRows * 4);
+  const size_t off_rotk = take(rotk ? size_t(num_kv_heads) * hp.rk_total * head_dim * 2 : 0);
   const size_t ws_bytes = off;
 
   // ---------------------------------------------------------------- staging + upload
@@ -449,6 +467,11 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
     std::memcpy(h + off_pitems, hp.pre.items.data(), hp.pre.items.size() * sizeof(DecodeItem));
   std::memcpy(h + off_cta_ptr, hp.pre.ptr.data(), hp.pre.ptr.size() * 4);
   if (rope) std::memcpy(h + off_rope, s->h_rope, 2 * rope_bytes);
+  if (rotk) {
+    std::memcpy(h + off_rk_off, hp.rk_off.data(), size_t(batch) * 4);
+    std::memcpy(h + off_rk_pbase, hp.rk_pbase.data(), hp.rk_pbase.size() * 4);
+    std::memcpy(h + off_rk_start, hp.rk_start.data(), hp.rk_start.size() * 4);
+  }
   ce = cudaMemcpyAsync(s->d_ws, h, image_bytes, cudaMemcpyHostToDevice, stream);
   if (ce != cudaSuccess) return bail(fail_cuda(ce));
   ce = cudaEventRecord(s->upload_done, stream);
@@ -488,6 +511,13 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->off_pcounters = off_pcounters;
   s->off_ppart_o = off_ppart_o;
   s->off_ppart_lse = off_ppart_lse;
+  s->off_rk_off = off_rk_off;
+  s->off_rk_pbase = off_rk_pbase;
+  s->off_rk_start = off_rk_start;
+  s->off_rotk = off_rotk;
+  s->rk_n = rotk ? int32_t(hp.rk_pbase.size()) : 0;
+  s->rk_total = rotk ? hp.rk_total : 0;
+  s->tm_rk_valid = false;   // encoded by run (the buffer's address may have moved)
   s->ws_used = ws_bytes;
   s->upload_bytes = image_bytes;
   s->off_indices = off_indices;

@@ -7,23 +7,25 @@
 // a tile of 128 packed (query, head) rows of one (request, kv head) against a
 // page-aligned key range; a CTA walks its planned list of units.
 //
-// Roles:
+// Roles (192 threads):
 //   warps 0-3  row owners: thread t owns packed row t of the tile and TMEM lane
 //              t.  They load Q (RoPE-rotated and split into bf16 hi + lo, so
-//              QK^T takes two passes), run the online softmax on S
-//              rows read from TMEM (two passes: row max, then exp2 / P), write
-//              P (bf16) to shared memory, rescale O in TMEM when the running
-//              max grows by more than 2^8, and write out / lse.
+//              QK^T takes two passes), run the online softmax on S rows read
+//              from TMEM (one 128-column load per tile), write P (bf16) to
+//              shared memory, rescale O in TMEM when the running max grows by
+//              more than 2^8, and write out / lse.
 //   warp 4     TMA producer: gathers 128-key K and V tiles page by page from
-//              `indices` (inactive blocks are absent, "Block-Sparse 포맷") into a
-//              two-stage ring of 128B-swizzled tiles.
+//              `indices` (inactive blocks are absent, "Block-Sparse 포맷") into
+//              two-stage K and V rings of 128B-swizzled tiles.  A K stage is
+//              released as soon as Q K^T has read it, so K runs ahead of V.
+//              With RoPE, K comes already rotated from a dense buffer that a
+//              pre-pass fills once per run (every key is read by many row
+//              tiles, so rotating it once is cheaper than once per tile).
 //   warp 5     allocates TMEM and issues the MMAs: S = Q K^T (M 128, N 128,
 //              8 x K16, K-major operands) into one of two TMEM S buffers, and
 //              O += P V (P K-major from shared memory, V MN-major) into a TMEM
-//              O buffer.  S is double-buffered so that QK^T of the next tile
-//              runs on the tensor cores while the row owners work on this one.
-//   warps 6-7  (RoPE only) rotate each landed K tile in place, ahead of the MMA
-//              ("JIT 컴파일은 …": RoPE fused into attention, k stored un-rotated).
+//              O buffer.  S is double-buffered so that Q K^T of a tile runs on
+//              the tensor cores while the row owners work on the previous one.
 // A unit whose key range was split writes an fp32 partial state; for each
 // 32-row quarter the last arriving warp merges the partials in key order.
 // Every mbarrier wait is bounded and warp-agreed.
@@ -49,15 +51,15 @@ constexpr uint32_t kTmemCols = 512;      // S0 | S1 | O | (unused)
 
 template <bool ROPE>
 struct PrefillSmem {
-  static constexpr int kThreads = ROPE ? 256 : 192;
+  static constexpr int kThreads = 192;
   static constexpr int kQ = 0;
   static constexpr int kQlo = kQ + kTileBytes;                     // RoPE: low half of the split q
-  static constexpr int kStage0 = ROPE ? kQlo + kTileBytes : kQlo;  // K then V per stage
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kP = kStage0 + 2 * kStageBytes;
+  static constexpr int kK0 = ROPE ? kQlo + kTileBytes : kQlo;      // K ring: 2 tiles
+  static constexpr int kV0 = kK0 + 2 * kTileBytes;                 // V ring: 2 tiles
+  static constexpr int kP = kV0 + 2 * kTileBytes;
   static constexpr int kBars = kP + kTileBytes;
-  // barriers: kv_full[2], kv_ready[2], kv_empty[2], s_full[2], p_full, pv_done, q_full
-  static constexpr int kNumBars = 11;
+  // barriers: k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full, pv_done, q_full
+  static constexpr int kNumBars = 13;
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kFlags = kTmemSlot + 16;   // abort flag
   static constexpr int kTotal = kFlags + 16;
@@ -112,36 +114,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                : "memory");
 }
 
-// Rotate one 128-column row of a swizzled tile in place at position `pos`
-// (rotate-half pairs (d, d + 64), cos/sin from the frequency-ordered table).
-__device__ __forceinline__ void rope_row_inplace(uint32_t tile, int r, const float2* rope_nat,
-                                                 int pos) {
-  const float4* tab = reinterpret_cast<const float4*>(rope_nat + size_t(pos) * (D / 2));
-#pragma unroll 2
-  for (int c = 0; c < 8; ++c) {
-    float4 cs[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) cs[e] = __ldg(tab + 4 * c + e);   // frequencies 8c + 2e, 8c + 2e + 1
-    uint4 av, bv;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(av.x), "=r"(av.y), "=r"(av.z), "=r"(av.w) : "r"(tile + sw_off(r, c)));
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(bv.x), "=r"(bv.y), "=r"(bv.z), "=r"(bv.w) : "r"(tile + sw_off(r, c + 8)));
-    const uint32_t* a = reinterpret_cast<const uint32_t*>(&av);
-    const uint32_t* b = reinterpret_cast<const uint32_t*>(&bv);
-    uint32_t xo[4], yo[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float a0 = ptx::bf16_lo(a[e]), a1 = ptx::bf16_hi(a[e]);
-      const float b0 = ptx::bf16_lo(b[e]), b1 = ptx::bf16_hi(b[e]);
-      xo[e] = ptx::pack_bf16(a0 * cs[e].x - b0 * cs[e].y, a1 * cs[e].z - b1 * cs[e].w);
-      yo[e] = ptx::pack_bf16(b0 * cs[e].x + a0 * cs[e].y, b1 * cs[e].z + a1 * cs[e].w);
-    }
-    sts128(tile + sw_off(r, c), xo[0], xo[1], xo[2], xo[3]);
-    sts128(tile + sw_off(r, c + 8), yo[0], yo[1], yo[2], yo[3]);
-  }
-}
-
 // Write 32 columns (chunk c) of one output row as bf16 or fp32.
 __device__ __forceinline__ void store_row_chunk(const PrefillParams& p, size_t orow, int c,
                                                 const float (&v)[32]) {
@@ -168,7 +140,8 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bar0 = base + L::kBars;
   auto BAR = [&](int i) { return bar0 + 8u * uint32_t(i); };
-  enum { KV_FULL = 0, KV_READY = 2, KV_EMPTY = 4, S_FULL = 6, P_FULL = 8, PV_DONE = 9, Q_FULL = 10 };
+  enum { K_FULL = 0, K_EMPTY = 2, V_FULL = 4, V_EMPTY = 6, S_FULL = 8, P_FULL = 10, PV_DONE = 11,
+         Q_FULL = 12 };
   const uint32_t abort_addr = base + L::kFlags;
   Waiter wt{abort_addr, p.wait_limit_ns, p.error};
 
@@ -176,9 +149,10 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      ptx::mbar_init(BAR(KV_FULL + i), 1);
-      ptx::mbar_init(BAR(KV_READY + i), 64);
-      ptx::mbar_init(BAR(KV_EMPTY + i), 1);
+      ptx::mbar_init(BAR(K_FULL + i), 1);
+      ptx::mbar_init(BAR(K_EMPTY + i), 1);
+      ptx::mbar_init(BAR(V_FULL + i), 1);
+      ptx::mbar_init(BAR(V_EMPTY + i), 1);
       ptx::mbar_init(BAR(S_FULL + i), 1);
     }
     ptx::mbar_init(BAR(P_FULL), 128);
@@ -198,7 +172,8 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(base + L::kTmemSlot));
   const uint32_t O_T = tmem + 256;
   auto S_T = [&](uint32_t g) { return tmem + 128u * (g & 1u); };
-  auto stage_k = [&](uint32_t g) { return base + L::kStage0 + (g & 1u) * L::kStageBytes; };
+  auto stage_k = [&](uint32_t g) { return base + L::kK0 + (g & 1u) * kTileBytes; };
+  auto stage_v = [&](uint32_t g) { return base + L::kV0 + (g & 1u) * kTileBytes; };
 
   if (warp == 4) {
     // ------------------------------------------------------------ TMA producer
@@ -206,31 +181,63 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
       // K/V tiles are re-read by the other row tiles of the same (request, kv head),
       // which run concurrently on other SMs: keep them in L2 at normal priority.
       const uint64_t pol = ptx::policy_evict_normal();
+      // Tiles are issued in order; the V of tile g - 1 goes out after the K of tile g,
+      // so K (released early, after Q K^T) runs ahead of V (released after P V).
+      struct Tile {
+        int pages[kTileN / 16];   // page id of each 16-key block
+        int kvh, nsub, key0, krow;
+      };
+      Tile cur{}, prev{};
+      bool have_prev = false;
       uint32_t gt = 0;
       bool ok = true;
+      auto issue_v = [&](const Tile& tl, uint32_t g) -> bool {
+        const int st = g & 1;
+        if (g >= 2 && !wt.wait(BAR(V_EMPTY + st), ((g >> 1) - 1) & 1)) return false;
+        ptx::mbar_arrive_expect_tx(BAR(V_FULL + st), uint32_t(tl.nsub) * 2u * 2048u);
+        const uint32_t vs = stage_v(g);
+        for (int sb = 0; sb < tl.nsub; ++sb) {
+          const int row = (tl.pages[sb] * p.Hk + tl.kvh) * p.P + ((tl.key0 + 16 * sb) % p.P);
+          for (int h = 0; h < 2; ++h)
+            ptx::tma_load_3d(vs + h * kHalfBytes + sb * 2048, &tm_v, BAR(V_FULL + st), 0, h, row, pol);
+        }
+        return true;
+      };
       for (int u = u_begin; u < u_end && ok; ++u) {
         const DecodeItem it = p.items[u];
         const int nt = ntiles_of(it);
+        const int koff = ROPE ? __ldg(p.rk_off + it.req) : 0;
         for (int j = 0; j < nt; ++j, ++gt) {
-          const int stage = gt & 1;
-          const uint32_t n = gt >> 1;
-          if (gt >= 2 && !wt.wait(BAR(KV_EMPTY + stage), (n - 1) & 1)) { ok = false; break; }
-          const int key0 = it.tok0 + kTileN * j;
-          const int nkeys = min(kTileN, it.tok1 - key0);
-          const int nsub = (nkeys + 15) >> 4;
-          const uint32_t ks = stage_k(gt), vs = ks + kTileBytes;
-          ptx::mbar_arrive_expect_tx(BAR(KV_FULL + stage), uint32_t(nsub) * 4u * 2048u);
-          for (int sb = 0; sb < nsub; ++sb) {
-            const int key = key0 + 16 * sb;
-            const int page = __ldg(p.indices + it.page_base + key / p.P);
-            const int row = (page * p.Hk + it.kvh) * p.P + (key % p.P);
-            for (int h = 0; h < 2; ++h) {
-              ptx::tma_load_3d(ks + h * kHalfBytes + sb * 2048, &tm_k, BAR(KV_FULL + stage), 0, h, row, pol);
-              ptx::tma_load_3d(vs + h * kHalfBytes + sb * 2048, &tm_v, BAR(KV_FULL + stage), 0, h, row, pol);
+          cur.kvh = it.kvh;
+          cur.key0 = it.tok0 + kTileN * j;
+          cur.nsub = (min(kTileN, it.tok1 - cur.key0) + 15) >> 4;
+          // all page ids of the tile first (independent loads), then the copies
+#pragma unroll
+          for (int sb = 0; sb < kTileN / 16; ++sb)
+            cur.pages[sb] = sb < cur.nsub ? __ldg(p.indices + it.page_base + (cur.key0 + 16 * sb) / p.P) : 0;
+          const int st = gt & 1;
+          if (gt >= 2 && !wt.wait(BAR(K_EMPTY + st), ((gt >> 1) - 1) & 1)) { ok = false; break; }
+          const uint32_t ks = stage_k(gt);
+          if (ROPE) {
+            // rotated keys are dense per (kv head, request): one box per 64-column block
+            ptx::mbar_arrive_expect_tx(BAR(K_FULL + st), 2u * uint32_t(kHalfBytes));
+            const int row = it.kvh * p.rk_total + koff + cur.key0;
+            for (int h = 0; h < 2; ++h)
+              ptx::tma_load_3d(ks + h * kHalfBytes, &tm_k, BAR(K_FULL + st), 0, h, row, pol);
+          } else {
+            ptx::mbar_arrive_expect_tx(BAR(K_FULL + st), uint32_t(cur.nsub) * 2u * 2048u);
+            for (int sb = 0; sb < cur.nsub; ++sb) {
+              const int row = (cur.pages[sb] * p.Hk + it.kvh) * p.P + ((cur.key0 + 16 * sb) % p.P);
+              for (int h = 0; h < 2; ++h)
+                ptx::tma_load_3d(ks + h * kHalfBytes + sb * 2048, &tm_k, BAR(K_FULL + st), 0, h, row, pol);
             }
           }
+          if (have_prev && !issue_v(prev, gt - 1)) { ok = false; break; }
+          prev = cur;
+          have_prev = true;
         }
       }
+      if (ok && have_prev) issue_v(prev, gt - 1);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -239,9 +246,10 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
       constexpr uint32_t idesc_pv = umma::idesc_bf16_f32(kTileM, D, 0, 1);
       uint32_t gt = 0, qc = 0;   // tiles and non-empty units seen so far
       bool ok = true;
-      // S(g) = Q K(g)^T into S buffer g % 2, once tile g's K is in shared memory
+      // S(g) = Q K(g)^T into S buffer g % 2, once tile g's K is in shared memory;
+      // the K stage is handed back to the producer as soon as these MMAs complete.
       auto issue_qk = [&](uint32_t g) -> bool {
-        if (!wt.wait(BAR((ROPE ? KV_READY : KV_FULL) + (g & 1)), (g >> 1) & 1)) return false;
+        if (!wt.wait(BAR(K_FULL + (g & 1)), (g >> 1) & 1)) return false;
         umma::fence_after_sync();
         const uint32_t ks = stage_k(g);
         for (int k = 0; k < D / 16; ++k) {
@@ -256,6 +264,7 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
                              umma::sdesc_sw128(ks + off, 16, 1024), idesc_qk, 1);
           }
         }
+        umma::commit(BAR(K_EMPTY + (g & 1)));
         umma::commit(BAR(S_FULL + (g & 1)));
         return true;
       };
@@ -270,8 +279,9 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
         if (nt > 1 && !issue_qk(gt + 1)) break;
         for (int j = 0; j < nt; ++j, ++gt) {
           if (!wt.wait(BAR(P_FULL), gt & 1)) { ok = false; break; }
+          if (!wt.wait(BAR(V_FULL + (gt & 1)), (gt >> 1) & 1)) { ok = false; break; }
           umma::fence_after_sync();
-          const uint32_t vs = stage_k(gt) + kTileBytes;
+          const uint32_t vs = stage_v(gt);
           const int key0 = it.tok0 + kTileN * j;
           const int nk16 = (min(kTileN, it.tok1 - key0) + 15) >> 4;
           for (int k = 0; k < nk16; ++k) {
@@ -280,30 +290,11 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
                              umma::sdesc_sw128(vs + k * 2048, kHalfBytes, 1024), idesc_pv,
                              (j > 0 || k > 0) ? 1u : 0u);
           }
-          umma::commit(BAR(KV_EMPTY + (gt & 1)));
+          umma::commit(BAR(V_EMPTY + (gt & 1)));
           umma::commit(BAR(PV_DONE));
           // S buffer gt % 2 was read by the row owners before P_FULL: refill it with tile j + 2
           if (j + 2 < nt && !issue_qk(gt + 2)) { ok = false; break; }
         }
-      }
-    }
-  } else if (warp >= 6) {
-    // ------------------------------------------------------------ RoPE on K (ROPE only)
-    const int t = tid - 192;           // this thread rotates key rows t and t + 64 of the tile
-    uint32_t gt = 0;
-    bool ok = true;
-    for (int u = u_begin; u < u_end && ok; ++u) {
-      const DecodeItem it = p.items[u];
-      const int nt = ntiles_of(it);
-      for (int j = 0; j < nt; ++j, ++gt) {
-        if (!wt.warp_wait(BAR(KV_FULL + (gt & 1)), (gt >> 1) & 1)) { ok = false; break; }
-        const int key0 = it.tok0 + kTileN * j;
-        const int nkeys = min(kTileN, it.tok1 - key0);
-#pragma unroll 1
-        for (int r = t; r < nkeys; r += 64)
-          rope_row_inplace(stage_k(gt), r, p.rope_nat, min(key0 + r, p.rope_max_pos));
-        ptx::fence_proxy_async_smem();
-        mbar_arrive(BAR(KV_READY + (gt & 1)));
       }
     }
   } else {
@@ -361,7 +352,6 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
         for (int j = 0; j < nt; ++j, ++gt) {
           const int key0 = it.tok0 + kTileN * j;
           const int nkeys = min(kTileN, it.tok1 - key0);
-          const uint32_t vs = stage_k(gt) + kTileBytes;
           const int klim = p.causal ? min(nkeys, qpos - key0 + 1) : nkeys;   // keys [0, klim) visible
 
           // ---- S row t: one 128-column TMEM load; mask, online softmax (log2, lazy rescale)
@@ -410,10 +400,17 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
             sts128(base + L::kP + sw_off(t, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
           l = l * alpha + rs;
           // V rows past the last valid key of the final 16-key group may hold
-          // another page's tail: zero them so that P = 0 contributes exactly 0.
-          if (t >= nkeys && t < ((nkeys + 15) & ~15)) {
+          // another page's tail: zero them (once the copy has landed) so that
+          // P = 0 contributes exactly 0.
+          if (nkeys & 15) {
+            const bool mine = t >= nkeys && t < ((nkeys + 15) & ~15);
+            if (__any_sync(0xffffffffu, mine)) {
+              if (!wt.warp_wait(BAR(V_FULL + (gt & 1)), (gt >> 1) & 1)) { ok = false; break; }
+              if (mine) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) sts128(vs + sw_off(t, c), 0u, 0u, 0u, 0u);
+                for (int c = 0; c < 16; ++c) sts128(stage_v(gt) + sw_off(t, c), 0u, 0u, 0u, 0u);
+              }
+            }
           }
           ptx::fence_proxy_async_smem();
           umma::fence_before_sync();
@@ -510,14 +507,57 @@ __global__ void __launch_bounds__(PrefillSmem<ROPE>::kThreads, 1)
     asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(ab) : "r"(abort_addr));
     if (ab) {   // let this CTA's copies land before its shared memory is released
       for (int i = 0; i < 2; ++i) {
-        ptx::mbar_wait_bounded(BAR(KV_FULL + i), 0, 50000000ull);
-        ptx::mbar_wait_bounded(BAR(KV_FULL + i), 1, 50000000ull);
+        for (int b = 0; b < 2; ++b) {
+          ptx::mbar_wait_bounded(BAR(K_FULL + i), b, 50000000ull);
+          ptx::mbar_wait_bounded(BAR(V_FULL + i), b, 50000000ull);
+        }
       }
     }
   }
   if (warp == 5) {
     umma::fence_after_sync();
     umma::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+
+// ---------------------------------------------------------------- RoPE pre-pass
+// One thread per (kv head, key row, 16-byte column chunk of the first half):
+// rotates the pair of chunks (d, d + 64) of one key at its position in the
+// request's page list and writes it to the dense rotated-K buffer.  Threads
+// walk rows fastest, so reads follow the pages and writes are contiguous.
+__global__ void __launch_bounds__(256) rope_k_prepass_kernel(const RopeKParams p) {
+  const int64_t total = int64_t(p.Hk) * p.rk_total * 8;
+  for (int64_t g = int64_t(blockIdx.x) * 256 + threadIdx.x; g < total; g += int64_t(gridDim.x) * 256) {
+    const int c = int(g & 7);
+    const int64_t hr = g >> 3;
+    const int kvh = int(hr / p.rk_total);
+    const int r = int(hr % p.rk_total);
+    int lo = 0, hi = p.n - 1;   // request i with rk_start[i] <= r < rk_start[i + 1]
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(p.rk_start + mid) <= r) lo = mid; else hi = mid - 1;
+    }
+    const int j = r - __ldg(p.rk_start + lo);
+    const int page = __ldg(p.indices + __ldg(p.rk_req_pbase + lo) + j / p.P);
+    const uint16_t* src = p.k_pages + ((size_t(page) * p.Hk + kvh) * p.P + (j % p.P)) * D;
+    const uint4 av = __ldg(reinterpret_cast<const uint4*>(src) + c);
+    const uint4 bv = __ldg(reinterpret_cast<const uint4*>(src) + 8 + c);
+    const float4* tab = reinterpret_cast<const float4*>(p.rope_nat + size_t(min(j, p.rope_max_pos)) * (D / 2));
+    const uint32_t* a = reinterpret_cast<const uint32_t*>(&av);
+    const uint32_t* b = reinterpret_cast<const uint32_t*>(&bv);
+    uint32_t xo[4], yo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float4 cs = __ldg(tab + 4 * c + e);   // frequencies 8c + 2e, 8c + 2e + 1
+      const float a0 = ptx::bf16_lo(a[e]), a1 = ptx::bf16_hi(a[e]);
+      const float b0 = ptx::bf16_lo(b[e]), b1 = ptx::bf16_hi(b[e]);
+      xo[e] = ptx::pack_bf16(a0 * cs.x - b0 * cs.y, a1 * cs.z - b1 * cs.w);
+      yo[e] = ptx::pack_bf16(b0 * cs.x + a0 * cs.y, b1 * cs.z + a1 * cs.w);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(p.rotk + (size_t(kvh) * p.rk_total + r) * D);
+    dst[c] = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+    dst[8 + c] = make_uint4(yo[0], yo[1], yo[2], yo[3]);
   }
 }
 
@@ -541,6 +581,15 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Prefi
 }
 
 }  // namespace
+
+cudaError_t launch_rope_k_prepass(const RopeKParams& p, int num_sms, cudaStream_t stream) {
+  const int64_t work = int64_t(p.Hk) * p.rk_total * 8;
+  int64_t grid = (work + 255) / 256;
+  if (grid > int64_t(num_sms) * 8) grid = int64_t(num_sms) * 8;
+  if (grid < 1) grid = 1;
+  rope_k_prepass_kernel<<<int(grid), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prefill(bool rope, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int grid, cudaStream_t stream) {

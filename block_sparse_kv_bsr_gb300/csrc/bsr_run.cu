@@ -136,7 +136,35 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     }
   }
   if (s->n_pitems > 0) {
+    const bool rotk = rope && s->rk_total > 0;
+    if (rotk) {
+      // rotate the prefill requests' keys once into the schedule's dense buffer
+      if (!s->tm_rk_valid) {
+        if (!encode_pool(&s->tm_rk, s->d_ws + s->off_rotk, int64_t(s->Hk) * s->rk_total, s->D,
+                         bsr::kPrefillRows))
+          return BSR_ERR_CUDA;
+        s->tm_rk_valid = true;
+      }
+      bsr::RopeKParams r{};
+      r.k_pages = static_cast<const uint16_t*>(k_pages);
+      r.indices = s->dev<const int32_t>(s->off_indices);
+      r.rk_req_pbase = s->dev<const int32_t>(s->off_rk_pbase);
+      r.rk_start = s->dev<const int32_t>(s->off_rk_start);
+      r.rope_nat = s->dev<const float2>(s->off_rope + s->rope_bytes);
+      r.rotk = s->dev<uint16_t>(s->off_rotk);
+      r.n = s->rk_n;
+      r.rk_total = s->rk_total;
+      r.Hk = s->Hk;
+      r.P = s->P;
+      r.rope_max_pos = s->rope_rows - 1;
+      if (bsr::launch_rope_k_prepass(r, s->num_sms, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return BSR_ERR_CUDA;
+      }
+    }
     bsr::PrefillParams p{};
+    p.rk_off = rotk ? s->dev<const int32_t>(s->off_rk_off) : nullptr;
+    p.rk_total = rotk ? s->rk_total : 0;
     p.items = s->dev<const bsr::DecodeItem>(s->off_pitems);
     p.cta_ptr = s->dev<const int32_t>(s->off_cta_ptr);
     p.counters = s->dev<int32_t>(s->off_pcounters);
@@ -158,7 +186,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.num_ctas = s->pre_ctas;
     p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
     p.wait_limit_ns = wait_limit_ns;
-    const cudaError_t e = bsr::launch_prefill(rope, tk, tv, p, s->pre_ctas, stream);
+    const cudaError_t e = bsr::launch_prefill(rotk, rotk ? s->tm_rk : tk, tv, p, s->pre_ctas, stream);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return BSR_ERR_CUDA;

@@ -35,6 +35,11 @@ struct bsr_schedule {
   size_t off_indices = 0, off_items = 0, off_warp_ptr = 0, off_counters = 0, off_rope = 0,
          off_error = 0, off_part_o = 0, off_part_lse = 0;
   size_t off_pitems = 0, off_cta_ptr = 0, off_pcounters = 0, off_ppart_o = 0, off_ppart_lse = 0;
+  // RoPE prefill: rotated-K buffer and the request list of its pre-pass
+  size_t off_rk_off = 0, off_rk_pbase = 0, off_rk_start = 0, off_rotk = 0;
+  int32_t rk_n = 0, rk_total = 0;
+  CUtensorMap tm_rk;
+  bool tm_rk_valid = false;
 
   // pinned staging buffer for the single host-to-device upload
   uint8_t* h_stage = nullptr;
@@ -67,4 +72,5 @@ cudaError_t launch_decode_d128(bool rope, bool r16, bool smallp, const CUtensorM
                                cudaStream_t stream);
 cudaError_t launch_prefill(bool rope, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_rope_k_prepass(const RopeKParams& p, int num_sms, cudaStream_t stream);
 }  // namespace bsr
