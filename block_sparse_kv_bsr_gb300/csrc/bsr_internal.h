@@ -71,13 +71,24 @@ struct DecodeParams {
 };
 
 // Work units of the tensor-core prefill kernel use the same record with up to
-// kPrefillRows packed rows; partial states are [slot][kPrefillRows][D].
-constexpr int kPrefillRows = 128;
+// kPrefillRows packed rows (two 128-row query tiles that share every key
+// tile); partial states are [slot][kPrefillRows][D].  Key ranges are cut at
+// multiples of kPrefillKeyTile keys.
+constexpr int kPrefillRows = 256;
+constexpr int kPrefillKeyTile = 128;
+constexpr int kPrefillWarps = 8;  // softmax warps, each owning 32 rows of a unit
+// Tensor-core operands of the RoPE prefill path are fp16 scaled by 2^-4 (an
+// exact power of two), so rotated values up to 2^20 in magnitude fit.
+constexpr float kRopeOperandScale = 0.0625f;
+constexpr float kRopeOperandMax = 65504.f;
+// Device status bits (the status word of a schedule).
+constexpr int32_t kStatusWaitTimeout = 1;
+constexpr int32_t kStatusRopeRange = 2;
 
 struct PrefillParams {
   const DecodeItem* items;
   const int32_t* cta_ptr;         // [num_ctas + 1] unit ranges per CTA
-  int32_t* counters;              // [num_partials, 4] arrivals per (split range, row-owner warp)
+  int32_t* counters;              // [num_partials, kPrefillWarps] arrivals per (split range, softmax warp)
   float* part_o;                  // [num_partials, kPrefillRows, D]
   float* part_lse;                // [num_partials, kPrefillRows] (log2 domain)
   const int32_t* indices;
@@ -102,7 +113,8 @@ struct RopeKParams {
   const int32_t* rk_req_pbase;    // [n] indptr[b] of each prefill request
   const int32_t* rk_start;        // [n + 1]
   const float2* rope_nat;
-  uint16_t* rotk;
+  uint16_t* rotk;                 // fp16, scaled by kRopeOperandScale
+  int32_t* error;                 // status word (kStatusRopeRange on overflow)
   int32_t n, rk_total, Hk, P, rope_max_pos;
 };
 

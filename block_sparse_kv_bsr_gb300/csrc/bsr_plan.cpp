@@ -298,8 +298,9 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
 
   // ---------------------------------------------------------------- units
   // A request goes to the tensor-core prefill kernel when its packed rows fill
-  // at least half of a 128-row tile (and the layout suits it); the others use
-  // the decode kernel's 16-row groups.
+  // at least half of a 128-row query tile (and the layout suits it); the
+  // others use the decode kernel's 16-row groups.  Prefill units hold up to
+  // two query tiles (256 rows).
   std::vector<Unit> dunits, punits;
   int32_t max_rows = 0;
   for (int32_t b = 0; b < batch; ++b) {
@@ -334,7 +335,7 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   hp->rk_total = hp->rk_start.back();
   balance(dunits, int64_t(num_sms) * kDecodeWarps, std::max<int64_t>(page_size, kStageTokens),
           kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec);
-  balance(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillRows), kPrefillOverhead,
+  balance(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillKeyTile), kPrefillOverhead,
           kPrefillMinPiece, kPrefillMinCtaWork, &hp->pre);
 
   hp->group = group;
@@ -413,7 +414,8 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const size_t off_counters = take(size_t(std::max(hp.dec.n_partials, 1)) * 4);
   const size_t off_pitems = take(hp.pre.items.size() * sizeof(DecodeItem));
   const size_t off_cta_ptr = take(hp.pre.ptr.size() * 4);
-  const size_t off_pcounters = take(size_t(std::max(hp.pre.n_partials, 1)) * 4 * 4);  // per row-owner warp
+  const size_t off_pcounters =
+      take(size_t(std::max(hp.pre.n_partials, 1)) * bsr::kPrefillWarps * 4);  // per softmax warp
   const bool rotk = rope && !hp.pre.items.empty() && hp.rk_total > 0;
   const size_t off_rk_off = take(rotk ? size_t(batch) * 4 : 0);
   const size_t off_rk_pbase = take(rotk ? hp.rk_pbase.size() * 4 : 0);

@@ -141,7 +141,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
       // rotate the prefill requests' keys once into the schedule's dense buffer
       if (!s->tm_rk_valid) {
         if (!encode_pool(&s->tm_rk, s->d_ws + s->off_rotk, int64_t(s->Hk) * s->rk_total, s->D,
-                         bsr::kPrefillRows))
+                         bsr::kPrefillKeyTile))
           return BSR_ERR_CUDA;
         s->tm_rk_valid = true;
       }
@@ -157,6 +157,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
       r.Hk = s->Hk;
       r.P = s->P;
       r.rope_max_pos = s->rope_rows - 1;
+      r.error = s->dev<int32_t>(s->off_error);
       if (bsr::launch_rope_k_prepass(r, s->num_sms, stream) != cudaSuccess) {
         cudaGetLastError();
         return BSR_ERR_CUDA;

@@ -230,8 +230,11 @@ int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_pa
                             int32_t out_dtype, float* lse, int32_t* device_status, void* stream);
 
 /* Device-side status word of a schedule (0 = fine; bit 0: a kernel gave up on
- * a bounded wait).  Synchronizes the schedule's device; returns the word, or
- * a negative BSR_ERR_* code. */
+ * a bounded wait; bit 1: with RoPE on the tensor-core prefill path, a rotated
+ * q or k value was at least 2^20 in magnitude, beyond the range of its fp16
+ * operand (x 2^-4), so scores involving it are not finite).  Bits stay set
+ * until the schedule is planned again.  Synchronizes the schedule's device;
+ * returns the word, or a negative BSR_ERR_* code. */
 int bsr_last_device_error(bsr_schedule_t schedule);
 
 /* Static, human-readable text for a status code. */

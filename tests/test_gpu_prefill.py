@@ -14,7 +14,8 @@ import torch
 import block_sparse_kv_bsr_gb300 as bsr
 import workloads as wl
 from block_sparse_kv_bsr_gb300 import _build
-from parity import (LSE_ATOL, assert_lse_close, assert_out_close, check_full, oracle_full, run)
+from parity import (LSE_ATOL, assert_lse_close, assert_out_close, check_full, device_tensors,
+                    oracle_full, plan, run)
 
 pytestmark = pytest.mark.gpu
 
@@ -65,10 +66,13 @@ def test_prefill_rows_at_the_class_boundary():
 
 
 def test_prefill_rope_short_keys_within_rounding_bound():
-    """RoPE with very few keys per query: the rotated keys are bf16 MMA operands (the
-    rotated query is split hi + lo), so each score can move by up to
-    2^-9 * sm_scale * sum_d |q_d k_d|; lse and out are checked against that bound (plus
-    the usual bars) instead of the bare 1e-3, which long key ranges meet by averaging."""
+    """RoPE with very few keys per query: the rotated q and k are fp16 MMA operands
+    (scaled by 2^-4), so each rotated element carries a rounding error of at most
+    2^-11 of itself plus 2^-21 (half the fp16 subnormal spacing, unscaled).  A score
+    then moves by at most sm_scale * (2^-10 * sum_f |q_f| |k_f| + 2^-21 * sum_d (|q_d| +
+    |k_d|)) with |x_f| the norm of rotation pair f (rotation keeps it).  lse and out
+    are checked against that bound (plus the usual bars) instead of the bare 1e-3,
+    which long key ranges meet by averaging."""
     w = wl.make_paged("pfshort", 54, [70, 130], Hq=32, Hk=8, D=128, P=16, qo_lens=[64, 64],
                       causal=True, rope_theta=1e4)
     out, lse, _ = run(w)
@@ -79,13 +83,35 @@ def test_prefill_rope_short_keys_within_rounding_bound():
         pages = w.indices[w.indptr[b]:w.indptr[b + 1]].long()
         K = w.k_pages[pages].permute(1, 0, 2, 3).reshape(w.num_kv_heads, -1, 128)[:, :w.kv_len[b]]
         qb = q[w.qo_indptr[b]:w.qo_indptr[b + 1]]
-        # |q|.|k| products bound the rotated products (rotation keeps pair norms)
+        # pair norms bound the rotated elements and products
         qa = qb.abs().view(qb.shape[0], qb.shape[1], 2, 64).pow(2).sum(2).sqrt()
         ka = K.double().abs().view(K.shape[0], K.shape[1], 2, 64).pow(2).sum(2).sqrt()
         kh = ka.repeat_interleave(w.num_qo_heads // w.num_kv_heads, 0)
-        s_abs = torch.einsum("nhf,hlf->nhl", qa, kh) * w.sm_scale
-        bound = max(bound, float(s_abs.max()) * 2.0 ** -9)
+        s_abs = torch.einsum("nhf,hlf->nhl", qa, kh)
+        sums = qa.sum(-1)[:, :, None] * 2 ** 0.5 + kh.sum(-1)[None, :, :] * 2 ** 0.5
+        b_all = (s_abs * 2.0 ** -10 + sums * 2.0 ** -21) * w.sm_scale
+        bound = max(bound, float(b_all.max()))
     err_l = np.abs(lse.cpu().numpy() - rl)
     assert err_l.max() <= LSE_ATOL + bound, (err_l.max(), bound)
     err_o = np.abs(out.float().cpu().numpy() - ro)
     assert err_o.max() <= 5e-3 + 2 * bound * np.abs(w.v_pages.float().nan_to_num()).max()
+
+
+def test_prefill_rope_operand_range_sets_status():
+    """A rotated key beyond the fp16 operand range (|x| >= 2^20) sets status bit 1;
+    planning again clears the word."""
+    w = wl.make_paged("pfrange", 55, [300], Hq=32, Hk=8, D=128, P=16, qo_lens=[64],
+                      causal=True, rope_theta=1e4)
+    q, k, v = device_tensors(w)
+    k = k.clone()
+    k[int(w.indices[0]), 0, 0, :] = 3.0e6       # key 0 of request 0, kv head 0
+    s = plan(w)
+    assert s.info()["num_prefill_items"] > 0
+    bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta, causal=w.causal)
+    torch.cuda.synchronize()
+    assert bsr.bsr_last_device_error(s) & 2
+    s = plan(w, s)
+    bsr.bsr_attn_run(s, q, *device_tensors(w)[1:], sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+                     causal=w.causal)
+    torch.cuda.synchronize()
+    assert bsr.bsr_last_device_error(s) == 0

@@ -31,12 +31,13 @@ def is_prefill(w: wl.Paged, b: int) -> bool:
 def check_coverage(w: wl.Paged, units: np.ndarray):
     """Every key of every (request, kv head, row group) in exactly one unit, in key order.
 
-    Decode units (warp >= 0) take 16-row groups; prefill units (warp < 0) 128-row tiles.
+    Decode units (warp >= 0) take 16-row groups; prefill units (warp < 0) 256 rows
+    (two 128-row query tiles) with key ranges cut at multiples of 128 keys.
     """
     g = w.num_qo_heads // w.num_kv_heads
     ranges = {}
     for req, kvh, row0, nrows, tok0, tok1, slot, warp in units.tolist():
-        step = 128 if warp < 0 else 16
+        step = 256 if warp < 0 else 16
         assert is_prefill(w, req) == (warp < 0)
         assert 1 <= nrows <= step
         align = max(w.page_size, 128 if warp < 0 else 16)
@@ -46,7 +47,7 @@ def check_coverage(w: wl.Paged, units: np.ndarray):
         L = w.kv_len[b]
         nq = int(w.qo_indptr[b + 1] - w.qo_indptr[b])
         rows = nq * g
-        step = 128 if is_prefill(w, b) else 16
+        step = 256 if is_prefill(w, b) else 16
         for kvh in range(w.num_kv_heads):
             for r0 in range(0, rows, step):
                 nr = min(step, rows - r0)
