@@ -41,9 +41,6 @@
 
 namespace bsr {
 
-// Key count below which the decode kernel also splits rotated keys hi + lo.
-constexpr int kRopeExactKeysBelow = 256;
-
 template <int D>
 struct DecodeCfg {
   static constexpr int kHalves = D / 64;                        // 128-byte column blocks per row
@@ -308,16 +305,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const bool vA = g4 < ci.nrows, vB = R16 && (g4 + 8 < ci.nrows);
     const int qposA = ci.qpos0 + rA / group, qposB = ci.qpos0 + rB / group;
     const int qpos_min = ci.qpos0 + ci.row0 / group;
-    // The rotated keys are bf16 MMA operands.  Their rounding error averages out
-    // over many keys; a unit whose rows see only a few keys also carries the low
-    // bf16 half of each rotated key (a third Q.K^T pass) so that even one key
-    // keeps the score exact to ~16 bits.
-    const bool ksplit = ROPE && qpos_min + 1 < kRopeExactKeysBelow;
 
     // q fragments (A operand): regs [0] and [NR/2] hold row g4 (columns 2t4.. and
     // 8+2t4..); with R16 regs [1] and [3] hold row g4 + 8.
+    // With RoPE the rotated q and k are fp16 operands scaled by 2^-4 (11
+    // significant bits; the scale keeps values up to 2^20 in range).
     uint32_t qh[KS][NR];
-    uint32_t ql[ROPE ? KS : 1][ROPE ? NR : 1];
     {
       const uint16_t* qa =
           p.q + (size_t(ci.q_row0 + rA / group) * p.Hq + ci.kvh * group + rA % group) * D;
@@ -355,12 +348,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             float x[2], y[2];
             rope_pair(raw[ks][r0], raw[ks + KH][r0], make_float2(c01.x, c01.y),
                       make_float2(c01.z, c01.w), x, y);
-            ptx::split_bf16(x[0], x[1], qh[ks][r0], ql[ks][r0]);
-            ptx::split_bf16(y[0], y[1], qh[ks + KH][r0], ql[ks + KH][r0]);
+            qh[ks][r0] = ptx::pack_f16(x[0] * kRopeOperandScale, x[1] * kRopeOperandScale);
+            qh[ks + KH][r0] = ptx::pack_f16(y[0] * kRopeOperandScale, y[1] * kRopeOperandScale);
             rope_pair(raw[ks][r1], raw[ks + KH][r1], make_float2(c23.x, c23.y),
                       make_float2(c23.z, c23.w), x, y);
-            ptx::split_bf16(x[0], x[1], qh[ks][r1], ql[ks][r1]);
-            ptx::split_bf16(y[0], y[1], qh[ks + KH][r1], ql[ks + KH][r1]);
+            qh[ks][r1] = ptx::pack_f16(x[0] * kRopeOperandScale, x[1] * kRopeOperandScale);
+            qh[ks + KH][r1] = ptx::pack_f16(y[0] * kRopeOperandScale, y[1] * kRopeOperandScale);
           }
         }
       }
@@ -454,7 +447,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
           ptx::ldsm_x4(kh, kt + tile_off(k_tok, 16 * (ks + KH) + 8 * k_hb));
           const float4 a01 = __ldg(tabA + 2 * ks), a23 = __ldg(tabA + 2 * ks + 1);
           const float4 b01 = __ldg(tabB + 2 * ks), b23 = __ldg(tabB + 2 * ks + 1);
-          uint32_t lh[4], ll[4] = {0u, 0u, 0u, 0u}, hh[4], hl[4] = {0u, 0u, 0u, 0u};
+          uint32_t lh[4], hh[4];
           // kl[0], kl[1]: key g4 (n-tile 0); kl[2], kl[3]: key 8 + g4 (n-tile 1)
           const float4 cs01[4] = {a01, a23, b01, b23};
 #pragma unroll
@@ -462,31 +455,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
             float x[2], y[2];
             rope_pair(kl[r], kh[r], make_float2(cs01[r].x, cs01[r].y),
                       make_float2(cs01[r].z, cs01[r].w), x, y);
-            if (ksplit) {
-              ptx::split_bf16(x[0], x[1], lh[r], ll[r]);
-              ptx::split_bf16(y[0], y[1], hh[r], hl[r]);
-            } else {
-              lh[r] = ptx::pack_bf16(x[0], x[1]);
-              hh[r] = ptx::pack_bf16(y[0], y[1]);
-            }
+            lh[r] = ptx::pack_f16(x[0] * kRopeOperandScale, x[1] * kRopeOperandScale);
+            hh[r] = ptx::pack_f16(y[0] * kRopeOperandScale, y[1] * kRopeOperandScale);
           }
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             const int kk = half == 0 ? ks : ks + KH;
             const uint32_t* bh = half == 0 ? lh : hh;
-            const uint32_t* bl = half == 0 ? ll : hl;
             const uint32_t h0 = qh[kk][0], h2 = qh[kk][NR / 2];
             const uint32_t h1 = R16 ? qh[kk][1] : 0u, h3 = R16 ? qh[kk][NR - 1] : 0u;
-            const uint32_t l0 = ql[kk][0], l2 = ql[kk][NR / 2];
-            const uint32_t l1 = R16 ? ql[kk][1] : 0u, l3 = R16 ? ql[kk][NR - 1] : 0u;
-            ptx::mma_bf16(s0[0], s0[1], s0[2], s0[3], h0, h1, h2, h3, bh[0], bh[1]);
-            ptx::mma_bf16(s1[0], s1[1], s1[2], s1[3], h0, h1, h2, h3, bh[2], bh[3]);
-            ptx::mma_bf16(s0[0], s0[1], s0[2], s0[3], l0, l1, l2, l3, bh[0], bh[1]);
-            ptx::mma_bf16(s1[0], s1[1], s1[2], s1[3], l0, l1, l2, l3, bh[2], bh[3]);
-            if (ksplit) {
-              ptx::mma_bf16(s0[0], s0[1], s0[2], s0[3], h0, h1, h2, h3, bl[0], bl[1]);
-              ptx::mma_bf16(s1[0], s1[1], s1[2], s1[3], h0, h1, h2, h3, bl[2], bl[3]);
-            }
+            ptx::mma_f16(s0[0], s0[1], s0[2], s0[3], h0, h1, h2, h3, bh[0], bh[1]);
+            ptx::mma_f16(s1[0], s1[1], s1[2], s1[3], h0, h1, h2, h3, bh[2], bh[3]);
           }
         }
       }
@@ -497,7 +476,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
           (nvalid == kStageTokens) && (!p.causal || tok + kStageTokens - 1 <= qpos_min);
       float xa[4], xb[4];
       {
-        const float sc = p.scale_log2;
+        // with RoPE both operands carry 2^-4
+        const float sc = ROPE ? p.scale_log2 * (1.f / (kRopeOperandScale * kRopeOperandScale))
+                              : p.scale_log2;
         const int k0 = tok + 2 * t4;
         const int kidx[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
         const float sa[4] = {s0[0], s0[1], s1[0], s1[1]};
@@ -595,6 +576,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     if constexpr (R16) {
       lB += __shfl_xor_sync(0xffffffffu, lB, 1);
       lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+    }
+    if constexpr (ROPE) {
+      // a rotated q or k beyond the fp16 operand range shows as a non-finite row sum
+      const bool bad = (vA && !isfinite(lA)) || (vB && !isfinite(lB));
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.error, kStatusRopeRange);
     }
     const float lseA = lA > 0.f ? mA + ptx::lg2(lA) : -INFINITY;
     const float lseB = lB > 0.f ? mB + ptx::lg2(lB) : -INFINITY;

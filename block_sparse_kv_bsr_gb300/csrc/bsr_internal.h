@@ -73,10 +73,10 @@ struct DecodeParams {
 // Work units of the tensor-core prefill kernel use the same record with up to
 // kPrefillRows packed rows (two 128-row query tiles that share every key
 // tile); partial states are [slot][kPrefillRows][D].  Key ranges are cut at
-// multiples of kPrefillKeyTile keys.
+// multiples of kPrefillKeyTile keys.  The head group divides 128, so a query
+// tile is whole queries and is one TMA box of q.
 constexpr int kPrefillRows = 256;
 constexpr int kPrefillKeyTile = 128;
-constexpr int kPrefillWarps = 8;  // softmax warps, each owning 32 rows of a unit
 // Tensor-core operands of the RoPE prefill path are fp16 scaled by 2^-4 (an
 // exact power of two), so rotated values up to 2^20 in magnitude fit.
 constexpr float kRopeOperandScale = 0.0625f;
@@ -88,34 +88,50 @@ constexpr int32_t kStatusRopeRange = 2;
 struct PrefillParams {
   const DecodeItem* items;
   const int32_t* cta_ptr;         // [num_ctas + 1] unit ranges per CTA
-  int32_t* counters;              // [num_partials, kPrefillWarps] arrivals per (split range, softmax warp)
-  float* part_o;                  // [num_partials, kPrefillRows, D]
+  float* part_o;                  // [num_partials, kPrefillRows, D] fp32
   float* part_lse;                // [num_partials, kPrefillRows] (log2 domain)
   const int32_t* indices;
-  const float2* rope_nat;         // [rope rows, D / 2] (cos, sin) by frequency, or null
-  const uint16_t* q;
+  const int32_t* rk_off;          // RoPE: first row of each request in the rotated-K buffer
+  int32_t rk_total;               // RoPE: rows per kv head in the rotated-K buffer
   void* out;
   float* lse;
   int32_t* error;
-  const int32_t* rk_off;          // RoPE: first row of each request in the rotated-K buffer
-  int32_t rk_total;               // RoPE: rows per kv head in the rotated-K buffer
   float scale_log2;
   int32_t Hq, Hk, group, P;
-  int32_t causal, out_f32, num_ctas, rope_max_pos;
+  int32_t causal, out_f32, out_v8, num_ctas;
   uint64_t wait_limit_ns;
 };
 
-// Rotate the keys of the prefill requests once per run into a dense buffer
-// [Hk][rk_total][D] (request rows at rk_start[i] .. rk_start[i + 1]).
-struct RopeKParams {
+// Second pass for split prefill units: one warp per packed row combines the
+// unit's partial states (in key order) into out / lse.
+struct PrefillMergeParams {
+  const DecodeItem* units;        // [n_units] the first piece of each split unit
+  const float* part_o;
+  const float* part_lse;
+  void* out;
+  float* lse;
+  int32_t n_units, Hq, group, out_f32;
+};
+
+// RoPE pre-pass of the prefill requests: their keys are rotated once per run
+// into a dense buffer [Hk][rk_total][D] (request rows at rk_start[i] ..
+// rk_start[i + 1]), their queries into a copy of q ([sum_qo][Hq][D], rows
+// rq_row0[i] .., first position rq_pos0[i]).  Both are fp16 scaled by
+// kRopeOperandScale.
+struct RopePrepassParams {
   const uint16_t* k_pages;
+  const uint16_t* q;
   const int32_t* indices;
   const int32_t* rk_req_pbase;    // [n] indptr[b] of each prefill request
   const int32_t* rk_start;        // [n + 1]
-  const float2* rope_nat;
-  uint16_t* rotk;                 // fp16, scaled by kRopeOperandScale
+  const int32_t* rq_row0;         // [n]
+  const int32_t* rq_start;        // [n + 1]
+  const int32_t* rq_pos0;         // [n]
+  const float2* rope_nat;         // [rope rows, D / 2] (cos, sin) by frequency
+  uint16_t* rotk;
+  uint16_t* rotq;
   int32_t* error;                 // status word (kStatusRopeRange on overflow)
-  int32_t n, rk_total, Hk, P, rope_max_pos;
+  int32_t n, rk_total, rq_total, Hk, Hq, P, rope_max_pos;
 };
 
 }  // namespace bsr

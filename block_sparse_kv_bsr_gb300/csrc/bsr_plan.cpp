@@ -242,9 +242,13 @@ struct HostPlan {
   int32_t max_len = 0, max_rows = 0;
   WorkList dec;   // split-KV decode kernel, workers = warps
   WorkList pre;   // tensor-core prefill kernel, workers = CTAs
-  // requests on the prefill kernel (for the rotated-K pre-pass when RoPE is on)
-  std::vector<int32_t> rk_off, rk_pbase, rk_start;
-  int32_t rk_total = 0;
+  std::vector<DecodeItem> pmerge;   // one entry per prefill unit whose key range was split
+  // requests on the prefill kernel (for the RoPE pre-pass): their keys go to a
+  // dense rotated-K buffer at rk_off / rk_start, their queries are rotated in place
+  // of a copy of q (rows rq_row0 .. + (rq_start[i + 1] - rq_start[i]), first
+  // position rq_pos0)
+  std::vector<int32_t> rk_off, rk_pbase, rk_start, rq_row0, rq_start, rq_pos0;
+  int32_t rk_total = 0, rq_total = 0;
 };
 
 int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
@@ -298,15 +302,17 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
 
   // ---------------------------------------------------------------- units
   // A request goes to the tensor-core prefill kernel when its packed rows fill
-  // at least half of a 128-row query tile (and the layout suits it); the
-  // others use the decode kernel's 16-row groups.  Prefill units hold up to
-  // two query tiles (256 rows).
+  // at least half of a 128-row query tile and the layout suits it (head_dim
+  // 128, pages of at least 16 keys, a head group that divides the 128-row
+  // tile, so that a tile is whole queries); the others use the decode
+  // kernel's 16-row groups.  Prefill units hold up to two query tiles (256 rows).
   std::vector<Unit> dunits, punits;
   int32_t max_rows = 0;
   for (int32_t b = 0; b < batch; ++b) {
     const int32_t rows = qo_len[b] * group;
     const int32_t qpos0 = kv_len[b] - qo_len[b];
-    const bool prefill = head_dim == 128 && page_size >= kStageTokens && rows >= kPrefillMinRows;
+    const bool prefill = head_dim == 128 && page_size >= kStageTokens && rows >= kPrefillMinRows &&
+                         bsr::kPrefillKeyTile % group == 0;
     const int32_t step = prefill ? bsr::kPrefillRows : kMaxDecodeRows;
     for (int32_t h = 0; h < num_kv_heads; ++h)
       for (int32_t r0 = 0; r0 < rows; r0 += step) {
@@ -326,17 +332,27 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   hp->rk_off.assign(batch, -1);
   hp->rk_pbase.clear();
   hp->rk_start.assign(1, 0);
+  hp->rq_row0.clear();
+  hp->rq_pos0.clear();
+  hp->rq_start.assign(1, 0);
   for (const Unit& u : punits) {
     if (hp->rk_off[u.req] >= 0 || kv_len[u.req] == 0) continue;
     hp->rk_off[u.req] = hp->rk_start.back();
     hp->rk_pbase.push_back(indptr[u.req]);
     hp->rk_start.push_back(hp->rk_start.back() + kv_len[u.req]);
+    hp->rq_row0.push_back(q_row0[u.req]);
+    hp->rq_pos0.push_back(kv_len[u.req] - qo_len[u.req]);
+    hp->rq_start.push_back(hp->rq_start.back() + qo_len[u.req]);
   }
   hp->rk_total = hp->rk_start.back();
+  hp->rq_total = hp->rq_start.back();
   balance(dunits, int64_t(num_sms) * kDecodeWarps, std::max<int64_t>(page_size, kStageTokens),
           kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec);
   balance(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillKeyTile), kPrefillOverhead,
           kPrefillMinPiece, kPrefillMinCtaWork, &hp->pre);
+  hp->pmerge.clear();
+  for (const DecodeItem& it : hp->pre.items)
+    if (it.slot >= 0 && it.slot == it.first_slot) hp->pmerge.push_back(it);
 
   hp->group = group;
   hp->sum_qo = sum_qo;
@@ -414,12 +430,14 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const size_t off_counters = take(size_t(std::max(hp.dec.n_partials, 1)) * 4);
   const size_t off_pitems = take(hp.pre.items.size() * sizeof(DecodeItem));
   const size_t off_cta_ptr = take(hp.pre.ptr.size() * 4);
-  const size_t off_pcounters =
-      take(size_t(std::max(hp.pre.n_partials, 1)) * bsr::kPrefillWarps * 4);  // per softmax warp
+  const size_t off_pmerge = take(hp.pmerge.size() * sizeof(DecodeItem));
   const bool rotk = rope && !hp.pre.items.empty() && hp.rk_total > 0;
   const size_t off_rk_off = take(rotk ? size_t(batch) * 4 : 0);
   const size_t off_rk_pbase = take(rotk ? hp.rk_pbase.size() * 4 : 0);
   const size_t off_rk_start = take(rotk ? hp.rk_start.size() * 4 : 0);
+  const size_t off_rq_row0 = take(rotk ? hp.rq_row0.size() * 4 : 0);
+  const size_t off_rq_start = take(rotk ? hp.rq_start.size() * 4 : 0);
+  const size_t off_rq_pos0 = take(rotk ? hp.rq_pos0.size() * 4 : 0);
   const size_t off_error = take(16);
   const size_t off_rope = take(rope ? 2 * rope_bytes : 0);
   const size_t image_bytes = off;  // everything above is uploaded
@@ -428,6 +446,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const size_t off_ppart_o = take(size_t(hp.pre.n_partials) * bsr::kPrefillRows * head_dim * 4);
   const size_t off_ppart_lse = take(size_t(hp.pre.n_partials) * bsr::kPrefillRows * 4);
   const size_t off_rotk = take(rotk ? size_t(num_kv_heads) * hp.rk_total * head_dim * 2 : 0);
+  const size_t off_rotq = take(rotk ? size_t(hp.sum_qo) * num_qo_heads * head_dim * 2 : 0);
   const size_t ws_bytes = off;
 
   // ---------------------------------------------------------------- staging + upload
@@ -468,11 +487,16 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   if (!hp.pre.items.empty())
     std::memcpy(h + off_pitems, hp.pre.items.data(), hp.pre.items.size() * sizeof(DecodeItem));
   std::memcpy(h + off_cta_ptr, hp.pre.ptr.data(), hp.pre.ptr.size() * 4);
+  if (!hp.pmerge.empty())
+    std::memcpy(h + off_pmerge, hp.pmerge.data(), hp.pmerge.size() * sizeof(DecodeItem));
   if (rope) std::memcpy(h + off_rope, s->h_rope, 2 * rope_bytes);
   if (rotk) {
     std::memcpy(h + off_rk_off, hp.rk_off.data(), size_t(batch) * 4);
     std::memcpy(h + off_rk_pbase, hp.rk_pbase.data(), hp.rk_pbase.size() * 4);
     std::memcpy(h + off_rk_start, hp.rk_start.data(), hp.rk_start.size() * 4);
+    std::memcpy(h + off_rq_row0, hp.rq_row0.data(), hp.rq_row0.size() * 4);
+    std::memcpy(h + off_rq_start, hp.rq_start.data(), hp.rq_start.size() * 4);
+    std::memcpy(h + off_rq_pos0, hp.rq_pos0.data(), hp.rq_pos0.size() * 4);
   }
   ce = cudaMemcpyAsync(s->d_ws, h, image_bytes, cudaMemcpyHostToDevice, stream);
   if (ce != cudaSuccess) return bail(fail_cuda(ce));
@@ -510,13 +534,20 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->rope_bytes = rope_bytes;
   s->off_pitems = off_pitems;
   s->off_cta_ptr = off_cta_ptr;
-  s->off_pcounters = off_pcounters;
+  s->off_pmerge = off_pmerge;
+  s->n_pmerge = int32_t(hp.pmerge.size());
   s->off_ppart_o = off_ppart_o;
   s->off_ppart_lse = off_ppart_lse;
   s->off_rk_off = off_rk_off;
   s->off_rk_pbase = off_rk_pbase;
   s->off_rk_start = off_rk_start;
   s->off_rotk = off_rotk;
+  s->off_rq_row0 = off_rq_row0;
+  s->off_rq_start = off_rq_start;
+  s->off_rq_pos0 = off_rq_pos0;
+  s->off_rotq = off_rotq;
+  s->rq_total = rotk ? hp.rq_total : 0;
+  s->tm_q_ptr = nullptr;    // Q tensor map: encoded by run
   s->rk_n = rotk ? int32_t(hp.rk_pbase.size()) : 0;
   s->rk_total = rotk ? hp.rk_total : 0;
   s->tm_rk_valid = false;   // encoded by run (the buffer's address may have moved)

@@ -12,26 +12,26 @@
 //
 // Roles (320 threads):
 //   warps 0-3, 4-7  softmax warpgroups, one per query tile: thread t owns row
-//              t of its tile and TMEM lane t.  They load Q (with RoPE: rotated
-//              at the query position and stored as fp16 scaled by 2^-4), run
-//              the online softmax on S rows read from TMEM (one 128-column
-//              load per key tile), write P (bf16) back into the S columns of
+//              t of its tile and TMEM lane t.  They run the online softmax on
+//              S rows read from TMEM, write P (bf16) back into the S columns of
 //              TMEM, rescale O in TMEM when the running max grows by more than
-//              2^8, and write out / lse.
-//   warp 8     TMA producer: fills one FIFO ring of 32 KB stages with the K
-//              and V tiles of every key tile in turn (K(j), V(j), K(j+1), ...),
-//              gathered 16 keys at a time page by page from `indices`
-//              (inactive blocks are absent, "Block-Sparse 포맷"), 128B-swizzled.
-//              With RoPE, K comes already rotated from a dense buffer that a
-//              pre-pass fills once per run.
+//              2^8, and write out / lse (or the fp32 partial state of a split
+//              key range, combined afterwards by bsr_prefill_merge_kernel).
+//   warp 8     TMA producer: loads each unit's query tiles (one box per 64
+//              columns: whole queries of the kv head's group, straight from q,
+//              or with RoPE from the copy the pre-pass rotated) as soon as the
+//              previous unit's last Q K^T has read them, and fills one FIFO ring
+//              of 32 KB stages with the K and V tiles of every key tile in turn
+//              (K(j), V(j), K(j+1), ...), gathered 16 keys at a time page by
+//              page from `indices` (inactive blocks are absent, "Block-Sparse
+//              포맷"), 128B-swizzled.  With RoPE, K comes already rotated from a
+//              dense buffer that the pre-pass fills once per run.
 //   warp 9     allocates TMEM and issues the MMAs: S_i = Q_i K^T (M 128, N 128,
 //              K-major operands from shared memory) and O_i += P_i V (P from
 //              TMEM, V MN-major from shared memory), i = 0, 1.
 // TMEM columns: S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_i overwrites
 // the first 64 columns of S_i.  MMAs run in issue order, so the QK^T of the
 // next key tile may be queued right behind the P V that reads P_i.
-// A unit whose key range was split writes an fp32 partial state; for each
-// 32-row quarter the last arriving warp merges the partials in key order.
 // Every mbarrier wait is bounded and warp-agreed.
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -57,15 +57,15 @@ constexpr uint32_t kTmemCols = 512;
 constexpr int kThreads = 320;
 constexpr int kProducerWarp = 8, kMmaWarp = 9;
 static_assert(kUnitRows == 2 * kTileM, "a unit is two query tiles");
-static_assert(kPrefillWarps == 8, "softmax warps");
 
 struct Smem {
   static constexpr int kQ = 0;                               // Q_0, Q_1
   static constexpr int kRing = 2 * kTileBytes;
   static constexpr int kBars = kRing + kStages * kTileBytes;
-  // full[kStages], empty[kStages], s_full[2], p_full[2], o_full[2], q_full[2], drain
+  // full[kStages], empty[kStages], s_full[2], p_full[2], o_full[2], q_full[2], q_empty[2], drain
   static constexpr int kFull = 0, kEmpty = kStages, kSFull = 2 * kStages, kPFull = kSFull + 2,
-                       kOFull = kPFull + 2, kQFull = kOFull + 2, kDrain = kQFull + 2;
+                       kOFull = kPFull + 2, kQFull = kOFull + 2, kQEmpty = kQFull + 2,
+                       kDrain = kQEmpty + 2;
   static constexpr int kNumBars = kDrain + 1;
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kFlags = kTmemSlot + 16;   // abort flag
@@ -116,30 +116,52 @@ __device__ __forceinline__ int ntiles_of(const DecodeItem& it) {
   return it.tok1 > it.tok0 ? (it.tok1 - it.tok0 + kTileN - 1) / kTileN : 0;
 }
 
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
-               : "memory");
+// Row of `out` (and `lse`) of packed row R of a unit: query R / group of the
+// request, head kvh * group + R % group.
+__device__ __forceinline__ size_t out_row(const DecodeItem& it, int R, int group, int Hq) {
+  return size_t(it.q_row0 + R / group) * Hq + it.kvh * group + R % group;
 }
 
-// Write 32 columns (chunk c) of one output row as bf16 or fp32.
+// Write 32 columns (chunk c) of one output row as bf16 or fp32; 32-byte stores
+// (one full sector per thread) when `out` allows them.
 __device__ __forceinline__ void store_row_chunk(const PrefillParams& p, size_t orow, int c,
                                                 const float (&v)[32]) {
   if (p.out_f32) {
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D + 32 * c);
+    float* dst = static_cast<float*>(p.out) + orow * D + 32 * c;
+    if (p.out_v8) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+      for (int i = 0; i < 4; ++i)
+        ptx::st_global_v8(dst + 8 * i, __float_as_uint(v[8 * i]), __float_as_uint(v[8 * i + 1]),
+                          __float_as_uint(v[8 * i + 2]), __float_as_uint(v[8 * i + 3]),
+                          __float_as_uint(v[8 * i + 4]), __float_as_uint(v[8 * i + 5]),
+                          __float_as_uint(v[8 * i + 6]), __float_as_uint(v[8 * i + 7]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    }
   } else {
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + orow * D + 32 * c);
+    uint16_t* dst = static_cast<uint16_t*>(p.out) + orow * D + 32 * c;
+    uint32_t w[16];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      dst[i] = make_uint4(ptx::pack_bf16(v[8 * i], v[8 * i + 1]), ptx::pack_bf16(v[8 * i + 2], v[8 * i + 3]),
-                          ptx::pack_bf16(v[8 * i + 4], v[8 * i + 5]), ptx::pack_bf16(v[8 * i + 6], v[8 * i + 7]));
+    for (int i = 0; i < 16; ++i) w[i] = ptx::pack_bf16(v[2 * i], v[2 * i + 1]);
+    if (p.out_v8) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+        ptx::st_global_v8(dst + 16 * i, w[8 * i], w[8 * i + 1], w[8 * i + 2], w[8 * i + 3],
+                          w[8 * i + 4], w[8 * i + 5], w[8 * i + 6], w[8 * i + 7]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        reinterpret_cast<uint4*>(dst)[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
   }
 }
 
 template <bool ROPE>
 __global__ void __launch_bounds__(kThreads, 1)
-    bsr_prefill_kernel(const __grid_constant__ CUtensorMap tm_k,
+    bsr_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = Smem;
   extern __shared__ uint8_t smem_raw[];
@@ -165,7 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(BAR(L::kSFull + i), 1);
       ptx::mbar_init(BAR(L::kPFull + i), kTileM);
       ptx::mbar_init(BAR(L::kOFull + i), 1);
-      ptx::mbar_init(BAR(L::kQFull + i), kTileM);
+      ptx::mbar_init(BAR(L::kQFull + i), 1);
+      ptx::mbar_init(BAR(L::kQEmpty + i), 1);
     }
     ptx::mbar_init(BAR(L::kDrain), 1);
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(abort_addr), "r"(0u));
@@ -189,9 +212,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       // K/V tiles are re-read by the other row units of the same (request, kv head),
       // which run concurrently on other SMs: keep them in L2 at normal priority.
+      // Query tiles are read once.
       const uint64_t pol = ptx::policy_evict_normal();
-      uint32_t c = 0;
+      const uint64_t pol_q = ptx::policy_evict_first();
+      uint32_t c = 0, nq0 = 0, nq1 = 0;
       bool ok = true;
+      // query tile i of a unit, once the previous unit's last Q K^T has read the buffer
+      auto load_q = [&](int i, uint32_t& nq, const DecodeItem& it) -> bool {
+        if (nq > 0 && !wt.wait(BAR(L::kQEmpty + i), (nq - 1) & 1u)) return false;
+        ++nq;
+        ptx::mbar_arrive_expect_tx(BAR(L::kQFull + i), uint32_t(kTileBytes));
+        const int q0 = it.q_row0 + (it.row0 + kTileM * i) / p.group;
+        for (int h = 0; h < 2; ++h)
+          ptx::tma_load_4d(Q_S(i) + h * kHalfBytes, &tm_q, BAR(L::kQFull + i), 0, h,
+                           it.kvh * p.group, q0, pol_q);
+        return true;
+      };
       for (int u = u_begin; u < u_end && ok; ++u) {
         const DecodeItem it = p.items[u];
         const int nt = ntiles_of(it);
@@ -222,6 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           ++c;
+          if (j == 0) {
+            if (!load_q(0, nq0, it) || (it.nrows > kTileM && !load_q(1, nq1, it))) { ok = false; break; }
+          }
           // V(j)
           if (c >= kStages && !wt.wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
           ptx::mbar_arrive_expect_tx(FULL(c), uint32_t(nsub) * 2u * 2048u);
@@ -239,6 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) {
         for (uint32_t k = c > kStages ? c - kStages : 0; k < c; ++k)
           ptx::mbar_wait_bounded(FULL(k), PHASE(k), 50000000ull);
+        if (nq0 > 0) ptx::mbar_wait_bounded(BAR(L::kQFull), (nq0 - 1) & 1u, 50000000ull);
+        if (nq1 > 0) ptx::mbar_wait_bounded(BAR(L::kQFull + 1), (nq1 - 1) & 1u, 50000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -286,12 +327,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         qk(0, c);
         if (two) qk(1, c);
         umma::commit(EMPTY(c));
+        if (nt == 1) {   // the query tiles are free once these products complete
+          umma::commit(BAR(L::kQEmpty));
+          if (two) umma::commit(BAR(L::kQEmpty + 1));
+        }
         ++c;
         for (int j = 0; j < nt; ++j) {
           const bool last = j + 1 == nt;
-          const int nk16 = (min(kTileN, it.tok1 - it.tok0 - kTileN * j) + 15) >> 4;
+          const int nkeys = min(kTileN, it.tok1 - it.tok0 - kTileN * j);
+          const int nk16 = (nkeys + 15) >> 4;
           const uint32_t vc = c, kc = c + 1;
-          if (!wt.wait(FULL(vc), PHASE(vc)) || !wait_p(0)) { ok = false; break; }
+          if (!wt.wait(FULL(vc), PHASE(vc))) { ok = false; break; }
+          if (nkeys & 15) {
+            // V rows past the last key of the final 16-key group may hold another
+            // page's tail: zero them so that P = 0 contributes exactly 0
+            const uint32_t vs = STAGE(vc);
+            for (int r = nkeys; r < 16 * nk16; ++r)
+#pragma unroll
+              for (int c16 = 0; c16 < 16; ++c16)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vs + sw_off(r, c16)), "r"(0u)
+                             : "memory");
+            ptx::fence_proxy_async_smem();
+          }
+          if (!wait_p(0)) { ok = false; break; }
           umma::fence_after_sync();
           pv(0, vc, nk16, j > 0);
           if (last) umma::commit(BAR(L::kOFull));
@@ -299,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wt.wait(FULL(kc), PHASE(kc))) { ok = false; break; }
             umma::fence_after_sync();
             qk(0, kc);
+            if (j + 2 == nt) umma::commit(BAR(L::kQEmpty));
           }
           if (two) {
             if (!wait_p(1)) { ok = false; break; }
@@ -308,7 +367,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           umma::commit(EMPTY(vc));
           if (!last) {
-            if (two) qk(1, kc);
+            if (two) {
+              qk(1, kc);
+              if (j + 2 == nt) umma::commit(BAR(L::kQEmpty + 1));
+            }
             umma::commit(EMPTY(kc));
           }
           c += last ? 1 : 2;
@@ -326,63 +388,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_t = S_T(qt) + lane_off, o_t = O_T(qt) + lane_off;
     const float sl2 = ROPE ? p.scale_log2 * (1.f / (kRopeOperandScale * kRopeOperandScale))
                            : p.scale_log2;
-    uint32_t c = 0, ns = 0, no = 0;
+    uint32_t ns = 0, no = 0;
     bool ok = true;
     for (int u = u_begin; u < u_end && ok; ++u) {
       const DecodeItem it = p.items[u];
       const int nt = ntiles_of(it);
       const int rows_here = it.nrows - kTileM * qt;
-      const uint32_t c_unit = c;
-      c += 2u * uint32_t(nt);
       if (rows_here <= 0) continue;        // second query tile of a short unit: nothing to do
       const int group = p.group;
-      const int R = it.row0 + kTileM * qt + t;
+      const int prow = kTileM * qt + t;    // row within the unit
+      const int R = it.row0 + prow;
       const bool vrow = t < rows_here;
       const int qpos = it.qpos0 + R / group;
-      const size_t orow = size_t(it.q_row0 + R / group) * p.Hq + it.kvh * group + R % group;
       float m_used = -INFINITY, l = 0.f;
       if (nt > 0) {
-        // ---- Q row t of this tile
-        uint4 qraw[16];
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + orow * D);
-#pragma unroll
-        for (int c16 = 0; c16 < 16; ++c16) qraw[c16] = vrow ? __ldg(src + c16) : make_uint4(0, 0, 0, 0);
-        const uint32_t qs = Q_S(qt);
-        if constexpr (!ROPE) {
-#pragma unroll
-          for (int c16 = 0; c16 < 16; ++c16)
-            sts128(qs + sw_off(t, c16), qraw[c16].x, qraw[c16].y, qraw[c16].z, qraw[c16].w);
-        } else {
-          // rotated at the query position; fp16 x 2^-4 keeps 11 significant bits
-          const float4* tab = reinterpret_cast<const float4*>(
-              p.rope_nat + size_t(vrow ? min(max(qpos, 0), p.rope_max_pos) : 0) * (D / 2));
-          bool bad = false;
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            const uint32_t* a = reinterpret_cast<const uint32_t*>(&qraw[c8]);
-            const uint32_t* b = reinterpret_cast<const uint32_t*>(&qraw[c8 + 8]);
-            uint32_t xo[4], yo[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float4 cs = __ldg(tab + 4 * c8 + e);   // frequencies 8c + 2e, 8c + 2e + 1
-              const float a0 = ptx::bf16_lo(a[e]), a1 = ptx::bf16_hi(a[e]);
-              const float b0 = ptx::bf16_lo(b[e]), b1 = ptx::bf16_hi(b[e]);
-              const float x0 = (a0 * cs.x - b0 * cs.y) * kRopeOperandScale;
-              const float x1 = (a1 * cs.z - b1 * cs.w) * kRopeOperandScale;
-              const float y0 = (b0 * cs.x + a0 * cs.y) * kRopeOperandScale;
-              const float y1 = (b1 * cs.z + a1 * cs.w) * kRopeOperandScale;
-              bad |= fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(y0), fabsf(y1))) > kRopeOperandMax;
-              xo[e] = ptx::pack_f16(x0, x1);
-              yo[e] = ptx::pack_f16(y0, y1);
-            }
-            sts128(qs + sw_off(t, c8), xo[0], xo[1], xo[2], xo[3]);
-            sts128(qs + sw_off(t, c8 + 8), yo[0], yo[1], yo[2], yo[3]);
-          }
-          if (bad) atomicOr(p.error, kStatusRopeRange);
-        }
-        ptx::fence_proxy_async_smem();
-        mbar_arrive(BAR(L::kQFull + qt));
-
         for (int j = 0; j < nt; ++j) {
           const int key0 = it.tok0 + kTileN * j;
           const int nkeys = min(kTileN, it.tok1 - key0);
@@ -453,23 +472,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 r01 = ptx::fadd2(rs2[0], rs2[1]), r23 = ptx::fadd2(rs2[2], rs2[3]);
           const float2 r = ptx::fadd2(r01, r23);
           l = l * alpha + (r.x + r.y);
-          // V rows past the last valid key of the final 16-key group may hold
-          // another page's tail: zero them (once the copy has landed) so that
-          // P = 0 contributes exactly 0.  The first warpgroup does it for both.
-          bool zeroed = false;
-          if (qt == 0 && (nkeys & 15)) {
-            const bool mine = t >= nkeys && t < ((nkeys + 15) & ~15);
-            if (__any_sync(0xffffffffu, mine)) {
-              const uint32_t vc = c_unit + 2u * uint32_t(j) + 1u;
-              if (!wt.warp_wait(FULL(vc), PHASE(vc))) { ok = false; break; }
-              if (mine) {
-#pragma unroll
-                for (int c16 = 0; c16 < 16; ++c16) sts128(STAGE(vc) + sw_off(t, c16), 0u, 0u, 0u, 0u);
-              }
-              zeroed = true;
-            }
-          }
-          if (zeroed) ptx::fence_proxy_async_smem();
           umma::fence_before_sync();
           mbar_arrive(BAR(L::kPFull + qt));
         }
@@ -478,11 +480,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++no;
         umma::fence_after_sync();
       }
-      // ---- epilogue: O row t / l  (an empty unit writes 0 / -inf), 32 columns at a time
+      // ---- epilogue: O row t / l (an empty unit writes 0 / -inf), 32 columns at a time;
+      // a split range writes its fp32 partial state instead
+      const size_t orow = out_row(it, R, group, p.Hq);
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse2 = l > 0.f ? m_used + ptx::lg2(l) : -INFINITY;
       constexpr float kLn2 = 0.69314718055994530942f;
-      const int prow = kTileM * qt + t;    // row within the unit
       float* part_row = p.part_o + (size_t(it.slot < 0 ? 0 : it.slot) * kUnitRows + prow) * D;
 #pragma unroll 1
       for (int c4 = 0; c4 < 4; ++c4) {
@@ -496,10 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) v[i] = 0.f;
         }
         if (it.slot >= 0) {
-          float4* dst = reinterpret_cast<float4*>(part_row + 32 * c4);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            __stcg(dst + i, make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]));
+          for (int i = 0; i < 4; ++i)
+            ptx::st_global_v8(part_row + 32 * c4 + 8 * i, __float_as_uint(v[8 * i]),
+                              __float_as_uint(v[8 * i + 1]), __float_as_uint(v[8 * i + 2]),
+                              __float_as_uint(v[8 * i + 3]), __float_as_uint(v[8 * i + 4]),
+                              __float_as_uint(v[8 * i + 5]), __float_as_uint(v[8 * i + 6]),
+                              __float_as_uint(v[8 * i + 7]));
         } else if (vrow) {
           store_row_chunk(p, orow, c4, v);
         }
@@ -508,52 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it.slot < 0) {
         if (vrow && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
       } else {
-        __stcg(p.part_lse + size_t(it.slot) * kUnitRows + prow, lse2);
-        __threadfence();
-        __syncwarp();
-        // each warp owns 32 rows of the unit and its own arrival counter, so the
-        // merge needs no CTA-wide synchronization
-        int last = 0;
-        if (lane == 0) last = atomicAdd(p.counters + it.first_slot * kPrefillWarps + warp, 1) == it.nchunks - 1;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();
-          if (vrow) {
-            const float* lse_k = p.part_lse + size_t(it.first_slot) * kUnitRows + prow;
-            float M = -INFINITY;
-            for (int k = 0; k < it.nchunks; ++k) M = fmaxf(M, __ldcg(lse_k + size_t(k) * kUnitRows));
-            float lt = -INFINITY;
-            if (M != -INFINITY) {
-              float sum = 0.f;
-              for (int k = 0; k < it.nchunks; ++k) sum += ptx::ex2(__ldcg(lse_k + size_t(k) * kUnitRows) - M);
-              lt = M + ptx::lg2(sum);
-            }
-#pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
-              float acc[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-              if (M != -INFINITY) {
-                for (int k = 0; k < it.nchunks; ++k) {
-                  const size_t sl = size_t(it.first_slot + k) * kUnitRows + prow;
-                  const float w = ptx::ex2(__ldcg(p.part_lse + sl) - lt);
-                  const float4* srcp = reinterpret_cast<const float4*>(p.part_o + sl * D + 32 * c4);
-#pragma unroll
-                  for (int i = 0; i < 8; ++i) {
-                    const float4 x = __ldcg(srcp + i);
-                    acc[4 * i] += w * x.x;
-                    acc[4 * i + 1] += w * x.y;
-                    acc[4 * i + 2] += w * x.z;
-                    acc[4 * i + 3] += w * x.w;
-                  }
-                }
-              }
-              store_row_chunk(p, orow, c4, acc);
-            }
-            if (p.lse != nullptr) p.lse[orow] = lt * kLn2;
-          }
-          if (lane == 0) atomicExch(p.counters + it.first_slot * kPrefillWarps + warp, 0);
-        }
+        p.part_lse[size_t(it.slot) * kUnitRows + prow] = lse2;
       }
     }
   }
@@ -567,58 +528,146 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- split-range merge
+// One warp per packed row of a split unit: lane l owns columns 4l .. 4l + 3.
+// The partial states (fp32, log2-domain lse) are combined in key order:
+//   lse = M + log2(sum_k 2^(lse_k - M)),  o = sum_k 2^(lse_k - lse) o_k.
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(const PrefillMergeParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int kCtasPerUnit = kUnitRows / kMergeWarps;
+  const int unit = blockIdx.x / kCtasPerUnit;
+  const int prow = (blockIdx.x % kCtasPerUnit) * kMergeWarps + warp;
+  if (unit >= p.n_units) return;
+  const DecodeItem it = p.units[unit];
+  if (prow >= it.nrows) return;
+  const int n = it.nchunks;
+  const float* lse_k = p.part_lse + size_t(it.first_slot) * kUnitRows + prow;
+  float M = -INFINITY;
+  for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldcg(lse_k + size_t(k) * kUnitRows));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float lt = -INFINITY;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
+    float sum = 0.f;
+    for (int k = lane; k < n; k += 32) sum += ptx::ex2(__ldcg(lse_k + size_t(k) * kUnitRows) - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    lt = M + ptx::lg2(sum);
+    const float* po = p.part_o + (size_t(it.first_slot) * kUnitRows + prow) * D + 4 * lane;
+    constexpr size_t kSlotStride = size_t(kUnitRows) * D;
+    for (int kb = 0; kb < n; kb += 32) {
+      const int m = min(32, n - kb);
+      const float wl = lane < m ? ptx::ex2(__ldcg(lse_k + size_t(kb + lane) * kUnitRows) - lt) : 0.f;
+      int j = 0;
+      for (; j + 8 <= m; j += 8) {
+        float4 x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = __ldcg(reinterpret_cast<const float4*>(po + size_t(kb + j + u) * kSlotStride));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float w = __shfl_sync(0xffffffffu, wl, j + u);
+          acc.x += w * x[u].x; acc.y += w * x[u].y; acc.z += w * x[u].z; acc.w += w * x[u].w;
+        }
+      }
+      for (; j < m; ++j) {
+        const float4 x = __ldcg(reinterpret_cast<const float4*>(po + size_t(kb + j) * kSlotStride));
+        const float w = __shfl_sync(0xffffffffu, wl, j);
+        acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
+      }
+    }
+  }
+  const size_t orow = out_row(it, it.row0 + prow, p.group, p.Hq);
+  if (p.out_f32) {
+    reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D)[lane] = acc;
+  } else {
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * D)[lane] =
+        make_uint2(ptx::pack_bf16(acc.x, acc.y), ptx::pack_bf16(acc.z, acc.w));
+  }
+  if (lane == 0 && p.lse != nullptr) p.lse[orow] = lt * 0.69314718055994530942f;
+}
 
 // ---------------------------------------------------------------- RoPE pre-pass
-// One thread per (kv head, key row, 16-byte column chunk of the first half):
-// rotates the pair of chunks (d, d + 64) of one key at its position in the
-// request's page list and writes it, as fp16 scaled by 2^-4 (the operand type
-// of the RoPE prefill's Q K^T), to the dense rotated-K buffer.  Threads
-// walk rows fastest, so reads follow the pages and writes are contiguous.
-__global__ void __launch_bounds__(256) rope_k_prepass_kernel(const RopeKParams p) {
-  const int64_t total = int64_t(p.Hk) * p.rk_total * 8;
+// Rotate the pair of 16-byte chunks (d, d + 64) of one row at its position and
+// store it as fp16 scaled by 2^-4 (the operand type of the RoPE prefill's
+// Q K^T); returns true when a value does not fit.
+__device__ __forceinline__ bool rotate_chunk(const uint16_t* src, uint16_t* dst, int c,
+                                             const float2* rope_row) {
+  const uint4 av = __ldg(reinterpret_cast<const uint4*>(src) + c);
+  const uint4 bv = __ldg(reinterpret_cast<const uint4*>(src) + 8 + c);
+  const float4* tab = reinterpret_cast<const float4*>(rope_row);
+  const uint32_t* a = reinterpret_cast<const uint32_t*>(&av);
+  const uint32_t* b = reinterpret_cast<const uint32_t*>(&bv);
+  uint32_t xo[4], yo[4];
+  bool bad = false;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float4 cs = __ldg(tab + 4 * c + e);   // frequencies 8c + 2e, 8c + 2e + 1
+    const float a0 = ptx::bf16_lo(a[e]), a1 = ptx::bf16_hi(a[e]);
+    const float b0 = ptx::bf16_lo(b[e]), b1 = ptx::bf16_hi(b[e]);
+    const float x0 = (a0 * cs.x - b0 * cs.y) * kRopeOperandScale;
+    const float x1 = (a1 * cs.z - b1 * cs.w) * kRopeOperandScale;
+    const float y0 = (b0 * cs.x + a0 * cs.y) * kRopeOperandScale;
+    const float y1 = (b1 * cs.z + a1 * cs.w) * kRopeOperandScale;
+    bad |= fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(y0), fabsf(y1))) > kRopeOperandMax;
+    xo[e] = ptx::pack_f16(x0, x1);
+    yo[e] = ptx::pack_f16(y0, y1);
+  }
+  reinterpret_cast<uint4*>(dst)[c] = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+  reinterpret_cast<uint4*>(dst)[8 + c] = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+  return bad;
+}
+
+// Request i with start[i] <= r < start[i + 1].
+__device__ __forceinline__ int find_request(const int32_t* start, int n, int r) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(start + mid) <= r) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// One thread per (row, 16-byte chunk of the first half): first every key of
+// the prefill requests (per kv head, at its position in the request's page
+// list, into the dense rotated-K buffer), then every query row of those
+// requests (all heads, at its position, into the rotated copy of q).
+// Threads walk chunks, then rows, so reads and writes are contiguous.
+__global__ void __launch_bounds__(256) rope_prepass_kernel(const RopePrepassParams p) {
+  const int64_t nk = int64_t(p.Hk) * p.rk_total * 8;
+  const int64_t total = nk + int64_t(p.rq_total) * p.Hq * 8;
+  bool bad = false;
   for (int64_t g = int64_t(blockIdx.x) * 256 + threadIdx.x; g < total; g += int64_t(gridDim.x) * 256) {
     const int c = int(g & 7);
-    const int64_t hr = g >> 3;
-    const int kvh = int(hr / p.rk_total);
-    const int r = int(hr % p.rk_total);
-    int lo = 0, hi = p.n - 1;   // request i with rk_start[i] <= r < rk_start[i + 1]
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(p.rk_start + mid) <= r) lo = mid; else hi = mid - 1;
+    if (g < nk) {
+      const int64_t hr = g >> 3;
+      const int kvh = int(hr / p.rk_total);
+      const int r = int(hr % p.rk_total);
+      const int i = find_request(p.rk_start, p.n, r);
+      const int j = r - __ldg(p.rk_start + i);
+      const int page = __ldg(p.indices + __ldg(p.rk_req_pbase + i) + j / p.P);
+      const uint16_t* src = p.k_pages + ((size_t(page) * p.Hk + kvh) * p.P + (j % p.P)) * D;
+      bad |= rotate_chunk(src, p.rotk + (size_t(kvh) * p.rk_total + r) * D, c,
+                          p.rope_nat + size_t(min(j, p.rope_max_pos)) * (D / 2));
+    } else {
+      const int64_t rh = (g - nk) >> 3;
+      const int head = int(rh % p.Hq);
+      const int r = int(rh / p.Hq);
+      const int i = find_request(p.rq_start, p.n, r);
+      const int j = r - __ldg(p.rq_start + i);
+      const size_t row = size_t(__ldg(p.rq_row0 + i) + j) * p.Hq + head;
+      const int pos = __ldg(p.rq_pos0 + i) + j;
+      bad |= rotate_chunk(p.q + row * D, p.rotq + row * D, c,
+                          p.rope_nat + size_t(min(pos, p.rope_max_pos)) * (D / 2));
     }
-    const int j = r - __ldg(p.rk_start + lo);
-    const int page = __ldg(p.indices + __ldg(p.rk_req_pbase + lo) + j / p.P);
-    const uint16_t* src = p.k_pages + ((size_t(page) * p.Hk + kvh) * p.P + (j % p.P)) * D;
-    const uint4 av = __ldg(reinterpret_cast<const uint4*>(src) + c);
-    const uint4 bv = __ldg(reinterpret_cast<const uint4*>(src) + 8 + c);
-    const float4* tab = reinterpret_cast<const float4*>(p.rope_nat + size_t(min(j, p.rope_max_pos)) * (D / 2));
-    const uint32_t* a = reinterpret_cast<const uint32_t*>(&av);
-    const uint32_t* b = reinterpret_cast<const uint32_t*>(&bv);
-    uint32_t xo[4], yo[4];
-    bool bad = false;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float4 cs = __ldg(tab + 4 * c + e);   // frequencies 8c + 2e, 8c + 2e + 1
-      const float a0 = ptx::bf16_lo(a[e]), a1 = ptx::bf16_hi(a[e]);
-      const float b0 = ptx::bf16_lo(b[e]), b1 = ptx::bf16_hi(b[e]);
-      const float x0 = (a0 * cs.x - b0 * cs.y) * kRopeOperandScale;
-      const float x1 = (a1 * cs.z - b1 * cs.w) * kRopeOperandScale;
-      const float y0 = (b0 * cs.x + a0 * cs.y) * kRopeOperandScale;
-      const float y1 = (b1 * cs.z + a1 * cs.w) * kRopeOperandScale;
-      bad |= fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(y0), fabsf(y1))) > kRopeOperandMax;
-      xo[e] = ptx::pack_f16(x0, x1);
-      yo[e] = ptx::pack_f16(y0, y1);
-    }
-    if (bad) atomicOr(p.error, kStatusRopeRange);
-    uint4* dst = reinterpret_cast<uint4*>(p.rotk + (size_t(kvh) * p.rk_total + r) * D);
-    dst[c] = make_uint4(xo[0], xo[1], xo[2], xo[3]);
-    dst[8 + c] = make_uint4(yo[0], yo[1], yo[2], yo[3]);
   }
+  if (bad) atomicOr(p.error, kStatusRopeRange);
 }
 
 template <bool ROPE>
-cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
-                       int grid, cudaStream_t stream) {
+cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const PrefillParams& p, int grid, cudaStream_t stream) {
   auto kern = bsr_prefill_kernel<ROPE>;
   constexpr size_t smem = Smem::kDynBytes;
   static bool opted_in[64] = {};
@@ -631,25 +680,33 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Prefi
     if (e != cudaSuccess) return e;
     opted_in[dev] = true;
   }
-  kern<<<grid, kThreads, smem, stream>>>(tk, tv, p);
+  kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_rope_k_prepass(const RopeKParams& p, int num_sms, cudaStream_t stream) {
-  const int64_t work = int64_t(p.Hk) * p.rk_total * 8;
+cudaError_t launch_rope_prepass(const RopePrepassParams& p, int num_sms, cudaStream_t stream) {
+  const int64_t work = (int64_t(p.Hk) * p.rk_total + int64_t(p.rq_total) * p.Hq) * 8;
   int64_t grid = (work + 255) / 256;
   if (grid > int64_t(num_sms) * 8) grid = int64_t(num_sms) * 8;
   if (grid < 1) grid = 1;
-  rope_k_prepass_kernel<<<int(grid), 256, 0, stream>>>(p);
+  rope_prepass_kernel<<<int(grid), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(bool rope, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int grid, cudaStream_t stream) {
-  return rope ? launch_one<true>(tk, tv, p, grid, stream)
-              : launch_one<false>(tk, tv, p, grid, stream);
+cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const PrefillParams& p, int grid,
+                           cudaStream_t stream) {
+  return rope ? launch_one<true>(tq, tk, tv, p, grid, stream)
+              : launch_one<false>(tq, tk, tv, p, grid, stream);
+}
+
+cudaError_t launch_prefill_merge(const PrefillMergeParams& p, cudaStream_t stream) {
+  const int64_t grid = int64_t(p.n_units) * (kUnitRows / kMergeWarps);
+  if (grid <= 0) return cudaSuccess;
+  bsr_prefill_merge_kernel<<<int(grid), kMergeWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace bsr

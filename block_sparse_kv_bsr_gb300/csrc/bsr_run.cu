@@ -61,6 +61,24 @@ bool encode_pool(CUtensorMap* tm, const void* base, int64_t rows, int D, int box
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map over q (or its rotated copy) [rows, Hq, D = 128] (16-bit) for the
+// prefill kernel's query tiles: rank 4 {64 cols, 2 column blocks, Hq heads,
+// rows}; one box is one 64-column block of `group` heads x 128 / group
+// queries -- the 128 packed rows of a query tile, 128B-swizzled.
+bool encode_q(CUtensorMap* tm, const void* base, int64_t rows, int Hq, int group) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[4] = {64, 2, cuuint64_t(Hq), cuuint64_t(rows)};
+  cuuint64_t strides[3] = {128, 256, cuuint64_t(Hq) * 256};
+  cuuint32_t box[4] = {64, 1, cuuint32_t(group), cuuint32_t(bsr::kPrefillKeyTile / group)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 }  // namespace
@@ -75,8 +93,8 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
   if (s->n_items == 0 && s->n_pitems == 0) return BSR_OK;
   if (q == nullptr || out == nullptr || k_pages == nullptr || v_pages == nullptr)
     return BSR_ERR_INVALID_ARGUMENT;
-  if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(q, 4) ||
-      !aligned(out, out_dtype == BSR_DTYPE_F32 ? 8 : 4) || (lse && !aligned(lse, 4)))
+  if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+      (lse && !aligned(lse, 4)))
     return BSR_ERR_INVALID_ARGUMENT;
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev != s->device) return BSR_ERR_SCHEDULE_MISMATCH;
@@ -138,42 +156,55 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
   if (s->n_pitems > 0) {
     const bool rotk = rope && s->rk_total > 0;
     if (rotk) {
-      // rotate the prefill requests' keys once into the schedule's dense buffer
+      // rotate the prefill requests' keys and queries once into the schedule's buffers
       if (!s->tm_rk_valid) {
         if (!encode_pool(&s->tm_rk, s->d_ws + s->off_rotk, int64_t(s->Hk) * s->rk_total, s->D,
                          bsr::kPrefillKeyTile))
           return BSR_ERR_CUDA;
         s->tm_rk_valid = true;
       }
-      bsr::RopeKParams r{};
+      bsr::RopePrepassParams r{};
       r.k_pages = static_cast<const uint16_t*>(k_pages);
+      r.q = static_cast<const uint16_t*>(q);
       r.indices = s->dev<const int32_t>(s->off_indices);
       r.rk_req_pbase = s->dev<const int32_t>(s->off_rk_pbase);
       r.rk_start = s->dev<const int32_t>(s->off_rk_start);
+      r.rq_row0 = s->dev<const int32_t>(s->off_rq_row0);
+      r.rq_start = s->dev<const int32_t>(s->off_rq_start);
+      r.rq_pos0 = s->dev<const int32_t>(s->off_rq_pos0);
       r.rope_nat = s->dev<const float2>(s->off_rope + s->rope_bytes);
       r.rotk = s->dev<uint16_t>(s->off_rotk);
+      r.rotq = s->dev<uint16_t>(s->off_rotq);
+      r.error = s->dev<int32_t>(s->off_error);
       r.n = s->rk_n;
       r.rk_total = s->rk_total;
+      r.rq_total = s->rq_total;
       r.Hk = s->Hk;
+      r.Hq = s->Hq;
       r.P = s->P;
       r.rope_max_pos = s->rope_rows - 1;
-      r.error = s->dev<int32_t>(s->off_error);
-      if (bsr::launch_rope_k_prepass(r, s->num_sms, stream) != cudaSuccess) {
+      if (bsr::launch_rope_prepass(r, s->num_sms, stream) != cudaSuccess) {
         cudaGetLastError();
         return BSR_ERR_CUDA;
       }
+    }
+    // query tiles come from q, or with RoPE from its rotated copy
+    const void* qsrc = rotk ? static_cast<const void*>(s->d_ws + s->off_rotq) : q;
+    if (s->tm_q_ptr != qsrc) {
+      if (!encode_q(&s->tm_q, qsrc, s->sum_qo, s->Hq, s->group)) {
+        s->tm_q_ptr = nullptr;
+        return BSR_ERR_CUDA;
+      }
+      s->tm_q_ptr = qsrc;
     }
     bsr::PrefillParams p{};
     p.rk_off = rotk ? s->dev<const int32_t>(s->off_rk_off) : nullptr;
     p.rk_total = rotk ? s->rk_total : 0;
     p.items = s->dev<const bsr::DecodeItem>(s->off_pitems);
     p.cta_ptr = s->dev<const int32_t>(s->off_cta_ptr);
-    p.counters = s->dev<int32_t>(s->off_pcounters);
     p.part_o = s->dev<float>(s->off_ppart_o);
     p.part_lse = s->dev<float>(s->off_ppart_lse);
     p.indices = s->dev<const int32_t>(s->off_indices);
-    p.rope_nat = rope ? s->dev<const float2>(s->off_rope + s->rope_bytes) : nullptr;
-    p.q = static_cast<const uint16_t*>(q);
     p.out = out;
     p.lse = lse;
     p.error = s->dev<int32_t>(s->off_error);
@@ -184,10 +215,23 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.P = s->P;
     p.causal = s->causal;
     p.out_f32 = out_dtype == BSR_DTYPE_F32;
+    p.out_v8 = aligned(out, 32);
     p.num_ctas = s->pre_ctas;
-    p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
     p.wait_limit_ns = wait_limit_ns;
-    const cudaError_t e = bsr::launch_prefill(rotk, rotk ? s->tm_rk : tk, tv, p, s->pre_ctas, stream);
+    cudaError_t e = bsr::launch_prefill(rotk, s->tm_q, rotk ? s->tm_rk : tk, tv, p, s->pre_ctas, stream);
+    if (e == cudaSuccess && s->n_pmerge > 0) {
+      bsr::PrefillMergeParams m{};
+      m.units = s->dev<const bsr::DecodeItem>(s->off_pmerge);
+      m.part_o = p.part_o;
+      m.part_lse = p.part_lse;
+      m.out = out;
+      m.lse = lse;
+      m.n_units = s->n_pmerge;
+      m.Hq = s->Hq;
+      m.group = s->group;
+      m.out_f32 = p.out_f32;
+      e = bsr::launch_prefill_merge(m, stream);
+    }
     if (e != cudaSuccess) {
       cudaGetLastError();
       return BSR_ERR_CUDA;

@@ -34,12 +34,17 @@ struct bsr_schedule {
   size_t ws_cap = 0, ws_used = 0, upload_bytes = 0;
   size_t off_indices = 0, off_items = 0, off_warp_ptr = 0, off_counters = 0, off_rope = 0,
          off_error = 0, off_part_o = 0, off_part_lse = 0;
-  size_t off_pitems = 0, off_cta_ptr = 0, off_pcounters = 0, off_ppart_o = 0, off_ppart_lse = 0;
-  // RoPE prefill: rotated-K buffer and the request list of its pre-pass
+  size_t off_pitems = 0, off_cta_ptr = 0, off_pmerge = 0, off_ppart_o = 0, off_ppart_lse = 0;
+  int32_t n_pmerge = 0;      // prefill units whose key range was split (merged by a second kernel)
+  // RoPE prefill: rotated-K and rotated-Q buffers and the request list of their pre-pass
   size_t off_rk_off = 0, off_rk_pbase = 0, off_rk_start = 0, off_rotk = 0;
-  int32_t rk_n = 0, rk_total = 0;
+  size_t off_rq_row0 = 0, off_rq_start = 0, off_rq_pos0 = 0, off_rotq = 0;
+  int32_t rk_n = 0, rk_total = 0, rq_total = 0;
   CUtensorMap tm_rk;
   bool tm_rk_valid = false;
+  // prefill query tiles: over q (no RoPE) or the rotated copy (RoPE)
+  CUtensorMap tm_q;
+  const void* tm_q_ptr = nullptr;
 
   // pinned staging buffer for the single host-to-device upload
   uint8_t* h_stage = nullptr;
@@ -70,7 +75,9 @@ cudaError_t launch_decode_d64(bool rope, bool r16, bool smallp, const CUtensorMa
 cudaError_t launch_decode_d128(bool rope, bool r16, bool smallp, const CUtensorMap& tk,
                                const CUtensorMap& tv, const DecodeParams& p, int grid,
                                cudaStream_t stream);
-cudaError_t launch_prefill(bool rope, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_rope_k_prepass(const RopeKParams& p, int num_sms, cudaStream_t stream);
+cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const PrefillParams& p, int grid,
+                           cudaStream_t stream);
+cudaError_t launch_prefill_merge(const PrefillMergeParams& p, cudaStream_t stream);
+cudaError_t launch_rope_prepass(const RopePrepassParams& p, int num_sms, cudaStream_t stream);
 }  // namespace bsr

@@ -109,7 +109,8 @@ int bsr_attn_plan(const int32_t* indptr, const int32_t* indices, const int32_t* 
  * be NULL) are written.  All are caller-owned device buffers; no buffer may
  * alias another.  sm_scale must be finite and > 0.  rope_theta and causal
  * must equal the values given to plan (else BSR_ERR_SCHEDULE_MISMATCH).
- * k_pages/v_pages must be 16-byte aligned.
+ * q, k_pages, v_pages and out must be 16-byte aligned (else
+ * BSR_ERR_INVALID_ARGUMENT).
  * The call allocates nothing, never synchronizes the host, and is
  * stream-ordered; it may be captured in a CUDA graph.  Two runs of one
  * schedule must not overlap in time (they share its merge workspace).

@@ -213,3 +213,26 @@ def test_append_rejects_out_of_range_page_on_device():
     torch.cuda.synchronize()
     assert int(status.item()) == 1
     assert np.array_equal(bits(k), before)
+
+
+def test_decode_rope_short_keys():
+    """RoPE decode rows with few keys: the rotated q and k are fp16 MMA operands (11
+    significant bits), so even a handful of keys keeps lse within 1e-3."""
+    w = wl.make_paged("decropeshort", 82, [5, 17, 40, 300], Hq=32, Hk=8, D=128, P=16,
+                      rope_theta=1e4)
+    out, lse, _ = run(w)
+    check_full(w, out, lse)
+
+
+def test_decode_rope_operand_range_sets_status():
+    """A rotated key beyond the fp16 operand range (|x| >= 2^20) on the decode path
+    sets status bit 1."""
+    w = wl.make_paged("decrange", 81, [300, 200], Hq=32, Hk=8, D=128, P=16, rope_theta=1e4)
+    q, k, v = device_tensors(w)
+    k = k.clone()
+    k[int(w.indices[0]), 0, 5, :] = 3.0e6       # key 5 of request 0, kv head 0
+    s = plan(w)
+    assert s.info()["num_decode_items"] > 0 and s.info()["num_prefill_items"] == 0
+    bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta, causal=w.causal)
+    torch.cuda.synchronize()
+    assert bsr.bsr_last_device_error(s) & 2

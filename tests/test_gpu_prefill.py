@@ -115,3 +115,24 @@ def test_prefill_rope_operand_range_sets_status():
                      causal=w.causal)
     torch.cuda.synchronize()
     assert bsr.bsr_last_device_error(s) == 0
+
+
+@pytest.mark.parametrize("Hq,rope", [(8, 0.0), (16, 0.0), (64, 1e4), (128, 0.0)])
+def test_prefill_group_sizes(Hq, rope):
+    """A query tile is 128 / group whole queries of one kv head's group (one TMA box)."""
+    g = Hq // 8
+    w = wl.make_paged(f"pfg{g}", 60 + g, [500, 900], Hq=Hq, Hk=8, D=128, P=16, qo_lens=[200, 77],
+                      causal=True, rope_theta=rope)
+    out, lse, s = run(w)
+    assert s.info()["num_prefill_items"] > 0
+    check_full(w, out, lse)
+
+
+def test_prefill_group_not_dividing_the_tile_takes_decode():
+    # group 3 does not divide a 128-row tile: every row goes to the decode kernel
+    w = wl.make_paged("pfg3", 70, [400, 260], Hq=24, Hk=8, D=128, P=16, qo_lens=[100, 64],
+                      causal=True, rope_theta=1e4)
+    out, lse, s = run(w)
+    info = s.info()
+    assert info["num_prefill_items"] == 0 and info["num_decode_items"] > 0
+    check_full(w, out, lse)
