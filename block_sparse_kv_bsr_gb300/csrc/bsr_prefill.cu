@@ -291,24 +291,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t c = 0;
       uint32_t nq[2] = {0, 0}, np[2] = {0, 0};
       bool ok = true;
+      // Shared-memory descriptors are built once; per MMA only a constant offset is
+      // added to the address field (bits 0-13, address / 16: shared memory ends below
+      // 256 KB, so the field never carries).
+      const uint64_t dq0 = umma::sdesc_sw128(Q_S(0), 16, 1024);
+      const uint64_t dq1 = umma::sdesc_sw128(Q_S(1), 16, 1024);
+      const uint64_t dk = umma::sdesc_sw128(STAGE(0), 16, 1024);            // K-major stage 0
+      const uint64_t dv = umma::sdesc_sw128(STAGE(0), kHalfBytes, 1024);    // MN-major stage 0
+      auto stage_field = [&](uint32_t c) { return uint64_t((c % kStages) * uint32_t(kTileBytes / 16)); };
       // S_i = Q_i K^T from the K stage at ring position kc
       auto qk = [&](int i, uint32_t kc) {
-        const uint32_t ks = STAGE(kc);
+        const uint64_t kd = dk + stage_field(kc), qd = i == 0 ? dq0 : dq1;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-          umma::mma_f16_ss(S_T(i), umma::sdesc_sw128(Q_S(i) + off, 16, 1024),
-                           umma::sdesc_sw128(ks + off, 16, 1024), idesc_qk, k > 0);
+          const uint64_t off = uint64_t(((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4);
+          umma::mma_f16_ss(S_T(i), qd + off, kd + off, idesc_qk, k > 0);
         }
         umma::commit(BAR(L::kSFull + i));
       };
       // O_i (+)= P_i V from the V stage at ring position vc
       auto pv = [&](int i, uint32_t vc, int nk16, bool acc) {
-        const uint32_t vs = STAGE(vc);
-        for (int k = 0; k < nk16; ++k)
-          umma::mma_f16_ts(O_T(i), S_T(i) + 8u * uint32_t(k),
-                           umma::sdesc_sw128(vs + k * 2048, kHalfBytes, 1024), idesc_pv,
-                           (acc || k > 0) ? 1u : 0u);
+        const uint64_t vd = dv + stage_field(vc);
+#pragma unroll
+        for (int k = 0; k < kTileN / 16; ++k)
+          if (k < nk16)
+            umma::mma_f16_ts(O_T(i), S_T(i) + 8u * uint32_t(k), vd + uint64_t((k * 2048) >> 4),
+                             idesc_pv, (acc || k > 0) ? 1u : 0u);
       };
       auto wait_p = [&](int i) {
         const bool r = wt.wait(BAR(L::kPFull + i), np[i] & 1u);
