@@ -37,7 +37,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "BSR decode attention achieved HBM GB/s & % of GB300 peak; µs/call (skewed)"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "bsr_decode_skewed_b128.md")
+PROFILES = os.path.join(ROOT, "profiles")
 
 
 def parse():
@@ -155,11 +155,11 @@ class ClockSampler:
                 "window": how}
 
 
-def traffic_from_profile(digest: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was captured on the
-    decode kernel built from the current sources (digest of those sources)."""
+def traffic_from_profile(name: str, digest: str):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, if it was
+    captured on the kernel built from the current sources (digest of those sources)."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(os.path.join(PROFILES, name)).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(build\s+([0-9a-f]+)\)", text)
@@ -190,12 +190,21 @@ def cpu_baseline(w, budget_s=10.0, min_passes=1):
 
 
 class Part:
-    """One library call of a step, timed with its own CUDA events."""
+    """One library call of a step, timed with its own CUDA events.
 
-    def __init__(self, label, fn, kernel, bound, work, work_unit):
+    For bsr_attn_run calls `sched`/`stage` name the schedule and the stage whose
+    kernel the roofline is about (timed by the library's stage events); `family`
+    and `profile` select the committed ncu summary holding its DRAM traffic.
+    """
+
+    def __init__(self, label, fn, kernel, bound, work, work_unit, launches=1, sched=None,
+                 stage=None, family=None, profile=None):
         self.label, self.fn, self.kernel, self.bound = label, fn, kernel, bound
         self.work, self.work_unit = work, work_unit      # algorithmic bytes or FLOPs per call
-        self.ms = []
+        self.launches, self.sched, self.stage = launches, sched, stage
+        self.family, self.profile = family, profile
+        self.ms = []          # whole call
+        self.kernel_ms = []   # the stage's kernel alone
 
 
 def attention_flops(w) -> int:
@@ -233,7 +242,10 @@ def build_job(cfg: int, dev, small: bool):
                                        causal=w.causal, out=out, lse=lse)
         alg = wl.algorithmic_bytes(w)
         kname = f"bsr_decode_kernel<{w.head_dim},{int(w.rope_theta > 0)},0,0>"
-        job["parts"] = [Part("decode", run, kname, "hbm", alg, "B")]
+        prof = {2: "bsr_decode_rope_llama8b_b64.md", 3: "bsr_decode_skewed_b128.md"}.get(cfg)
+        job["parts"] = [Part("decode", run, kname, "hbm", alg, "B",
+                             launches=s.info()["kernels_per_run"], sched=s, stage="decode",
+                             family="decode", profile=None if small else prof)]
         job["schedules"] = [s]
         job.update(workload=w, metric=METRIC, unit="GB/s", numerator=alg, scale=1e9,
                    config={"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads,
@@ -281,10 +293,14 @@ def build_job(cfg: int, dev, small: bool):
         job["parts"] = [
             Part("prefix", lambda: bsr.bsr_attn_run(sp, q, pk, pv, sm_scale=pre.sm_scale,
                                                     out=o_p, lse=l_p),
-                 "bsr_prefill_kernel<0>", "tensor", attention_flops(pre), "FLOP"),
+                 "bsr_prefill_kernel<0>", "tensor", attention_flops(pre), "FLOP",
+                 launches=sp.info()["kernels_per_run"], sched=sp, stage="prefill",
+                 family="prefill", profile=None if small else "bsr_prefill_cascade_prefix8192.md"),
             Part("suffix", lambda: bsr.bsr_attn_run(ss, q, sk, sv, sm_scale=suf.sm_scale,
                                                     out=o_s, lse=l_s),
-                 "bsr_decode_kernel<128,0,0,0>", "hbm", kv_s + qo + st, "B"),
+                 "bsr_decode_kernel<128,0,0,0>", "hbm", kv_s + qo + st, "B",
+                 launches=ss.info()["kernels_per_run"], sched=ss, stage="decode",
+                 family="decode", profile=None if small else "bsr_decode_cascade_suffix.md"),
             Part("merge", lambda: bsr.bsr_merge_states(o_p, l_p, o_s, l_s, o_out=o, lse_out=l),
                  "merge_states_kernel<128,1>", "hbm", 3 * st, "B"),
         ]
@@ -312,7 +328,9 @@ def build_job(cfg: int, dev, small: bool):
             Part("prefill", lambda: bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale,
                                                      rope_theta=w.rope_theta, causal=True,
                                                      out=out, lse=lse),
-                 "bsr_prefill_kernel<1>", "tensor", flops, "FLOP"),
+                 "bsr_prefill_kernel<1>", "tensor", flops, "FLOP",
+                 launches=s.info()["kernels_per_run"], sched=s, stage="prefill",
+                 family="prefill", profile=None if small else "bsr_prefill_chunked_b16_q512.md"),
         ]
         job["schedules"] = [s]
         job.update(workload=w, metric="BSR chunked-prefill attention (causal, RoPE): TFLOP/s",
@@ -354,9 +372,7 @@ def main():
         step()
     torch.cuda.synchronize()
 
-    # ---- device-timed steps: one event pair per call (kernel duration) + the whole region
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in parts] for _ in range(args.steps)]
+    # ---- region 1: K steps with events only at its ends (whole-job time, clocks)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -365,11 +381,8 @@ def main():
     t_end = torch.cuda.Event(enable_timing=True)
     clocks.mark_start()
     t_start.record(stream)
-    for row in evs:
-        for pt, (a, b) in zip(parts, row):
-            a.record(stream)
-            pt.fn()
-            b.record(stream)
+    for _ in range(args.steps):
+        step()
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks.mark_end()
@@ -377,9 +390,31 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
+
+    # ---- region 2: K more steps timed per call (CUDA events around each library call)
+    # and per kernel (the library's own events around each kernel of a bsr_attn_run
+    # call); these records sit between kernels, so they are kept out of region 1
+    for pt in parts:
+        if pt.sched is not None:
+            bsr.bsr_schedule_set_stage_timing(pt.sched, args.steps)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in parts] for _ in range(args.steps)]
+    for row in evs:
+        for pt, (a, b) in zip(parts, row):
+            a.record(stream)
+            pt.fn()
+            b.record(stream)
+    torch.cuda.synchronize()
     for row in evs:
         for pt, (a, b) in zip(parts, row):
             pt.ms.append(a.elapsed_time(b))
+    for pt in parts:
+        if pt.sched is not None:
+            for call in range(args.steps):
+                t = bsr.bsr_schedule_stage_times(pt.sched, call)
+                if pt.stage in t:
+                    pt.kernel_ms.append(t[pt.stage])
+            bsr.bsr_schedule_set_stage_timing(pt.sched, 0)
     ms_step = total_ms / args.steps
     if world > 1:
         t = torch.tensor([ms_step], device=dev)
@@ -408,7 +443,15 @@ def main():
     peak_tensor, tensor_kind = tensor_peak()
     # the roofline reports the call that takes the most time in a step
     dom = max(parts, key=lambda pt: sum(pt.ms))
-    dom_ms = sum(dom.ms) / len(dom.ms)
+    call_ms = sum(dom.ms) / len(dom.ms)
+    # the kernel's own duration (library stage events) where the call launches more than one
+    kms = dom.kernel_ms if dom.kernel_ms else dom.ms
+    dom_ms = sum(kms) / len(kms)
+    traffic = None
+    if dom.profile is not None:
+        sources = {"decode": _build.DECODE_KERNEL_SOURCES,
+                   "prefill": _build.PREFILL_KERNEL_SOURCES}[dom.family]
+        traffic = traffic_from_profile(dom.profile, _build.kernel_digest(sources))
     if dom.bound == "hbm":
         achieved, peak, unit, kind = dom.work / (dom_ms * 1e-3) / 1e9, peak_hbm, "GB/s", hbm_kind
         kind = f"{kind} hbm_gbs (copy)"
@@ -433,11 +476,17 @@ def main():
         "config": dict(job["config"], parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
         "roofline": {"bound": dom.bound, "achieved": round(achieved, 1), "peak": peak,
                      "unit": unit, "frac": round(achieved / peak, 4), "peak_kind": kind,
-                     "traffic": traffic_from_profile(_build.kernel_digest()) if args.config == 3 else None,
-                     "kernel": dom.kernel, "kernel_us_mean": round(dom_ms * 1e3, 2),
-                     "kernel_us_min": round(min(dom.ms) * 1e3, 2)},
+                     "traffic": traffic, "kernel": dom.kernel,
+                     "kernel_us_mean": round(dom_ms * 1e3, 2),
+                     "kernel_us_min": round(min(kms) * 1e3, 2),
+                     "timed_by": ("library stage events around the kernel" if dom.kernel_ms
+                                  else "CUDA events around the call") + ", second timed pass of K steps",
+                     "call_us_mean": round(call_ms * 1e3, 2)},
         "parts_us": {pt.label: round(sum(pt.ms) / len(pt.ms) * 1e3, 2) for pt in parts},
-        "gpu_launches": args.steps * len(parts),
+        "kernels_us": {f"{pt.label}.{pt.stage}": round(sum(pt.kernel_ms) / len(pt.kernel_ms) * 1e3, 2)
+                       for pt in parts if pt.kernel_ms},
+        "gpu_launches": args.steps * sum(pt.launches for pt in parts),
+        "gpu_launches_note": "kernels launched in the whole-job timed region (region 1)",
         "clocks": clocks.summary(),
     }
     if e2e is not None:

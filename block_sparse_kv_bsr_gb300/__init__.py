@@ -19,7 +19,7 @@ __all__ = [
     "BsrError", "load", "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run",
     "bsr_merge_states", "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info",
     "bsr_last_device_error", "bsr_status_string", "bsr_attn_decode_noalloc", "Schedule",
-    "EXPORTED_SYMBOLS",
+    "bsr_schedule_set_stage_timing", "bsr_schedule_stage_times", "STAGES", "EXPORTED_SYMBOLS",
 ]
 
 BSR_OK = 0
@@ -29,7 +29,8 @@ BSR_DTYPE_F32 = 1
 EXPORTED_SYMBOLS = (
     "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run", "bsr_merge_states", "bsr_append_kv",
     "bsr_schedule_destroy", "bsr_schedule_get_info", "bsr_last_device_error",
-    "bsr_status_string", "bsr_attn_decode_noalloc",
+    "bsr_status_string", "bsr_attn_decode_noalloc", "bsr_schedule_set_stage_timing",
+    "bsr_schedule_stage_times",
 )
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -56,6 +57,7 @@ class _Info(ctypes.Structure):
         ("num_sms", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
         ("upload_bytes", ctypes.c_int64),
         ("decode_imbalance", ctypes.c_double), ("prefill_imbalance", ctypes.c_double),
+        ("kernels_per_run", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -96,6 +98,10 @@ def load(path: str | None = None):
     lib.bsr_schedule_get_info.argtypes = [_vp, ctypes.POINTER(_Info)]
     lib.bsr_last_device_error.restype = ctypes.c_int
     lib.bsr_last_device_error.argtypes = [_vp]
+    lib.bsr_schedule_set_stage_timing.restype = ctypes.c_int
+    lib.bsr_schedule_set_stage_timing.argtypes = [_vp, ctypes.c_int32]
+    lib.bsr_schedule_stage_times.restype = ctypes.c_int
+    lib.bsr_schedule_stage_times.argtypes = [_vp, ctypes.c_int32, ctypes.POINTER(ctypes.c_float)]
     lib.bsr_attn_decode_noalloc.restype = ctypes.c_int
     lib.bsr_attn_decode_noalloc.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32,
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
@@ -280,6 +286,24 @@ def bsr_last_device_error(schedule: Schedule) -> int:
     if code < 0:
         raise BsrError(code, "bsr_last_device_error")
     return code
+
+
+STAGES = ("decode", "rope_prepass", "prefill", "merge")
+
+
+def bsr_schedule_set_stage_timing(schedule: Schedule, max_calls: int):
+    """Record CUDA events around each kernel of the next runs (keeps the last max_calls)."""
+    _check(load().bsr_schedule_set_stage_timing(_vp(schedule.handle), int(max_calls)),
+           "bsr_schedule_set_stage_timing")
+
+
+def bsr_schedule_stage_times(schedule: Schedule, call: int) -> dict:
+    """Stage durations (ms) of kept run `call` (0 = oldest kept); absent stages omitted."""
+    ms = (ctypes.c_float * 4)()
+    code = load().bsr_schedule_stage_times(_vp(schedule.handle), int(call), ms)
+    if code < 0:
+        raise BsrError(code, "bsr_schedule_stage_times")
+    return {name: float(ms[i]) for i, name in enumerate(STAGES) if ms[i] >= 0}
 
 
 def bsr_attn_decode_noalloc(q, k_pages, v_pages, indptr, indices, last_page_len, *,

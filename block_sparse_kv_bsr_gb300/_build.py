@@ -47,8 +47,9 @@ def _digest() -> str:
     return h.hexdigest()[:16]
 
 
-# Sources that determine the decode kernel's machine code (for matching a profile to a build).
+# Sources that determine a kernel family's machine code (for matching a profile to a build).
 DECODE_KERNEL_SOURCES = ("bsr_decode.cuh", "bsr_decode_d128.cu", "bsr_internal.h", "ptx.cuh")
+PREFILL_KERNEL_SOURCES = ("bsr_prefill.cu", "bsr_internal.h", "ptx.cuh", "umma.cuh")
 
 
 def kernel_digest(names=DECODE_KERNEL_SOURCES) -> str:

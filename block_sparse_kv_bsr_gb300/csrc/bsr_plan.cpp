@@ -573,6 +573,7 @@ extern "C" void bsr_schedule_destroy(bsr_schedule_t s) {
     cudaFree(s->d_ws);
   }
   if (s->upload_done) cudaEventDestroy(s->upload_done);
+  for (cudaEvent_t e : s->t_ev) cudaEventDestroy(e);
   if (s->h_stage) cudaFreeHost(s->h_stage);
   std::free(s->h_rope);
   cudaGetLastError();
@@ -603,6 +604,8 @@ extern "C" int bsr_schedule_get_info(bsr_schedule_t s, bsr_schedule_info_t* info
   info->upload_bytes = int64_t(s->upload_bytes);
   info->decode_imbalance = s->dec_imbalance;
   info->prefill_imbalance = s->pre_imbalance;
+  info->kernels_per_run = (s->n_items > 0 ? 1 : 0) + (s->n_pitems > 0 ? 1 : 0) +
+                          (s->n_pitems > 0 && s->rk_total > 0 ? 1 : 0) + (s->n_pmerge > 0 ? 1 : 0);
   return BSR_OK;
 }
 
@@ -639,6 +642,9 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
     info->num_sms = num_sms;
     info->decode_imbalance = hp.dec.imbalance;
     info->prefill_imbalance = hp.pre.imbalance;
+    info->kernels_per_run = (hp.dec.items.empty() ? 0 : 1) + (hp.pre.items.empty() ? 0 : 1) +
+                            (!hp.pre.items.empty() && rope_theta > 0.f && hp.rk_total > 0 ? 1 : 0) +
+                            (hp.pmerge.empty() ? 0 : 1);
   }
   const int64_t n = int64_t(hp.dec.items.size() + hp.pre.items.size());
   if (units != nullptr) {

@@ -112,6 +112,19 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     s->tm_v_ptr = v_pages;
   }
 
+  // optional stage timing: events around each launch, in the next slot of the ring
+  int t_slot = -1;
+  if (s->t_max > 0) {
+    t_slot = int(s->t_count % s->t_max);
+    ++s->t_count;
+    for (int st = 0; st < bsr_schedule::kStages; ++st) s->t_ran[t_slot * bsr_schedule::kStages + st] = 0;
+  }
+  auto t_mark = [&](int stage, int edge) {
+    if (t_slot < 0) return;
+    cudaEventRecord(s->t_ev[(t_slot * bsr_schedule::kStages + stage) * 2 + edge], stream);
+    if (edge == 1) s->t_ran[t_slot * bsr_schedule::kStages + stage] = 1;
+  };
+
   const bool rope = s->rope_rows > 0;
   const float scale_log2 = float(double(sm_scale) * 1.4426950408889634);
   const uint64_t wait_limit_ns = 1000000000ull;  // 1 s: orders of magnitude above any healthy wait
@@ -145,9 +158,11 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
     p.wait_limit_ns = wait_limit_ns;
     const bool r16 = s->max_rows > 8;
+    t_mark(0, 0);
     const cudaError_t e =
         s->D == 128 ? bsr::launch_decode_d128(rope, r16, smallp, tk, tv, p, s->dec_ctas, stream)
                     : bsr::launch_decode_d64(rope, r16, smallp, tk, tv, p, s->dec_ctas, stream);
+    t_mark(0, 1);
     if (e != cudaSuccess) {
       cudaGetLastError();
       return BSR_ERR_CUDA;
@@ -183,10 +198,12 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
       r.Hq = s->Hq;
       r.P = s->P;
       r.rope_max_pos = s->rope_rows - 1;
+      t_mark(1, 0);
       if (bsr::launch_rope_prepass(r, s->num_sms, stream) != cudaSuccess) {
         cudaGetLastError();
         return BSR_ERR_CUDA;
       }
+      t_mark(1, 1);
     }
     // query tiles come from q, or with RoPE from its rotated copy
     const void* qsrc = rotk ? static_cast<const void*>(s->d_ws + s->off_rotq) : q;
@@ -218,7 +235,9 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.out_v8 = aligned(out, 32);
     p.num_ctas = s->pre_ctas;
     p.wait_limit_ns = wait_limit_ns;
+    t_mark(2, 0);
     cudaError_t e = bsr::launch_prefill(rotk, s->tm_q, rotk ? s->tm_rk : tk, tv, p, s->pre_ctas, stream);
+    t_mark(2, 1);
     if (e == cudaSuccess && s->n_pmerge > 0) {
       bsr::PrefillMergeParams m{};
       m.units = s->dev<const bsr::DecodeItem>(s->off_pmerge);
@@ -230,7 +249,9 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
       m.Hq = s->Hq;
       m.group = s->group;
       m.out_f32 = p.out_f32;
+      t_mark(3, 0);
       e = bsr::launch_prefill_merge(m, stream);
+      t_mark(3, 1);
     }
     if (e != cudaSuccess) {
       cudaGetLastError();
@@ -238,4 +259,48 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     }
   }
   return BSR_OK;
+}
+
+extern "C" int bsr_schedule_set_stage_timing(bsr_schedule_t s, int32_t max_calls) {
+  if (s == nullptr || max_calls < 0 || max_calls > (1 << 16)) return BSR_ERR_INVALID_ARGUMENT;
+  if (s->device >= 0 && cudaSetDevice(s->device) != cudaSuccess) return BSR_ERR_CUDA;
+  for (cudaEvent_t e : s->t_ev) cudaEventDestroy(e);
+  s->t_ev.clear();
+  s->t_ran.clear();
+  s->t_max = 0;
+  s->t_count = 0;
+  if (max_calls == 0) return BSR_OK;
+  const size_t n = size_t(max_calls) * bsr_schedule::kStages * 2;
+  s->t_ev.reserve(n);
+  for (size_t i = 0; i < n; ++i) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) {
+      cudaGetLastError();
+      for (cudaEvent_t x : s->t_ev) cudaEventDestroy(x);
+      s->t_ev.clear();
+      return BSR_ERR_CUDA;
+    }
+    s->t_ev.push_back(e);
+  }
+  s->t_ran.assign(size_t(max_calls) * bsr_schedule::kStages, 0);
+  s->t_max = max_calls;
+  return BSR_OK;
+}
+
+extern "C" int bsr_schedule_stage_times(bsr_schedule_t s, int32_t call, float* ms) {
+  if (s == nullptr || ms == nullptr || s->t_max == 0) return BSR_ERR_INVALID_ARGUMENT;
+  const int64_t kept = s->t_count < s->t_max ? s->t_count : s->t_max;
+  if (call < 0 || call >= kept) return BSR_ERR_INVALID_ARGUMENT;
+  const int slot = int((s->t_count - kept + call) % s->t_max);
+  for (int st = 0; st < bsr_schedule::kStages; ++st) {
+    ms[st] = -1.f;
+    if (!s->t_ran[size_t(slot) * bsr_schedule::kStages + st]) continue;
+    cudaEvent_t b = s->t_ev[(size_t(slot) * bsr_schedule::kStages + st) * 2];
+    cudaEvent_t e = s->t_ev[(size_t(slot) * bsr_schedule::kStages + st) * 2 + 1];
+    if (cudaEventSynchronize(e) != cudaSuccess || cudaEventElapsedTime(&ms[st], b, e) != cudaSuccess) {
+      cudaGetLastError();
+      return BSR_ERR_CUDA;
+    }
+  }
+  return int(kept);
 }

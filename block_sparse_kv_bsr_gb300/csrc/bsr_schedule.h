@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <vector>
 
 #include "bsr_internal.h"
 
@@ -62,6 +63,13 @@ struct bsr_schedule {
   CUtensorMap tm_v;
   const void* tm_k_ptr = nullptr;
   const void* tm_v_ptr = nullptr;
+
+  // optional per-stage timing of runs: events [run slot][stage][begin, end]
+  static constexpr int kStages = 4;   // decode, RoPE pre-pass, prefill, merge
+  std::vector<cudaEvent_t> t_ev;
+  std::vector<uint8_t> t_ran;         // [run slot][stage]
+  int32_t t_max = 0;
+  int64_t t_count = 0;
 
   template <typename T>
   T* dev(size_t off) const { return reinterpret_cast<T*>(d_ws + off); }

@@ -176,9 +176,30 @@ typedef struct bsr_schedule_info {
   int64_t upload_bytes;       /* bytes of the one host-to-device copy a plan makes */
   double decode_imbalance;    /* max / mean planned cost over decode warps */
   double prefill_imbalance;   /* max / mean planned cost over prefill CTAs */
+  int32_t kernels_per_run;    /* kernels one bsr_attn_run launches (decode, RoPE pre-pass,
+                                 prefill, split-range merge; 0 when there is no work) */
+  int32_t reserved;
 } bsr_schedule_info_t;
 
 int bsr_schedule_get_info(bsr_schedule_t schedule, bsr_schedule_info_t* info);
+
+/*
+ * Optional per-stage timing of bsr_attn_run (a measurement hook; the pages
+ * have no counterpart).  Off by default.
+ *
+ * bsr_schedule_set_stage_timing: with max_calls > 0 every later run records
+ * CUDA events on its stream around each kernel it launches -- stage 0 decode,
+ * 1 RoPE pre-pass, 2 prefill, 3 split-range merge -- and the schedule keeps
+ * the last max_calls runs; 0 turns timing off and frees the events.  Returns
+ * BSR_OK or a negative BSR_ERR_* code.
+ *
+ * bsr_schedule_stage_times: waits for the events of kept run `call` (0 = the
+ * oldest kept) and writes its four stage durations in milliseconds to ms[4]
+ * (-1 for a stage that did not run).  Returns the number of runs kept, or a
+ * negative BSR_ERR_* code (BSR_ERR_INVALID_ARGUMENT for a call not kept).
+ */
+int bsr_schedule_set_stage_timing(bsr_schedule_t schedule, int32_t max_calls);
+int bsr_schedule_stage_times(bsr_schedule_t schedule, int32_t call, float* ms);
 
 /*
  * bsr_attn_plan_host — the host half of bsr_attn_plan, for a given SM count,

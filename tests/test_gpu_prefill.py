@@ -136,3 +136,25 @@ def test_prefill_group_not_dividing_the_tile_takes_decode():
     info = s.info()
     assert info["num_prefill_items"] == 0 and info["num_decode_items"] > 0
     check_full(w, out, lse)
+
+
+def test_stage_timing_hook():
+    """Per-stage events of bsr_attn_run: RoPE pre-pass, prefill and (with split ranges)
+    merge are timed for the kept runs; a run that was not kept is refused."""
+    w = wl.make_paged("pftime", 57, [20000], Hq=32, Hk=8, D=128, P=16, qo_lens=[64],
+                      causal=True, rope_theta=1e4)
+    q, k, v = device_tensors(w)
+    s = plan(w)
+    info = s.info()
+    assert info["kernels_per_run"] == 3 and info["num_split_streams"] > 0
+    bsr.bsr_schedule_set_stage_timing(s, 2)
+    for _ in range(3):
+        bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta, causal=True)
+    for call in range(2):
+        t = bsr.bsr_schedule_stage_times(s, call)
+        assert set(t) == {"rope_prepass", "prefill", "merge"} and all(x > 0 for x in t.values())
+    with pytest.raises(bsr.BsrError):
+        bsr.bsr_schedule_stage_times(s, 2)
+    bsr.bsr_schedule_set_stage_timing(s, 0)
+    with pytest.raises(bsr.BsrError):
+        bsr.bsr_schedule_stage_times(s, 0)
