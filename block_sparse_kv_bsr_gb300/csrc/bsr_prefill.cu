@@ -52,21 +52,25 @@ constexpr int kUnitRows = kPrefillRows;     // two query tiles
 constexpr int kTileN = kPrefillKeyTile;     // keys per key tile
 constexpr int kHalfBytes = kTileN * 128;    // one 64-column block of a 128-row tile: 16 KB
 constexpr int kTileBytes = 2 * kHalfBytes;
-constexpr int kStages = 5;                  // K/V ring depth (32 KB stages)
+constexpr int kStages = 4;                  // K/V ring depth (32 KB stages)
 constexpr uint32_t kTmemCols = 512;
-constexpr int kThreads = 320;
-constexpr int kProducerWarp = 8, kMmaWarp = 9;
+constexpr int kSoftmaxWarps = 16;           // two per row quarter and query tile
+constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
+constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
 static_assert(kUnitRows == 2 * kTileM, "a unit is two query tiles");
 
 struct Smem {
   static constexpr int kQ = 0;                               // Q_0, Q_1
   static constexpr int kRing = 2 * kTileBytes;
-  static constexpr int kBars = kRing + kStages * kTileBytes;
-  // full[kStages], empty[kStages], s_full[2], p_full[2], o_full[2], q_full[2], q_empty[2], drain
+  // row-half exchange: [parity][query tile][half][row] fp32
+  static constexpr int kXchData = kRing + kStages * kTileBytes;
+  static constexpr int kBars = kXchData + 2 * 2 * 2 * kTileM * 4;
+  // full[kStages], empty[kStages], s_full[2], p_full[2], o_full[2], q_full[2], q_empty[2],
+  // drain, xch[2][4] (query tile, row quarter)
   static constexpr int kFull = 0, kEmpty = kStages, kSFull = 2 * kStages, kPFull = kSFull + 2,
                        kOFull = kPFull + 2, kQFull = kOFull + 2, kQEmpty = kQFull + 2,
-                       kDrain = kQEmpty + 2;
-  static constexpr int kNumBars = kDrain + 1;
+                       kDrain = kQEmpty + 2, kXch = kDrain + 1;
+  static constexpr int kNumBars = kXch + 8;
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kFlags = kTmemSlot + 16;   // abort flag
   static constexpr int kTotal = kFlags + 16;
@@ -185,12 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       ptx::mbar_init(BAR(L::kSFull + i), 1);
-      ptx::mbar_init(BAR(L::kPFull + i), kTileM);
+      ptx::mbar_init(BAR(L::kPFull + i), kSoftmaxWarps / 2);   // one arrival per warp of the tile
       ptx::mbar_init(BAR(L::kOFull + i), 1);
       ptx::mbar_init(BAR(L::kQFull + i), 1);
       ptx::mbar_init(BAR(L::kQEmpty + i), 1);
     }
     ptx::mbar_init(BAR(L::kDrain), 1);
+    for (int i = 0; i < 8; ++i) ptx::mbar_init(BAR(L::kXch + i), 2);   // the two halves of a row quarter
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(abort_addr), "r"(0u));
     ptx::fence_barrier_init();
   }
@@ -315,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kTileN / 16; ++k)
           if (k < nk16)
-            umma::mma_f16_ts(O_T(i), S_T(i) + 8u * uint32_t(k), vd + uint64_t((k * 2048) >> 4),
+            umma::mma_f16_ts(O_T(i), S_T(i) + 8u * uint32_t(k) + (k >= 4 ? 32u : 0u), vd + uint64_t((k * 2048) >> 4),
                              idesc_pv, (acc || k > 0) ? 1u : 0u);
       };
       auto wait_p = [&](int i) {
@@ -389,15 +394,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_wait_bounded(BAR(L::kDrain), 0, 50000000ull);
     }
   } else {
-    // ------------------------------------------------------------ softmax warpgroups
-    const int qt = warp >> 2;              // query tile of this warpgroup
-    const int t = tid & (kTileM - 1);      // row within the tile == TMEM lane
-    const uint32_t lane_off = uint32_t((warp & 3) * 32) << 16;
-    const uint32_t s_t = S_T(qt) + lane_off, o_t = O_T(qt) + lane_off;
+    // ------------------------------------------------------------ softmax warps
+    // Two threads per row: warp w works on query tile w / 8, key/column half
+    // (w / 4) % 2 and row quarter w % 4 (the TMEM lanes it may access); thread t of
+    // the quarter owns row t.  The halves of a row exchange their partial max (and
+    // at the end their partial sum) through shared memory and an mbarrier.
+    const int qt = warp >> 3;
+    const int half = (warp >> 2) & 1;
+    const int quad = warp & 3;
+    const int t = quad * 32 + lane;        // row within the tile == TMEM lane
+    const uint32_t lane_off = uint32_t(quad * 32) << 16;
+    // this half's 64 S columns (keys 64 half ..), later its 32 columns of P; its O columns
+    const uint32_t s_t = S_T(qt) + lane_off + 64u * half, o_t = O_T(qt) + lane_off + 64u * half;
+    const uint32_t xbar = BAR(L::kXch + qt * 4 + quad);
+    auto xslot = [&](uint32_t par, int h) {
+      return base + L::kXchData + uint32_t((((par * 2 + qt) * 2 + h) * kTileM + t) * 4);
+    };
     const float sl2 = ROPE ? p.scale_log2 * (1.f / (kRopeOperandScale * kRopeOperandScale))
                            : p.scale_log2;
-    uint32_t ns = 0, no = 0;
+    uint32_t ns = 0, no = 0, nx = 0;
     bool ok = true;
+    // Swap a value with the other half of the row; false when this CTA is aborting.
+    auto exchange = [&](float mine, float& other) -> bool {
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(xslot(nx & 1u, half)), "f"(mine) : "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xbar);
+      if (!wt.warp_wait(xbar, nx & 1u)) return false;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(other) : "r"(xslot(nx & 1u, half ^ 1)) : "memory");
+      ++nx;
+      return true;
+    };
     for (int u = u_begin; u < u_end && ok; ++u) {
       const DecodeItem it = p.items[u];
       const int nt = ntiles_of(it);
@@ -408,35 +434,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int R = it.row0 + prow;
       const bool vrow = t < rows_here;
       const int qpos = it.qpos0 + R / group;
-      float m_used = -INFINITY, l = 0.f;
+      float m_used = -INFINITY, l = 0.f;   // l: this half's partial sum
       if (nt > 0) {
         for (int j = 0; j < nt; ++j) {
-          const int key0 = it.tok0 + kTileN * j;
-          const int nkeys = min(kTileN, it.tok1 - key0);
+          const int key0 = it.tok0 + kTileN * j + 64 * half;
+          const int nkeys = min(64, it.tok1 - key0);                          // may be <= 0
           const int klim = p.causal ? min(nkeys, qpos - key0 + 1) : nkeys;   // keys [0, klim) visible
 
-          // ---- S row t, online softmax (log2 domain, lazy rescale).  Two passes over
-          // the row in 64-column halves (max, then exp2 / pack / store of P) keep
-          // the live registers low; TMEM reads are cheap.
+          // ---- online softmax (log2 domain, lazy rescale) over this half's 64 scores,
+          // read in 32-column quarters: max pass, exchange, exp2 / pack / store pass
           if (!wt.warp_wait(BAR(L::kSFull + qt), ns & 1u)) { ok = false; break; }
           ++ns;
           umma::fence_after_sync();
-          const bool masked = __any_sync(0xffffffffu, klim < kTileN);
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float sv[64];
-            umma::tmem_ld64(s_t + 64 * h, sv);
+          const bool masked = __any_sync(0xffffffffu, klim < 64);
+          auto load_quarter = [&](int qq, float (&sv)[32]) {
+            umma::tmem_ld32(s_t + 32 * qq, sv);
             if (masked) {
 #pragma unroll
-              for (int i = 0; i < 64; ++i) sv[i] = 64 * h + i < klim ? sv[i] : -INFINITY;
+              for (int i = 0; i < 32; ++i) sv[i] = 32 * qq + i < klim ? sv[i] : -INFINITY;
             }
+          };
+          float mpart = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 64; i += 8)
+          for (int qq = 0; qq < 2; ++qq) {
+            float sv[32];
+            load_quarter(qq, sv);
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int i = 0; i < 32; i += 8)
 #pragma unroll
               for (int k = 0; k < 4; ++k) m4[k] = ptx::fmax3(m4[k], sv[i + 2 * k], sv[i + 2 * k + 1]);
+            mpart = ptx::fmax3(mpart, ptx::fmax3(m4[0], m4[1], m4[2]), m4[3]);
           }
-          float mx = ptx::fmax3(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+          float mother;
+          if (!exchange(mpart, mother)) { ok = false; break; }
+          float mx = fmaxf(mpart, mother);
           mx = mx == -INFINITY ? mx : mx * sl2;
           float alpha = 1.f;
           if (mx > m_used + 8.f) {          // also true the first time a row sees a key
@@ -447,59 +479,60 @@ __global__ void __launch_bounds__(kThreads, 1)
           // O_i is stable here: this S was committed after the previous P V
           if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
+            for (int c2 = 0; c2 < 2; ++c2) {
               float v[32];
-              umma::tmem_ld32(o_t + 32 * c4, v);
+              umma::tmem_ld32(o_t + 32 * c2, v);
 #pragma unroll
               for (int i = 0; i < 32; ++i) v[i] *= alpha;
-              umma::tmem_st32(o_t + 32 * c4, v);
+              umma::tmem_st32(o_t + 32 * c2, v);
             }
           }
           const float2 sc2 = make_float2(sl2, sl2), nmu2 = make_float2(-mu, -mu);
           float2 rs2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                            make_float2(0.f, 0.f)};
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            float sv[64];
-            umma::tmem_ld64(s_t + 64 * h, sv);
-            if (masked) {
+          for (int qq = 0; qq < 2; ++qq) {
+            float sv[32];
+            load_quarter(qq, sv);
+            uint32_t pk[16];
 #pragma unroll
-              for (int i = 0; i < 64; ++i) sv[i] = 64 * h + i < klim ? sv[i] : -INFINITY;
-            }
-            uint32_t pk[32];
-#pragma unroll
-            for (int i = 0; i < 64; i += 2) {
+            for (int i = 0; i < 32; i += 2) {
               const float2 x = ptx::ffma2(make_float2(sv[i], sv[i + 1]), sc2, nmu2);
               const float2 e = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
               rs2[(i >> 1) & 3] = ptx::fadd2(rs2[(i >> 1) & 3], e);
               pk[i / 2] = ptx::pack_bf16(e.x, e.y);
             }
-            // P (bf16 pairs) over the S columns already read
-            umma::tmem_st32u(s_t + 32 * h, pk);
+            // P (bf16 pairs) over this half's S columns already read
+            umma::tmem_st16u(s_t + 16 * qq, pk);
           }
           const float2 r01 = ptx::fadd2(rs2[0], rs2[1]), r23 = ptx::fadd2(rs2[2], rs2[3]);
           const float2 r = ptx::fadd2(r01, r23);
           l = l * alpha + (r.x + r.y);
           umma::fence_before_sync();
-          mbar_arrive(BAR(L::kPFull + qt));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(L::kPFull + qt));
         }
         if (!ok) break;
         if (!wt.warp_wait(BAR(L::kOFull + qt), no & 1u)) { ok = false; break; }
         ++no;
         umma::fence_after_sync();
+        float lother;
+        if (!exchange(l, lother)) { ok = false; break; }
+        l += lother;
       }
-      // ---- epilogue: O row t / l (an empty unit writes 0 / -inf), 32 columns at a time;
-      // a split range writes its fp32 partial state instead
+      // ---- epilogue: this half's 64 columns of O row t / l (an empty unit writes 0 /
+      // -inf); a split range writes its fp32 partial state instead
       const size_t orow = out_row(it, R, group, p.Hq);
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse2 = l > 0.f ? m_used + ptx::lg2(l) : -INFINITY;
       constexpr float kLn2 = 0.69314718055994530942f;
       float* part_row = p.part_o + (size_t(it.slot < 0 ? 0 : it.slot) * kUnitRows + prow) * D;
 #pragma unroll 1
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int c2 = 0; c2 < 2; ++c2) {
+        const int c4 = 2 * half + c2;      // 32-column chunk of the row
         float v[32];
         if (nt > 0) {
-          umma::tmem_ld32(o_t + 32 * c4, v);
+          umma::tmem_ld32(o_t + 32 * c2, v);
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= inv;
         } else {
@@ -519,10 +552,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       umma::fence_before_sync();
-      if (it.slot < 0) {
-        if (vrow && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
-      } else {
-        p.part_lse[size_t(it.slot) * kUnitRows + prow] = lse2;
+      if (half == 0) {
+        if (it.slot < 0) {
+          if (vrow && p.lse != nullptr) p.lse[orow] = lse2 * kLn2;
+        } else {
+          p.part_lse[size_t(it.slot) * kUnitRows + prow] = lse2;
+        }
       }
     }
   }
