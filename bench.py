@@ -205,6 +205,7 @@ class Part:
         self.family, self.profile = family, profile
         self.ms = []          # whole call
         self.kernel_ms = []   # the stage's kernel alone
+        self.stage_ms = {}    # every kernel the call launched, by stage
 
 
 def attention_flops(w) -> int:
@@ -414,6 +415,8 @@ def main():
                 t = bsr.bsr_schedule_stage_times(pt.sched, call)
                 if pt.stage in t:
                     pt.kernel_ms.append(t[pt.stage])
+                for name, ms in t.items():
+                    pt.stage_ms.setdefault(name, []).append(ms)
             bsr.bsr_schedule_set_stage_timing(pt.sched, 0)
     ms_step = total_ms / args.steps
     if world > 1:
@@ -483,8 +486,8 @@ def main():
                                   else "CUDA events around the call") + ", second timed pass of K steps",
                      "call_us_mean": round(call_ms * 1e3, 2)},
         "parts_us": {pt.label: round(sum(pt.ms) / len(pt.ms) * 1e3, 2) for pt in parts},
-        "kernels_us": {f"{pt.label}.{pt.stage}": round(sum(pt.kernel_ms) / len(pt.kernel_ms) * 1e3, 2)
-                       for pt in parts if pt.kernel_ms},
+        "kernels_us": {f"{pt.label}.{name}": round(sum(v) / len(v) * 1e3, 2)
+                       for pt in parts for name, v in pt.stage_ms.items()},
         "gpu_launches": args.steps * sum(pt.launches for pt in parts),
         "gpu_launches_note": "kernels launched in the whole-job timed region (region 1)",
         "clocks": clocks.summary(),

@@ -575,6 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // One warp per packed row of a split unit: lane l owns columns 4l .. 4l + 3.
 // The partial states (fp32, log2-domain lse) are combined in key order:
 //   lse = M + log2(sum_k 2^(lse_k - M)),  o = sum_k 2^(lse_k - lse) o_k.
+// Lane k holds lse_k (chunks in groups of 32); the partial rows of up to eight
+// chunks are loaded before the weights are known, so the loads overlap.
 constexpr int kMergeWarps = 8;
 __global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(const PrefillMergeParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -586,6 +588,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(con
   if (prow >= it.nrows) return;
   const int n = it.nchunks;
   const float* lse_k = p.part_lse + size_t(it.first_slot) * kUnitRows + prow;
+  const float* po = p.part_o + (size_t(it.first_slot) * kUnitRows + prow) * D + 4 * lane;
+  constexpr size_t kSlotStride = size_t(kUnitRows) * D;
+  // the first chunks' partial rows, before anything depends on the lse values
+  float4 x[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    x[u] = u < n ? __ldcg(reinterpret_cast<const float4*>(po + size_t(u) * kSlotStride))
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
   float M = -INFINITY;
   for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldcg(lse_k + size_t(k) * kUnitRows));
 #pragma unroll
@@ -598,26 +608,23 @@ __global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(con
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     lt = M + ptx::lg2(sum);
-    const float* po = p.part_o + (size_t(it.first_slot) * kUnitRows + prow) * D + 4 * lane;
-    constexpr size_t kSlotStride = size_t(kUnitRows) * D;
     for (int kb = 0; kb < n; kb += 32) {
       const int m = min(32, n - kb);
       const float wl = lane < m ? ptx::ex2(__ldcg(lse_k + size_t(kb + lane) * kUnitRows) - lt) : 0.f;
-      int j = 0;
-      for (; j + 8 <= m; j += 8) {
-        float4 x[8];
+      for (int j = 0; j < m; j += 8) {
+        if (kb + j >= 8) {   // chunks past the first eight: load this group now
 #pragma unroll
-        for (int u = 0; u < 8; ++u) x[u] = __ldcg(reinterpret_cast<const float4*>(po + size_t(kb + j + u) * kSlotStride));
+          for (int u = 0; u < 8; ++u)
+            x[u] = j + u < m ? __ldcg(reinterpret_cast<const float4*>(po + size_t(kb + j + u) * kSlotStride))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float w = __shfl_sync(0xffffffffu, wl, j + u);
-          acc.x += w * x[u].x; acc.y += w * x[u].y; acc.z += w * x[u].z; acc.w += w * x[u].w;
+          const float w = __shfl_sync(0xffffffffu, wl, (j + u) & 31);
+          if (j + u < m) {
+            acc.x += w * x[u].x; acc.y += w * x[u].y; acc.z += w * x[u].z; acc.w += w * x[u].w;
+          }
         }
-      }
-      for (; j < m; ++j) {
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(po + size_t(kb + j) * kSlotStride));
-        const float w = __shfl_sync(0xffffffffu, wl, j);
-        acc.x += w * x.x; acc.y += w * x.y; acc.z += w * x.z; acc.w += w * x.w;
       }
     }
   }
@@ -632,21 +639,34 @@ __global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(con
 }
 
 // ---------------------------------------------------------------- RoPE pre-pass
-// Rotate the pair of 16-byte chunks (d, d + 64) of one row at its position and
-// store it as fp16 scaled by 2^-4 (the operand type of the RoPE prefill's
-// Q K^T); returns true when a value does not fit.
+// The cos/sin of frequencies 8c .. 8c + 7 at one position (as four float4, two
+// (cos, sin) pairs each).
+struct RopeChunk {
+  float4 cs[4];
+};
+
+__device__ __forceinline__ RopeChunk rope_chunk(const float2* rope_row, int c) {
+  const float4* tab = reinterpret_cast<const float4*>(rope_row);
+  RopeChunk r;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) r.cs[e] = __ldg(tab + 4 * c + e);
+  return r;
+}
+
+// Rotate the pair of 16-byte chunks (c, c + 8) of one row -- dimensions 8c .. 8c + 7
+// and their partners 64 further -- and store it as fp16 scaled by 2^-4 (the operand
+// type of the RoPE prefill's Q K^T); returns true when a value does not fit.
 __device__ __forceinline__ bool rotate_chunk(const uint16_t* src, uint16_t* dst, int c,
-                                             const float2* rope_row) {
+                                             const RopeChunk& t) {
   const uint4 av = __ldg(reinterpret_cast<const uint4*>(src) + c);
   const uint4 bv = __ldg(reinterpret_cast<const uint4*>(src) + 8 + c);
-  const float4* tab = reinterpret_cast<const float4*>(rope_row);
   const uint32_t* a = reinterpret_cast<const uint32_t*>(&av);
   const uint32_t* b = reinterpret_cast<const uint32_t*>(&bv);
   uint32_t xo[4], yo[4];
   bool bad = false;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float4 cs = __ldg(tab + 4 * c + e);   // frequencies 8c + 2e, 8c + 2e + 1
+    const float4 cs = t.cs[e];   // frequencies 8c + 2e, 8c + 2e + 1
     const float a0 = ptx::bf16_lo(a[e]), a1 = ptx::bf16_hi(a[e]);
     const float b0 = ptx::bf16_lo(b[e]), b1 = ptx::bf16_hi(b[e]);
     const float x0 = (a0 * cs.x - b0 * cs.y) * kRopeOperandScale;
@@ -672,37 +692,44 @@ __device__ __forceinline__ int find_request(const int32_t* start, int n, int r) 
   return lo;
 }
 
-// One thread per (row, 16-byte chunk of the first half): first every key of
-// the prefill requests (per kv head, at its position in the request's page
-// list, into the dense rotated-K buffer), then every query row of those
-// requests (all heads, at its position, into the rotated copy of q).
-// Threads walk chunks, then rows, so reads and writes are contiguous.
+// A block of 256 threads rotates 32 rows; thread (row, c) handles the chunk pair
+// (c, c + 8) of its row for every head.  The first blocks take the keys of the
+// prefill requests (each key row at its position in the request's page list,
+// for every kv head, into the dense rotated-K buffer), the rest their query rows
+// (every qo head, into the rotated copy of q).  The request, page id and cos/sin
+// of a row are looked up once and reused for all its heads, which keeps the
+// heads' loads independent (many in flight per thread).
+constexpr int kRopeRowsPerBlock = 32;
 __global__ void __launch_bounds__(256) rope_prepass_kernel(const RopePrepassParams p) {
-  const int64_t nk = int64_t(p.Hk) * p.rk_total * 8;
-  const int64_t total = nk + int64_t(p.rq_total) * p.Hq * 8;
+  const int c = threadIdx.x & 7;
+  const int rl = threadIdx.x >> 3;
+  const int nkb = (p.rk_total + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock;
   bool bad = false;
-  for (int64_t g = int64_t(blockIdx.x) * 256 + threadIdx.x; g < total; g += int64_t(gridDim.x) * 256) {
-    const int c = int(g & 7);
-    if (g < nk) {
-      const int64_t hr = g >> 3;
-      const int kvh = int(hr / p.rk_total);
-      const int r = int(hr % p.rk_total);
+  if (int(blockIdx.x) < nkb) {
+    const int r = int(blockIdx.x) * kRopeRowsPerBlock + rl;
+    if (r < p.rk_total) {
       const int i = find_request(p.rk_start, p.n, r);
       const int j = r - __ldg(p.rk_start + i);
       const int page = __ldg(p.indices + __ldg(p.rk_req_pbase + i) + j / p.P);
-      const uint16_t* src = p.k_pages + ((size_t(page) * p.Hk + kvh) * p.P + (j % p.P)) * D;
-      bad |= rotate_chunk(src, p.rotk + (size_t(kvh) * p.rk_total + r) * D, c,
-                          p.rope_nat + size_t(min(j, p.rope_max_pos)) * (D / 2));
-    } else {
-      const int64_t rh = (g - nk) >> 3;
-      const int head = int(rh % p.Hq);
-      const int r = int(rh / p.Hq);
+      const RopeChunk t = rope_chunk(p.rope_nat + size_t(min(j, p.rope_max_pos)) * (D / 2), c);
+      const size_t head_stride = size_t(p.P) * D;
+      const uint16_t* src = p.k_pages + (size_t(page) * p.Hk * p.P + (j % p.P)) * D;
+      uint16_t* dst = p.rotk + size_t(r) * D;
+#pragma unroll 4
+      for (int kvh = 0; kvh < p.Hk; ++kvh)
+        bad |= rotate_chunk(src + kvh * head_stride, dst + size_t(kvh) * p.rk_total * D, c, t);
+    }
+  } else {
+    const int r = (int(blockIdx.x) - nkb) * kRopeRowsPerBlock + rl;
+    if (r < p.rq_total) {
       const int i = find_request(p.rq_start, p.n, r);
       const int j = r - __ldg(p.rq_start + i);
-      const size_t row = size_t(__ldg(p.rq_row0 + i) + j) * p.Hq + head;
+      const size_t row0 = size_t(__ldg(p.rq_row0 + i) + j) * p.Hq;
       const int pos = __ldg(p.rq_pos0 + i) + j;
-      bad |= rotate_chunk(p.q + row * D, p.rotq + row * D, c,
-                          p.rope_nat + size_t(min(pos, p.rope_max_pos)) * (D / 2));
+      const RopeChunk t = rope_chunk(p.rope_nat + size_t(min(pos, p.rope_max_pos)) * (D / 2), c);
+#pragma unroll 4
+      for (int h = 0; h < p.Hq; ++h)
+        bad |= rotate_chunk(p.q + (row0 + h) * D, p.rotq + (row0 + h) * D, c, t);
     }
   }
   if (bad) atomicOr(p.error, kStatusRopeRange);
@@ -730,10 +757,11 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 }  // namespace
 
 cudaError_t launch_rope_prepass(const RopePrepassParams& p, int num_sms, cudaStream_t stream) {
-  const int64_t work = (int64_t(p.Hk) * p.rk_total + int64_t(p.rq_total) * p.Hq) * 8;
-  int64_t grid = (work + 255) / 256;
-  if (grid > int64_t(num_sms) * 8) grid = int64_t(num_sms) * 8;
-  if (grid < 1) grid = 1;
+  (void)num_sms;
+  const int64_t grid = (int64_t(p.rk_total) + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock +
+                       (int64_t(p.rq_total) + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock;
+  if (grid <= 0) return cudaSuccess;
+  if (grid > INT32_MAX) return cudaErrorInvalidValue;
   rope_prepass_kernel<<<int(grid), 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
