@@ -60,6 +60,16 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (the slowest replica sets the job's time)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def tensor_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -418,11 +428,7 @@ def main():
                 for name, ms in t.items():
                     pt.stage_ms.setdefault(name, []).append(ms)
             bsr.bsr_schedule_set_stage_timing(pt.sched, 0)
-    ms_step = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(total_ms / args.steps, world, dev)
     for s in job["schedules"]:
         assert bsr.bsr_last_device_error(s) == 0
 
