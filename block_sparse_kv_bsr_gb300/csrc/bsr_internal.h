@@ -99,6 +99,7 @@ struct PrefillParams {
   float scale_log2;
   int32_t Hq, Hk, group, P;
   int32_t causal, out_f32, out_v8, num_ctas;
+  int32_t box_rows;               // rows per K/V box of the prefill tensor maps: min(P, 128)
   uint64_t wait_limit_ns;
 };
 

@@ -548,6 +548,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->off_rotq = off_rotq;
   s->rq_total = rotk ? hp.rq_total : 0;
   s->tm_q_ptr = nullptr;    // Q tensor map: encoded by run
+  s->tm_pk_ptr = s->tm_pv_ptr = nullptr;   // prefill K/V maps depend on the page size
   s->rk_n = rotk ? int32_t(hp.rk_pbase.size()) : 0;
   s->rk_total = rotk ? hp.rk_total : 0;
   s->tm_rk_valid = false;   // encoded by run (the buffer's address may have moved)

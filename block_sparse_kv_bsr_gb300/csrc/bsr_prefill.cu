@@ -237,13 +237,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const DecodeItem it = p.items[u];
         const int nt = ntiles_of(it);
         const int koff = ROPE ? __ldg(p.rk_off + it.req) : 0;
+        // K/V come in boxes of R = min(P, 128) rows: one page holds a whole box, and a key
+        // tile (its start a multiple of max(P, 128)) is 128 / R boxes
+        const int R = p.box_rows;
         for (int j = 0; j < nt; ++j) {
           const int key0 = it.tok0 + kTileN * j;
-          const int nsub = (min(kTileN, it.tok1 - key0) + 15) >> 4;
+          const int nsub = (min(kTileN, it.tok1 - key0) + R - 1) / R;
           int pages[kTileN / 16];   // all page ids of the tile first (independent loads)
 #pragma unroll
           for (int sb = 0; sb < kTileN / 16; ++sb)
-            pages[sb] = sb < nsub ? __ldg(p.indices + it.page_base + (key0 + 16 * sb) / p.P) : 0;
+            pages[sb] = sb < nsub ? __ldg(p.indices + it.page_base + (key0 + R * sb) / p.P) : 0;
+          const uint32_t box_bytes = uint32_t(R) * 128u;
           // K(j)
           if (c >= kStages && !wt.wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
           if (ROPE) {
@@ -253,13 +257,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < 2; ++h)
               ptx::tma_load_3d(STAGE(c) + h * kHalfBytes, &tm_k, FULL(c), 0, h, row, pol);
           } else {
-            ptx::mbar_arrive_expect_tx(FULL(c), uint32_t(nsub) * 2u * 2048u);
+            ptx::mbar_arrive_expect_tx(FULL(c), uint32_t(nsub) * 2u * box_bytes);
 #pragma unroll
             for (int sb = 0; sb < kTileN / 16; ++sb) {
               if (sb >= nsub) break;
-              const int row = (pages[sb] * p.Hk + it.kvh) * p.P + ((key0 + 16 * sb) % p.P);
+              const int row = (pages[sb] * p.Hk + it.kvh) * p.P + ((key0 + R * sb) % p.P);
               for (int h = 0; h < 2; ++h)
-                ptx::tma_load_3d(STAGE(c) + h * kHalfBytes + sb * 2048, &tm_k, FULL(c), 0, h, row, pol);
+                ptx::tma_load_3d(STAGE(c) + h * kHalfBytes + sb * box_bytes, &tm_k, FULL(c), 0, h, row, pol);
             }
           }
           ++c;
@@ -268,13 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // V(j)
           if (c >= kStages && !wt.wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(FULL(c), uint32_t(nsub) * 2u * 2048u);
+          ptx::mbar_arrive_expect_tx(FULL(c), uint32_t(nsub) * 2u * box_bytes);
 #pragma unroll
           for (int sb = 0; sb < kTileN / 16; ++sb) {
             if (sb >= nsub) break;
-            const int row = (pages[sb] * p.Hk + it.kvh) * p.P + ((key0 + 16 * sb) % p.P);
+            const int row = (pages[sb] * p.Hk + it.kvh) * p.P + ((key0 + R * sb) % p.P);
             for (int h = 0; h < 2; ++h)
-              ptx::tma_load_3d(STAGE(c) + h * kHalfBytes + sb * 2048, &tm_v, FULL(c), 0, h, row, pol);
+              ptx::tma_load_3d(STAGE(c) + h * kHalfBytes + sb * box_bytes, &tm_v, FULL(c), 0, h, row, pol);
           }
           ++c;
         }

@@ -214,7 +214,19 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
       }
       s->tm_q_ptr = qsrc;
     }
+    // K/V boxes of min(P, 128) rows (the prefill class has P >= 16)
+    const int box_rows = s->P < bsr::kPrefillKeyTile ? s->P : bsr::kPrefillKeyTile;
+    if (s->tm_pk_ptr != k_pages || s->tm_pv_ptr != v_pages) {
+      if (rows <= 0 || !encode_pool(&s->tm_pk, k_pages, rows, s->D, box_rows) ||
+          !encode_pool(&s->tm_pv, v_pages, rows, s->D, box_rows)) {
+        s->tm_pk_ptr = s->tm_pv_ptr = nullptr;
+        return BSR_ERR_CUDA;
+      }
+      s->tm_pk_ptr = k_pages;
+      s->tm_pv_ptr = v_pages;
+    }
     bsr::PrefillParams p{};
+    p.box_rows = box_rows;
     p.rk_off = rotk ? s->dev<const int32_t>(s->off_rk_off) : nullptr;
     p.rk_total = rotk ? s->rk_total : 0;
     p.items = s->dev<const bsr::DecodeItem>(s->off_pitems);
@@ -236,7 +248,8 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.num_ctas = s->pre_ctas;
     p.wait_limit_ns = wait_limit_ns;
     t_mark(2, 0);
-    cudaError_t e = bsr::launch_prefill(rotk, s->tm_q, rotk ? s->tm_rk : tk, tv, p, s->pre_ctas, stream);
+    cudaError_t e =
+        bsr::launch_prefill(rotk, s->tm_q, rotk ? s->tm_rk : s->tm_pk, s->tm_pv, p, s->pre_ctas, stream);
     t_mark(2, 1);
     if (e == cudaSuccess && s->n_pmerge > 0) {
       bsr::PrefillMergeParams m{};

@@ -43,6 +43,11 @@ struct bsr_schedule {
   int32_t rk_n = 0, rk_total = 0, rq_total = 0;
   CUtensorMap tm_rk;
   bool tm_rk_valid = false;
+  // prefill K/V tiles: boxes of min(P, 128) rows over the caller's pools
+  CUtensorMap tm_pk;
+  CUtensorMap tm_pv;
+  const void* tm_pk_ptr = nullptr;
+  const void* tm_pv_ptr = nullptr;
   // prefill query tiles: over q (no RoPE) or the rotated copy (RoPE)
   CUtensorMap tm_q;
   const void* tm_q_ptr = nullptr;
