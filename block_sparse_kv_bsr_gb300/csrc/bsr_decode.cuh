@@ -20,8 +20,11 @@
 //    of warp-level m16n8k16 bf16 MMAs: S = Q K^T for 16 keys, online softmax
 //    in registers (exp2 domain), O += P V with P split into bf16 hi + lo so
 //    the probabilities keep ~16 bits.  K is rotated on load when RoPE is on
-//    (section "JIT 컴파일은 …": RoPE fused into attention), with q and k also
-//    split hi + lo so the rotation costs no accuracy.
+//    (section "JIT 컴파일은 …": RoPE fused into attention); rotated q and k
+//    are fp16 operands scaled by 2^-4.  The angle of key p0 + t (p0 the
+//    stage's first key) is composed from the table row of p0, copied into
+//    the stage with its K and V, and the row of t < 16, kept in shared memory
+//    for the whole CTA, so no table load waits on L2 inside the stage.
 //  * A unit that covers all keys of its range writes out (bf16 / fp32) and the
 //    natural-log LSE; a split unit writes a normalized fp32 partial state and
 //    the last arriving unit of the range merges all partials in chunk order
@@ -49,10 +52,21 @@ struct DecodeCfg {
   static constexpr int kStages = (D == 128) ? BSR_DECODE_STAGES_D128 : BSR_DECODE_STAGES_D64;
   static constexpr int kKSteps = D / 16;
   static constexpr int kNTiles = D / 8;
-  static constexpr int kRopeK = D / 8;                           // (cos, sin) pairs per (pos, quad)
-  static constexpr size_t kSmemBytes =
-      size_t(kDecodeWarps) * kStages * kStageBytes + size_t(kDecodeWarps) * kStages * 8 + 1024;
-  static_assert(kSmemBytes <= 232448, "decode stages exceed the shared memory of one SM");
+  // cos/sin table: one position is D/2 (cos, sin) fp32 pairs = D/4 float4s,
+  // float4 (i, quad t) at i * 4 + t holding frequencies 16(i/2) + 8(i%2) + 2t + {0, 1}
+  static constexpr int kRopeRowF4 = D / 4;
+  static constexpr int kRopeRowBytes = 16 * kRopeRowF4;
+  // offset rows t < 16 in shared memory, padded so that rows t and t + 1 fall
+  // on different bank halves (conflict-free 16-byte loads)
+  static constexpr int kRopeOffStride = kRopeRowBytes + 64;
+  static constexpr size_t kRingBytes = size_t(kDecodeWarps) * kStages * kStageBytes;
+  static constexpr size_t kBarBytes = size_t(kDecodeWarps) * kStages * 8;
+  static constexpr size_t kSmemBytes = kRingBytes + kBarBytes + 1024;
+  static constexpr size_t kSmemBytesRope = kSmemBytes +
+                                           size_t(kDecodeWarps) * kStages * kRopeRowBytes +
+                                           size_t(kStageTokens) * kRopeOffStride;
+  static_assert(kBarBytes % 16 == 0, "stage-row copies need 16-byte aligned destinations");
+  static_assert(kSmemBytesRope <= 232448, "decode stages exceed the shared memory of one SM");
 };
 
 // Byte offset of (token t, column d) in a 16-token tile stored as
@@ -87,6 +101,12 @@ __device__ __forceinline__ void rope_pair(uint32_t xlo, uint32_t xhi, float2 cs0
   y[0] = b0 * cs0.x + a0 * cs0.y;
   x[1] = a1 * cs1.x - b1 * cs1.y;
   y[1] = b1 * cs1.x + a1 * cs1.y;
+}
+
+// (cos, sin) of a + b from those of a and b, for the two frequencies of a table float4.
+__device__ __forceinline__ float4 rot_compose(float4 a, float4 b) {
+  return make_float4(a.x * b.x - a.y * b.y, a.y * b.x + a.x * b.y,
+                     a.z * b.z - a.w * b.w, a.w * b.z + a.z * b.w);
 }
 
 // Merge the partial states of one split range (the last-arriving warp calls
@@ -199,15 +219,29 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   extern __shared__ uint8_t smem_raw[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - ptx::smem_u32(smem_raw));
+  const uint32_t ring = base + uint32_t(warp * C::kStages * C::kStageBytes);
+  const uint32_t bars = base + uint32_t(C::kRingBytes + warp * C::kStages * 8);
+  // RoPE: this warp's per-stage table rows, then the CTA's offset rows t < 16
+  const uint32_t grows =
+      base + uint32_t(C::kRingBytes + C::kBarBytes + warp * C::kStages * C::kRopeRowBytes);
+  uint8_t* const goff_ptr = base_ptr + (grows - base);
+  uint8_t* const frows_ptr =
+      base_ptr + C::kRingBytes + C::kBarBytes + size_t(kDecodeWarps) * C::kStages * C::kRopeRowBytes;
+  if constexpr (ROPE) {
+    const float4* src = reinterpret_cast<const float4*>(p.rope);
+    for (int i = threadIdx.x; i < kStageTokens * C::kRopeRowF4; i += kDecodeWarps * 32) {
+      const int t = i / C::kRopeRowF4, c = i % C::kRopeRowF4;
+      *reinterpret_cast<float4*>(frows_ptr + t * C::kRopeOffStride + 16 * c) = __ldg(src + i);
+    }
+    __syncthreads();
+  }
+
   const int gw = blockIdx.x * kDecodeWarps + warp;
   if (gw >= p.num_warps) return;
   const int it_begin = __ldg(p.warp_ptr + gw), it_end = __ldg(p.warp_ptr + gw + 1);
   if (it_begin >= it_end) return;
-
-  const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
-  const uint32_t ring = base + uint32_t(warp * C::kStages * C::kStageBytes);
-  const uint32_t bars =
-      base + uint32_t(kDecodeWarps * C::kStages * C::kStageBytes + warp * C::kStages * 8);
   if (!SMALLP) {
     if (lane == 0) {
 #pragma unroll
@@ -217,6 +251,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     __syncwarp();
   }
   const uint64_t pol = ptx::policy_evict_first();
+  const uint64_t pol_rope = ptx::policy_evict_normal();   // table rows are shared by all units
   const int g4 = lane >> 2, t4 = lane & 3;
   const int log2P = 31 - __clz(p.P);
 
@@ -255,7 +290,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       const uint32_t dk = ring + uint32_t(slot * C::kStageBytes), dv = dk + C::kStageKBytes;
       const int tok = pi.tok0 + kStageTokens * p_st;
       const int row = (page * p.Hk + pi.kvh) * p.P + (tok & (p.P - 1));
-      ptx::mbar_arrive_expect_tx(bar, C::kStageBytes);
+      ptx::mbar_arrive_expect_tx(bar, C::kStageBytes + (ROPE ? C::kRopeRowBytes : 0));
+      if constexpr (ROPE)
+        ptx::bulk_load(grows + slot * C::kRopeRowBytes,
+                       reinterpret_cast<const float4*>(p.rope) + size_t(tok) * C::kRopeRowF4,
+                       C::kRopeRowBytes, bar, pol_rope);
       if constexpr (D == 128) {
 #pragma unroll
         for (int h = 0; h < C::kHalves; ++h) {
@@ -340,11 +379,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
           const bool ok = rr == 0 ? vA : vB;
           const int tpos = ok ? min(max(pos, 0), p.rope_max_pos) : 0;
           const float4* tab =
-              reinterpret_cast<const float4*>(p.rope + (size_t(tpos) * 4 + t4) * C::kRopeK);
+              reinterpret_cast<const float4*>(p.rope) + size_t(tpos) * C::kRopeRowF4 + t4;
           const int r0 = rr == 0 ? 0 : 1, r1 = rr == 0 ? NR / 2 : 3;
 #pragma unroll
           for (int ks = 0; ks < KH; ++ks) {
-            const float4 c01 = __ldg(tab + 2 * ks), c23 = __ldg(tab + 2 * ks + 1);
+            const float4 c01 = __ldg(tab + 8 * ks), c23 = __ldg(tab + 8 * ks + 4);
             float x[2], y[2];
             rope_pair(raw[ks][r0], raw[ks + KH][r0], make_float2(c01.x, c01.y),
                       make_float2(c01.z, c01.w), x, y);
@@ -392,6 +431,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                        "r"(vv.y), "r"(vv.z), "r"(vv.w)
                        : "memory");
         }
+        if constexpr (ROPE) {
+          if (lane < C::kRopeRowF4)
+            reinterpret_cast<float4*>(goff_ptr)[lane] =
+                __ldg(reinterpret_cast<const float4*>(p.rope) + size_t(tok) * C::kRopeRowF4 + lane);
+        }
       } else {
         if (!ptx::mbar_wait_bounded(bars + 8 * slot, (c_seq / C::kStages) & 1u, p.wait_limit_ns)) {
           failed = true;
@@ -435,21 +479,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
           s1[r] += u1[r];
         }
       } else {
-        const int posA = min(tok + g4, p.rope_max_pos), posB = min(tok + 8 + g4, p.rope_max_pos);
-        const float4* tabA =
-            reinterpret_cast<const float4*>(p.rope + (size_t(posA) * 4 + t4) * C::kRopeK);
-        const float4* tabB =
-            reinterpret_cast<const float4*>(p.rope + (size_t(posB) * 4 + t4) * C::kRopeK);
+        // angle of key tok + t = angle of tok (this stage's table row) + angle of t
+        const float4* g = reinterpret_cast<const float4*>(goff_ptr + slot * C::kRopeRowBytes) + t4;
+        const float4* fa = reinterpret_cast<const float4*>(frows_ptr + g4 * C::kRopeOffStride) + t4;
+        const float4* fb =
+            reinterpret_cast<const float4*>(frows_ptr + (g4 + 8) * C::kRopeOffStride) + t4;
 #pragma unroll
         for (int ks = 0; ks < KH; ++ks) {
           uint32_t kl[4], kh[4];
           ptx::ldsm_x4(kl, kt + tile_off(k_tok, 16 * ks + 8 * k_hb));
           ptx::ldsm_x4(kh, kt + tile_off(k_tok, 16 * (ks + KH) + 8 * k_hb));
-          const float4 a01 = __ldg(tabA + 2 * ks), a23 = __ldg(tabA + 2 * ks + 1);
-          const float4 b01 = __ldg(tabB + 2 * ks), b23 = __ldg(tabB + 2 * ks + 1);
+          const float4 g01 = g[8 * ks], g23 = g[8 * ks + 4];
           uint32_t lh[4], hh[4];
           // kl[0], kl[1]: key g4 (n-tile 0); kl[2], kl[3]: key 8 + g4 (n-tile 1)
-          const float4 cs01[4] = {a01, a23, b01, b23};
+          const float4 cs01[4] = {rot_compose(g01, fa[8 * ks]), rot_compose(g23, fa[8 * ks + 4]),
+                                  rot_compose(g01, fb[8 * ks]), rot_compose(g23, fb[8 * ks + 4])};
 #pragma unroll
           for (int r = 0; r < 4; ++r) {
             float x[2], y[2];

@@ -11,7 +11,7 @@ template <bool ROPE, bool R16, bool SMALLP>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                        int grid, cudaStream_t stream) {
   auto kern = bsr_decode_kernel<64, ROPE, R16, SMALLP>;
-  constexpr size_t smem = DecodeCfg<64>::kSmemBytes;
+  constexpr size_t smem = ROPE ? DecodeCfg<64>::kSmemBytesRope : DecodeCfg<64>::kSmemBytes;
   // The shared-memory opt-in is per device; set it on the first launch there so
   // that later launches (including ones under stream capture) make no extra call.
   static bool opted_in[kMaxDevices] = {};

@@ -62,23 +62,23 @@ struct Piece {
 };
 
 // cos/sin of every (position, frequency) in the order the decode kernel's
-// fragments consume them: [pos][quad t][k] with k = 4*ks + j and frequency
-// 16*ks + 2t + j (j < 2) or 16*ks + 8 + 2t + (j - 2) (j >= 2).  Angles are
-// computed in fp64 and rounded once to fp32.
+// fragments consume them: per position D/4 groups of two (cos, sin) pairs,
+// group i * 4 + t (quad t < 4, i < D/16) holding frequencies
+// 16 * (i / 2) + 8 * (i % 2) + 2t + {0, 1}.  Angles are computed in fp64 and
+// rounded once to fp32.
 void build_rope_table(float* dst, int32_t rows, int32_t D, double theta) {
-  const int per_quad = D / 8;
   std::vector<double> omega(D / 2);
   for (int f = 0; f < D / 2; ++f) omega[f] = std::pow(theta, -2.0 * double(f) / double(D));
   for (int32_t pos = 0; pos < rows; ++pos)
-    for (int t = 0; t < 4; ++t)
-      for (int k = 0; k < per_quad; ++k) {
-        const int ks = k / 4, j = k % 4;
-        const int f = 16 * ks + (j < 2 ? 2 * t + j : 8 + 2 * t + (j - 2));
-        const double a = double(pos) * omega[f];
-        float* e = dst + ((size_t(pos) * 4 + t) * per_quad + k) * 2;
-        e[0] = float(std::cos(a));
-        e[1] = float(std::sin(a));
-      }
+    for (int i = 0; i < D / 16; ++i)
+      for (int t = 0; t < 4; ++t)
+        for (int e = 0; e < 2; ++e) {
+          const int f = 16 * (i / 2) + 8 * (i % 2) + 2 * t + e;
+          const double a = double(pos) * omega[f];
+          float* el = dst + ((size_t(pos) * (D / 4) + i * 4 + t) * 2 + e) * 2;
+          el[0] = float(std::cos(a));
+          el[1] = float(std::sin(a));
+        }
 }
 
 // The same angles in frequency order, [pos][f] with f = 0 .. D/2-1 (prefill kernel).
