@@ -61,37 +61,24 @@ struct Piece {
   int64_t cost;
 };
 
-// cos/sin of every (position, frequency) in the order the decode kernel's
-// fragments consume them: per position D/4 groups of two (cos, sin) pairs,
-// group i * 4 + t (quad t < 4, i < D/16) holding frequencies
-// 16 * (i / 2) + 8 * (i % 2) + 2t + {0, 1}.  Angles are computed in fp64 and
-// rounded once to fp32.
-void build_rope_table(float* dst, int32_t rows, int32_t D, double theta) {
+// cos/sin of every (position, frequency), angles in fp64 rounded once to fp32, in two
+// orders.  frag: the order the decode kernel's fragments consume them, per position
+// D/4 groups of two (cos, sin) pairs, group i * 4 + t (quad t < 4, i < D/16) holding
+// frequencies 16 * (i / 2) + 8 * (i % 2) + 2t + {0, 1}.  nat: frequency order,
+// [pos][f] (RoPE pre-pass of the prefill kernel).
+void build_rope_tables(float* frag, float* nat, int32_t rows, int32_t D, double theta) {
   std::vector<double> omega(D / 2);
   for (int f = 0; f < D / 2; ++f) omega[f] = std::pow(theta, -2.0 * double(f) / double(D));
   for (int32_t pos = 0; pos < rows; ++pos)
-    for (int i = 0; i < D / 16; ++i)
-      for (int t = 0; t < 4; ++t)
-        for (int e = 0; e < 2; ++e) {
-          const int f = 16 * (i / 2) + 8 * (i % 2) + 2 * t + e;
-          const double a = double(pos) * omega[f];
-          float* el = dst + ((size_t(pos) * (D / 4) + i * 4 + t) * 2 + e) * 2;
-          el[0] = float(std::cos(a));
-          el[1] = float(std::sin(a));
-        }
-}
-
-// The same angles in frequency order, [pos][f] with f = 0 .. D/2-1 (prefill kernel).
-void build_rope_table_natural(float* dst, int32_t rows, int32_t D, double theta) {
-  for (int f = 0; f < D / 2; ++f) {
-    const double omega = std::pow(theta, -2.0 * double(f) / double(D));
-    for (int32_t pos = 0; pos < rows; ++pos) {
-      const double a = double(pos) * omega;
-      float* e = dst + (size_t(pos) * (D / 2) + f) * 2;
-      e[0] = float(std::cos(a));
-      e[1] = float(std::sin(a));
+    for (int f = 0; f < D / 2; ++f) {
+      const double a = double(pos) * omega[f];
+      const float c = float(std::cos(a)), sn = float(std::sin(a));
+      const int i = 2 * (f / 16) + (f % 16) / 8, t = (f % 8) / 2, e = f % 2;
+      float* fr = frag + ((size_t(pos) * (D / 4) + i * 4 + t) * 2 + e) * 2;
+      float* na = nat + (size_t(pos) * (D / 2) + f) * 2;
+      fr[0] = na[0] = c;
+      fr[1] = na[1] = sn;
     }
-  }
 }
 
 int fail_cuda(cudaError_t e) {
@@ -397,24 +384,44 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
     return code;
   };
 
-  // ---------------------------------------------------------------- RoPE table (cached)
-  const int32_t rope_rows =
+  // ---------------------------------------------------------------- RoPE tables (cached)
+  const int32_t need_rows =
       rope ? int32_t(align_up(size_t(hp.max_len), kStageTokens)) + kStageTokens : 0;
-  const size_t rope_bytes = size_t(rope_rows) * head_dim / 2 * sizeof(float) * 2;
-  if (rope) {
-    if (s->h_rope == nullptr || s->rope_cache_theta != rope_theta || s->rope_cache_D != head_dim ||
-        s->rope_cache_rows < rope_rows) {
-      std::free(s->h_rope);
-      // two tables of the same angles: fragment order (decode) then frequency order (prefill)
-      s->h_rope = static_cast<uint8_t*>(std::malloc(2 * rope_bytes));
-      if (s->h_rope == nullptr) return bail(BSR_ERR_OUT_OF_MEMORY);
-      build_rope_table(reinterpret_cast<float*>(s->h_rope), rope_rows, head_dim, double(rope_theta));
-      build_rope_table_natural(reinterpret_cast<float*>(s->h_rope + rope_bytes), rope_rows,
-                               head_dim, double(rope_theta));
-      s->rope_cache_theta = rope_theta;
-      s->rope_cache_D = head_dim;
-      s->rope_cache_rows = rope_rows;
+  if (rope && (s->h_rope == nullptr || s->rope_cache_theta != rope_theta ||
+               s->rope_cache_D != head_dim || s->rope_cache_rows < need_rows)) {
+    int64_t rows = 4096;
+    while (rows < need_rows) rows *= 2;
+    const size_t bytes = size_t(rows) * head_dim / 2 * sizeof(float) * 2;
+    std::free(s->h_rope);
+    s->rope_cache_rows = 0;
+    s->d_rope_valid = false;
+    s->h_rope = static_cast<uint8_t*>(std::malloc(2 * bytes));
+    if (s->h_rope == nullptr) return bail(BSR_ERR_OUT_OF_MEMORY);
+    build_rope_tables(reinterpret_cast<float*>(s->h_rope),
+                      reinterpret_cast<float*>(s->h_rope + bytes), int32_t(rows), head_dim,
+                      double(rope_theta));
+    s->rope_cache_theta = rope_theta;
+    s->rope_cache_D = head_dim;
+    s->rope_cache_rows = int32_t(rows);
+  }
+  const size_t rope_bytes =
+      rope ? size_t(s->rope_cache_rows) * head_dim / 2 * sizeof(float) * 2 : 0;
+  if (rope && !s->d_rope_valid) {
+    if (s->d_rope_cap < 2 * rope_bytes) {
+      if (s->d_rope) {
+        ce = cudaFree(s->d_rope);  // synchronizes: no kernel can still be reading it
+        s->d_rope = nullptr;
+        s->d_rope_cap = 0;
+        if (ce != cudaSuccess) return bail(fail_cuda(ce));
+      }
+      ce = cudaMalloc(reinterpret_cast<void**>(&s->d_rope), 2 * rope_bytes);
+      if (ce != cudaSuccess) return bail(fail_cuda(ce));
+      s->d_rope_cap = 2 * rope_bytes;
     }
+    // pageable source: returns once the bytes are staged; ordered on the stream
+    ce = cudaMemcpyAsync(s->d_rope, s->h_rope, 2 * rope_bytes, cudaMemcpyHostToDevice, stream);
+    if (ce != cudaSuccess) return bail(fail_cuda(ce));
+    s->d_rope_valid = true;
   }
 
   // ---------------------------------------------------------------- workspace layout
@@ -439,7 +446,6 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const size_t off_rq_start = take(rotk ? hp.rq_start.size() * 4 : 0);
   const size_t off_rq_pos0 = take(rotk ? hp.rq_pos0.size() * 4 : 0);
   const size_t off_error = take(16);
-  const size_t off_rope = take(rope ? 2 * rope_bytes : 0);
   const size_t image_bytes = off;  // everything above is uploaded
   const size_t off_part_o = take(size_t(hp.dec.n_partials) * kMaxDecodeRows * head_dim * 4);
   const size_t off_part_lse = take(size_t(hp.dec.n_partials) * kMaxDecodeRows * 4);
@@ -479,7 +485,9 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
     if (ce != cudaSuccess) return bail(fail_cuda(ce));
   }
   uint8_t* h = s->h_stage;
-  std::memset(h, 0, image_bytes);
+  // every region is written below except the split-range counters and the status word
+  std::memset(h + off_counters, 0, size_t(std::max(hp.dec.n_partials, 1)) * 4);
+  std::memset(h + off_error, 0, 16);
   if (nnz > 0) std::memcpy(h + off_indices, indices, size_t(nnz) * 4);
   if (!hp.dec.items.empty())
     std::memcpy(h + off_items, hp.dec.items.data(), hp.dec.items.size() * sizeof(DecodeItem));
@@ -489,7 +497,6 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   std::memcpy(h + off_cta_ptr, hp.pre.ptr.data(), hp.pre.ptr.size() * 4);
   if (!hp.pmerge.empty())
     std::memcpy(h + off_pmerge, hp.pmerge.data(), hp.pmerge.size() * sizeof(DecodeItem));
-  if (rope) std::memcpy(h + off_rope, s->h_rope, 2 * rope_bytes);
   if (rotk) {
     std::memcpy(h + off_rk_off, hp.rk_off.data(), size_t(batch) * 4);
     std::memcpy(h + off_rk_pbase, hp.rk_pbase.data(), hp.rk_pbase.size() * 4);
@@ -518,7 +525,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->num_pages = num_pages_in_pool;
   s->sum_qo = hp.sum_qo;
   s->active_tokens = hp.active;
-  s->rope_rows = rope_rows;
+  s->rope_rows = rope ? s->rope_cache_rows : 0;
   s->max_rows = hp.max_rows;
   s->n_items = int32_t(hp.dec.items.size());
   s->n_partials = hp.dec.n_partials;
@@ -559,7 +566,6 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->off_warp_ptr = off_warp_ptr;
   s->off_counters = off_counters;
   s->off_error = off_error;
-  s->off_rope = off_rope;
   s->off_part_o = off_part_o;
   s->off_part_lse = off_part_lse;
   *schedule = s;
@@ -576,6 +582,7 @@ extern "C" void bsr_schedule_destroy(bsr_schedule_t s) {
   if (s->upload_done) cudaEventDestroy(s->upload_done);
   for (cudaEvent_t e : s->t_ev) cudaEventDestroy(e);
   if (s->h_stage) cudaFreeHost(s->h_stage);
+  if (s->d_rope) cudaFree(s->d_rope);
   std::free(s->h_rope);
   cudaGetLastError();
   delete s;

@@ -214,82 +214,101 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      // K/V tiles are re-read by the other row units of the same (request, kv head),
-      // which run concurrently on other SMs: keep them in L2 at normal priority.
-      // Query tiles are read once.
-      const uint64_t pol = ptx::policy_evict_normal();
-      const uint64_t pol_q = ptx::policy_evict_first();
-      uint32_t c = 0, nq0 = 0, nq1 = 0;
-      bool ok = true;
-      // query tile i of a unit, once the previous unit's last Q K^T has read the buffer
-      auto load_q = [&](int i, uint32_t& nq, const DecodeItem& it) -> bool {
-        if (nq > 0 && !wt.wait(BAR(L::kQEmpty + i), (nq - 1) & 1u)) return false;
-        ++nq;
+    // The whole warp runs the loop: lane 0 waits on the ring and posts the byte
+    // counts, lane b gathers box b of a paged key tile, and each lane fetches its
+    // box's page id one tile ahead, so no page-table load is on the issue path.
+    // K/V tiles are re-read by the other row units of the same (request, kv head),
+    // which run concurrently on other SMs: keep them in L2 at normal priority.
+    // Query tiles are read once.
+    const uint64_t pol = ptx::policy_evict_normal();
+    const uint64_t pol_q = ptx::policy_evict_first();
+    uint32_t c = 0, nq0 = 0, nq1 = 0;
+    bool ok = true;
+    // lane 0 waits; the warp goes on only if the wait succeeded
+    auto ring_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+      bool r = true;
+      if (lane == 0) r = wt.wait(bar, parity);
+      return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+    };
+    // query tile i of a unit, once the previous unit's last Q K^T has read the buffer
+    auto load_q = [&](int i, uint32_t& nq, const DecodeItem& it) -> bool {
+      if (nq > 0 && !ring_wait(BAR(L::kQEmpty + i), (nq - 1) & 1u)) return false;
+      ++nq;
+      if (lane == 0) {
         ptx::mbar_arrive_expect_tx(BAR(L::kQFull + i), uint32_t(kTileBytes));
         const int q0 = it.q_row0 + (it.row0 + kTileM * i) / p.group;
         for (int h = 0; h < 2; ++h)
           ptx::tma_load_4d(Q_S(i) + h * kHalfBytes, &tm_q, BAR(L::kQFull + i), 0, h,
                            it.kvh * p.group, q0, pol_q);
-        return true;
-      };
-      for (int u = u_begin; u < u_end && ok; ++u) {
-        const DecodeItem it = p.items[u];
-        const int nt = ntiles_of(it);
-        const int koff = ROPE ? __ldg(p.rk_off + it.req) : 0;
-        // K/V come in boxes of R = min(P, 128) rows: one page holds a whole box, and a key
-        // tile (its start a multiple of max(P, 128)) is 128 / R boxes
-        const int R = p.box_rows;
-        for (int j = 0; j < nt; ++j) {
-          const int key0 = it.tok0 + kTileN * j;
-          const int nsub = (min(kTileN, it.tok1 - key0) + R - 1) / R;
-          int pages[kTileN / 16];   // all page ids of the tile first (independent loads)
-#pragma unroll
-          for (int sb = 0; sb < kTileN / 16; ++sb)
-            pages[sb] = sb < nsub ? __ldg(p.indices + it.page_base + (key0 + R * sb) / p.P) : 0;
-          const uint32_t box_bytes = uint32_t(R) * 128u;
-          // K(j)
-          if (c >= kStages && !wt.wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
-          if (ROPE) {
-            // rotated keys are dense per (kv head, request): one box per 64-column block
+      }
+      return true;
+    };
+    // K/V come in boxes of R = min(P, 128) rows (R and P powers of two): one page
+    // holds a whole box, and a key tile (its start a multiple of max(P, 128)) is
+    // 128 / R boxes
+    const int lr = 31 - __clz(p.box_rows), lp = 31 - __clz(p.P);
+    const uint32_t box_bytes = 128u << lr;
+    auto boxes_of = [&](const DecodeItem& it, int j) {
+      return (min(kTileN, it.tok1 - it.tok0 - kTileN * j) + p.box_rows - 1) >> lr;
+    };
+    auto page_of = [&](const DecodeItem& it, int j, int nsub) {
+      return lane < nsub ? __ldg(p.indices + it.page_base + ((it.tok0 + kTileN * j + (lane << lr)) >> lp))
+                         : 0;
+    };
+    // gather the paged boxes of key tile j into stage c (lane b: box b)
+    auto issue_paged = [&](const CUtensorMap* tm, uint32_t cc, const DecodeItem& it, int j,
+                           int nsub, int page) {
+      if (lane == 0) ptx::mbar_arrive_expect_tx(FULL(cc), uint32_t(nsub) * 2u * box_bytes);
+      __syncwarp();
+      if (lane < nsub) {
+        const int key = it.tok0 + kTileN * j + (lane << lr);
+        const int row = (page * p.Hk + it.kvh) * p.P + (key & (p.P - 1));
+        for (int h = 0; h < 2; ++h)
+          ptx::tma_load_3d(STAGE(cc) + h * kHalfBytes + uint32_t(lane) * box_bytes, tm, FULL(cc),
+                           0, h, row, pol);
+      }
+    };
+    for (int u = u_begin; u < u_end && ok; ++u) {
+      const DecodeItem it = p.items[u];
+      const int nt = ntiles_of(it);
+      const int koff = ROPE ? __ldg(p.rk_off + it.req) : 0;
+      int nsub_next = nt > 0 ? boxes_of(it, 0) : 0;
+      int page_next = nt > 0 ? page_of(it, 0, nsub_next) : 0;
+      for (int j = 0; j < nt; ++j) {
+        const int nsub = nsub_next, page = page_next;
+        if (j + 1 < nt) {
+          nsub_next = boxes_of(it, j + 1);
+          page_next = page_of(it, j + 1, nsub_next);
+        }
+        // K(j)
+        if (c >= kStages && !ring_wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
+        if (ROPE) {
+          // rotated keys are dense per (kv head, request): one box per 64-column block
+          if (lane == 0) {
             ptx::mbar_arrive_expect_tx(FULL(c), uint32_t(kTileBytes));
-            const int row = it.kvh * p.rk_total + koff + key0;
+            const int row = it.kvh * p.rk_total + koff + it.tok0 + kTileN * j;
             for (int h = 0; h < 2; ++h)
               ptx::tma_load_3d(STAGE(c) + h * kHalfBytes, &tm_k, FULL(c), 0, h, row, pol);
-          } else {
-            ptx::mbar_arrive_expect_tx(FULL(c), uint32_t(nsub) * 2u * box_bytes);
-#pragma unroll
-            for (int sb = 0; sb < kTileN / 16; ++sb) {
-              if (sb >= nsub) break;
-              const int row = (pages[sb] * p.Hk + it.kvh) * p.P + ((key0 + R * sb) % p.P);
-              for (int h = 0; h < 2; ++h)
-                ptx::tma_load_3d(STAGE(c) + h * kHalfBytes + sb * box_bytes, &tm_k, FULL(c), 0, h, row, pol);
-            }
           }
-          ++c;
-          if (j == 0) {
-            if (!load_q(0, nq0, it) || (it.nrows > kTileM && !load_q(1, nq1, it))) { ok = false; break; }
-          }
-          // V(j)
-          if (c >= kStages && !wt.wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
-          ptx::mbar_arrive_expect_tx(FULL(c), uint32_t(nsub) * 2u * box_bytes);
-#pragma unroll
-          for (int sb = 0; sb < kTileN / 16; ++sb) {
-            if (sb >= nsub) break;
-            const int row = (pages[sb] * p.Hk + it.kvh) * p.P + ((key0 + R * sb) % p.P);
-            for (int h = 0; h < 2; ++h)
-              ptx::tma_load_3d(STAGE(c) + h * kHalfBytes + sb * box_bytes, &tm_v, FULL(c), 0, h, row, pol);
-          }
-          ++c;
+        } else {
+          issue_paged(&tm_k, c, it, j, nsub, page);
         }
+        ++c;
+        if (j == 0) {
+          if (!load_q(0, nq0, it) || (it.nrows > kTileM && !load_q(1, nq1, it))) { ok = false; break; }
+        }
+        // V(j)
+        if (c >= kStages && !ring_wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
+        issue_paged(&tm_v, c, it, j, nsub, page);
+        ++c;
       }
-      // on abort, let the copies still in flight land before shared memory is released
-      if (!ok) {
-        for (uint32_t k = c > kStages ? c - kStages : 0; k < c; ++k)
-          ptx::mbar_wait_bounded(FULL(k), PHASE(k), 50000000ull);
-        if (nq0 > 0) ptx::mbar_wait_bounded(BAR(L::kQFull), (nq0 - 1) & 1u, 50000000ull);
-        if (nq1 > 0) ptx::mbar_wait_bounded(BAR(L::kQFull + 1), (nq1 - 1) & 1u, 50000000ull);
-      }
+    }
+    // on abort, let the copies still in flight land before shared memory is released
+    if (!ok && lane == 0) {
+      for (uint32_t k = c > kStages ? c - kStages : 0; k < c; ++k)
+        ptx::mbar_wait_bounded(FULL(k), PHASE(k), 50000000ull);
+      if (nq0 > 0) ptx::mbar_wait_bounded(BAR(L::kQFull), (nq0 - 1) & 1u, 50000000ull);
+      if (nq1 > 0) ptx::mbar_wait_bounded(BAR(L::kQFull + 1), (nq1 - 1) & 1u, 50000000ull);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer

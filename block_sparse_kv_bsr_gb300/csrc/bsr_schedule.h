@@ -28,13 +28,13 @@ struct bsr_schedule {
   // prefill plan (tensor-core kernel)
   int32_t n_pitems = 0, n_ppartials = 0, n_psplit = 0, pre_ctas = 0;
   double pre_imbalance = 1.0;
-  size_t rope_bytes = 0;     // one of the two cos/sin tables (fragment order, then frequency order)
+  size_t rope_bytes = 0;     // one of the two device cos/sin tables (fragment, then frequency order)
 
   // one device allocation holding everything the kernels read or own
   uint8_t* d_ws = nullptr;
   size_t ws_cap = 0, ws_used = 0, upload_bytes = 0;
-  size_t off_indices = 0, off_items = 0, off_warp_ptr = 0, off_counters = 0, off_rope = 0,
-         off_error = 0, off_part_o = 0, off_part_lse = 0;
+  size_t off_indices = 0, off_items = 0, off_warp_ptr = 0, off_counters = 0, off_error = 0,
+         off_part_o = 0, off_part_lse = 0;
   size_t off_pitems = 0, off_cta_ptr = 0, off_pmerge = 0, off_ppart_o = 0, off_ppart_lse = 0;
   int32_t n_pmerge = 0;      // prefill units whose key range was split (merged by a second kernel)
   // RoPE prefill: rotated-K and rotated-Q buffers and the request list of their pre-pass
@@ -58,10 +58,15 @@ struct bsr_schedule {
   cudaEvent_t upload_done = nullptr;
   bool upload_pending = false;
 
-  // cos/sin table cache: rebuilt only when theta, head_dim or the length grow
+  // cos/sin tables: built on the host and uploaded to their own device buffer only
+  // when theta or head_dim change or the longest request outgrows them (rows grow
+  // in powers of two), so re-planning a decode step uploads no table
   float rope_cache_theta = 0.f;
   int32_t rope_cache_D = 0, rope_cache_rows = 0;
-  uint8_t* h_rope = nullptr;   // host copy in fragment order (malloc)
+  uint8_t* h_rope = nullptr;   // [fragment order | frequency order] (malloc)
+  uint8_t* d_rope = nullptr;   // device copy of h_rope
+  size_t d_rope_cap = 0;
+  bool d_rope_valid = false;
 
   // tensor maps of the last k/v pools seen by run (re-encoded when they change)
   CUtensorMap tm_k;

@@ -158,3 +158,19 @@ def test_stage_timing_hook():
     bsr.bsr_schedule_set_stage_timing(s, 0)
     with pytest.raises(bsr.BsrError):
         bsr.bsr_schedule_stage_times(s, 0)
+
+
+def test_replan_grow_then_shrink_keeps_rope_tables():
+    # One schedule re-planned for longer, then shorter requests: the cos/sin tables it
+    # keeps (grown once, reused after) must serve the decode kernel and the prefill
+    # RoPE pre-pass alike.
+    short = wl.make_paged("rp_short", 54, [900, 40], Hq=32, Hk=8, D=128, P=16,
+                          qo_lens=[100, 1], causal=True, rope_theta=5e5)
+    long_ = wl.make_paged("rp_long", 55, [6000, 77], Hq=32, Hk=8, D=128, P=16,
+                          qo_lens=[150, 1], causal=True, rope_theta=5e5)
+    s = None
+    for w in (short, long_, short):
+        out, lse, s = run(w, schedule=s)
+        info = s.info()
+        assert info["num_prefill_items"] > 0 and info["num_decode_items"] > 0
+        check_full(w, out, lse)
