@@ -462,11 +462,12 @@ def main():
     # the kernel's own duration (library stage events) where the call launches more than one
     kms = dom.kernel_ms if dom.kernel_ms else dom.ms
     dom_ms = sum(kms) / len(kms)
+    sources = {"decode": _build.DECODE_KERNEL_SOURCES,
+               "prefill": _build.PREFILL_KERNEL_SOURCES}[dom.family]
+    build_digest = _build.kernel_digest(sources)
     traffic = None
     if dom.profile is not None:
-        sources = {"decode": _build.DECODE_KERNEL_SOURCES,
-                   "prefill": _build.PREFILL_KERNEL_SOURCES}[dom.family]
-        traffic = traffic_from_profile(dom.profile, _build.kernel_digest(sources))
+        traffic = traffic_from_profile(dom.profile, build_digest)
     if dom.bound == "hbm":
         achieved, peak, unit, kind = dom.work / (dom_ms * 1e-3) / 1e9, peak_hbm, "GB/s", hbm_kind
         kind = f"{kind} hbm_gbs (copy)"
@@ -491,7 +492,9 @@ def main():
         "config": dict(job["config"], parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
         "roofline": {"bound": dom.bound, "achieved": round(achieved, 1), "peak": peak,
                      "unit": unit, "frac": round(achieved / peak, 4), "peak_kind": kind,
-                     "traffic": traffic, "kernel": dom.kernel,
+                     "traffic": traffic, "traffic_source": (f"profiles/{dom.profile}"
+                                                            if traffic is not None else None),
+                     "kernel": dom.kernel, "kernel_build": build_digest,
                      "kernel_us_mean": round(dom_ms * 1e3, 2),
                      "kernel_us_min": round(min(kms) * 1e3, 2),
                      "timed_by": ("library stage events around the kernel" if dom.kernel_ms

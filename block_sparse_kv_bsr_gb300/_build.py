@@ -21,7 +21,8 @@ OUT = os.path.join(PKG, "_build")
 LIB_NAME = "libbsrattn.so"
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", f"-I{INCLUDE}", f"-I{CSRC}"]
+FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC"]
+COMMON = FLAGS + [f"-I{INCLUDE}", f"-I{CSRC}"]
 
 
 def _nvcc() -> str:
@@ -58,7 +59,7 @@ def kernel_digest(names=DECODE_KERNEL_SOURCES) -> str:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
-    h.update(" ".join(ARCH + COMMON).encode())
+    h.update(" ".join(ARCH + FLAGS).encode())   # no paths: the same on every machine
     return h.hexdigest()[:16]
 
 
