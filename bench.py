@@ -456,15 +456,16 @@ def main():
 
     peak_hbm, hbm_kind = peaks()
     peak_tensor, tensor_kind = tensor_peak()
-    # the roofline reports the call that takes the most time in a step
-    dom = max(parts, key=lambda pt: sum(pt.ms))
+    # the roofline reports the call that takes the most time in a step (among the calls
+    # of the attention kernels: a short timed region can make a setup call look longest)
+    dom = max([pt for pt in parts if pt.family is not None] or parts, key=lambda pt: sum(pt.ms))
     call_ms = sum(dom.ms) / len(dom.ms)
     # the kernel's own duration (library stage events) where the call launches more than one
     kms = dom.kernel_ms if dom.kernel_ms else dom.ms
     dom_ms = sum(kms) / len(kms)
     sources = {"decode": _build.DECODE_KERNEL_SOURCES,
-               "prefill": _build.PREFILL_KERNEL_SOURCES}[dom.family]
-    build_digest = _build.kernel_digest(sources)
+               "prefill": _build.PREFILL_KERNEL_SOURCES}.get(dom.family)
+    build_digest = _build.kernel_digest(sources) if sources else None
     traffic = None
     if dom.profile is not None:
         traffic = traffic_from_profile(dom.profile, build_digest)
