@@ -14,7 +14,10 @@
 //    one elected lane issues TMA (cp.async.bulk.tensor) loads of the next
 //    16-token K and V tiles of the unit's pages, straight from the page ids
 //    in `indices` (dropped blocks are absent there and never read), into
-//    128B-swizzled tiles completing on an mbarrier.  Only active blocks are
+//    128B-swizzled tiles completing on an mbarrier -- one box per tile (with
+//    D = 128 the map takes the two 64-column blocks as its outer dimension,
+//    so one 4 KB copy lands both: the copy engine's cost is mostly per box,
+//    and two 2 KB boxes per tile held a CTA to ~20 B/clk).  Only active blocks are
 //    gathered ("Block-Sparse 포맷").
 //  * The (query, head) rows of one GQA group are packed into the M dimension
 //    of warp-level m16n8k16 bf16 MMAs: S = Q K^T for 16 keys, online softmax
@@ -296,11 +299,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                        reinterpret_cast<const float4*>(p.rope) + size_t(tok) * C::kRopeRowF4,
                        C::kRopeRowBytes, bar, pol_rope);
       if constexpr (D == 128) {
-#pragma unroll
-        for (int h = 0; h < C::kHalves; ++h) {
-          ptx::tma_load_3d(dk + h * kStageTokens * 128, &tm_k, bar, 0, h, row, pol);
-          ptx::tma_load_3d(dv + h * kStageTokens * 128, &tm_v, bar, 0, h, row, pol);
-        }
+        // one box per tile: both 64-column blocks, [block][16 rows][128 B]
+        ptx::tma_load_3d(dk, &tm_k, bar, 0, row, 0, pol);
+        ptx::tma_load_3d(dv, &tm_v, bar, 0, row, 0, pol);
       } else {
         ptx::tma_load_2d(dk, &tm_k, bar, 0, row, pol);
         ptx::tma_load_2d(dv, &tm_v, bar, 0, row, pol);

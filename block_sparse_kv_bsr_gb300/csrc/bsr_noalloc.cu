@@ -135,7 +135,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Same tile geometry as the planned path: 16 rows x 64 columns, 128B swizzle.
+// Same stage geometry as the planned path: 16 rows x 64 columns, 128B swizzle; with
+// D = 128 both 64-column blocks of a stage in one box (rows as the inner dimension).
 bool encode_pool(CUtensorMap* tm, const void* base, int64_t rows, int D) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
@@ -146,9 +147,9 @@ bool encode_pool(CUtensorMap* tm, const void* base, int64_t rows, int D) {
   cuuint32_t rank;
   if (D == 128) {
     rank = 3;
-    dims[0] = 64; dims[1] = 2; dims[2] = cuuint64_t(rows);
-    strides[0] = 128; strides[1] = 256;
-    box[0] = 64; box[1] = 1; box[2] = kStageTokens;
+    dims[0] = 64; dims[1] = cuuint64_t(rows); dims[2] = 2;
+    strides[0] = 256; strides[1] = 128;
+    box[0] = 64; box[1] = kStageTokens; box[2] = 2;
   } else {
     rank = 2;
     dims[0] = 64; dims[1] = cuuint64_t(rows);

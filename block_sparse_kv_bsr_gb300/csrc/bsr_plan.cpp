@@ -221,6 +221,118 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
   }
 }
 
+// Prefill units of one (request, kv head) read the same K/V tiles.  They are planned in
+// gangs of up to kMaxGang row units: the gangs are cut and balanced over groups of G
+// CTAs (G = the largest gang; balance() with a gang's longest member as its key
+// range), and every piece of a gang goes to all its members at once, member r of the
+// k-th piece of a group to CTA G * group + (r + k) mod G.  The members of a gang thus
+// read each K/V tile within a short window, all but the first from L2, where a cut of
+// single units would run them on neighbouring CTAs at drifting times (K/V then come
+// from DRAM once per member); the rotation spreads the longer causal members over the
+// group.  Gangs too uneven to fill their groups (cost-weighted fill below 90 %) fall
+// back to the cut of single units.
+void balance_gangs(const std::vector<Unit>& units, int64_t num_ctas, int64_t align,
+                   int64_t overhead, int64_t min_piece, int64_t min_cta_work, WorkList* out) {
+  constexpr int kMaxGang = 8;
+  // gangs: runs of consecutive units of the same (request, kv head), at most kMaxGang long
+  std::vector<int32_t> gstart;
+  for (size_t i = 0; i < units.size(); ++i) {
+    const bool fresh = gstart.empty() || units[i].req != units[gstart.back()].req ||
+                       units[i].kvh != units[gstart.back()].kvh ||
+                       int32_t(i) - gstart.back() == kMaxGang;
+    if (fresh) gstart.push_back(int32_t(i));
+  }
+  const int ngang = int(gstart.size());
+  gstart.push_back(int32_t(units.size()));
+  int kGang = 1;
+  double filled = 0.0, offered = 0.0;
+  for (int g = 0; g < ngang; ++g) kGang = std::max(kGang, int(gstart[g + 1] - gstart[g]));
+  for (int g = 0; g < ngang; ++g) {
+    int64_t kend = 0, sum = 0;
+    for (int32_t i = gstart[g]; i < gstart[g + 1]; ++i) {
+      kend = std::max<int64_t>(kend, units[i].kend);
+      sum += units[i].kend + overhead;
+    }
+    filled += double(sum);
+    offered += double(kGang) * double(kend + overhead);
+  }
+  if (kGang == 1 || num_ctas < kGang || filled < 0.9 * offered) {
+    balance(units, num_ctas, align, overhead, min_piece, min_cta_work, out);
+    return;
+  }
+  std::vector<Unit> gunits(ngang);
+  for (int g = 0; g < ngang; ++g) {
+    Unit u = units[gstart[g]];
+    for (int32_t i = gstart[g]; i < gstart[g + 1]; ++i) u.kend = std::max(u.kend, units[i].kend);
+    u.row0 = g;   // carried through balance() to name the gang
+    gunits[g] = u;
+  }
+  WorkList gw;
+  balance(gunits, std::max<int64_t>(1, num_ctas / kGang), align, overhead, min_piece,
+          min_cta_work, &gw);
+
+  // a member takes the part of a piece below its own key end (at least one, possibly
+  // empty, piece when it has no key at all)
+  auto takes = [&](const DecodeItem& gp, const Unit& u) {
+    return std::min(gp.tok1, u.kend) > gp.tok0 || u.kend == 0;
+  };
+  std::vector<int32_t> npieces(units.size(), 0);
+  for (const DecodeItem& gp : gw.items)
+    for (int32_t i = gstart[gp.row0]; i < gstart[gp.row0 + 1]; ++i)
+      if (takes(gp, units[i])) ++npieces[i];
+  std::vector<int32_t> first_slot(units.size(), -1), next_slot(units.size(), 0);
+  out->n_partials = 0;
+  out->n_split = 0;
+  for (size_t i = 0; i < units.size(); ++i)
+    if (npieces[i] > 1) {
+      first_slot[i] = out->n_partials;
+      out->n_partials += npieces[i];
+      ++out->n_split;
+    }
+  const int workers = gw.workers * kGang;
+  std::vector<std::vector<DecodeItem>> per(workers);
+  std::vector<int64_t> load(workers, 0);
+  // balance() emits a gang's pieces in key order over consecutive groups, so each
+  // member meets its pieces in key order: slot order is key order
+  for (int w = 0; w < gw.workers; ++w)
+    for (int32_t idx = gw.ptr[w], k = 0; idx < gw.ptr[w + 1]; ++idx, ++k) {
+      const DecodeItem& gp = gw.items[idx];
+      for (int32_t i = gstart[gp.row0]; i < gstart[gp.row0 + 1]; ++i) {
+        const Unit& u = units[i];
+        if (!takes(gp, u)) continue;
+        DecodeItem it{};
+        it.req = u.req;
+        it.kvh = u.kvh;
+        it.row0 = u.row0;
+        it.nrows = u.nrows;
+        it.tok0 = gp.tok0;
+        it.tok1 = std::max(gp.tok0, std::min(gp.tok1, u.kend));
+        it.nchunks = npieces[i];
+        it.first_slot = first_slot[i];
+        it.slot = it.nchunks > 1 ? first_slot[i] + next_slot[i]++ : -1;
+        it.page_base = u.page_base;
+        it.q_row0 = u.q_row0;
+        it.qpos0 = u.qpos0;
+        const int cta = w * kGang + int((i - gstart[gp.row0] + k) % kGang);
+        per[cta].push_back(it);
+        load[cta] += int64_t(it.tok1 - it.tok0) + overhead;
+      }
+    }
+  out->items.clear();
+  out->ptr.assign(workers + 1, 0);
+  for (int w = 0; w < workers; ++w) {
+    out->items.insert(out->items.end(), per[w].begin(), per[w].end());
+    out->ptr[w + 1] = int32_t(out->items.size());
+  }
+  out->workers = workers;
+  out->imbalance = 1.0;
+  if (workers > 0) {
+    const int64_t mx = *std::max_element(load.begin(), load.end());
+    const double mean = double(std::accumulate(load.begin(), load.end(), int64_t(0))) / workers;
+    out->imbalance = mean > 0 ? double(mx) / mean : 1.0;
+  }
+}
+
 // Everything the planner decides without a GPU: validation, units, cuts,
 // per-warp item lists.
 struct HostPlan {
@@ -335,8 +447,8 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   hp->rq_total = hp->rq_start.back();
   balance(dunits, int64_t(num_sms) * kDecodeWarps, std::max<int64_t>(page_size, kStageTokens),
           kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec);
-  balance(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillKeyTile), kPrefillOverhead,
-          kPrefillMinPiece, kPrefillMinCtaWork, &hp->pre);
+  balance_gangs(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillKeyTile),
+                kPrefillOverhead, kPrefillMinPiece, kPrefillMinCtaWork, &hp->pre);
   hp->pmerge.clear();
   for (const DecodeItem& it : hp->pre.items)
     if (it.slot >= 0 && it.slot == it.first_slot) hp->pmerge.push_back(it);

@@ -61,6 +61,38 @@ bool encode_pool(CUtensorMap* tm, const void* base, int64_t rows, int D, int box
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map over a page pool for the decode kernel's 16-key stages.  D = 128: rank 3
+// {64 cols, rows, 2 column blocks} with the column blocks as the outer dimension (row
+// stride 256 B, block stride 128 B), so that one box {64, 16, 2} lands the stage as
+// [column block][16 rows][128 B], 128B-swizzled: one 4 KB copy where two 2 KB ones
+// would do (a TMA copy's cost is mostly per box: ~26 B/clk per SM with 4 KB boxes
+// against ~20 with 2 KB ones).  D = 64: rank 2, one 2 KB box.
+bool encode_pool_stage(CUtensorMap* tm, const void* base, int64_t rows, int D) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+  cuuint32_t estr[3] = {1, 1, 1};
+  cuuint32_t rank;
+  if (D == 128) {
+    rank = 3;
+    dims[0] = 64; dims[1] = cuuint64_t(rows); dims[2] = 2;
+    strides[0] = 256; strides[1] = 128;
+    box[0] = 64; box[1] = bsr::kStageTokens; box[2] = 2;
+  } else {
+    rank = 2;
+    dims[0] = 64; dims[1] = cuuint64_t(rows);
+    strides[0] = 128;
+    box[0] = 64; box[1] = bsr::kStageTokens;
+  }
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Tensor map over q (or its rotated copy) [rows, Hq, D = 128] (16-bit) for the
 // prefill kernel's query tiles: rank 4 {64 cols, 2 column blocks, Hq heads,
 // rows}; one box is one 64-column block of `group` heads x 128 / group
@@ -103,8 +135,8 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
   const bool smallp = s->P < bsr::kStageTokens;
   const int64_t rows = int64_t(s->num_pages) * s->Hk * s->P;
   if (!smallp && (s->tm_k_ptr != k_pages || s->tm_v_ptr != v_pages)) {
-    if (rows <= 0 || !encode_pool(&s->tm_k, k_pages, rows, s->D, bsr::kStageTokens) ||
-        !encode_pool(&s->tm_v, v_pages, rows, s->D, bsr::kStageTokens)) {
+    if (rows <= 0 || !encode_pool_stage(&s->tm_k, k_pages, rows, s->D) ||
+        !encode_pool_stage(&s->tm_v, v_pages, rows, s->D)) {
       s->tm_k_ptr = s->tm_v_ptr = nullptr;
       return BSR_ERR_CUDA;
     }
