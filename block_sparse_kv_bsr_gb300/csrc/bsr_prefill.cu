@@ -78,10 +78,10 @@ struct Smem {
   static_assert(kDynBytes <= 232448, "prefill tiles exceed the shared memory of one SM");
 };
 
-// Offset of (row r, 16-byte chunk c of 16) in a [2 blocks][128 rows][128 B]
-// 128B-swizzled tile.
-__device__ __forceinline__ uint32_t sw_off(int r, int c) {
-  return uint32_t((c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// Offset of (row r, 16-byte chunk c of 16) in a V tile stored by row groups:
+// [row / 8][column block][row % 8][128 B], 128B-swizzled.
+__device__ __forceinline__ uint32_t vg_off(int r, int c) {
+  return uint32_t((r >> 3) * 2048 + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 struct Waiter {
@@ -255,17 +255,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       return lane < nsub ? __ldg(p.indices + it.page_base + ((it.tok0 + kTileN * j + (lane << lr)) >> lp))
                          : 0;
     };
-    // gather the paged boxes of key tile j into stage c (lane b: box b)
-    auto issue_paged = [&](const CUtensorMap* tm, uint32_t cc, const DecodeItem& it, int j,
-                           int nsub, int page) {
+    // gather the paged boxes of key tile j into stage c (lane b: box b).  K: with boxes
+    // of 128 rows one copy lands both column blocks ([block][128 rows]); smaller boxes
+    // go one per column block.  V: one copy per box in the row-group layout.
+    auto issue_paged = [&](bool is_v, uint32_t cc, const DecodeItem& it, int j, int nsub,
+                           int page) {
       if (lane == 0) ptx::mbar_arrive_expect_tx(FULL(cc), uint32_t(nsub) * 2u * box_bytes);
       __syncwarp();
       if (lane < nsub) {
         const int key = it.tok0 + kTileN * j + (lane << lr);
         const int row = (page * p.Hk + it.kvh) * p.P + (key & (p.P - 1));
-        for (int h = 0; h < 2; ++h)
-          ptx::tma_load_3d(STAGE(cc) + h * kHalfBytes + uint32_t(lane) * box_bytes, tm, FULL(cc),
-                           0, h, row, pol);
+        if (is_v) {
+          ptx::tma_load_4d(STAGE(cc) + uint32_t(lane) * 2u * box_bytes, &tm_v, FULL(cc), 0, 0, 0,
+                           row >> 3, pol);
+        } else if (p.box_rows == kTileN) {
+          ptx::tma_load_3d(STAGE(cc), &tm_k, FULL(cc), 0, row, 0, pol);
+        } else {
+          for (int h = 0; h < 2; ++h)
+            ptx::tma_load_3d(STAGE(cc) + h * kHalfBytes + uint32_t(lane) * box_bytes, &tm_k,
+                             FULL(cc), 0, h, row, pol);
+        }
       }
     };
     for (int u = u_begin; u < u_end && ok; ++u) {
@@ -287,11 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             ptx::mbar_arrive_expect_tx(FULL(c), uint32_t(kTileBytes));
             const int row = it.kvh * p.rk_total + koff + it.tok0 + kTileN * j;
-            for (int h = 0; h < 2; ++h)
-              ptx::tma_load_3d(STAGE(c) + h * kHalfBytes, &tm_k, FULL(c), 0, h, row, pol);
+            ptx::tma_load_3d(STAGE(c), &tm_k, FULL(c), 0, row, 0, pol);   // both column blocks
           }
         } else {
-          issue_paged(&tm_k, c, it, j, nsub, page);
+          issue_paged(false, c, it, j, nsub, page);
         }
         ++c;
         if (j == 0) {
@@ -299,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // V(j)
         if (c >= kStages && !ring_wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
-        issue_paged(&tm_v, c, it, j, nsub, page);
+        issue_paged(true, c, it, j, nsub, page);
         ++c;
       }
     }
@@ -325,7 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dq0 = umma::sdesc_sw128(Q_S(0), 16, 1024);
       const uint64_t dq1 = umma::sdesc_sw128(Q_S(1), 16, 1024);
       const uint64_t dk = umma::sdesc_sw128(STAGE(0), 16, 1024);            // K-major stage 0
-      const uint64_t dv = umma::sdesc_sw128(STAGE(0), kHalfBytes, 1024);    // MN-major stage 0
+      // V (MN-major) by row groups: column blocks 1 KB apart (LBO), 8-key groups 2 KB
+      // apart (SBO), a 16-key step 4 KB
+      const uint64_t dv = umma::sdesc_sw128(STAGE(0), 1024, 2048);
       auto stage_field = [&](uint32_t c) { return uint64_t((c % kStages) * uint32_t(kTileBytes / 16)); };
       // S_i = Q_i K^T from the K stage at ring position kc
       auto qk = [&](int i, uint32_t kc) {
@@ -343,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < kTileN / 16; ++k)
           if (k < nk16)
-            umma::mma_f16_ts(O_T(i), S_T(i) + 8u * uint32_t(k) + (k >= 4 ? 32u : 0u), vd + uint64_t((k * 2048) >> 4),
+            umma::mma_f16_ts(O_T(i), S_T(i) + 8u * uint32_t(k) + (k >= 4 ? 32u : 0u), vd + uint64_t((k * 4096) >> 4),
                              idesc_pv, (acc || k > 0) ? 1u : 0u);
       };
       auto wait_p = [&](int i) {
@@ -381,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int r = nkeys; r < 16 * nk16; ++r)
 #pragma unroll
               for (int c16 = 0; c16 < 16; ++c16)
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vs + sw_off(r, c16)), "r"(0u)
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vs + vg_off(r, c16)), "r"(0u)
                              : "memory");
             ptx::fence_proxy_async_smem();
           }

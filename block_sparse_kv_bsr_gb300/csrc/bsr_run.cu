@@ -67,7 +67,8 @@ bool encode_pool(CUtensorMap* tm, const void* base, int64_t rows, int D, int box
 // [column block][16 rows][128 B], 128B-swizzled: one 4 KB copy where two 2 KB ones
 // would do (a TMA copy's cost is mostly per box: ~26 B/clk per SM with 4 KB boxes
 // against ~20 with 2 KB ones).  D = 64: rank 2, one 2 KB box.
-bool encode_pool_stage(CUtensorMap* tm, const void* base, int64_t rows, int D) {
+bool encode_pool_stage(CUtensorMap* tm, const void* base, int64_t rows, int D,
+                       int box_rows = bsr::kStageTokens) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[3];
@@ -79,14 +80,34 @@ bool encode_pool_stage(CUtensorMap* tm, const void* base, int64_t rows, int D) {
     rank = 3;
     dims[0] = 64; dims[1] = cuuint64_t(rows); dims[2] = 2;
     strides[0] = 256; strides[1] = 128;
-    box[0] = 64; box[1] = bsr::kStageTokens; box[2] = 2;
+    box[0] = 64; box[1] = cuuint32_t(box_rows); box[2] = 2;
   } else {
     rank = 2;
     dims[0] = 64; dims[1] = cuuint64_t(rows);
     strides[0] = 128;
-    box[0] = 64; box[1] = bsr::kStageTokens;
+    box[0] = 64; box[1] = cuuint32_t(box_rows);
   }
   const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Tensor map over a D = 128 page pool for the prefill kernel's V tiles: rank 4 {64
+// cols, 8 rows, 2 column blocks, rows / 8 row groups}; a box {64, 8, 2, box_rows / 8}
+// lands as [row group][column block][8 rows][128 B], 128B-swizzled, so the boxes of a
+// 128-key tile stack into one uniform layout (8-row groups 2 KB apart, the column
+// blocks of a group 1 KB apart) whatever the page size: one box per page-sized piece.
+// rows must be a multiple of 8.
+bool encode_pool_groups(CUtensorMap* tm, const void* base, int64_t rows, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr || rows % 8 != 0 || box_rows % 8 != 0) return false;
+  cuuint64_t dims[4] = {64, 8, 2, cuuint64_t(rows / 8)};
+  cuuint64_t strides[3] = {256, 128, 2048};
+  cuuint32_t box[4] = {64, 8, 2, cuuint32_t(box_rows / 8)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -205,8 +226,8 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     if (rotk) {
       // rotate the prefill requests' keys and queries once into the schedule's buffers
       if (!s->tm_rk_valid) {
-        if (!encode_pool(&s->tm_rk, s->d_ws + s->off_rotk, int64_t(s->Hk) * s->rk_total, s->D,
-                         bsr::kPrefillKeyTile))
+        if (!encode_pool_stage(&s->tm_rk, s->d_ws + s->off_rotk, int64_t(s->Hk) * s->rk_total,
+                               s->D, bsr::kPrefillKeyTile))
           return BSR_ERR_CUDA;
         s->tm_rk_valid = true;
       }
@@ -249,8 +270,13 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     // K/V boxes of min(P, 128) rows (the prefill class has P >= 16)
     const int box_rows = s->P < bsr::kPrefillKeyTile ? s->P : bsr::kPrefillKeyTile;
     if (s->tm_pk_ptr != k_pages || s->tm_pv_ptr != v_pages) {
-      if (rows <= 0 || !encode_pool(&s->tm_pk, k_pages, rows, s->D, box_rows) ||
-          !encode_pool(&s->tm_pv, v_pages, rows, s->D, box_rows)) {
+      // K: a whole 128-key tile in one box when a page holds it, else one box per
+      // column block and page; V: one box per page-sized piece (row-group layout)
+      const bool k_whole = box_rows == bsr::kPrefillKeyTile;
+      if (rows <= 0 ||
+          !(k_whole ? encode_pool_stage(&s->tm_pk, k_pages, rows, s->D, box_rows)
+                    : encode_pool(&s->tm_pk, k_pages, rows, s->D, box_rows)) ||
+          !encode_pool_groups(&s->tm_pv, v_pages, rows, box_rows)) {
         s->tm_pk_ptr = s->tm_pv_ptr = nullptr;
         return BSR_ERR_CUDA;
       }
