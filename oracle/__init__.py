@@ -39,6 +39,7 @@ _lib = None
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _i64p = ctypes.POINTER(ctypes.c_int64)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 _f64p = ctypes.POINTER(ctypes.c_double)
 
 
@@ -68,6 +69,14 @@ def _configure(lib):
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int64, ctypes.c_double, ctypes.c_double, ctypes.c_int32,
         _i64p, _i32p, ctypes.c_int64, _f64p, _f64p, ctypes.c_int32]
+    lib.oracle_attention_kv8.restype = ctypes.c_int
+    lib.oracle_attention_kv8.argtypes = [
+        _u16p, _u8p, _u8p, ctypes.c_double, ctypes.c_double, _i32p, _i32p, _i32p, _i32p,
+        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+        ctypes.c_int64, ctypes.c_double, ctypes.c_double, ctypes.c_int32,
+        _i64p, _i32p, ctypes.c_int64, _f64p, _f64p, ctypes.c_int32]
+    lib.oracle_e4m3.restype = ctypes.c_double
+    lib.oracle_e4m3.argtypes = [ctypes.c_uint8]
     lib.oracle_merge_states.restype = None
     lib.oracle_merge_states.argtypes = [_f64p, _f64p, _f64p, _f64p, ctypes.c_int64,
                                         ctypes.c_int32, _f64p, _f64p]
@@ -133,6 +142,27 @@ def default_threads() -> int:
     return len(os.sched_getaffinity(0))
 
 
+def _codes(x) -> np.ndarray:
+    """FP8 (E4M3) data as a contiguous uint8 numpy array of its codes."""
+    if hasattr(x, "numpy"):
+        x = x.detach().contiguous()
+        if str(x.dtype) != "torch.uint8":
+            import torch
+            x = x.view(torch.uint8)
+        x = x.numpy()
+    a = np.ascontiguousarray(x)
+    if a.dtype != np.uint8:
+        raise TypeError(f"expected E4M3 codes as uint8, got {a.dtype}")
+    return a
+
+
+def e4m3(codes) -> np.ndarray:
+    """Values (fp64) of OCP FP8 E4M3 codes (NaN for S.1111.111)."""
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8).ravel()
+    return np.array([lib.oracle_e4m3(int(v)) for v in c], dtype=np.float64).reshape(np.shape(codes))
+
+
 def attention(q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr, *,
               num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
               sm_scale: float, rope_theta: float = 0.0, causal: bool = False,
@@ -146,8 +176,32 @@ def attention(q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr, *,
     Returns ``(out [n, D] float64, lse [n] float64)``; for the full case the
     arrays are reshaped to ``[sum_qo, Hq, D]`` and ``[sum_qo, Hq]``.
     """
+    return _attention(None, q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr,
+                      num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, rope_theta,
+                      causal, rows, heads, threads)
+
+
+def attention_kv8(q, k_pages, v_pages, k_scale: float, v_scale: float, indptr, indices,
+                  last_page_len, qo_indptr, *, num_qo_heads: int, num_kv_heads: int,
+                  head_dim: int, page_size: int, sm_scale: float, rope_theta: float = 0.0,
+                  causal: bool = False, rows=None, heads=None, threads: int | None = None):
+    """:func:`attention` over an FP8 KV cache: ``k_pages``/``v_pages`` hold E4M3
+    codes (uint8, same layout) and the keys / values are ``k_scale * code`` and
+    ``v_scale * code``."""
+    return _attention((float(k_scale), float(v_scale)), q, k_pages, v_pages, indptr, indices,
+                      last_page_len, qo_indptr, num_qo_heads, num_kv_heads, head_dim,
+                      page_size, sm_scale, rope_theta, causal, rows, heads, threads)
+
+
+def _attention(kv8, q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr,
+               num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, rope_theta, causal,
+               rows, heads, threads):
     lib = _load()
-    qb, kb, vb = _bits(q), _bits(k_pages), _bits(v_pages)
+    qb = _bits(q)
+    if kv8 is None:
+        kb, vb = _bits(k_pages), _bits(v_pages)
+    else:
+        kb, vb = _codes(k_pages), _codes(v_pages)
     ip, ix, lp, qi = _i32(indptr), _i32(indices), _i32(last_page_len), _i32(qo_indptr)
     batch = len(ip) - 1
     num_pages = kb.size // (num_kv_heads * page_size * head_dim)
@@ -164,12 +218,15 @@ def attention(q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr, *,
     lse = np.zeros((n,), dtype=np.float64)
     if len(ix) == 0:
         ix = np.zeros((1,), dtype=np.int32)
-    rc = lib.oracle_attention(
-        _ptr(qb, _u16p), _ptr(kb, _u16p), _ptr(vb, _u16p), _ptr(ip, _i32p), _ptr(ix, _i32p),
-        _ptr(lp, _i32p) if len(lp) else None, _ptr(qi, _i32p), batch, num_qo_heads,
-        num_kv_heads, head_dim, page_size, num_pages, float(sm_scale), float(rope_theta),
-        int(bool(causal)), srp, shp, n, _ptr(out, _f64p), _ptr(lse, _f64p),
-        int(threads or default_threads()))
+    table = (_ptr(ip, _i32p), _ptr(ix, _i32p), _ptr(lp, _i32p) if len(lp) else None,
+             _ptr(qi, _i32p), batch, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
+             float(sm_scale), float(rope_theta), int(bool(causal)), srp, shp, n,
+             _ptr(out, _f64p), _ptr(lse, _f64p), int(threads or default_threads()))
+    if kv8 is None:
+        rc = lib.oracle_attention(_ptr(qb, _u16p), _ptr(kb, _u16p), _ptr(vb, _u16p), *table)
+    else:
+        rc = lib.oracle_attention_kv8(_ptr(qb, _u16p), _ptr(kb, _u8p), _ptr(vb, _u8p),
+                                      kv8[0], kv8[1], *table)
     if rc != 0:
         raise ValueError("oracle_attention: malformed input")
     if rows is None:

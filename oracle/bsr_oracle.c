@@ -29,6 +29,8 @@
  *   q        bf16 bits [sum_qo, Hq, D]
  *   k_pages  bf16 bits [num_pages, Hk, P, D]   (one (page, head) is P*D contiguous)
  *   v_pages  same as k_pages
+ *   FP8 KV cache: k_pages / v_pages as E4M3 codes (one byte each, same
+ *   layout) with one float scale per pool (oracle_attention_kv8)
  *   indptr [B+1], indices [indptr[B]], last_page_len [B], qo_indptr [B+1]
  */
 #include <math.h>
@@ -45,6 +47,27 @@ static double bf16_bits_to_double(uint16_t bits) {
   float f;
   memcpy(&f, &u, sizeof f);
   return (double)f;
+}
+
+/* OCP 8-bit floating point E4M3 (the FP8 KV-cache format): 1 sign bit, 4
+ * exponent bits with bias 7, 3 mantissa bits.  Exponent field 0 holds the
+ * subnormals m/8 * 2^-6; there are no infinities, S.1111.111 is NaN and the
+ * largest finite magnitude is 1.75 * 2^8 = 448.  Every code is exact in fp64. */
+static double e4m3_to_double(uint8_t c) {
+  const int s = c >> 7, e = (c >> 3) & 0xF, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double v = e == 0 ? ldexp((double)m / 8.0, -6) : ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+double oracle_e4m3(uint8_t code) { return e4m3_to_double(code); }
+
+/* One K or V element of the page pools: bf16 bits (kv_fp8 = 0) or an E4M3 code
+ * times the pool's per-tensor scale (kv_fp8 = 1; the FP8 KV cache stores
+ * value / scale, "quantisation/dequant" fused into attention). */
+static double kv_elem(const void* pool, int32_t kv_fp8, double scale, int64_t idx) {
+  if (kv_fp8) return scale * e4m3_to_double(((const uint8_t*)pool)[idx]);
+  return bf16_bits_to_double(((const uint16_t*)pool)[idx]);
 }
 
 /* Attended KV length of request b: all of its pages are full except the last,
@@ -112,14 +135,15 @@ static int32_t owner_of(const int32_t* qo_indptr, int32_t batch, int64_t t) {
  * (sum_qo * Hq) in [t][h] order or num_sel in selection order.
  * Returns 0, or -1 for a malformed input (bad page id, last_page_len, heads).
  */
-int oracle_attention(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
-                     const int32_t* indptr, const int32_t* indices,
-                     const int32_t* last_page_len, const int32_t* qo_indptr,
-                     int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
-                     int32_t head_dim, int32_t page_size, int64_t num_pages,
-                     double sm_scale, double rope_theta, int32_t causal,
-                     const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
-                     double* out, double* lse, int32_t num_threads) {
+static int attention_impl(const uint16_t* q, const void* k_pages, const void* v_pages,
+                          int32_t kv_fp8, double k_scale, double v_scale,
+                          const int32_t* indptr, const int32_t* indices,
+                          const int32_t* last_page_len, const int32_t* qo_indptr,
+                          int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t page_size, int64_t num_pages,
+                          double sm_scale, double rope_theta, int32_t causal,
+                          const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
+                          double* out, double* lse, int32_t num_threads) {
   const int32_t D = head_dim, P = page_size, Hq = num_qo_heads, Hk = num_kv_heads;
   if (batch < 0 || Hq <= 0 || Hk <= 0 || Hq % Hk != 0 || D <= 0 || D % 2 != 0 || P <= 0)
     return -1;
@@ -172,7 +196,7 @@ int oracle_attention(const uint16_t* q, const uint16_t* k_pages, const uint16_t*
         if (causal && j > qpos) { scores[j] = -INFINITY; continue; }
         const int64_t page = indices[indptr[b] + j / P];
         const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;
-        for (int32_t d = 0; d < D; ++d) kv[d] = bf16_bits_to_double(k_pages[off + d]);
+        for (int32_t d = 0; d < D; ++d) kv[d] = kv_elem(k_pages, kv_fp8, k_scale, off + d);
         if (rope_theta > 0.0) rope_rotate(kv, D, (double)j, rope_theta);
         double dot = 0.0;
         for (int32_t d = 0; d < D; ++d) dot += qv[d] * kv[d];
@@ -192,7 +216,7 @@ int oracle_attention(const uint16_t* q, const uint16_t* k_pages, const uint16_t*
         const double p = exp(scores[j] - l);
         const int64_t page = indices[indptr[b] + j / P];
         const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;
-        for (int32_t d = 0; d < D; ++d) o[d] += p * bf16_bits_to_double(v_pages[off + d]);
+        for (int32_t d = 0; d < D; ++d) o[d] += p * kv_elem(v_pages, kv_fp8, v_scale, off + d);
       }
     }
     free(scores);
@@ -200,6 +224,37 @@ int oracle_attention(const uint16_t* q, const uint16_t* k_pages, const uint16_t*
     free(kv);
   }
   return bad ? -1 : 0;
+}
+
+int oracle_attention(const uint16_t* q, const uint16_t* k_pages, const uint16_t* v_pages,
+                     const int32_t* indptr, const int32_t* indices,
+                     const int32_t* last_page_len, const int32_t* qo_indptr,
+                     int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                     int32_t head_dim, int32_t page_size, int64_t num_pages,
+                     double sm_scale, double rope_theta, int32_t causal,
+                     const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
+                     double* out, double* lse, int32_t num_threads) {
+  return attention_impl(q, k_pages, v_pages, 0, 1.0, 1.0, indptr, indices, last_page_len,
+                        qo_indptr, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
+                        num_pages, sm_scale, rope_theta, causal, sel_rows, sel_heads, num_sel,
+                        out, lse, num_threads);
+}
+
+/* The same attention over an FP8 (E4M3) KV cache: K = k_scale * code,
+ * V = v_scale * code, everything else as above. */
+int oracle_attention_kv8(const uint16_t* q, const uint8_t* k_pages, const uint8_t* v_pages,
+                         double k_scale, double v_scale,
+                         const int32_t* indptr, const int32_t* indices,
+                         const int32_t* last_page_len, const int32_t* qo_indptr,
+                         int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t page_size, int64_t num_pages,
+                         double sm_scale, double rope_theta, int32_t causal,
+                         const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
+                         double* out, double* lse, int32_t num_threads) {
+  return attention_impl(q, k_pages, v_pages, 1, k_scale, v_scale, indptr, indices,
+                        last_page_len, qo_indptr, batch, num_qo_heads, num_kv_heads, head_dim,
+                        page_size, num_pages, sm_scale, rope_theta, causal, sel_rows, sel_heads,
+                        num_sel, out, lse, num_threads);
 }
 
 /*

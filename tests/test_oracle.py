@@ -494,3 +494,69 @@ def test_bf16_round_helper():
     r = oracle.bf16_round(x)
     ref = torch.from_numpy(x).to(torch.bfloat16).double().numpy()
     assert np.array_equal(r, ref)
+
+
+# ---------------------------------------------------------------- FP8 (E4M3) KV cache
+
+def test_e4m3_decoder_matches_torch_and_closed_forms():
+    codes = np.arange(256, dtype=np.uint8)
+    v = oracle.e4m3(codes)
+    t = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(t)
+    assert nan.sum() == 2 and np.array_equal(np.isnan(v), nan)       # S.1111.111 only
+    assert np.array_equal(v[~nan], t[~nan])
+    # the format's landmarks: 1 = 0.0111.000, -1, 448 = 0.1111.110 (largest), smallest
+    # normal 2^-6 = 0.0001.000, smallest subnormal 2^-9 = 0.0000.001, +-0
+    assert v[0x38] == 1.0 and v[0xB8] == -1.0 and v[0x7E] == 448.0 and v[0xFE] == -448.0
+    assert v[0x08] == 2.0 ** -6 and v[0x01] == 2.0 ** -9 and v[0x00] == 0.0 and v[0x80] == 0.0
+    # every binade holds 8 evenly spaced values
+    pos = v[0x08:0x7F]
+    assert np.all(np.diff(pos) > 0)
+
+
+def _kv8_pools_as_bf16(w: wl.Paged):
+    """bf16 pools holding exactly the FP8 cache's values (an E4M3 value times a power of
+    two is exact in bf16), via torch's own E4M3 conversion."""
+    k = (w.k_codes.view(torch.float8_e4m3fn).to(torch.float64) * w.k_scale).to(torch.bfloat16)
+    v = (w.v_codes.view(torch.float8_e4m3fn).to(torch.float64) * w.v_scale).to(torch.bfloat16)
+    return k, v
+
+
+def run_oracle_kv8(w: wl.Paged, **kw):
+    return oracle.attention_kv8(w.q, w.k_codes, w.v_codes, w.k_scale, w.v_scale, w.indptr,
+                                w.indices, w.last_page_len, w.qo_indptr,
+                                num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
+                                head_dim=w.head_dim, page_size=w.page_size,
+                                sm_scale=w.sm_scale, rope_theta=w.rope_theta, causal=w.causal,
+                                **kw)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(qo_lens=[1, 3, 5, 2], causal=True),
+                                dict(rope_theta=10000.0), dict(Hq=8, Hk=1, P=1)])
+def test_kv8_equals_attention_over_the_decoded_values(kw):
+    w = wl.with_kv8(tiny(**kw), 77)
+    o8, l8 = run_oracle_kv8(w)
+    k, v = _kv8_pools_as_bf16(w)
+    w.k_pages, w.v_pages = k, v
+    o, l = run_oracle(w)
+    assert np.array_equal(o8, o) and np.array_equal(l8, l)
+    ro, rl = dense_reference(w)
+    _close(o8, ro)
+    _close(l8, rl)
+    assert np.isfinite(o8).all()
+
+
+def test_kv8_scales_apply_to_keys_and_values():
+    # doubling v_scale doubles the output; k_scale rescales the logits like sm_scale
+    w = wl.with_kv8(tiny(), 78)
+    o1, l1 = run_oracle_kv8(w)
+    w.v_scale *= 2.0
+    o2, l2 = run_oracle_kv8(w)
+    assert np.array_equal(o2, 2.0 * o1) and np.array_equal(l2, l1)
+    w.k_scale *= 2.0
+    o3, l3 = run_oracle_kv8(w)
+    w.k_scale /= 2.0
+    w.sm_scale *= 2.0
+    o4, l4 = run_oracle_kv8(w)
+    _close(o3, o4)
+    _close(l3, l4)

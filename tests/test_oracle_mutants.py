@@ -35,9 +35,13 @@ MUTANTS = {
     "last_page_len": ("return (n - 1) * page_size + last_page_len[b];", "return n * page_size;"),
     "lse_drops_max": ("const double l = m + log(sum);", "const double l = log(sum);"),
     "scale_dropped": ("scores[j] = sm_scale * dot;", "scores[j] = dot;"),
-    "v_reads_k": ("o[d] += p * bf16_bits_to_double(v_pages[off + d]);",
-                  "o[d] += p * bf16_bits_to_double(k_pages[off + d]);"),
+    "v_reads_k": ("o[d] += p * kv_elem(v_pages, kv_fp8, v_scale, off + d);",
+                  "o[d] += p * kv_elem(k_pages, kv_fp8, v_scale, off + d);"),
     "merge_weight": ("wb * o_b[r * D + d]", "wa * o_b[r * D + d]"),
+    "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
+    "e4m3_subnormal": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "kv8_v_scale": ("o[d] += p * kv_elem(v_pages, kv_fp8, v_scale, off + d);",
+                    "o[d] += p * kv_elem(v_pages, kv_fp8, k_scale, off + d);"),
     "merge_lse": ("const double l = M + log(exp(a - M) + exp(b - M));",
                   "const double l = M + log(exp(a - M) + exp(b - M) + 1.0);"),
     "append_pos": ("const int64_t pos = L - n_new + i;", "const int64_t pos = L - n_new + i - 1;"),
@@ -61,7 +65,10 @@ def _checks():
           pins.test_rope_d2_is_rotation_by_position_radians,
           pins.test_causal_row_equals_decode_at_shorter_length,
           pins.test_append_then_attend_equals_concatenation,
-          pins.test_kv_len_and_malformed_tables]
+          pins.test_kv_len_and_malformed_tables,
+          pins.test_e4m3_decoder_matches_torch_and_closed_forms,
+          lambda: pins.test_kv8_equals_attention_over_the_decoded_values(dict()),
+          pins.test_kv8_scales_apply_to_keys_and_values]
     return c
 
 

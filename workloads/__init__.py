@@ -30,6 +30,7 @@ from dataclasses import dataclass, field
 import torch
 
 NAN_BF16 = 0x7FC0
+NAN_E4M3 = 0x7F
 
 
 @dataclass
@@ -56,6 +57,12 @@ class Paged:
     k_new: torch.Tensor | None = None           # bf16 [sum_append, Hk, D]
     v_new: torch.Tensor | None = None
     meta: dict = field(default_factory=dict)
+    # FP8 KV cache (E4M3 codes, uint8, same layout as k_pages / v_pages): the keys and
+    # values are k_scale * code and v_scale * code
+    k_codes: torch.Tensor | None = None
+    v_codes: torch.Tensor | None = None
+    k_scale: float = 1.0
+    v_scale: float = 1.0
 
     @property
     def batch(self) -> int:
@@ -128,15 +135,17 @@ def _poison_unused(w: Paged, fill_from: list | None = None):
         valid_to = w.kv_len[b] if fill_from is None else fill_from[b]
         for j, e in enumerate(range(lo, hi)):
             valid[ind[e]] = min(max(valid_to - j * P, 0), P)
-    for t in (w.k_pages, w.v_pages):
-        bits = t.view(torch.int16)
+    pools = [(w.k_pages.view(torch.int16), NAN_BF16), (w.v_pages.view(torch.int16), NAN_BF16)]
+    if w.k_codes is not None:
+        pools += [(w.k_codes, NAN_E4M3), (w.v_codes, NAN_E4M3)]
+    for bits, nan in pools:
         empty = (valid == 0).nonzero().flatten()
         if len(empty):
-            bits[empty] = NAN_BF16
+            bits[empty] = nan
         for s in range(P):
             sel = ((valid <= s) & (valid > 0)).nonzero().flatten()
             if len(sel):
-                bits[sel, :, s, :] = NAN_BF16
+                bits[sel, :, s, :] = nan
 
 
 def make_paged(name, seed, lens, *, Hq, Hk, D, P, qo_lens=None, drop=0.0, rope_theta=0.0,
@@ -270,9 +279,31 @@ def config5(small: bool = False) -> Paged:
                          rope_theta=5e5, causal=True, append=True)
 
 
+def with_kv8(w: Paged, seed: int, spread: float = 16.0) -> Paged:
+    """The same batch with an FP8 (E4M3) KV cache: fresh N(0, 1) keys and values
+    drawn (generator seeded with ``seed``), multiplied by ``spread``, rounded to E4M3
+    codes (round to nearest even, torch's conversion) and stored with scale
+    1 / spread, so the cached values are N(0, 1)-like as in the bf16 workloads.
+    Unowned slots hold the E4M3 NaN code."""
+    g = torch.Generator().manual_seed(seed)
+    shape = tuple(w.k_pages.shape)
+    w.k_codes = (torch.randn(shape, generator=g) * spread).to(torch.float8_e4m3fn).view(torch.uint8)
+    w.v_codes = (torch.randn(shape, generator=g) * spread).to(torch.float8_e4m3fn).view(torch.uint8)
+    w.k_scale = w.v_scale = 1.0 / spread
+    w.name = w.name + "_kv_e4m3"
+    _poison_unused(w)
+    return w
+
+
+def config6(small: bool = False) -> Paged:
+    """The skewed block-sparse decode with an FP8 (E4M3) KV cache."""
+    return with_kv8(config3(small), 1006)
+
+
 def by_name(cfg: int, small: bool = False):
     return {1: lambda: config1(), 2: lambda: config2(small), 3: lambda: config3(small),
-            4: lambda: config4(small), 5: lambda: config5(small)}[cfg]()
+            4: lambda: config4(small), 5: lambda: config5(small),
+            6: lambda: config6(small)}[cfg]()
 
 
 def flat_cascade(c: Cascade) -> Paged:
@@ -324,8 +355,9 @@ def flat_cascade(c: Cascade) -> Paged:
 
 def algorithmic_bytes(w: Paged) -> int:
     """Bytes the attention must touch at least once: active K and V, q, out, lse, page table."""
-    elt = 2
-    kv = w.active_tokens * 2 * w.num_kv_heads * w.head_dim * elt
+    elt = 2                                            # q and out are bf16
+    kv_elt = 1 if w.k_codes is not None else 2         # E4M3 or bf16 KV cache
+    kv = w.active_tokens * 2 * w.num_kv_heads * w.head_dim * kv_elt
     rows = int(w.qo_indptr[-1]) * w.num_qo_heads
     qo = rows * w.head_dim * elt * 2 + rows * 4
     table = 4 * (len(w.indptr) + len(w.indices) + len(w.last_page_len) + len(w.qo_indptr))
