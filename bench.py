@@ -15,8 +15,8 @@ roofline  = the decode kernel's algorithmic bytes / its mean CUDA-event duration
 cpu_baseline = the fp64 oracle on this host's cores (a bounded sample of the batch).
 
 --config selects another workload for measurement (2: Llama-3-8B-shaped decode with RoPE,
-4: shared-prefix cascade, 5: chunked prefill with append, reported in TFLOP/s); the
-default is the skewed decode above.  --impl reference times the oracle (the only
+4: shared-prefix cascade, 5: chunked prefill with append, reported in TFLOP/s, 6: the
+skewed decode over an FP8 (E4M3) KV cache); the default is the skewed decode above.  --impl reference times the oracle (the only
 reference this method has here) on the same workload.  Under torchrun each rank runs an
 independent replica (weak scaling).
 """
@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--small", action="store_true", help="small case (profiling, smoke)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5],
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6],
                     help="workload; 3 (skewed block-sparse decode) is the headline")
     return ap.parse_args()
 
@@ -187,10 +187,14 @@ def cpu_baseline(w, budget_s=10.0, min_passes=1):
     passes, spent = 0, 0.0
     while passes < min_passes or spent < budget_s:
         t0 = time.perf_counter()
-        oracle.attention(w.q, w.k_pages, w.v_pages, w.indptr, w.indices, w.last_page_len,
-                         w.qo_indptr, num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
-                         head_dim=w.head_dim, page_size=w.page_size, sm_scale=w.sm_scale,
-                         rope_theta=w.rope_theta, causal=w.causal, threads=threads)
+        table = (w.indptr, w.indices, w.last_page_len, w.qo_indptr)
+        kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                  page_size=w.page_size, sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+                  causal=w.causal, threads=threads)
+        if w.k_codes is not None:
+            oracle.attention_kv8(w.q, w.k_codes, w.v_codes, w.k_scale, w.v_scale, *table, **kw)
+        else:
+            oracle.attention(w.q, w.k_pages, w.v_pages, *table, **kw)
         spent += time.perf_counter() - t0
         passes += 1
     return {"value": round(alg * passes / spent / 1e9, 3), "unit": "GB/s", "cores": threads,
@@ -277,6 +281,46 @@ def build_job(cfg: int, dev, small: bool):
             q_dev.copy_(q_host, non_blocking=True)
             bsr.bsr_attn_run(s, q_dev, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta,
                              causal=w.causal, out=out, lse=lse)
+            out_host.copy_(out, non_blocking=True)
+            lse_host.copy_(lse, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+
+        job["e2e"] = e2e
+        job["e2e_bytes"] = lambda: (q.numel() * 2 + int(s.info()["upload_bytes"]),
+                                    out.numel() * 2 + lse.numel() * 4)
+    elif cfg == 6:
+        w = wl.config6(small)
+        q = w.q.to(dev)
+        k, v = w.k_codes.to(dev), w.v_codes.to(dev)
+        out = torch.empty_like(q)
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        s = plan(w)
+        run = lambda: bsr.bsr_attn_run_kv8(s, q, k, v, k_scale=w.k_scale, v_scale=w.v_scale,
+                                           sm_scale=w.sm_scale, causal=w.causal, out=out, lse=lse)
+        alg = wl.algorithmic_bytes(w)
+        job["parts"] = [Part("decode", run, "bsr_decode_kv8_kernel", "hbm", alg, "B",
+                             launches=s.info()["kernels_per_run"], sched=s, stage="decode",
+                             family="decode_kv8",
+                             profile=None if small else "bsr_decode_kv8_skewed_b128.md")]
+        job["schedules"] = [s]
+        job["dtype"] = "f16 MMA on E4M3 codes, fp32 accumulate"
+        job.update(workload=w, metric=METRIC, unit="GB/s", numerator=alg, scale=1e9,
+                   config={"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads,
+                           "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                           "page_size": w.page_size, "active_kv_tokens": w.active_tokens,
+                           "kv_cache": "E4M3 codes + per-pool scales (q, out bf16)",
+                           "algorithmic_bytes": alg, "drop": "25% of non-final pages",
+                           "l2": "inputs larger than L2, no flush"})
+        q_host = w.q.pin_memory()
+        out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        q_dev = torch.empty_like(q)
+
+        def e2e():
+            plan(w, s)
+            q_dev.copy_(q_host, non_blocking=True)
+            bsr.bsr_attn_run_kv8(s, q_dev, k, v, k_scale=w.k_scale, v_scale=w.v_scale,
+                                 sm_scale=w.sm_scale, causal=w.causal, out=out, lse=lse)
             out_host.copy_(out, non_blocking=True)
             lse_host.copy_(lse, non_blocking=True)
             torch.cuda.current_stream().synchronize()
@@ -464,6 +508,7 @@ def main():
     kms = dom.kernel_ms if dom.kernel_ms else dom.ms
     dom_ms = sum(kms) / len(kms)
     sources = {"decode": _build.DECODE_KERNEL_SOURCES,
+               "decode_kv8": _build.DECODE_KV8_KERNEL_SOURCES,
                "prefill": _build.PREFILL_KERNEL_SOURCES}.get(dom.family)
     build_digest = _build.kernel_digest(sources) if sources else None
     traffic = None
@@ -488,7 +533,7 @@ def main():
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": job.get("dtype", "bf16"),
         "data": "synthetic (seeded N(0,1) bf16, page table drawn per workloads/)",
         "config": dict(job["config"], parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
         "roofline": {"bound": dom.bound, "achieved": round(achieved, 1), "peak": peak,
@@ -530,7 +575,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     import workloads as wl
-    w = wl.config3(small=args.small)
+    w = wl.by_name(args.config if args.config in (1, 2, 3, 6) else 3, args.small)
     for _ in range(args.warmup):
         cpu_baseline(w, budget_s=0.0)
     t0 = time.perf_counter()

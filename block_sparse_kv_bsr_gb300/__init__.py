@@ -17,7 +17,7 @@ from . import _build
 
 __all__ = [
     "BsrError", "load", "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run",
-    "bsr_merge_states", "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info",
+    "bsr_attn_run_kv8", "bsr_merge_states", "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info",
     "bsr_last_device_error", "bsr_status_string", "bsr_attn_decode_noalloc", "Schedule",
     "bsr_schedule_set_stage_timing", "bsr_schedule_stage_times", "STAGES", "EXPORTED_SYMBOLS",
 ]
@@ -27,8 +27,8 @@ BSR_DTYPE_BF16 = 0
 BSR_DTYPE_F32 = 1
 
 EXPORTED_SYMBOLS = (
-    "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run", "bsr_merge_states", "bsr_append_kv",
-    "bsr_schedule_destroy", "bsr_schedule_get_info", "bsr_last_device_error",
+    "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run", "bsr_attn_run_kv8", "bsr_merge_states",
+    "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info", "bsr_last_device_error",
     "bsr_status_string", "bsr_attn_decode_noalloc", "bsr_schedule_set_stage_timing",
     "bsr_schedule_stage_times",
 )
@@ -82,6 +82,10 @@ def load(path: str | None = None):
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
                                        ctypes.c_int32, ctypes.POINTER(_Info), _i32p,
                                        ctypes.c_int64]
+    lib.bsr_attn_run_kv8.restype = ctypes.c_int
+    lib.bsr_attn_run_kv8.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
+                                     ctypes.c_float, ctypes.c_float, ctypes.c_int32, _vp,
+                                     ctypes.c_int32, _vp, _vp]
     lib.bsr_attn_run.restype = ctypes.c_int
     lib.bsr_attn_run.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                  ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp]
@@ -238,6 +242,33 @@ def bsr_attn_run(schedule: Schedule, q, k_pages, v_pages, *, sm_scale: float,
                             float(sm_scale), float(rope_theta), int(bool(causal)), _dptr(out), dt,
                             _dptr(lse), _vp(_stream_ptr(stream)))
     _check(code, "bsr_attn_run")
+    return out, lse
+
+
+def bsr_attn_run_kv8(schedule: Schedule, q, k_pages, v_pages, *, k_scale: float, v_scale: float,
+                     sm_scale: float, rope_theta: float = 0.0, causal: bool = False, out=None,
+                     lse=None, out_dtype=None, want_lse: bool = True, stream=None):
+    """Run a schedule over an FP8 (E4M3) KV cache: ``k_pages``/``v_pages`` are uint8
+    (or float8_e4m3fn) codes, the cached values ``k_scale * code`` / ``v_scale * code``."""
+    import torch
+    lib = load()
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or torch.bfloat16, device=q.device)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out must be bf16 or fp32")
+    if q.dtype != torch.bfloat16:
+        raise ValueError("q must be bf16")
+    for t in (k_pages, v_pages):
+        if t.element_size() != 1:
+            raise ValueError("k_pages, v_pages must hold one-byte E4M3 codes")
+    dt = BSR_DTYPE_F32 if out.dtype == torch.float32 else BSR_DTYPE_BF16
+    code = lib.bsr_attn_run_kv8(_vp(schedule.handle), _dptr(q), _dptr(k_pages), _dptr(v_pages),
+                                float(k_scale), float(v_scale), float(sm_scale),
+                                float(rope_theta), int(bool(causal)), _dptr(out), dt, _dptr(lse),
+                                _vp(_stream_ptr(stream)))
+    _check(code, "bsr_attn_run_kv8")
     return out, lse
 
 

@@ -51,6 +51,7 @@ def _digest() -> str:
 # Sources that determine a kernel family's machine code (for matching a profile to a build).
 DECODE_KERNEL_SOURCES = ("bsr_decode.cuh", "bsr_decode_d128.cu", "bsr_internal.h", "ptx.cuh")
 PREFILL_KERNEL_SOURCES = ("bsr_prefill.cu", "bsr_internal.h", "ptx.cuh", "umma.cuh")
+DECODE_KV8_KERNEL_SOURCES = ("bsr_decode_kv8.cu", "bsr_decode.cuh", "bsr_internal.h", "ptx.cuh")
 
 
 def kernel_digest(names=DECODE_KERNEL_SOURCES) -> str:

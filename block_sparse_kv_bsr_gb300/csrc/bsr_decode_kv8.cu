@@ -1,0 +1,446 @@
+// Split-KV decode attention over an FP8 (E4M3) paged KV cache, sm_103a.
+//
+// The "quantisation / dequant" variant of the attention operator ("FlashInfer:
+// Block-Sparse KV 캐시로 어텐션 병목을 해소하다", section "JIT 컴파일은 …"):
+// the cache holds K and V as one-byte E4M3 codes with one float scale per pool
+// (K = k_scale * code, V = v_scale * code), which halves the bytes a decode
+// step streams from HBM.  The dequantisation is fused into the page gather:
+// TMA copies the codes (one 2 KB box per 16-key stage for K and for V: a
+// 128-byte row is a whole D = 128 head), and each warp converts them to fp16
+// in registers right before its MMAs.  Every E4M3 code is exact in fp16, so
+// QK^T and PV see the cached values unchanged; k_scale folds into the logit
+// scale and v_scale into the output normalisation.
+//
+// Structure and scheduling are the bf16 decode kernel's (persistent warps,
+// private TMA rings, planned work units, in-kernel merge of split ranges).
+// What differs is how fragments are formed from one-byte elements:
+//  * S = Q K^T: ldmatrix on the code tile gives a thread 4 consecutive codes
+//    (dims 4t..4t+3 of a 16-dim block) of one key.  The head dimension is
+//    taken in that order for q as well (q . k is a sum over dims, so the same
+//    permutation on both sides leaves it unchanged): a0 = q dims 4t, 4t+1,
+//    a2 = dims 4t+2, 4t+3.
+//  * O += P V: ldmatrix.trans on byte pairs gives a thread dims (2g, 2g+1) of
+//    keys 2t and 2t+1; a byte permute splits them into the even-dim and the
+//    odd-dim n-tile of the block, so each thread's accumulators hold dims
+//    4t..4t+3 of every 16-dim block (stored contiguously).
+//  * P enters PV as fp16 (11 significant bits).
+// Every barrier wait is bounded; on timeout the warp sets bit 0 of the status
+// word, drains its own copies (bounded) and exits.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "bsr_decode.cuh"
+#include "bsr_schedule.h"
+
+#ifndef BSR_DECODE_STAGES_KV8
+#define BSR_DECODE_STAGES_KV8 6
+#endif
+
+namespace bsr {
+namespace {
+
+constexpr int kD8 = 128;                                      // head dim (bytes per row)
+constexpr int kTile8 = kStageTokens * kD8;                    // one K (or V) stage: 2 KB
+constexpr int kStage8 = 2 * kTile8;
+constexpr int kStages8 = BSR_DECODE_STAGES_KV8;
+constexpr size_t kSmem8 = size_t(kDecodeWarps) * kStages8 * kStage8 +
+                          size_t(kDecodeWarps) * kStages8 * 8 + 1024;
+static_assert(kSmem8 <= 232448, "FP8 decode stages exceed the shared memory of one SM");
+
+// Byte offset of (token t, 16-byte chunk c of 8) in a [16 rows][128 B] tile with
+// the TMA 128-byte swizzle.
+__device__ __forceinline__ uint32_t tile8_off(int t, int c) {
+  return uint32_t((t << 7) + ((c ^ (t & 7)) << 4));
+}
+
+// Two E4M3 codes (the low 16 bits, low byte first) as an fp16 pair (low half
+// first): the PTX conversion instruction, exact (every E4M3 value is an fp16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}" : "=r"(d) : "r"(two));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+  return ptx::pack_f16(ptx::bf16_lo(v), ptx::bf16_hi(v));
+}
+
+template <bool R16>
+__global__ void __launch_bounds__(kDecodeWarps * 32, 1)
+    bsr_decode_kv8_kernel(const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
+  constexpr int D = kD8;
+  constexpr int NR = R16 ? 4 : 2;       // accumulator registers per n-tile that carry rows
+  constexpr int KB = D / 16;            // 16-dim blocks
+  constexpr int NT = D / 8;             // n-tiles of the output
+  extern __shared__ uint8_t smem_raw[];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kDecodeWarps + warp;
+  if (gw >= p.num_warps) return;
+  const int it_begin = __ldg(p.warp_ptr + gw), it_end = __ldg(p.warp_ptr + gw + 1);
+  if (it_begin >= it_end) return;
+
+  const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t ring = base + uint32_t(warp * kStages8 * kStage8);
+  const uint32_t bars = base + uint32_t(kDecodeWarps * kStages8 * kStage8 + warp * kStages8 * 8);
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages8; ++s) ptx::mbar_init(bars + 8 * s, 1);
+    ptx::fence_barrier_init();
+  }
+  __syncwarp();
+  const uint64_t pol = ptx::policy_evict_first();
+  const int g4 = lane >> 2, t4 = lane & 3;
+  const int log2P = 31 - __clz(p.P);
+
+  // ------------------------------------------------------------------ producer
+  // Up to kStages8 stages ahead of the consumer; page ids of the next 32 stages
+  // of the current unit sit one per lane in `win`.
+  int p_it = it_begin, p_st = 0, p_nst = 0, win = 0, win_next = 0, win_base = 0;
+  uint32_t p_seq = 0;
+  DecodeItem pi;
+  auto load_window = [&](const DecodeItem& it, int ws) -> int {
+    const int s = ws + lane;
+    if (s < stages_of(it))
+      return __ldg(p.indices + it.page_base + ((it.tok0 + kStageTokens * s) >> log2P));
+    return 0;
+  };
+  auto producer_seek = [&]() {
+    while (p_it < it_end) {
+      pi = load_item(p.items, p_it);
+      p_nst = stages_of(pi);
+      if (p_nst > 0) break;
+      ++p_it;
+    }
+    if (p_it < it_end) {
+      win_base = 0;
+      win = load_window(pi, 0);
+      win_next = load_window(pi, 32);
+    }
+  };
+  auto producer_issue = [&]() {
+    if (p_it >= it_end) return;
+    const int slot = int(p_seq % kStages8);
+    const int page = __shfl_sync(0xffffffffu, win, p_st - win_base);
+    if (lane == 0) {
+      const uint32_t bar = bars + 8 * slot;
+      const uint32_t dk = ring + uint32_t(slot * kStage8), dv = dk + kTile8;
+      const int tok = pi.tok0 + kStageTokens * p_st;
+      const int row = (page * p.Hk + pi.kvh) * p.P + (tok & (p.P - 1));
+      ptx::mbar_arrive_expect_tx(bar, kStage8);
+      ptx::tma_load_2d(dk, &tm_k, bar, 0, row, pol);
+      ptx::tma_load_2d(dv, &tm_v, bar, 0, row, pol);
+    }
+    ++p_seq;
+    ++p_st;
+    if (p_st == p_nst) {
+      ++p_it;
+      p_st = 0;
+      producer_seek();
+    } else if (p_st - win_base == 32) {
+      win_base += 32;
+      win = win_next;
+      win_next = load_window(pi, win_base + 32);
+    }
+  };
+  producer_seek();
+#pragma unroll 1
+  for (int i = 0; i < kStages8; ++i) producer_issue();
+
+  // ------------------------------------------------------------------ consumer
+  // ldmatrix lane addressing (matrix mi = lane / 8, row lane % 8):
+  //  K (x4): mi covers keys (mi / 2) * 8.., 16-byte chunk 2 * pair + mi % 2
+  //  V (x4, trans): mi covers keys (mi % 2) * 8.., chunk 2 * pair + mi / 2
+  const int mi = lane >> 3;
+  const int k_tok = ((mi >> 1) << 3) + (lane & 7), k_cb = mi & 1;
+  const int v_tok = ((mi & 1) << 3) + (lane & 7), v_cb = mi >> 1;
+  constexpr float kLn2 = 0.69314718055994530942f;
+
+  uint32_t c_seq = 0;
+  bool failed = false;
+#pragma unroll 1
+  for (int c_it = it_begin; c_it < it_end; ++c_it) {
+    const DecodeItem ci = load_item(p.items, c_it);
+    const int nst = stages_of(ci);
+    const int group = p.group;
+    const int rA = ci.row0 + g4, rB = ci.row0 + g4 + 8;
+    const bool vA = g4 < ci.nrows, vB = R16 && (g4 + 8 < ci.nrows);
+    const int qposA = ci.qpos0 + rA / group, qposB = ci.qpos0 + rB / group;
+    const int qpos_min = ci.qpos0 + ci.row0 / group;
+
+    // q fragments in fp16, head dims of block kb in the order 4t..4t+3:
+    // [kb][0] = row g4 dims 4t, 4t+1; [kb][NR/2] = row g4 dims 4t+2, 4t+3;
+    // with R16 [kb][1] / [kb][3] the same for row g4 + 8.
+    uint32_t qh[KB][NR];
+    {
+      const uint16_t* qa =
+          p.q + (size_t(ci.q_row0 + rA / group) * p.Hq + ci.kvh * group + rA % group) * D;
+      const uint16_t* qb =
+          p.q + (size_t(ci.q_row0 + rB / group) * p.Hq + ci.kvh * group + rB % group) * D;
+#pragma unroll
+      for (int kb = 0; kb < KB; ++kb) {
+        const int d0 = 16 * kb + 4 * t4;
+        const uint2 a = vA ? __ldg(reinterpret_cast<const uint2*>(qa + d0)) : make_uint2(0u, 0u);
+        qh[kb][0] = bf16x2_to_f16x2(a.x);
+        qh[kb][NR / 2] = bf16x2_to_f16x2(a.y);
+        if constexpr (R16) {
+          const uint2 b = vB ? __ldg(reinterpret_cast<const uint2*>(qb + d0)) : make_uint2(0u, 0u);
+          qh[kb][1] = bf16x2_to_f16x2(b.x);
+          qh[kb][3] = bf16x2_to_f16x2(b.y);
+        }
+      }
+    }
+
+    float o[NT][NR];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int r = 0; r < NR; ++r) o[n][r] = 0.f;
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
+
+#pragma unroll 1
+    for (int st = 0; st < nst; ++st) {
+      const int slot = int(c_seq % kStages8);
+      const uint32_t kt = ring + uint32_t(slot * kStage8), vt = kt + kTile8;
+      const int tok = ci.tok0 + kStageTokens * st;
+      const int nvalid = min(kStageTokens, ci.tok1 - tok);
+      if (!ptx::mbar_wait_bounded(bars + 8 * slot, (c_seq / kStages8) & 1u, p.wait_limit_ns)) {
+        failed = true;
+        break;
+      }
+      if (nvalid < kStageTokens) {
+        // Rows past the valid keys may hold another page's tail (NaN codes
+        // included): zero their V codes so that P = 0 contributes exactly 0.
+#pragma unroll 1
+        for (int idx = lane; idx < (kStageTokens - nvalid) * 8; idx += 32) {
+          const int t = nvalid + idx / 8, c = idx % 8;
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vt + tile8_off(t, c)),
+                       "r"(0u)
+                       : "memory");
+        }
+      }
+      __syncwarp();
+
+      // ---------------- S = Q K^T  (two n-tiles of 8 keys), 32 dims per ldmatrix
+      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int pr = 0; pr < KB / 2; ++pr) {
+        uint32_t kr[4];
+        ptx::ldsm_x4(kr, kt + tile8_off(k_tok, 2 * pr + k_cb));
+        // kr[h]: keys g4 (n-tile 0), block 2 pr + h; kr[2 + h]: keys 8 + g4 (n-tile 1)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int kb = 2 * pr + h;
+          const uint32_t a0 = qh[kb][0], a2 = qh[kb][NR / 2];
+          const uint32_t a1 = R16 ? qh[kb][1] : 0u, a3 = R16 ? qh[kb][NR - 1] : 0u;
+          ptx::mma_f16(s0[0], s0[1], s0[2], s0[3], a0, a1, a2, a3, e4m3x2_to_f16x2(kr[h]),
+                       e4m3x2_to_f16x2(kr[h] >> 16));
+          ptx::mma_f16(s1[0], s1[1], s1[2], s1[3], a0, a1, a2, a3, e4m3x2_to_f16x2(kr[2 + h]),
+                       e4m3x2_to_f16x2(kr[2 + h] >> 16));
+        }
+      }
+
+      // ---------------- mask + online softmax (log2 domain; k_scale is in scale_log2)
+      const bool full =
+          (nvalid == kStageTokens) && (!p.causal || tok + kStageTokens - 1 <= qpos_min);
+      float xa[4], xb[4];
+      {
+        const float sc = p.scale_log2;
+        const int k0 = tok + 2 * t4;
+        const int kidx[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
+        const float sa[4] = {s0[0], s0[1], s1[0], s1[1]};
+        const float sb[4] = {s0[2], s0[3], s1[2], s1[3]};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const bool inr = full || (kidx[j] < ci.tok1);
+          const bool okA = full || (inr && (!p.causal || kidx[j] <= qposA));
+          const bool okB = full || (inr && (!p.causal || kidx[j] <= qposB));
+          xa[j] = okA ? sa[j] * sc : -INFINITY;
+          xb[j] = okB ? sb[j] * sc : -INFINITY;
+        }
+      }
+      float mxA = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
+      mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
+      mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
+      const float mnA = fmaxf(mA, mxA);
+      const float muA = mnA == -INFINITY ? 0.f : mnA;
+      const float alA = ptx::ex2(mA - muA);
+      mA = mnA;
+      float pa[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) pa[j] = ptx::ex2(xa[j] - muA);
+      lA = lA * alA + ((pa[0] + pa[1]) + (pa[2] + pa[3]));
+      float alB = 1.f;
+      float pb[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (R16) {
+        float mxB = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
+        mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
+        const float mnB = fmaxf(mB, mxB);
+        const float muB = mnB == -INFINITY ? 0.f : mnB;
+        alB = ptx::ex2(mB - muB);
+        mB = mnB;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pb[j] = ptx::ex2(xb[j] - muB);
+        lB = lB * alB + ((pb[0] + pb[1]) + (pb[2] + pb[3]));
+      }
+      if (__any_sync(0xffffffffu, alA != 1.f || alB != 1.f)) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+          o[n][0] *= alA;
+          o[n][1] *= alA;
+          if constexpr (R16) {
+            o[n][NR - 2] *= alB;
+            o[n][NR - 1] *= alB;
+          }
+        }
+      }
+
+      // ---------------- O += P V  (P in fp16), 32 dims per ldmatrix
+      const uint32_t ph0 = ptx::pack_f16(pa[0], pa[1]), ph2 = ptx::pack_f16(pa[2], pa[3]);
+      const uint32_t ph1 = R16 ? ptx::pack_f16(pb[0], pb[1]) : 0u;
+      const uint32_t ph3 = R16 ? ptx::pack_f16(pb[2], pb[3]) : 0u;
+#pragma unroll
+      for (int pr = 0; pr < KB / 2; ++pr) {
+        uint32_t vr[4];
+        ptx::ldsm_x4_trans(vr, vt + tile8_off(v_tok, 2 * pr + v_cb));
+        // vr[2h]: keys 2t, 2t+1 of the first 8 keys, dims (2 g4, 2 g4 + 1) of block
+        // 2 pr + h; vr[2h + 1]: the same for keys 8 + 2t, 8 + 2t + 1
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int cb = 2 * pr + h;
+          const uint32_t lo = vr[2 * h], hi = vr[2 * h + 1];
+          // even dims of the block (2 g4), then odd dims (2 g4 + 1)
+          const uint32_t be0 = e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0020));
+          const uint32_t be1 = e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0020));
+          const uint32_t bo0 = e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0031));
+          const uint32_t bo1 = e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0031));
+          float* e = o[2 * cb];
+          float* f = o[2 * cb + 1];
+          if constexpr (R16) {
+            ptx::mma_f16(e[0], e[1], e[NR - 2], e[NR - 1], ph0, ph1, ph2, ph3, be0, be1);
+            ptx::mma_f16(f[0], f[1], f[NR - 2], f[NR - 1], ph0, ph1, ph2, ph3, bo0, bo1);
+          } else {
+            // rows g4 + 8 are padding: their accumulators are dead scratch
+            float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+            ptx::mma_f16(e[0], e[1], z0, z1, ph0, 0u, ph2, 0u, be0, be1);
+            ptx::mma_f16(f[0], f[1], z2, z3, ph0, 0u, ph2, 0u, bo0, bo1);
+          }
+        }
+      }
+      __syncwarp();
+      // generic writes (the zero fill) must be ordered before the TMA that reuses the slot
+      if (nvalid < kStageTokens) ptx::fence_proxy_async_smem();
+      __syncwarp();
+      ++c_seq;
+      producer_issue();
+    }
+    if (failed) break;
+
+    // ---------------- epilogue: dims 16 c + 4 t .. + 3 of every block c are
+    // o[2c][c0], o[2c+1][c0], o[2c][c0+1], o[2c+1][c0+1]
+    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+    if constexpr (R16) {
+      lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+      lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+    }
+    const float lseA = lA > 0.f ? mA + ptx::lg2(lA) : -INFINITY;
+    const float lseB = lB > 0.f ? mB + ptx::lg2(lB) : -INFINITY;
+    const float invA = lA > 0.f ? p.v_scale / lA : 0.f;
+    const float invB = lB > 0.f ? p.v_scale / lB : 0.f;
+    if (ci.slot < 0) {
+#pragma unroll
+      for (int rr = 0; rr < (R16 ? 2 : 1); ++rr) {
+        const bool ok = rr == 0 ? vA : vB;
+        if (!ok) continue;
+        const int R = rr == 0 ? rA : rB;
+        const float inv = rr == 0 ? invA : invB;
+        const int c0 = rr == 0 ? 0 : NR - 2;
+        const size_t orow = size_t(ci.q_row0 + R / group) * p.Hq + ci.kvh * group + R % group;
+        if (p.out_f32) {
+          float* dst = static_cast<float*>(p.out) + orow * D + 4 * t4;
+#pragma unroll
+          for (int cb = 0; cb < KB; ++cb)
+            *reinterpret_cast<float4*>(dst + 16 * cb) =
+                make_float4(o[2 * cb][c0] * inv, o[2 * cb + 1][c0] * inv,
+                            o[2 * cb][c0 + 1] * inv, o[2 * cb + 1][c0 + 1] * inv);
+        } else {
+          uint16_t* dst = static_cast<uint16_t*>(p.out) + orow * D + 4 * t4;
+#pragma unroll
+          for (int cb = 0; cb < KB; ++cb)
+            *reinterpret_cast<uint2*>(dst + 16 * cb) =
+                make_uint2(ptx::pack_bf16(o[2 * cb][c0] * inv, o[2 * cb + 1][c0] * inv),
+                           ptx::pack_bf16(o[2 * cb][c0 + 1] * inv, o[2 * cb + 1][c0 + 1] * inv));
+        }
+        if (p.lse != nullptr && t4 == 0) p.lse[orow] = (rr == 0 ? lseA : lseB) * kLn2;
+      }
+    } else {
+#pragma unroll
+      for (int rr = 0; rr < (R16 ? 2 : 1); ++rr) {
+        const int r = g4 + 8 * rr;
+        const float inv = rr == 0 ? invA : invB;
+        const int c0 = rr == 0 ? 0 : NR - 2;
+        float* dst = p.part_o + (size_t(ci.slot) * kMaxDecodeRows + r) * D + 4 * t4;
+#pragma unroll
+        for (int cb = 0; cb < KB; ++cb)
+          __stcg(reinterpret_cast<float4*>(dst + 16 * cb),
+                 make_float4(o[2 * cb][c0] * inv, o[2 * cb + 1][c0] * inv,
+                             o[2 * cb][c0 + 1] * inv, o[2 * cb + 1][c0 + 1] * inv));
+        if (t4 == 0)
+          __stcg(p.part_lse + size_t(ci.slot) * kMaxDecodeRows + r, rr == 0 ? lseA : lseB);
+      }
+      __threadfence();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(p.counters + ci.first_slot, 1) == ci.nchunks - 1;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        merge_range<D>(p, ci, lane);
+        if (lane == 0) atomicExch(p.counters + ci.first_slot, 0);
+      }
+    }
+  }
+
+  if (failed) {
+    if (lane == 0) atomicOr(p.error, 1);
+    // let the copies this warp still has in flight land before the CTA exits
+#pragma unroll 1
+    for (uint32_t s = c_seq; s < p_seq; ++s)
+      ptx::mbar_wait_bounded(bars + 8 * (s % kStages8), (s / kStages8) & 1u, 50000000ull);
+  }
+}
+
+constexpr int kMaxDevices = 64;
+
+template <bool R16>
+cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                       int grid, cudaStream_t stream) {
+  auto kern = bsr_decode_kv8_kernel<R16>;
+  static bool opted_in[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!opted_in[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem8));
+    if (e != cudaSuccess) return e;
+    opted_in[dev] = true;
+  }
+  kern<<<grid, kDecodeWarps * 32, kSmem8, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode_kv8(bool r16, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const DecodeParams& p, int grid, cudaStream_t stream) {
+  return r16 ? launch_one<true>(tk, tv, p, grid, stream) : launch_one<false>(tk, tv, p, grid, stream);
+}
+
+}  // namespace bsr

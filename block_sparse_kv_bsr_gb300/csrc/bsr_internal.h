@@ -63,7 +63,8 @@ struct DecodeParams {
   void* out;                      // bf16 or fp32 [sum_qo, Hq, D]
   float* lse;                     // fp32 [sum_qo, Hq] or null
   int32_t* error;                 // device status word
-  float scale_log2;               // sm_scale * log2(e)
+  float scale_log2;               // sm_scale * log2(e) (times k_scale for an FP8 cache)
+  float v_scale;                  // FP8 cache: value of one V code unit (1 otherwise)
   int32_t Hq, Hk, group, P;
   int32_t causal, out_f32, num_warps;
   int32_t rope_max_pos;           // last row of the cos/sin table

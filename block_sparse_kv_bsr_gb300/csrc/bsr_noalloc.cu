@@ -263,6 +263,7 @@ extern "C" int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const
   p.lse = lse;
   p.error = status;
   p.scale_log2 = float(double(sm_scale) * 1.4426950408889634);
+  p.v_scale = 1.f;
   p.Hq = num_qo_heads;
   p.Hk = num_kv_heads;
   p.group = group;

@@ -94,6 +94,23 @@ bool encode_pool_stage(CUtensorMap* tm, const void* base, int64_t rows, int D,
   return r == CUDA_SUCCESS;
 }
 
+// Tensor map over an FP8 (E4M3, one byte per element) page pool with D = 128:
+// rank 2 {128 bytes, rows}; one box is a 16-key stage, [16 rows][128 B],
+// 128B-swizzled (a row is one whole head).
+bool encode_pool_e4m3(CUtensorMap* tm, const void* base, int64_t rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {128, cuuint64_t(rows)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, bsr::kStageTokens};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Tensor map over a D = 128 page pool for the prefill kernel's V tiles: rank 4 {64
 // cols, 8 rows, 2 column blocks, rows / 8 row groups}; a box {64, 8, 2, box_rows / 8}
 // lands as [row group][column block][8 rows][128 B], 128B-swizzled, so the boxes of a
@@ -201,6 +218,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.lse = lse;
     p.error = s->dev<int32_t>(s->off_error);
     p.scale_log2 = scale_log2;
+    p.v_scale = 1.f;
     p.Hq = s->Hq;
     p.Hk = s->Hk;
     p.group = s->group;
@@ -374,4 +392,84 @@ extern "C" int bsr_schedule_stage_times(bsr_schedule_t s, int32_t call, float* m
     }
   }
   return int(kept);
+}
+
+extern "C" int bsr_attn_run_kv8(bsr_schedule_t s, const void* q, const void* k_pages,
+                                const void* v_pages, float k_scale, float v_scale, float sm_scale,
+                                float rope_theta, int32_t causal, void* out, int32_t out_dtype,
+                                float* lse, void* stream_v) {
+  if (s == nullptr || s->d_ws == nullptr) return BSR_ERR_INVALID_ARGUMENT;
+  if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return BSR_ERR_INVALID_ARGUMENT;
+  if (!(k_scale > 0.f) || !std::isfinite(k_scale) || !(v_scale > 0.f) || !std::isfinite(v_scale))
+    return BSR_ERR_INVALID_ARGUMENT;
+  if (out_dtype != BSR_DTYPE_BF16 && out_dtype != BSR_DTYPE_F32) return BSR_ERR_INVALID_ARGUMENT;
+  if (rope_theta != s->rope_theta || causal != s->causal) return BSR_ERR_SCHEDULE_MISMATCH;
+  // the FP8 path covers the decode kernel's work: D = 128, pages of at least 16
+  // keys, no RoPE, every request on the decode kernel
+  if (s->D != 128 || s->P < bsr::kStageTokens || s->rope_rows > 0 || s->n_pitems > 0)
+    return BSR_ERR_UNSUPPORTED;
+  if (s->n_items == 0) return BSR_OK;
+  if (q == nullptr || out == nullptr || k_pages == nullptr || v_pages == nullptr)
+    return BSR_ERR_INVALID_ARGUMENT;
+  if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(q, 16) || !aligned(out, 16) ||
+      (lse && !aligned(lse, 4)))
+    return BSR_ERR_INVALID_ARGUMENT;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != s->device) return BSR_ERR_SCHEDULE_MISMATCH;
+  const cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const int64_t rows = int64_t(s->num_pages) * s->Hk * s->P;
+  if (s->tm_k8_ptr != k_pages || s->tm_v8_ptr != v_pages) {
+    if (rows <= 0 || !encode_pool_e4m3(&s->tm_k8, k_pages, rows) ||
+        !encode_pool_e4m3(&s->tm_v8, v_pages, rows)) {
+      s->tm_k8_ptr = s->tm_v8_ptr = nullptr;
+      return BSR_ERR_CUDA;
+    }
+    s->tm_k8_ptr = k_pages;
+    s->tm_v8_ptr = v_pages;
+  }
+  int t_slot = -1;
+  if (s->t_max > 0) {
+    t_slot = int(s->t_count % s->t_max);
+    ++s->t_count;
+    for (int st = 0; st < bsr_schedule::kStages; ++st) s->t_ran[t_slot * bsr_schedule::kStages + st] = 0;
+  }
+  auto t_mark = [&](int stage, int edge) {
+    if (t_slot < 0) return;
+    cudaEventRecord(s->t_ev[(t_slot * bsr_schedule::kStages + stage) * 2 + edge], stream);
+    if (edge == 1) s->t_ran[t_slot * bsr_schedule::kStages + stage] = 1;
+  };
+  bsr::DecodeParams p{};
+  p.items = s->dev<const bsr::DecodeItem>(s->off_items);
+  p.warp_ptr = s->dev<const int32_t>(s->off_warp_ptr);
+  p.counters = s->dev<int32_t>(s->off_counters);
+  p.part_o = s->dev<float>(s->off_part_o);
+  p.part_lse = s->dev<float>(s->off_part_lse);
+  p.indices = s->dev<const int32_t>(s->off_indices);
+  p.rope = nullptr;
+  p.q = static_cast<const uint16_t*>(q);
+  p.k_pages = k_pages;
+  p.v_pages = v_pages;
+  p.out = out;
+  p.lse = lse;
+  p.error = s->dev<int32_t>(s->off_error);
+  p.scale_log2 = float(double(sm_scale) * double(k_scale) * 1.4426950408889634);
+  p.v_scale = v_scale;
+  p.Hq = s->Hq;
+  p.Hk = s->Hk;
+  p.group = s->group;
+  p.P = s->P;
+  p.causal = s->causal;
+  p.out_f32 = out_dtype == BSR_DTYPE_F32;
+  p.num_warps = s->dec_warps;
+  p.rope_max_pos = 0;
+  p.wait_limit_ns = 1000000000ull;
+  t_mark(0, 0);
+  const cudaError_t e = bsr::launch_decode_kv8(s->max_rows > 8, s->tm_k8, s->tm_v8, p,
+                                               s->dec_ctas, stream);
+  t_mark(0, 1);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return BSR_ERR_CUDA;
+  }
+  return BSR_OK;
 }

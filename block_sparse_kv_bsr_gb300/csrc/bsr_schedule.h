@@ -73,6 +73,11 @@ struct bsr_schedule {
   CUtensorMap tm_v;
   const void* tm_k_ptr = nullptr;
   const void* tm_v_ptr = nullptr;
+  // the same for FP8 (E4M3) pools
+  CUtensorMap tm_k8;
+  CUtensorMap tm_v8;
+  const void* tm_k8_ptr = nullptr;
+  const void* tm_v8_ptr = nullptr;
 
   // optional per-stage timing of runs: events [run slot][stage][begin, end]
   static constexpr int kStages = 4;   // decode, RoPE pre-pass, prefill, merge
@@ -93,6 +98,8 @@ cudaError_t launch_decode_d64(bool rope, bool r16, bool smallp, const CUtensorMa
 cudaError_t launch_decode_d128(bool rope, bool r16, bool smallp, const CUtensorMap& tk,
                                const CUtensorMap& tv, const DecodeParams& p, int grid,
                                cudaStream_t stream);
+cudaError_t launch_decode_kv8(bool r16, const CUtensorMap& tk, const CUtensorMap& tv,
+                              const DecodeParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillParams& p, int grid,
                            cudaStream_t stream);

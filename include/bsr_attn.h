@@ -120,6 +120,24 @@ int bsr_attn_run(bsr_schedule_t schedule, const void* q, const void* k_pages, co
                  float* lse, void* stream);
 
 /*
+ * bsr_attn_run_kv8 — bsr_attn_run over an FP8 KV cache (the quantisation /
+ * dequant variant of the attention operator, "JIT 컴파일은 …"): k_pages and
+ * v_pages hold OCP FP8 E4M3 codes, one byte per element, in the same
+ * [num_pages_in_pool, Hk, P, D] layout; the cached keys and values are
+ * k_scale * code and v_scale * code (per-pool scales, finite and > 0; codes
+ * S.1111.111 are NaN).  Dequantisation is fused into the page gather: the
+ * codes are converted to fp16 in registers (exact) right before the MMAs.
+ * Everything else (q bf16, out, lse, alignment, ownership, stream semantics)
+ * is as for bsr_attn_run.  Covered: head_dim 128, page_size >= 16, no RoPE,
+ * every request on the decode kernel (info.num_prefill_items == 0); other
+ * schedules return BSR_ERR_UNSUPPORTED.
+ */
+int bsr_attn_run_kv8(bsr_schedule_t schedule, const void* q, const void* k_pages,
+                     const void* v_pages, float k_scale, float v_scale, float sm_scale,
+                     float rope_theta, int32_t causal, void* out, int32_t out_dtype, float* lse,
+                     void* stream);
+
+/*
  * bsr_merge_states — combine two attention states over disjoint key sets
  * (split chunks, or the shared-prefix and suffix levels of a cascade;
  * "Block-Sparse 포맷", composition of a stored-once prefix with suffixes):

@@ -1,0 +1,112 @@
+"""GPU parity of the FP8 (E4M3) KV-cache decode path against the fp64 oracle.
+
+The cache holds E4M3 codes with one scale per pool; the oracle decodes the
+codes from the format definition.  Cases: the skewed block-sparse decode
+(small, element by element; full size, sampled rows), ragged tails and split
+ranges, a 16-row GQA group, causal multi-query decode rows, page sizes 16 to
+256, fp32 output, NaN codes in unowned slots, and the schedules the path does
+not cover (refused, not run).
+"""
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_kv_bsr_gb300 as bsr
+import oracle
+import workloads as wl
+from block_sparse_kv_bsr_gb300 import _build
+from parity import assert_lse_close, assert_out_close, plan, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_device):
+    _build.build()
+    bsr.load()
+
+
+def run_kv8(w: wl.Paged, out_dtype=torch.bfloat16):
+    dev = "cuda:0"
+    s = plan(w)
+    out, lse = bsr.bsr_attn_run_kv8(s, w.q.to(dev), w.k_codes.to(dev), w.v_codes.to(dev),
+                                    k_scale=w.k_scale, v_scale=w.v_scale, sm_scale=w.sm_scale,
+                                    rope_theta=w.rope_theta, causal=w.causal, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert bsr.bsr_last_device_error(s) == 0
+    return out, lse, s
+
+
+def oracle_kv8(w: wl.Paged, rows=None, heads=None):
+    return oracle.attention_kv8(w.q, w.k_codes, w.v_codes, w.k_scale, w.v_scale, w.indptr,
+                                w.indices, w.last_page_len, w.qo_indptr,
+                                num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
+                                head_dim=w.head_dim, page_size=w.page_size,
+                                sm_scale=w.sm_scale, rope_theta=w.rope_theta, causal=w.causal,
+                                rows=rows, heads=heads)
+
+
+def check_full_kv8(w, out, lse):
+    ro, rl = oracle_kv8(w)
+    bf16 = out.dtype == torch.bfloat16
+    assert_out_close(out.float().cpu().numpy(), ro, bf16, w.name)
+    assert_lse_close(lse.cpu().numpy(), rl, w.name)
+
+
+def test_kv8_skewed_small():
+    w = wl.config6(small=True)
+    out, lse, s = run_kv8(w)
+    assert s.info()["num_split_streams"] > 0
+    check_full_kv8(w, out, lse)
+
+
+def test_kv8_skewed_full_size_sampled():
+    w = wl.config6()
+    out, lse, _ = run_kv8(w)
+    rows, heads = sample_rows(w, 1536)
+    ro, rl = oracle_kv8(w, rows, heads)
+    assert_out_close(out.float().cpu().numpy()[rows, heads], ro, True, w.name)
+    assert_lse_close(lse.cpu().numpy()[rows, heads], rl, w.name)
+
+
+@pytest.mark.parametrize("P", [16, 32, 256])
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_kv8_page_sizes_and_ragged_tails(P, out_dtype):
+    w = wl.with_kv8(wl.make_paged(f"kv8p{P}", 60 + P, [1, 15, 17, 300, 1000, 2600], Hq=32, Hk=8,
+                                  D=128, P=P, drop=0.2), 601 + P)
+    out, lse, _ = run_kv8(w, out_dtype)
+    check_full_kv8(w, out, lse)
+
+
+def test_kv8_sixteen_row_group_and_long_split():
+    # GQA group 16 (two 8-row halves in one MMA row tile), one long request cut into chunks
+    w = wl.with_kv8(wl.make_paged("kv8g16", 71, [9000, 40, 333], Hq=32, Hk=2, D=128, P=16), 701)
+    out, lse, s = run_kv8(w)
+    assert s.info()["num_split_streams"] > 0
+    check_full_kv8(w, out, lse)
+
+
+def test_kv8_causal_multi_query_rows():
+    w = wl.with_kv8(wl.make_paged("kv8causal", 72, [50, 400, 1200], Hq=32, Hk=8, D=128, P=16,
+                                  qo_lens=[3, 1, 2], causal=True), 702)
+    out, lse, s = run_kv8(w)
+    assert s.info()["num_prefill_items"] == 0
+    check_full_kv8(w, out, lse)
+
+
+def test_kv8_unsupported_schedules_are_refused():
+    dev = "cuda:0"
+    cases = [
+        wl.make_paged("kv8d64", 73, [100, 200], Hq=8, Hk=2, D=64, P=16),          # head_dim 64
+        wl.make_paged("kv8rope", 74, [100, 200], Hq=32, Hk=8, D=128, P=16, rope_theta=1e4),
+        wl.make_paged("kv8pf", 75, [700], Hq=32, Hk=8, D=128, P=16, qo_lens=[300],
+                      causal=True),                                                # prefill class
+        wl.make_paged("kv8p8", 76, [100, 200], Hq=32, Hk=8, D=128, P=8),            # P < 16
+    ]
+    for w in cases:
+        w = wl.with_kv8(w, 703)
+        s = plan(w)
+        with pytest.raises(bsr.BsrError):
+            bsr.bsr_attn_run_kv8(s, w.q.to(dev), w.k_codes.to(dev), w.v_codes.to(dev),
+                                 k_scale=w.k_scale, v_scale=w.v_scale, sm_scale=w.sm_scale,
+                                 rope_theta=w.rope_theta, causal=w.causal)
