@@ -142,9 +142,11 @@ static int attention_impl(const uint16_t* q, const void* k_pages, const void* v_
                           int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                           int32_t head_dim, int32_t page_size, int64_t num_pages,
                           double sm_scale, double rope_theta, int32_t causal,
+                          int32_t window_left,
                           const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
                           double* out, double* lse, int32_t num_threads) {
   const int32_t D = head_dim, P = page_size, Hq = num_qo_heads, Hk = num_kv_heads;
+  if (window_left < 0) return -1;
   if (batch < 0 || Hq <= 0 || Hk <= 0 || Hq % Hk != 0 || D <= 0 || D % 2 != 0 || P <= 0)
     return -1;
   const int32_t group = Hq / Hk;
@@ -194,6 +196,9 @@ static int attention_impl(const uint16_t* q, const void* k_pages, const void* v_
       double m = -INFINITY;
       for (int64_t j = 0; j < L; ++j) {
         if (causal && j > qpos) { scores[j] = -INFINITY; continue; }
+        /* sliding window: only the window_left most recent positions up to the
+         * query's own (reading of the JIT section's "Sliding Window" variant) */
+        if (window_left > 0 && j < qpos - window_left + 1) { scores[j] = -INFINITY; continue; }
         const int64_t page = indices[indptr[b] + j / P];
         const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;
         for (int32_t d = 0; d < D; ++d) kv[d] = kv_elem(k_pages, kv_fp8, k_scale, off + d);
@@ -231,13 +236,13 @@ int oracle_attention(const uint16_t* q, const uint16_t* k_pages, const uint16_t*
                      const int32_t* last_page_len, const int32_t* qo_indptr,
                      int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                      int32_t head_dim, int32_t page_size, int64_t num_pages,
-                     double sm_scale, double rope_theta, int32_t causal,
+                     double sm_scale, double rope_theta, int32_t causal, int32_t window_left,
                      const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
                      double* out, double* lse, int32_t num_threads) {
   return attention_impl(q, k_pages, v_pages, 0, 1.0, 1.0, indptr, indices, last_page_len,
                         qo_indptr, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                        num_pages, sm_scale, rope_theta, causal, sel_rows, sel_heads, num_sel,
-                        out, lse, num_threads);
+                        num_pages, sm_scale, rope_theta, causal, window_left, sel_rows,
+                        sel_heads, num_sel, out, lse, num_threads);
 }
 
 /* The same attention over an FP8 (E4M3) KV cache: K = k_scale * code,
@@ -249,12 +254,13 @@ int oracle_attention_kv8(const uint16_t* q, const uint8_t* k_pages, const uint8_
                          int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                          int32_t head_dim, int32_t page_size, int64_t num_pages,
                          double sm_scale, double rope_theta, int32_t causal,
+                         int32_t window_left,
                          const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
                          double* out, double* lse, int32_t num_threads) {
   return attention_impl(q, k_pages, v_pages, 1, k_scale, v_scale, indptr, indices,
                         last_page_len, qo_indptr, batch, num_qo_heads, num_kv_heads, head_dim,
-                        page_size, num_pages, sm_scale, rope_theta, causal, sel_rows, sel_heads,
-                        num_sel, out, lse, num_threads);
+                        page_size, num_pages, sm_scale, rope_theta, causal, window_left,
+                        sel_rows, sel_heads, num_sel, out, lse, num_threads);
 }
 
 /*

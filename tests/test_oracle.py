@@ -560,3 +560,80 @@ def test_kv8_scales_apply_to_keys_and_values():
     o4, l4 = run_oracle_kv8(w)
     _close(o3, o4)
     _close(l3, l4)
+
+
+# ---------------------------------------------------------------- sliding window
+
+def _windowed_dense(w: wl.Paged, W: int):
+    """dense_reference with every key older than the window masked (a drop mask)."""
+    masks = []
+    for b in range(w.batch):
+        L = w.kv_len[b]
+        n = int(w.qo_indptr[b + 1] - w.qo_indptr[b])
+        masks.append(None if n != 1 else torch.arange(L) >= L - W)
+    return masks
+
+
+def test_window_wider_than_every_request_changes_nothing():
+    w = tiny(qo_lens=[1, 3, 5, 2], causal=True, rope_theta=300.0)
+    o, l = run_oracle(w)
+    o2, l2 = run_oracle(w, window_left=max(w.kv_len))
+    assert np.array_equal(o, o2) and np.array_equal(l, l2)
+
+
+def test_window_of_one_sees_only_its_own_key():
+    w = tiny()                      # decode rows: position L - 1
+    o, l = run_oracle(w, window_left=1)
+    g = w.num_qo_heads // w.num_kv_heads
+    for b in range(w.batch):
+        L = w.kv_len[b]
+        page = int(w.indices[w.indptr[b] + (L - 1) // w.page_size])
+        for h in range(w.num_qo_heads):
+            k = w.k_pages[page, h // g, (L - 1) % w.page_size].double()
+            v = w.v_pages[page, h // g, (L - 1) % w.page_size].double()
+            s = float(w.q[b, h].double() @ k) * w.sm_scale
+            _close(o[b, h], v.numpy())
+            _close(l[b, h], s)
+
+
+@pytest.mark.parametrize("W", [2, 5, 9])
+def test_window_equals_masking_older_keys(W):
+    # decode rows: the window keeps keys L - W .. L - 1, i.e. drops the older ones
+    w = tiny(lens=(1, 7, 13, 30, 41))
+    o, l = run_oracle(w, window_left=W)
+    ro, rl = dense_reference(w, drop_mask=_windowed_dense(w, W))
+    _close(o, ro)
+    _close(l, rl)
+
+
+def test_window_causal_rows_equal_decode_with_window():
+    # a causal row at position p with window W equals a decode of the first p + 1 keys
+    w = tiny(qo_lens=[1, 3, 5, 2], causal=True, rope_theta=100.0)
+    W = 4
+    o, l = run_oracle(w, window_left=W)
+    b, t = 2, int(w.qo_indptr[2]) + 3          # request 2, its 4th query
+    L = w.kv_len[b]
+    p = L - 5 + 3
+    d = wl.make_paged("tiny", 7, [1], Hq=4, Hk=2, D=8, P=4)   # shape holder, replaced below
+    d.indptr = torch.tensor([0, int(w.indptr[b + 1] - w.indptr[b])], dtype=torch.int32)
+    d.indices = w.indices[w.indptr[b]:w.indptr[b + 1]].clone()
+    d.last_page_len = torch.tensor([(p + 1) - ((p + 1 + w.page_size - 1) // w.page_size - 1)
+                                    * w.page_size], dtype=torch.int32)
+    n_pages = (p + 1 + w.page_size - 1) // w.page_size
+    d.indptr[1] = n_pages
+    d.indices = d.indices[:n_pages]
+    d.kv_len = [p + 1]
+    d.qo_indptr = torch.tensor([0, 1], dtype=torch.int32)
+    d.q = w.q[t:t + 1].clone()
+    d.k_pages, d.v_pages, d.num_pages = w.k_pages, w.v_pages, w.num_pages
+    d.rope_theta = w.rope_theta
+    od, ld = run_oracle(d, window_left=W)
+    _close(o[t], od[0])
+    _close(l[t], ld[0])
+
+
+def test_window_workload_reads_nothing_outside_the_window():
+    w = wl.config7(small=True)
+    assert int((w.indices == 0).sum()) > 0          # pages aliased to the poisoned page
+    o, l = run_oracle(w, window_left=w.window_left)
+    assert np.isfinite(o).all() and np.isfinite(l).all()

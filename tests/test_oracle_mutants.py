@@ -40,6 +40,8 @@ MUTANTS = {
     "merge_weight": ("wb * o_b[r * D + d]", "wa * o_b[r * D + d]"),
     "e4m3_bias": ("ldexp(1.0 + (double)m / 8.0, e - 7)", "ldexp(1.0 + (double)m / 8.0, e - 8)"),
     "e4m3_subnormal": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
+    "window_off_by_one": ("j < qpos - window_left + 1)", "j < qpos - window_left)"),
+    "window_from_end": ("j < qpos - window_left + 1)", "j < L - window_left)"),
     "kv8_v_scale": ("o[d] += p * kv_elem(v_pages, kv_fp8, v_scale, off + d);",
                     "o[d] += p * kv_elem(v_pages, kv_fp8, k_scale, off + d);"),
     "merge_lse": ("const double l = M + log(exp(a - M) + exp(b - M));",
@@ -68,7 +70,10 @@ def _checks():
           pins.test_kv_len_and_malformed_tables,
           pins.test_e4m3_decoder_matches_torch_and_closed_forms,
           lambda: pins.test_kv8_equals_attention_over_the_decoded_values(dict()),
-          pins.test_kv8_scales_apply_to_keys_and_values]
+          pins.test_kv8_scales_apply_to_keys_and_values,
+          pins.test_window_of_one_sees_only_its_own_key,
+          lambda: pins.test_window_equals_masking_older_keys(5),
+          pins.test_window_causal_rows_equal_decode_with_window]
     return c
 
 

@@ -63,6 +63,7 @@ class Paged:
     v_codes: torch.Tensor | None = None
     k_scale: float = 1.0
     v_scale: float = 1.0
+    window_left: int = 0          # sliding window (0: none)
 
     @property
     def batch(self) -> int:
@@ -70,7 +71,12 @@ class Paged:
 
     @property
     def active_tokens(self) -> int:
-        return int(sum(self.kv_len))
+        """Keys some query attends: the whole history, or with a sliding window the
+        union of the request's windows."""
+        if self.window_left <= 0:
+            return int(sum(self.kv_len))
+        n = (self.qo_indptr[1:] - self.qo_indptr[:-1]).tolist()
+        return int(sum(L - max(0, L - q - self.window_left + 1) for L, q in zip(self.kv_len, n)))
 
 
 @dataclass
@@ -295,6 +301,61 @@ def with_kv8(w: Paged, seed: int, spread: float = 16.0) -> Paged:
     return w
 
 
+def sliding_window_decode(name, seed, lens, window, *, Hq, Hk, D, P, qo_lens=None,
+                          causal=True) -> Paged:
+    """Long requests attended through a sliding window of ``window`` keys.  Only the
+    pages that hold a key some query may see get pool pages of their own (values
+    N(0, 1) in bf16); every older page of a request points at one shared page poisoned
+    with NaN, so the pool stays small and a read outside the window shows as NaN."""
+    g = torch.Generator().manual_seed(seed)
+    B = len(lens)
+    qo_lens = [1] * B if qo_lens is None else list(qo_lens)
+    counts, first_live, last = [], [], []
+    for L, n in zip(lens, qo_lens):
+        npg = (L + P - 1) // P
+        lo = max(0, L - n - window + 1)             # first key any of the request's rows sees
+        counts.append(npg)
+        first_live.append(lo // P)
+        last.append(L - (npg - 1) * P if npg else 0)
+    live = sum(c - f for c, f in zip(counts, first_live))
+    pool = live + 1                                 # page 0: the shared poisoned page
+    perm = (torch.randperm(live, generator=g) + 1).to(torch.int32).tolist()
+    indices, k = [], 0
+    for c, f in zip(counts, first_live):
+        indices += [0] * f + perm[k:k + c - f]
+        k += c - f
+    indptr = torch.zeros(B + 1, dtype=torch.int32)
+    indptr[1:] = torch.cumsum(torch.tensor(counts, dtype=torch.int64), 0).to(torch.int32)
+    qo_indptr = torch.zeros(B + 1, dtype=torch.int32)
+    qo_indptr[1:] = torch.cumsum(torch.tensor(qo_lens, dtype=torch.int64), 0).to(torch.int32)
+    q = _bf16(torch.randn(int(qo_indptr[-1]), Hq, D, generator=g))
+    kp = _fill_pool(pool, Hk, P, D, g)
+    vp = _fill_pool(pool, Hk, P, D, g)
+    w = Paged(name=name, num_qo_heads=Hq, num_kv_heads=Hk, head_dim=D, page_size=P,
+              num_pages=pool, indptr=indptr, indices=torch.tensor(indices, dtype=torch.int32),
+              last_page_len=torch.tensor(last, dtype=torch.int32), qo_indptr=qo_indptr,
+              kv_len=list(lens), q=q, k_pages=kp, v_pages=vp, sm_scale=1.0 / math.sqrt(D),
+              causal=causal, window_left=window)
+    _poison_unused(w)                 # unused slots of the last pages
+    for t in (w.k_pages, w.v_pages):
+        t.view(torch.int16)[0] = NAN_BF16
+    return w
+
+
+def config7(small: bool = False) -> Paged:
+    """Sliding-window decode: long histories, each query sees its last 2048 keys."""
+    g = torch.Generator().manual_seed(1007)
+    if small:
+        B, lens_, window = 12, (300, 2500), 257
+        name = "sliding_window_decode_small"
+    else:
+        B, lens_, window = 64, (8192, 32768), 2048
+        name = "sliding_window_decode_b64_w2048"
+    lens = torch.randint(lens_[0], lens_[1] + 1, (B,), generator=g).tolist()
+    return sliding_window_decode(name, 2007 if small else 3007, lens, window, Hq=32, Hk=8,
+                                 D=128, P=16)
+
+
 def config6(small: bool = False) -> Paged:
     """The skewed block-sparse decode with an FP8 (E4M3) KV cache."""
     return with_kv8(config3(small), 1006)
@@ -303,7 +364,7 @@ def config6(small: bool = False) -> Paged:
 def by_name(cfg: int, small: bool = False):
     return {1: lambda: config1(), 2: lambda: config2(small), 3: lambda: config3(small),
             4: lambda: config4(small), 5: lambda: config5(small),
-            6: lambda: config6(small)}[cfg]()
+            6: lambda: config6(small), 7: lambda: config7(small)}[cfg]()
 
 
 def flat_cascade(c: Cascade) -> Paged:
