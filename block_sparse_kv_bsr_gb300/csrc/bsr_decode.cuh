@@ -40,6 +40,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "bsr_internal.h"
@@ -345,6 +346,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const bool vA = g4 < ci.nrows, vB = R16 && (g4 + 8 < ci.nrows);
     const int qposA = ci.qpos0 + rA / group, qposB = ci.qpos0 + rB / group;
     const int qpos_min = ci.qpos0 + ci.row0 / group;
+    // sliding window: row r sees keys >= its position - window_left + 1; the last
+    // row's bound is the highest, so a stage at or above it is unmasked for all rows
+    const int wlo_A = p.window_left > 0 ? qposA - p.window_left + 1 : INT_MIN;
+    const int wlo_B = p.window_left > 0 ? qposB - p.window_left + 1 : INT_MIN;
+    const int wlo_max = p.window_left > 0
+                            ? ci.qpos0 + (ci.row0 + ci.nrows - 1) / group - p.window_left + 1
+                            : INT_MIN;
+    const int wlo_min = p.window_left > 0 ? qpos_min - p.window_left + 1 : INT_MIN;
 
     // q fragments (A operand): regs [0] and [NR/2] hold row g4 (columns 2t4.. and
     // 8+2t4..); with R16 regs [1] and [3] hold row g4 + 8.
@@ -420,10 +429,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         for (int idx = lane; idx < nvalid * (D / 8); idx += 32) {
           const int t = idx / (D / 8), c = idx % (D / 8);
           const int key = tok + t;
-          const int page = __ldg(p.indices + ci.page_base + (key >> log2P));
-          const size_t off = (size_t(page * p.Hk + ci.kvh) * p.P + (key & (p.P - 1))) * D + c * 8;
-          const uint4 kv = __ldg(reinterpret_cast<const uint4*>(kp + off));
-          const uint4 vv = __ldg(reinterpret_cast<const uint4*>(vp + off));
+          uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
+          // keys older than every row's window: their page may be recycled, not read
+          if (key >= wlo_min) {
+            const int page = __ldg(p.indices + ci.page_base + (key >> log2P));
+            const size_t off =
+                (size_t(page * p.Hk + ci.kvh) * p.P + (key & (p.P - 1))) * D + c * 8;
+            kv = __ldg(reinterpret_cast<const uint4*>(kp + off));
+            vv = __ldg(reinterpret_cast<const uint4*>(vp + off));
+          }
           const uint32_t to = tile_off(t, c * 8);
           asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(kt + to), "r"(kv.x),
                        "r"(kv.y), "r"(kv.z), "r"(kv.w)
@@ -517,8 +531,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
       // ---------------- mask + online softmax (log2 domain)
       // s*[0..1]: row g4, keys tok + {0,8} + 2t4 + {0,1};  s*[2..3]: row g4 + 8
-      const bool full =
-          (nvalid == kStageTokens) && (!p.causal || tok + kStageTokens - 1 <= qpos_min);
+      const bool full = (nvalid == kStageTokens) &&
+                        (!p.causal || tok + kStageTokens - 1 <= qpos_min) && tok >= wlo_max;
       float xa[4], xb[4];
       {
         // with RoPE both operands carry 2^-4
@@ -531,8 +545,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const bool inr = full || (kidx[j] < ci.tok1);
-          const bool okA = full || (inr && (!p.causal || kidx[j] <= qposA));
-          const bool okB = full || (inr && (!p.causal || kidx[j] <= qposB));
+          const bool okA = full || (inr && (!p.causal || kidx[j] <= qposA) && kidx[j] >= wlo_A);
+          const bool okB = full || (inr && (!p.causal || kidx[j] <= qposB) && kidx[j] >= wlo_B);
           xa[j] = okA ? sa[j] * sc : -INFINITY;
           xb[j] = okB ? sb[j] * sc : -INFINITY;
         }

@@ -29,6 +29,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "bsr_decode.cuh"
@@ -171,6 +172,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const bool vA = g4 < ci.nrows, vB = R16 && (g4 + 8 < ci.nrows);
     const int qposA = ci.qpos0 + rA / group, qposB = ci.qpos0 + rB / group;
     const int qpos_min = ci.qpos0 + ci.row0 / group;
+    // sliding window: row r sees keys >= its position - window_left + 1; the last
+    // row's bound is the highest, so a stage at or above it is unmasked for all rows
+    const int wlo_A = p.window_left > 0 ? qposA - p.window_left + 1 : INT_MIN;
+    const int wlo_B = p.window_left > 0 ? qposB - p.window_left + 1 : INT_MIN;
+    const int wlo_max = p.window_left > 0
+                            ? ci.qpos0 + (ci.row0 + ci.nrows - 1) / group - p.window_left + 1
+                            : INT_MIN;
 
     // q fragments in fp16, head dims of block kb in the order 4t..4t+3:
     // [kb][0] = row g4 dims 4t, 4t+1; [kb][NR/2] = row g4 dims 4t+2, 4t+3;
@@ -245,8 +253,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       }
 
       // ---------------- mask + online softmax (log2 domain; k_scale is in scale_log2)
-      const bool full =
-          (nvalid == kStageTokens) && (!p.causal || tok + kStageTokens - 1 <= qpos_min);
+      const bool full = (nvalid == kStageTokens) &&
+                        (!p.causal || tok + kStageTokens - 1 <= qpos_min) && tok >= wlo_max;
       float xa[4], xb[4];
       {
         const float sc = p.scale_log2;
@@ -257,8 +265,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const bool inr = full || (kidx[j] < ci.tok1);
-          const bool okA = full || (inr && (!p.causal || kidx[j] <= qposA));
-          const bool okB = full || (inr && (!p.causal || kidx[j] <= qposB));
+          const bool okA = full || (inr && (!p.causal || kidx[j] <= qposA) && kidx[j] >= wlo_A);
+          const bool okB = full || (inr && (!p.causal || kidx[j] <= qposB) && kidx[j] >= wlo_B);
           xa[j] = okA ? sa[j] * sc : -INFINITY;
           xb[j] = okB ? sb[j] * sc : -INFINITY;
         }

@@ -68,6 +68,7 @@ struct DecodeParams {
   int32_t Hq, Hk, group, P;
   int32_t causal, out_f32, num_warps;
   int32_t rope_max_pos;           // last row of the cos/sin table
+  int32_t window_left;            // sliding window: keys >= position - window_left + 1 (0: none)
   uint64_t wait_limit_ns;         // bound on every barrier wait
 };
 
@@ -100,6 +101,7 @@ struct PrefillParams {
   float scale_log2;
   int32_t Hq, Hk, group, P;
   int32_t causal, out_f32, out_v8, num_ctas;
+  int32_t window_left;            // sliding window (0: none)
   int32_t box_rows;               // rows per K/V box of the prefill tensor maps: min(P, 128)
   uint64_t wait_limit_ns;
 };

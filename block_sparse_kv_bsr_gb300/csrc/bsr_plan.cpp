@@ -54,6 +54,7 @@ bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 struct Unit {
   int32_t req, kvh, row0, nrows, kend;
   int32_t page_base, q_row0, qpos0;
+  int32_t kbegin;   // first key any of the rows may see (aligned down to the cut alignment)
 };
 
 struct Piece {
@@ -109,9 +110,11 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
   std::vector<int32_t> order(units.size());
   std::iota(order.begin(), order.end(), 0);
   std::stable_sort(order.begin(), order.end(),
-                   [&](int32_t x, int32_t y) { return units[x].kend > units[y].kend; });
+                   [&](int32_t x, int32_t y) {
+                     return units[x].kend - units[x].kbegin > units[y].kend - units[y].kbegin;
+                   });
   int64_t total = 0;
-  for (const Unit& u : units) total += u.kend + overhead;
+  for (const Unit& u : units) total += u.kend - u.kbegin + overhead;
   const int workers =
       units.empty() ? 0
                     : int(std::max<int64_t>(1, std::min<int64_t>(max_workers, (total + min_worker_work - 1) / min_worker_work)));
@@ -127,7 +130,7 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
     int64_t w = 0, room = T;
     for (int32_t u : order) {
       const int64_t kend = units[u].kend;
-      int64_t pos = 0;
+      int64_t pos = units[u].kbegin;
       bool placed = false;  // the piece ending at kend (an empty range still needs one)
       while (!placed) {
         const int64_t rest = kend - pos;
@@ -248,13 +251,14 @@ void balance_gangs(const std::vector<Unit>& units, int64_t num_ctas, int64_t ali
   double filled = 0.0, offered = 0.0;
   for (int g = 0; g < ngang; ++g) kGang = std::max(kGang, int(gstart[g + 1] - gstart[g]));
   for (int g = 0; g < ngang; ++g) {
-    int64_t kend = 0, sum = 0;
+    int64_t kend = 0, kbegin = INT64_MAX, sum = 0;
     for (int32_t i = gstart[g]; i < gstart[g + 1]; ++i) {
       kend = std::max<int64_t>(kend, units[i].kend);
-      sum += units[i].kend + overhead;
+      kbegin = std::min<int64_t>(kbegin, units[i].kbegin);
+      sum += units[i].kend - units[i].kbegin + overhead;
     }
     filled += double(sum);
-    offered += double(kGang) * double(kend + overhead);
+    offered += double(kGang) * double(kend - kbegin + overhead);
   }
   if (kGang == 1 || num_ctas < kGang || filled < 0.9 * offered) {
     balance(units, num_ctas, align, overhead, min_piece, min_cta_work, out);
@@ -263,7 +267,10 @@ void balance_gangs(const std::vector<Unit>& units, int64_t num_ctas, int64_t ali
   std::vector<Unit> gunits(ngang);
   for (int g = 0; g < ngang; ++g) {
     Unit u = units[gstart[g]];
-    for (int32_t i = gstart[g]; i < gstart[g + 1]; ++i) u.kend = std::max(u.kend, units[i].kend);
+    for (int32_t i = gstart[g]; i < gstart[g + 1]; ++i) {
+      u.kend = std::max(u.kend, units[i].kend);
+      u.kbegin = std::min(u.kbegin, units[i].kbegin);
+    }
     u.row0 = g;   // carried through balance() to name the gang
     gunits[g] = u;
   }
@@ -271,10 +278,11 @@ void balance_gangs(const std::vector<Unit>& units, int64_t num_ctas, int64_t ali
   balance(gunits, std::max<int64_t>(1, num_ctas / kGang), align, overhead, min_piece,
           min_cta_work, &gw);
 
-  // a member takes the part of a piece below its own key end (at least one, possibly
+  // a member takes the part of a piece inside its own key range (at least one, possibly
   // empty, piece when it has no key at all)
   auto takes = [&](const DecodeItem& gp, const Unit& u) {
-    return std::min(gp.tok1, u.kend) > gp.tok0 || u.kend == 0;
+    const int32_t lo = std::max(gp.tok0, u.kbegin), hi = std::min(gp.tok1, u.kend);
+    return hi > lo || (u.kend == u.kbegin && gp.tok0 <= u.kbegin && u.kbegin <= gp.tok1);
   };
   std::vector<int32_t> npieces(units.size(), 0);
   for (const DecodeItem& gp : gw.items)
@@ -305,8 +313,8 @@ void balance_gangs(const std::vector<Unit>& units, int64_t num_ctas, int64_t ali
         it.kvh = u.kvh;
         it.row0 = u.row0;
         it.nrows = u.nrows;
-        it.tok0 = gp.tok0;
-        it.tok1 = std::max(gp.tok0, std::min(gp.tok1, u.kend));
+        it.tok0 = std::max(gp.tok0, u.kbegin);
+        it.tok1 = std::max(it.tok0, std::min(gp.tok1, u.kend));
         it.nchunks = npieces[i];
         it.first_slot = first_slot[i];
         it.slot = it.nchunks > 1 ? first_slot[i] + next_slot[i]++ : -1;
@@ -353,13 +361,15 @@ struct HostPlan {
 int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
                    int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                    int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
-                   int32_t causal, float rope_theta, int num_sms, HostPlan* hp) {
+                   int32_t causal, int32_t window_left, float rope_theta, int num_sms,
+                   HostPlan* hp) {
   if (indptr == nullptr || batch < 0 || num_pages_in_pool < 0 || num_sms <= 0)
     return BSR_ERR_INVALID_ARGUMENT;
   if (batch > 0 && last_page_len == nullptr) return BSR_ERR_INVALID_ARGUMENT;
   if (num_qo_heads <= 0 || num_kv_heads <= 0) return BSR_ERR_INVALID_ARGUMENT;
   if (!(rope_theta >= 0.f) || !std::isfinite(rope_theta)) return BSR_ERR_INVALID_ARGUMENT;
   if (causal != 0 && causal != 1) return BSR_ERR_INVALID_ARGUMENT;
+  if (window_left < 0) return BSR_ERR_INVALID_ARGUMENT;
   if (head_dim != 64 && head_dim != 128) return BSR_ERR_UNSUPPORTED;
   if (!is_pow2(page_size) || page_size > 256) return BSR_ERR_UNSUPPORTED;
   if (num_qo_heads % num_kv_heads != 0) return BSR_ERR_UNSUPPORTED;
@@ -390,7 +400,8 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
     qo_len[b] = int32_t(nq);
     q_row0[b] = int32_t(sum_qo);
     sum_qo += nq;
-    active += L;
+    // keys some row attends: all of them, or the union of the rows' windows
+    active += window_left > 0 ? L - std::max<int64_t>(0, L - nq - window_left + 1) : L;
     max_len = std::max<int32_t>(max_len, int32_t(L));
   }
   if (sum_qo > INT32_MAX / num_qo_heads) return BSR_ERR_UNSUPPORTED;
@@ -419,7 +430,16 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
         int64_t kend = kv_len[b];
         if (causal)
           kend = std::min<int64_t>(kend, std::max<int64_t>(0, int64_t(qpos0) + (r0 + nr - 1) / group + 1));
-        const Unit unit{b, h, r0, nr, int32_t(kend), indptr[b], q_row0[b], qpos0};
+        // sliding window: the first row (the earliest position) sees the oldest key;
+        // the unit starts at the page (or 16-key stage) holding it, so pages wholly
+        // before every row's window are never read (they may have been recycled)
+        int64_t kbegin = 0;
+        if (window_left > 0) {
+          const int64_t align = std::max<int64_t>(page_size, kStageTokens);
+          kbegin = std::max<int64_t>(0, int64_t(qpos0) + r0 / group - window_left + 1);
+          kbegin = std::min(kbegin, kend) / align * align;
+        }
+        const Unit unit{b, h, r0, nr, int32_t(kend), indptr[b], q_row0[b], qpos0, int32_t(kbegin)};
         if (prefill) {
           punits.push_back(unit);
         } else {
@@ -467,7 +487,8 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
                              const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
                              int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                              const int32_t* qo_indptr, int32_t num_pages_in_pool, int32_t causal,
-                             float rope_theta, void* stream_v, bsr_schedule_t* schedule) {
+                             int32_t window_left, float rope_theta, void* stream_v,
+                             bsr_schedule_t* schedule) {
   if (schedule == nullptr) return BSR_ERR_INVALID_ARGUMENT;
   const cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const bool rope = rope_theta > 0.f;
@@ -479,7 +500,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   HostPlan hp;
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
-                                rope_theta, num_sms, &hp);
+                                window_left, rope_theta, num_sms, &hp);
   if (rc != BSR_OK) return rc;
   const int64_t nnz = indptr[batch];
 
@@ -633,6 +654,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->P = page_size;
   s->group = hp.group;
   s->causal = causal;
+  s->window_left = window_left;
   s->rope_theta = rope_theta;
   s->num_pages = num_pages_in_pool;
   s->sum_qo = hp.sum_qo;
@@ -709,6 +731,7 @@ extern "C" int bsr_schedule_get_info(bsr_schedule_t s, bsr_schedule_info_t* info
   info->head_dim = s->D;
   info->page_size = s->P;
   info->causal = s->causal;
+  info->window_left = s->window_left;
   info->rope_theta = s->rope_theta;
   info->sum_qo = s->sum_qo;
   info->active_tokens = s->active_tokens;
@@ -733,13 +756,13 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
                                   const int32_t* last_page_len, int32_t batch,
                                   int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t page_size, const int32_t* qo_indptr,
-                                  int32_t num_pages_in_pool, int32_t causal, float rope_theta,
-                                  int32_t num_sms, bsr_schedule_info_t* info, int32_t* units,
-                                  int64_t max_units) {
+                                  int32_t num_pages_in_pool, int32_t causal,
+                                  int32_t window_left, float rope_theta, int32_t num_sms,
+                                  bsr_schedule_info_t* info, int32_t* units, int64_t max_units) {
   HostPlan hp;
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
-                                rope_theta, num_sms, &hp);
+                                window_left, rope_theta, num_sms, &hp);
   if (rc != BSR_OK) return rc;
   if (info != nullptr) {
     std::memset(info, 0, sizeof(*info));
@@ -749,6 +772,7 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
     info->head_dim = head_dim;
     info->page_size = page_size;
     info->causal = causal;
+    info->window_left = window_left;
     info->rope_theta = rope_theta;
     info->sum_qo = hp.sum_qo;
     info->active_tokens = hp.active;

@@ -36,6 +36,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
 
 #include "bsr_internal.h"
@@ -472,19 +473,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < nt; ++j) {
           const int key0 = it.tok0 + kTileN * j + 64 * half;
           const int nkeys = min(64, it.tok1 - key0);                          // may be <= 0
-          const int klim = p.causal ? min(nkeys, qpos - key0 + 1) : nkeys;   // keys [0, klim) visible
+          const int klim = p.causal ? min(nkeys, qpos - key0 + 1) : nkeys;
+          // sliding window: keys [klo, klim) of this half are visible
+          const int klo = p.window_left > 0 ? qpos - p.window_left + 1 - key0 : INT_MIN;
 
           // ---- online softmax (log2 domain, lazy rescale) over this half's 64 scores,
           // read in 32-column quarters: max pass, exchange, exp2 / pack / store pass
           if (!wt.warp_wait(BAR(L::kSFull + qt), ns & 1u)) { ok = false; break; }
           ++ns;
           umma::fence_after_sync();
-          const bool masked = __any_sync(0xffffffffu, klim < 64);
+          const bool masked = __any_sync(0xffffffffu, klim < 64 || klo > 0);
           auto load_quarter = [&](int qq, float (&sv)[32]) {
             umma::tmem_ld32(s_t + 32 * qq, sv);
             if (masked) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) sv[i] = 32 * qq + i < klim ? sv[i] : -INFINITY;
+              for (int i = 0; i < 32; ++i)
+                sv[i] = (32 * qq + i < klim && 32 * qq + i >= klo) ? sv[i] : -INFINITY;
             }
           };
           float mpart = -INFINITY;

@@ -227,6 +227,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.out_f32 = out_dtype == BSR_DTYPE_F32;
     p.num_warps = s->dec_warps;
     p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
+    p.window_left = s->window_left;
     p.wait_limit_ns = wait_limit_ns;
     const bool r16 = s->max_rows > 8;
     t_mark(0, 0);
@@ -322,6 +323,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.out_f32 = out_dtype == BSR_DTYPE_F32;
     p.out_v8 = aligned(out, 32);
     p.num_ctas = s->pre_ctas;
+    p.window_left = s->window_left;
     p.wait_limit_ns = wait_limit_ns;
     t_mark(2, 0);
     cudaError_t e =
@@ -462,6 +464,7 @@ extern "C" int bsr_attn_run_kv8(bsr_schedule_t s, const void* q, const void* k_p
   p.out_f32 = out_dtype == BSR_DTYPE_F32;
   p.num_warps = s->dec_warps;
   p.rope_max_pos = 0;
+  p.window_left = s->window_left;
   p.wait_limit_ns = 1000000000ull;
   t_mark(0, 0);
   const cudaError_t e = bsr::launch_decode_kv8(s->max_rows > 8, s->tm_k8, s->tm_v8, p,

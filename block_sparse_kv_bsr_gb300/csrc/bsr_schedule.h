@@ -20,6 +20,7 @@ struct bsr_schedule {
   int32_t num_pages = 0;
   int64_t sum_qo = 0, active_tokens = 0;
   int32_t rope_rows = 0;       // rows of the cos/sin table (0 without RoPE)
+  int32_t window_left = 0;     // sliding window (0: none)
   int32_t max_rows = 0;        // largest packed-row count of one decode unit
 
   // decode plan

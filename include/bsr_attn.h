@@ -83,9 +83,18 @@ typedef struct bsr_schedule* bsr_schedule_t;
  * page_size for non-empty requests, qo_len <= kv_len when causal or RoPE),
  * cuts every (request, kv head) key range into page-aligned chunks, spreads
  * the chunks over persistent warps at equal cost (long sequences cut and
- * interleaved with short ones), and uploads the page table, the work lists,
- * zeroed merge counters and (rope_theta > 0) an fp32 cos/sin table built in
- * fp64 with ONE asynchronous host-to-device copy on `stream`.
+ * interleaved with short ones), and uploads the page table, the work lists and
+ * zeroed merge counters with ONE asynchronous host-to-device copy on `stream`;
+ * with rope_theta > 0 an fp32 cos/sin table built in fp64 goes to its own
+ * device buffer, uploaded only when theta or head_dim change or the longest
+ * request outgrows it.
+ *
+ * window_left >= 0: 0 attends every key; W > 0 is the sliding-window variant
+ * ("JIT 컴파일은 …": Sliding Window among the fused variants) -- a query at
+ * position p sees keys p - W + 1 .. p (and causal still bounds it above).  The
+ * planner starts each work unit at the oldest key any of its rows sees, so
+ * pages wholly older than every window are never read.  The window is part of
+ * the schedule (reported in bsr_schedule_info_t.window_left).
  *
  * *schedule must be NULL (a new schedule is created) or a schedule returned
  * by an earlier plan, which is then re-planned in place: its device workspace
@@ -97,7 +106,8 @@ typedef struct bsr_schedule* bsr_schedule_t;
 int bsr_attn_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
                   int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                   int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
-                  int32_t causal, float rope_theta, void* stream, bsr_schedule_t* schedule);
+                  int32_t causal, int32_t window_left, float rope_theta, void* stream,
+                  bsr_schedule_t* schedule);
 
 /*
  * bsr_attn_run — execute a schedule: out = softmax(sm_scale * q k^T) v and
@@ -196,7 +206,7 @@ typedef struct bsr_schedule_info {
   double prefill_imbalance;   /* max / mean planned cost over prefill CTAs */
   int32_t kernels_per_run;    /* kernels one bsr_attn_run launches (decode, RoPE pre-pass,
                                  prefill, split-range merge; 0 when there is no work) */
-  int32_t reserved;
+  int32_t window_left;        /* sliding window given to plan (0: none) */
 } bsr_schedule_info_t;
 
 int bsr_schedule_get_info(bsr_schedule_t schedule, bsr_schedule_info_t* info);
@@ -235,8 +245,8 @@ int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
                        const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
                        int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                        const int32_t* qo_indptr, int32_t num_pages_in_pool, int32_t causal,
-                       float rope_theta, int32_t num_sms, bsr_schedule_info_t* info,
-                       int32_t* units, int64_t max_units);
+                       int32_t window_left, float rope_theta, int32_t num_sms,
+                       bsr_schedule_info_t* info, int32_t* units, int64_t max_units);
 
 /*
  * bsr_attn_decode_noalloc — decode attention that allocates nothing.

@@ -32,6 +32,7 @@ def plan(w: wl.Paged, schedule=None):
                              num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
                              head_dim=w.head_dim, page_size=w.page_size, num_pages=w.num_pages,
                              qo_indptr=w.qo_indptr, causal=w.causal, rope_theta=w.rope_theta,
+                             window_left=w.window_left,
                              schedule=schedule)
 
 

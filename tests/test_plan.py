@@ -19,7 +19,7 @@ def plan_of(w: wl.Paged, num_sms=152):
         w.indptr, w.indices, w.last_page_len, num_qo_heads=w.num_qo_heads,
         num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, page_size=w.page_size,
         num_pages=w.num_pages, num_sms=num_sms, qo_indptr=w.qo_indptr, causal=w.causal,
-        rope_theta=w.rope_theta)
+        rope_theta=w.rope_theta, window_left=w.window_left)
 
 
 def is_prefill(w: wl.Paged, b: int) -> bool:
@@ -40,7 +40,8 @@ def check_coverage(w: wl.Paged, units: np.ndarray):
         step = 256 if warp < 0 else 16
         assert is_prefill(w, req) == (warp < 0)
         assert 1 <= nrows <= step
-        align = max(w.page_size, 128 if warp < 0 else 16)
+        # prefill cuts fall on 128-key tiles, a windowed start on its page (or 16 keys)
+        align = max(w.page_size, 128 if warp < 0 and w.window_left == 0 else 16)
         assert tok0 % align == 0
         ranges.setdefault((req, kvh, row0, nrows), []).append((tok0, tok1, slot))
     for b in range(w.batch):
@@ -60,9 +61,15 @@ def check_coverage(w: wl.Paged, units: np.ndarray):
                 else:
                     slots = [p[2] for p in pieces]
                     assert slots == list(range(slots[0], slots[0] + len(slots)))
-                pos = 0
+                # sliding window: from the oldest key the first row sees, aligned down
+                kbegin = 0
+                if w.window_left > 0:
+                    align = max(w.page_size, 16)
+                    kbegin = max(0, (L - nq) + r0 // g - w.window_left + 1)
+                    kbegin = min(kbegin, kend) // align * align
+                pos = kbegin
                 for tok0, tok1, _ in pieces:
-                    assert tok0 == pos and (tok1 > tok0 or kend == 0)
+                    assert tok0 == pos and (tok1 > tok0 or kend == kbegin)
                     pos = tok1
                 assert pos == kend
     assert not ranges, "units for ranges that do not exist"
@@ -129,3 +136,43 @@ def test_plan_is_deterministic():
     a = plan_of(w, num_sms=16)[1]
     b = plan_of(w, num_sms=16)[1]
     assert np.array_equal(a, b)
+
+
+def test_sliding_window_plans_only_the_window():
+    w = wl.config7(small=True)
+    info, units = plan_of(w, num_sms=8)
+    check_coverage(w, units)
+    assert info["window_left"] == w.window_left
+    assert info["active_tokens"] == w.active_tokens < sum(w.kv_len)
+    planned = int((units[:, 5] - units[:, 4]).sum()) // w.num_kv_heads
+    # at most one page (aligned down) more than the window per request
+    assert planned <= w.active_tokens + w.batch * max(w.page_size, 16)
+    # no planned key lies on the poisoned page every older page points at
+    for req, kvh, row0, nrows, tok0, tok1, slot, warp in units.tolist():
+        first = int(w.indptr[req]) + tok0 // w.page_size
+        last = int(w.indptr[req]) + (tok1 - 1) // w.page_size
+        assert (w.indices[first:last + 1] != 0).all()
+
+
+def test_sliding_window_prefill_units():
+    w = wl.make_paged("swpf", 31, [3000, 900], Hq=32, Hk=8, D=128, P=16, qo_lens=[300, 1],
+                      causal=True)
+    w.window_left = 700
+    info, units = plan_of(w, num_sms=16)
+    assert info["num_prefill_items"] > 0
+    check_coverage(w, units)
+
+
+def test_negative_window_is_refused():
+    w = wl.config1()
+    with pytest.raises(bsr.BsrError):
+        bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len, num_qo_heads=w.num_qo_heads,
+                               num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                               page_size=w.page_size, num_pages=w.num_pages, num_sms=8,
+                               qo_indptr=w.qo_indptr, window_left=-1)
+
+
+def test_sliding_window_small_pages():
+    w = wl.sliding_window_decode("swp4", 32, [300, 700, 45], 37, Hq=8, Hk=2, D=64, P=4)
+    info, units = plan_of(w, num_sms=4)
+    check_coverage(w, units)

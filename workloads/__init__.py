@@ -298,6 +298,9 @@ def with_kv8(w: Paged, seed: int, spread: float = 16.0) -> Paged:
     w.k_scale = w.v_scale = 1.0 / spread
     w.name = w.name + "_kv_e4m3"
     _poison_unused(w)
+    for bf, codes in ((w.k_pages, w.k_codes), (w.v_pages, w.v_codes)):
+        dead = torch.isnan(bf.float()).flatten(1).all(dim=1)    # wholly poisoned pages
+        codes[dead] = NAN_E4M3
     return w
 
 
