@@ -24,6 +24,7 @@ independent replica (weak scaling).
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import math
 import os
@@ -487,7 +488,9 @@ def main():
     if "e2e" in job:
         for _ in range(max(1, args.warmup)):
             job["e2e"]()
-        # every step ends in a host read of its result, so each is timed on its own
+        # every step ends in a host read of its result, so each is timed on its own;
+        # a collection first keeps a full garbage-collector pass out of the timed steps
+        gc.collect()
         e2e_steps = max(3, min(5 * args.steps, 100))
         times = []
         for _ in range(e2e_steps):

@@ -211,7 +211,7 @@ __device__ __forceinline__ void merge_range(const DecodeParams& p, const DecodeI
   }
 }
 
-template <int D, bool ROPE, bool R16, bool SMALLP>
+template <int D, bool ROPE, bool R16, bool SMALLP, bool WIN>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     bsr_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
@@ -348,12 +348,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const int qpos_min = ci.qpos0 + ci.row0 / group;
     // sliding window: row r sees keys >= its position - window_left + 1; the last
     // row's bound is the highest, so a stage at or above it is unmasked for all rows
-    const int wlo_A = p.window_left > 0 ? qposA - p.window_left + 1 : INT_MIN;
-    const int wlo_B = p.window_left > 0 ? qposB - p.window_left + 1 : INT_MIN;
-    const int wlo_max = p.window_left > 0
-                            ? ci.qpos0 + (ci.row0 + ci.nrows - 1) / group - p.window_left + 1
-                            : INT_MIN;
-    const int wlo_min = p.window_left > 0 ? qpos_min - p.window_left + 1 : INT_MIN;
+    // (compiled in only for WIN: the predicates cost a few percent in the hot loop)
+    const int wlo_A = WIN ? qposA - p.window_left + 1 : 0;
+    const int wlo_B = WIN ? qposB - p.window_left + 1 : 0;
+    const int wlo_max = WIN ? ci.qpos0 + (ci.row0 + ci.nrows - 1) / group - p.window_left + 1 : 0;
+    const int wlo_min = WIN ? qpos_min - p.window_left + 1 : 0;
 
     // q fragments (A operand): regs [0] and [NR/2] hold row g4 (columns 2t4.. and
     // 8+2t4..); with R16 regs [1] and [3] hold row g4 + 8.
@@ -431,7 +430,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
           const int key = tok + t;
           uint4 kv = make_uint4(0u, 0u, 0u, 0u), vv = kv;
           // keys older than every row's window: their page may be recycled, not read
-          if (key >= wlo_min) {
+          if (!WIN || key >= wlo_min) {
             const int page = __ldg(p.indices + ci.page_base + (key >> log2P));
             const size_t off =
                 (size_t(page * p.Hk + ci.kvh) * p.P + (key & (p.P - 1))) * D + c * 8;
@@ -532,7 +531,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       // ---------------- mask + online softmax (log2 domain)
       // s*[0..1]: row g4, keys tok + {0,8} + 2t4 + {0,1};  s*[2..3]: row g4 + 8
       const bool full = (nvalid == kStageTokens) &&
-                        (!p.causal || tok + kStageTokens - 1 <= qpos_min) && tok >= wlo_max;
+                        (!p.causal || tok + kStageTokens - 1 <= qpos_min) &&
+                        (!WIN || tok >= wlo_max);
       float xa[4], xb[4];
       {
         // with RoPE both operands carry 2^-4
@@ -545,8 +545,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const bool inr = full || (kidx[j] < ci.tok1);
-          const bool okA = full || (inr && (!p.causal || kidx[j] <= qposA) && kidx[j] >= wlo_A);
-          const bool okB = full || (inr && (!p.causal || kidx[j] <= qposB) && kidx[j] >= wlo_B);
+          const bool okA =
+              full || (inr && (!p.causal || kidx[j] <= qposA) && (!WIN || kidx[j] >= wlo_A));
+          const bool okB =
+              full || (inr && (!p.causal || kidx[j] <= qposB) && (!WIN || kidx[j] >= wlo_B));
           xa[j] = okA ? sa[j] * sc : -INFINITY;
           xb[j] = okB ? sb[j] * sc : -INFINITY;
         }

@@ -7,10 +7,10 @@ namespace bsr {
 namespace {
 constexpr int kMaxDevices = 64;
 
-template <bool ROPE, bool R16, bool SMALLP>
+template <bool ROPE, bool R16, bool SMALLP, bool WIN>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                        int grid, cudaStream_t stream) {
-  auto kern = bsr_decode_kernel<64, ROPE, R16, SMALLP>;
+  auto kern = bsr_decode_kernel<64, ROPE, R16, SMALLP, WIN>;
   constexpr size_t smem = ROPE ? DecodeCfg<64>::kSmemBytesRope : DecodeCfg<64>::kSmemBytes;
   // The shared-memory opt-in is per device; set it on the first launch there so
   // that later launches (including ones under stream capture) make no extra call.
@@ -33,15 +33,27 @@ cudaError_t launch_decode_d64(bool rope, bool r16, bool smallp, const CUtensorMa
                                const CUtensorMap& tv, const DecodeParams& p, int grid,
                                cudaStream_t stream) {
   const int key = (rope ? 4 : 0) | (r16 ? 2 : 0) | (smallp ? 1 : 0);
+  if (p.window_left > 0) {
+    switch (key) {
+      case 0: return launch_one<false, false, false, true>(tk, tv, p, grid, stream);
+      case 1: return launch_one<false, false, true, true>(tk, tv, p, grid, stream);
+      case 2: return launch_one<false, true, false, true>(tk, tv, p, grid, stream);
+      case 3: return launch_one<false, true, true, true>(tk, tv, p, grid, stream);
+      case 4: return launch_one<true, false, false, true>(tk, tv, p, grid, stream);
+      case 5: return launch_one<true, false, true, true>(tk, tv, p, grid, stream);
+      case 6: return launch_one<true, true, false, true>(tk, tv, p, grid, stream);
+      default: return launch_one<true, true, true, true>(tk, tv, p, grid, stream);
+    }
+  }
   switch (key) {
-    case 0: return launch_one<false, false, false>(tk, tv, p, grid, stream);
-    case 1: return launch_one<false, false, true>(tk, tv, p, grid, stream);
-    case 2: return launch_one<false, true, false>(tk, tv, p, grid, stream);
-    case 3: return launch_one<false, true, true>(tk, tv, p, grid, stream);
-    case 4: return launch_one<true, false, false>(tk, tv, p, grid, stream);
-    case 5: return launch_one<true, false, true>(tk, tv, p, grid, stream);
-    case 6: return launch_one<true, true, false>(tk, tv, p, grid, stream);
-    default: return launch_one<true, true, true>(tk, tv, p, grid, stream);
+    case 0: return launch_one<false, false, false, false>(tk, tv, p, grid, stream);
+    case 1: return launch_one<false, false, true, false>(tk, tv, p, grid, stream);
+    case 2: return launch_one<false, true, false, false>(tk, tv, p, grid, stream);
+    case 3: return launch_one<false, true, true, false>(tk, tv, p, grid, stream);
+    case 4: return launch_one<true, false, false, false>(tk, tv, p, grid, stream);
+    case 5: return launch_one<true, false, true, false>(tk, tv, p, grid, stream);
+    case 6: return launch_one<true, true, false, false>(tk, tv, p, grid, stream);
+    default: return launch_one<true, true, true, false>(tk, tv, p, grid, stream);
   }
 }
 

@@ -69,7 +69,7 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return ptx::pack_f16(ptx::bf16_lo(v), ptx::bf16_hi(v));
 }
 
-template <bool R16>
+template <bool R16, bool WIN>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     bsr_decode_kv8_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
@@ -174,11 +174,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const int qpos_min = ci.qpos0 + ci.row0 / group;
     // sliding window: row r sees keys >= its position - window_left + 1; the last
     // row's bound is the highest, so a stage at or above it is unmasked for all rows
-    const int wlo_A = p.window_left > 0 ? qposA - p.window_left + 1 : INT_MIN;
-    const int wlo_B = p.window_left > 0 ? qposB - p.window_left + 1 : INT_MIN;
-    const int wlo_max = p.window_left > 0
-                            ? ci.qpos0 + (ci.row0 + ci.nrows - 1) / group - p.window_left + 1
-                            : INT_MIN;
+    // (compiled in only for WIN: the predicates cost a few percent in the hot loop)
+    const int wlo_A = WIN ? qposA - p.window_left + 1 : 0;
+    const int wlo_B = WIN ? qposB - p.window_left + 1 : 0;
+    const int wlo_max = WIN ? ci.qpos0 + (ci.row0 + ci.nrows - 1) / group - p.window_left + 1 : 0;
 
     // q fragments in fp16, head dims of block kb in the order 4t..4t+3:
     // [kb][0] = row g4 dims 4t, 4t+1; [kb][NR/2] = row g4 dims 4t+2, 4t+3;
@@ -254,7 +253,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
       // ---------------- mask + online softmax (log2 domain; k_scale is in scale_log2)
       const bool full = (nvalid == kStageTokens) &&
-                        (!p.causal || tok + kStageTokens - 1 <= qpos_min) && tok >= wlo_max;
+                        (!p.causal || tok + kStageTokens - 1 <= qpos_min) &&
+                        (!WIN || tok >= wlo_max);
       float xa[4], xb[4];
       {
         const float sc = p.scale_log2;
@@ -265,8 +265,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const bool inr = full || (kidx[j] < ci.tok1);
-          const bool okA = full || (inr && (!p.causal || kidx[j] <= qposA) && kidx[j] >= wlo_A);
-          const bool okB = full || (inr && (!p.causal || kidx[j] <= qposB) && kidx[j] >= wlo_B);
+          const bool okA =
+              full || (inr && (!p.causal || kidx[j] <= qposA) && (!WIN || kidx[j] >= wlo_A));
+          const bool okB =
+              full || (inr && (!p.causal || kidx[j] <= qposB) && (!WIN || kidx[j] >= wlo_B));
           xa[j] = okA ? sa[j] * sc : -INFINITY;
           xb[j] = okB ? sb[j] * sc : -INFINITY;
         }
@@ -426,10 +428,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
 constexpr int kMaxDevices = 64;
 
-template <bool R16>
+template <bool R16, bool WIN>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                        int grid, cudaStream_t stream) {
-  auto kern = bsr_decode_kv8_kernel<R16>;
+  auto kern = bsr_decode_kv8_kernel<R16, WIN>;
   static bool opted_in[kMaxDevices] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -448,7 +450,11 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
 
 cudaError_t launch_decode_kv8(bool r16, const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, int grid, cudaStream_t stream) {
-  return r16 ? launch_one<true>(tk, tv, p, grid, stream) : launch_one<false>(tk, tv, p, grid, stream);
+  const bool win = p.window_left > 0;
+  if (r16) return win ? launch_one<true, true>(tk, tv, p, grid, stream)
+                      : launch_one<true, false>(tk, tv, p, grid, stream);
+  return win ? launch_one<false, true>(tk, tv, p, grid, stream)
+             : launch_one<false, false>(tk, tv, p, grid, stream);
 }
 
 }  // namespace bsr

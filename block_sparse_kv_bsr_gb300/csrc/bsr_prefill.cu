@@ -163,7 +163,7 @@ __device__ __forceinline__ void store_row_chunk(const PrefillParams& p, size_t o
   }
 }
 
-template <bool ROPE>
+template <bool ROPE, bool WIN>
 __global__ void __launch_bounds__(kThreads, 1)
     bsr_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -475,20 +475,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nkeys = min(64, it.tok1 - key0);                          // may be <= 0
           const int klim = p.causal ? min(nkeys, qpos - key0 + 1) : nkeys;
           // sliding window: keys [klo, klim) of this half are visible
-          const int klo = p.window_left > 0 ? qpos - p.window_left + 1 - key0 : INT_MIN;
+          // (compiled in only for WIN)
+          const int klo = WIN ? qpos - p.window_left + 1 - key0 : 0;
 
           // ---- online softmax (log2 domain, lazy rescale) over this half's 64 scores,
           // read in 32-column quarters: max pass, exchange, exp2 / pack / store pass
           if (!wt.warp_wait(BAR(L::kSFull + qt), ns & 1u)) { ok = false; break; }
           ++ns;
           umma::fence_after_sync();
-          const bool masked = __any_sync(0xffffffffu, klim < 64 || klo > 0);
+          const bool masked = __any_sync(0xffffffffu, klim < 64 || (WIN && klo > 0));
           auto load_quarter = [&](int qq, float (&sv)[32]) {
             umma::tmem_ld32(s_t + 32 * qq, sv);
             if (masked) {
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                sv[i] = (32 * qq + i < klim && 32 * qq + i >= klo) ? sv[i] : -INFINITY;
+                sv[i] = (32 * qq + i < klim && (!WIN || 32 * qq + i >= klo)) ? sv[i] : -INFINITY;
             }
           };
           float mpart = -INFINITY;
@@ -772,10 +773,10 @@ __global__ void __launch_bounds__(256) rope_prepass_kernel(const RopePrepassPara
   if (bad) atomicOr(p.error, kStatusRopeRange);
 }
 
-template <bool ROPE>
+template <bool ROPE, bool WIN>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const PrefillParams& p, int grid, cudaStream_t stream) {
-  auto kern = bsr_prefill_kernel<ROPE>;
+  auto kern = bsr_prefill_kernel<ROPE, WIN>;
   constexpr size_t smem = Smem::kDynBytes;
   static bool opted_in[64] = {};
   int dev = 0;
@@ -806,8 +807,11 @@ cudaError_t launch_rope_prepass(const RopePrepassParams& p, int num_sms, cudaStr
 cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillParams& p, int grid,
                            cudaStream_t stream) {
-  return rope ? launch_one<true>(tq, tk, tv, p, grid, stream)
-              : launch_one<false>(tq, tk, tv, p, grid, stream);
+  if (p.window_left > 0)
+    return rope ? launch_one<true, true>(tq, tk, tv, p, grid, stream)
+                : launch_one<false, true>(tq, tk, tv, p, grid, stream);
+  return rope ? launch_one<true, false>(tq, tk, tv, p, grid, stream)
+              : launch_one<false, false>(tq, tk, tv, p, grid, stream);
 }
 
 cudaError_t launch_prefill_merge(const PrefillMergeParams& p, cudaStream_t stream) {
