@@ -68,13 +68,13 @@ def _configure(lib):
         _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, _i32p,
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int64, ctypes.c_double, ctypes.c_double, ctypes.c_int32, ctypes.c_int32,
-        _i64p, _i32p, ctypes.c_int64, _f64p, _f64p, ctypes.c_int32]
+        _i32p, _i64p, _i32p, ctypes.c_int64, _f64p, _f64p, ctypes.c_int32]
     lib.oracle_attention_kv8.restype = ctypes.c_int
     lib.oracle_attention_kv8.argtypes = [
         _u16p, _u8p, _u8p, ctypes.c_double, ctypes.c_double, _i32p, _i32p, _i32p, _i32p,
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int64, ctypes.c_double, ctypes.c_double, ctypes.c_int32, ctypes.c_int32,
-        _i64p, _i32p, ctypes.c_int64, _f64p, _f64p, ctypes.c_int32]
+        _i32p, _i64p, _i32p, ctypes.c_int64, _f64p, _f64p, ctypes.c_int32]
     lib.oracle_e4m3.restype = ctypes.c_double
     lib.oracle_e4m3.argtypes = [ctypes.c_uint8]
     lib.oracle_merge_states.restype = None
@@ -166,7 +166,8 @@ def e4m3(codes) -> np.ndarray:
 def attention(q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr, *,
               num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
               sm_scale: float, rope_theta: float = 0.0, causal: bool = False,
-              window_left: int = 0, rows=None, heads=None, threads: int | None = None):
+              window_left: int = 0, page_pos=None, rows=None, heads=None,
+              threads: int | None = None):
     """Exact (fp64) attention over a paged KV cache.
 
     ``q`` is bf16 [sum_qo, Hq, D]; ``k_pages``/``v_pages`` are bf16
@@ -177,28 +178,31 @@ def attention(q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr, *,
     arrays are reshaped to ``[sum_qo, Hq, D]`` and ``[sum_qo, Hq]``.
     ``window_left`` > 0 restricts a query at position p to keys p - window_left + 1 .. p
     (sliding window; with causal the upper bound is p, else the request's end).
+    ``page_pos`` (int32 [len(indices)]): logical position of each page's first token,
+    for RoPE over caches whose dropped blocks leave gaps (default: the cached order).
     """
     return _attention(None, q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr,
                       num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, rope_theta,
-                      causal, window_left, rows, heads, threads)
+                      causal, window_left, page_pos, rows, heads, threads)
 
 
 def attention_kv8(q, k_pages, v_pages, k_scale: float, v_scale: float, indptr, indices,
                   last_page_len, qo_indptr, *, num_qo_heads: int, num_kv_heads: int,
                   head_dim: int, page_size: int, sm_scale: float, rope_theta: float = 0.0,
-                  causal: bool = False, window_left: int = 0, rows=None, heads=None,
-                  threads: int | None = None):
+                  causal: bool = False, window_left: int = 0, page_pos=None, rows=None,
+                  heads=None, threads: int | None = None):
     """:func:`attention` over an FP8 KV cache: ``k_pages``/``v_pages`` hold E4M3
     codes (uint8, same layout) and the keys / values are ``k_scale * code`` and
     ``v_scale * code``."""
     return _attention((float(k_scale), float(v_scale)), q, k_pages, v_pages, indptr, indices,
                       last_page_len, qo_indptr, num_qo_heads, num_kv_heads, head_dim,
-                      page_size, sm_scale, rope_theta, causal, window_left, rows, heads, threads)
+                      page_size, sm_scale, rope_theta, causal, window_left, page_pos, rows, heads,
+                      threads)
 
 
 def _attention(kv8, q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr,
                num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, rope_theta, causal,
-               window_left, rows, heads, threads):
+               window_left, page_pos, rows, heads, threads):
     lib = _load()
     qb = _bits(q)
     if kv8 is None:
@@ -221,9 +225,15 @@ def _attention(kv8, q, k_pages, v_pages, indptr, indices, last_page_len, qo_indp
     lse = np.zeros((n,), dtype=np.float64)
     if len(ix) == 0:
         ix = np.zeros((1,), dtype=np.int32)
+    pp = None
+    if page_pos is not None:
+        pp = _i32(page_pos)
+        if len(pp) != len(ix) and not (len(pp) == 0 and int(ip[-1]) == 0):
+            raise ValueError("page_pos needs one entry per page-table entry")
     table = (_ptr(ip, _i32p), _ptr(ix, _i32p), _ptr(lp, _i32p) if len(lp) else None,
              _ptr(qi, _i32p), batch, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
-             float(sm_scale), float(rope_theta), int(bool(causal)), int(window_left), srp, shp, n,
+             float(sm_scale), float(rope_theta), int(bool(causal)), int(window_left),
+             _ptr(pp, _i32p) if pp is not None else None, srp, shp, n,
              _ptr(out, _f64p), _ptr(lse, _f64p), int(threads or default_threads()))
     if kv8 is None:
         rc = lib.oracle_attention(_ptr(qb, _u16p), _ptr(kb, _u16p), _ptr(vb, _u16p), *table)

@@ -142,7 +142,7 @@ static int attention_impl(const uint16_t* q, const void* k_pages, const void* v_
                           int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                           int32_t head_dim, int32_t page_size, int64_t num_pages,
                           double sm_scale, double rope_theta, int32_t causal,
-                          int32_t window_left,
+                          int32_t window_left, const int32_t* page_pos,
                           const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
                           double* out, double* lse, int32_t num_threads) {
   const int32_t D = head_dim, P = page_size, Hq = num_qo_heads, Hk = num_kv_heads;
@@ -184,9 +184,18 @@ static int attention_impl(const uint16_t* q, const void* k_pages, const void* v_
       const int64_t qo_len = (int64_t)qo_indptr[b + 1] - qo_indptr[b];
       const int64_t qpos = L - qo_len + (t - qo_indptr[b]);
       const int32_t kvh = h / group;
+      /* RoPE positions: the key index j, or with page_pos (per-page logical
+       * position of its first token, for caches whose dropped blocks leave gaps)
+       * page_pos[page entry] + j mod P; the queries follow the last cached token,
+       * at page_pos[last] + last_page_len - qo_len + i.  Causal and window masks
+       * use the cached order (the two agree while page positions increase). */
+      const int64_t qlog = (page_pos && L > 0)
+                               ? (int64_t)page_pos[indptr[b + 1] - 1] + last_page_len[b] - qo_len +
+                                     (t - qo_indptr[b])
+                               : qpos;
       for (int32_t d = 0; d < D; ++d)
         qv[d] = bf16_bits_to_double(q[(t * Hq + h) * (int64_t)D + d]);
-      if (rope_theta > 0.0) rope_rotate(qv, D, (double)qpos, rope_theta);
+      if (rope_theta > 0.0) rope_rotate(qv, D, (double)qlog, rope_theta);
       if (L > scores_cap) {
         free(scores);
         scores_cap = L;
@@ -202,7 +211,10 @@ static int attention_impl(const uint16_t* q, const void* k_pages, const void* v_
         const int64_t page = indices[indptr[b] + j / P];
         const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;
         for (int32_t d = 0; d < D; ++d) kv[d] = kv_elem(k_pages, kv_fp8, k_scale, off + d);
-        if (rope_theta > 0.0) rope_rotate(kv, D, (double)j, rope_theta);
+        if (rope_theta > 0.0) {
+          const int64_t kpos = page_pos ? (int64_t)page_pos[indptr[b] + j / P] + j % P : j;
+          rope_rotate(kv, D, (double)kpos, rope_theta);
+        }
         double dot = 0.0;
         for (int32_t d = 0; d < D; ++d) dot += qv[d] * kv[d];
         scores[j] = sm_scale * dot;
@@ -237,12 +249,12 @@ int oracle_attention(const uint16_t* q, const uint16_t* k_pages, const uint16_t*
                      int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                      int32_t head_dim, int32_t page_size, int64_t num_pages,
                      double sm_scale, double rope_theta, int32_t causal, int32_t window_left,
-                     const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
+                     const int32_t* page_pos, const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
                      double* out, double* lse, int32_t num_threads) {
   return attention_impl(q, k_pages, v_pages, 0, 1.0, 1.0, indptr, indices, last_page_len,
                         qo_indptr, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                        num_pages, sm_scale, rope_theta, causal, window_left, sel_rows,
-                        sel_heads, num_sel, out, lse, num_threads);
+                        num_pages, sm_scale, rope_theta, causal, window_left, page_pos,
+                        sel_rows, sel_heads, num_sel, out, lse, num_threads);
 }
 
 /* The same attention over an FP8 (E4M3) KV cache: K = k_scale * code,
@@ -254,13 +266,13 @@ int oracle_attention_kv8(const uint16_t* q, const uint8_t* k_pages, const uint8_
                          int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                          int32_t head_dim, int32_t page_size, int64_t num_pages,
                          double sm_scale, double rope_theta, int32_t causal,
-                         int32_t window_left,
+                         int32_t window_left, const int32_t* page_pos,
                          const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
                          double* out, double* lse, int32_t num_threads) {
   return attention_impl(q, k_pages, v_pages, 1, k_scale, v_scale, indptr, indices,
                         last_page_len, qo_indptr, batch, num_qo_heads, num_kv_heads, head_dim,
                         page_size, num_pages, sm_scale, rope_theta, causal, window_left,
-                        sel_rows, sel_heads, num_sel, out, lse, num_threads);
+                        page_pos, sel_rows, sel_heads, num_sel, out, lse, num_threads);
 }
 
 /*

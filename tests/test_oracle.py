@@ -637,3 +637,69 @@ def test_window_workload_reads_nothing_outside_the_window():
     assert int((w.indices == 0).sum()) > 0          # pages aliased to the poisoned page
     o, l = run_oracle(w, window_left=w.window_left)
     assert np.isfinite(o).all() and np.isfinite(l).all()
+
+
+# ---------------------------------------------------------------- per-page positions
+
+def _dense_with_positions(w: wl.Paged):
+    """Dense torch fp64 attention with RoPE at the logical positions w.page_pos gives."""
+    Hq, Hk, D, P = w.num_qo_heads, w.num_kv_heads, w.head_dim, w.page_size
+    g = Hq // Hk
+    q = w.q.to(torch.float64)
+    kp, vp = w.k_pages.to(torch.float64), w.v_pages.to(torch.float64)
+    outs, lses = [], []
+    for b in range(w.batch):
+        e0, e1 = int(w.indptr[b]), int(w.indptr[b + 1])
+        pages = w.indices[e0:e1].long()
+        L = w.kv_len[b]
+        K = kp[pages].permute(1, 0, 2, 3).reshape(Hk, -1, D)[:, :L]
+        V = vp[pages].permute(1, 0, 2, 3).reshape(Hk, -1, D)[:, :L]
+        kpos = (w.page_pos[e0:e1].long()[:, None] + torch.arange(P)[None, :]).reshape(-1)[:L]
+        qb = q[w.qo_indptr[b]:w.qo_indptr[b + 1]]
+        n = qb.shape[0]
+        qlog = int(w.page_pos[e1 - 1]) + int(w.last_page_len[b]) - n + torch.arange(n)
+        qb = _rope_complex(qb, qlog[:, None].expand(n, Hq), w.rope_theta)
+        K = _rope_complex(K, kpos[None, :].expand(Hk, L), w.rope_theta)
+        s = torch.einsum("nhd,hld->nhl", qb, K.repeat_interleave(g, dim=0)) * w.sm_scale
+        if w.causal:
+            keep = torch.arange(L)[None, :] <= torch.arange(L - n, L)[:, None]
+            s = s.masked_fill(~keep[:, None, :], -math.inf)
+        outs.append(torch.einsum("nhl,hld->nhd", torch.softmax(s, -1),
+                                 V.repeat_interleave(g, dim=0)))
+        lses.append(torch.logsumexp(s, -1))
+    return torch.cat(outs).numpy(), torch.cat(lses).numpy()
+
+
+def test_identity_page_positions_change_nothing():
+    w = tiny(rope_theta=300.0, qo_lens=[1, 3, 5, 2], causal=True)
+    ident = torch.cat([torch.arange(int(w.indptr[b + 1] - w.indptr[b])) * w.page_size
+                       for b in range(w.batch)]).to(torch.int32)
+    o, l = run_oracle(w)
+    o2, l2 = run_oracle(w, page_pos=ident)
+    assert np.array_equal(o, o2) and np.array_equal(l, l2)
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(qo_lens=[1, 3, 2, 2, 4], causal=True)])
+def test_page_positions_rotate_at_the_logical_positions(kw):
+    w = tiny(lens=(30, 9, 41, 64, 70), rope_theta=500.0, drop=0.4, **kw)
+    assert w.page_pos is not None and int(w.page_pos.max()) > 0
+    o, l = run_oracle(w, page_pos=w.page_pos)
+    ro, rl = _dense_with_positions(w)
+    _close(o, ro, 1e-10)
+    _close(l, rl, 1e-10)
+    # and they matter: the cached order gives another result when blocks were dropped
+    o0, _ = run_oracle(w)
+    assert np.abs(o0 - o).max() > 1e-3
+
+
+def test_page_positions_shift_invariance():
+    # RoPE scores depend on position differences only: moving every page of a request
+    # (and hence its queries) by the same amount changes nothing
+    w = tiny(lens=(30, 9, 41), rope_theta=500.0, drop=0.4)
+    o, l = run_oracle(w, page_pos=w.page_pos)
+    shifted = w.page_pos.clone()
+    e0, e1 = int(w.indptr[1]), int(w.indptr[2])
+    shifted[e0:e1] += 1000
+    o2, l2 = run_oracle(w, page_pos=shifted)
+    _close(o, o2, 1e-9)
+    _close(l, l2, 1e-9)

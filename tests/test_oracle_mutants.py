@@ -42,6 +42,10 @@ MUTANTS = {
     "e4m3_subnormal": ("ldexp((double)m / 8.0, -6)", "ldexp((double)m / 8.0, -7)"),
     "window_off_by_one": ("j < qpos - window_left + 1)", "j < qpos - window_left)"),
     "window_from_end": ("j < qpos - window_left + 1)", "j < L - window_left)"),
+    "page_pos_keys_ignored": ("const int64_t kpos = page_pos ? (int64_t)page_pos[indptr[b] + j / P] + j % P : j;",
+                              "const int64_t kpos = j;"),
+    "page_pos_query_ignored": ("      if (rope_theta > 0.0) rope_rotate(qv, D, (double)qlog, rope_theta);",
+                               "      if (rope_theta > 0.0) rope_rotate(qv, D, (double)qpos, rope_theta);"),
     "kv8_v_scale": ("o[d] += p * kv_elem(v_pages, kv_fp8, v_scale, off + d);",
                     "o[d] += p * kv_elem(v_pages, kv_fp8, k_scale, off + d);"),
     "merge_lse": ("const double l = M + log(exp(a - M) + exp(b - M));",
@@ -73,7 +77,9 @@ def _checks():
           pins.test_kv8_scales_apply_to_keys_and_values,
           pins.test_window_of_one_sees_only_its_own_key,
           lambda: pins.test_window_equals_masking_older_keys(5),
-          pins.test_window_causal_rows_equal_decode_with_window]
+          pins.test_window_causal_rows_equal_decode_with_window,
+          lambda: pins.test_page_positions_rotate_at_the_logical_positions(dict()),
+          pins.test_page_positions_shift_invariance]
     return c
 
 

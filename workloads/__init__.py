@@ -64,6 +64,9 @@ class Paged:
     k_scale: float = 1.0
     v_scale: float = 1.0
     window_left: int = 0          # sliding window (0: none)
+    # logical position of each page-table entry's first token (int32 [len(indices)]):
+    # with dropped blocks the kept pages keep their original positions
+    page_pos: torch.Tensor | None = None
 
     @property
     def batch(self) -> int:
@@ -124,6 +127,7 @@ def _layout(lens, page_size, drop, g, pool_factor=1.25, pool_pages=None):
     last_page_len = torch.tensor([l if c > 0 else 0 for l, c in zip(last, counts)],
                                  dtype=torch.int32)
     attended = [(c - 1) * page_size + l if c > 0 else 0 for c, l in zip(counts, last)]
+    _layout.kept = kept        # logical page ordinals of the last layout (for page_pos)
     return indptr, perm, last_page_len, pool, attended
 
 
@@ -185,6 +189,9 @@ def _make_paged_g(name, g, lens, *, Hq, Hk, D, P, qo_lens=None, drop=0.0, rope_t
               qo_indptr=qo_indptr, kv_len=attended, q=q, k_pages=k, v_pages=v,
               sm_scale=sm_scale if sm_scale is not None else 1.0 / math.sqrt(D),
               rope_theta=rope_theta, causal=causal)
+    if drop > 0:
+        w.page_pos = torch.tensor([j * P for kept in _layout.kept for j in kept],
+                                  dtype=torch.int32)
     if append:
         n_new = int(qo_indptr[-1])
         w.append_indptr = qo_indptr.clone()
