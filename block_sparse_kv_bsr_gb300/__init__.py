@@ -74,12 +74,12 @@ def load(path: str | None = None):
     lib.bsr_attn_plan.restype = ctypes.c_int
     lib.bsr_attn_plan.argtypes = [_i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
-                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
-                                  _vp, ctypes.POINTER(_vp)]
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
+                                  ctypes.c_float, _vp, ctypes.POINTER(_vp)]
     lib.bsr_attn_plan_host.restype = ctypes.c_int
     lib.bsr_attn_plan_host.argtypes = [_i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
-                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
                                        ctypes.c_float, ctypes.c_int32, ctypes.POINTER(_Info),
                                        _i32p, ctypes.c_int64]
     lib.bsr_attn_run_kv8.restype = ctypes.c_int
@@ -186,13 +186,15 @@ def _plan_args(indptr, indices, last_page_len, qo_indptr):
 def bsr_attn_plan(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_heads: int,
                   head_dim: int, page_size: int, num_pages: int, qo_indptr=None,
                   causal: bool = False, rope_theta: float = 0.0, window_left: int = 0,
-                  stream=None, schedule: Schedule | None = None) -> Schedule:
+                  page_pos=None, stream=None, schedule: Schedule | None = None) -> Schedule:
     """Plan one batch from HOST page-table arrays; returns (or re-plans) a Schedule."""
     lib = load()
     keep, (ip, ix, lp, qi), batch = _plan_args(indptr, indices, last_page_len, qo_indptr)
     handle = _vp(schedule.handle if schedule is not None else None)
+    pp = None if page_pos is None else _host_i32(page_pos)
     code = lib.bsr_attn_plan(ip, ix, lp, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
                              qi, int(num_pages), int(bool(causal)), int(window_left),
+                             pp.ctypes.data_as(_i32p) if pp is not None and pp.size else None,
                              float(rope_theta), _vp(_stream_ptr(stream)), ctypes.byref(handle))
     del keep
     _check(code, "bsr_attn_plan")
@@ -205,12 +207,15 @@ def bsr_attn_plan(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_h
 def bsr_attn_plan_host(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_heads: int,
                        head_dim: int, page_size: int, num_pages: int, num_sms: int,
                        qo_indptr=None, causal: bool = False, rope_theta: float = 0.0,
-                       window_left: int = 0):
+                       window_left: int = 0, page_pos=None):
     """Host-only planning for `num_sms` SMs: returns (info dict, units int32 [n, 8])."""
     lib = load()
     keep, (ip, ix, lp, qi), batch = _plan_args(indptr, indices, last_page_len, qo_indptr)
+    pp = None if page_pos is None else _host_i32(page_pos)
     args = [ip, ix, lp, batch, num_qo_heads, num_kv_heads, head_dim, page_size, qi,
-            int(num_pages), int(bool(causal)), int(window_left), float(rope_theta), int(num_sms)]
+            int(num_pages), int(bool(causal)), int(window_left),
+            pp.ctypes.data_as(_i32p) if pp is not None and pp.size else None,
+            float(rope_theta), int(num_sms)]
     info = _Info()
     n = lib.bsr_attn_plan_host(*args, ctypes.byref(info), None, 0)
     if n < 0:

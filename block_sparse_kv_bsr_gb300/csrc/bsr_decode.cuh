@@ -264,6 +264,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   // the next 32 stages of the current unit sit one per lane in `win`; the next
   // window is requested before it is needed.
   int p_it = it_begin, p_st = 0, p_nst = 0, win = 0, win_next = 0, win_base = 0;
+  // with RoPE and per-page positions: each stage's logical position, same windows
+  int wpos = 0, wpos_next = 0;
   uint32_t p_seq = 0;
   DecodeItem pi;
   auto load_window = [&](const DecodeItem& it, int ws) -> int {
@@ -271,6 +273,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     if (s < stages_of(it))
       return __ldg(p.indices + it.page_base + ((it.tok0 + kStageTokens * s) >> log2P));
     return 0;
+  };
+  auto load_pos_window = [&](const DecodeItem& it, int ws) -> int {
+    const int s = ws + lane;
+    if (!ROPE || p.page_pos == nullptr || s >= stages_of(it)) return 0;
+    const int tok = it.tok0 + kStageTokens * s;
+    return __ldg(p.page_pos + it.page_base + (tok >> log2P)) + (tok & (p.P - 1));
   };
   auto producer_seek = [&]() {
     while (p_it < it_end) {
@@ -283,22 +291,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       win_base = 0;
       win = load_window(pi, 0);
       win_next = load_window(pi, 32);
+      if constexpr (ROPE) {
+        wpos = load_pos_window(pi, 0);
+        wpos_next = load_pos_window(pi, 32);
+      }
     }
   };
   auto producer_issue = [&]() {
     if (p_it >= it_end) return;
     const int slot = int(p_seq % C::kStages);
     const int page = __shfl_sync(0xffffffffu, win, p_st - win_base);
+    const int spos = ROPE ? __shfl_sync(0xffffffffu, wpos, p_st - win_base) : 0;
     if (lane == 0) {
       const uint32_t bar = bars + 8 * slot;
       const uint32_t dk = ring + uint32_t(slot * C::kStageBytes), dv = dk + C::kStageKBytes;
       const int tok = pi.tok0 + kStageTokens * p_st;
       const int row = (page * p.Hk + pi.kvh) * p.P + (tok & (p.P - 1));
       ptx::mbar_arrive_expect_tx(bar, C::kStageBytes + (ROPE ? C::kRopeRowBytes : 0));
-      if constexpr (ROPE)
+      if constexpr (ROPE) {
+        // the table row of the stage's first key: its index, or its logical position
+        const int rpos = p.page_pos ? spos : tok;
         ptx::bulk_load(grows + slot * C::kRopeRowBytes,
-                       reinterpret_cast<const float4*>(p.rope) + size_t(tok) * C::kRopeRowF4,
+                       reinterpret_cast<const float4*>(p.rope) + size_t(rpos) * C::kRopeRowF4,
                        C::kRopeRowBytes, bar, pol_rope);
+      }
       if constexpr (D == 128) {
         // one box per tile: both 64-column blocks, [block][16 rows][128 B]
         ptx::tma_load_3d(dk, &tm_k, bar, 0, row, 0, pol);
@@ -318,6 +334,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       win_base += 32;
       win = win_next;
       win_next = load_window(pi, win_base + 32);
+      if constexpr (ROPE) {
+        wpos = wpos_next;
+        wpos_next = load_pos_window(pi, win_base + 32);
+      }
     }
   };
 
@@ -346,6 +366,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const bool vA = g4 < ci.nrows, vB = R16 && (g4 + 8 < ci.nrows);
     const int qposA = ci.qpos0 + rA / group, qposB = ci.qpos0 + rB / group;
     const int qpos_min = ci.qpos0 + ci.row0 / group;
+    // RoPE with per-page positions: queries sit after the request's last logical key
+    const int qsh = (ROPE && p.qshift != nullptr) ? __ldg(p.qshift + ci.req) : 0;
     // sliding window: row r sees keys >= its position - window_left + 1; the last
     // row's bound is the highest, so a stage at or above it is unmasked for all rows
     // (compiled in only for WIN: the predicates cost a few percent in the hot loop)
@@ -384,7 +406,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         // rotate the (ks, ks + KH) pairs at the query positions of rows g4 / g4 + 8
 #pragma unroll
         for (int rr = 0; rr < (R16 ? 2 : 1); ++rr) {
-          const int pos = rr == 0 ? qposA : qposB;
+          const int pos = (rr == 0 ? qposA : qposB) + qsh;
           const bool ok = rr == 0 ? vA : vB;
           const int tpos = ok ? min(max(pos, 0), p.rope_max_pos) : 0;
           const float4* tab =

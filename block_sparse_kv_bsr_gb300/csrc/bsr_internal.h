@@ -57,6 +57,8 @@ struct DecodeParams {
   float* part_lse;                // [num_partials, kMaxDecodeRows] partial LSE (log2 domain)
   const int32_t* indices;         // [nnz] page ids
   const float2* rope;             // [rope rows, 4, D / 8] (cos, sin) in fragment order, or null
+  const int32_t* page_pos;        // RoPE: logical position of each page entry's first key, or null
+  const int32_t* qshift;          // RoPE with page_pos: logical minus cached end per request
   const uint16_t* q;              // bf16 [sum_qo, Hq, D]
   const void* k_pages;            // bf16 [num_pages, Hk, P, D] (read directly when P < 16)
   const void* v_pages;
@@ -130,7 +132,8 @@ struct RopePrepassParams {
   const int32_t* rk_start;        // [n + 1]
   const int32_t* rq_row0;         // [n]
   const int32_t* rq_start;        // [n + 1]
-  const int32_t* rq_pos0;         // [n]
+  const int32_t* rq_pos0;         // [n] (logical positions)
+  const int32_t* page_pos;        // logical position of each page entry's first key, or null
   const float2* rope_nat;         // [rope rows, D / 2] (cos, sin) by frequency
   uint16_t* rotk;
   uint16_t* rotq;

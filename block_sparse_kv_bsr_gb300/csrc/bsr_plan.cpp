@@ -356,13 +356,17 @@ struct HostPlan {
   // position rq_pos0)
   std::vector<int32_t> rk_off, rk_pbase, rk_start, rq_row0, rq_start, rq_pos0;
   int32_t rk_total = 0, rq_total = 0;
+  // per-page positions: logical minus cached end of each request, and one past the
+  // largest position a stage may touch (sizes the cos/sin table)
+  std::vector<int32_t> qshift;
+  int64_t max_pos_end = 0;
 };
 
 int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
                    int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                    int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
-                   int32_t causal, int32_t window_left, float rope_theta, int num_sms,
-                   HostPlan* hp) {
+                   int32_t causal, int32_t window_left, const int32_t* page_pos,
+                   float rope_theta, int num_sms, HostPlan* hp) {
   if (indptr == nullptr || batch < 0 || num_pages_in_pool < 0 || num_sms <= 0)
     return BSR_ERR_INVALID_ARGUMENT;
   if (batch > 0 && last_page_len == nullptr) return BSR_ERR_INVALID_ARGUMENT;
@@ -409,6 +413,21 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   if (nnz > 0 && indices == nullptr) return BSR_ERR_INVALID_ARGUMENT;
   for (int64_t e = 0; e < nnz; ++e)
     if (indices[e] < 0 || indices[e] >= num_pages_in_pool) return BSR_ERR_PAGE_TABLE;
+  // per-page logical positions (RoPE over caches with dropped blocks): a 16-key stage
+  // must lie inside one page, so pages of fewer than 16 keys are refused with RoPE
+  hp->qshift.assign(page_pos ? batch : 0, 0);
+  hp->max_pos_end = 0;
+  if (page_pos != nullptr) {
+    if (rope && page_size < kStageTokens) return BSR_ERR_UNSUPPORTED;
+    for (int64_t e = 0; e < nnz; ++e) {
+      if (page_pos[e] < 0 || page_pos[e] > INT32_MAX / 4) return BSR_ERR_PAGE_TABLE;
+      hp->max_pos_end = std::max<int64_t>(hp->max_pos_end, int64_t(page_pos[e]) + page_size);
+    }
+    for (int32_t b = 0; b < batch; ++b)
+      if (indptr[b + 1] > indptr[b])
+        hp->qshift[b] = int32_t(int64_t(page_pos[indptr[b + 1] - 1]) + last_page_len[b] -
+                                kv_len[b]);
+  }
 
   // ---------------------------------------------------------------- units
   // A request goes to the tensor-core prefill kernel when its packed rows fill
@@ -460,7 +479,8 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
     hp->rk_pbase.push_back(indptr[u.req]);
     hp->rk_start.push_back(hp->rk_start.back() + kv_len[u.req]);
     hp->rq_row0.push_back(q_row0[u.req]);
-    hp->rq_pos0.push_back(kv_len[u.req] - qo_len[u.req]);
+    hp->rq_pos0.push_back(kv_len[u.req] - qo_len[u.req] +
+                          (page_pos != nullptr ? hp->qshift[u.req] : 0));
     hp->rq_start.push_back(hp->rq_start.back() + qo_len[u.req]);
   }
   hp->rk_total = hp->rk_start.back();
@@ -487,8 +507,8 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
                              const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
                              int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                              const int32_t* qo_indptr, int32_t num_pages_in_pool, int32_t causal,
-                             int32_t window_left, float rope_theta, void* stream_v,
-                             bsr_schedule_t* schedule) {
+                             int32_t window_left, const int32_t* page_pos, float rope_theta,
+                             void* stream_v, bsr_schedule_t* schedule) {
   if (schedule == nullptr) return BSR_ERR_INVALID_ARGUMENT;
   const cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const bool rope = rope_theta > 0.f;
@@ -500,7 +520,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   HostPlan hp;
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
-                                window_left, rope_theta, num_sms, &hp);
+                                window_left, page_pos, rope_theta, num_sms, &hp);
   if (rc != BSR_OK) return rc;
   const int64_t nnz = indptr[batch];
 
@@ -518,8 +538,9 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   };
 
   // ---------------------------------------------------------------- RoPE tables (cached)
+  const int64_t pos_end = std::max<int64_t>(hp.max_len, hp.max_pos_end);
   const int32_t need_rows =
-      rope ? int32_t(align_up(size_t(hp.max_len), kStageTokens)) + kStageTokens : 0;
+      rope ? int32_t(align_up(size_t(pos_end), kStageTokens)) + kStageTokens : 0;
   if (rope && (s->h_rope == nullptr || s->rope_cache_theta != rope_theta ||
                s->rope_cache_D != head_dim || s->rope_cache_rows < need_rows)) {
     int64_t rows = 4096;
@@ -578,6 +599,9 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const size_t off_rq_row0 = take(rotk ? hp.rq_row0.size() * 4 : 0);
   const size_t off_rq_start = take(rotk ? hp.rq_start.size() * 4 : 0);
   const size_t off_rq_pos0 = take(rotk ? hp.rq_pos0.size() * 4 : 0);
+  const bool with_pos = page_pos != nullptr && rope;   // positions matter only for RoPE
+  const size_t off_page_pos = take(with_pos ? size_t(std::max<int64_t>(nnz, 1)) * 4 : 0);
+  const size_t off_qshift = take(with_pos ? size_t(std::max(batch, 1)) * 4 : 0);
   const size_t off_error = take(16);
   const size_t image_bytes = off;  // everything above is uploaded
   const size_t off_part_o = take(size_t(hp.dec.n_partials) * kMaxDecodeRows * head_dim * 4);
@@ -625,6 +649,10 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   if (!hp.dec.items.empty())
     std::memcpy(h + off_items, hp.dec.items.data(), hp.dec.items.size() * sizeof(DecodeItem));
   std::memcpy(h + off_warp_ptr, hp.dec.ptr.data(), hp.dec.ptr.size() * 4);
+  if (with_pos) {
+    if (nnz > 0) std::memcpy(h + off_page_pos, page_pos, size_t(nnz) * 4);
+    if (batch > 0) std::memcpy(h + off_qshift, hp.qshift.data(), size_t(batch) * 4);
+  }
   if (!hp.pre.items.empty())
     std::memcpy(h + off_pitems, hp.pre.items.data(), hp.pre.items.size() * sizeof(DecodeItem));
   std::memcpy(h + off_cta_ptr, hp.pre.ptr.data(), hp.pre.ptr.size() * 4);
@@ -700,6 +728,9 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->off_warp_ptr = off_warp_ptr;
   s->off_counters = off_counters;
   s->off_error = off_error;
+  s->off_page_pos = with_pos ? off_page_pos : 0;
+  s->off_qshift = with_pos ? off_qshift : 0;
+  s->has_page_pos = with_pos;
   s->off_part_o = off_part_o;
   s->off_part_lse = off_part_lse;
   *schedule = s;
@@ -757,12 +788,13 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
                                   int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                                   int32_t page_size, const int32_t* qo_indptr,
                                   int32_t num_pages_in_pool, int32_t causal,
-                                  int32_t window_left, float rope_theta, int32_t num_sms,
-                                  bsr_schedule_info_t* info, int32_t* units, int64_t max_units) {
+                                  int32_t window_left, const int32_t* page_pos,
+                                  float rope_theta, int32_t num_sms, bsr_schedule_info_t* info,
+                                  int32_t* units, int64_t max_units) {
   HostPlan hp;
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
-                                window_left, rope_theta, num_sms, &hp);
+                                window_left, page_pos, rope_theta, num_sms, &hp);
   if (rc != BSR_OK) return rc;
   if (info != nullptr) {
     std::memset(info, 0, sizeof(*info));

@@ -748,8 +748,11 @@ __global__ void __launch_bounds__(256) rope_prepass_kernel(const RopePrepassPara
     if (r < p.rk_total) {
       const int i = find_request(p.rk_start, p.n, r);
       const int j = r - __ldg(p.rk_start + i);
-      const int page = __ldg(p.indices + __ldg(p.rk_req_pbase + i) + j / p.P);
-      const RopeChunk t = rope_chunk(p.rope_nat + size_t(min(j, p.rope_max_pos)) * (D / 2), c);
+      const int entry = __ldg(p.rk_req_pbase + i) + j / p.P;
+      const int page = __ldg(p.indices + entry);
+      // the key's position: its index, or its page's logical position + slot
+      const int kpos = p.page_pos ? __ldg(p.page_pos + entry) + j % p.P : j;
+      const RopeChunk t = rope_chunk(p.rope_nat + size_t(min(kpos, p.rope_max_pos)) * (D / 2), c);
       const size_t head_stride = size_t(p.P) * D;
       const uint16_t* src = p.k_pages + (size_t(page) * p.Hk * p.P + (j % p.P)) * D;
       uint16_t* dst = p.rotk + size_t(r) * D;

@@ -211,6 +211,8 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.part_lse = s->dev<float>(s->off_part_lse);
     p.indices = s->dev<const int32_t>(s->off_indices);
     p.rope = rope ? reinterpret_cast<const float2*>(s->d_rope) : nullptr;
+    p.page_pos = s->has_page_pos ? s->dev<const int32_t>(s->off_page_pos) : nullptr;
+    p.qshift = s->has_page_pos ? s->dev<const int32_t>(s->off_qshift) : nullptr;
     p.q = static_cast<const uint16_t*>(q);
     p.k_pages = k_pages;
     p.v_pages = v_pages;
@@ -259,6 +261,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
       r.rq_row0 = s->dev<const int32_t>(s->off_rq_row0);
       r.rq_start = s->dev<const int32_t>(s->off_rq_start);
       r.rq_pos0 = s->dev<const int32_t>(s->off_rq_pos0);
+      r.page_pos = s->has_page_pos ? s->dev<const int32_t>(s->off_page_pos) : nullptr;
       r.rope_nat = reinterpret_cast<const float2*>(s->d_rope + s->rope_bytes);
       r.rotk = s->dev<uint16_t>(s->off_rotk);
       r.rotq = s->dev<uint16_t>(s->off_rotq);

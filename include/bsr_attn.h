@@ -96,6 +96,16 @@ typedef struct bsr_schedule* bsr_schedule_t;
  * pages wholly older than every window are never read.  The window is part of
  * the schedule (reported in bsr_schedule_info_t.window_left).
  *
+ * page_pos (HOST int32 [indptr[batch]], may be NULL): the logical position of
+ * each page-table entry's first token, for RoPE over a cache whose inactive
+ * blocks were dropped ("Block-Sparse 포맷": discarded blocks are skipped; the
+ * kept tokens keep their positions).  Key j of request b is rotated at
+ * page_pos[indptr[b] + j / P] + j % P and its queries at the positions after
+ * the last cached token, page_pos[last entry] + last_page_len - qo_len + i.
+ * NULL: positions are the cached order j.  Causal and window masks use the
+ * cached order.  Entries must be in [0, 2^29); with RoPE, page_size must be at
+ * least 16 (else BSR_ERR_UNSUPPORTED).  Without RoPE the array is not used.
+ *
  * *schedule must be NULL (a new schedule is created) or a schedule returned
  * by an earlier plan, which is then re-planned in place: its device workspace
  * is reused when large enough.  Re-planning is ordered on `stream` after work
@@ -106,8 +116,8 @@ typedef struct bsr_schedule* bsr_schedule_t;
 int bsr_attn_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
                   int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                   int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
-                  int32_t causal, int32_t window_left, float rope_theta, void* stream,
-                  bsr_schedule_t* schedule);
+                  int32_t causal, int32_t window_left, const int32_t* page_pos, float rope_theta,
+                  void* stream, bsr_schedule_t* schedule);
 
 /*
  * bsr_attn_run — execute a schedule: out = softmax(sm_scale * q k^T) v and
@@ -245,8 +255,9 @@ int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
                        const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
                        int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                        const int32_t* qo_indptr, int32_t num_pages_in_pool, int32_t causal,
-                       int32_t window_left, float rope_theta, int32_t num_sms,
-                       bsr_schedule_info_t* info, int32_t* units, int64_t max_units);
+                       int32_t window_left, const int32_t* page_pos, float rope_theta,
+                       int32_t num_sms, bsr_schedule_info_t* info, int32_t* units,
+                       int64_t max_units);
 
 /*
  * bsr_attn_decode_noalloc — decode attention that allocates nothing.

@@ -32,7 +32,7 @@ def plan(w: wl.Paged, schedule=None):
                              num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
                              head_dim=w.head_dim, page_size=w.page_size, num_pages=w.num_pages,
                              qo_indptr=w.qo_indptr, causal=w.causal, rope_theta=w.rope_theta,
-                             window_left=w.window_left,
+                             window_left=w.window_left, page_pos=w.page_pos,
                              schedule=schedule)
 
 
@@ -52,7 +52,8 @@ def oracle_full(w: wl.Paged, k_pages=None, v_pages=None):
                             w.last_page_len, w.qo_indptr, num_qo_heads=w.num_qo_heads,
                             num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                             page_size=w.page_size, sm_scale=w.sm_scale,
-                            rope_theta=w.rope_theta, causal=w.causal)
+                            rope_theta=w.rope_theta, causal=w.causal,
+                            window_left=w.window_left, page_pos=w.page_pos)
 
 
 def oracle_rows(w: wl.Paged, rows, heads, k_pages=None, v_pages=None):
@@ -61,7 +62,9 @@ def oracle_rows(w: wl.Paged, rows, heads, k_pages=None, v_pages=None):
                             w.last_page_len, w.qo_indptr, num_qo_heads=w.num_qo_heads,
                             num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                             page_size=w.page_size, sm_scale=w.sm_scale,
-                            rope_theta=w.rope_theta, causal=w.causal, rows=rows, heads=heads)
+                            rope_theta=w.rope_theta, causal=w.causal,
+                            window_left=w.window_left, page_pos=w.page_pos, rows=rows,
+                            heads=heads)
 
 
 def sample_rows(w: wl.Paged, n: int, seed: int = 0):

@@ -176,3 +176,19 @@ def test_sliding_window_small_pages():
     w = wl.sliding_window_decode("swp4", 32, [300, 700, 45], 37, Hq=8, Hk=2, D=64, P=4)
     info, units = plan_of(w, num_sms=4)
     check_coverage(w, units)
+
+
+def test_page_positions_validation():
+    w = wl.make_paged("pp", 33, [100, 300], Hq=8, Hk=2, D=64, P=8, drop=0.3, rope_theta=1e4)
+    kw = dict(num_qo_heads=8, num_kv_heads=2, head_dim=64, page_size=8, num_pages=w.num_pages,
+              num_sms=4, qo_indptr=w.qo_indptr)
+    # RoPE with positions needs pages of at least 16 keys
+    with pytest.raises(bsr.BsrError):
+        bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len, rope_theta=1e4,
+                               page_pos=w.page_pos, **kw)
+    # without RoPE they are accepted (and unused); negative positions are refused
+    bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len, page_pos=w.page_pos, **kw)
+    bad = w.page_pos.clone()
+    bad[0] = -16
+    with pytest.raises(bsr.BsrError):
+        bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len, page_pos=bad, **kw)

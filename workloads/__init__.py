@@ -366,6 +366,15 @@ def config7(small: bool = False) -> Paged:
                                  D=128, P=16)
 
 
+def config8(small: bool = False) -> Paged:
+    """The skewed block-sparse decode with RoPE (theta 5e5) at the kept blocks' logical
+    positions (``page_pos``): the same table and values as the skewed decode."""
+    w = config3(small)
+    w.rope_theta = 5e5
+    w.name = w.name + "_rope_positions"
+    return w
+
+
 def config6(small: bool = False) -> Paged:
     """The skewed block-sparse decode with an FP8 (E4M3) KV cache."""
     return with_kv8(config3(small), 1006)
@@ -374,7 +383,8 @@ def config6(small: bool = False) -> Paged:
 def by_name(cfg: int, small: bool = False):
     return {1: lambda: config1(), 2: lambda: config2(small), 3: lambda: config3(small),
             4: lambda: config4(small), 5: lambda: config5(small),
-            6: lambda: config6(small), 7: lambda: config7(small)}[cfg]()
+            6: lambda: config6(small), 7: lambda: config7(small),
+            8: lambda: config8(small)}[cfg]()
 
 
 def flat_cascade(c: Cascade) -> Paged:
