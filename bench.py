@@ -17,7 +17,8 @@ cpu_baseline = the fp64 oracle on this host's cores (a bounded sample of the bat
 --config selects another workload for measurement (2: Llama-3-8B-shaped decode with RoPE,
 4: shared-prefix cascade, 5: chunked prefill with append, reported in TFLOP/s, 6: the
 skewed decode over an FP8 (E4M3) KV cache, 7: sliding-window decode over long histories,
-8: the skewed decode with RoPE at the kept blocks' logical positions);
+8: the skewed decode with RoPE at the kept blocks' logical positions, 9: a three-level
+cascade of shared prefixes);
 the default is the skewed decode above.  --impl reference times the oracle (the only
 reference this method has here) on the same workload.  Under torchrun each rank runs an
 independent replica (weak scaling).
@@ -51,7 +52,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--small", action="store_true", help="small case (profiling, smoke)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8],
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9],
                     help="workload; 3 (skewed block-sparse decode) is the headline")
     return ap.parse_args()
 
@@ -379,6 +380,52 @@ def build_job(cfg: int, dev, small: bool):
                            "prefix_tokens": pre.kv_len[0], "prefix_page_size": pre.page_size,
                            "suffix_tokens": suf.active_tokens, "algorithmic_bytes": alg,
                            "levels": "prefix (tensor cores) + suffix (decode) + LSE merge"})
+    elif cfg == 9:
+        c = wl.config9(small)
+        q = c.levels[0].q.to(dev)
+        parts, scheds, alg = [], [], 0
+        st = q.shape[0] * q.shape[1] * (q.shape[2] + 1) * 4          # one fp32 state
+        outs = []
+        for i, w in enumerate(c.levels):
+            k, v = w.k_pages.to(dev), w.v_pages.to(dev)
+            o_i = torch.empty(q.shape, dtype=torch.float32, device=dev)
+            l_i = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+            s = plan(w)
+            pre = s.info()["num_prefill_items"] > 0
+            kv = w.active_tokens * 2 * w.num_kv_heads * w.head_dim * 2
+            fn = (lambda s=s, k=k, v=v, w=w, o_i=o_i, l_i=l_i:
+                  bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, out=o_i, lse=l_i))
+            parts.append(Part(f"level{i + 1}", fn,
+                              "bsr_prefill_kernel<0>" if pre else "bsr_decode_kernel<128,0,0,0>",
+                              "tensor" if pre else "hbm",
+                              attention_flops(w) if pre else kv + q.numel() * 2 + st,
+                              "FLOP" if pre else "B", launches=s.info()["kernels_per_run"],
+                              sched=s, stage="prefill" if pre else "decode",
+                              family="prefill" if pre else "decode"))
+            scheds.append(s)
+            outs.append((o_i, l_i))
+            alg += kv
+        acc_o = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        acc_l = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
+        parts.append(Part("merge12", lambda: bsr.bsr_merge_states(outs[0][0], outs[0][1],
+                                                                  outs[1][0], outs[1][1],
+                                                                  o_out=acc_o, lse_out=acc_l),
+                          "merge_states_kernel<128,1>", "hbm", 3 * st, "B"))
+        parts.append(Part("merge123", lambda: bsr.bsr_merge_states(acc_o, acc_l, outs[2][0],
+                                                                   outs[2][1], o_out=acc_o,
+                                                                   lse_out=acc_l),
+                          "merge_states_kernel<128,1>", "hbm", 3 * st, "B"))
+        job["parts"] = parts
+        job["schedules"] = scheds
+        alg += q.numel() * 2 + st
+        job.update(workload=c.levels[-1], metric="BSR multi-level cascade decode: achieved GB/s; us/call",
+                   unit="GB/s", numerator=alg, scale=1e9,
+                   config={"workload": c.name, "requests": c.levels[-1].batch,
+                           "levels": [{"segments": w.batch, "tokens": w.active_tokens,
+                                       "page_size": w.page_size} for w in c.levels],
+                           "algorithmic_bytes": alg,
+                           "composition": "system prefix + group prefixes (tensor cores) + "
+                                          "suffixes (decode), LSE-merged level by level"})
     elif cfg == 5:
         w = wl.config5(small)
         q, k, v = w.q.to(dev), w.k_pages.to(dev), w.v_pages.to(dev)

@@ -703,3 +703,16 @@ def test_page_positions_shift_invariance():
     o2, l2 = run_oracle(w, page_pos=shifted)
     _close(o, o2, 1e-9)
     _close(l, l2, 1e-9)
+
+
+def test_three_level_cascade_equals_flat():
+    # system prefix + group prefixes + suffixes, merged level by level == flat attention
+    c = wl.config9(small=True)
+    o, l = None, None
+    for w in c.levels:
+        ow, lw = run_oracle(w)
+        o, l = (ow, lw) if o is None else oracle.merge_states(o, l, ow, lw)
+    f = wl.flat_multi_cascade(c)
+    ro, rl = run_oracle(f)
+    _close(o, ro, 1e-10)
+    _close(l, rl, 1e-10)

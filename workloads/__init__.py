@@ -277,6 +277,95 @@ def config4(small: bool = False) -> Cascade:
     return Cascade(name=name, prefix=prefix, suffix=suffix)
 
 
+@dataclass
+class MultiCascade:
+    """Several levels of shared KV segments: each level is a batch whose requests are
+    that level's segments, every query row (all levels share ``q``) attending the one
+    segment of each level its group points at; the levels' states are LSE-merged."""
+    name: str
+    levels: list      # [Paged]; level i's qo_indptr groups the query rows by segment
+
+
+def multi_cascade(name, seed, level_lens, level_pages, groups, *, Hq=32, Hk=8, D=128):
+    """``groups[i]``: number of segments of level i (the query rows are split evenly
+    among them, in order); ``level_lens[i]``: (lo, hi) segment lengths (multiples of 16
+    at the levels above the last); ``level_pages[i]``: page size of level i."""
+    g = torch.Generator().manual_seed(seed)
+    n_req = groups[-1]
+    q = _bf16(torch.randn(n_req, Hq, D, generator=g))
+    levels = []
+    for i, (lens_, P, nseg) in enumerate(zip(level_lens, level_pages, groups)):
+        lens = torch.randint(lens_[0], lens_[1] + 1, (nseg,), generator=g)
+        if i < len(groups) - 1:
+            lens = lens // 16 * 16
+        indptr, indices, last, pool, att = _layout(lens.tolist(), P, 0.0, g)
+        per = n_req // nseg
+        qo = torch.arange(nseg + 1, dtype=torch.int32) * per
+        w = Paged(name=f"{name}.level{i + 1}", num_qo_heads=Hq, num_kv_heads=Hk, head_dim=D,
+                  page_size=P, num_pages=pool, indptr=indptr, indices=indices,
+                  last_page_len=last, qo_indptr=qo, kv_len=att, q=q,
+                  k_pages=_fill_pool(pool, Hk, P, D, g), v_pages=_fill_pool(pool, Hk, P, D, g),
+                  sm_scale=1.0 / math.sqrt(D))
+        _poison_unused(w)
+        levels.append(w)
+    return MultiCascade(name=name, levels=levels)
+
+
+def config9(small: bool = False) -> MultiCascade:
+    """Three-level cascade: one system prefix shared by every request, 8 group
+    prefixes each shared by an eighth of the requests, per-request suffixes."""
+    if small:
+        return multi_cascade("cascade3_small", 1009, [(320, 320), (96, 208), (1, 90)],
+                             [256, 64, 16], [1, 2, 16])
+    return multi_cascade("cascade3_r256", 1009, [(4096, 4096), (1024, 2048), (64, 1024)],
+                         [256, 64, 16], [1, 8, 256])
+
+
+def _tokens(w: Paged, b: int, pool: torch.Tensor) -> torch.Tensor:
+    """Request b's cached tokens [Hk, L, D] in order."""
+    P, L = w.page_size, w.kv_len[b]
+    pages = w.indices[int(w.indptr[b]):int(w.indptr[b + 1])].long()
+    return pool[pages].permute(1, 0, 2, 3).reshape(w.num_kv_heads, -1, w.head_dim)[:, :L]
+
+
+def flat_multi_cascade(c: MultiCascade) -> Paged:
+    """Each query row's concatenation of its segments, laid out as one flat P-16 batch
+    (used only to state "cascade == flat attention" as a check)."""
+    base = c.levels[-1]
+    Hq, Hk, D, P = base.num_qo_heads, base.num_kv_heads, base.head_dim, 16
+    n_req = base.batch
+    ks, vs, lens = [], [], []
+    for r in range(n_req):
+        kk, vv = [], []
+        for w in c.levels:
+            b = int(torch.searchsorted(w.qo_indptr, torch.tensor(r), right=True)) - 1
+            kk.append(_tokens(w, b, w.k_pages))
+            vv.append(_tokens(w, b, w.v_pages))
+        ks.append(torch.cat(kk, 1))
+        vs.append(torch.cat(vv, 1))
+        lens.append(ks[-1].shape[1])
+    npg = [(L + P - 1) // P for L in lens]
+    pool = sum(npg)
+    kp = torch.full((pool, Hk, P, D), float("nan"), dtype=torch.bfloat16)
+    vp = kp.clone()
+    indices, e = [], 0
+    for r in range(n_req):
+        for j in range(npg[r]):
+            n = min(P, lens[r] - j * P)
+            kp[e, :, :n] = ks[r][:, j * P:j * P + n]
+            vp[e, :, :n] = vs[r][:, j * P:j * P + n]
+            indices.append(e)
+            e += 1
+    indptr = torch.zeros(n_req + 1, dtype=torch.int32)
+    indptr[1:] = torch.cumsum(torch.tensor(npg), 0).to(torch.int32)
+    last = torch.tensor([L - (n - 1) * P for L, n in zip(lens, npg)], dtype=torch.int32)
+    return Paged(name=c.name + ".flat", num_qo_heads=Hq, num_kv_heads=Hk, head_dim=D,
+                 page_size=P, num_pages=pool, indptr=indptr,
+                 indices=torch.tensor(indices, dtype=torch.int32), last_page_len=last,
+                 qo_indptr=torch.arange(n_req + 1, dtype=torch.int32), kv_len=lens, q=base.q,
+                 k_pages=kp, v_pages=vp, sm_scale=base.sm_scale)
+
+
 def config5(small: bool = False) -> Paged:
     """Chunked prefill: append qo tokens after kv_len cached ones, causal, RoPE 5e5."""
     g = torch.Generator().manual_seed(1005)
@@ -384,7 +473,7 @@ def by_name(cfg: int, small: bool = False):
     return {1: lambda: config1(), 2: lambda: config2(small), 3: lambda: config3(small),
             4: lambda: config4(small), 5: lambda: config5(small),
             6: lambda: config6(small), 7: lambda: config7(small),
-            8: lambda: config8(small)}[cfg]()
+            8: lambda: config8(small), 9: lambda: config9(small)}[cfg]()
 
 
 def flat_cascade(c: Cascade) -> Paged:
