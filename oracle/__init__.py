@@ -68,13 +68,13 @@ def _configure(lib):
         _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, _i32p,
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int64, ctypes.c_double, ctypes.c_double, ctypes.c_int32, ctypes.c_int32,
-        _i32p, _i64p, _i32p, ctypes.c_int64, _f64p, _f64p, ctypes.c_int32]
+        _i32p, ctypes.c_int32, _i64p, _i32p, ctypes.c_int64, _f64p, _f64p, ctypes.c_int32]
     lib.oracle_attention_kv8.restype = ctypes.c_int
     lib.oracle_attention_kv8.argtypes = [
         _u16p, _u8p, _u8p, ctypes.c_double, ctypes.c_double, _i32p, _i32p, _i32p, _i32p,
         ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
         ctypes.c_int64, ctypes.c_double, ctypes.c_double, ctypes.c_int32, ctypes.c_int32,
-        _i32p, _i64p, _i32p, ctypes.c_int64, _f64p, _f64p, ctypes.c_int32]
+        _i32p, ctypes.c_int32, _i64p, _i32p, ctypes.c_int64, _f64p, _f64p, ctypes.c_int32]
     lib.oracle_e4m3.restype = ctypes.c_double
     lib.oracle_e4m3.argtypes = [ctypes.c_uint8]
     lib.oracle_merge_states.restype = None
@@ -83,7 +83,8 @@ def _configure(lib):
     lib.oracle_append_kv.restype = ctypes.c_int
     lib.oracle_append_kv.argtypes = [_u16p, _u16p, _i32p, _i32p, _i32p, _i32p,
                                      ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                     ctypes.c_int32, ctypes.c_int64, _u16p, _u16p]
+                                     ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, _u16p,
+                                     _u16p]
     lib.oracle_kv_len.restype = ctypes.c_int
     lib.oracle_kv_len.argtypes = [_i32p, _i32p, ctypes.c_int32, ctypes.c_int32, _i64p]
     lib.oracle_rope.restype = None
@@ -138,6 +139,12 @@ def _ptr(a: np.ndarray, t):
     return a.ctypes.data_as(t)
 
 
+def _layout_code(kv_layout: str) -> int:
+    if kv_layout not in ("HND", "NHD"):
+        raise ValueError("kv_layout must be 'HND' or 'NHD'")
+    return 1 if kv_layout == "NHD" else 0
+
+
 def default_threads() -> int:
     return len(os.sched_getaffinity(0))
 
@@ -166,8 +173,8 @@ def e4m3(codes) -> np.ndarray:
 def attention(q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr, *,
               num_qo_heads: int, num_kv_heads: int, head_dim: int, page_size: int,
               sm_scale: float, rope_theta: float = 0.0, causal: bool = False,
-              window_left: int = 0, page_pos=None, rows=None, heads=None,
-              threads: int | None = None):
+              window_left: int = 0, page_pos=None, kv_layout: str = "HND", rows=None,
+              heads=None, threads: int | None = None):
     """Exact (fp64) attention over a paged KV cache.
 
     ``q`` is bf16 [sum_qo, Hq, D]; ``k_pages``/``v_pages`` are bf16
@@ -180,29 +187,30 @@ def attention(q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr, *,
     (sliding window; with causal the upper bound is p, else the request's end).
     ``page_pos`` (int32 [len(indices)]): logical position of each page's first token,
     for RoPE over caches whose dropped blocks leave gaps (default: the cached order).
+    ``kv_layout``: "HND" pages [num_pages, Hk, P, D] or "NHD" pages [num_pages, P, Hk, D].
     """
     return _attention(None, q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr,
                       num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, rope_theta,
-                      causal, window_left, page_pos, rows, heads, threads)
+                      causal, window_left, page_pos, kv_layout, rows, heads, threads)
 
 
 def attention_kv8(q, k_pages, v_pages, k_scale: float, v_scale: float, indptr, indices,
                   last_page_len, qo_indptr, *, num_qo_heads: int, num_kv_heads: int,
                   head_dim: int, page_size: int, sm_scale: float, rope_theta: float = 0.0,
-                  causal: bool = False, window_left: int = 0, page_pos=None, rows=None,
-                  heads=None, threads: int | None = None):
+                  causal: bool = False, window_left: int = 0, page_pos=None,
+                  kv_layout: str = "HND", rows=None, heads=None, threads: int | None = None):
     """:func:`attention` over an FP8 KV cache: ``k_pages``/``v_pages`` hold E4M3
     codes (uint8, same layout) and the keys / values are ``k_scale * code`` and
     ``v_scale * code``."""
     return _attention((float(k_scale), float(v_scale)), q, k_pages, v_pages, indptr, indices,
                       last_page_len, qo_indptr, num_qo_heads, num_kv_heads, head_dim,
-                      page_size, sm_scale, rope_theta, causal, window_left, page_pos, rows, heads,
-                      threads)
+                      page_size, sm_scale, rope_theta, causal, window_left, page_pos, kv_layout,
+                      rows, heads, threads)
 
 
 def _attention(kv8, q, k_pages, v_pages, indptr, indices, last_page_len, qo_indptr,
                num_qo_heads, num_kv_heads, head_dim, page_size, sm_scale, rope_theta, causal,
-               window_left, page_pos, rows, heads, threads):
+               window_left, page_pos, kv_layout, rows, heads, threads):
     lib = _load()
     qb = _bits(q)
     if kv8 is None:
@@ -233,7 +241,7 @@ def _attention(kv8, q, k_pages, v_pages, indptr, indices, last_page_len, qo_indp
     table = (_ptr(ip, _i32p), _ptr(ix, _i32p), _ptr(lp, _i32p) if len(lp) else None,
              _ptr(qi, _i32p), batch, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
              float(sm_scale), float(rope_theta), int(bool(causal)), int(window_left),
-             _ptr(pp, _i32p) if pp is not None else None, srp, shp, n,
+             _ptr(pp, _i32p) if pp is not None else None, _layout_code(kv_layout), srp, shp, n,
              _ptr(out, _f64p), _ptr(lse, _f64p), int(threads or default_threads()))
     if kv8 is None:
         rc = lib.oracle_attention(_ptr(qb, _u16p), _ptr(kb, _u16p), _ptr(vb, _u16p), *table)
@@ -264,7 +272,7 @@ def merge_states(o_a, lse_a, o_b, lse_b):
 
 
 def append_kv(k_new, v_new, append_indptr, indptr, indices, last_page_len, k_pages, v_pages, *,
-              num_kv_heads: int, head_dim: int, page_size: int):
+              num_kv_heads: int, head_dim: int, page_size: int, kv_layout: str = "HND"):
     """Return copies of the page pools with the new tokens written in (bit exact)."""
     lib = _load()
     kn, vn = _bits(k_new), _bits(v_new)
@@ -275,7 +283,7 @@ def append_kv(k_new, v_new, append_indptr, indptr, indices, last_page_len, k_pag
     rc = lib.oracle_append_kv(_ptr(kn, _u16p), _ptr(vn, _u16p), _ptr(ai, _i32p),
                               _ptr(ip, _i32p), _ptr(ix, _i32p), _ptr(lp, _i32p), batch,
                               num_kv_heads, head_dim, page_size, num_pages,
-                              _ptr(kp, _u16p), _ptr(vp, _u16p))
+                              _layout_code(kv_layout), _ptr(kp, _u16p), _ptr(vp, _u16p))
     if rc != 0:
         raise ValueError("oracle_append_kv: malformed input")
     return kp, vp

@@ -70,6 +70,15 @@ static double kv_elem(const void* pool, int32_t kv_fp8, double scale, int64_t id
   return bf16_bits_to_double(((const uint16_t*)pool)[idx]);
 }
 
+/* Element offset of (page, kv head h, slot t) in a page pool: HND pages hold
+ * [Hk][P][D] (one head's P tokens contiguous), NHD pages [P][Hk][D] (one token's
+ * heads contiguous, the token-major layout some serving engines keep). */
+static int64_t kv_off(int64_t page, int32_t h, int64_t t, int32_t Hk, int32_t P, int32_t D,
+                      int32_t nhd) {
+  if (nhd) return ((page * P + t) * Hk + h) * (int64_t)D;
+  return ((page * Hk + h) * P + t) * (int64_t)D;
+}
+
 /* Attended KV length of request b: all of its pages are full except the last,
  * which holds last_page_len tokens (reading: 1 <= last_page_len <= P whenever
  * the request has a page; a request with no page has length 0). Returns -1 on
@@ -142,10 +151,11 @@ static int attention_impl(const uint16_t* q, const void* k_pages, const void* v_
                           int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                           int32_t head_dim, int32_t page_size, int64_t num_pages,
                           double sm_scale, double rope_theta, int32_t causal,
-                          int32_t window_left, const int32_t* page_pos,
+                          int32_t window_left, const int32_t* page_pos, int32_t nhd,
                           const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
                           double* out, double* lse, int32_t num_threads) {
   const int32_t D = head_dim, P = page_size, Hq = num_qo_heads, Hk = num_kv_heads;
+  if (nhd != 0 && nhd != 1) return -1;
   if (window_left < 0) return -1;
   if (batch < 0 || Hq <= 0 || Hk <= 0 || Hq % Hk != 0 || D <= 0 || D % 2 != 0 || P <= 0)
     return -1;
@@ -209,7 +219,7 @@ static int attention_impl(const uint16_t* q, const void* k_pages, const void* v_
          * query's own (reading of the JIT section's "Sliding Window" variant) */
         if (window_left > 0 && j < qpos - window_left + 1) { scores[j] = -INFINITY; continue; }
         const int64_t page = indices[indptr[b] + j / P];
-        const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;
+        const int64_t off = kv_off(page, kvh, j % P, Hk, P, D, nhd);
         for (int32_t d = 0; d < D; ++d) kv[d] = kv_elem(k_pages, kv_fp8, k_scale, off + d);
         if (rope_theta > 0.0) {
           const int64_t kpos = page_pos ? (int64_t)page_pos[indptr[b] + j / P] + j % P : j;
@@ -232,7 +242,7 @@ static int attention_impl(const uint16_t* q, const void* k_pages, const void* v_
         if (scores[j] == -INFINITY) continue;
         const double p = exp(scores[j] - l);
         const int64_t page = indices[indptr[b] + j / P];
-        const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;
+        const int64_t off = kv_off(page, kvh, j % P, Hk, P, D, nhd);
         for (int32_t d = 0; d < D; ++d) o[d] += p * kv_elem(v_pages, kv_fp8, v_scale, off + d);
       }
     }
@@ -249,12 +259,12 @@ int oracle_attention(const uint16_t* q, const uint16_t* k_pages, const uint16_t*
                      int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                      int32_t head_dim, int32_t page_size, int64_t num_pages,
                      double sm_scale, double rope_theta, int32_t causal, int32_t window_left,
-                     const int32_t* page_pos, const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
+                     const int32_t* page_pos, int32_t kv_layout, const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
                      double* out, double* lse, int32_t num_threads) {
   return attention_impl(q, k_pages, v_pages, 0, 1.0, 1.0, indptr, indices, last_page_len,
                         qo_indptr, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
                         num_pages, sm_scale, rope_theta, causal, window_left, page_pos,
-                        sel_rows, sel_heads, num_sel, out, lse, num_threads);
+                        kv_layout, sel_rows, sel_heads, num_sel, out, lse, num_threads);
 }
 
 /* The same attention over an FP8 (E4M3) KV cache: K = k_scale * code,
@@ -266,13 +276,14 @@ int oracle_attention_kv8(const uint16_t* q, const uint8_t* k_pages, const uint8_
                          int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads,
                          int32_t head_dim, int32_t page_size, int64_t num_pages,
                          double sm_scale, double rope_theta, int32_t causal,
-                         int32_t window_left, const int32_t* page_pos,
+                         int32_t window_left, const int32_t* page_pos, int32_t kv_layout,
                          const int64_t* sel_rows, const int32_t* sel_heads, int64_t num_sel,
                          double* out, double* lse, int32_t num_threads) {
   return attention_impl(q, k_pages, v_pages, 1, k_scale, v_scale, indptr, indices,
                         last_page_len, qo_indptr, batch, num_qo_heads, num_kv_heads, head_dim,
                         page_size, num_pages, sm_scale, rope_theta, causal, window_left,
-                        page_pos, sel_rows, sel_heads, num_sel, out, lse, num_threads);
+                        page_pos, kv_layout, sel_rows, sel_heads, num_sel, out, lse,
+                        num_threads);
 }
 
 /*
@@ -314,8 +325,10 @@ int oracle_append_kv(const uint16_t* k_new, const uint16_t* v_new,
                      const int32_t* append_indptr, const int32_t* indptr,
                      const int32_t* indices, const int32_t* last_page_len, int32_t batch,
                      int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
-                     int64_t num_pages, uint16_t* k_pages, uint16_t* v_pages) {
-  const int32_t D = head_dim, P = page_size, Hk = num_kv_heads;
+                     int64_t num_pages, int32_t kv_layout, uint16_t* k_pages,
+                     uint16_t* v_pages) {
+  const int32_t D = head_dim, P = page_size, Hk = num_kv_heads, nhd = kv_layout;
+  if (nhd != 0 && nhd != 1) return -1;
   for (int32_t b = 0; b < batch; ++b) {
     const int64_t L = kv_len_of(indptr, last_page_len, b, P);
     const int64_t n_new = (int64_t)append_indptr[b + 1] - append_indptr[b];
@@ -326,7 +339,7 @@ int oracle_append_kv(const uint16_t* k_new, const uint16_t* v_new,
       if (page < 0 || page >= num_pages) return -1;
       const int64_t src_tok = append_indptr[b] + i;
       for (int32_t h = 0; h < Hk; ++h) {
-        const int64_t dst = ((page * Hk + h) * P + pos % P) * (int64_t)D;
+        const int64_t dst = kv_off(page, h, pos % P, Hk, P, D, nhd);
         const int64_t src = (src_tok * Hk + h) * (int64_t)D;
         memcpy(k_pages + dst, k_new + src, sizeof(uint16_t) * (size_t)D);
         memcpy(v_pages + dst, v_new + src, sizeof(uint16_t) * (size_t)D);

@@ -716,3 +716,30 @@ def test_three_level_cascade_equals_flat():
     ro, rl = run_oracle(f)
     _close(o, ro, 1e-10)
     _close(l, rl, 1e-10)
+
+
+# ---------------------------------------------------------------- NHD pages
+
+def test_nhd_pages_equal_hnd_pages():
+    # token-major pools hold the same tokens: every result is identical
+    for kw in (dict(), dict(qo_lens=[1, 3, 5, 2], causal=True, rope_theta=300.0),
+               dict(Hq=6, Hk=3, D=6, P=3)):
+        w = tiny(**kw)
+        o, l = run_oracle(w)
+        n = wl.to_nhd(tiny(**kw))
+        o2, l2 = run_oracle(n, kv_layout="NHD")
+        assert np.array_equal(o, o2) and np.array_equal(l, l2)
+
+
+def test_nhd_append_writes_the_same_tokens():
+    w = wl.make_paged("app", 11, [9, 20, 5], Hq=4, Hk=2, D=8, P=4, qo_lens=[3, 4, 2],
+                      causal=True, append=True)
+    kw = dict(num_kv_heads=2, head_dim=8, page_size=4)
+    args = (w.k_new, w.v_new, w.append_indptr, w.indptr, w.indices, w.last_page_len)
+    kp, vp = oracle.append_kv(*args, w.k_pages, w.v_pages, **kw)
+    n = wl.to_nhd(w)
+    kn, vn = oracle.append_kv(*args, n.k_pages, n.v_pages, kv_layout="NHD", **kw)
+    shape = tuple(n.k_pages.shape)
+    to_hnd = lambda a: np.ascontiguousarray(a.reshape(shape).transpose(0, 2, 1, 3))
+    assert np.array_equal(to_hnd(kn), kp.reshape(to_hnd(kn).shape))
+    assert np.array_equal(to_hnd(vn), vp.reshape(to_hnd(vn).shape))

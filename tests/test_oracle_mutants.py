@@ -23,15 +23,15 @@ MUTANTS = {
     "query_alignment": ("const int64_t qpos = L - qo_len + (t - qo_indptr[b]);",
                         "const int64_t qpos = (t - qo_indptr[b]);"),
     "page_offset": ("const int64_t page = indices[indptr[b] + j / P];\n"
-                    "        const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;\n"
+                    "        const int64_t off = kv_off(page, kvh, j % P, Hk, P, D, nhd);\n"
                     "        for (int32_t d = 0; d < D; ++d) kv[d]",
                     "const int64_t page = indices[j / P];\n"
-                    "        const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;\n"
+                    "        const int64_t off = kv_off(page, kvh, j % P, Hk, P, D, nhd);\n"
                     "        for (int32_t d = 0; d < D; ++d) kv[d]"),
-    "head_page_layout": ("const int64_t off = ((page * Hk + kvh) * P + j % P) * (int64_t)D;\n"
-                         "        for (int32_t d = 0; d < D; ++d) kv[d]",
-                         "const int64_t off = ((page * P + j % P) * Hk + kvh) * (int64_t)D;\n"
-                         "        for (int32_t d = 0; d < D; ++d) kv[d]"),
+    "head_page_layout": ("return ((page * Hk + h) * P + t) * (int64_t)D;",
+                         "return ((page * P + t) * Hk + h) * (int64_t)D;"),
+    "nhd_layout": ("if (nhd) return ((page * P + t) * Hk + h) * (int64_t)D;",
+                   "if (nhd) return ((page * Hk + h) * P + t) * (int64_t)D;"),
     "last_page_len": ("return (n - 1) * page_size + last_page_len[b];", "return n * page_size;"),
     "lse_drops_max": ("const double l = m + log(sum);", "const double l = log(sum);"),
     "scale_dropped": ("scores[j] = sm_scale * dot;", "scores[j] = dot;"),
@@ -79,7 +79,8 @@ def _checks():
           lambda: pins.test_window_equals_masking_older_keys(5),
           pins.test_window_causal_rows_equal_decode_with_window,
           lambda: pins.test_page_positions_rotate_at_the_logical_positions(dict()),
-          pins.test_page_positions_shift_invariance]
+          pins.test_page_positions_shift_invariance,
+          pins.test_nhd_pages_equal_hnd_pages]
     return c
 
 

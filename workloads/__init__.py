@@ -67,6 +67,7 @@ class Paged:
     # logical position of each page-table entry's first token (int32 [len(indices)]):
     # with dropped blocks the kept pages keep their original positions
     page_pos: torch.Tensor | None = None
+    kv_layout: str = "HND"        # "NHD": pools are [num_pages, P, Hk, D]
 
     @property
     def batch(self) -> int:
@@ -464,6 +465,22 @@ def config8(small: bool = False) -> Paged:
     return w
 
 
+def to_nhd(w: Paged) -> Paged:
+    """The same batch with token-major (NHD) page pools [num_pages, P, Hk, D]."""
+    for name in ("k_pages", "v_pages", "k_codes", "v_codes"):
+        t = getattr(w, name)
+        if t is not None:
+            setattr(w, name, t.permute(0, 2, 1, 3).contiguous())
+    w.kv_layout = "NHD"
+    w.name = w.name + "_nhd"
+    return w
+
+
+def config10(small: bool = False) -> Paged:
+    """The skewed block-sparse decode over token-major (NHD) pages."""
+    return to_nhd(config3(small))
+
+
 def config6(small: bool = False) -> Paged:
     """The skewed block-sparse decode with an FP8 (E4M3) KV cache."""
     return with_kv8(config3(small), 1006)
@@ -473,7 +490,8 @@ def by_name(cfg: int, small: bool = False):
     return {1: lambda: config1(), 2: lambda: config2(small), 3: lambda: config3(small),
             4: lambda: config4(small), 5: lambda: config5(small),
             6: lambda: config6(small), 7: lambda: config7(small),
-            8: lambda: config8(small), 9: lambda: config9(small)}[cfg]()
+            8: lambda: config8(small), 9: lambda: config9(small),
+            10: lambda: config10(small)}[cfg]()
 
 
 def flat_cascade(c: Cascade) -> Paged:
