@@ -18,7 +18,7 @@ cpu_baseline = the fp64 oracle on this host's cores (a bounded sample of the bat
 4: shared-prefix cascade, 5: chunked prefill with append, reported in TFLOP/s, 6: the
 skewed decode over an FP8 (E4M3) KV cache, 7: sliding-window decode over long histories,
 8: the skewed decode with RoPE at the kept blocks' logical positions, 9: a three-level
-cascade of shared prefixes);
+cascade of shared prefixes, 10: the skewed decode over token-major (NHD) pages);
 the default is the skewed decode above.  --impl reference times the oracle (the only
 reference this method has here) on the same workload.  Under torchrun each rank runs an
 independent replica (weak scaling).
@@ -52,7 +52,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--small", action="store_true", help="small case (profiling, smoke)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9],
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10],
                     help="workload; 3 (skewed block-sparse decode) is the headline")
     return ap.parse_args()
 
@@ -195,7 +195,7 @@ def cpu_baseline(w, budget_s=10.0, min_passes=1):
         kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                   page_size=w.page_size, sm_scale=w.sm_scale, rope_theta=w.rope_theta,
                   causal=w.causal, window_left=w.window_left, page_pos=w.page_pos,
-                  threads=threads)
+                  kv_layout=w.kv_layout, threads=threads)
         if w.k_codes is not None:
             oracle.attention_kv8(w.q, w.k_codes, w.v_codes, w.k_scale, w.v_scale, *table, **kw)
         else:
@@ -250,10 +250,11 @@ def build_job(cfg: int, dev, small: bool):
                                  head_dim=w.head_dim, page_size=w.page_size,
                                  num_pages=w.num_pages, qo_indptr=w.qo_indptr, causal=w.causal,
                                  rope_theta=w.rope_theta, window_left=w.window_left,
-                                 page_pos=w.page_pos, schedule=schedule)
+                                 page_pos=w.page_pos, kv_layout=w.kv_layout,
+                                 schedule=schedule)
 
     job = {"parts": [], "schedules": []}
-    if cfg in (1, 2, 3, 7, 8):
+    if cfg in (1, 2, 3, 7, 8, 10):
         w = wl.by_name(cfg, small)
         q, k, v = w.q.to(dev), w.k_pages.to(dev), w.v_pages.to(dev)
         out = torch.empty_like(q)
@@ -265,7 +266,8 @@ def build_job(cfg: int, dev, small: bool):
         kname = f"bsr_decode_kernel<{w.head_dim},{int(w.rope_theta > 0)},0,0>"
         prof = {2: "bsr_decode_rope_llama8b_b64.md", 3: "bsr_decode_skewed_b128.md",
                 7: "bsr_decode_window_b64_w2048.md",
-                8: "bsr_decode_rope_positions_b128.md"}.get(cfg)
+                8: "bsr_decode_rope_positions_b128.md",
+                10: "bsr_decode_skewed_b128_nhd.md"}.get(cfg)
         job["parts"] = [Part("decode", run, kname, "hbm", alg, "B",
                              launches=s.info()["kernels_per_run"], sched=s, stage="decode",
                              family="decode", profile=None if small else prof)]
@@ -277,8 +279,10 @@ def build_job(cfg: int, dev, small: bool):
                            "algorithmic_bytes": alg, "rope_theta": w.rope_theta,
                            "l2": "inputs larger than L2, no flush" if alg > 2e8 else
                                  "inputs smaller than L2: L2-warm"})
-        if cfg in (3, 8):
+        if cfg in (3, 8, 10):
             job["config"]["drop"] = "25% of non-final pages"
+        if cfg == 10:
+            job["config"]["kv_layout"] = "NHD (token-major pages)"
         if cfg == 8:
             job["config"]["rope_positions"] = "logical (per-page positions of the kept blocks)"
         if cfg == 7:
@@ -636,7 +640,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     import workloads as wl
-    w = wl.by_name(args.config if args.config in (1, 2, 3, 6, 7, 8) else 3, args.small)
+    w = wl.by_name(args.config if args.config in (1, 2, 3, 6, 7, 8, 10) else 3, args.small)
     for _ in range(args.warmup):
         cpu_baseline(w, budget_s=0.0)
     t0 = time.perf_counter()

@@ -58,6 +58,7 @@ class _Info(ctypes.Structure):
         ("upload_bytes", ctypes.c_int64),
         ("decode_imbalance", ctypes.c_double), ("prefill_imbalance", ctypes.c_double),
         ("kernels_per_run", ctypes.c_int32), ("window_left", ctypes.c_int32),
+        ("kv_layout", ctypes.c_int32), ("reserved", ctypes.c_int32),
     ]
 
 
@@ -75,13 +76,13 @@ def load(path: str | None = None):
     lib.bsr_attn_plan.argtypes = [_i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
-                                  ctypes.c_float, _vp, ctypes.POINTER(_vp)]
+                                  ctypes.c_int32, ctypes.c_float, _vp, ctypes.POINTER(_vp)]
     lib.bsr_attn_plan_host.restype = ctypes.c_int
     lib.bsr_attn_plan_host.argtypes = [_i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
-                                       ctypes.c_float, ctypes.c_int32, ctypes.POINTER(_Info),
-                                       _i32p, ctypes.c_int64]
+                                       ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
+                                       ctypes.POINTER(_Info), _i32p, ctypes.c_int64]
     lib.bsr_attn_run_kv8.restype = ctypes.c_int
     lib.bsr_attn_run_kv8.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                      ctypes.c_float, ctypes.c_float, ctypes.c_int32, _vp,
@@ -95,7 +96,7 @@ def load(path: str | None = None):
     lib.bsr_append_kv.restype = ctypes.c_int
     lib.bsr_append_kv.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32, ctypes.c_int64,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
-                                  _vp, _vp, _vp, _vp]
+                                  ctypes.c_int32, _vp, _vp, _vp, _vp]
     lib.bsr_schedule_destroy.restype = None
     lib.bsr_schedule_destroy.argtypes = [_vp]
     lib.bsr_schedule_get_info.restype = ctypes.c_int
@@ -119,6 +120,17 @@ def load(path: str | None = None):
 
 def bsr_status_string(code: int) -> str:
     return load().bsr_status_string(int(code)).decode()
+
+
+BSR_KV_HND = 0
+BSR_KV_NHD = 1
+
+
+def _layout(kv_layout: str) -> int:
+    """Page pool layout: "HND" [pages, Hk, P, D] or "NHD" [pages, P, Hk, D]."""
+    if kv_layout not in ("HND", "NHD"):
+        raise ValueError("kv_layout must be 'HND' or 'NHD'")
+    return BSR_KV_NHD if kv_layout == "NHD" else BSR_KV_HND
 
 
 def _check(code: int, where: str):
@@ -186,7 +198,8 @@ def _plan_args(indptr, indices, last_page_len, qo_indptr):
 def bsr_attn_plan(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_heads: int,
                   head_dim: int, page_size: int, num_pages: int, qo_indptr=None,
                   causal: bool = False, rope_theta: float = 0.0, window_left: int = 0,
-                  page_pos=None, stream=None, schedule: Schedule | None = None) -> Schedule:
+                  page_pos=None, kv_layout: str = "HND", stream=None,
+                  schedule: Schedule | None = None) -> Schedule:
     """Plan one batch from HOST page-table arrays; returns (or re-plans) a Schedule."""
     lib = load()
     keep, (ip, ix, lp, qi), batch = _plan_args(indptr, indices, last_page_len, qo_indptr)
@@ -195,7 +208,8 @@ def bsr_attn_plan(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_h
     code = lib.bsr_attn_plan(ip, ix, lp, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
                              qi, int(num_pages), int(bool(causal)), int(window_left),
                              pp.ctypes.data_as(_i32p) if pp is not None and pp.size else None,
-                             float(rope_theta), _vp(_stream_ptr(stream)), ctypes.byref(handle))
+                             _layout(kv_layout), float(rope_theta), _vp(_stream_ptr(stream)),
+                             ctypes.byref(handle))
     del keep
     _check(code, "bsr_attn_plan")
     if schedule is not None:
@@ -207,7 +221,7 @@ def bsr_attn_plan(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_h
 def bsr_attn_plan_host(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_heads: int,
                        head_dim: int, page_size: int, num_pages: int, num_sms: int,
                        qo_indptr=None, causal: bool = False, rope_theta: float = 0.0,
-                       window_left: int = 0, page_pos=None):
+                       window_left: int = 0, page_pos=None, kv_layout: str = "HND"):
     """Host-only planning for `num_sms` SMs: returns (info dict, units int32 [n, 8])."""
     lib = load()
     keep, (ip, ix, lp, qi), batch = _plan_args(indptr, indices, last_page_len, qo_indptr)
@@ -215,7 +229,7 @@ def bsr_attn_plan_host(indptr, indices, last_page_len, *, num_qo_heads: int, num
     args = [ip, ix, lp, batch, num_qo_heads, num_kv_heads, head_dim, page_size, qi,
             int(num_pages), int(bool(causal)), int(window_left),
             pp.ctypes.data_as(_i32p) if pp is not None and pp.size else None,
-            float(rope_theta), int(num_sms)]
+            _layout(kv_layout), float(rope_theta), int(num_sms)]
     info = _Info()
     n = lib.bsr_attn_plan_host(*args, ctypes.byref(info), None, 0)
     if n < 0:
@@ -295,14 +309,19 @@ def bsr_merge_states(o_a, lse_a, o_b, lse_b, *, o_out=None, lse_out=None, stream
 
 
 def bsr_append_kv(k_new, v_new, append_indptr, indptr, indices, last_page_len, k_pages, v_pages,
-                  *, device_status=None, stream=None):
-    """Write new tokens' k/v into their pages (all arguments are device tensors)."""
+                  *, kv_layout: str = "HND", device_status=None, stream=None):
+    """Write new tokens' k/v into their pages (all arguments are device tensors); the
+    pools are [pages, Hk, P, D] ("HND") or [pages, P, Hk, D] ("NHD")."""
     lib = load()
-    num_pages, Hk, P, D = k_pages.shape
+    if kv_layout == "NHD":
+        num_pages, P, Hk, D = k_pages.shape
+    else:
+        num_pages, Hk, P, D = k_pages.shape
     code = lib.bsr_append_kv(_dptr(k_new), _dptr(v_new), _dptr(append_indptr), _dptr(indptr),
                              _dptr(indices), _dptr(last_page_len), len(indptr) - 1,
-                             int(k_new.shape[0]), Hk, D, P, num_pages, _dptr(k_pages),
-                             _dptr(v_pages), _dptr(device_status), _vp(_stream_ptr(stream)))
+                             int(k_new.shape[0]), Hk, D, P, num_pages, _layout(kv_layout),
+                             _dptr(k_pages), _dptr(v_pages), _dptr(device_status),
+                             _vp(_stream_ptr(stream)))
     _check(code, "bsr_append_kv")
 
 

@@ -85,8 +85,8 @@ __global__ void __launch_bounds__(kThreads) append_kv_kernel(
     const uint4* __restrict__ k_new, const uint4* __restrict__ v_new,
     const int32_t* __restrict__ append_indptr, const int32_t* __restrict__ indptr,
     const int32_t* __restrict__ indices, const int32_t* __restrict__ last_page_len, int32_t batch,
-    int64_t ntok, int32_t Hk, int32_t chunks, int32_t P, int32_t num_pages, uint4* k_pages,
-    uint4* v_pages, int32_t* status) {
+    int64_t ntok, int32_t Hk, int32_t chunks, int32_t P, int32_t num_pages, int32_t nhd,
+    uint4* k_pages, uint4* v_pages, int32_t* status) {
   const int64_t total = ntok * Hk * chunks;
   for (int64_t g = int64_t(blockIdx.x) * kThreads + threadIdx.x; g < total;
        g += int64_t(gridDim.x) * kThreads) {
@@ -115,7 +115,9 @@ __global__ void __launch_bounds__(kThreads) append_kv_kernel(
       if (status) atomicOr(status, 1);
       continue;
     }
-    const size_t dst = ((size_t(page) * Hk + h) * P + size_t(pos % P)) * chunks + c;
+    // head-major pages [page][Hk][P][D] or token-major [page][P][Hk][D]
+    const size_t dst = nhd ? ((size_t(page) * P + size_t(pos % P)) * Hk + h) * chunks + c
+                           : ((size_t(page) * Hk + h) * P + size_t(pos % P)) * chunks + c;
     const size_t src = (size_t(t) * Hk + h) * chunks + c;
     k_pages[dst] = k_new[src];
     v_pages[dst] = v_new[src];
@@ -168,10 +170,11 @@ extern "C" int bsr_append_kv(const void* k_new, const void* v_new, const int32_t
                              const int32_t* indptr, const int32_t* indices,
                              const int32_t* last_page_len, int32_t batch, int64_t num_new_tokens,
                              int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
-                             int32_t num_pages_in_pool, void* k_pages, void* v_pages,
-                             int32_t* device_status, void* stream_v) {
+                             int32_t num_pages_in_pool, int32_t kv_layout, void* k_pages,
+                             void* v_pages, int32_t* device_status, void* stream_v) {
   if (batch < 0 || num_new_tokens < 0 || num_kv_heads <= 0 || num_pages_in_pool < 0)
     return BSR_ERR_INVALID_ARGUMENT;
+  if (kv_layout != BSR_KV_HND && kv_layout != BSR_KV_NHD) return BSR_ERR_INVALID_ARGUMENT;
   if (head_dim != 64 && head_dim != 128) return BSR_ERR_UNSUPPORTED;
   if (page_size <= 0 || page_size > 256 || (page_size & (page_size - 1))) return BSR_ERR_UNSUPPORTED;
   if (num_new_tokens == 0) return BSR_OK;
@@ -187,8 +190,8 @@ extern "C" int bsr_append_kv(const void* k_new, const void* v_new, const int32_t
   append_kv_kernel<<<grid_for(work, kThreads), kThreads, 0, stream>>>(
       static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), append_indptr, indptr,
       indices, last_page_len, batch, num_new_tokens, num_kv_heads, chunks, page_size,
-      num_pages_in_pool, static_cast<uint4*>(k_pages), static_cast<uint4*>(v_pages),
-      device_status);
+      num_pages_in_pool, kv_layout == BSR_KV_NHD ? 1 : 0, static_cast<uint4*>(k_pages),
+      static_cast<uint4*>(v_pages), device_status);
   if (cudaGetLastError() != cudaSuccess) return BSR_ERR_CUDA;
   return BSR_OK;
 }

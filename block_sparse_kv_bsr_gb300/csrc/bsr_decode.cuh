@@ -315,13 +315,26 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
                        reinterpret_cast<const float4*>(p.rope) + size_t(rpos) * C::kRopeRowF4,
                        C::kRopeRowBytes, bar, pol_rope);
       }
+      // HND pools: row (page * Hk + head) * P + slot; NHD: token row page * P + slot
+      // and the head as the map's outer coordinate
+      const int trow = page * p.P + (tok & (p.P - 1));
       if constexpr (D == 128) {
         // one box per tile: both 64-column blocks, [block][16 rows][128 B]
-        ptx::tma_load_3d(dk, &tm_k, bar, 0, row, 0, pol);
-        ptx::tma_load_3d(dv, &tm_v, bar, 0, row, 0, pol);
+        if (p.nhd) {
+          ptx::tma_load_4d(dk, &tm_k, bar, 0, trow, 0, pi.kvh, pol);
+          ptx::tma_load_4d(dv, &tm_v, bar, 0, trow, 0, pi.kvh, pol);
+        } else {
+          ptx::tma_load_3d(dk, &tm_k, bar, 0, row, 0, pol);
+          ptx::tma_load_3d(dv, &tm_v, bar, 0, row, 0, pol);
+        }
       } else {
-        ptx::tma_load_2d(dk, &tm_k, bar, 0, row, pol);
-        ptx::tma_load_2d(dv, &tm_v, bar, 0, row, pol);
+        if (p.nhd) {
+          ptx::tma_load_3d(dk, &tm_k, bar, 0, trow, pi.kvh, pol);
+          ptx::tma_load_3d(dv, &tm_v, bar, 0, trow, pi.kvh, pol);
+        } else {
+          ptx::tma_load_2d(dk, &tm_k, bar, 0, row, pol);
+          ptx::tma_load_2d(dv, &tm_v, bar, 0, row, pol);
+        }
       }
     }
     ++p_seq;
@@ -455,7 +468,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
           if (!WIN || key >= wlo_min) {
             const int page = __ldg(p.indices + ci.page_base + (key >> log2P));
             const size_t off =
-                (size_t(page * p.Hk + ci.kvh) * p.P + (key & (p.P - 1))) * D + c * 8;
+                (p.nhd ? size_t(page * p.P + (key & (p.P - 1))) * p.Hk + ci.kvh
+                       : size_t(page * p.Hk + ci.kvh) * p.P + (key & (p.P - 1))) * D + c * 8;
             kv = __ldg(reinterpret_cast<const uint4*>(kp + off));
             vv = __ldg(reinterpret_cast<const uint4*>(vp + off));
           }

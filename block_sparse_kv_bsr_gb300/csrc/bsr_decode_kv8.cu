@@ -133,8 +133,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       const int tok = pi.tok0 + kStageTokens * p_st;
       const int row = (page * p.Hk + pi.kvh) * p.P + (tok & (p.P - 1));
       ptx::mbar_arrive_expect_tx(bar, kStage8);
-      ptx::tma_load_2d(dk, &tm_k, bar, 0, row, pol);
-      ptx::tma_load_2d(dv, &tm_v, bar, 0, row, pol);
+      if (p.nhd) {   // token row page * P + slot, the head as the map's outer coordinate
+        const int trow = page * p.P + (tok & (p.P - 1));
+        ptx::tma_load_3d(dk, &tm_k, bar, 0, trow, pi.kvh, pol);
+        ptx::tma_load_3d(dv, &tm_v, bar, 0, trow, pi.kvh, pol);
+      } else {
+        ptx::tma_load_2d(dk, &tm_k, bar, 0, row, pol);
+        ptx::tma_load_2d(dv, &tm_v, bar, 0, row, pol);
+      }
     }
     ++p_seq;
     ++p_st;

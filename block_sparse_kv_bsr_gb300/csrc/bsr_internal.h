@@ -71,6 +71,7 @@ struct DecodeParams {
   int32_t causal, out_f32, num_warps;
   int32_t rope_max_pos;           // last row of the cos/sin table
   int32_t window_left;            // sliding window: keys >= position - window_left + 1 (0: none)
+  int32_t nhd;                    // page pools token-major [pages, P, Hk, D] (else [pages, Hk, P, D])
   uint64_t wait_limit_ns;         // bound on every barrier wait
 };
 
@@ -104,6 +105,7 @@ struct PrefillParams {
   int32_t Hq, Hk, group, P;
   int32_t causal, out_f32, out_v8, num_ctas;
   int32_t window_left;            // sliding window (0: none)
+  int32_t nhd;                    // page pools token-major (else head-major)
   int32_t box_rows;               // rows per K/V box of the prefill tensor maps: min(P, 128)
   uint64_t wait_limit_ns;
 };
@@ -139,6 +141,7 @@ struct RopePrepassParams {
   uint16_t* rotq;
   int32_t* error;                 // status word (kStatusRopeRange on overflow)
   int32_t n, rk_total, rq_total, Hk, Hq, P, rope_max_pos;
+  int32_t nhd;                    // page pools token-major (else head-major)
 };
 
 }  // namespace bsr

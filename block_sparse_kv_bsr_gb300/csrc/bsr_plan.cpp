@@ -507,8 +507,9 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
                              const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
                              int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                              const int32_t* qo_indptr, int32_t num_pages_in_pool, int32_t causal,
-                             int32_t window_left, const int32_t* page_pos, float rope_theta,
-                             void* stream_v, bsr_schedule_t* schedule) {
+                             int32_t window_left, const int32_t* page_pos, int32_t kv_layout,
+                             float rope_theta, void* stream_v, bsr_schedule_t* schedule) {
+  if (kv_layout != BSR_KV_HND && kv_layout != BSR_KV_NHD) return BSR_ERR_INVALID_ARGUMENT;
   if (schedule == nullptr) return BSR_ERR_INVALID_ARGUMENT;
   const cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const bool rope = rope_theta > 0.f;
@@ -683,6 +684,9 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->group = hp.group;
   s->causal = causal;
   s->window_left = window_left;
+  s->kv_layout = kv_layout;
+  s->tm_k_ptr = s->tm_v_ptr = nullptr;      // the maps depend on the layout
+  s->tm_k8_ptr = s->tm_v8_ptr = nullptr;
   s->rope_theta = rope_theta;
   s->num_pages = num_pages_in_pool;
   s->sum_qo = hp.sum_qo;
@@ -763,6 +767,7 @@ extern "C" int bsr_schedule_get_info(bsr_schedule_t s, bsr_schedule_info_t* info
   info->page_size = s->P;
   info->causal = s->causal;
   info->window_left = s->window_left;
+  info->kv_layout = s->kv_layout;
   info->rope_theta = s->rope_theta;
   info->sum_qo = s->sum_qo;
   info->active_tokens = s->active_tokens;
@@ -789,8 +794,9 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
                                   int32_t page_size, const int32_t* qo_indptr,
                                   int32_t num_pages_in_pool, int32_t causal,
                                   int32_t window_left, const int32_t* page_pos,
-                                  float rope_theta, int32_t num_sms, bsr_schedule_info_t* info,
-                                  int32_t* units, int64_t max_units) {
+                                  int32_t kv_layout, float rope_theta, int32_t num_sms,
+                                  bsr_schedule_info_t* info, int32_t* units, int64_t max_units) {
+  if (kv_layout != BSR_KV_HND && kv_layout != BSR_KV_NHD) return BSR_ERR_INVALID_ARGUMENT;
   HostPlan hp;
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
@@ -805,6 +811,7 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
     info->page_size = page_size;
     info->causal = causal;
     info->window_left = window_left;
+    info->kv_layout = kv_layout;
     info->rope_theta = rope_theta;
     info->sum_qo = hp.sum_qo;
     info->active_tokens = hp.active;

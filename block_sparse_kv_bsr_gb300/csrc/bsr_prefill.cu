@@ -265,16 +265,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane < nsub) {
         const int key = it.tok0 + kTileN * j + (lane << lr);
-        const int row = (page * p.Hk + it.kvh) * p.P + (key & (p.P - 1));
+        // HND pools: row (page * Hk + head) * P + slot; NHD: token row page * P + slot
+        // with the head as the map's outer coordinate
+        const int row = p.nhd ? page * p.P + (key & (p.P - 1))
+                              : (page * p.Hk + it.kvh) * p.P + (key & (p.P - 1));
+        const uint32_t vdst = STAGE(cc) + uint32_t(lane) * 2u * box_bytes;
         if (is_v) {
-          ptx::tma_load_4d(STAGE(cc) + uint32_t(lane) * 2u * box_bytes, &tm_v, FULL(cc), 0, 0, 0,
-                           row >> 3, pol);
+          if (p.nhd) ptx::tma_load_5d(vdst, &tm_v, FULL(cc), 0, 0, 0, row >> 3, it.kvh, pol);
+          else ptx::tma_load_4d(vdst, &tm_v, FULL(cc), 0, 0, 0, row >> 3, pol);
         } else if (p.box_rows == kTileN) {
-          ptx::tma_load_3d(STAGE(cc), &tm_k, FULL(cc), 0, row, 0, pol);
+          if (p.nhd) ptx::tma_load_4d(STAGE(cc), &tm_k, FULL(cc), 0, row, 0, it.kvh, pol);
+          else ptx::tma_load_3d(STAGE(cc), &tm_k, FULL(cc), 0, row, 0, pol);
         } else {
-          for (int h = 0; h < 2; ++h)
-            ptx::tma_load_3d(STAGE(cc) + h * kHalfBytes + uint32_t(lane) * box_bytes, &tm_k,
-                             FULL(cc), 0, h, row, pol);
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t kdst = STAGE(cc) + h * kHalfBytes + uint32_t(lane) * box_bytes;
+            if (p.nhd) ptx::tma_load_4d(kdst, &tm_k, FULL(cc), 0, h, row, it.kvh, pol);
+            else ptx::tma_load_3d(kdst, &tm_k, FULL(cc), 0, h, row, pol);
+          }
         }
       }
     };
@@ -753,8 +760,11 @@ __global__ void __launch_bounds__(256) rope_prepass_kernel(const RopePrepassPara
       // the key's position: its index, or its page's logical position + slot
       const int kpos = p.page_pos ? __ldg(p.page_pos + entry) + j % p.P : j;
       const RopeChunk t = rope_chunk(p.rope_nat + size_t(min(kpos, p.rope_max_pos)) * (D / 2), c);
-      const size_t head_stride = size_t(p.P) * D;
-      const uint16_t* src = p.k_pages + (size_t(page) * p.Hk * p.P + (j % p.P)) * D;
+      // HND: a head's P rows are contiguous; NHD: a token's Hk heads are
+      const size_t head_stride = p.nhd ? size_t(D) : size_t(p.P) * D;
+      const uint16_t* src =
+          p.k_pages + (p.nhd ? (size_t(page) * p.P + (j % p.P)) * p.Hk * D
+                             : (size_t(page) * p.Hk * p.P + (j % p.P)) * D);
       uint16_t* dst = p.rotk + size_t(r) * D;
 #pragma unroll 4
       for (int kvh = 0; kvh < p.Hk; ++kvh)

@@ -35,100 +35,117 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // elements, loaded 16 rows x 64 columns at a time into 128B-swizzled tiles.
 // D = 128: rank 3 {64 cols, 2 column blocks, rows} so one box is one column
 // block of 16 rows; D = 64: rank 2 {64 cols, rows}.
-bool encode_pool(CUtensorMap* tm, const void* base, int64_t rows, int D, int box_rows) {
+// Page pools are [pages, Hk, P, D] (HND: a (page, head) block of P rows is
+// contiguous; rows = pages * Hk * P, row (page * Hk + h) * P + t) or
+// [pages, P, Hk, D] (NHD: token-major; token rows = pages * P, row page * P + t,
+// the head an outer map dimension of stride D elements).  Every map below lands
+// the same shared-memory layout in both cases; only the coordinates differ.
+struct PoolGeom {
+  int64_t rows;     // HND rows (pages * Hk * P)
+  int32_t Hk;
+  bool nhd;
+  int64_t tok_rows() const { return rows / Hk; }
+};
+
+bool encode(CUtensorMap* tm, CUtensorMapDataType dt, cuuint32_t rank, const void* base,
+            const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[3];
-  cuuint64_t strides[2];
-  cuuint32_t box[3];
-  cuuint32_t estr[3] = {1, 1, 1};
-  cuuint32_t rank;
-  if (D == 128) {
-    rank = 3;
-    dims[0] = 64; dims[1] = 2; dims[2] = cuuint64_t(rows);
-    strides[0] = 128; strides[1] = 256;
-    box[0] = 64; box[1] = 1; box[2] = cuuint32_t(box_rows);
-  } else {
-    rank = 2;
-    dims[0] = 64; dims[1] = cuuint64_t(rows);
-    strides[0] = 128;
-    box[0] = 64; box[1] = cuuint32_t(box_rows);
-  }
-  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  const CUresult r = fn(tm, dt, rank, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
-// Tensor map over a page pool for the decode kernel's 16-key stages.  D = 128: rank 3
-// {64 cols, rows, 2 column blocks} with the column blocks as the outer dimension (row
-// stride 256 B, block stride 128 B), so that one box {64, 16, 2} lands the stage as
-// [column block][16 rows][128 B], 128B-swizzled: one 4 KB copy where two 2 KB ones
-// would do (a TMA copy's cost is mostly per box: ~26 B/clk per SM with 4 KB boxes
-// against ~20 with 2 KB ones).  D = 64: rank 2, one 2 KB box.
-bool encode_pool_stage(CUtensorMap* tm, const void* base, int64_t rows, int D,
+// Prefill K tiles of fewer than 128 rows: one 64-column block of R rows per box,
+// landing [R rows][128 B] (D = 128).
+bool encode_pool(CUtensorMap* tm, const void* base, const PoolGeom& g, int box_rows) {
+  constexpr auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (!g.nhd) {
+    const cuuint64_t dims[3] = {64, 2, cuuint64_t(g.rows)};
+    const cuuint64_t strides[2] = {128, 256};
+    const cuuint32_t box[3] = {64, 1, cuuint32_t(box_rows)};
+    return encode(tm, BF, 3, base, dims, strides, box);
+  }
+  const cuuint64_t dims[4] = {64, 2, cuuint64_t(g.tok_rows()), cuuint64_t(g.Hk)};
+  const cuuint64_t strides[3] = {128, cuuint64_t(g.Hk) * 256, 256};
+  const cuuint32_t box[4] = {64, 1, cuuint32_t(box_rows), 1};
+  return encode(tm, BF, 4, base, dims, strides, box);
+}
+
+// Tensor map over a page pool for the decode kernel's 16-key stages (and the
+// prefill kernel's whole 128-row K tiles).  D = 128: the two 64-column blocks are
+// an outer dimension (stride 128 B), so one box {64, rows, 2} lands the tile as
+// [column block][rows][128 B], 128B-swizzled: one copy where two would do (a TMA
+// copy's cost is mostly per box: ~26 B/clk per SM with 4 KB boxes against ~20
+// with 2 KB ones).  D = 64: one box of [rows][128 B].
+bool encode_pool_stage(CUtensorMap* tm, const void* base, const PoolGeom& g, int D,
                        int box_rows = bsr::kStageTokens) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[3];
-  cuuint64_t strides[2];
-  cuuint32_t box[3];
-  cuuint32_t estr[3] = {1, 1, 1};
-  cuuint32_t rank;
+  constexpr auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const cuuint64_t hs = cuuint64_t(D) * 2;   // bytes of one head row
   if (D == 128) {
-    rank = 3;
-    dims[0] = 64; dims[1] = cuuint64_t(rows); dims[2] = 2;
-    strides[0] = 256; strides[1] = 128;
-    box[0] = 64; box[1] = cuuint32_t(box_rows); box[2] = 2;
-  } else {
-    rank = 2;
-    dims[0] = 64; dims[1] = cuuint64_t(rows);
-    strides[0] = 128;
-    box[0] = 64; box[1] = cuuint32_t(box_rows);
+    if (!g.nhd) {
+      const cuuint64_t dims[3] = {64, cuuint64_t(g.rows), 2};
+      const cuuint64_t strides[2] = {hs, 128};
+      const cuuint32_t box[3] = {64, cuuint32_t(box_rows), 2};
+      return encode(tm, BF, 3, base, dims, strides, box);
+    }
+    const cuuint64_t dims[4] = {64, cuuint64_t(g.tok_rows()), 2, cuuint64_t(g.Hk)};
+    const cuuint64_t strides[3] = {cuuint64_t(g.Hk) * hs, 128, hs};
+    const cuuint32_t box[4] = {64, cuuint32_t(box_rows), 2, 1};
+    return encode(tm, BF, 4, base, dims, strides, box);
   }
-  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  if (!g.nhd) {
+    const cuuint64_t dims[2] = {64, cuuint64_t(g.rows)};
+    const cuuint64_t strides[1] = {hs};
+    const cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+    return encode(tm, BF, 2, base, dims, strides, box);
+  }
+  const cuuint64_t dims[3] = {64, cuuint64_t(g.tok_rows()), cuuint64_t(g.Hk)};
+  const cuuint64_t strides[2] = {cuuint64_t(g.Hk) * hs, hs};
+  const cuuint32_t box[3] = {64, cuuint32_t(box_rows), 1};
+  return encode(tm, BF, 3, base, dims, strides, box);
 }
 
-// Tensor map over an FP8 (E4M3, one byte per element) page pool with D = 128:
-// rank 2 {128 bytes, rows}; one box is a 16-key stage, [16 rows][128 B],
-// 128B-swizzled (a row is one whole head).
-bool encode_pool_e4m3(CUtensorMap* tm, const void* base, int64_t rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {128, cuuint64_t(rows)};
-  cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {128, bsr::kStageTokens};
-  cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+// Tensor map over an FP8 (E4M3, one byte per element) page pool with D = 128: one
+// box is a 16-key stage, [16 rows][128 B], 128B-swizzled (a row is a whole head).
+bool encode_pool_e4m3(CUtensorMap* tm, const void* base, const PoolGeom& g) {
+  constexpr auto U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if (!g.nhd) {
+    const cuuint64_t dims[2] = {128, cuuint64_t(g.rows)};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, bsr::kStageTokens};
+    return encode(tm, U8, 2, base, dims, strides, box);
+  }
+  const cuuint64_t dims[3] = {128, cuuint64_t(g.tok_rows()), cuuint64_t(g.Hk)};
+  const cuuint64_t strides[2] = {cuuint64_t(g.Hk) * 128, 128};
+  const cuuint32_t box[3] = {128, bsr::kStageTokens, 1};
+  return encode(tm, U8, 3, base, dims, strides, box);
 }
 
-// Tensor map over a D = 128 page pool for the prefill kernel's V tiles: rank 4 {64
-// cols, 8 rows, 2 column blocks, rows / 8 row groups}; a box {64, 8, 2, box_rows / 8}
-// lands as [row group][column block][8 rows][128 B], 128B-swizzled, so the boxes of a
-// 128-key tile stack into one uniform layout (8-row groups 2 KB apart, the column
-// blocks of a group 1 KB apart) whatever the page size: one box per page-sized piece.
-// rows must be a multiple of 8.
-bool encode_pool_groups(CUtensorMap* tm, const void* base, int64_t rows, int box_rows) {
-  auto fn = encode_fn();
-  if (fn == nullptr || rows % 8 != 0 || box_rows % 8 != 0) return false;
-  cuuint64_t dims[4] = {64, 8, 2, cuuint64_t(rows / 8)};
-  cuuint64_t strides[3] = {256, 128, 2048};
-  cuuint32_t box[4] = {64, 8, 2, cuuint32_t(box_rows / 8)};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
-                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+// Tensor map over a D = 128 page pool for the prefill kernel's V tiles: a box {64
+// cols, 8 rows, 2 column blocks, box_rows / 8 row groups} lands as [row group]
+// [column block][8 rows][128 B], 128B-swizzled, so the boxes of a 128-key tile
+// stack into one uniform layout (8-row groups 2 KB apart, the column blocks of a
+// group 1 KB apart) whatever the page size: one box per page-sized piece.
+// Rows (token rows with NHD) must be a multiple of 8.
+bool encode_pool_groups(CUtensorMap* tm, const void* base, const PoolGeom& g, int box_rows) {
+  constexpr auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  if (box_rows % 8 != 0) return false;
+  if (!g.nhd) {
+    if (g.rows % 8 != 0) return false;
+    const cuuint64_t dims[4] = {64, 8, 2, cuuint64_t(g.rows / 8)};
+    const cuuint64_t strides[3] = {256, 128, 2048};
+    const cuuint32_t box[4] = {64, 8, 2, cuuint32_t(box_rows / 8)};
+    return encode(tm, BF, 4, base, dims, strides, box);
+  }
+  if (g.tok_rows() % 8 != 0) return false;
+  const cuuint64_t rs = cuuint64_t(g.Hk) * 256;   // token row stride
+  const cuuint64_t dims[5] = {64, 8, 2, cuuint64_t(g.tok_rows() / 8), cuuint64_t(g.Hk)};
+  const cuuint64_t strides[4] = {rs, 128, 8 * rs, 256};
+  const cuuint32_t box[5] = {64, 8, 2, cuuint32_t(box_rows / 8), 1};
+  return encode(tm, BF, 5, base, dims, strides, box);
 }
 
 // Tensor map over q (or its rotated copy) [rows, Hq, D = 128] (16-bit) for the
@@ -173,8 +190,9 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
   const bool smallp = s->P < bsr::kStageTokens;
   const int64_t rows = int64_t(s->num_pages) * s->Hk * s->P;
   if (!smallp && (s->tm_k_ptr != k_pages || s->tm_v_ptr != v_pages)) {
-    if (rows <= 0 || !encode_pool_stage(&s->tm_k, k_pages, rows, s->D) ||
-        !encode_pool_stage(&s->tm_v, v_pages, rows, s->D)) {
+    const PoolGeom geom{rows, s->Hk, s->kv_layout == BSR_KV_NHD};
+    if (rows <= 0 || !encode_pool_stage(&s->tm_k, k_pages, geom, s->D) ||
+        !encode_pool_stage(&s->tm_v, v_pages, geom, s->D)) {
       s->tm_k_ptr = s->tm_v_ptr = nullptr;
       return BSR_ERR_CUDA;
     }
@@ -230,6 +248,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.num_warps = s->dec_warps;
     p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
     p.window_left = s->window_left;
+    p.nhd = s->kv_layout == BSR_KV_NHD;
     p.wait_limit_ns = wait_limit_ns;
     const bool r16 = s->max_rows > 8;
     t_mark(0, 0);
@@ -247,8 +266,9 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     if (rotk) {
       // rotate the prefill requests' keys and queries once into the schedule's buffers
       if (!s->tm_rk_valid) {
-        if (!encode_pool_stage(&s->tm_rk, s->d_ws + s->off_rotk, int64_t(s->Hk) * s->rk_total,
-                               s->D, bsr::kPrefillKeyTile))
+        // the dense rotated-K buffer [Hk][rk_total][D] is head-major like an HND pool
+        const PoolGeom rk{int64_t(s->Hk) * s->rk_total, s->Hk, false};
+        if (!encode_pool_stage(&s->tm_rk, s->d_ws + s->off_rotk, rk, s->D, bsr::kPrefillKeyTile))
           return BSR_ERR_CUDA;
         s->tm_rk_valid = true;
       }
@@ -262,6 +282,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
       r.rq_start = s->dev<const int32_t>(s->off_rq_start);
       r.rq_pos0 = s->dev<const int32_t>(s->off_rq_pos0);
       r.page_pos = s->has_page_pos ? s->dev<const int32_t>(s->off_page_pos) : nullptr;
+      r.nhd = s->kv_layout == BSR_KV_NHD;
       r.rope_nat = reinterpret_cast<const float2*>(s->d_rope + s->rope_bytes);
       r.rotk = s->dev<uint16_t>(s->off_rotk);
       r.rotq = s->dev<uint16_t>(s->off_rotq);
@@ -292,13 +313,14 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     // K/V boxes of min(P, 128) rows (the prefill class has P >= 16)
     const int box_rows = s->P < bsr::kPrefillKeyTile ? s->P : bsr::kPrefillKeyTile;
     if (s->tm_pk_ptr != k_pages || s->tm_pv_ptr != v_pages) {
+      const PoolGeom pgeom{rows, s->Hk, s->kv_layout == BSR_KV_NHD};
       // K: a whole 128-key tile in one box when a page holds it, else one box per
       // column block and page; V: one box per page-sized piece (row-group layout)
       const bool k_whole = box_rows == bsr::kPrefillKeyTile;
       if (rows <= 0 ||
-          !(k_whole ? encode_pool_stage(&s->tm_pk, k_pages, rows, s->D, box_rows)
-                    : encode_pool(&s->tm_pk, k_pages, rows, s->D, box_rows)) ||
-          !encode_pool_groups(&s->tm_pv, v_pages, rows, box_rows)) {
+          !(k_whole ? encode_pool_stage(&s->tm_pk, k_pages, pgeom, s->D, box_rows)
+                    : encode_pool(&s->tm_pk, k_pages, pgeom, box_rows)) ||
+          !encode_pool_groups(&s->tm_pv, v_pages, pgeom, box_rows)) {
         s->tm_pk_ptr = s->tm_pv_ptr = nullptr;
         return BSR_ERR_CUDA;
       }
@@ -327,6 +349,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.out_v8 = aligned(out, 32);
     p.num_ctas = s->pre_ctas;
     p.window_left = s->window_left;
+    p.nhd = s->kv_layout == BSR_KV_NHD;
     p.wait_limit_ns = wait_limit_ns;
     t_mark(2, 0);
     cudaError_t e =
@@ -424,8 +447,9 @@ extern "C" int bsr_attn_run_kv8(bsr_schedule_t s, const void* q, const void* k_p
   const cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const int64_t rows = int64_t(s->num_pages) * s->Hk * s->P;
   if (s->tm_k8_ptr != k_pages || s->tm_v8_ptr != v_pages) {
-    if (rows <= 0 || !encode_pool_e4m3(&s->tm_k8, k_pages, rows) ||
-        !encode_pool_e4m3(&s->tm_v8, v_pages, rows)) {
+    const PoolGeom geom{rows, s->Hk, s->kv_layout == BSR_KV_NHD};
+    if (rows <= 0 || !encode_pool_e4m3(&s->tm_k8, k_pages, geom) ||
+        !encode_pool_e4m3(&s->tm_v8, v_pages, geom)) {
       s->tm_k8_ptr = s->tm_v8_ptr = nullptr;
       return BSR_ERR_CUDA;
     }
@@ -468,6 +492,7 @@ extern "C" int bsr_attn_run_kv8(bsr_schedule_t s, const void* q, const void* k_p
   p.num_warps = s->dec_warps;
   p.rope_max_pos = 0;
   p.window_left = s->window_left;
+  p.nhd = s->kv_layout == BSR_KV_NHD;
   p.wait_limit_ns = 1000000000ull;
   t_mark(0, 0);
   const cudaError_t e = bsr::launch_decode_kv8(s->max_rows > 8, s->tm_k8, s->tm_v8, p,

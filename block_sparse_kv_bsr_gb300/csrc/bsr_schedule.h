@@ -21,6 +21,7 @@ struct bsr_schedule {
   int64_t sum_qo = 0, active_tokens = 0;
   int32_t rope_rows = 0;       // rows of the cos/sin table (0 without RoPE)
   int32_t window_left = 0;     // sliding window (0: none)
+  int32_t kv_layout = 0;       // BSR_KV_HND or BSR_KV_NHD
   // per-page logical positions for RoPE (uploaded with the image when given)
   bool has_page_pos = false;
   size_t off_page_pos = 0, off_qshift = 0;

@@ -67,6 +67,8 @@ enum {
 };
 
 enum { BSR_DTYPE_BF16 = 0, BSR_DTYPE_F32 = 1 };
+/* page pool layouts: head-major [pages, Hk, P, D] or token-major [pages, P, Hk, D] */
+enum { BSR_KV_HND = 0, BSR_KV_NHD = 1 };
 
 typedef struct bsr_schedule* bsr_schedule_t;
 
@@ -106,6 +108,11 @@ typedef struct bsr_schedule* bsr_schedule_t;
  * cached order.  Entries must be in [0, 2^29); with RoPE, page_size must be at
  * least 16 (else BSR_ERR_UNSUPPORTED).  Without RoPE the array is not used.
  *
+ * kv_layout: BSR_KV_HND, pages [num_pages_in_pool, Hk, P, D] (one head's P
+ * tokens contiguous), or BSR_KV_NHD, pages [num_pages_in_pool, P, Hk, D] (one
+ * token's heads contiguous, the token-major layout some serving engines keep).
+ * Every run of the schedule reads k_pages / v_pages in that layout.
+ *
  * *schedule must be NULL (a new schedule is created) or a schedule returned
  * by an earlier plan, which is then re-planned in place: its device workspace
  * is reused when large enough.  Re-planning is ordered on `stream` after work
@@ -116,8 +123,8 @@ typedef struct bsr_schedule* bsr_schedule_t;
 int bsr_attn_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
                   int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                   int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
-                  int32_t causal, int32_t window_left, const int32_t* page_pos, float rope_theta,
-                  void* stream, bsr_schedule_t* schedule);
+                  int32_t causal, int32_t window_left, const int32_t* page_pos,
+                  int32_t kv_layout, float rope_theta, void* stream, bsr_schedule_t* schedule);
 
 /*
  * bsr_attn_run — execute a schedule: out = softmax(sm_scale * q k^T) v and
@@ -181,7 +188,8 @@ int bsr_merge_states(const void* o_a, const float* lse_a, const void* o_b, const
  * request b appends n_b = append_indptr[b+1] - append_indptr[b] tokens, which
  * take positions L_b - n_b .. L_b - 1.  k_new, v_new: bf16
  * [num_new_tokens, Hk, D]; k_pages, v_pages: bf16 [num_pages_in_pool, Hk, P, D],
- * written in place; every other slot keeps its bits.  The device-resident
+ * written in place (kv_layout: BSR_KV_HND or BSR_KV_NHD, as for plan); every
+ * other slot keeps its bits.  The device-resident
  * table cannot be checked on the host: a token whose page id falls outside
  * [0, num_pages_in_pool) or whose request cannot hold it is skipped, and bit
  * 1 is OR-ed into *device_status (a device int32, may be NULL) for the caller
@@ -190,8 +198,8 @@ int bsr_merge_states(const void* o_a, const float* lse_a, const void* o_b, const
 int bsr_append_kv(const void* k_new, const void* v_new, const int32_t* append_indptr,
                   const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
                   int32_t batch, int64_t num_new_tokens, int32_t num_kv_heads, int32_t head_dim,
-                  int32_t page_size, int32_t num_pages_in_pool, void* k_pages, void* v_pages,
-                  int32_t* device_status, void* stream);
+                  int32_t page_size, int32_t num_pages_in_pool, int32_t kv_layout,
+                  void* k_pages, void* v_pages, int32_t* device_status, void* stream);
 
 /* Free a schedule's device workspace and host buffers after synchronizing
  * the device.  NULL is ignored. */
@@ -217,6 +225,8 @@ typedef struct bsr_schedule_info {
   int32_t kernels_per_run;    /* kernels one bsr_attn_run launches (decode, RoPE pre-pass,
                                  prefill, split-range merge; 0 when there is no work) */
   int32_t window_left;        /* sliding window given to plan (0: none) */
+  int32_t kv_layout;          /* BSR_KV_HND or BSR_KV_NHD */
+  int32_t reserved;
 } bsr_schedule_info_t;
 
 int bsr_schedule_get_info(bsr_schedule_t schedule, bsr_schedule_info_t* info);
@@ -255,9 +265,9 @@ int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
                        const int32_t* last_page_len, int32_t batch, int32_t num_qo_heads,
                        int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                        const int32_t* qo_indptr, int32_t num_pages_in_pool, int32_t causal,
-                       int32_t window_left, const int32_t* page_pos, float rope_theta,
-                       int32_t num_sms, bsr_schedule_info_t* info, int32_t* units,
-                       int64_t max_units);
+                       int32_t window_left, const int32_t* page_pos, int32_t kv_layout,
+                       float rope_theta, int32_t num_sms, bsr_schedule_info_t* info,
+                       int32_t* units, int64_t max_units);
 
 /*
  * bsr_attn_decode_noalloc — decode attention that allocates nothing.

@@ -33,6 +33,7 @@ def plan(w: wl.Paged, schedule=None):
                              head_dim=w.head_dim, page_size=w.page_size, num_pages=w.num_pages,
                              qo_indptr=w.qo_indptr, causal=w.causal, rope_theta=w.rope_theta,
                              window_left=w.window_left, page_pos=w.page_pos,
+                             kv_layout=w.kv_layout,
                              schedule=schedule)
 
 
@@ -53,7 +54,8 @@ def oracle_full(w: wl.Paged, k_pages=None, v_pages=None):
                             num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                             page_size=w.page_size, sm_scale=w.sm_scale,
                             rope_theta=w.rope_theta, causal=w.causal,
-                            window_left=w.window_left, page_pos=w.page_pos)
+                            window_left=w.window_left, page_pos=w.page_pos,
+                            kv_layout=w.kv_layout)
 
 
 def oracle_rows(w: wl.Paged, rows, heads, k_pages=None, v_pages=None):
@@ -63,8 +65,8 @@ def oracle_rows(w: wl.Paged, rows, heads, k_pages=None, v_pages=None):
                             num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
                             page_size=w.page_size, sm_scale=w.sm_scale,
                             rope_theta=w.rope_theta, causal=w.causal,
-                            window_left=w.window_left, page_pos=w.page_pos, rows=rows,
-                            heads=heads)
+                            window_left=w.window_left, page_pos=w.page_pos,
+                            kv_layout=w.kv_layout, rows=rows, heads=heads)
 
 
 def sample_rows(w: wl.Paged, n: int, seed: int = 0):

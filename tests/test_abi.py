@@ -85,5 +85,8 @@ def test_plan_host_rejects(lib, kw, code):
 def test_entry_points_reject_bad_arguments_without_a_gpu(lib):
     assert lib.bsr_attn_run(None, None, None, None, 1.0, 0.0, 0, None, 0, None, None) == -1
     assert lib.bsr_merge_states(None, None, None, None, 1, 1, 96, 0, None, None, None) == -2
-    assert lib.bsr_append_kv(None, None, None, None, None, None, 1, 1, 1, 128, 3, 1,
+    assert lib.bsr_append_kv(None, None, None, None, None, None, 1, 1, 1, 128, 3, 1, 0,
                              None, None, None, None) == -2
+    # an unknown page layout
+    assert lib.bsr_append_kv(None, None, None, None, None, None, 1, 1, 1, 128, 16, 1, 7,
+                             None, None, None, None) == -1
