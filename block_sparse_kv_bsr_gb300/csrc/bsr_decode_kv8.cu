@@ -31,6 +31,7 @@
 
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 
 #include "bsr_decode.cuh"
 #include "bsr_schedule.h"
@@ -215,59 +216,86 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       for (int r = 0; r < NR; ++r) o[n][r] = 0.f;
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
 
-#pragma unroll 1
-    for (int st = 0; st < nst; ++st) {
-      const int slot = int(c_seq % kStages8);
-      const uint32_t kt = ring + uint32_t(slot * kStage8), vt = kt + kTile8;
-      const int tok = ci.tok0 + kStageTokens * st;
-      const int nvalid = min(kStageTokens, ci.tok1 - tok);
-      if (!ptx::mbar_wait_bounded(bars + 8 * slot, (c_seq / kStages8) & 1u, p.wait_limit_ns)) {
-        failed = true;
-        break;
+    // One step consumes NS ring stages (16 keys each): two while at least two
+    // remain, so that the Q K^T products of both interleave (four independent
+    // accumulator chains) and the max, its shuffles and the O rescale run once
+    // per 32 keys; a last odd stage goes alone.
+    auto step = [&](auto ns_c, int st) -> bool {
+      constexpr int NS = decltype(ns_c)::value;
+      uint32_t kt[NS], vt[NS];
+      int tok[NS], nvalid[NS];
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        const uint32_t sq = c_seq + uint32_t(s);
+        const int slot = int(sq % kStages8);
+        kt[s] = ring + uint32_t(slot * kStage8);
+        vt[s] = kt[s] + kTile8;
+        tok[s] = ci.tok0 + kStageTokens * (st + s);
+        nvalid[s] = min(kStageTokens, ci.tok1 - tok[s]);
+        if (!ptx::mbar_wait_bounded(bars + 8 * slot, (sq / kStages8) & 1u, p.wait_limit_ns))
+          return false;
       }
-      if (nvalid < kStageTokens) {
-        // Rows past the valid keys may hold another page's tail (NaN codes
-        // included): zero their V codes so that P = 0 contributes exactly 0.
+      bool zeroed = false;
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        if (nvalid[s] < kStageTokens) {
+          // Rows past the valid keys may hold another page's tail (NaN codes
+          // included): zero their V codes so that P = 0 contributes exactly 0.
+          zeroed = true;
 #pragma unroll 1
-        for (int idx = lane; idx < (kStageTokens - nvalid) * 8; idx += 32) {
-          const int t = nvalid + idx / 8, c = idx % 8;
-          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vt + tile8_off(t, c)),
-                       "r"(0u)
-                       : "memory");
+          for (int idx = lane; idx < (kStageTokens - nvalid[s]) * 8; idx += 32) {
+            const int t = nvalid[s] + idx / 8, c = idx % 8;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vt[s] + tile8_off(t, c)),
+                         "r"(0u)
+                         : "memory");
+          }
         }
       }
       __syncwarp();
 
-      // ---------------- S = Q K^T  (two n-tiles of 8 keys), 32 dims per ldmatrix
-      float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+      // ---------------- S = Q K^T  (per stage two n-tiles of 8 keys), 32 dims per ldmatrix
+      float sacc[NS][2][4];
+#pragma unroll
+      for (int s = 0; s < NS; ++s)
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) sacc[s][n][r] = 0.f;
 #pragma unroll
       for (int pr = 0; pr < KB / 2; ++pr) {
-        uint32_t kr[4];
-        ptx::ldsm_x4(kr, kt + tile8_off(k_tok, 2 * pr + k_cb));
-        // kr[h]: keys g4 (n-tile 0), block 2 pr + h; kr[2 + h]: keys 8 + g4 (n-tile 1)
+        uint32_t kr[NS][4];
+#pragma unroll
+        for (int s = 0; s < NS; ++s) ptx::ldsm_x4(kr[s], kt[s] + tile8_off(k_tok, 2 * pr + k_cb));
+        // kr[s][h]: keys g4 (n-tile 0), block 2 pr + h; kr[s][2 + h]: keys 8 + g4 (n-tile 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int kb = 2 * pr + h;
           const uint32_t a0 = qh[kb][0], a2 = qh[kb][NR / 2];
           const uint32_t a1 = R16 ? qh[kb][1] : 0u, a3 = R16 ? qh[kb][NR - 1] : 0u;
-          ptx::mma_f16(s0[0], s0[1], s0[2], s0[3], a0, a1, a2, a3, e4m3x2_to_f16x2(kr[h]),
-                       e4m3x2_to_f16x2(kr[h] >> 16));
-          ptx::mma_f16(s1[0], s1[1], s1[2], s1[3], a0, a1, a2, a3, e4m3x2_to_f16x2(kr[2 + h]),
-                       e4m3x2_to_f16x2(kr[2 + h] >> 16));
+#pragma unroll
+          for (int s = 0; s < NS; ++s) {
+            float* s0 = sacc[s][0];
+            float* s1 = sacc[s][1];
+            ptx::mma_f16(s0[0], s0[1], s0[2], s0[3], a0, a1, a2, a3, e4m3x2_to_f16x2(kr[s][h]),
+                         e4m3x2_to_f16x2(kr[s][h] >> 16));
+            ptx::mma_f16(s1[0], s1[1], s1[2], s1[3], a0, a1, a2, a3, e4m3x2_to_f16x2(kr[s][2 + h]),
+                         e4m3x2_to_f16x2(kr[s][2 + h] >> 16));
+          }
         }
       }
 
       // ---------------- mask + online softmax (log2 domain; k_scale is in scale_log2)
-      const bool full = (nvalid == kStageTokens) &&
-                        (!p.causal || tok + kStageTokens - 1 <= qpos_min) &&
-                        (!WIN || tok >= wlo_max);
-      float xa[4], xb[4];
-      {
+      float xa[NS][4], xb[NS][4];
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        const bool full = (nvalid[s] == kStageTokens) &&
+                          (!p.causal || tok[s] + kStageTokens - 1 <= qpos_min) &&
+                          (!WIN || tok[s] >= wlo_max);
         const float sc = p.scale_log2;
-        const int k0 = tok + 2 * t4;
+        const int k0 = tok[s] + 2 * t4;
         const int kidx[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
-        const float sa[4] = {s0[0], s0[1], s1[0], s1[1]};
-        const float sb[4] = {s0[2], s0[3], s1[2], s1[3]};
+        const float sa[4] = {sacc[s][0][0], sacc[s][0][1], sacc[s][1][0], sacc[s][1][1]};
+        const float sb[4] = {sacc[s][0][2], sacc[s][0][3], sacc[s][1][2], sacc[s][1][3]};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const bool inr = full || (kidx[j] < ci.tok1);
@@ -275,34 +303,54 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
               full || (inr && (!p.causal || kidx[j] <= qposA) && (!WIN || kidx[j] >= wlo_A));
           const bool okB =
               full || (inr && (!p.causal || kidx[j] <= qposB) && (!WIN || kidx[j] >= wlo_B));
-          xa[j] = okA ? sa[j] * sc : -INFINITY;
-          xb[j] = okB ? sb[j] * sc : -INFINITY;
+          xa[s][j] = okA ? sa[j] * sc : -INFINITY;
+          xb[s][j] = okB ? sb[j] * sc : -INFINITY;
         }
       }
-      float mxA = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
+      float mxA = -INFINITY;
+#pragma unroll
+      for (int s = 0; s < NS; ++s)
+        mxA = fmaxf(mxA, fmaxf(fmaxf(xa[s][0], xa[s][1]), fmaxf(xa[s][2], xa[s][3])));
       mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 1));
       mxA = fmaxf(mxA, __shfl_xor_sync(0xffffffffu, mxA, 2));
       const float mnA = fmaxf(mA, mxA);
       const float muA = mnA == -INFINITY ? 0.f : mnA;
       const float alA = ptx::ex2(mA - muA);
       mA = mnA;
-      float pa[4];
+      float pa[NS][4];
+      float sumA = 0.f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) pa[j] = ptx::ex2(xa[j] - muA);
-      lA = lA * alA + ((pa[0] + pa[1]) + (pa[2] + pa[3]));
+      for (int s = 0; s < NS; ++s) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pa[s][j] = ptx::ex2(xa[s][j] - muA);
+        sumA += (pa[s][0] + pa[s][1]) + (pa[s][2] + pa[s][3]);
+      }
+      lA = lA * alA + sumA;
       float alB = 1.f;
-      float pb[4] = {0.f, 0.f, 0.f, 0.f};
+      float pb[NS][4];
+#pragma unroll
+      for (int s = 0; s < NS; ++s)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) pb[s][j] = 0.f;
       if constexpr (R16) {
-        float mxB = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
+        float mxB = -INFINITY;
+#pragma unroll
+        for (int s = 0; s < NS; ++s)
+          mxB = fmaxf(mxB, fmaxf(fmaxf(xb[s][0], xb[s][1]), fmaxf(xb[s][2], xb[s][3])));
         mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 1));
         mxB = fmaxf(mxB, __shfl_xor_sync(0xffffffffu, mxB, 2));
         const float mnB = fmaxf(mB, mxB);
         const float muB = mnB == -INFINITY ? 0.f : mnB;
         alB = ptx::ex2(mB - muB);
         mB = mnB;
+        float sumB = 0.f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) pb[j] = ptx::ex2(xb[j] - muB);
-        lB = lB * alB + ((pb[0] + pb[1]) + (pb[2] + pb[3]));
+        for (int s = 0; s < NS; ++s) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) pb[s][j] = ptx::ex2(xb[s][j] - muB);
+          sumB += (pb[s][0] + pb[s][1]) + (pb[s][2] + pb[s][3]);
+        }
+        lB = lB * alB + sumB;
       }
       if (__any_sync(0xffffffffu, alA != 1.f || alB != 1.f)) {
 #pragma unroll
@@ -316,44 +364,62 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         }
       }
 
-      // ---------------- O += P V  (P in fp16), 32 dims per ldmatrix
-      const uint32_t ph0 = ptx::pack_f16(pa[0], pa[1]), ph2 = ptx::pack_f16(pa[2], pa[3]);
-      const uint32_t ph1 = R16 ? ptx::pack_f16(pb[0], pb[1]) : 0u;
-      const uint32_t ph3 = R16 ? ptx::pack_f16(pb[2], pb[3]) : 0u;
+      // ---------------- O += P V  (P in fp16), 32 dims per ldmatrix; stage by stage,
+      // so that the two products into one accumulator are 16 MMAs apart
 #pragma unroll
-      for (int pr = 0; pr < KB / 2; ++pr) {
-        uint32_t vr[4];
-        ptx::ldsm_x4_trans(vr, vt + tile8_off(v_tok, 2 * pr + v_cb));
-        // vr[2h]: keys 2t, 2t+1 of the first 8 keys, dims (2 g4, 2 g4 + 1) of block
-        // 2 pr + h; vr[2h + 1]: the same for keys 8 + 2t, 8 + 2t + 1
+      for (int s = 0; s < NS; ++s) {
+        const uint32_t ph0 = ptx::pack_f16(pa[s][0], pa[s][1]), ph2 = ptx::pack_f16(pa[s][2], pa[s][3]);
+        [[maybe_unused]] const uint32_t ph1 = R16 ? ptx::pack_f16(pb[s][0], pb[s][1]) : 0u;
+        [[maybe_unused]] const uint32_t ph3 = R16 ? ptx::pack_f16(pb[s][2], pb[s][3]) : 0u;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int cb = 2 * pr + h;
-          const uint32_t lo = vr[2 * h], hi = vr[2 * h + 1];
-          // even dims of the block (2 g4), then odd dims (2 g4 + 1)
-          const uint32_t be0 = e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0020));
-          const uint32_t be1 = e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0020));
-          const uint32_t bo0 = e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0031));
-          const uint32_t bo1 = e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0031));
-          float* e = o[2 * cb];
-          float* f = o[2 * cb + 1];
-          if constexpr (R16) {
-            ptx::mma_f16(e[0], e[1], e[NR - 2], e[NR - 1], ph0, ph1, ph2, ph3, be0, be1);
-            ptx::mma_f16(f[0], f[1], f[NR - 2], f[NR - 1], ph0, ph1, ph2, ph3, bo0, bo1);
-          } else {
-            // rows g4 + 8 are padding: their accumulators are dead scratch
-            float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
-            ptx::mma_f16(e[0], e[1], z0, z1, ph0, 0u, ph2, 0u, be0, be1);
-            ptx::mma_f16(f[0], f[1], z2, z3, ph0, 0u, ph2, 0u, bo0, bo1);
+        for (int pr = 0; pr < KB / 2; ++pr) {
+          uint32_t vr[4];
+          ptx::ldsm_x4_trans(vr, vt[s] + tile8_off(v_tok, 2 * pr + v_cb));
+          // vr[2h]: keys 2t, 2t+1 of the first 8 keys, dims (2 g4, 2 g4 + 1) of block
+          // 2 pr + h; vr[2h + 1]: the same for keys 8 + 2t, 8 + 2t + 1
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int cb = 2 * pr + h;
+            const uint32_t lo = vr[2 * h], hi = vr[2 * h + 1];
+            // even dims of the block (2 g4), then odd dims (2 g4 + 1)
+            const uint32_t be0 = e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0020));
+            const uint32_t be1 = e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0020));
+            const uint32_t bo0 = e4m3x2_to_f16x2(__byte_perm(lo, 0u, 0x0031));
+            const uint32_t bo1 = e4m3x2_to_f16x2(__byte_perm(hi, 0u, 0x0031));
+            float* e = o[2 * cb];
+            float* f = o[2 * cb + 1];
+            if constexpr (R16) {
+              ptx::mma_f16(e[0], e[1], e[NR - 2], e[NR - 1], ph0, ph1, ph2, ph3, be0, be1);
+              ptx::mma_f16(f[0], f[1], f[NR - 2], f[NR - 1], ph0, ph1, ph2, ph3, bo0, bo1);
+            } else {
+              // rows g4 + 8 are padding: their accumulators are dead scratch
+              float z0 = 0.f, z1 = 0.f, z2 = 0.f, z3 = 0.f;
+              ptx::mma_f16(e[0], e[1], z0, z1, ph0, 0u, ph2, 0u, be0, be1);
+              ptx::mma_f16(f[0], f[1], z2, z3, ph0, 0u, ph2, 0u, bo0, bo1);
+            }
           }
         }
       }
       __syncwarp();
       // generic writes (the zero fill) must be ordered before the TMA that reuses the slot
-      if (nvalid < kStageTokens) ptx::fence_proxy_async_smem();
+      if (zeroed) ptx::fence_proxy_async_smem();
       __syncwarp();
-      ++c_seq;
-      producer_issue();
+#pragma unroll
+      for (int s = 0; s < NS; ++s) {
+        ++c_seq;
+        producer_issue();
+      }
+      return true;
+    };
+    {
+      int st = 0;
+#pragma unroll 1
+      for (; st + 2 <= nst; st += 2)
+        if (!step(std::integral_constant<int, 2>{}, st)) {
+          failed = true;
+          break;
+        }
+      if (!failed && st < nst && !step(std::integral_constant<int, 1>{}, st)) failed = true;
     }
     if (failed) break;
 
