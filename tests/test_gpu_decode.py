@@ -9,7 +9,7 @@ import oracle
 import workloads as wl
 from block_sparse_kv_bsr_gb300 import _build
 from parity import (assert_lse_close, assert_out_close, bits, check_full, device_tensors, plan,
-                    run)
+                    run, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -236,3 +236,44 @@ def test_decode_rope_operand_range_sets_status():
     bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta, causal=w.causal)
     torch.cuda.synchronize()
     assert bsr.bsr_last_device_error(s) & 2
+
+
+@pytest.mark.parametrize("kv8", [False, True])
+def test_repeated_launches_bit_exact(kv8):
+    # Full-size skewed batch: every unit is computed exactly once per launch (outputs
+    # start as NaN each time) and the split-range counters end each launch at zero,
+    # so repeated launches of one schedule are bit-identical and match the oracle.
+    w = wl.config3(small=False)
+    if kv8:
+        w = wl.with_kv8(w, 91)
+    s = plan(w)
+    dev = "cuda:0"
+    q = w.q.to(dev)
+    k, v = ((w.k_codes, w.v_codes) if kv8 else (w.k_pages, w.v_pages))
+    k, v = k.to(dev), v.to(dev)
+    outs = []
+    for _ in range(4):
+        out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=dev)
+        lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=dev)
+        if kv8:
+            bsr.bsr_attn_run_kv8(s, q, k, v, k_scale=w.k_scale, v_scale=w.v_scale,
+                                 sm_scale=w.sm_scale, causal=w.causal, out=out, lse=lse)
+        else:
+            bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, causal=w.causal, out=out, lse=lse)
+        torch.cuda.synchronize()
+        assert bsr.bsr_last_device_error(s) == 0
+        assert not torch.isnan(out).any() and not torch.isnan(lse).any()
+        outs.append((bits_t(out).clone(), lse.clone()))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    rows, heads = sample_rows(w, 512)
+    kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+              page_size=w.page_size, sm_scale=w.sm_scale, causal=w.causal, rows=rows, heads=heads)
+    table = (w.indptr, w.indices, w.last_page_len, w.qo_indptr)
+    if kv8:
+        ro, rl = oracle.attention_kv8(w.q, w.k_codes, w.v_codes, w.k_scale, w.v_scale, *table, **kw)
+    else:
+        ro, rl = oracle.attention(w.q, w.k_pages, w.v_pages, *table, **kw)
+    o = outs[0][0].view(torch.bfloat16).float().cpu().numpy()[rows, heads]
+    assert_out_close(o, ro, True, w.name)
+    assert_lse_close(outs[0][1].cpu().numpy()[rows, heads], rl, w.name)
