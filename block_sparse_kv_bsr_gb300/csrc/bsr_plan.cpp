@@ -107,19 +107,41 @@ struct WorkList {
 // is a pure function of its inputs.
 void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align, int64_t overhead,
              int64_t min_piece, int64_t min_worker_work, WorkList* out) {
-  std::vector<int32_t> order(units.size());
-  std::iota(order.begin(), order.end(), 0);
-  std::stable_sort(order.begin(), order.end(),
-                   [&](int32_t x, int32_t y) {
-                     return units[x].kend - units[x].kbegin > units[y].kend - units[y].kbegin;
-                   });
+  // Working arrays live across calls (per thread), so a plan per decode step reuses
+  // their memory instead of faulting in fresh pages.
+  struct Scratch {
+    std::vector<uint64_t> keys;
+    std::vector<int32_t> order, owner, pieces_of_unit, first_slot, next_slot;
+    std::vector<int64_t> kb, ke, load;
+    std::vector<Piece> pieces;
+  };
+  thread_local Scratch sc;
+  // longest first, ties in unit order: one integer key per unit
+  sc.keys.resize(units.size());
+  for (size_t i = 0; i < units.size(); ++i)
+    sc.keys[i] = (uint64_t(uint32_t(INT32_MAX - (units[i].kend - units[i].kbegin))) << 32) | uint64_t(i);
+  std::sort(sc.keys.begin(), sc.keys.end());
+  std::vector<int32_t>& order = sc.order;
+  order.resize(units.size());
+  // key ranges in that order, contiguous for the cut passes
+  std::vector<int64_t>& kb = sc.kb;
+  std::vector<int64_t>& ke = sc.ke;
+  kb.resize(units.size());
+  ke.resize(units.size());
+  for (size_t i = 0; i < units.size(); ++i) {
+    order[i] = int32_t(sc.keys[i] & 0xffffffffu);
+    kb[i] = units[order[i]].kbegin;
+    ke[i] = units[order[i]].kend;
+  }
   int64_t total = 0;
   for (const Unit& u : units) total += u.kend - u.kbegin + overhead;
   const int workers =
       units.empty() ? 0
                     : int(std::max<int64_t>(1, std::min<int64_t>(max_workers, (total + min_worker_work - 1) / min_worker_work)));
-  std::vector<Piece> pieces;
-  std::vector<int32_t> owner;
+  std::vector<Piece>& pieces = sc.pieces;
+  std::vector<int32_t>& owner = sc.owner;
+  pieces.clear();
+  owner.clear();
   // Cut with budget T; returns the number of workers the cut needs (anything
   // above `workers` means "does not fit").
   auto partition = [&](int64_t T, bool record) -> int64_t {
@@ -128,9 +150,11 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
       owner.clear();
     }
     int64_t w = 0, room = T;
-    for (int32_t u : order) {
-      const int64_t kend = units[u].kend;
-      int64_t pos = units[u].kbegin;
+    const size_t n = order.size();
+    for (size_t oi = 0; oi < n; ++oi) {
+      const int32_t u = order[oi];
+      const int64_t kend = ke[oi];
+      int64_t pos = kb[oi];
       bool placed = false;  // the piece ending at kend (an empty range still needs one)
       while (!placed) {
         const int64_t rest = kend - pos;
@@ -165,19 +189,25 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
   };
   if (!units.empty()) {
     int64_t lo = std::max<int64_t>((total + workers - 1) / workers, 2 * min_piece + overhead + align);
-    // the optimum is rarely more than a few pieces' slack above the mean
+    // the optimum is rarely more than a few pieces' slack above the mean; the search
+    // stops within one alignment step of it (a budget at most `align` keys above
+    // the smallest that fits)
     int64_t hi = lo + 2 * (align + overhead + min_piece);
     while (partition(hi, false) > workers) hi *= 2;
-    while (lo < hi) {
+    while (hi - lo > align) {
       const int64_t mid = lo + (hi - lo) / 2;
       if (partition(mid, false) <= workers) hi = mid; else lo = mid + 1;
     }
-    partition(lo, true);
+    partition(hi, true);
   }
 
-  std::vector<int32_t> pieces_of_unit(units.size(), 0);
+  std::vector<int32_t>& pieces_of_unit = sc.pieces_of_unit;
+  pieces_of_unit.assign(units.size(), 0);
   for (const Piece& pc : pieces) pieces_of_unit[pc.unit]++;
-  std::vector<int32_t> first_slot(units.size(), -1), next_slot(units.size(), 0);
+  std::vector<int32_t>& first_slot = sc.first_slot;
+  std::vector<int32_t>& next_slot = sc.next_slot;
+  first_slot.assign(units.size(), -1);
+  next_slot.assign(units.size(), 0);
   out->n_partials = 0;
   out->n_split = 0;
   for (size_t u = 0; u < units.size(); ++u)
@@ -190,7 +220,8 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
   out->items.clear();
   out->items.reserve(pieces.size());
   out->ptr.assign(workers + 1, 0);
-  std::vector<int64_t> load(workers, 0);
+  std::vector<int64_t>& load = sc.load;
+  load.assign(workers, 0);
   size_t i = 0;
   for (int w = 0; w < workers; ++w) {
     for (; i < pieces.size() && owner[i] == w; ++i) {
@@ -518,7 +549,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   if (ce != cudaSuccess) return fail_cuda(ce);
   ce = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
   if (ce != cudaSuccess) return fail_cuda(ce);
-  HostPlan hp;
+  thread_local HostPlan hp;   // reused: its vectors keep their memory between plans
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
                                 window_left, page_pos, rope_theta, num_sms, &hp);
@@ -797,7 +828,7 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
                                   int32_t kv_layout, float rope_theta, int32_t num_sms,
                                   bsr_schedule_info_t* info, int32_t* units, int64_t max_units) {
   if (kv_layout != BSR_KV_HND && kv_layout != BSR_KV_NHD) return BSR_ERR_INVALID_ARGUMENT;
-  HostPlan hp;
+  thread_local HostPlan hp;   // reused: its vectors keep their memory between plans
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
                                 window_left, page_pos, rope_theta, num_sms, &hp);
