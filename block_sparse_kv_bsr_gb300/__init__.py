@@ -73,16 +73,16 @@ def load(path: str | None = None):
                            "(block_sparse_kv_bsr_gb300._build.build())")
     lib = ctypes.CDLL(path)
     lib.bsr_attn_plan.restype = ctypes.c_int
-    lib.bsr_attn_plan.argtypes = [_i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
-                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
-                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
+    lib.bsr_attn_plan.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
                                   ctypes.c_int32, ctypes.c_float, _vp, ctypes.POINTER(_vp)]
     lib.bsr_attn_plan_host.restype = ctypes.c_int
-    lib.bsr_attn_plan_host.argtypes = [_i32p, _i32p, _i32p, ctypes.c_int32, ctypes.c_int32,
-                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
-                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _i32p,
+    lib.bsr_attn_plan_host.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
                                        ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
-                                       ctypes.POINTER(_Info), _i32p, ctypes.c_int64]
+                                       ctypes.POINTER(_Info), _vp, ctypes.c_int64]
     lib.bsr_attn_run_kv8.restype = ctypes.c_int
     lib.bsr_attn_run_kv8.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                      ctypes.c_float, ctypes.c_float, ctypes.c_int32, _vp,
@@ -146,6 +146,25 @@ def _host_i32(x) -> np.ndarray:
     return np.ascontiguousarray(x, dtype=np.int32)
 
 
+def _host_i32_addr(x):
+    """(object to keep alive, address or None) of a host int32 array; CPU int32 tensors and
+    C-contiguous int32 numpy arrays are passed in place, anything else is converted."""
+    if hasattr(x, "data_ptr"):
+        if x.is_cuda:
+            raise ValueError("plan reads host arrays: pass CPU tensors / numpy arrays")
+        if x.dtype == _torch_int32() and x.is_contiguous():
+            return x, (x.data_ptr() if x.numel() else None)
+    elif isinstance(x, np.ndarray) and x.dtype == np.int32 and x.flags.c_contiguous:
+        return x, (x.__array_interface__["data"][0] if x.size else None)
+    a = _host_i32(x)
+    return a, (a.__array_interface__["data"][0] if a.size else None)
+
+
+def _torch_int32():
+    import torch
+    return torch.int32
+
+
 def _stream_ptr(stream):
     import torch
     if stream is None:
@@ -186,13 +205,10 @@ class Schedule:
 
 
 def _plan_args(indptr, indices, last_page_len, qo_indptr):
-    ip, ix, lp = _host_i32(indptr), _host_i32(indices), _host_i32(last_page_len)
-    qi = None if qo_indptr is None else _host_i32(qo_indptr)
-    keep = (ip, ix, lp, qi)
-    ptrs = (ip.ctypes.data_as(_i32p), ix.ctypes.data_as(_i32p) if ix.size else None,
-            lp.ctypes.data_as(_i32p) if lp.size else None,
-            qi.ctypes.data_as(_i32p) if qi is not None else None)
-    return keep, ptrs, len(ip) - 1
+    ip, ix, lp = _host_i32_addr(indptr), _host_i32_addr(indices), _host_i32_addr(last_page_len)
+    qi = (None, None) if qo_indptr is None else _host_i32_addr(qo_indptr)
+    keep = (ip[0], ix[0], lp[0], qi[0])
+    return keep, (ip[1], ix[1], lp[1], qi[1]), len(ip[0]) - 1
 
 
 def bsr_attn_plan(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_heads: int,
@@ -204,11 +220,10 @@ def bsr_attn_plan(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_h
     lib = load()
     keep, (ip, ix, lp, qi), batch = _plan_args(indptr, indices, last_page_len, qo_indptr)
     handle = _vp(schedule.handle if schedule is not None else None)
-    pp = None if page_pos is None else _host_i32(page_pos)
+    pp = (None, None) if page_pos is None else _host_i32_addr(page_pos)
     code = lib.bsr_attn_plan(ip, ix, lp, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
-                             qi, int(num_pages), int(bool(causal)), int(window_left),
-                             pp.ctypes.data_as(_i32p) if pp is not None and pp.size else None,
-                             _layout(kv_layout), float(rope_theta), _vp(_stream_ptr(stream)),
+                             qi, int(num_pages), int(bool(causal)), int(window_left), pp[1],
+                             _layout(kv_layout), float(rope_theta), _stream_ptr(stream),
                              ctypes.byref(handle))
     del keep
     _check(code, "bsr_attn_plan")
@@ -225,17 +240,16 @@ def bsr_attn_plan_host(indptr, indices, last_page_len, *, num_qo_heads: int, num
     """Host-only planning for `num_sms` SMs: returns (info dict, units int32 [n, 8])."""
     lib = load()
     keep, (ip, ix, lp, qi), batch = _plan_args(indptr, indices, last_page_len, qo_indptr)
-    pp = None if page_pos is None else _host_i32(page_pos)
+    pp = (None, None) if page_pos is None else _host_i32_addr(page_pos)
     args = [ip, ix, lp, batch, num_qo_heads, num_kv_heads, head_dim, page_size, qi,
-            int(num_pages), int(bool(causal)), int(window_left),
-            pp.ctypes.data_as(_i32p) if pp is not None and pp.size else None,
+            int(num_pages), int(bool(causal)), int(window_left), pp[1],
             _layout(kv_layout), float(rope_theta), int(num_sms)]
     info = _Info()
     n = lib.bsr_attn_plan_host(*args, ctypes.byref(info), None, 0)
     if n < 0:
         raise BsrError(n, "bsr_attn_plan_host")
     units = np.zeros((max(n, 1), 8), dtype=np.int32)
-    n2 = lib.bsr_attn_plan_host(*args, None, units.ctypes.data_as(_i32p), units.shape[0])
+    n2 = lib.bsr_attn_plan_host(*args, None, units.__array_interface__["data"][0], units.shape[0])
     del keep
     if n2 < 0:
         raise BsrError(n2, "bsr_attn_plan_host")

@@ -106,7 +106,7 @@ struct WorkList {
 // worker carries about one piece-alignment more than the mean.  The result
 // is a pure function of its inputs.
 void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align, int64_t overhead,
-             int64_t min_piece, int64_t min_worker_work, WorkList* out) {
+             int64_t min_piece, int64_t min_worker_work, WorkList* out, int64_t* k_hint = nullptr) {
   // Working arrays live across calls (per thread), so a plan per decode step reuses
   // their memory instead of faulting in fresh pages.
   struct Scratch {
@@ -189,16 +189,32 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
   };
   if (!units.empty()) {
     int64_t lo = std::max<int64_t>((total + workers - 1) / workers, 2 * min_piece + overhead + align);
-    // the optimum is rarely more than a few pieces' slack above the mean; the search
-    // stops within one alignment step of it (a budget at most `align` keys above
-    // the smallest that fits)
-    int64_t hi = lo + 2 * (align + overhead + min_piece);
-    while (partition(hi, false) > workers) hi *= 2;
-    while (hi - lo > align) {
-      const int64_t mid = lo + (hi - lo) / 2;
-      if (partition(mid, false) <= workers) hi = mid; else lo = mid + 1;
+    // The budget is the smallest T = lo + k (k >= 0) for which the cut fits (the cut
+    // needs fewer workers as T grows).  A caller that re-plans similar batches passes
+    // the last k as a hint: two cuts confirm it (it fits, k - 1 does not); otherwise
+    // a doubling search from one alignment step, then halving.  Either way the same k.
+    auto fits = [&](int64_t k) { return partition(lo + k, false) <= workers; };
+    int64_t k = -1;
+    if (k_hint != nullptr && *k_hint >= 0 && fits(*k_hint) && (*k_hint == 0 || !fits(*k_hint - 1)))
+      k = *k_hint;
+    if (k < 0) {
+      if (fits(0)) {
+        k = 0;
+      } else {
+        int64_t bad = 0, good = align;
+        while (!fits(good)) {
+          bad = good;
+          good *= 2;
+        }
+        while (good - bad > 1) {
+          const int64_t mid = bad + (good - bad) / 2;
+          if (fits(mid)) good = mid; else bad = mid;
+        }
+        k = good;
+      }
     }
-    partition(hi, true);
+    if (k_hint != nullptr) *k_hint = k;
+    partition(lo + k, true);
   }
 
   std::vector<int32_t>& pieces_of_unit = sc.pieces_of_unit;
@@ -516,8 +532,10 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   }
   hp->rk_total = hp->rk_start.back();
   hp->rq_total = hp->rq_start.back();
+  // consecutive plans of a serving loop are alike: start from the last budget step
+  thread_local int64_t dec_k = -1;
   balance(dunits, int64_t(num_sms) * kDecodeWarps, std::max<int64_t>(page_size, kStageTokens),
-          kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec);
+          kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec, &dec_k);
   balance_gangs(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillKeyTile),
                 kPrefillOverhead, kPrefillMinPiece, kPrefillMinCtaWork, &hp->pre);
   hp->pmerge.clear();

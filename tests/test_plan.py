@@ -192,3 +192,14 @@ def test_page_positions_validation():
     bad[0] = -16
     with pytest.raises(bsr.BsrError):
         bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len, page_pos=bad, **kw)
+
+
+def test_plan_does_not_depend_on_earlier_plans():
+    # the budget search starts from the last plan's step; the result must not depend on it
+    a, b = wl.config3(small=False), wl.config2(small=False)
+    first = plan_of(a, num_sms=152)[1]
+    plan_of(b, num_sms=152)
+    again = plan_of(a, num_sms=152)[1]
+    assert np.array_equal(first, again)
+    plan_of(wl.config1(), num_sms=152)
+    assert np.array_equal(first, plan_of(a, num_sms=152)[1])
