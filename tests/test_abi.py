@@ -75,6 +75,7 @@ def test_plan_host_accepts_a_valid_table(lib):
     (dict(num_sms=0), -1),
     (dict(qo_indptr=[0, 40, 41], causal=True), -3),      # more queries than keys
     (dict(rope_theta=-1.0), -1),
+    (dict(num_pages=1 << 27), -2),                       # pool rows beyond 32-bit indexing
 ])
 def test_plan_host_rejects(lib, kw, code):
     with pytest.raises(bsr.BsrError) as e:

@@ -277,3 +277,13 @@ def test_repeated_launches_bit_exact(kv8):
     o = outs[0][0].view(torch.bfloat16).float().cpu().numpy()[rows, heads]
     assert_out_close(o, ro, True, w.name)
     assert_lse_close(outs[0][1].cpu().numpy()[rows, heads], rl, w.name)
+
+
+def test_longest_context_one_request():
+    # one request of 262,144 keys (16,384 pages, 1 GB of K/V): every kv head's range is
+    # cut over ~150 warps and merged in the kernel from that many partial states
+    w = wl.make_paged("long256k", 16, [262144], Hq=32, Hk=8, D=128, P=16)
+    out, lse, s = run(w)
+    info = s.info()
+    assert info["num_split_streams"] == 8 and info["num_partials"] >= 8 * 100
+    check_full(w, out, lse)
