@@ -1,0 +1,90 @@
+"""Randomized GPU parity against the fp64 oracle: seeded batches drawn over the
+parameters the path supports together (batch size, lengths with empty and ragged
+requests, dropped blocks, page size, GQA group, head dim, query rows per request with
+the causal mask, RoPE, sliding window, token-major pages, FP8 cache), each compared
+element by element.  The draw is a fixed function of the case index, so a failure
+reproduces from its id."""
+import random
+
+import numpy as np
+import pytest
+import torch
+
+import block_sparse_kv_bsr_gb300 as bsr
+import oracle
+import workloads as wl
+from block_sparse_kv_bsr_gb300 import _build
+from parity import assert_lse_close, assert_out_close, plan
+
+pytestmark = pytest.mark.gpu
+
+N_CASES = 48
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(cuda_device):
+    _build.build()
+    bsr.load()
+
+
+def draw(i: int):
+    r = random.Random(9000 + i)
+    D = r.choice([64, 128])
+    Hk = r.choice([1, 2, 4, 8])
+    group = r.choice([g for g in (1, 2, 4, 8, 16) if g * Hk <= 64])
+    P = r.choice([1, 4, 8, 16, 32, 64] if D == 64 else [8, 16, 32, 128, 256])
+    batch = r.randint(1, 9)
+    lens = [r.choice([0, 1, r.randint(2, 40), r.randint(40, 700), r.randint(700, 3000)])
+            for _ in range(batch)]
+    multi = r.random() < 0.4
+    qo = [min(max(1, n), r.randint(1, 24)) if multi else 1 for n in lens]
+    causal = multi and r.random() < 0.7
+    rope = r.choice([0.0, 0.0, 1e4, 5e5]) if P >= 16 else 0.0
+    drop = r.choice([0.0, 0.0, 0.25])
+    kv8 = D == 128 and P >= 16 and rope == 0.0 and not multi and r.random() < 0.3
+    nhd = r.random() < 0.3
+    window = r.choice([0, 0, 0, r.randint(1, 300)])
+    return dict(D=D, Hk=Hk, Hq=Hk * group, P=P, lens=lens, qo=qo, causal=causal, rope=rope,
+                drop=drop, kv8=kv8, nhd=nhd, window=window)
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
+def test_random_batch(i):
+    c = draw(i)
+    # requests with queries need at least as many keys as queries (causal bottom-right)
+    lens = [max(n, q) if c["causal"] else n for n, q in zip(c["lens"], c["qo"])]
+    qo = [q if n > 0 else (1 if not c["causal"] else 0) for n, q in zip(lens, c["qo"])]
+    if sum(qo) == 0:
+        qo[0], lens[0] = 1, max(lens[0], 1)
+    w = wl.make_paged(f"rand{i}", 9100 + i, lens, Hq=c["Hq"], Hk=c["Hk"], D=c["D"], P=c["P"],
+                      qo_lens=qo, drop=c["drop"], rope_theta=c["rope"], causal=c["causal"])
+    w.window_left = c["window"]
+    if c["kv8"]:
+        w = wl.with_kv8(w, 9200 + i)
+    if c["nhd"]:
+        w = wl.to_nhd(w)
+    dev = "cuda:0"
+    s = plan(w)
+    q = w.q.to(dev)
+    if c["kv8"]:
+        out, lse = bsr.bsr_attn_run_kv8(s, q, w.k_codes.to(dev), w.v_codes.to(dev),
+                                        k_scale=w.k_scale, v_scale=w.v_scale,
+                                        sm_scale=w.sm_scale, causal=w.causal)
+    else:
+        out, lse = bsr.bsr_attn_run(s, q, w.k_pages.to(dev), w.v_pages.to(dev),
+                                    sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+                                    causal=w.causal, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert bsr.bsr_last_device_error(s) == 0
+    kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+              page_size=w.page_size, sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+              causal=w.causal, window_left=w.window_left, page_pos=w.page_pos,
+              kv_layout=w.kv_layout)
+    table = (w.indptr, w.indices, w.last_page_len, w.qo_indptr)
+    if c["kv8"]:
+        ro, rl = oracle.attention_kv8(w.q, w.k_codes, w.v_codes, w.k_scale, w.v_scale, *table,
+                                      **kw)
+    else:
+        ro, rl = oracle.attention(w.q, w.k_pages, w.v_pages, *table, **kw)
+    assert_out_close(out.float().cpu().numpy(), ro, out.dtype == torch.bfloat16, f"{w.name} {c}")
+    assert_lse_close(lse.cpu().numpy(), rl, f"{w.name} {c}")
