@@ -641,21 +641,25 @@ __global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(con
   for (int u = 0; u < 8; ++u)
     x[u] = u < n ? __ldcg(reinterpret_cast<const float4*>(po + size_t(u) * kSlotStride))
                  : make_float4(0.f, 0.f, 0.f, 0.f);
-  float M = -INFINITY;
-  for (int k = lane; k < n; k += 32) M = fmaxf(M, __ldcg(lse_k + size_t(k) * kUnitRows));
+  // chunk lse values: lane k holds chunk k (and k + 32, ... for longer splits: read
+  // again there); one load round trip before the weights when n <= 32
+  const float l0 = lane < n ? __ldcg(lse_k + size_t(lane) * kUnitRows) : -INFINITY;
+  float M = l0;
+  for (int k = lane + 32; k < n; k += 32) M = fmaxf(M, __ldcg(lse_k + size_t(k) * kUnitRows));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float lt = -INFINITY;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   if (M != -INFINITY) {
-    float sum = 0.f;
-    for (int k = lane; k < n; k += 32) sum += ptx::ex2(__ldcg(lse_k + size_t(k) * kUnitRows) - M);
+    float sum = lane < n ? ptx::ex2(l0 - M) : 0.f;
+    for (int k = lane + 32; k < n; k += 32) sum += ptx::ex2(__ldcg(lse_k + size_t(k) * kUnitRows) - M);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
     lt = M + ptx::lg2(sum);
     for (int kb = 0; kb < n; kb += 32) {
       const int m = min(32, n - kb);
-      const float wl = lane < m ? ptx::ex2(__ldcg(lse_k + size_t(kb + lane) * kUnitRows) - lt) : 0.f;
+      const float lk = kb == 0 ? l0 : (lane < m ? __ldcg(lse_k + size_t(kb + lane) * kUnitRows) : 0.f);
+      const float wl = lane < m ? ptx::ex2(lk - lt) : 0.f;
       for (int j = 0; j < m; j += 8) {
         if (kb + j >= 8) {   // chunks past the first eight: load this group now
 #pragma unroll
