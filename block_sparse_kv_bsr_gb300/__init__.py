@@ -20,6 +20,7 @@ __all__ = [
     "bsr_attn_run_kv8", "bsr_merge_states", "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info",
     "bsr_last_device_error", "bsr_status_string", "bsr_attn_decode_noalloc", "Schedule",
     "bsr_schedule_set_stage_timing", "bsr_schedule_stage_times", "STAGES", "EXPORTED_SYMBOLS",
+    "bsr_selftest_bounded_wait",
 ]
 
 BSR_OK = 0
@@ -30,7 +31,7 @@ EXPORTED_SYMBOLS = (
     "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run", "bsr_attn_run_kv8", "bsr_merge_states",
     "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info", "bsr_last_device_error",
     "bsr_status_string", "bsr_attn_decode_noalloc", "bsr_schedule_set_stage_timing",
-    "bsr_schedule_stage_times",
+    "bsr_schedule_stage_times", "bsr_selftest_bounded_wait",
 )
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -103,6 +104,8 @@ def load(path: str | None = None):
     lib.bsr_schedule_get_info.argtypes = [_vp, ctypes.POINTER(_Info)]
     lib.bsr_last_device_error.restype = ctypes.c_int
     lib.bsr_last_device_error.argtypes = [_vp]
+    lib.bsr_selftest_bounded_wait.restype = ctypes.c_int
+    lib.bsr_selftest_bounded_wait.argtypes = [_vp, ctypes.c_int64, _vp]
     lib.bsr_schedule_set_stage_timing.restype = ctypes.c_int
     lib.bsr_schedule_set_stage_timing.argtypes = [_vp, ctypes.c_int32]
     lib.bsr_schedule_stage_times.restype = ctypes.c_int
@@ -356,6 +359,14 @@ def bsr_last_device_error(schedule: Schedule) -> int:
     if code < 0:
         raise BsrError(code, "bsr_last_device_error")
     return code
+
+
+def bsr_selftest_bounded_wait(device_status, limit_ns: int, stream=None):
+    """Run one bounded wait that must run out (nothing arrives): sets bit 0 of the int32
+    CUDA tensor `device_status` after `limit_ns`."""
+    _check(load().bsr_selftest_bounded_wait(_vp(device_status.data_ptr()), int(limit_ns),
+                                            _vp(_stream_ptr(stream))),
+           "bsr_selftest_bounded_wait")
 
 
 STAGES = ("decode", "rope_prepass", "prefill", "merge")

@@ -300,6 +300,13 @@ int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_pa
                             int32_t num_pages_in_pool, float sm_scale, void* out,
                             int32_t out_dtype, float* lse, int32_t* device_status, void* stream);
 
+/* Self-test of failure detection (no GPU fault involved): runs, on `stream`, the
+ * bounded mbarrier wait the library's kernels use, on a barrier that nothing ever
+ * arrives on; after `limit_ns` (1 ns .. 10 s) the wait gives up and bit 0 of the
+ * int32 at `device_status` (device memory) is set, as a kernel whose wait ran out
+ * sets its schedule's status word.  BSR_OK once launched. */
+int bsr_selftest_bounded_wait(int32_t* device_status, int64_t limit_ns, void* stream);
+
 /* Device-side status word of a schedule (0 = fine; bit 0: a kernel gave up on
  * a bounded wait; bit 1: with RoPE on the tensor-core prefill path, a rotated
  * q or k value was at least 2^20 in magnitude, beyond the range of its fp16

@@ -88,6 +88,7 @@ def test_entry_points_reject_bad_arguments_without_a_gpu(lib):
     assert lib.bsr_merge_states(None, None, None, None, 1, 1, 96, 0, None, None, None) == -2
     assert lib.bsr_append_kv(None, None, None, None, None, None, 1, 1, 1, 128, 3, 1, 0,
                              None, None, None, None) == -2
+    assert lib.bsr_selftest_bounded_wait(None, 1000, None) == -1
     # an unknown page layout
     assert lib.bsr_append_kv(None, None, None, None, None, None, 1, 1, 1, 128, 16, 1, 7,
                              None, None, None, None) == -1

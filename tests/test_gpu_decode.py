@@ -287,3 +287,20 @@ def test_longest_context_one_request():
     info = s.info()
     assert info["num_split_streams"] == 8 and info["num_partials"] >= 8 * 100
     check_full(w, out, lse)
+
+
+def test_bounded_wait_gives_up_and_reports():
+    # failure detection without a fault: a wait on a barrier nothing arrives on gives up
+    # after its limit, sets bit 0 of the status word, and the context stays usable
+    status = torch.zeros(1, dtype=torch.int32, device="cuda:0")
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    bsr.bsr_selftest_bounded_wait(status, 20_000_000)   # 20 ms
+    t1.record()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    assert t0.elapsed_time(t1) >= 19.0
+    w = wl.config1()
+    out, lse, s = run(w)
+    check_full(w, out, lse)
