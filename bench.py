@@ -182,11 +182,12 @@ def traffic_from_profile(name: str, digest: str):
     return float(m.group(1))
 
 
-def cpu_baseline(w, budget_s=10.0, min_passes=1):
-    """Time the fp64 oracle over whole passes of the batch until `budget_s` is spent."""
+def cpu_baseline(w, budget_s=10.0, min_passes=1, threads=None):
+    """Time the fp64 oracle over whole passes of the batch until `budget_s` is spent
+    (all host cores unless `threads` is given)."""
     import oracle
     import workloads as wl
-    threads = oracle.default_threads()
+    threads = oracle.default_threads() if threads is None else threads
     alg = wl.algorithmic_bytes(w)
     passes, spent = 0, 0.0
     while passes < min_passes or spent < budget_s:
@@ -572,6 +573,8 @@ def main():
     # the kernel's own duration (library stage events) where the call launches more than one
     kms = dom.kernel_ms if dom.kernel_ms else dom.ms
     dom_ms = sum(kms) / len(kms)
+    deciles = (statistics.quantiles(kms, n=10, method="inclusive") if len(kms) > 1
+               else [kms[0]] * 9)
     sources = {"decode": _build.DECODE_KERNEL_SOURCES,
                "decode_kv8": _build.DECODE_KV8_KERNEL_SOURCES,
                "prefill": _build.PREFILL_KERNEL_SOURCES}.get(dom.family)
@@ -608,6 +611,9 @@ def main():
                      "kernel": dom.kernel, "kernel_build": build_digest,
                      "kernel_us_mean": round(dom_ms * 1e3, 2),
                      "kernel_us_min": round(min(kms) * 1e3, 2),
+                     "kernel_us_p10": round(deciles[0] * 1e3, 2),
+                     "kernel_us_median": round(statistics.median(kms) * 1e3, 2),
+                     "kernel_us_p90": round(deciles[-1] * 1e3, 2),
                      "timed_by": ("library stage events around the kernel" if dom.kernel_ms
                                   else "CUDA events around the call") + ", second timed pass of K steps",
                      "call_us_mean": round(call_ms * 1e3, 2)},
@@ -627,8 +633,14 @@ def main():
                        "prefill_items": info["num_prefill_items"],
                        "split_ranges": info["num_split_streams"],
                        "imbalance": round(max(info["decode_imbalance"], info["prefill_imbalance"]), 4)}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.config == 3:
+    # the oracle on the host cores, for the decode workloads (a pass takes well under a
+    # second there); on the tiny and the Llama-8B-shaped ones also on one thread
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.config in (1, 2, 3, 6, 7, 8, 10):
         res["cpu_baseline"] = cpu_baseline(job["workload"])
+        if args.config in (1, 2):
+            one = cpu_baseline(job["workload"], budget_s=3.0, threads=1)
+            res["cpu_baseline"]["single_thread"] = {"value": one["value"], "unit": one["unit"],
+                                                    "sample": one["sample"]}
     if rank == 0:
         print(json.dumps(res))
     if world > 1:
