@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import hashlib
+import re
 import os
 import shutil
 import subprocess
@@ -54,12 +55,23 @@ PREFILL_KERNEL_SOURCES = ("bsr_prefill.cu", "bsr_internal.h", "ptx.cuh", "umma.c
 DECODE_KV8_KERNEL_SOURCES = ("bsr_decode_kv8.cu", "bsr_decode.cuh", "bsr_internal.h", "ptx.cuh")
 
 
+_COMMENT = re.compile(rb"//[^\n]*|/\*.*?\*/", re.S)
+
+
+def _code_of(text: bytes) -> bytes:
+    """Source text without comments and blank-space differences (what the compiler sees),
+    so that editing a comment does not change a kernel's build digest.  String literals
+    in these sources hold inline PTX, which has no comment markers."""
+    lines = (ln.rstrip() for ln in _COMMENT.sub(b"", text).split(b"\n"))
+    return b"\n".join(ln for ln in lines if ln)
+
+
 def kernel_digest(names=DECODE_KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
     for name in names:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
-            h.update(f.read())
+            h.update(_code_of(f.read()))
     h.update(" ".join(ARCH + FLAGS).encode())   # no paths: the same on every machine
     return h.hexdigest()[:16]
 

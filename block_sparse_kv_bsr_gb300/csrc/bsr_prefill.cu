@@ -10,28 +10,31 @@
 // tile is staged once for 256 rows, and while the softmax of one query tile
 // runs, the tensor cores work on the other's products.
 //
-// Roles (320 threads):
-//   warps 0-3, 4-7  softmax warpgroups, one per query tile: thread t owns row
-//              t of its tile and TMEM lane t.  They run the online softmax on
-//              S rows read from TMEM, write P (bf16) back into the S columns of
-//              TMEM, rescale O in TMEM when the running max grows by more than
-//              2^8, and write out / lse (or the fp32 partial state of a split
-//              key range, combined afterwards by bsr_prefill_merge_kernel).
-//   warp 8     TMA producer: loads each unit's query tiles (one box per 64
-//              columns: whole queries of the kv head's group, straight from q,
+// Roles (576 threads):
+//   warps 0-15 softmax, two threads per row: warp w works on query tile w / 8,
+//              key/column half (w / 4) % 2 and row quarter w % 4 (the TMEM lanes
+//              it may access).  Each half reads its 64 scores of a row from TMEM,
+//              the halves swap their partial max (and at the end their partial
+//              sum) through shared memory and an mbarrier, then each writes its
+//              half of P (bf16) over S columns it has already read, rescales its
+//              64 O columns in TMEM when the running max grows by more than 2^8,
+//              and writes out / lse (or the fp32 partial state of a split key
+//              range, combined afterwards by bsr_prefill_merge_kernel).
+//   warp 16    TMA producer, the whole warp: each unit's query tiles (one box per
+//              64 columns: whole queries of the kv head's group, straight from q,
 //              or with RoPE from the copy the pre-pass rotated) as soon as the
-//              previous unit's last Q K^T has read them, and fills one FIFO ring
-//              of 32 KB stages with the K and V tiles of every key tile in turn
-//              (K(j), V(j), K(j+1), ...), gathered 16 keys at a time page by
-//              page from `indices` (inactive blocks are absent, "Block-Sparse
-//              포맷"), 128B-swizzled.  With RoPE, K comes already rotated from a
-//              dense buffer that the pre-pass fills once per run.
-//   warp 9     allocates TMEM and issues the MMAs: S_i = Q_i K^T (M 128, N 128,
+//              previous unit's last Q K^T has read them, and a FIFO ring of 32 KB
+//              stages with the K and V tiles of every key tile in turn (K(j),
+//              V(j), K(j+1), ...), gathered box by box from `indices` (inactive
+//              blocks are absent, "Block-Sparse 포맷"), 128B-swizzled; lane b
+//              fetches box b's page id one key tile ahead.  With RoPE, K comes
+//              already rotated from a dense buffer the pre-pass fills once per run.
+//   warp 17    allocates TMEM and issues the MMAs: S_i = Q_i K^T (M 128, N 128,
 //              K-major operands from shared memory) and O_i += P_i V (P from
 //              TMEM, V MN-major from shared memory), i = 0, 1.
-// TMEM columns: S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_i overwrites
-// the first 64 columns of S_i.  MMAs run in issue order, so the QK^T of the
-// next key tile may be queued right behind the P V that reads P_i.
+// TMEM columns: S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_i (bf16 pairs)
+// overwrites columns 0-31 and 64-95 of S_i.  MMAs run in issue order, so the
+// Q K^T of the next key tile may be queued right behind the P V that reads P_i.
 // Every mbarrier wait is bounded and warp-agreed.
 #include <cuda.h>
 #include <cuda_runtime.h>
