@@ -24,6 +24,10 @@
 //    odd-dim n-tile of the block, so each thread's accumulators hold dims
 //    4t..4t+3 of every 16-dim block (stored contiguously).
 //  * P enters PV as fp16 (11 significant bits).
+//  * A step consumes two ring stages (32 keys) while two remain: their Q K^T
+//    products interleave and the max, its shuffles and the O rescale run once
+//    per 32 keys (the conversions make a stage about three times the bf16
+//    kernel's instructions per byte, so per-step latency matters here).
 // Every barrier wait is bounded; on timeout the warp sets bit 0 of the status
 // word, drains its own copies (bounded) and exits.
 #include <cuda.h>
