@@ -41,7 +41,7 @@
 #include "bsr_schedule.h"
 
 #ifndef BSR_DECODE_STAGES_KV8
-#define BSR_DECODE_STAGES_KV8 6
+#define BSR_DECODE_STAGES_KV8 4
 #endif
 
 namespace bsr {
