@@ -7,6 +7,7 @@ import socket
 import subprocess
 import sys
 
+import numpy as np
 import torch
 import torch.distributed as dist
 import torch.multiprocessing as mp
@@ -55,3 +56,28 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     res = json.loads(lines[0])
     assert res["impl"] == "reference" and res["n_gpus"] == 2 and res["value"] > 0
+
+
+def test_reference_step_samples_cover_the_batch():
+    """A sampled reference step (every k-th request) is the same attention on those
+    requests; the k offsets together cover the batch once."""
+    import bench
+    import oracle
+    import workloads as wl
+    w = wl.config8(small=True)          # drops and per-page positions
+    kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+              page_size=w.page_size, sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+              causal=w.causal)
+    full_o, full_l = oracle.attention(w.q, w.k_pages, w.v_pages, w.indptr, w.indices,
+                                      w.last_page_len, w.qo_indptr, page_pos=w.page_pos, **kw)
+    qo = w.qo_indptr.tolist()
+    seen = []
+    for off in range(3):
+        reqs = list(range(off, w.batch, 3))
+        s = bench.sub_batch(w, reqs)
+        o, l = oracle.attention(s.q, s.k_pages, s.v_pages, s.indptr, s.indices,
+                                s.last_page_len, s.qo_indptr, page_pos=s.page_pos, **kw)
+        rows = [r for b in reqs for r in range(qo[b], qo[b + 1])]
+        assert np.array_equal(o, full_o[rows]) and np.array_equal(l, full_l[rows])
+        seen += reqs
+    assert sorted(seen) == list(range(w.batch))
