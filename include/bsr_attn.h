@@ -90,6 +90,10 @@ typedef struct bsr_schedule* bsr_schedule_t;
  * with rope_theta > 0 an fp32 cos/sin table built in fp64 goes to its own
  * device buffer, uploaded only when theta or head_dim change or the longest
  * request outgrows it.
+ * The planner's host working arrays are kept per calling thread and reused by
+ * that thread's later plans (a serving loop that re-plans every step allocates
+ * nothing on the host once they have grown), and its budget search starts from
+ * the last plan's; the resulting schedule depends only on the arguments.
  *
  * window_left >= 0: 0 attends every key; W > 0 is the sliding-window variant
  * ("JIT 컴파일은 …": Sliding Window among the fused variants) -- a query at
