@@ -91,8 +91,8 @@ typedef struct bsr_schedule* bsr_schedule_t;
  * device buffer, uploaded only when theta or head_dim change or the longest
  * request outgrows it.
  * The planner's host working arrays are kept per calling thread and reused by
- * that thread's later plans (a serving loop that re-plans every step allocates
- * nothing on the host once they have grown), and its budget search starts from
+ * that thread's later plans (in a serving loop that re-plans every step the
+ * large per-plan arrays are not allocated again), and its budget search starts from
  * the last plan's; the resulting schedule depends only on the arguments.
  *
  * window_left >= 0: 0 attends every key; W > 0 is the sliding-window variant
