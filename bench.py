@@ -27,6 +27,7 @@ from __future__ import annotations
 
 import argparse
 import gc
+import itertools
 import json
 import math
 import os
@@ -656,8 +657,9 @@ def sub_batch(w, reqs):
     rows = [torch.arange(qo[b], qo[b + 1]) for b in reqs]
     sel_p = torch.cat(pages) if pages else torch.zeros(0, dtype=torch.int64)
     sel_q = torch.cat(rows) if rows else torch.zeros(0, dtype=torch.int64)
-    cum = lambda lens: torch.tensor([0] + list(__import__("itertools").accumulate(lens)),
-                                    dtype=torch.int32)
+    def cum(lens):
+        return torch.tensor([0] + list(itertools.accumulate(lens)), dtype=torch.int32)
+
     return dataclasses.replace(
         w, indptr=cum([ip[b + 1] - ip[b] for b in reqs]), indices=w.indices[sel_p].contiguous(),
         last_page_len=w.last_page_len[list(reqs)].contiguous(),
