@@ -19,6 +19,7 @@ __all__ = [
     "BsrError", "load", "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run",
     "bsr_attn_run_kv8", "bsr_merge_states", "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info",
     "bsr_last_device_error", "bsr_status_string", "bsr_attn_decode_noalloc", "Schedule",
+    "bsr_attn_decode_noalloc_kv8",
     "bsr_schedule_set_stage_timing", "bsr_schedule_stage_times", "STAGES", "EXPORTED_SYMBOLS",
     "bsr_selftest_bounded_wait",
 ]
@@ -30,7 +31,8 @@ BSR_DTYPE_F32 = 1
 EXPORTED_SYMBOLS = (
     "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run", "bsr_attn_run_kv8", "bsr_merge_states",
     "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info", "bsr_last_device_error",
-    "bsr_status_string", "bsr_attn_decode_noalloc", "bsr_schedule_set_stage_timing",
+    "bsr_status_string", "bsr_attn_decode_noalloc", "bsr_attn_decode_noalloc_kv8",
+    "bsr_schedule_set_stage_timing",
     "bsr_schedule_stage_times", "bsr_selftest_bounded_wait",
 )
 
@@ -115,6 +117,12 @@ def load(path: str | None = None):
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _vp,
                                             ctypes.c_int32, _vp, _vp, _vp]
+    lib.bsr_attn_decode_noalloc_kv8.restype = ctypes.c_int
+    lib.bsr_attn_decode_noalloc_kv8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32,
+                                                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                                ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                                ctypes.c_float, ctypes.c_float, _vp,
+                                                ctypes.c_int32, _vp, _vp, _vp]
     lib.bsr_status_string.restype = ctypes.c_char_p
     lib.bsr_status_string.argtypes = [ctypes.c_int]
     _lib = lib
@@ -406,4 +414,24 @@ def bsr_attn_decode_noalloc(q, k_pages, v_pages, indptr, indices, last_page_len,
                                        num_pages, float(sm_scale), _dptr(out), dt, _dptr(lse),
                                        _dptr(device_status), _vp(_stream_ptr(stream)))
     _check(code, "bsr_attn_decode_noalloc")
+    return out, lse
+
+
+def bsr_attn_decode_noalloc_kv8(q, k_pages, v_pages, indptr, indices, last_page_len, *,
+                                sm_scale: float, k_scale: float, v_scale: float, out, lse=None,
+                                device_status=None, stream=None):
+    """bsr_attn_decode_noalloc over an FP8 (E4M3) cache: uint8 (or float8_e4m3fn) codes,
+    the cached values ``k_scale * code`` / ``v_scale * code``."""
+    import torch
+    lib = load()
+    num_pages, Hk, P, D = k_pages.shape
+    batch, Hq = q.shape[0], q.shape[1]
+    dt = BSR_DTYPE_F32 if out.dtype == torch.float32 else BSR_DTYPE_BF16
+    code = lib.bsr_attn_decode_noalloc_kv8(_dptr(q), _dptr(k_pages), _dptr(v_pages),
+                                           _dptr(indptr), _dptr(indices), _dptr(last_page_len),
+                                           batch, Hq, Hk, D, P, num_pages, float(sm_scale),
+                                           float(k_scale), float(v_scale), _dptr(out), dt,
+                                           _dptr(lse), _dptr(device_status),
+                                           _vp(_stream_ptr(stream)))
+    _check(code, "bsr_attn_decode_noalloc_kv8")
     return out, lse

@@ -161,6 +161,20 @@ bool encode_pool(CUtensorMap* tm, const void* base, int64_t rows, int D) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor map over an FP8 (E4M3) page pool [num_pages, Hk, P, 128] seen as rows of 128
+// one-byte codes: one box of 16 rows x 128 B per 16-key stage, 128B-swizzled.
+bool encode_pool_e4m3(CUtensorMap* tm, const void* base, int64_t rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {128, cuuint64_t(rows)};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, kStageTokens};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Device address of the scratch array, looked up once per device (with that
 // device current) on the first call made there.
 uint8_t* scratch_on(int dev) {
@@ -180,19 +194,21 @@ uint8_t* scratch_on(int dev) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-}  // namespace
-
-extern "C" int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_pages,
-                                       const int32_t* indptr, const int32_t* indices,
-                                       const int32_t* last_page_len, int32_t batch,
-                                       int32_t num_qo_heads, int32_t num_kv_heads,
-                                       int32_t head_dim, int32_t page_size,
-                                       int32_t num_pages_in_pool, float sm_scale, void* out,
-                                       int32_t out_dtype, float* lse, int32_t* device_status,
-                                       void* stream_v) {
+// Both entry points: a bf16 cache, or (kv8) E4M3 codes with one scale per pool.
+int noalloc_impl(const void* q, const void* k_pages, const void* v_pages, const int32_t* indptr,
+                 const int32_t* indices, const int32_t* last_page_len, int32_t batch,
+                 int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                 int32_t num_pages_in_pool, float sm_scale, bool kv8, float k_scale,
+                 float v_scale, void* out, int32_t out_dtype, float* lse,
+                 int32_t* device_status, void* stream_v) {
   if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || num_pages_in_pool < 0)
     return BSR_ERR_INVALID_ARGUMENT;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return BSR_ERR_INVALID_ARGUMENT;
+  if (kv8 && (!(k_scale > 0.f) || !std::isfinite(k_scale) || !(v_scale > 0.f) ||
+              !std::isfinite(v_scale)))
+    return BSR_ERR_INVALID_ARGUMENT;
+  // the FP8 kernel covers head_dim 128 with pages of at least one 16-key stage
+  if (kv8 && (head_dim != 128 || page_size < kStageTokens)) return BSR_ERR_UNSUPPORTED;
   if (out_dtype != BSR_DTYPE_BF16 && out_dtype != BSR_DTYPE_F32) return BSR_ERR_INVALID_ARGUMENT;
   if (head_dim != 64 && head_dim != 128) return BSR_ERR_UNSUPPORTED;
   if (page_size <= 0 || page_size > 256 || (page_size & (page_size - 1))) return BSR_ERR_UNSUPPORTED;
@@ -243,7 +259,10 @@ extern "C" int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const
   const bool smallp = page_size < kStageTokens;
   CUtensorMap tk{}, tv{};
   const int64_t rows = int64_t(num_pages_in_pool) * num_kv_heads * page_size;
-  if (!smallp) {
+  if (kv8) {
+    if (rows <= 0 || !encode_pool_e4m3(&tk, k_pages, rows) || !encode_pool_e4m3(&tv, v_pages, rows))
+      return BSR_ERR_CUDA;
+  } else if (!smallp) {
     if (rows <= 0 || !encode_pool(&tk, k_pages, rows, head_dim) ||
         !encode_pool(&tv, v_pages, rows, head_dim))
       return BSR_ERR_CUDA;
@@ -262,8 +281,9 @@ extern "C" int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const
   p.out = out;
   p.lse = lse;
   p.error = status;
-  p.scale_log2 = float(double(sm_scale) * 1.4426950408889634);
-  p.v_scale = 1.f;
+  // an FP8 cache's k_scale folds into the logit scale, v_scale into the normalisation
+  p.scale_log2 = float(double(sm_scale) * (kv8 ? double(k_scale) : 1.0) * 1.4426950408889634);
+  p.v_scale = kv8 ? v_scale : 1.f;
   p.Hq = num_qo_heads;
   p.Hk = num_kv_heads;
   p.group = group;
@@ -276,11 +296,41 @@ extern "C" int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const
   const int grid = (units + kDecodeWarps - 1) / kDecodeWarps;
   const bool r16 = group > 8;
   const cudaError_t e =
-      head_dim == 128 ? bsr::launch_decode_d128(false, r16, smallp, tk, tv, p, grid, stream)
-                      : bsr::launch_decode_d64(false, r16, smallp, tk, tv, p, grid, stream);
+      kv8 ? bsr::launch_decode_kv8(r16, tk, tv, p, grid, stream)
+          : head_dim == 128 ? bsr::launch_decode_d128(false, r16, smallp, tk, tv, p, grid, stream)
+                            : bsr::launch_decode_d64(false, r16, smallp, tk, tv, p, grid, stream);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return BSR_ERR_CUDA;
   }
   return BSR_OK;
+}
+
+}  // namespace
+
+extern "C" int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_pages,
+                                       const int32_t* indptr, const int32_t* indices,
+                                       const int32_t* last_page_len, int32_t batch,
+                                       int32_t num_qo_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t page_size,
+                                       int32_t num_pages_in_pool, float sm_scale, void* out,
+                                       int32_t out_dtype, float* lse, int32_t* device_status,
+                                       void* stream) {
+  return noalloc_impl(q, k_pages, v_pages, indptr, indices, last_page_len, batch, num_qo_heads,
+                      num_kv_heads, head_dim, page_size, num_pages_in_pool, sm_scale, false, 1.f,
+                      1.f, out, out_dtype, lse, device_status, stream);
+}
+
+extern "C" int bsr_attn_decode_noalloc_kv8(const void* q, const void* k_pages,
+                                           const void* v_pages, const int32_t* indptr,
+                                           const int32_t* indices, const int32_t* last_page_len,
+                                           int32_t batch, int32_t num_qo_heads,
+                                           int32_t num_kv_heads, int32_t head_dim,
+                                           int32_t page_size, int32_t num_pages_in_pool,
+                                           float sm_scale, float k_scale, float v_scale,
+                                           void* out, int32_t out_dtype, float* lse,
+                                           int32_t* device_status, void* stream) {
+  return noalloc_impl(q, k_pages, v_pages, indptr, indices, last_page_len, batch, num_qo_heads,
+                      num_kv_heads, head_dim, page_size, num_pages_in_pool, sm_scale, true,
+                      k_scale, v_scale, out, out_dtype, lse, device_status, stream);
 }

@@ -304,6 +304,19 @@ int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_pa
                             int32_t num_pages_in_pool, float sm_scale, void* out,
                             int32_t out_dtype, float* lse, int32_t* device_status, void* stream);
 
+/* bsr_attn_decode_noalloc over an FP8 (E4M3) KV cache: k_pages / v_pages hold one-byte
+ * codes in the same layout, the cached values k_scale * code and v_scale * code (as
+ * bsr_attn_run_kv8).  head_dim 128 and page_size >= 16 only (else
+ * BSR_ERR_UNSUPPORTED); k_scale and v_scale finite and > 0.  Allocation, scratch,
+ * status and ordering as bsr_attn_decode_noalloc. */
+int bsr_attn_decode_noalloc_kv8(const void* q, const void* k_pages, const void* v_pages,
+                                const int32_t* indptr, const int32_t* indices,
+                                const int32_t* last_page_len, int32_t batch,
+                                int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t page_size, int32_t num_pages_in_pool, float sm_scale,
+                                float k_scale, float v_scale, void* out, int32_t out_dtype,
+                                float* lse, int32_t* device_status, void* stream);
+
 /* Self-test of failure detection (no GPU fault involved): runs, on `stream`, the
  * bounded mbarrier wait the library's kernels use, on a barrier that nothing ever
  * arrives on; after `limit_ns` (1 ns .. 10 s) the wait gives up and bit 0 of the

@@ -89,6 +89,11 @@ def test_entry_points_reject_bad_arguments_without_a_gpu(lib):
     assert lib.bsr_append_kv(None, None, None, None, None, None, 1, 1, 1, 128, 3, 1, 0,
                              None, None, None, None) == -2
     assert lib.bsr_selftest_bounded_wait(None, 1000, None) == -1
+    # FP8 without a GPU: head_dim 64 is outside the FP8 kernel's set; a zero scale is refused
+    assert lib.bsr_attn_decode_noalloc_kv8(None, None, None, None, None, None, 1, 8, 2, 64, 16,
+                                           4, 0.125, 1.0, 1.0, None, 0, None, None, None) == -2
+    assert lib.bsr_attn_decode_noalloc_kv8(None, None, None, None, None, None, 1, 8, 2, 128, 16,
+                                           4, 0.125, 0.0, 1.0, None, 0, None, None, None) == -1
     # an unknown page layout
     assert lib.bsr_append_kv(None, None, None, None, None, None, 1, 1, 1, 128, 16, 1, 7,
                              None, None, None, None) == -1

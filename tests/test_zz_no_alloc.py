@@ -95,3 +95,27 @@ def test_noalloc_reports_pages_outside_the_pool():
     assert call_noalloc(w, tensors, out, lse, status) == 0
     assert int(status.item()) & 2
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("P", [16, 32])
+def test_noalloc_fp8_cache_matches_the_oracle_twice(P):
+    import oracle
+    w = wl.with_kv8(wl.make_paged(f"na8p{P}", 35 + P, [300, 17, 0, 1500, 64], Hq=32, Hk=8,
+                                  D=128, P=P), 36 + P)
+    dev = "cuda:0"
+    q, kc, vc = w.q.to(dev), w.k_codes.to(dev), w.v_codes.to(dev)
+    tab = [w.indptr.to(dev), w.indices.to(dev), w.last_page_len.to(dev)]
+    ro, rl = oracle.attention_kv8(w.q, w.k_codes, w.v_codes, w.k_scale, w.v_scale, w.indptr,
+                                  w.indices, w.last_page_len, w.qo_indptr,
+                                  num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
+                                  head_dim=w.head_dim, page_size=w.page_size, sm_scale=w.sm_scale)
+    for call in range(2):
+        out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=dev)
+        lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        bsr.bsr_attn_decode_noalloc_kv8(q, kc, vc, *tab, sm_scale=w.sm_scale, k_scale=w.k_scale,
+                                        v_scale=w.v_scale, out=out, lse=lse, device_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert_out_close(out.cpu().numpy(), ro, False, f"noalloc fp8 P{P} call {call}")
+        assert_lse_close(lse.cpu().numpy(), rl, f"noalloc fp8 P{P} call {call}")
