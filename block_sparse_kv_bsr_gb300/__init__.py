@@ -19,7 +19,7 @@ __all__ = [
     "BsrError", "load", "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run",
     "bsr_attn_run_kv8", "bsr_merge_states", "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info",
     "bsr_last_device_error", "bsr_status_string", "bsr_attn_decode_noalloc", "Schedule",
-    "bsr_attn_decode_noalloc_kv8",
+    "bsr_attn_decode_noalloc_kv8", "bsr_attn_decode_noalloc_ex",
     "bsr_schedule_set_stage_timing", "bsr_schedule_stage_times", "STAGES", "EXPORTED_SYMBOLS",
     "bsr_selftest_bounded_wait",
 ]
@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run", "bsr_attn_run_kv8", "bsr_merge_states",
     "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info", "bsr_last_device_error",
     "bsr_status_string", "bsr_attn_decode_noalloc", "bsr_attn_decode_noalloc_kv8",
+    "bsr_attn_decode_noalloc_ex",
     "bsr_schedule_set_stage_timing",
     "bsr_schedule_stage_times", "bsr_selftest_bounded_wait",
 )
@@ -123,6 +124,13 @@ def load(path: str | None = None):
                                                 ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
                                                 ctypes.c_float, ctypes.c_float, _vp,
                                                 ctypes.c_int32, _vp, _vp, _vp]
+    lib.bsr_attn_decode_noalloc_ex.restype = ctypes.c_int
+    lib.bsr_attn_decode_noalloc_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_int32,
+                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                               ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                               ctypes.c_int32, ctypes.c_float, ctypes.c_float,
+                                               ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp,
+                                               _vp]
     lib.bsr_status_string.restype = ctypes.c_char_p
     lib.bsr_status_string.argtypes = [ctypes.c_int]
     _lib = lib
@@ -434,4 +442,26 @@ def bsr_attn_decode_noalloc_kv8(q, k_pages, v_pages, indptr, indices, last_page_
                                            _dptr(lse), _dptr(device_status),
                                            _vp(_stream_ptr(stream)))
     _check(code, "bsr_attn_decode_noalloc_kv8")
+    return out, lse
+
+
+def bsr_attn_decode_noalloc_ex(q, k_pages, v_pages, indptr, indices, last_page_len, *,
+                               sm_scale: float, out, kv_dtype: str = "bf16", k_scale: float = 1.0,
+                               v_scale: float = 1.0, window_left: int = 0, lse=None,
+                               device_status=None, stream=None):
+    """No-allocation decode with the cache element type ("bf16" or "e4m3", the latter with
+    k_scale / v_scale) and an optional sliding window of ``window_left`` keys."""
+    import torch
+    lib = load()
+    num_pages, Hk, P, D = k_pages.shape
+    batch, Hq = q.shape[0], q.shape[1]
+    kd = {"bf16": 0, "e4m3": 1}[kv_dtype]
+    dt = BSR_DTYPE_F32 if out.dtype == torch.float32 else BSR_DTYPE_BF16
+    code = lib.bsr_attn_decode_noalloc_ex(_dptr(q), _dptr(k_pages), _dptr(v_pages),
+                                          _dptr(indptr), _dptr(indices), _dptr(last_page_len),
+                                          batch, Hq, Hk, D, P, num_pages, float(sm_scale), kd,
+                                          float(k_scale), float(v_scale), int(window_left),
+                                          _dptr(out), dt, _dptr(lse), _dptr(device_status),
+                                          _vp(_stream_ptr(stream)))
+    _check(code, "bsr_attn_decode_noalloc_ex")
     return out, lse

@@ -66,7 +66,7 @@ __global__ void fill_units_kernel(uint8_t* scratch, const int32_t* __restrict__ 
                                   const int32_t* __restrict__ indices,
                                   const int32_t* __restrict__ last_page_len, int32_t batch,
                                   int32_t Hk, int32_t group, int32_t P, int32_t num_pages,
-                                  int32_t splits, int32_t* status) {
+                                  int32_t splits, int32_t window_left, int32_t* status) {
   DecodeItem* items = reinterpret_cast<DecodeItem*>(scratch + kOffItems);
   int32_t* warp_ptr = reinterpret_cast<int32_t*>(scratch + kOffWarpPtr);
   int32_t* counters = reinterpret_cast<int32_t*>(scratch + kOffCounters);
@@ -90,9 +90,13 @@ __global__ void fill_units_kernel(uint8_t* scratch, const int32_t* __restrict__ 
     atomicOr(status, 2);
   }
   const int32_t align = P > kStageTokens ? P : kStageTokens;
-  int32_t len = (L + splits - 1) / splits;
+  // sliding window: the range starts at the page (or 16-key stage) holding the oldest
+  // key the query sees; older pages are never read
+  int32_t kb = 0;
+  if (window_left > 0 && L > window_left) kb = (L - window_left) / align * align;
+  int32_t len = (L - kb + splits - 1) / splits;
   len = (len + align - 1) / align * align;
-  int32_t t0 = s * len, t1 = t0 + len < L ? t0 + len : L;
+  int32_t t0 = kb + s * len, t1 = t0 + len < L ? t0 + len : L;
   if (t0 >= L) t0 = t1 = 0;  // an empty chunk still reports an empty state to the merge
   // The device table cannot be checked on the host: a chunk that names a page
   // outside the pool is dropped (reported in the status word) instead of read.
@@ -199,8 +203,9 @@ int noalloc_impl(const void* q, const void* k_pages, const void* v_pages, const 
                  const int32_t* indices, const int32_t* last_page_len, int32_t batch,
                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                  int32_t num_pages_in_pool, float sm_scale, bool kv8, float k_scale,
-                 float v_scale, void* out, int32_t out_dtype, float* lse,
+                 float v_scale, int32_t window_left, void* out, int32_t out_dtype, float* lse,
                  int32_t* device_status, void* stream_v) {
+  if (window_left < 0) return BSR_ERR_INVALID_ARGUMENT;
   if (batch < 0 || num_qo_heads <= 0 || num_kv_heads <= 0 || num_pages_in_pool < 0)
     return BSR_ERR_INVALID_ARGUMENT;
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return BSR_ERR_INVALID_ARGUMENT;
@@ -253,7 +258,7 @@ int noalloc_impl(const void* q, const void* k_pages, const void* v_pages, const 
 
   fill_units_kernel<<<(units + 255) / 256, 256, 0, stream>>>(
       scratch, indptr, indices, last_page_len, batch, num_kv_heads, group, page_size,
-      num_pages_in_pool, int32_t(splits), status);
+      num_pages_in_pool, int32_t(splits), window_left, status);
   if (cudaGetLastError() != cudaSuccess) return BSR_ERR_CUDA;
 
   const bool smallp = page_size < kStageTokens;
@@ -291,6 +296,7 @@ int noalloc_impl(const void* q, const void* k_pages, const void* v_pages, const 
   p.causal = 0;
   p.out_f32 = out_dtype == BSR_DTYPE_F32;
   p.num_warps = units;
+  p.window_left = window_left;
   p.rope_max_pos = 0;
   p.wait_limit_ns = 1000000000ull;
   const int grid = (units + kDecodeWarps - 1) / kDecodeWarps;
@@ -318,7 +324,7 @@ extern "C" int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const
                                        void* stream) {
   return noalloc_impl(q, k_pages, v_pages, indptr, indices, last_page_len, batch, num_qo_heads,
                       num_kv_heads, head_dim, page_size, num_pages_in_pool, sm_scale, false, 1.f,
-                      1.f, out, out_dtype, lse, device_status, stream);
+                      1.f, 0, out, out_dtype, lse, device_status, stream);
 }
 
 extern "C" int bsr_attn_decode_noalloc_kv8(const void* q, const void* k_pages,
@@ -332,5 +338,22 @@ extern "C" int bsr_attn_decode_noalloc_kv8(const void* q, const void* k_pages,
                                            int32_t* device_status, void* stream) {
   return noalloc_impl(q, k_pages, v_pages, indptr, indices, last_page_len, batch, num_qo_heads,
                       num_kv_heads, head_dim, page_size, num_pages_in_pool, sm_scale, true,
-                      k_scale, v_scale, out, out_dtype, lse, device_status, stream);
+                      k_scale, v_scale, 0, out, out_dtype, lse, device_status, stream);
+}
+
+extern "C" int bsr_attn_decode_noalloc_ex(const void* q, const void* k_pages, const void* v_pages,
+                                          const int32_t* indptr, const int32_t* indices,
+                                          const int32_t* last_page_len, int32_t batch,
+                                          int32_t num_qo_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t page_size,
+                                          int32_t num_pages_in_pool, float sm_scale,
+                                          int32_t kv_dtype, float k_scale, float v_scale,
+                                          int32_t window_left, void* out, int32_t out_dtype,
+                                          float* lse, int32_t* device_status, void* stream) {
+  if (kv_dtype != BSR_KV_DTYPE_BF16 && kv_dtype != BSR_KV_DTYPE_E4M3) return BSR_ERR_INVALID_ARGUMENT;
+  const bool kv8 = kv_dtype == BSR_KV_DTYPE_E4M3;
+  return noalloc_impl(q, k_pages, v_pages, indptr, indices, last_page_len, batch, num_qo_heads,
+                      num_kv_heads, head_dim, page_size, num_pages_in_pool, sm_scale, kv8,
+                      kv8 ? k_scale : 1.f, kv8 ? v_scale : 1.f, window_left, out, out_dtype, lse,
+                      device_status, stream);
 }

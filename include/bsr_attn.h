@@ -69,6 +69,8 @@ enum {
 enum { BSR_DTYPE_BF16 = 0, BSR_DTYPE_F32 = 1 };
 /* page pool layouts: head-major [pages, Hk, P, D] or token-major [pages, P, Hk, D] */
 enum { BSR_KV_HND = 0, BSR_KV_NHD = 1 };
+/* element type of a KV cache (bsr_attn_decode_noalloc_ex) */
+enum { BSR_KV_DTYPE_BF16 = 0, BSR_KV_DTYPE_E4M3 = 1 };
 
 typedef struct bsr_schedule* bsr_schedule_t;
 
@@ -316,6 +318,20 @@ int bsr_attn_decode_noalloc_kv8(const void* q, const void* k_pages, const void* 
                                 int32_t page_size, int32_t num_pages_in_pool, float sm_scale,
                                 float k_scale, float v_scale, void* out, int32_t out_dtype,
                                 float* lse, int32_t* device_status, void* stream);
+
+/* The general no-allocation decode: kv_dtype BSR_KV_DTYPE_BF16 (k_scale / v_scale
+ * ignored) or BSR_KV_DTYPE_E4M3 (as bsr_attn_decode_noalloc_kv8), and window_left >= 0
+ * (0: every key; W > 0: the query at position L - 1 sees keys L - W .. L - 1, and each
+ * (request, kv head) range starts at the page holding key L - W, so older pages are
+ * never read). */
+int bsr_attn_decode_noalloc_ex(const void* q, const void* k_pages, const void* v_pages,
+                               const int32_t* indptr, const int32_t* indices,
+                               const int32_t* last_page_len, int32_t batch,
+                               int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t page_size, int32_t num_pages_in_pool, float sm_scale,
+                               int32_t kv_dtype, float k_scale, float v_scale,
+                               int32_t window_left, void* out, int32_t out_dtype, float* lse,
+                               int32_t* device_status, void* stream);
 
 /* Self-test of failure detection (no GPU fault involved): runs, on `stream`, the
  * bounded mbarrier wait the library's kernels use, on a barrier that nothing ever

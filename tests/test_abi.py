@@ -94,6 +94,13 @@ def test_entry_points_reject_bad_arguments_without_a_gpu(lib):
                                            4, 0.125, 1.0, 1.0, None, 0, None, None, None) == -2
     assert lib.bsr_attn_decode_noalloc_kv8(None, None, None, None, None, None, 1, 8, 2, 128, 16,
                                            4, 0.125, 0.0, 1.0, None, 0, None, None, None) == -1
+    # the general entry: an unknown cache dtype and a negative window are refused
+    assert lib.bsr_attn_decode_noalloc_ex(None, None, None, None, None, None, 1, 8, 2, 128, 16,
+                                          4, 0.125, 7, 1.0, 1.0, 0, None, 0, None, None,
+                                          None) == -1
+    assert lib.bsr_attn_decode_noalloc_ex(None, None, None, None, None, None, 1, 8, 2, 128, 16,
+                                          4, 0.125, 0, 1.0, 1.0, -5, None, 0, None, None,
+                                          None) == -1
     # an unknown page layout
     assert lib.bsr_append_kv(None, None, None, None, None, None, 1, 1, 1, 128, 16, 1, 7,
                              None, None, None, None) == -1

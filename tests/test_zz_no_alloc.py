@@ -119,3 +119,35 @@ def test_noalloc_fp8_cache_matches_the_oracle_twice(P):
         assert int(status.item()) == 0
         assert_out_close(out.cpu().numpy(), ro, False, f"noalloc fp8 P{P} call {call}")
         assert_lse_close(lse.cpu().numpy(), rl, f"noalloc fp8 P{P} call {call}")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "e4m3"])
+def test_noalloc_sliding_window(kv_dtype):
+    # pages wholly older than every window point at one NaN-poisoned page: a read there
+    # would show as NaN
+    import oracle
+    w = wl.sliding_window_decode("naw", 37, [900, 3000, 40, 1700], 300, Hq=32, Hk=8, D=128,
+                                 P=16, causal=False)
+    if kv_dtype == "e4m3":
+        w = wl.with_kv8(w, 38)
+    dev = "cuda:0"
+    q = w.q.to(dev)
+    k, v = ((w.k_codes, w.v_codes) if kv_dtype == "e4m3" else (w.k_pages, w.v_pages))
+    tab = [w.indptr.to(dev), w.indices.to(dev), w.last_page_len.to(dev)]
+    kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+              page_size=w.page_size, sm_scale=w.sm_scale, window_left=w.window_left)
+    table = (w.indptr, w.indices, w.last_page_len, w.qo_indptr)
+    if kv_dtype == "e4m3":
+        ro, rl = oracle.attention_kv8(w.q, w.k_codes, w.v_codes, w.k_scale, w.v_scale, *table, **kw)
+    else:
+        ro, rl = oracle.attention(w.q, w.k_pages, w.v_pages, *table, **kw)
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    bsr.bsr_attn_decode_noalloc_ex(q, k.to(dev), v.to(dev), *tab, sm_scale=w.sm_scale, out=out,
+                                   kv_dtype=kv_dtype, k_scale=w.k_scale, v_scale=w.v_scale,
+                                   window_left=w.window_left, lse=lse, device_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert_out_close(out.cpu().numpy(), ro, False, f"noalloc window {kv_dtype}")
+    assert_lse_close(lse.cpu().numpy(), rl, f"noalloc window {kv_dtype}")
