@@ -10,9 +10,13 @@ of active KV against 129 MB of L2), so consecutive steps read KV from HBM.
 value     = algorithmic bytes (active K+V, q, out, lse, page table) / device time per step.
 e2e       = the same bytes / time of the call a user makes with HOST buffers:
             re-plan from host page-table arrays, H2D of q, run, D2H of out and lse.
-roofline  = the decode kernel's algorithmic bytes / its mean CUDA-event duration,
-            against the measured HBM copy bandwidth.
-cpu_baseline = the fp64 oracle on this host's cores (a bounded sample of the batch).
+roofline  = the dominant kernel's algorithmic bytes (or FLOPs) / its mean CUDA-event
+            duration, against the measured HBM copy bandwidth (or bf16 dense peak); also
+            its p10 / median / p90 over the timed calls and the DRAM traffic from the
+            committed ncu summary of the same build.
+cpu_baseline = the fp64 oracle on this host's cores over whole passes for ~10 s (decode
+            workloads; configs 1 and 2 add a one-thread figure).
+clocks    = nvidia-smi samples taken during the first timed region.
 
 --config selects another workload for measurement (2: Llama-3-8B-shaped decode with RoPE,
 4: shared-prefix cascade, 5: chunked prefill with append, reported in TFLOP/s, 6: the
@@ -20,7 +24,8 @@ skewed decode over an FP8 (E4M3) KV cache, 7: sliding-window decode over long hi
 8: the skewed decode with RoPE at the kept blocks' logical positions, 9: a three-level
 cascade of shared prefixes, 10: the skewed decode over token-major (NHD) pages);
 the default is the skewed decode above.  --impl reference times the oracle (the only
-reference this method has here) on the same workload.  Under torchrun each rank runs an
+reference this method has here) on the same workload, each step one pass over the batch
+or, when K passes would take more than ~90 s, over every k-th request.  Under torchrun each rank runs an
 independent replica (weak scaling).
 """
 from __future__ import annotations
