@@ -203,3 +203,23 @@ def test_plan_does_not_depend_on_earlier_plans():
     assert np.array_equal(first, again)
     plan_of(wl.config1(), num_sms=152)
     assert np.array_equal(first, plan_of(a, num_sms=152)[1])
+
+
+def test_host_array_forms_give_the_same_plan():
+    # CPU int32 tensors and int32 numpy arrays go to the planner in place; other forms
+    # (int64, non-contiguous, lists) are converted: every form plans the same batch
+    import torch
+    w = wl.config3(small=True)
+    base = plan_of(w, num_sms=8)[1]
+    kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+              page_size=w.page_size, num_pages=w.num_pages, num_sms=8)
+    forms = [
+        lambda t: t.numpy(),                                        # int32 numpy, in place
+        lambda t: t.to(torch.int64),                                # converted
+        lambda t: torch.stack([t, t], 1)[:, 0],                     # non-contiguous view
+        lambda t: t.tolist(),                                       # a list
+    ]
+    for f in forms:
+        _, units = bsr.bsr_attn_plan_host(f(w.indptr), f(w.indices), f(w.last_page_len),
+                                          qo_indptr=f(w.qo_indptr), **kw)
+        assert np.array_equal(units, base)
