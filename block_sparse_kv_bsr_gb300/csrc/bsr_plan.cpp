@@ -57,11 +57,6 @@ struct Unit {
   int32_t kbegin;   // first key any of the rows may see (aligned down to the cut alignment)
 };
 
-struct Piece {
-  int32_t unit, tok0, tok1;
-  int64_t cost;
-};
-
 // cos/sin of every (position, frequency), angles in fp64 rounded once to fp32, in two
 // orders.  frag: the order the decode kernel's fragments consume them, per position
 // D/4 groups of two (cos, sin) pairs, group i * 4 + t (quad t < 4, i < D/16) holding
@@ -95,6 +90,51 @@ struct WorkList {
   double imbalance = 1.0;
 };
 
+// The ranges to cut, longest first, and the limits of the cut.
+struct CutInput {
+  const int64_t* kb;   // first key of each range, in cut order
+  const int64_t* ke;   // one past its last key
+  size_t n;
+  int64_t overhead, align_mask, min_piece, max_workers;   // align_mask: ~(align - 1)
+  int workers;
+};
+
+// Cut with budget T: ranges are laid end to end and each worker takes pieces until
+// the next one would pass T; a range that does not fit is cut at an `align`-key
+// boundary (no piece shorter than `min_piece`) and continues on the next worker.
+// `align` is a power of two, so rounding down is a mask (a negative length rounds
+// to a negative take, which places no piece, as a truncating division would).
+// Calls emit(range, tok0, tok1, worker) for every piece in order and returns the
+// number of workers the cut needs (anything above `workers` means "does not fit").
+template <class Emit>
+int64_t cut_ranges(const CutInput& in, int64_t T, Emit&& emit) {
+  int64_t w = 0, room = T;
+  for (size_t oi = 0; oi < in.n; ++oi) {
+    const int64_t kend = in.ke[oi];
+    int64_t pos = in.kb[oi];
+    for (;;) {   // until the piece ending at kend is placed (an empty range still needs one)
+      const int64_t rest = kend - pos;
+      if (rest + in.overhead <= room) {
+        emit(oi, pos, kend, w);
+        room -= rest + in.overhead;
+        break;
+      }
+      int64_t take = (room - in.overhead) & in.align_mask;
+      if (rest - take < in.min_piece) take = (rest - in.min_piece) & in.align_mask;
+      if (take >= in.min_piece) {
+        emit(oi, pos, pos + take, w);
+        pos += take;
+      } else if (room == T) {
+        return in.max_workers + 2;  // budget below one piece: cannot make progress
+      }
+      ++w;
+      room = T;
+      if (w >= in.workers) return w + 1;
+    }
+  }
+  return w + 1;
+}
+
 // Cut key ranges into pieces and spread them over at most `max_workers`
 // workers at equal cost.  Ranges are laid end to end, longest first, and the
 // sequence is cut into consecutive per-worker segments of (almost) equal
@@ -104,32 +144,55 @@ struct WorkList {
 // (the interleaving of long and short work).  The budget is the smallest one
 // for which the cut fits the workers, found by bisection, so the busiest
 // worker carries about one piece-alignment more than the mean.  The result
-// is a pure function of its inputs.
+// is a pure function of its inputs.  `align` is a power of two (a page or a
+// key tile).
 void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align, int64_t overhead,
              int64_t min_piece, int64_t min_worker_work, WorkList* out, int64_t* k_hint = nullptr) {
   // Working arrays live across calls (per thread), so a plan per decode step reuses
   // their memory instead of faulting in fresh pages.
   struct Scratch {
-    std::vector<uint64_t> keys;
-    std::vector<int32_t> order, owner, pieces_of_unit, first_slot, next_slot;
+    std::vector<uint32_t> key, key_tmp;
+    std::vector<int32_t> order, order_tmp, pieces_of_unit, first_slot, next_slot;
     std::vector<int64_t> kb, ke, load;
-    std::vector<Piece> pieces;
   };
   thread_local Scratch sc;
-  // longest first, ties in unit order: one integer key per unit
-  sc.keys.resize(units.size());
-  for (size_t i = 0; i < units.size(); ++i)
-    sc.keys[i] = (uint64_t(uint32_t(INT32_MAX - (units[i].kend - units[i].kbegin))) << 32) | uint64_t(i);
-  std::sort(sc.keys.begin(), sc.keys.end());
-  std::vector<int32_t>& order = sc.order;
-  order.resize(units.size());
+  const size_t n = units.size();
+  // Longest first, ties in unit order: a stable radix sort (8-bit digits, least
+  // significant first) on INT32_MAX - length, skipping digits all ranges share.
+  sc.key.resize(n);
+  sc.key_tmp.resize(n);
+  sc.order.resize(n);
+  sc.order_tmp.resize(n);
+  uint32_t hist[4][256] = {};
+  for (size_t i = 0; i < n; ++i) {
+    const uint32_t d = uint32_t(INT32_MAX - (units[i].kend - units[i].kbegin));
+    sc.key[i] = d;
+    sc.order[i] = int32_t(i);
+    for (int b = 0; b < 4; ++b) ++hist[b][(d >> (8 * b)) & 255u];
+  }
+  for (int b = 0; b < 4 && n > 0; ++b) {
+    const int sh = 8 * b;
+    if (hist[b][(sc.key[0] >> sh) & 255u] == n) continue;
+    uint32_t off[256], run = 0;
+    for (int v = 0; v < 256; ++v) {
+      off[v] = run;
+      run += hist[b][v];
+    }
+    for (size_t i = 0; i < n; ++i) {
+      const uint32_t dst = off[(sc.key[i] >> sh) & 255u]++;
+      sc.key_tmp[dst] = sc.key[i];
+      sc.order_tmp[dst] = sc.order[i];
+    }
+    sc.key.swap(sc.key_tmp);
+    sc.order.swap(sc.order_tmp);
+  }
+  const std::vector<int32_t>& order = sc.order;
   // key ranges in that order, contiguous for the cut passes
   std::vector<int64_t>& kb = sc.kb;
   std::vector<int64_t>& ke = sc.ke;
-  kb.resize(units.size());
-  ke.resize(units.size());
-  for (size_t i = 0; i < units.size(); ++i) {
-    order[i] = int32_t(sc.keys[i] & 0xffffffffu);
+  kb.resize(n);
+  ke.resize(n);
+  for (size_t i = 0; i < n; ++i) {
     kb[i] = units[order[i]].kbegin;
     ke[i] = units[order[i]].kend;
   }
@@ -138,62 +201,19 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
   const int workers =
       units.empty() ? 0
                     : int(std::max<int64_t>(1, std::min<int64_t>(max_workers, (total + min_worker_work - 1) / min_worker_work)));
-  std::vector<Piece>& pieces = sc.pieces;
-  std::vector<int32_t>& owner = sc.owner;
-  pieces.clear();
-  owner.clear();
-  // Cut with budget T; returns the number of workers the cut needs (anything
-  // above `workers` means "does not fit").
-  auto partition = [&](int64_t T, bool record) -> int64_t {
-    if (record) {
-      pieces.clear();
-      owner.clear();
-    }
-    int64_t w = 0, room = T;
-    const size_t n = order.size();
-    for (size_t oi = 0; oi < n; ++oi) {
-      const int32_t u = order[oi];
-      const int64_t kend = ke[oi];
-      int64_t pos = kb[oi];
-      bool placed = false;  // the piece ending at kend (an empty range still needs one)
-      while (!placed) {
-        const int64_t rest = kend - pos;
-        if (rest + overhead <= room) {
-          if (record) {
-            pieces.push_back({u, int32_t(pos), int32_t(kend), rest + overhead});
-            owner.push_back(int32_t(w));
-          }
-          room -= rest + overhead;
-          pos = kend;
-          placed = true;
-        } else {
-          int64_t take = (room - overhead) / align * align;
-          if (rest - take < min_piece) take = (rest - min_piece) / align * align;
-          const bool fresh = room == T;
-          if (take >= min_piece) {
-            if (record) {
-              pieces.push_back({u, int32_t(pos), int32_t(pos + take), take + overhead});
-              owner.push_back(int32_t(w));
-            }
-            pos += take;
-          } else if (fresh) {
-            return max_workers + 2;  // budget below one piece: cannot make progress
-          }
-          ++w;
-          room = T;
-          if (w >= workers) return w + 1;
-        }
-      }
-    }
-    return w + 1;
-  };
+  const CutInput in{kb.data(), ke.data(), n, overhead, ~(align - 1), min_piece, max_workers, workers};
+  std::vector<int32_t>& pieces_of_unit = sc.pieces_of_unit;
+  pieces_of_unit.assign(n, 0);
+  int64_t T = 0;
   if (!units.empty()) {
     int64_t lo = std::max<int64_t>((total + workers - 1) / workers, 2 * min_piece + overhead + align);
     // The budget is the smallest T = lo + k (k >= 0) for which the cut fits (the cut
     // needs fewer workers as T grows).  A caller that re-plans similar batches passes
     // the last k as a hint: two cuts confirm it (it fits, k - 1 does not); otherwise
     // a doubling search from one alignment step, then halving.  Either way the same k.
-    auto fits = [&](int64_t k) { return partition(lo + k, false) <= workers; };
+    auto fits = [&](int64_t k) {
+      return cut_ranges(in, lo + k, [](size_t, int64_t, int64_t, int64_t) {}) <= workers;
+    };
     int64_t k = -1;
     if (k_hint != nullptr && *k_hint >= 0 && fits(*k_hint) && (*k_hint == 0 || !fits(*k_hint - 1)))
       k = *k_hint;
@@ -214,53 +234,54 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
       }
     }
     if (k_hint != nullptr) *k_hint = k;
-    partition(lo + k, true);
+    T = lo + k;
+    cut_ranges(in, T, [&](size_t oi, int64_t, int64_t, int64_t) { ++pieces_of_unit[order[oi]]; });
   }
 
-  std::vector<int32_t>& pieces_of_unit = sc.pieces_of_unit;
-  pieces_of_unit.assign(units.size(), 0);
-  for (const Piece& pc : pieces) pieces_of_unit[pc.unit]++;
   std::vector<int32_t>& first_slot = sc.first_slot;
   std::vector<int32_t>& next_slot = sc.next_slot;
-  first_slot.assign(units.size(), -1);
-  next_slot.assign(units.size(), 0);
+  first_slot.assign(n, -1);
+  next_slot.assign(n, 0);
   out->n_partials = 0;
   out->n_split = 0;
-  for (size_t u = 0; u < units.size(); ++u)
+  int64_t n_pieces = 0;
+  for (size_t u = 0; u < n; ++u) {
+    n_pieces += pieces_of_unit[u];
     if (pieces_of_unit[u] > 1) {
       first_slot[u] = out->n_partials;
       out->n_partials += pieces_of_unit[u];
       ++out->n_split;
     }
-  // the cut emits pieces worker by worker, so piece order is already grouped by worker
-  out->items.clear();
-  out->items.reserve(pieces.size());
+  }
+  // the cut emits pieces worker by worker, so item order is grouped by worker
+  out->items.resize(size_t(n_pieces));
   out->ptr.assign(workers + 1, 0);
   std::vector<int64_t>& load = sc.load;
   load.assign(workers, 0);
-  size_t i = 0;
-  for (int w = 0; w < workers; ++w) {
-    for (; i < pieces.size() && owner[i] == w; ++i) {
-      const Piece& pc = pieces[i];
-      const Unit& u = units[pc.unit];
-      DecodeItem it{};
+  if (!units.empty()) {
+    int64_t cur = 0;
+    int32_t idx = 0;
+    cut_ranges(in, T, [&](size_t oi, int64_t tok0, int64_t tok1, int64_t w) {
+      while (cur < w) out->ptr[++cur] = idx;
+      const int32_t ui = order[oi];
+      const Unit& u = units[ui];
+      DecodeItem& it = out->items[idx++];
       it.req = u.req;
       it.kvh = u.kvh;
       it.row0 = u.row0;
       it.nrows = u.nrows;
-      it.tok0 = pc.tok0;
-      it.tok1 = pc.tok1;
-      it.nchunks = pieces_of_unit[pc.unit];
-      it.first_slot = first_slot[pc.unit];
+      it.tok0 = int32_t(tok0);
+      it.tok1 = int32_t(tok1);
+      it.nchunks = pieces_of_unit[ui];
+      it.first_slot = first_slot[ui];
       // pieces of a range are cut in key order, so slot order is key order
-      it.slot = it.nchunks > 1 ? first_slot[pc.unit] + next_slot[pc.unit]++ : -1;
+      it.slot = it.nchunks > 1 ? first_slot[ui] + next_slot[ui]++ : -1;
       it.page_base = u.page_base;
       it.q_row0 = u.q_row0;
       it.qpos0 = u.qpos0;
-      out->items.push_back(it);
-      load[w] += pc.cost;
-    }
-    out->ptr[w + 1] = int32_t(out->items.size());
+      load[w] += tok1 - tok0 + overhead;
+    });
+    while (cur < workers) out->ptr[++cur] = idx;
   }
   out->workers = workers;
   out->imbalance = 1.0;
@@ -407,6 +428,9 @@ struct HostPlan {
   // largest position a stage may touch (sizes the cos/sin table)
   std::vector<int32_t> qshift;
   int64_t max_pos_end = 0;
+  // working arrays, kept with the plan so that re-planning reuses their memory
+  std::vector<int32_t> kv_len, qo_len, q_row0;
+  std::vector<Unit> dunits, punits;
 };
 
 int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
@@ -432,7 +456,12 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   // ---------------------------------------------------------------- table validation
   if (indptr[0] != 0) return BSR_ERR_PAGE_TABLE;
   if (qo_indptr != nullptr && qo_indptr[0] != 0) return BSR_ERR_PAGE_TABLE;
-  std::vector<int32_t> kv_len(batch), qo_len(batch), q_row0(batch);
+  std::vector<int32_t>& kv_len = hp->kv_len;
+  std::vector<int32_t>& qo_len = hp->qo_len;
+  std::vector<int32_t>& q_row0 = hp->q_row0;
+  kv_len.resize(batch);
+  qo_len.resize(batch);
+  q_row0.resize(batch);
   int64_t sum_qo = 0, active = 0;
   int32_t max_len = 0;
   for (int32_t b = 0; b < batch; ++b) {
@@ -458,17 +487,32 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   if (sum_qo > INT32_MAX / num_qo_heads) return BSR_ERR_UNSUPPORTED;
   const int64_t nnz = indptr[batch];
   if (nnz > 0 && indices == nullptr) return BSR_ERR_INVALID_ARGUMENT;
-  for (int64_t e = 0; e < nnz; ++e)
-    if (indices[e] < 0 || indices[e] >= num_pages_in_pool) return BSR_ERR_PAGE_TABLE;
+  // range checks as min/max reductions (no early exit, so the loops vectorize)
+  auto min_max = [](const int32_t* v, int64_t n, int32_t* mn, int32_t* mx) {
+    int32_t a = INT32_MAX, b = INT32_MIN;
+    for (int64_t e = 0; e < n; ++e) {
+      a = std::min(a, v[e]);
+      b = std::max(b, v[e]);
+    }
+    *mn = a;
+    *mx = b;
+  };
+  if (nnz > 0) {
+    int32_t mn, mx;
+    min_max(indices, nnz, &mn, &mx);
+    if (mn < 0 || mx >= num_pages_in_pool) return BSR_ERR_PAGE_TABLE;
+  }
   // per-page logical positions (RoPE over caches with dropped blocks): a 16-key stage
   // must lie inside one page, so pages of fewer than 16 keys are refused with RoPE
   hp->qshift.assign(page_pos ? batch : 0, 0);
   hp->max_pos_end = 0;
   if (page_pos != nullptr) {
     if (rope && page_size < kStageTokens) return BSR_ERR_UNSUPPORTED;
-    for (int64_t e = 0; e < nnz; ++e) {
-      if (page_pos[e] < 0 || page_pos[e] > INT32_MAX / 4) return BSR_ERR_PAGE_TABLE;
-      hp->max_pos_end = std::max<int64_t>(hp->max_pos_end, int64_t(page_pos[e]) + page_size);
+    if (nnz > 0) {
+      int32_t mn, mx;
+      min_max(page_pos, nnz, &mn, &mx);
+      if (mn < 0 || mx > INT32_MAX / 4) return BSR_ERR_PAGE_TABLE;
+      hp->max_pos_end = int64_t(mx) + page_size;
     }
     for (int32_t b = 0; b < batch; ++b)
       if (indptr[b + 1] > indptr[b])
@@ -482,7 +526,10 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   // 128, pages of at least 16 keys, a head group that divides the 128-row
   // tile, so that a tile is whole queries); the others use the decode
   // kernel's 16-row groups.  Prefill units hold up to two query tiles (256 rows).
-  std::vector<Unit> dunits, punits;
+  std::vector<Unit>& dunits = hp->dunits;
+  std::vector<Unit>& punits = hp->punits;
+  dunits.clear();
+  punits.clear();
   int32_t max_rows = 0;
   for (int32_t b = 0; b < batch; ++b) {
     const int32_t rows = qo_len[b] * group;
