@@ -223,3 +223,28 @@ def test_host_array_forms_give_the_same_plan():
         _, units = bsr.bsr_attn_plan_host(f(w.indptr), f(w.indices), f(w.last_page_len),
                                           qo_indptr=f(w.qo_indptr), **kw)
         assert np.array_equal(units, base)
+
+
+def test_ranges_are_cut_longest_first_in_unit_order():
+    # The cut lays the key ranges end to end, longest first and equal lengths in unit
+    # order (request, then kv head), so in worker order every range's pieces are
+    # consecutive and the ranges appear by non-increasing length.  Lengths above 2^16
+    # and 2^24 keys and many ties exercise every digit of the length sort.
+    P, Hk = 16, 2
+    lens = [1000, 300000, 70000, 0, 1000, 70000, 65541, 16, 17000000, 1000, 1, 65541]
+    npages = [(n + P - 1) // P for n in lens]
+    indptr = np.concatenate([[0], np.cumsum(npages)]).astype(np.int32)
+    indices = np.arange(indptr[-1], dtype=np.int32)
+    last = np.array([n - (m - 1) * P if m else 0 for n, m in zip(lens, npages)], np.int32)
+    info, units = bsr.bsr_attn_plan_host(indptr, indices, last, num_qo_heads=Hk, num_kv_heads=Hk,
+                                         head_dim=128, page_size=P, num_pages=int(indptr[-1]),
+                                         num_sms=4)
+    assert info["num_split_streams"] > 0
+    seen = []
+    for req, kvh, *_ in units.tolist():
+        if not seen or seen[-1] != (req, kvh):
+            assert (req, kvh) not in seen, "a range's pieces are not consecutive"
+            seen.append((req, kvh))
+    expect = sorted(((b, h) for b in range(len(lens)) for h in range(Hk)),
+                    key=lambda u: (-lens[u[0]], u))
+    assert seen == expect
