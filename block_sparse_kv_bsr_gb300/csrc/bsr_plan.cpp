@@ -214,9 +214,14 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
     auto fits = [&](int64_t k) {
       return cut_ranges(in, lo + k, [](size_t, int64_t, int64_t, int64_t) {}) <= workers;
     };
+    auto count = [&](size_t oi, int64_t, int64_t, int64_t) { ++pieces_of_unit[order[oi]]; };
     int64_t k = -1;
-    if (k_hint != nullptr && *k_hint >= 0 && fits(*k_hint) && (*k_hint == 0 || !fits(*k_hint - 1)))
+    bool counted = false;   // pieces_of_unit holds the cut at lo + k
+    if (k_hint != nullptr && *k_hint >= 0 && cut_ranges(in, lo + *k_hint, count) <= workers &&
+        (*k_hint == 0 || !fits(*k_hint - 1))) {
       k = *k_hint;
+      counted = true;
+    }
     if (k < 0) {
       if (fits(0)) {
         k = 0;
@@ -235,7 +240,10 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
     }
     if (k_hint != nullptr) *k_hint = k;
     T = lo + k;
-    cut_ranges(in, T, [&](size_t oi, int64_t, int64_t, int64_t) { ++pieces_of_unit[order[oi]]; });
+    if (!counted) {
+      pieces_of_unit.assign(n, 0);
+      cut_ranges(in, T, count);
+    }
   }
 
   std::vector<int32_t>& first_slot = sc.first_slot;
