@@ -21,6 +21,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -59,70 +60,76 @@ static_assert(kOffWarpPtr % 256 == 0 && kOffCounters % 256 == 0 && kOffStatus % 
 // cudaGetSymbolAddress for the current device.
 static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
 
-// Writes one work unit per (request, kv head, chunk) and the per-warp ranges
-// (one unit per warp), and clears the merge counters: every call starts from
-// a known state whatever the previous call left behind.
-__global__ void fill_units_kernel(uint8_t* scratch, const int32_t* __restrict__ indptr,
-                                  const int32_t* __restrict__ indices,
-                                  const int32_t* __restrict__ last_page_len, int32_t batch,
-                                  int32_t Hk, int32_t group, int32_t P, int32_t num_pages,
-                                  int32_t splits, int32_t window_left, int32_t* status) {
+// One block per request.  The block checks the request's table entries and every
+// page its query reads, then writes the request's work units (one per (kv head,
+// chunk)), points one warp at each, and clears their merge counters: every call
+// starts from a known state whatever the previous call left behind.  A request
+// whose entries are malformed (negative page count or offset, last_page_len
+// outside [1, P], a length beyond 32-bit keys) or which reads a page outside the
+// pool gets empty units -- all of its chunks, so its out is 0 and its lse -inf --
+// and bit 1 of the status word is set.
+constexpr int kFillThreads = 256;
+__global__ void __launch_bounds__(kFillThreads)
+    fill_units_kernel(uint8_t* scratch, const int32_t* __restrict__ indptr,
+                      const int32_t* __restrict__ indices,
+                      const int32_t* __restrict__ last_page_len, int32_t batch, int32_t Hk,
+                      int32_t group, int32_t P, int32_t num_pages, int32_t splits,
+                      int32_t window_left, int32_t* status) {
   DecodeItem* items = reinterpret_cast<DecodeItem*>(scratch + kOffItems);
   int32_t* warp_ptr = reinterpret_cast<int32_t*>(scratch + kOffWarpPtr);
   int32_t* counters = reinterpret_cast<int32_t*>(scratch + kOffCounters);
-  const int32_t units = batch * Hk * splits;
-  const int32_t u = blockIdx.x * blockDim.x + threadIdx.x;
-  if (u == 0) warp_ptr[units] = units;
-  if (u >= units) return;
-  const int32_t s = u % splits;
-  const int32_t bh = u / splits;
-  const int32_t b = bh / Hk, kvh = bh % Hk;
-  const int32_t n = indptr[b + 1] - indptr[b];
-  int32_t L = 0;
-  if (n > 0) {
+  const int32_t b = blockIdx.x;
+  if (b == 0 && threadIdx.x == 0) warp_ptr[batch * Hk * splits] = batch * Hk * splits;
+  const int32_t base = indptr[b];
+  const int64_t n = int64_t(indptr[b + 1]) - base;
+  bool bad = base < 0 || n < 0;
+  int64_t L = 0;
+  if (!bad && n > 0) {
     const int32_t last = last_page_len[b];
-    if (last >= 1 && last <= P) {
-      L = (n - 1) * P + last;
-    } else if (status != nullptr) {
-      atomicOr(status, 2);
-    }
-  } else if (n < 0 && status != nullptr) {
-    atomicOr(status, 2);
+    L = (n - 1) * P + last;
+    bad = last < 1 || last > P || L > INT32_MAX;
   }
   const int32_t align = P > kStageTokens ? P : kStageTokens;
   // sliding window: the range starts at the page (or 16-key stage) holding the oldest
-  // key the query sees; older pages are never read
-  int32_t kb = 0;
-  if (window_left > 0 && L > window_left) kb = (L - window_left) / align * align;
-  int32_t len = (L - kb + splits - 1) / splits;
-  len = (len + align - 1) / align * align;
-  int32_t t0 = kb + s * len, t1 = t0 + len < L ? t0 + len : L;
-  if (t0 >= L) t0 = t1 = 0;  // an empty chunk still reports an empty state to the merge
-  // The device table cannot be checked on the host: a chunk that names a page
-  // outside the pool is dropped (reported in the status word) instead of read.
-  for (int32_t j = t0 / P; t1 > t0 && j < (t1 + P - 1) / P; ++j) {
-    const int32_t page = indices[indptr[b] + j];
-    if (page < 0 || page >= num_pages) {
-      if (status != nullptr) atomicOr(status, 2);
-      t0 = t1 = 0;
+  // key the query sees; older pages are never read (and not checked)
+  int64_t kb = 0;
+  if (!bad && window_left > 0 && L > window_left) kb = (L - window_left) / align * align;
+  // the device table cannot be checked on the host: check the pages this query reads
+  if (!bad)
+    for (int64_t j = kb / P + threadIdx.x; j < (L + P - 1) / P; j += kFillThreads) {
+      const int32_t page = indices[base + j];
+      bad |= page < 0 || page >= num_pages;
     }
+  bad = __syncthreads_or(bad) != 0;
+  if (bad) {
+    if (threadIdx.x == 0 && status != nullptr) atomicOr(status, 2);
+    L = kb = 0;
   }
-  DecodeItem it;
-  it.req = b;
-  it.kvh = kvh;
-  it.row0 = 0;
-  it.nrows = group;
-  it.tok0 = t0;
-  it.tok1 = t1;
-  it.nchunks = splits;
-  it.first_slot = bh * splits;
-  it.slot = splits > 1 ? u : -1;
-  it.page_base = indptr[b];
-  it.q_row0 = b;
-  it.qpos0 = L - 1;
-  items[u] = it;
-  warp_ptr[u] = u;
-  if (s == 0) counters[bh * splits] = 0;
+  int64_t len = (L - kb + splits - 1) / splits;
+  len = (len + align - 1) / align * align;
+  for (int32_t i = threadIdx.x; i < Hk * splits; i += kFillThreads) {
+    const int32_t kvh = i / splits, s = i % splits;
+    const int32_t bh = b * Hk + kvh;
+    const int32_t u = bh * splits + s;
+    int64_t t0 = kb + s * len, t1 = t0 + len < L ? t0 + len : L;
+    if (t0 >= L) t0 = t1 = 0;  // an empty chunk still reports an empty state to the merge
+    DecodeItem it;
+    it.req = b;
+    it.kvh = kvh;
+    it.row0 = 0;
+    it.nrows = group;
+    it.tok0 = int32_t(t0);
+    it.tok1 = int32_t(t1);
+    it.nchunks = splits;
+    it.first_slot = bh * splits;
+    it.slot = splits > 1 ? u : -1;
+    it.page_base = bad ? 0 : base;
+    it.q_row0 = b;
+    it.qpos0 = int32_t(L) - 1;
+    items[u] = it;
+    warp_ptr[u] = u;
+    if (s == 0) counters[bh * splits] = 0;
+  }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -256,7 +263,7 @@ int noalloc_impl(const void* q, const void* k_pages, const void* v_pages, const 
                         ? device_status
                         : reinterpret_cast<int32_t*>(scratch + kOffStatus);
 
-  fill_units_kernel<<<(units + 255) / 256, 256, 0, stream>>>(
+  fill_units_kernel<<<batch, kFillThreads, 0, stream>>>(
       scratch, indptr, indices, last_page_len, batch, num_kv_heads, group, page_size,
       num_pages_in_pool, int32_t(splits), window_left, status);
   if (cudaGetLastError() != cudaSuccess) return BSR_ERR_CUDA;

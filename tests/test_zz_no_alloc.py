@@ -83,18 +83,63 @@ def test_noalloc_refuses_batches_beyond_its_scratch():
     assert call_noalloc(w, tensors, out, lse, status) == -2     # BSR_ERR_UNSUPPORTED
 
 
-def test_noalloc_reports_pages_outside_the_pool():
+@pytest.mark.parametrize("bad_entry", [0, 2])
+def test_noalloc_reports_pages_outside_the_pool(bad_entry):
+    """A request naming a page outside the pool is dropped as a whole: every chunk of
+    it (the range of 40 keys is cut into several chunks, the bad page sits in the first
+    or the last), so its out rows are 0 and its lse -inf; the other request is
+    unaffected and still matches the planned entry point."""
     w = wl.make_paged("badpage", 34, [40, 20], Hq=8, Hk=2, D=128, P=16)
-    bad = w.indices.clone()
-    bad[0] = w.num_pages + 3
-    w.indices = bad
     tensors = device_tensors(w)
-    out = torch.empty_like(tensors[0])
-    lse = torch.empty(tensors[0].shape[:2], dtype=torch.float32, device=out.device)
+    ref_out, ref_lse, _ = run(w, tensors, out_dtype=torch.float32)
+    bad = w.indices.clone()
+    bad[bad_entry] = w.num_pages + 3          # entries 0..2 belong to request 0
+    w.indices = bad
+    out = torch.full_like(ref_out, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=out.device)
+    for call in range(2):
+        assert call_noalloc(w, tensors, out, lse, status) == 0
+        assert int(status.item()) & 2
+        assert torch.equal(out[0].cpu(), torch.zeros_like(out[0].cpu()))
+        assert torch.isneginf(lse[0]).all()
+        assert_out_close(out[1:].cpu().numpy(), ref_out[1:].cpu().numpy().astype(np.float64),
+                         False, "good request beside a bad one")
+        assert_lse_close(lse[1:].cpu().numpy(), ref_lse[1:].cpu().numpy().astype(np.float64),
+                         "good request beside a bad one")
+
+
+@pytest.mark.parametrize("fault", ["last_page_len", "huge_count"])
+def test_noalloc_malformed_lengths_are_empty(fault):
+    """A last_page_len beyond the page size, or a page count whose key count passes
+    2^31 - 1 (which also leaves the next request with a negative count), makes only
+    the requests concerned empty (status bit 1), and nothing outside the table is read."""
+    w = wl.make_paged("badlen", 39, [40, 20, 33], Hq=8, Hk=2, D=128, P=16)
+    tensors = device_tensors(w)
+    ref_out, ref_lse, _ = run(w, tensors, out_dtype=torch.float32)
+    if fault == "last_page_len":
+        lpl = w.last_page_len.clone()
+        lpl[1] = 17
+        w.last_page_len = lpl
+        empty, good = [1], [0, 2]
+    else:
+        ip = w.indptr.clone()
+        ip[2] = 1 << 28                        # request 1: 2^28 pages of 16 keys
+        w.indptr = ip
+        empty, good = [1, 2], [0]
+    out = torch.full_like(ref_out, float("nan"))
+    lse = torch.full_like(ref_lse, float("nan"))
     status = torch.zeros(1, dtype=torch.int32, device=out.device)
     assert call_noalloc(w, tensors, out, lse, status) == 0
     assert int(status.item()) & 2
-    assert torch.isfinite(out.float()).all()
+    for r in empty:
+        assert torch.equal(out[r].cpu(), torch.zeros_like(out[r].cpu()))
+        assert torch.isneginf(lse[r]).all()
+    for r in good:
+        assert_out_close(out[r].cpu().numpy(), ref_out[r].cpu().numpy().astype(np.float64), False,
+                         f"request {r}")
+        assert_lse_close(lse[r].cpu().numpy(), ref_lse[r].cpu().numpy().astype(np.float64),
+                         f"request {r}")
 
 
 @pytest.mark.parametrize("P", [16, 32])
