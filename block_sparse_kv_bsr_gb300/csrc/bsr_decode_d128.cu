@@ -1,4 +1,5 @@
 // Instantiations of the decode kernel for head_dim 128 and their launcher.
+#include <atomic>
 #include "bsr_decode.cuh"
 #include "bsr_schedule.h"
 
@@ -14,15 +15,15 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
   constexpr size_t smem = ROPE ? DecodeCfg<128>::kSmemBytesRope : DecodeCfg<128>::kSmemBytes;
   // The shared-memory opt-in is per device; set it on the first launch there so
   // that later launches (including ones under stream capture) make no extra call.
-  static bool opted_in[kMaxDevices] = {};
+  static std::atomic<bool> opted_in[kMaxDevices];   // zero-initialized: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!opted_in[dev]) {
+  if (!opted_in[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    opted_in[dev] = true;
+    opted_in[dev].store(true, std::memory_order_release);
   }
   kern<<<grid, kDecodeWarps * 32, smem, stream>>>(tk, tv, p);
   return cudaGetLastError();

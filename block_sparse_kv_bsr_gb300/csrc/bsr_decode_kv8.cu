@@ -30,6 +30,7 @@
 //    kernel's instructions per byte, so per-step latency matters here).
 // Every barrier wait is bounded; on timeout the warp sets bit 0 of the status
 // word, drains its own copies (bounded) and exits.
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -508,15 +509,15 @@ template <bool R16, bool WIN>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                        int grid, cudaStream_t stream) {
   auto kern = bsr_decode_kv8_kernel<R16, WIN>;
-  static bool opted_in[kMaxDevices] = {};
+  static std::atomic<bool> opted_in[kMaxDevices];   // zero-initialized: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!opted_in[dev]) {
+  if (!opted_in[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem8));
     if (e != cudaSuccess) return e;
-    opted_in[dev] = true;
+    opted_in[dev].store(true, std::memory_order_release);
   }
   kern<<<grid, kDecodeWarps * 32, kSmem8, stream>>>(tk, tv, p);
   return cudaGetLastError();
