@@ -21,7 +21,7 @@ __all__ = [
     "bsr_last_device_error", "bsr_status_string", "bsr_attn_decode_noalloc", "Schedule",
     "bsr_attn_decode_noalloc_kv8", "bsr_attn_decode_noalloc_ex",
     "bsr_schedule_set_stage_timing", "bsr_schedule_stage_times", "STAGES", "EXPORTED_SYMBOLS",
-    "bsr_selftest_bounded_wait",
+    "bsr_selftest_bounded_wait", "bsr_schedule_create",
 ]
 
 BSR_OK = 0
@@ -34,7 +34,7 @@ EXPORTED_SYMBOLS = (
     "bsr_status_string", "bsr_attn_decode_noalloc", "bsr_attn_decode_noalloc_kv8",
     "bsr_attn_decode_noalloc_ex",
     "bsr_schedule_set_stage_timing",
-    "bsr_schedule_stage_times", "bsr_selftest_bounded_wait",
+    "bsr_schedule_stage_times", "bsr_selftest_bounded_wait", "bsr_schedule_create",
 )
 
 _i32p = ctypes.POINTER(ctypes.c_int32)
@@ -103,6 +103,8 @@ def load(path: str | None = None):
                                   ctypes.c_int32, _vp, _vp, _vp, _vp]
     lib.bsr_schedule_destroy.restype = None
     lib.bsr_schedule_destroy.argtypes = [_vp]
+    lib.bsr_schedule_create.restype = ctypes.c_int
+    lib.bsr_schedule_create.argtypes = [ctypes.c_int32, ctypes.POINTER(_vp)]
     lib.bsr_schedule_get_info.restype = ctypes.c_int
     lib.bsr_schedule_get_info.argtypes = [_vp, ctypes.POINTER(_Info)]
     lib.bsr_last_device_error.restype = ctypes.c_int
@@ -221,6 +223,14 @@ class Schedule:
             self.close()
         except Exception:
             pass
+
+
+def bsr_schedule_create(sm_budget: int = 0) -> Schedule:
+    """An empty schedule whose plans use at most `sm_budget` SMs (0: all); plan into it
+    with bsr_attn_plan(..., schedule=...)."""
+    handle = _vp(None)
+    _check(load().bsr_schedule_create(int(sm_budget), ctypes.byref(handle)), "bsr_schedule_create")
+    return Schedule(handle.value)
 
 
 def _plan_args(indptr, indices, last_page_len, qo_indptr):
@@ -385,7 +395,7 @@ def bsr_selftest_bounded_wait(device_status, limit_ns: int, stream=None):
            "bsr_selftest_bounded_wait")
 
 
-STAGES = ("decode", "rope_prepass", "prefill", "merge")
+STAGES = ("decode", "prefill", "merge")
 
 
 def bsr_schedule_set_stage_timing(schedule: Schedule, max_calls: int):
@@ -396,7 +406,7 @@ def bsr_schedule_set_stage_timing(schedule: Schedule, max_calls: int):
 
 def bsr_schedule_stage_times(schedule: Schedule, call: int) -> dict:
     """Stage durations (ms) of kept run `call` (0 = oldest kept); absent stages omitted."""
-    ms = (ctypes.c_float * 4)()
+    ms = (ctypes.c_float * len(STAGES))()
     code = load().bsr_schedule_stage_times(_vp(schedule.handle), int(call), ms)
     if code < 0:
         raise BsrError(code, "bsr_schedule_stage_times")

@@ -677,7 +677,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     if constexpr (ROPE) {
       // a rotated q or k beyond the fp16 operand range shows as a non-finite row sum
       const bool bad = (vA && !isfinite(lA)) || (vB && !isfinite(lB));
-      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.error, kStatusRopeRange);
+      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(p.error, kStatusOperandRange);
     }
     const float lseA = lA > 0.f ? mA + ptx::lg2(lA) : -INFINITY;
     const float lseB = lB > 0.f ? mB + ptx::lg2(lB) : -INFINITY;

@@ -82,13 +82,16 @@ struct DecodeParams {
 // tile is whole queries and is one TMA box of q.
 constexpr int kPrefillRows = 256;
 constexpr int kPrefillKeyTile = 128;
-// Tensor-core operands of the RoPE prefill path are fp16 scaled by 2^-4 (an
-// exact power of two), so rotated values up to 2^20 in magnitude fit.
+// Rotated (RoPE) q and k enter the products as fp16 scaled by 2^-4 (an exact
+// power of two), so rotated values up to 2^20 in magnitude fit.
 constexpr float kRopeOperandScale = 0.0625f;
 constexpr float kRopeOperandMax = 65504.f;
-// Device status bits (the status word of a schedule).
+// Device status bits (the status word of a schedule).  Bit 1: an fp16 operand of
+// the products was out of range -- a rotated q or k of magnitude 2^20 or more, or
+// on the tensor-core prefill path a V value beyond 65504 -- so the scores or
+// outputs involving it are not finite.
 constexpr int32_t kStatusWaitTimeout = 1;
-constexpr int32_t kStatusRopeRange = 2;
+constexpr int32_t kStatusOperandRange = 2;
 
 struct PrefillParams {
   const DecodeItem* items;
@@ -96,8 +99,10 @@ struct PrefillParams {
   float* part_o;                  // [num_partials, kPrefillRows, D] fp32
   float* part_lse;                // [num_partials, kPrefillRows] (log2 domain)
   const int32_t* indices;
-  const int32_t* rk_off;          // RoPE: first row of each request in the rotated-K buffer
-  int32_t rk_total;               // RoPE: rows per kv head in the rotated-K buffer
+  const float4* rope;             // RoPE: [rope rows, D / 4] (cos f, cos f+1, sin f, sin f+1), f even; or null
+  const int32_t* page_pos;        // RoPE: logical position of each page entry's first key, or null
+  const int32_t* qshift;          // RoPE with page_pos: logical minus cached end per request
+  int32_t rope_max_pos;           // last row of the cos/sin table
   void* out;
   float* lse;
   int32_t* error;
@@ -119,29 +124,6 @@ struct PrefillMergeParams {
   void* out;
   float* lse;
   int32_t n_units, Hq, group, out_f32;
-};
-
-// RoPE pre-pass of the prefill requests: their keys are rotated once per run
-// into a dense buffer [Hk][rk_total][D] (request rows at rk_start[i] ..
-// rk_start[i + 1]), their queries into a copy of q ([sum_qo][Hq][D], rows
-// rq_row0[i] .., first position rq_pos0[i]).  Both are fp16 scaled by
-// kRopeOperandScale.
-struct RopePrepassParams {
-  const uint16_t* k_pages;
-  const uint16_t* q;
-  const int32_t* indices;
-  const int32_t* rk_req_pbase;    // [n] indptr[b] of each prefill request
-  const int32_t* rk_start;        // [n + 1]
-  const int32_t* rq_row0;         // [n]
-  const int32_t* rq_start;        // [n + 1]
-  const int32_t* rq_pos0;         // [n] (logical positions)
-  const int32_t* page_pos;        // logical position of each page entry's first key, or null
-  const float2* rope_nat;         // [rope rows, D / 2] (cos, sin) by frequency
-  uint16_t* rotk;
-  uint16_t* rotq;
-  int32_t* error;                 // status word (kStatusRopeRange on overflow)
-  int32_t n, rk_total, rq_total, Hk, Hq, P, rope_max_pos;
-  int32_t nhd;                    // page pools token-major (else head-major)
 };
 
 }  // namespace bsr

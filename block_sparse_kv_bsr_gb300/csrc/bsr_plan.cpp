@@ -60,9 +60,11 @@ struct Unit {
 // cos/sin of every (position, frequency), angles in fp64 rounded once to fp32, in two
 // orders.  frag: the order the decode kernel's fragments consume them, per position
 // D/4 groups of two (cos, sin) pairs, group i * 4 + t (quad t < 4, i < D/16) holding
-// frequencies 16 * (i / 2) + 8 * (i % 2) + 2t + {0, 1}.  nat: frequency order,
-// [pos][f] (RoPE pre-pass of the prefill kernel).
-void build_rope_tables(float* frag, float* nat, int32_t rows, int32_t D, double theta) {
+// frequencies 16 * (i / 2) + 8 * (i % 2) + 2t + {0, 1}.  pairs: frequency order by
+// pairs, per position D/4 float4 (cos f, cos f+1, sin f, sin f+1) for f = 0, 2, ...
+// (the tensor-core prefill kernel, which rotates its tiles in shared memory two
+// frequencies per packed instruction).
+void build_rope_tables(float* frag, float* pairs, int32_t rows, int32_t D, double theta) {
   std::vector<double> omega(D / 2);
   for (int f = 0; f < D / 2; ++f) omega[f] = std::pow(theta, -2.0 * double(f) / double(D));
   for (int32_t pos = 0; pos < rows; ++pos)
@@ -71,9 +73,9 @@ void build_rope_tables(float* frag, float* nat, int32_t rows, int32_t D, double 
       const float c = float(std::cos(a)), sn = float(std::sin(a));
       const int i = 2 * (f / 16) + (f % 16) / 8, t = (f % 8) / 2, e = f % 2;
       float* fr = frag + ((size_t(pos) * (D / 4) + i * 4 + t) * 2 + e) * 2;
-      float* na = nat + (size_t(pos) * (D / 2) + f) * 2;
-      fr[0] = na[0] = c;
-      fr[1] = na[1] = sn;
+      float* pr = pairs + (size_t(pos) * (D / 4) + f / 2) * 4 + e;
+      fr[0] = pr[0] = c;
+      fr[1] = pr[2] = sn;
     }
 }
 
@@ -216,7 +218,11 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
     };
     auto count = [&](size_t oi, int64_t, int64_t, int64_t) { ++pieces_of_unit[order[oi]]; };
     int64_t k = -1;
-    bool counted = false;   // pieces_of_unit holds the cut at lo + k
+    // pieces_of_unit is valid only while `counted` is true: the hinted cut below fills it
+    // as a side effect, and every path that leaves `counted` false (the hint does not fit,
+    // is not the smallest, or the cut stops early) is followed by a reset and a fresh
+    // counting cut at the final budget.  Never set `counted` on any other path.
+    bool counted = false;
     if (k_hint != nullptr && *k_hint >= 0 && cut_ranges(in, lo + *k_hint, count) <= workers &&
         (*k_hint == 0 || !fits(*k_hint - 1))) {
       k = *k_hint;
@@ -426,12 +432,6 @@ struct HostPlan {
   WorkList dec;   // split-KV decode kernel, workers = warps
   WorkList pre;   // tensor-core prefill kernel, workers = CTAs
   std::vector<DecodeItem> pmerge;   // one entry per prefill unit whose key range was split
-  // requests on the prefill kernel (for the RoPE pre-pass): their keys go to a
-  // dense rotated-K buffer at rk_off / rk_start, their queries are rotated in place
-  // of a copy of q (rows rq_row0 .. + (rq_start[i + 1] - rq_start[i]), first
-  // position rq_pos0)
-  std::vector<int32_t> rk_off, rk_pbase, rk_start, rq_row0, rq_start, rq_pos0;
-  int32_t rk_total = 0, rq_total = 0;
   // per-page positions: logical minus cached end of each request, and one past the
   // largest position a stage may touch (sizes the cos/sin table)
   std::vector<int32_t> qshift;
@@ -569,24 +569,6 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
         }
       }
   }
-  hp->rk_off.assign(batch, -1);
-  hp->rk_pbase.clear();
-  hp->rk_start.assign(1, 0);
-  hp->rq_row0.clear();
-  hp->rq_pos0.clear();
-  hp->rq_start.assign(1, 0);
-  for (const Unit& u : punits) {
-    if (hp->rk_off[u.req] >= 0 || kv_len[u.req] == 0) continue;
-    hp->rk_off[u.req] = hp->rk_start.back();
-    hp->rk_pbase.push_back(indptr[u.req]);
-    hp->rk_start.push_back(hp->rk_start.back() + kv_len[u.req]);
-    hp->rq_row0.push_back(q_row0[u.req]);
-    hp->rq_pos0.push_back(kv_len[u.req] - qo_len[u.req] +
-                          (page_pos != nullptr ? hp->qshift[u.req] : 0));
-    hp->rq_start.push_back(hp->rq_start.back() + qo_len[u.req]);
-  }
-  hp->rk_total = hp->rk_start.back();
-  hp->rq_total = hp->rq_start.back();
   // consecutive plans of a serving loop are alike: start from the last budget step
   thread_local int64_t dec_k = -1;
   balance(dunits, int64_t(num_sms) * kDecodeWarps, std::max<int64_t>(page_size, kStageTokens),
@@ -622,6 +604,8 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   if (ce != cudaSuccess) return fail_cuda(ce);
   ce = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device);
   if (ce != cudaSuccess) return fail_cuda(ce);
+  if (*schedule != nullptr && (*schedule)->sm_budget > 0)
+    num_sms = std::min(num_sms, int((*schedule)->sm_budget));
   thread_local HostPlan hp;   // reused: its vectors keep their memory between plans
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
@@ -697,13 +681,6 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const size_t off_pitems = take(hp.pre.items.size() * sizeof(DecodeItem));
   const size_t off_cta_ptr = take(hp.pre.ptr.size() * 4);
   const size_t off_pmerge = take(hp.pmerge.size() * sizeof(DecodeItem));
-  const bool rotk = rope && !hp.pre.items.empty() && hp.rk_total > 0;
-  const size_t off_rk_off = take(rotk ? size_t(batch) * 4 : 0);
-  const size_t off_rk_pbase = take(rotk ? hp.rk_pbase.size() * 4 : 0);
-  const size_t off_rk_start = take(rotk ? hp.rk_start.size() * 4 : 0);
-  const size_t off_rq_row0 = take(rotk ? hp.rq_row0.size() * 4 : 0);
-  const size_t off_rq_start = take(rotk ? hp.rq_start.size() * 4 : 0);
-  const size_t off_rq_pos0 = take(rotk ? hp.rq_pos0.size() * 4 : 0);
   const bool with_pos = page_pos != nullptr && rope;   // positions matter only for RoPE
   const size_t off_page_pos = take(with_pos ? size_t(std::max<int64_t>(nnz, 1)) * 4 : 0);
   const size_t off_qshift = take(with_pos ? size_t(std::max(batch, 1)) * 4 : 0);
@@ -713,8 +690,6 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const size_t off_part_lse = take(size_t(hp.dec.n_partials) * kMaxDecodeRows * 4);
   const size_t off_ppart_o = take(size_t(hp.pre.n_partials) * bsr::kPrefillRows * head_dim * 4);
   const size_t off_ppart_lse = take(size_t(hp.pre.n_partials) * bsr::kPrefillRows * 4);
-  const size_t off_rotk = take(rotk ? size_t(num_kv_heads) * hp.rk_total * head_dim * 2 : 0);
-  const size_t off_rotq = take(rotk ? size_t(hp.sum_qo) * num_qo_heads * head_dim * 2 : 0);
   const size_t ws_bytes = off;
 
   // ---------------------------------------------------------------- staging + upload
@@ -763,14 +738,6 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   std::memcpy(h + off_cta_ptr, hp.pre.ptr.data(), hp.pre.ptr.size() * 4);
   if (!hp.pmerge.empty())
     std::memcpy(h + off_pmerge, hp.pmerge.data(), hp.pmerge.size() * sizeof(DecodeItem));
-  if (rotk) {
-    std::memcpy(h + off_rk_off, hp.rk_off.data(), size_t(batch) * 4);
-    std::memcpy(h + off_rk_pbase, hp.rk_pbase.data(), hp.rk_pbase.size() * 4);
-    std::memcpy(h + off_rk_start, hp.rk_start.data(), hp.rk_start.size() * 4);
-    std::memcpy(h + off_rq_row0, hp.rq_row0.data(), hp.rq_row0.size() * 4);
-    std::memcpy(h + off_rq_start, hp.rq_start.data(), hp.rq_start.size() * 4);
-    std::memcpy(h + off_rq_pos0, hp.rq_pos0.data(), hp.rq_pos0.size() * 4);
-  }
   ce = cudaMemcpyAsync(s->d_ws, h, image_bytes, cudaMemcpyHostToDevice, stream);
   if (ce != cudaSuccess) return bail(fail_cuda(ce));
   ce = cudaEventRecord(s->upload_done, stream);
@@ -815,20 +782,8 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->n_pmerge = int32_t(hp.pmerge.size());
   s->off_ppart_o = off_ppart_o;
   s->off_ppart_lse = off_ppart_lse;
-  s->off_rk_off = off_rk_off;
-  s->off_rk_pbase = off_rk_pbase;
-  s->off_rk_start = off_rk_start;
-  s->off_rotk = off_rotk;
-  s->off_rq_row0 = off_rq_row0;
-  s->off_rq_start = off_rq_start;
-  s->off_rq_pos0 = off_rq_pos0;
-  s->off_rotq = off_rotq;
-  s->rq_total = rotk ? hp.rq_total : 0;
   s->tm_q_ptr = nullptr;    // Q tensor map: encoded by run
   s->tm_pk_ptr = s->tm_pv_ptr = nullptr;   // prefill K/V maps depend on the page size
-  s->rk_n = rotk ? int32_t(hp.rk_pbase.size()) : 0;
-  s->rk_total = rotk ? hp.rk_total : 0;
-  s->tm_rk_valid = false;   // encoded by run (the buffer's address may have moved)
   s->ws_used = ws_bytes;
   s->upload_bytes = image_bytes;
   s->off_indices = off_indices;
@@ -841,6 +796,19 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->has_page_pos = with_pos;
   s->off_part_o = off_part_o;
   s->off_part_lse = off_part_lse;
+  *schedule = s;
+  return BSR_OK;
+}
+
+extern "C" int bsr_schedule_create(int32_t sm_budget, bsr_schedule_t* schedule) {
+  if (schedule == nullptr || sm_budget < 0) return BSR_ERR_INVALID_ARGUMENT;
+  int device = 0;
+  const cudaError_t ce = cudaGetDevice(&device);
+  if (ce != cudaSuccess) return fail_cuda(ce);
+  bsr_schedule* s = new (std::nothrow) bsr_schedule();
+  if (s == nullptr) return BSR_ERR_OUT_OF_MEMORY;
+  s->device = device;
+  s->sm_budget = sm_budget;
   *schedule = s;
   return BSR_OK;
 }
@@ -888,7 +856,7 @@ extern "C" int bsr_schedule_get_info(bsr_schedule_t s, bsr_schedule_info_t* info
   info->decode_imbalance = s->dec_imbalance;
   info->prefill_imbalance = s->pre_imbalance;
   info->kernels_per_run = (s->n_items > 0 ? 1 : 0) + (s->n_pitems > 0 ? 1 : 0) +
-                          (s->n_pitems > 0 && s->rk_total > 0 ? 1 : 0) + (s->n_pmerge > 0 ? 1 : 0);
+                          (s->n_pmerge > 0 ? 1 : 0);
   return BSR_OK;
 }
 
@@ -930,7 +898,6 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
     info->decode_imbalance = hp.dec.imbalance;
     info->prefill_imbalance = hp.pre.imbalance;
     info->kernels_per_run = (hp.dec.items.empty() ? 0 : 1) + (hp.pre.items.empty() ? 0 : 1) +
-                            (!hp.pre.items.empty() && rope_theta > 0.f && hp.rk_total > 0 ? 1 : 0) +
                             (hp.pmerge.empty() ? 0 : 1);
   }
   const int64_t n = int64_t(hp.dec.items.size() + hp.pre.items.size());

@@ -10,35 +10,47 @@
 // tile is staged once for 256 rows, and while the softmax of one query tile
 // runs, the tensor cores work on the other's products.
 //
-// Roles (576 threads):
+// Roles (576 threads; 704 with RoPE):
 //   warps 0-15 softmax, two threads per row: warp w works on query tile w / 8,
 //              key/column half (w / 4) % 2 and row quarter w % 4 (the TMEM lanes
 //              it may access).  Each half reads its 64 scores of a row from TMEM,
 //              the halves swap their partial max (and at the end their partial
 //              sum) through shared memory and an mbarrier, then each writes its
-//              half of P (bf16) over S columns it has already read, rescales its
+//              half of P (fp16) over S columns it has already read, rescales its
 //              64 O columns in TMEM when the running max grows by more than 2^8,
 //              and writes out / lse (or the fp32 partial state of a split key
-//              range, combined afterwards by bsr_prefill_merge_kernel).
+//              range, combined afterwards by bsr_prefill_merge_kernel).  Between
+//              handing over P of key tile j and waiting for the scores of tile
+//              j + 1 -- time they would otherwise spend idle -- they turn V of tile
+//              j + 1 into fp16 in place: P enters P V as fp16 (11 significant bits),
+//              because rows that see only a few keys, such as the first rows of a
+//              causal prompt, cannot average out the rounding of a bf16 P.  Rows past
+//              the last key of a ragged tile are zeroed there (they may hold another
+//              page's tail, NaN included, and P = 0 must contribute exactly 0).
 //   warp 16    TMA producer, the whole warp: each unit's query tiles (one box per
-//              64 columns: whole queries of the kv head's group, straight from q,
-//              or with RoPE from the copy the pre-pass rotated) as soon as the
-//              previous unit's last Q K^T has read them, and a FIFO ring of 32 KB
-//              stages with the K and V tiles of every key tile in turn (K(j),
-//              V(j), K(j+1), ...), gathered box by box from `indices` (inactive
-//              blocks are absent, "Block-Sparse 포맷"), 128B-swizzled; lane b
-//              fetches box b's page id one key tile ahead.  With RoPE, K comes
-//              already rotated from a dense buffer the pre-pass fills once per run.
+//              64 columns: whole queries of the kv head's group, straight from q)
+//              as soon as the previous unit's last Q K^T has read them, and a FIFO
+//              ring of 32 KB stages with the K and V tiles of every key tile in
+//              turn (K(j), V(j), K(j+1), ...), gathered box by box from `indices`
+//              (inactive blocks are absent, "Block-Sparse 포맷"), 128B-swizzled;
+//              lane b fetches box b's page id one key tile ahead.
 //   warp 17    allocates TMEM and issues the MMAs: S_i = Q_i K^T (M 128, N 128,
 //              K-major operands from shared memory) and O_i += P_i V (P from
 //              TMEM, V MN-major from shared memory), i = 0, 1.
-// TMEM columns: S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_i (bf16 pairs)
+//   warps 18-21 (RoPE) rotate every query tile and every K tile in shared memory
+//              once its copy has landed and before the MMA reads it -- RoPE fused
+//              into the attention kernel, so rotated keys never go back to global
+//              memory ("JIT 컴파일은 어텐션을 어떻게 빠르게 만드는가?") -- and write
+//              them in place as fp16 scaled by 2^-4, the operand type of the RoPE
+//              Q K^T.
+// TMEM columns: S_0 | S_1 | O_0 | O_1, 128 fp32 columns each; P_i (fp16 pairs)
 // overwrites columns 0-31 and 64-95 of S_i.  MMAs run in issue order, so the
 // Q K^T of the next key tile may be queued right behind the P V that reads P_i.
 // Every mbarrier wait is bounded and warp-agreed.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 
@@ -59,34 +71,43 @@ constexpr int kTileBytes = 2 * kHalfBytes;
 constexpr int kStages = 4;                  // K/V ring depth (32 KB stages)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSoftmaxWarps = 16;           // two per row quarter and query tile
-constexpr int kThreads = 32 * (kSoftmaxWarps + 2);
 constexpr int kProducerWarp = kSoftmaxWarps, kMmaWarp = kSoftmaxWarps + 1;
+// RoPE warps (the RoPE variant only) rotate the query and K tiles.
+constexpr int kRotWarp0 = kSoftmaxWarps + 2, kRotWarps = 4;
+constexpr int kRotThreads = 32 * kRotWarps;
+template <bool ROPE>
+constexpr int threads_of() { return 32 * (kSoftmaxWarps + 2 + (ROPE ? kRotWarps : 0)); }
 static_assert(kUnitRows == 2 * kTileM, "a unit is two query tiles");
+// A rotating thread takes one 16-byte chunk (8 frequencies) of 8 consecutive rows of a
+// tile: 16 row blocks x 8 chunks = 128 threads, a row block inside one 16-key group.
+static_assert(kRotThreads == (kTileN / 8) * 8 && kTileM == kTileN, "RoPE thread map");
+constexpr int kVChunks = kTileBytes / 16;    // 16-byte chunks of a V stage
+// Largest magnitude of an fp16 tensor-core operand.
+constexpr float kF16Max = 65504.f;
 
 struct Smem {
   static constexpr int kQ = 0;                               // Q_0, Q_1
   static constexpr int kRing = 2 * kTileBytes;
   // row-half exchange: [parity][query tile][half][row] fp32
   static constexpr int kXchData = kRing + kStages * kTileBytes;
-  static constexpr int kBars = kXchData + 2 * 2 * 2 * kTileM * 4;
+  // RoPE: cos / sin of t * omega_f for t < 16, times the operand scale, as
+  // [t][frequency pair within the chunk][chunk] float4 (cos_f, sin_f, cos_f+1, sin_f+1)
+  static constexpr int kRopeT = kXchData + 2 * 2 * 2 * kTileM * 4;
+  static constexpr int kBars = kRopeT + 16 * (D / 2) * 8;
   // full[kStages], empty[kStages], s_full[2], p_full[2], o_full[2], q_full[2], q_empty[2],
-  // drain, xch[2][4] (query tile, row quarter)
+  // drain, xch[2][4] (query tile, row quarter), ready[kStages] (the operand warps are
+  // done with a stage: every V stage, and with RoPE every K stage), q_rot[2] (RoPE)
   static constexpr int kFull = 0, kEmpty = kStages, kSFull = 2 * kStages, kPFull = kSFull + 2,
                        kOFull = kPFull + 2, kQFull = kOFull + 2, kQEmpty = kQFull + 2,
-                       kDrain = kQEmpty + 2, kXch = kDrain + 1;
-  static constexpr int kNumBars = kXch + 8;
+                       kDrain = kQEmpty + 2, kXch = kDrain + 1, kReady = kXch + 8,
+                       kQRot = kReady + kStages;
+  static constexpr int kNumBars = kQRot + 2;
   static constexpr int kTmemSlot = kBars + 8 * kNumBars;
   static constexpr int kFlags = kTmemSlot + 16;   // abort flag
   static constexpr int kTotal = kFlags + 16;
   static constexpr size_t kDynBytes = size_t(kTotal) + 1024;
   static_assert(kDynBytes <= 232448, "prefill tiles exceed the shared memory of one SM");
 };
-
-// Offset of (row r, 16-byte chunk c of 16) in a V tile stored by row groups:
-// [row / 8][column block][row % 8][128 B], 128B-swizzled.
-__device__ __forceinline__ uint32_t vg_off(int r, int c) {
-  return uint32_t((r >> 3) * 2048 + (c >> 3) * 1024 + (r & 7) * 128 + (((c & 7) ^ (r & 7)) << 4));
-}
 
 struct Waiter {
   uint32_t abort_flag;  // smem address of the shared abort word
@@ -166,8 +187,62 @@ __device__ __forceinline__ void store_row_chunk(const PrefillParams& p, size_t o
   }
 }
 
+// (cos, sin) of the frequency pairs (8 ch + 2 e, 8 ch + 2 e + 1), e < 4, of one chunk.
+struct Angles {
+  float2 c[4], s[4];
+};
+
+// Angles of chunk ch at table row `pos` (four float4 of the pair-order table).
+__device__ __forceinline__ Angles load_angles(const float4* rope, int pos, int ch) {
+  const float4* row = rope + size_t(pos) * (D / 4) + 4 * ch;
+  Angles an;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float4 v = __ldg(row + e);
+    an.c[e] = make_float2(v.x, v.y);
+    an.s[e] = make_float2(v.z, v.w);
+  }
+  return an;
+}
+
+// Rotate dimensions 8 ch .. 8 ch + 7 of row r of a [2 column blocks][128 rows][128 B]
+// 128B-swizzled bf16 tile together with their rotate-half partners 64 further (the same
+// bytes of the other column block), two frequencies per packed instruction, and write
+// both back in place as fp16.  The angles are already times the operand scale.
+// Returns the largest magnitude written.
+__device__ __forceinline__ float rotate_row_chunk(uint32_t tile, int r, int ch, const Angles& an) {
+  const uint32_t lo = tile + uint32_t(r) * 128u + (uint32_t(ch ^ (r & 7)) << 4);
+  const uint32_t hi = lo + kHalfBytes;
+  uint32_t a[4], b[4];
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(lo));
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]) : "r"(hi));
+  float m = 0.f;
+  uint32_t xo[4], yo[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float2 x = make_float2(ptx::bf16_lo(a[e]), ptx::bf16_hi(a[e]));
+    const float2 y = make_float2(ptx::bf16_lo(b[e]), ptx::bf16_hi(b[e]));
+    const float2 u = ptx::fsub2(ptx::fmul2(x, an.c[e]), ptx::fmul2(y, an.s[e]));
+    const float2 v = ptx::ffma2(y, an.c[e], ptx::fmul2(x, an.s[e]));
+    m = ptx::fmax3(m, fabsf(u.x), fabsf(u.y));
+    m = ptx::fmax3(m, fabsf(v.x), fabsf(v.y));
+    xo[e] = ptx::pack_f16(u.x, u.y);
+    yo[e] = ptx::pack_f16(v.x, v.y);
+  }
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+               ::"r"(lo), "r"(xo[0]), "r"(xo[1]), "r"(xo[2]), "r"(xo[3]) : "memory");
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+               ::"r"(hi), "r"(yo[0]), "r"(yo[1]), "r"(yo[2]), "r"(yo[3]) : "memory");
+  return m;
+}
+
+// One CTA per SM.  Each of the 4 SM sub-partitions holds a quarter of the register
+// file (16K registers) and up to 6 of the 22 warps of the RoPE variant, so 80
+// registers per thread is its ceiling (96 for the 18 warps without RoPE).
 template <bool ROPE, bool WIN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96)
     bsr_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -200,6 +275,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     ptx::mbar_init(BAR(L::kDrain), 1);
     for (int i = 0; i < 8; ++i) ptx::mbar_init(BAR(L::kXch + i), 2);   // the two halves of a row quarter
+    // ready: K stages sit at even ring positions (one arrival per RoPE warp), V stages
+    // at odd ones (arrivals of the softmax warps: 16 in all per use)
+    for (int i = 0; i < kStages; ++i)
+      ptx::mbar_init(BAR(L::kReady + i), (i & 1) ? kSoftmaxWarps : kRotWarps);
+    for (int i = 0; i < 2; ++i) ptx::mbar_init(BAR(L::kQRot + i), kRotWarps);
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(abort_addr), "r"(0u));
     ptx::fence_barrier_init();
   }
@@ -291,7 +371,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = u_begin; u < u_end && ok; ++u) {
       const DecodeItem it = p.items[u];
       const int nt = ntiles_of(it);
-      const int koff = ROPE ? __ldg(p.rk_off + it.req) : 0;
       int nsub_next = nt > 0 ? boxes_of(it, 0) : 0;
       int page_next = nt > 0 ? page_of(it, 0, nsub_next) : 0;
       for (int j = 0; j < nt; ++j) {
@@ -302,16 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // K(j)
         if (c >= kStages && !ring_wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
-        if (ROPE) {
-          // rotated keys are dense per (kv head, request): one box per 64-column block
-          if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(FULL(c), uint32_t(kTileBytes));
-            const int row = it.kvh * p.rk_total + koff + it.tok0 + kTileN * j;
-            ptx::tma_load_3d(STAGE(c), &tm_k, FULL(c), 0, row, 0, pol);   // both column blocks
-          }
-        } else {
-          issue_paged(false, c, it, j, nsub, page);
-        }
+        issue_paged(false, c, it, j, nsub, page);
         ++c;
         if (j == 0) {
           if (!load_q(0, nq0, it) || (it.nrows > kTileM && !load_q(1, nq1, it))) { ok = false; break; }
@@ -334,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = ROPE ? umma::idesc_f16_f32(kTileM, kTileN, 0, 0)
                                          : umma::idesc_bf16_f32(kTileM, kTileN, 0, 0);
-      constexpr uint32_t idesc_pv = umma::idesc_bf16_f32(kTileM, D, 0, 1);
+      constexpr uint32_t idesc_pv = umma::idesc_f16_f32(kTileM, D, 0, 1);
       uint32_t c = 0;
       uint32_t nq[2] = {0, 0}, np[2] = {0, 0};
       bool ok = true;
@@ -372,14 +442,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++np[i];
         return r;
       };
+      // V stages (and with RoPE the query tiles and K stages) are read once the operand
+      // warps are done with them; their barriers complete once per use, like full / q_full
+      const int q_ready = ROPE ? L::kQRot : L::kQFull;
+      auto ready = [&](uint32_t c) { return BAR(L::kReady + int(c % kStages)); };
+      auto k_ready = [&](uint32_t c) { return ROPE ? ready(c) : FULL(c); };
       for (int u = u_begin; u < u_end && ok; ++u) {
         const DecodeItem it = p.items[u];
         const int nt = ntiles_of(it);
         if (nt == 0) continue;
         const bool two = it.nrows > kTileM;
-        if (!wt.wait(BAR(L::kQFull), nq[0]++ & 1u)) break;
-        if (two && !wt.wait(BAR(L::kQFull + 1), nq[1]++ & 1u)) break;
-        if (!wt.wait(FULL(c), PHASE(c))) break;
+        if (!wt.wait(BAR(q_ready), nq[0]++ & 1u)) break;
+        if (two && !wt.wait(BAR(q_ready + 1), nq[1]++ & 1u)) break;
+        if (!wt.wait(k_ready(c), PHASE(c))) break;
         umma::fence_after_sync();
         qk(0, c);
         if (two) qk(1, c);
@@ -394,24 +469,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nkeys = min(kTileN, it.tok1 - it.tok0 - kTileN * j);
           const int nk16 = (nkeys + 15) >> 4;
           const uint32_t vc = c, kc = c + 1;
-          if (!wt.wait(FULL(vc), PHASE(vc))) { ok = false; break; }
-          if (nkeys & 15) {
-            // V rows past the last key of the final 16-key group may hold another
-            // page's tail: zero them so that P = 0 contributes exactly 0
-            const uint32_t vs = STAGE(vc);
-            for (int r = nkeys; r < 16 * nk16; ++r)
-#pragma unroll
-              for (int c16 = 0; c16 < 16; ++c16)
-                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vs + vg_off(r, c16)), "r"(0u)
-                             : "memory");
-            ptx::fence_proxy_async_smem();
-          }
+          if (!wt.wait(ready(vc), PHASE(vc))) { ok = false; break; }
           if (!wait_p(0)) { ok = false; break; }
           umma::fence_after_sync();
           pv(0, vc, nk16, j > 0);
           if (last) umma::commit(BAR(L::kOFull));
           if (!last) {
-            if (!wt.wait(FULL(kc), PHASE(kc))) { ok = false; break; }
+            if (!wt.wait(k_ready(kc), PHASE(kc))) { ok = false; break; }
             umma::fence_after_sync();
             qk(0, kc);
             if (j + 2 == nt) umma::commit(BAR(L::kQEmpty));
@@ -437,6 +501,112 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma::commit(BAR(L::kDrain));
       ptx::mbar_wait_bounded(BAR(L::kDrain), 0, 50000000ull);
     }
+  } else if (ROPE && warp >= kRotWarp0) {
+    // ------------------------------------------------------------ RoPE warps
+    // Thread rt rotates chunk ch (frequencies 8 ch .. 8 ch + 7 and their partners 64
+    // further) of rows 8 blk .. 8 blk + 7 of each query and K tile.  A row's angles come
+    // from two table rows by angle addition: a base position (a key row: the first key
+    // of its 16-key group, from `indices` order or the page's logical position; a query
+    // row: the position of the thread's first row) and an offset below 16, whose (cos,
+    // sin) sit in shared memory.  Base rows are fetched a tile ahead.  A quarter warp
+    // covers one row's eight chunks, so its shared-memory accesses hit distinct banks.
+    const int rt = tid - 32 * kRotWarp0;
+    const int ch = rt & 7, blk = rt >> 3;
+    const uint32_t ttab = base + L::kRopeT;
+    for (int i = rt; i < 16 * (D / 4); i += kRotThreads) {
+      const int t = i / (D / 4), fp = i % (D / 4);   // offset, frequency pair
+      const float4 v = __ldg(p.rope + size_t(t) * (D / 4) + fp);
+      const uint32_t dst = ttab + uint32_t(((t * 4 + (fp & 3)) * 8 + (fp >> 2)) * 16);
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
+                   "f"(v.x * kRopeOperandScale), "f"(v.y * kRopeOperandScale),
+                   "f"(v.z * kRopeOperandScale), "f"(v.w * kRopeOperandScale) : "memory");
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kRotThreads) : "memory");
+    const int lp = 31 - __clz(p.P);
+    const int g = blk >> 1;                  // 16-key group of this thread's key rows
+    const int t0 = (blk & 1) * 8;            // offset of its first row within the group
+    uint32_t c = 0, nq[2] = {0, 0};
+    float mag = 0.f;                         // largest rotated magnitude of a valid row
+    bool ok = true;
+    // base angles of this thread's key rows in tile j (nothing to rotate past the end)
+    auto key_base = [&](const DecodeItem& it, int j) {
+      Angles b{};
+      const int nkeys = min(kTileN, it.tok1 - it.tok0 - kTileN * j);
+      if (j < ntiles_of(it) && 16 * g < nkeys) {
+        const int kg = it.tok0 + kTileN * j + 16 * g;
+        const int bpos = p.page_pos != nullptr
+                             ? __ldg(p.page_pos + it.page_base + (kg >> lp)) + (kg & (p.P - 1))
+                             : kg;
+        b = load_angles(p.rope, min(bpos, p.rope_max_pos), ch);
+      }
+      return b;
+    };
+    // rows 8 blk + t of a tile at `tile`: compose base (+) offset off(t), rotate in place
+    auto rotate_rows = [&](uint32_t tile, const Angles& b, int first_off, int step_div,
+                           int valid_rows) {
+#pragma unroll 1
+      for (int t = 0; t < 8; ++t) {
+        const int r = 8 * blk + t;
+        const int off = step_div == 1 ? first_off + t : (first_off + t) / step_div;
+        const uint32_t trow = ttab + uint32_t((off * 32 + ch) * 16);
+        Angles an;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 ct, st;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(ct.x), "=f"(ct.y), "=f"(st.x), "=f"(st.y) : "r"(trow + e * 128));
+          an.c[e] = ptx::fsub2(ptx::fmul2(b.c[e], ct), ptx::fmul2(b.s[e], st));
+          an.s[e] = ptx::ffma2(b.s[e], ct, ptx::fmul2(b.c[e], st));
+        }
+        const float m = rotate_row_chunk(tile, r, ch, an);
+        if (r < valid_rows) mag = fmaxf(mag, m);
+      }
+    };
+    // query tile i: row R of the unit is query R / group at position qpos0 + R / group
+    // (plus the logical shift of a cache with dropped blocks); this thread's rows start
+    // at R0 = row0 + 128 i + 8 blk, and row R0 + t sits (R0 % group + t) / group after it
+    auto q_base = [&](const DecodeItem& it, int i) {
+      const int qsh = p.qshift != nullptr ? __ldg(p.qshift + it.req) : 0;
+      const int R0 = it.row0 + kTileM * i + 8 * blk;
+      const int pos = min(max(it.qpos0 + R0 / p.group + qsh, 0), p.rope_max_pos);
+      return load_angles(p.rope, pos, ch);
+    };
+    auto rotate_q = [&](const DecodeItem& it, int i, const Angles& b) -> bool {
+      if (!wt.warp_wait(BAR(L::kQFull + i), nq[i] & 1u)) return false;
+      ++nq[i];
+      const int R0 = it.row0 + kTileM * i + 8 * blk;
+      rotate_rows(Q_S(i), b, R0 % p.group, p.group, it.nrows - kTileM * i);
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(L::kQRot + i));
+      return true;
+    };
+    for (int u = u_begin; u < u_end && ok; ++u) {
+      const DecodeItem it = p.items[u];
+      const int nt = ntiles_of(it);
+      if (nt == 0) continue;
+      const bool two = it.nrows > kTileM;
+      Angles bk = key_base(it, 0);
+      // K(0) lands first (the producer issues it before the query tiles), then the
+      // query tiles, then K(1), ... (every key tile's K at an even ring position)
+      for (int j = 0; j < nt && ok; ++j) {
+        const uint32_t kc = c + 2 * uint32_t(j);
+        const int nkeys = min(kTileN, it.tok1 - it.tok0 - kTileN * j);
+        if (!wt.warp_wait(FULL(kc), PHASE(kc))) { ok = false; break; }
+        const Angles bnext = key_base(it, j + 1);
+        rotate_rows(STAGE(kc), bk, t0, 1, nkeys);
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(L::kReady + int(kc % kStages)));
+        bk = bnext;
+        if (j == 0) {
+          ok = rotate_q(it, 0, q_base(it, 0));
+          if (ok && two) ok = rotate_q(it, 1, q_base(it, 1));
+        }
+      }
+      c += 2 * uint32_t(nt);
+    }
+    if (mag > kF16Max) atomicOr(p.error, kStatusOperandRange);
   } else {
     // ------------------------------------------------------------ softmax warps
     // Two threads per row: warp w works on query tile w / 8, key/column half
@@ -468,11 +638,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++nx;
       return true;
     };
+    // V of key tile j of a unit (ring position cring + 2 j + 1) to fp16 in place, rows
+    // past the last key zeroed.  Every softmax warp takes 1 / 16 of the 16-byte chunks
+    // of every V tile (q = 32 warp + lane + 512 k: a quarter warp covers 128 contiguous
+    // bytes), in ring order, even for a unit where its query tile has no rows: a barrier
+    // wait more than one use ahead of a stage would be satisfied by an older phase of
+    // the same parity.  In the row-group layout chunk q holds row 8 (q / 128) + (q / 8) % 8.
+    uint32_t cring = 0;
+    float vmag = 0.f;                      // largest V magnitude of a valid row
+    auto convert_v = [&](const DecodeItem& it, int j) -> bool {
+      const uint32_t vc = cring + 2 * uint32_t(j) + 1;
+      if (!wt.warp_wait(FULL(vc), PHASE(vc))) return false;
+      const int nkeys = min(kTileN, it.tok1 - it.tok0 - kTileN * j);
+      const uint32_t vs = STAGE(vc);
+#pragma unroll 2
+      for (int q = 32 * warp + lane; q < kVChunks; q += 32 * kSoftmaxWarps) {
+        const int r = 8 * (q >> 7) + ((q >> 3) & 7);
+        const uint32_t addr = vs + uint32_t(q) * 16u;
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        if (r < nkeys) {
+          uint32_t a[4];
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(addr));
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float x0 = ptx::bf16_lo(a[e]), x1 = ptx::bf16_hi(a[e]);
+            vmag = ptx::fmax3(vmag, fabsf(x0), fabsf(x1));
+            o[e] = ptx::pack_f16(x0, x1);
+          }
+        }
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};"
+                     ::"r"(addr), "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]) : "memory");
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(L::kReady + int(vc % kStages)));
+      return true;
+    };
     for (int u = u_begin; u < u_end && ok; ++u) {
       const DecodeItem it = p.items[u];
       const int nt = ntiles_of(it);
       const int rows_here = it.nrows - kTileM * qt;
-      if (rows_here <= 0) continue;        // second query tile of a short unit: nothing to do
+      if (rows_here <= 0) {
+        // second query tile of a short unit: only its share of the unit's V tiles
+        for (int j = 0; j < nt && ok; ++j) ok = convert_v(it, j);
+        cring += 2 * uint32_t(nt);
+        continue;
+      }
       const int group = p.group;
       const int prow = kTileM * qt + t;    // row within the unit
       const int R = it.row0 + prow;
@@ -480,6 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qpos = it.qpos0 + R / group;
       float m_used = -INFINITY, l = 0.f;   // l: this half's partial sum
       if (nt > 0) {
+        if (!convert_v(it, 0)) { ok = false; break; }
         for (int j = 0; j < nt; ++j) {
           const int key0 = it.tok0 + kTileN * j + 64 * half;
           const int nkeys = min(64, it.tok1 - key0);                          // may be <= 0
@@ -548,9 +761,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float2 x = ptx::ffma2(make_float2(sv[i], sv[i + 1]), sc2, nmu2);
               const float2 e = make_float2(ptx::ex2(x.x), ptx::ex2(x.y));
               rs2[(i >> 1) & 3] = ptx::fadd2(rs2[(i >> 1) & 3], e);
-              pk[i / 2] = ptx::pack_bf16(e.x, e.y);
+              pk[i / 2] = ptx::pack_f16(e.x, e.y);
             }
-            // P (bf16 pairs) over this half's S columns already read
+            // P (fp16 pairs, at most 2^8 with the lazy rescale) over this half's S
+            // columns already read
             umma::tmem_st16u(s_t + 16 * qq, pk);
           }
           const float2 r01 = ptx::fadd2(rs2[0], rs2[1]), r23 = ptx::fadd2(rs2[2], rs2[3]);
@@ -559,8 +773,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma::fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(L::kPFull + qt));
+          // while the tensor cores take P V and the next Q K^T: V of the next key tile
+          if (j + 1 < nt && !convert_v(it, j + 1)) { ok = false; break; }
         }
         if (!ok) break;
+        cring += 2 * uint32_t(nt);
         if (!wt.warp_wait(BAR(L::kOFull + qt), no & 1u)) { ok = false; break; }
         ++no;
         umma::fence_after_sync();
@@ -608,6 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (vmag > kF16Max) atomicOr(p.error, kStatusOperandRange);
   }
 
   // ------------------------------------------------------------ teardown
@@ -690,139 +908,26 @@ __global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(con
   if (lane == 0 && p.lse != nullptr) p.lse[orow] = lt * 0.69314718055994530942f;
 }
 
-// ---------------------------------------------------------------- RoPE pre-pass
-// The cos/sin of frequencies 8c .. 8c + 7 at one position (as four float4, two
-// (cos, sin) pairs each).
-struct RopeChunk {
-  float4 cs[4];
-};
-
-__device__ __forceinline__ RopeChunk rope_chunk(const float2* rope_row, int c) {
-  const float4* tab = reinterpret_cast<const float4*>(rope_row);
-  RopeChunk r;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) r.cs[e] = __ldg(tab + 4 * c + e);
-  return r;
-}
-
-// Rotate the pair of 16-byte chunks (c, c + 8) of one row -- dimensions 8c .. 8c + 7
-// and their partners 64 further -- and store it as fp16 scaled by 2^-4 (the operand
-// type of the RoPE prefill's Q K^T); returns true when a value does not fit.
-__device__ __forceinline__ bool rotate_chunk(const uint16_t* src, uint16_t* dst, int c,
-                                             const RopeChunk& t) {
-  const uint4 av = __ldg(reinterpret_cast<const uint4*>(src) + c);
-  const uint4 bv = __ldg(reinterpret_cast<const uint4*>(src) + 8 + c);
-  const uint32_t* a = reinterpret_cast<const uint32_t*>(&av);
-  const uint32_t* b = reinterpret_cast<const uint32_t*>(&bv);
-  uint32_t xo[4], yo[4];
-  bool bad = false;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float4 cs = t.cs[e];   // frequencies 8c + 2e, 8c + 2e + 1
-    const float a0 = ptx::bf16_lo(a[e]), a1 = ptx::bf16_hi(a[e]);
-    const float b0 = ptx::bf16_lo(b[e]), b1 = ptx::bf16_hi(b[e]);
-    const float x0 = (a0 * cs.x - b0 * cs.y) * kRopeOperandScale;
-    const float x1 = (a1 * cs.z - b1 * cs.w) * kRopeOperandScale;
-    const float y0 = (b0 * cs.x + a0 * cs.y) * kRopeOperandScale;
-    const float y1 = (b1 * cs.z + a1 * cs.w) * kRopeOperandScale;
-    bad |= fmaxf(fmaxf(fabsf(x0), fabsf(x1)), fmaxf(fabsf(y0), fabsf(y1))) > kRopeOperandMax;
-    xo[e] = ptx::pack_f16(x0, x1);
-    yo[e] = ptx::pack_f16(y0, y1);
-  }
-  reinterpret_cast<uint4*>(dst)[c] = make_uint4(xo[0], xo[1], xo[2], xo[3]);
-  reinterpret_cast<uint4*>(dst)[8 + c] = make_uint4(yo[0], yo[1], yo[2], yo[3]);
-  return bad;
-}
-
-// Request i with start[i] <= r < start[i + 1].
-__device__ __forceinline__ int find_request(const int32_t* start, int n, int r) {
-  int lo = 0, hi = n - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(start + mid) <= r) lo = mid; else hi = mid - 1;
-  }
-  return lo;
-}
-
-// A block of 256 threads rotates 32 rows; thread (row, c) handles the chunk pair
-// (c, c + 8) of its row for every head.  The first blocks take the keys of the
-// prefill requests (each key row at its position in the request's page list,
-// for every kv head, into the dense rotated-K buffer), the rest their query rows
-// (every qo head, into the rotated copy of q).  The request, page id and cos/sin
-// of a row are looked up once and reused for all its heads, which keeps the
-// heads' loads independent (many in flight per thread).
-constexpr int kRopeRowsPerBlock = 32;
-__global__ void __launch_bounds__(256) rope_prepass_kernel(const RopePrepassParams p) {
-  const int c = threadIdx.x & 7;
-  const int rl = threadIdx.x >> 3;
-  const int nkb = (p.rk_total + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock;
-  bool bad = false;
-  if (int(blockIdx.x) < nkb) {
-    const int r = int(blockIdx.x) * kRopeRowsPerBlock + rl;
-    if (r < p.rk_total) {
-      const int i = find_request(p.rk_start, p.n, r);
-      const int j = r - __ldg(p.rk_start + i);
-      const int entry = __ldg(p.rk_req_pbase + i) + j / p.P;
-      const int page = __ldg(p.indices + entry);
-      // the key's position: its index, or its page's logical position + slot
-      const int kpos = p.page_pos ? __ldg(p.page_pos + entry) + j % p.P : j;
-      const RopeChunk t = rope_chunk(p.rope_nat + size_t(min(kpos, p.rope_max_pos)) * (D / 2), c);
-      // HND: a head's P rows are contiguous; NHD: a token's Hk heads are
-      const size_t head_stride = p.nhd ? size_t(D) : size_t(p.P) * D;
-      const uint16_t* src =
-          p.k_pages + (p.nhd ? (size_t(page) * p.P + (j % p.P)) * p.Hk * D
-                             : (size_t(page) * p.Hk * p.P + (j % p.P)) * D);
-      uint16_t* dst = p.rotk + size_t(r) * D;
-#pragma unroll 4
-      for (int kvh = 0; kvh < p.Hk; ++kvh)
-        bad |= rotate_chunk(src + kvh * head_stride, dst + size_t(kvh) * p.rk_total * D, c, t);
-    }
-  } else {
-    const int r = (int(blockIdx.x) - nkb) * kRopeRowsPerBlock + rl;
-    if (r < p.rq_total) {
-      const int i = find_request(p.rq_start, p.n, r);
-      const int j = r - __ldg(p.rq_start + i);
-      const size_t row0 = size_t(__ldg(p.rq_row0 + i) + j) * p.Hq;
-      const int pos = __ldg(p.rq_pos0 + i) + j;
-      const RopeChunk t = rope_chunk(p.rope_nat + size_t(min(pos, p.rope_max_pos)) * (D / 2), c);
-#pragma unroll 4
-      for (int h = 0; h < p.Hq; ++h)
-        bad |= rotate_chunk(p.q + (row0 + h) * D, p.rotq + (row0 + h) * D, c, t);
-    }
-  }
-  if (bad) atomicOr(p.error, kStatusRopeRange);
-}
-
 template <bool ROPE, bool WIN>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const PrefillParams& p, int grid, cudaStream_t stream) {
   auto kern = bsr_prefill_kernel<ROPE, WIN>;
   constexpr size_t smem = Smem::kDynBytes;
-  static bool opted_in[64] = {};
+  static std::atomic<bool> opted_in[64];   // zero-initialized: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!opted_in[dev]) {
+  if (!opted_in[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
-    opted_in[dev] = true;
+    opted_in[dev].store(true, std::memory_order_release);
   }
-  kern<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
+  kern<<<grid, threads_of<ROPE>(), smem, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
-
-cudaError_t launch_rope_prepass(const RopePrepassParams& p, int num_sms, cudaStream_t stream) {
-  (void)num_sms;
-  const int64_t grid = (int64_t(p.rk_total) + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock +
-                       (int64_t(p.rq_total) + kRopeRowsPerBlock - 1) / kRopeRowsPerBlock;
-  if (grid <= 0) return cudaSuccess;
-  if (grid > INT32_MAX) return cudaErrorInvalidValue;
-  rope_prepass_kernel<<<int(grid), 256, 0, stream>>>(p);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillParams& p, int grid,

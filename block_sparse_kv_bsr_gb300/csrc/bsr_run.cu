@@ -148,7 +148,7 @@ bool encode_pool_groups(CUtensorMap* tm, const void* base, const PoolGeom& g, in
   return encode(tm, BF, 5, base, dims, strides, box);
 }
 
-// Tensor map over q (or its rotated copy) [rows, Hq, D = 128] (16-bit) for the
+// Tensor map over q [rows, Hq, D = 128] (bf16) for the
 // prefill kernel's query tiles: rank 4 {64 cols, 2 column blocks, Hq heads,
 // rows}; one box is one 64-column block of `group` heads x 128 / group
 // queries -- the 128 packed rows of a query tile, 128B-swizzled.
@@ -262,53 +262,13 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     }
   }
   if (s->n_pitems > 0) {
-    const bool rotk = rope && s->rk_total > 0;
-    if (rotk) {
-      // rotate the prefill requests' keys and queries once into the schedule's buffers
-      if (!s->tm_rk_valid) {
-        // the dense rotated-K buffer [Hk][rk_total][D] is head-major like an HND pool
-        const PoolGeom rk{int64_t(s->Hk) * s->rk_total, s->Hk, false};
-        if (!encode_pool_stage(&s->tm_rk, s->d_ws + s->off_rotk, rk, s->D, bsr::kPrefillKeyTile))
-          return BSR_ERR_CUDA;
-        s->tm_rk_valid = true;
-      }
-      bsr::RopePrepassParams r{};
-      r.k_pages = static_cast<const uint16_t*>(k_pages);
-      r.q = static_cast<const uint16_t*>(q);
-      r.indices = s->dev<const int32_t>(s->off_indices);
-      r.rk_req_pbase = s->dev<const int32_t>(s->off_rk_pbase);
-      r.rk_start = s->dev<const int32_t>(s->off_rk_start);
-      r.rq_row0 = s->dev<const int32_t>(s->off_rq_row0);
-      r.rq_start = s->dev<const int32_t>(s->off_rq_start);
-      r.rq_pos0 = s->dev<const int32_t>(s->off_rq_pos0);
-      r.page_pos = s->has_page_pos ? s->dev<const int32_t>(s->off_page_pos) : nullptr;
-      r.nhd = s->kv_layout == BSR_KV_NHD;
-      r.rope_nat = reinterpret_cast<const float2*>(s->d_rope + s->rope_bytes);
-      r.rotk = s->dev<uint16_t>(s->off_rotk);
-      r.rotq = s->dev<uint16_t>(s->off_rotq);
-      r.error = s->dev<int32_t>(s->off_error);
-      r.n = s->rk_n;
-      r.rk_total = s->rk_total;
-      r.rq_total = s->rq_total;
-      r.Hk = s->Hk;
-      r.Hq = s->Hq;
-      r.P = s->P;
-      r.rope_max_pos = s->rope_rows - 1;
-      t_mark(1, 0);
-      if (bsr::launch_rope_prepass(r, s->num_sms, stream) != cudaSuccess) {
-        cudaGetLastError();
-        return BSR_ERR_CUDA;
-      }
-      t_mark(1, 1);
-    }
-    // query tiles come from q, or with RoPE from its rotated copy
-    const void* qsrc = rotk ? static_cast<const void*>(s->d_ws + s->off_rotq) : q;
-    if (s->tm_q_ptr != qsrc) {
-      if (!encode_q(&s->tm_q, qsrc, s->sum_qo, s->Hq, s->group)) {
+    // query tiles come straight from q (with RoPE the kernel rotates them in shared memory)
+    if (s->tm_q_ptr != q) {
+      if (!encode_q(&s->tm_q, q, s->sum_qo, s->Hq, s->group)) {
         s->tm_q_ptr = nullptr;
         return BSR_ERR_CUDA;
       }
-      s->tm_q_ptr = qsrc;
+      s->tm_q_ptr = q;
     }
     // K/V boxes of min(P, 128) rows (the prefill class has P >= 16)
     const int box_rows = s->P < bsr::kPrefillKeyTile ? s->P : bsr::kPrefillKeyTile;
@@ -329,8 +289,10 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     }
     bsr::PrefillParams p{};
     p.box_rows = box_rows;
-    p.rk_off = rotk ? s->dev<const int32_t>(s->off_rk_off) : nullptr;
-    p.rk_total = rotk ? s->rk_total : 0;
+    p.rope = rope ? reinterpret_cast<const float4*>(s->d_rope + s->rope_bytes) : nullptr;
+    p.page_pos = rope && s->has_page_pos ? s->dev<const int32_t>(s->off_page_pos) : nullptr;
+    p.qshift = rope && s->has_page_pos ? s->dev<const int32_t>(s->off_qshift) : nullptr;
+    p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
     p.items = s->dev<const bsr::DecodeItem>(s->off_pitems);
     p.cta_ptr = s->dev<const int32_t>(s->off_cta_ptr);
     p.part_o = s->dev<float>(s->off_ppart_o);
@@ -351,10 +313,10 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.window_left = s->window_left;
     p.nhd = s->kv_layout == BSR_KV_NHD;
     p.wait_limit_ns = wait_limit_ns;
-    t_mark(2, 0);
+    t_mark(1, 0);
     cudaError_t e =
-        bsr::launch_prefill(rotk, s->tm_q, rotk ? s->tm_rk : s->tm_pk, s->tm_pv, p, s->pre_ctas, stream);
-    t_mark(2, 1);
+        bsr::launch_prefill(rope, s->tm_q, s->tm_pk, s->tm_pv, p, s->pre_ctas, stream);
+    t_mark(1, 1);
     if (e == cudaSuccess && s->n_pmerge > 0) {
       bsr::PrefillMergeParams m{};
       m.units = s->dev<const bsr::DecodeItem>(s->off_pmerge);
@@ -366,9 +328,9 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
       m.Hq = s->Hq;
       m.group = s->group;
       m.out_f32 = p.out_f32;
-      t_mark(3, 0);
+      t_mark(2, 0);
       e = bsr::launch_prefill_merge(m, stream);
-      t_mark(3, 1);
+      t_mark(2, 1);
     }
     if (e != cudaSuccess) {
       cudaGetLastError();

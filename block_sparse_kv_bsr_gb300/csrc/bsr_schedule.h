@@ -13,6 +13,7 @@
 struct bsr_schedule {
   int device = -1;
   int num_sms = 0;
+  int32_t sm_budget = 0;       // plans spread their work over at most this many SMs (0: all)
 
   // problem the schedule was planned for
   int32_t batch = 0, Hq = 0, Hk = 0, D = 0, P = 0, group = 0, causal = 0;
@@ -42,18 +43,12 @@ struct bsr_schedule {
          off_part_o = 0, off_part_lse = 0;
   size_t off_pitems = 0, off_cta_ptr = 0, off_pmerge = 0, off_ppart_o = 0, off_ppart_lse = 0;
   int32_t n_pmerge = 0;      // prefill units whose key range was split (merged by a second kernel)
-  // RoPE prefill: rotated-K and rotated-Q buffers and the request list of their pre-pass
-  size_t off_rk_off = 0, off_rk_pbase = 0, off_rk_start = 0, off_rotk = 0;
-  size_t off_rq_row0 = 0, off_rq_start = 0, off_rq_pos0 = 0, off_rotq = 0;
-  int32_t rk_n = 0, rk_total = 0, rq_total = 0;
-  CUtensorMap tm_rk;
-  bool tm_rk_valid = false;
   // prefill K/V tiles: boxes of min(P, 128) rows over the caller's pools
   CUtensorMap tm_pk;
   CUtensorMap tm_pv;
   const void* tm_pk_ptr = nullptr;
   const void* tm_pv_ptr = nullptr;
-  // prefill query tiles: over q (no RoPE) or the rotated copy (RoPE)
+  // prefill query tiles over q
   CUtensorMap tm_q;
   const void* tm_q_ptr = nullptr;
 
@@ -85,7 +80,7 @@ struct bsr_schedule {
   const void* tm_v8_ptr = nullptr;
 
   // optional per-stage timing of runs: events [run slot][stage][begin, end]
-  static constexpr int kStages = 4;   // decode, RoPE pre-pass, prefill, merge
+  static constexpr int kStages = 3;   // decode, prefill, prefill merge
   std::vector<cudaEvent_t> t_ev;
   std::vector<uint8_t> t_ran;         // [run slot][stage]
   int32_t t_max = 0;
@@ -109,5 +104,4 @@ cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& 
                            const CUtensorMap& tv, const PrefillParams& p, int grid,
                            cudaStream_t stream);
 cudaError_t launch_prefill_merge(const PrefillMergeParams& p, cudaStream_t stream);
-cudaError_t launch_rope_prepass(const RopePrepassParams& p, int num_sms, cudaStream_t stream);
 }  // namespace bsr

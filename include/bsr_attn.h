@@ -120,8 +120,8 @@ typedef struct bsr_schedule* bsr_schedule_t;
  * Every run of the schedule reads k_pages / v_pages in that layout.
  *
  * *schedule must be NULL (a new schedule is created) or a schedule returned
- * by an earlier plan, which is then re-planned in place: its device workspace
- * is reused when large enough.  Re-planning is ordered on `stream` after work
+ * by an earlier plan or by bsr_schedule_create, which is then (re-)planned in
+ * place: its device workspace is reused when large enough.  Re-planning is ordered on `stream` after work
  * already queued there; work on other streams that still reads the old
  * schedule is the caller's to finish first.
  * The schedule binds the current CUDA device.
@@ -131,6 +131,19 @@ int bsr_attn_plan(const int32_t* indptr, const int32_t* indices, const int32_t* 
                   int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
                   int32_t causal, int32_t window_left, const int32_t* page_pos,
                   int32_t kv_layout, float rope_theta, void* stream, bsr_schedule_t* schedule);
+
+/*
+ * bsr_schedule_create — an empty schedule, bound to the current CUDA device,
+ * whose plans spread their work over at most sm_budget SMs (0: all of the
+ * device's SMs); plan into it with bsr_attn_plan.  A budget lets two schedules
+ * run at the same time on disjoint parts of the GPU, each launched on its own
+ * stream -- the composable levels of a cascade ("Block-Sparse 포맷": a shared
+ * prefix stored once, composed with per-request suffixes), whose prefix level
+ * keeps the tensor cores busy while the suffix level streams its pages from
+ * HBM.  sm_budget >= 0 (else BSR_ERR_INVALID_ARGUMENT).  Free with
+ * bsr_schedule_destroy.
+ */
+int bsr_schedule_create(int32_t sm_budget, bsr_schedule_t* schedule);
 
 /*
  * bsr_attn_run — execute a schedule: out = softmax(sm_scale * q k^T) v and
@@ -228,8 +241,8 @@ typedef struct bsr_schedule_info {
   int64_t upload_bytes;       /* bytes of the one host-to-device copy a plan makes */
   double decode_imbalance;    /* max / mean planned cost over decode warps */
   double prefill_imbalance;   /* max / mean planned cost over prefill CTAs */
-  int32_t kernels_per_run;    /* kernels one bsr_attn_run launches (decode, RoPE pre-pass,
-                                 prefill, split-range merge; 0 when there is no work) */
+  int32_t kernels_per_run;    /* kernels one bsr_attn_run launches (decode, prefill,
+                                 split-range merge; 0 when there is no work) */
   int32_t window_left;        /* sliding window given to plan (0: none) */
   int32_t kv_layout;          /* BSR_KV_HND or BSR_KV_NHD */
   int32_t reserved;
@@ -243,12 +256,12 @@ int bsr_schedule_get_info(bsr_schedule_t schedule, bsr_schedule_info_t* info);
  *
  * bsr_schedule_set_stage_timing: with max_calls > 0 every later run records
  * CUDA events on its stream around each kernel it launches -- stage 0 decode,
- * 1 RoPE pre-pass, 2 prefill, 3 split-range merge -- and the schedule keeps
+ * 1 prefill, 2 split-range merge of the prefill -- and the schedule keeps
  * the last max_calls runs; 0 turns timing off and frees the events.  Returns
  * BSR_OK or a negative BSR_ERR_* code.
  *
  * bsr_schedule_stage_times: waits for the events of kept run `call` (0 = the
- * oldest kept) and writes its four stage durations in milliseconds to ms[4]
+ * oldest kept) and writes its three stage durations in milliseconds to ms[3]
  * (-1 for a stage that did not run).  Returns the number of runs kept, or a
  * negative BSR_ERR_* code (BSR_ERR_INVALID_ARGUMENT for a call not kept).
  */
@@ -295,9 +308,15 @@ int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
  * call on a device looks up the array's device address (make that call before
  * any stream capture).  All calls on a device share the array and every call
  * rewrites it: calls whose kernels overlap on the GPU race, so keep them on
- * one stream.  A request whose table entries are malformed, or whose pages
- * fall outside the pool, is treated as empty and bit 1 is OR-ed into
- * *device_status (device int32, may be NULL); bit 0 means a bounded wait gave up.
+ * one stream.  The device table is checked on the device, request by request:
+ * a request whose entries are malformed (indptr[b] < 0, a negative page count,
+ * last_page_len outside [1, page_size], a length beyond 2^31 - 1 keys) or any
+ * page of which that its query reads lies outside [0, num_pages_in_pool) is
+ * treated as empty as a whole -- its out rows are 0 and its lse -inf -- and bit
+ * 1 is OR-ed into *device_status (device int32, may be NULL); the other
+ * requests are unaffected.  indptr[b + 1] must not exceed the length of
+ * `indices` (the library is not told that length).  Bit 0 means a bounded
+ * wait gave up.
  */
 int bsr_attn_decode_noalloc(const void* q, const void* k_pages, const void* v_pages,
                             const int32_t* indptr, const int32_t* indices,
@@ -341,11 +360,13 @@ int bsr_attn_decode_noalloc_ex(const void* q, const void* k_pages, const void* v
 int bsr_selftest_bounded_wait(int32_t* device_status, int64_t limit_ns, void* stream);
 
 /* Device-side status word of a schedule (0 = fine; bit 0: a kernel gave up on
- * a bounded wait; bit 1: with RoPE on the tensor-core prefill path, a rotated
- * q or k value was at least 2^20 in magnitude, beyond the range of its fp16
- * operand (x 2^-4), so scores involving it are not finite).  Bits stay set
- * until the schedule is planned again.  Synchronizes the schedule's device;
- * returns the word, or a negative BSR_ERR_* code. */
+ * a bounded wait; bit 1: a value was beyond the range of its fp16 operand, so
+ * the scores or outputs involving it are not finite -- with RoPE a rotated q or
+ * k of magnitude 2^20 or more (the rotated operands are fp16 x 2^-4), or, for
+ * requests on the tensor-core prefill path, a V value beyond 65504 (P and V
+ * enter P.V as fp16)).  Bits stay set until the schedule is planned again.
+ * Synchronizes the schedule's device; returns the word, or a negative BSR_ERR_*
+ * code. */
 int bsr_last_device_error(bsr_schedule_t schedule);
 
 /* Static, human-readable text for a status code. */

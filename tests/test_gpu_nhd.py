@@ -1,7 +1,7 @@
 """GPU parity over token-major (NHD) page pools [pages, P, Hk, D]: the same batches as
 the head-major tests, with the pools transposed, through every kernel path (decode
 with TMA stages and with pages below 16 keys, FP8 decode, tensor-core prefill with
-page-sized and whole-tile K boxes, the RoPE pre-pass, append_kv) against the oracle
+page-sized and whole-tile K boxes, RoPE rotated in the prefill kernel, append_kv) against the oracle
 reading the same NHD pools."""
 import numpy as np
 import pytest

@@ -1,7 +1,7 @@
 """GPU parity of RoPE at per-page logical positions (caches whose inactive blocks were
 dropped keep their tokens' positions) against the fp64 oracle: the decode kernel
 (the stage's cos/sin row follows its page's position, queries follow the last logical
-key), the RoPE pre-pass of the tensor-core prefill kernel, and identity positions."""
+key), the RoPE rotation inside the tensor-core prefill kernel, and identity positions."""
 import pytest
 import torch
 
