@@ -7,26 +7,34 @@ Workload (one "step" = one plan-free bsr_attn_run over the whole batch):
 Inputs are synthetic (seeded, see workloads/) and larger than L2 (about 1 GB
 of active KV against 129 MB of L2), so consecutive steps read KV from HBM.
 
-value     = algorithmic bytes (active K+V, q, out, lse, page table) / device time per step.
-e2e       = the same bytes / time of the call a user makes with HOST buffers:
-            re-plan from host page-table arrays, H2D of q, run, D2H of out and lse.
+value     = algorithmic bytes (active K+V, q, out, lse, page table) / device time per step
+            (K steps, CUDA events at the ends of the region only).
+hot, cold = the same steps timed one by one: back to back, and after a write of twice the
+            L2 before each step (outside its events), so that every step starts cold.
+e2e       = the same bytes / time of the call a user makes with HOST buffers: per step the
+            plan of the page table (on the host, overlapping the previous step's kernel as
+            a serving loop would), H2D of q and the plan, run, D2H of out and lse, and the
+            host's wait for them; the serialised form is reported beside it.
 roofline  = the dominant kernel's algorithmic bytes (or FLOPs) / its mean CUDA-event
             duration, against the measured HBM copy bandwidth (or bf16 dense peak); also
             its p10 / median / p90 over the timed calls and the DRAM traffic from the
             committed ncu summary of the same build.
 cpu_baseline = the fp64 oracle on this host's cores over whole passes for ~10 s (decode
             workloads; configs 1 and 2 add a one-thread figure).
-clocks    = nvidia-smi samples taken during the first timed region.
+clocks    = SM clock and clock-event reasons polled through NVML every ~0.5 ms during the
+            first timed region (nvidia-smi samples where NVML does not load).
+configs   = after the headline, the other workloads (--configs), each with hot and cold
+            timings, its kernels, its roofline and (decode) its e2e figure.
 
---config selects another workload for measurement (2: Llama-3-8B-shaped decode with RoPE,
+--config selects the headline workload (2: Llama-3-8B-shaped decode with RoPE,
 4: shared-prefix cascade, 5: chunked prefill with append, reported in TFLOP/s, 6: the
 skewed decode over an FP8 (E4M3) KV cache, 7: sliding-window decode over long histories,
 8: the skewed decode with RoPE at the kept blocks' logical positions, 9: a three-level
 cascade of shared prefixes, 10: the skewed decode over token-major (NHD) pages);
 the default is the skewed decode above.  --impl reference times the oracle (the only
 reference this method has here) on the same workload, each step one pass over the batch
-or, when K passes would take more than ~90 s, over every k-th request.  Under torchrun each rank runs an
-independent replica (weak scaling).
+or, when K passes would take more than ~90 s, over every k-th request.  Under torchrun each
+rank runs an independent replica (weak scaling).
 """
 from __future__ import annotations
 
@@ -60,7 +68,13 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10],
                     help="workload; 3 (skewed block-sparse decode) is the headline")
-    return ap.parse_args()
+    ap.add_argument("--configs", default="1,2,4,5,6,7,8,9,10",
+                    help="further workloads measured after the headline (comma list; '' for none)")
+    ap.add_argument("--time-budget", type=float, default=240.0,
+                    help="seconds after which further workloads are skipped (and listed as such)")
+    args = ap.parse_args()
+    args.configs = [int(x) for x in args.configs.split(",") if x.strip()]
+    return args
 
 
 def dist_env():
@@ -175,6 +189,99 @@ class ClockSampler:
                 "window": how}
 
 
+class NvmlClocks:
+    """SM clock and clock-event reasons polled through NVML (the driver's own library,
+    loaded with ctypes) in a background thread every ~0.5 ms, so that even a timed region
+    of a few milliseconds holds several samples.  Same interface as ClockSampler; the
+    device is matched to the CUDA device by UUID, then by PCI bus id."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int, period_s: float = 0.0005):
+        import ctypes
+        import torch
+        self.period = period_s
+        self.samples = []
+        self.t0 = self.t1 = None
+        self._stop = False
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        props = torch.cuda.get_device_properties(cuda_index)
+        ok = False
+        try:
+            ok = lib.nvmlDeviceGetHandleByUUID(f"GPU-{props.uuid}".encode(), ctypes.byref(self.h)) == 0
+        except Exception:
+            ok = False
+        if not ok:
+            bus = f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+            ok = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0
+        if not ok:
+            raise RuntimeError("no NVML handle for the CUDA device")
+        try:
+            self._reasons_fn = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons_fn = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = (float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0
+                        else None)
+
+    def _sample(self):
+        import ctypes
+        sm = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(sm)) != 0:
+            return
+        reasons = set()
+        if self._reasons_fn(self.h, ctypes.byref(rs)) == 0:
+            reasons = {n for bit, n in self.REASONS.items() if rs.value & bit}
+        self.samples.append((time.time(), float(sm.value), self.max_mhz, reasons))
+
+    def _loop(self):
+        while not self._stop:
+            self._sample()
+            time.sleep(self.period)
+
+    def start(self):
+        self._sample()
+        self.thread = threading.Thread(target=self._loop, daemon=True)
+        self.thread.start()
+        return self
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        self._stop = True
+        self.thread.join(timeout=1.0)
+
+    def summary(self):
+        inside = [x for x in self.samples if self.t0 is not None and self.t0 <= x[0] <= self.t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml"}
+        reasons = set()
+        for x in inside:
+            reasons |= x[3]
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(x[1] for x in inside), "reasons": sorted(reasons),
+                "samples": len(inside), "period_ms": self.period * 1e3,
+                "window": "inside timed region", "source": "nvml"}
+
+
+def clock_sampler(local: int):
+    """NVML polling when the driver library loads, else nvidia-smi samples."""
+    try:
+        return NvmlClocks(local).start()
+    except Exception:
+        return ClockSampler(local).start()
+
+
 def traffic_from_profile(name: str, digest: str):
     """DRAM bytes per launch from a committed ncu summary under profiles/, if it was
     captured on the kernel built from the current sources (digest of those sources)."""
@@ -245,6 +352,20 @@ def attention_flops(w) -> int:
     return total * w.num_qo_heads * 4 * w.head_dim
 
 
+def cascade_prefix_sms(num_sms: int, prefix_flops: float, suffix_bytes: float) -> int:
+    """SMs for a cascade's tensor-core prefix level when it runs beside the HBM-bound
+    suffix level on the other SMs: the split that evens out the two levels' times, from
+    per-SM rates measured on GB300 (the prefill kernel ~5.3 TFLOP/s per SM; the decode
+    kernel streams ~55 GB/s per SM, ~6.3 TB/s at most over the whole GPU)."""
+    best = (float("inf"), num_sms // 2)
+    for s1 in range(8, num_sms - 7):
+        t = max(prefix_flops / (s1 * 5.3e12),
+                suffix_bytes / min((num_sms - s1) * 55e9, 6.3e12))
+        if t < best[0]:
+            best = (t, s1)
+    return best[1]
+
+
 def build_job(cfg: int, dev, small: bool):
     """Device tensors, schedules and the per-step calls of one workload."""
     import torch
@@ -300,16 +421,14 @@ def build_job(cfg: int, dev, small: bool):
         lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         q_dev = torch.empty_like(q)
 
-        def e2e():
-            plan(w, s)
+        def e2e_launch():
             q_dev.copy_(q_host, non_blocking=True)
             bsr.bsr_attn_run(s, q_dev, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta,
                              causal=w.causal, out=out, lse=lse)
             out_host.copy_(out, non_blocking=True)
             lse_host.copy_(lse, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
 
-        job["e2e"] = e2e
+        job["e2e"] = (lambda: plan(w, s), e2e_launch)
         job["e2e_bytes"] = lambda: (q.numel() * 2 + int(s.info()["upload_bytes"]),
                                     out.numel() * 2 + lse.numel() * 4)
     elif cfg == 6:
@@ -340,16 +459,14 @@ def build_job(cfg: int, dev, small: bool):
         lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         q_dev = torch.empty_like(q)
 
-        def e2e():
-            plan(w, s)
+        def e2e_launch():
             q_dev.copy_(q_host, non_blocking=True)
             bsr.bsr_attn_run_kv8(s, q_dev, k, v, k_scale=w.k_scale, v_scale=w.v_scale,
                                  sm_scale=w.sm_scale, causal=w.causal, out=out, lse=lse)
             out_host.copy_(out, non_blocking=True)
             lse_host.copy_(lse, non_blocking=True)
-            torch.cuda.current_stream().synchronize()
 
-        job["e2e"] = e2e
+        job["e2e"] = (lambda: plan(w, s), e2e_launch)
         job["e2e_bytes"] = lambda: (q.numel() * 2 + int(s.info()["upload_bytes"]),
                                     out.numel() * 2 + lse.numel() * 4)
     elif cfg == 4:
@@ -364,14 +481,32 @@ def build_job(cfg: int, dev, small: bool):
         l_s = torch.empty_like(l_p)
         o = torch.empty_like(o_p)
         l = torch.empty_like(l_p)
-        sp, ss = plan(pre), plan(suf)
         kv_p = pre.active_tokens * 2 * pre.num_kv_heads * pre.head_dim * 2
         kv_s = suf.active_tokens * 2 * suf.num_kv_heads * suf.head_dim * 2
         qo = q.numel() * 2
         st = o.numel() * 4 + l.numel() * 4                  # one fp32 state
+        # the two levels side by side: the prefix level (tensor cores) on its own stream
+        # and share of the SMs, the suffix level (HBM) on the rest; the merge waits for both
+        n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        s_pre = cascade_prefix_sms(n_sms, attention_flops(pre), kv_s + qo + st)
+        sp = plan(pre, bsr.bsr_schedule_create(s_pre))
+        ss = plan(suf, bsr.bsr_schedule_create(n_sms - s_pre))
+        side = torch.cuda.Stream(dev)
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+
+        def prefix_level():
+            main = torch.cuda.current_stream()
+            fork.record(main)
+            side.wait_event(fork)
+            bsr.bsr_attn_run(sp, q, pk, pv, sm_scale=pre.sm_scale, out=o_p, lse=l_p, stream=side)
+            join.record(side)
+
+        def merge_levels():
+            torch.cuda.current_stream().wait_event(join)
+            bsr.bsr_merge_states(o_p, l_p, o_s, l_s, o_out=o, lse_out=l)
+
         job["parts"] = [
-            Part("prefix", lambda: bsr.bsr_attn_run(sp, q, pk, pv, sm_scale=pre.sm_scale,
-                                                    out=o_p, lse=l_p),
+            Part("prefix", prefix_level,
                  "bsr_prefill_kernel<0>", "tensor", attention_flops(pre), "FLOP",
                  launches=sp.info()["kernels_per_run"], sched=sp, stage="prefill",
                  family="prefill", profile=None if small else "bsr_prefill_cascade_prefix8192.md"),
@@ -380,8 +515,7 @@ def build_job(cfg: int, dev, small: bool):
                  "bsr_decode_kernel<128,0,0,0>", "hbm", kv_s + qo + st, "B",
                  launches=ss.info()["kernels_per_run"], sched=ss, stage="decode",
                  family="decode", profile=None if small else "bsr_decode_cascade_suffix.md"),
-            Part("merge", lambda: bsr.bsr_merge_states(o_p, l_p, o_s, l_s, o_out=o, lse_out=l),
-                 "merge_states_kernel<128,1>", "hbm", 3 * st, "B"),
+            Part("merge", merge_levels, "merge_states_kernel<128,1>", "hbm", 3 * st, "B"),
         ]
         job["schedules"] = [sp, ss]
         alg = kv_p + kv_s + qo + st
@@ -390,7 +524,8 @@ def build_job(cfg: int, dev, small: bool):
                    config={"workload": c.name, "requests": suf.batch,
                            "prefix_tokens": pre.kv_len[0], "prefix_page_size": pre.page_size,
                            "suffix_tokens": suf.active_tokens, "algorithmic_bytes": alg,
-                           "levels": "prefix (tensor cores) + suffix (decode) + LSE merge"})
+                           "levels": "prefix (tensor cores) beside suffix (decode), then LSE merge",
+                           "sm_split": {"prefix": s_pre, "suffix": n_sms - s_pre}})
     elif cfg == 9:
         c = wl.config9(small)
         q = c.levels[0].q.to(dev)
@@ -466,6 +601,181 @@ def build_job(cfg: int, dev, small: bool):
     return job
 
 
+def timed_steps(step, steps, stream, flush=None):
+    """Device time (ms) of each of `steps` steps, CUDA events around each on `stream`.
+    With `flush` (an int32 tensor over twice the L2), every step is preceded, outside
+    its events, by a write of the whole buffer, so the step starts with a cold L2."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i, (a, b) in enumerate(evs):
+        if flush is not None:
+            flush.fill_(i + 1)
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def kernel_pass(parts, steps, stream, bsr):
+    """K more steps with CUDA events around each library call and the library's own
+    stage events around each kernel of a bsr_attn_run call (records that sit between
+    kernels, which is why the whole-job region has none)."""
+    import torch
+    for pt in parts:
+        pt.ms, pt.kernel_ms, pt.stage_ms = [], [], {}
+        if pt.sched is not None:
+            bsr.bsr_schedule_set_stage_timing(pt.sched, steps)
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+            for _ in parts] for _ in range(steps)]
+    for row in evs:
+        for pt, (a, b) in zip(parts, row):
+            a.record(stream)
+            pt.fn()
+            b.record(stream)
+    torch.cuda.synchronize()
+    for row in evs:
+        for pt, (a, b) in zip(parts, row):
+            pt.ms.append(a.elapsed_time(b))
+    for pt in parts:
+        if pt.sched is not None:
+            for call in range(steps):
+                t = bsr.bsr_schedule_stage_times(pt.sched, call)
+                if pt.stage in t:
+                    pt.kernel_ms.append(t[pt.stage])
+                for name, ms in t.items():
+                    pt.stage_ms.setdefault(name, []).append(ms)
+            bsr.bsr_schedule_set_stage_timing(pt.sched, 0)
+
+
+def spread(ms):
+    """mean / median / p10 / p90 of a list of milliseconds, in microseconds."""
+    dec = statistics.quantiles(ms, n=10, method="inclusive") if len(ms) > 1 else [ms[0]] * 9
+    return {"us_mean": round(sum(ms) / len(ms) * 1e3, 2),
+            "us_median": round(statistics.median(ms) * 1e3, 2),
+            "us_p10": round(dec[0] * 1e3, 2), "us_p90": round(dec[-1] * 1e3, 2)}
+
+
+def roofline_of(parts, _build):
+    """Roofline of the call that takes the most time in a step (among the attention
+    kernels' calls): its algorithmic bytes or FLOPs over its kernel's mean duration."""
+    peak_hbm, hbm_kind = peaks()
+    peak_tensor, tensor_kind = tensor_peak()
+    dom = max([pt for pt in parts if pt.family is not None] or parts, key=lambda pt: sum(pt.ms))
+    call_ms = sum(dom.ms) / len(dom.ms)
+    kms = dom.kernel_ms if dom.kernel_ms else dom.ms
+    dom_ms = sum(kms) / len(kms)
+    sources = {"decode": _build.DECODE_KERNEL_SOURCES,
+               "decode_kv8": _build.DECODE_KV8_KERNEL_SOURCES,
+               "prefill": _build.PREFILL_KERNEL_SOURCES}.get(dom.family)
+    build_digest = _build.kernel_digest(sources) if sources else None
+    traffic = traffic_from_profile(dom.profile, build_digest) if dom.profile is not None else None
+    if dom.bound == "hbm":
+        achieved, peak, unit = dom.work / (dom_ms * 1e-3) / 1e9, peak_hbm, "GB/s"
+        kind = f"{hbm_kind} hbm_gbs (copy)"
+    else:
+        achieved, peak, unit = dom.work / (dom_ms * 1e-3) / 1e12, peak_tensor, "TFLOP/s"
+        kind = f"{tensor_kind} bf16 dense (cuBLAS GEMM)"
+    sp = spread(kms)
+    return {"bound": dom.bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "peak_kind": kind, "traffic": traffic,
+            "traffic_source": f"profiles/{dom.profile}" if traffic is not None else None,
+            "kernel": dom.kernel, "kernel_build": build_digest,
+            "kernel_us_mean": sp["us_mean"], "kernel_us_min": round(min(kms) * 1e3, 2),
+            "kernel_us_p10": sp["us_p10"], "kernel_us_median": sp["us_median"],
+            "kernel_us_p90": sp["us_p90"],
+            "timed_by": ("library stage events around the kernel" if dom.kernel_ms
+                         else "CUDA events around the call") + ", a separate timed pass of K steps",
+            "call_us_mean": round(call_ms * 1e3, 2)}
+
+
+def l2_flush_buffer(dev):
+    """An int32 buffer over twice the L2 (written before each cold step)."""
+    import torch
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)) or (129 << 20)
+    return torch.empty(2 * l2 // 4 + 1024, dtype=torch.int32, device=dev), l2
+
+
+def e2e_run(job, steps, warmup, stream):
+    """The same metric through the public API with host buffers, every step: H2D of q
+    from pinned memory, bsr_attn_run, D2H of out and lse, and a host wait for them.
+    Pipelined as a serving loop would run it: the page table of step i + 1 depends only
+    on the lengths, so it is planned on the host while the GPU runs step i; q of step
+    i + 1 is uploaded after the result of step i has been read back.  The serialised
+    form (plan, then copy, run, read) is timed too."""
+    plan, launch = job["e2e"]
+    for _ in range(max(1, warmup)):
+        plan()
+        launch()
+        stream.synchronize()
+    gc.collect()
+    n = max(3, min(5 * steps, 100))
+    plan()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        launch()
+        plan()                   # the next step's table, while the GPU runs this one
+        stream.synchronize()     # this step's out / lse are on the host
+    piped_ms = (time.perf_counter() - t0) * 1e3 / n
+    serial = []
+    for _ in range(n):
+        t = time.perf_counter()
+        plan()
+        launch()
+        stream.synchronize()
+        serial.append((time.perf_counter() - t) * 1e3)
+    h2d, d2h = job["e2e_bytes"]()
+    return {"value": round(job["numerator"] / (piped_ms * 1e-3) / job["scale"], 1),
+            "unit": job["unit"], "ms_per_step": round(piped_ms, 4), "steps": n,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "includes": "per step: plan of the page table (overlapping the previous step's "
+                        "kernel), H2D of q and of the plan, run, D2H of out and lse, host wait",
+            "serial": {"value": round(job["numerator"] / (statistics.mean(serial) * 1e-3) / job["scale"], 1),
+                       "ms_per_step": round(statistics.mean(serial), 4),
+                       "ms_per_step_median": round(statistics.median(serial), 4),
+                       "includes": "plan, then H2D q + run + D2H out/lse, host wait"}}
+
+
+def measure_config(cfg, dev, args, stream, flush, bsr, _build):
+    """Hot and cold-L2 timings, per-kernel times and the roofline of one more workload."""
+    import torch
+    job = build_job(cfg, dev, False)
+    parts = job["parts"]
+
+    def step():
+        for pt in parts:
+            pt.fn()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    hot = timed_steps(step, args.steps, stream)
+    cold = timed_steps(step, args.steps, stream, flush)
+    kernel_pass(parts, args.steps, stream, bsr)
+    for s in job["schedules"]:
+        assert bsr.bsr_last_device_error(s) == 0
+    unit, num, scale = job["unit"], job["numerator"], job["scale"]
+    res = {"workload": job["config"]["workload"], "metric": job["metric"], "unit": unit,
+           "hot": dict(spread(hot), value=round(num / (statistics.median(hot) * 1e-3) / scale, 1)),
+           "cold": dict(spread(cold), value=round(num / (statistics.median(cold) * 1e-3) / scale, 1)),
+           "roofline": roofline_of(parts, _build),
+           "kernels_us": {f"{pt.label}.{name}": round(sum(v) / len(v) * 1e3, 2)
+                          for pt in parts for name, v in pt.stage_ms.items()},
+           "config": job["config"]}
+    if "e2e" in job:
+        res["e2e"] = e2e_run(job, args.steps, args.warmup, stream)
+    if cfg in (1, 2) and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(job["workload"], budget_s=2.0)
+        one = cpu_baseline(job["workload"], budget_s=2.0, threads=1)
+        res["cpu_baseline"]["single_thread"] = {"value": one["value"], "unit": one["unit"],
+                                                "sample": one["sample"]}
+    del job, parts
+    gc.collect()
+    torch.cuda.empty_cache()
+    return res
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
@@ -477,13 +787,13 @@ def main():
     if args.impl == "reference":
         return run_reference(args, rank, world)
 
-    import workloads as wl
     import block_sparse_kv_bsr_gb300 as bsr
     from block_sparse_kv_bsr_gb300 import _build
     _build.build()
     bsr.load()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    t_begin = time.time()
 
     job = build_job(args.config, dev, args.small)
     parts = job["parts"]
@@ -501,7 +811,7 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local).start()
+    clocks = clock_sampler(local)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks.mark_start()
@@ -516,89 +826,26 @@ def main():
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
 
-    # ---- region 2: K more steps timed per call (CUDA events around each library call)
-    # and per kernel (the library's own events around each kernel of a bsr_attn_run
-    # call); these records sit between kernels, so they are kept out of region 1
-    for pt in parts:
-        if pt.sched is not None:
-            bsr.bsr_schedule_set_stage_timing(pt.sched, args.steps)
-    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in parts] for _ in range(args.steps)]
-    for row in evs:
-        for pt, (a, b) in zip(parts, row):
-            a.record(stream)
-            pt.fn()
-            b.record(stream)
-    torch.cuda.synchronize()
-    for row in evs:
-        for pt, (a, b) in zip(parts, row):
-            pt.ms.append(a.elapsed_time(b))
-    for pt in parts:
-        if pt.sched is not None:
-            for call in range(args.steps):
-                t = bsr.bsr_schedule_stage_times(pt.sched, call)
-                if pt.stage in t:
-                    pt.kernel_ms.append(t[pt.stage])
-                for name, ms in t.items():
-                    pt.stage_ms.setdefault(name, []).append(ms)
-            bsr.bsr_schedule_set_stage_timing(pt.sched, 0)
+    # ---- region 2: per call and per kernel (library stage events)
+    kernel_pass(parts, args.steps, stream, bsr)
     ms_step = max_over_ranks(total_ms / args.steps, world, dev)
     for s in job["schedules"]:
         assert bsr.bsr_last_device_error(s) == 0
 
-    # ---- end to end through the public API with host buffers
-    e2e = None
-    if "e2e" in job:
-        for _ in range(max(1, args.warmup)):
-            job["e2e"]()
-        # every step ends in a host read of its result, so each is timed on its own;
-        # a collection first keeps a full garbage-collector pass out of the timed steps
-        gc.collect()
-        e2e_steps = max(3, min(5 * args.steps, 100))
-        times = []
-        for _ in range(e2e_steps):
-            t0 = time.perf_counter()
-            job["e2e"]()
-            times.append((time.perf_counter() - t0) * 1e3)
-        e2e_ms = sum(times) / len(times)
-        h2d, d2h = job["e2e_bytes"]()
-        e2e = {"value": round(job["numerator"] / (e2e_ms * 1e-3) / job["scale"], 1),
-               "unit": job["unit"], "ms_per_step": round(e2e_ms, 4),
-               "ms_per_step_median": round(statistics.median(times), 4),
-               "ms_per_step_max": round(max(times), 4), "steps": e2e_steps,
-               "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h,
-               "includes": "re-plan from host page table + H2D q + run + D2H out/lse"}
+    # ---- the same steps one by one, hot and after an L2 flush
+    flush, l2_bytes = l2_flush_buffer(dev)
+    hot = timed_steps(step, args.steps, stream)
+    cold = timed_steps(step, args.steps, stream, flush)
 
-    peak_hbm, hbm_kind = peaks()
-    peak_tensor, tensor_kind = tensor_peak()
-    # the roofline reports the call that takes the most time in a step (among the calls
-    # of the attention kernels: a short timed region can make a setup call look longest)
-    dom = max([pt for pt in parts if pt.family is not None] or parts, key=lambda pt: sum(pt.ms))
-    call_ms = sum(dom.ms) / len(dom.ms)
-    # the kernel's own duration (library stage events) where the call launches more than one
-    kms = dom.kernel_ms if dom.kernel_ms else dom.ms
-    dom_ms = sum(kms) / len(kms)
-    deciles = (statistics.quantiles(kms, n=10, method="inclusive") if len(kms) > 1
-               else [kms[0]] * 9)
-    sources = {"decode": _build.DECODE_KERNEL_SOURCES,
-               "decode_kv8": _build.DECODE_KV8_KERNEL_SOURCES,
-               "prefill": _build.PREFILL_KERNEL_SOURCES}.get(dom.family)
-    build_digest = _build.kernel_digest(sources) if sources else None
-    traffic = None
-    if dom.profile is not None:
-        traffic = traffic_from_profile(dom.profile, build_digest)
-    if dom.bound == "hbm":
-        achieved, peak, unit, kind = dom.work / (dom_ms * 1e-3) / 1e9, peak_hbm, "GB/s", hbm_kind
-        kind = f"{kind} hbm_gbs (copy)"
-    else:
-        achieved, peak, unit = dom.work / (dom_ms * 1e-3) / 1e12, peak_tensor, "TFLOP/s"
-        kind = f"{tensor_kind} bf16 dense (cuBLAS GEMM)"
+    # ---- end to end through the public API with host buffers
+    e2e = e2e_run(job, args.steps, args.warmup, stream) if "e2e" in job else None
+
     value = job["numerator"] * world / (ms_step * 1e-3) / job["scale"]
+    unit, num, scale = job["unit"], job["numerator"], job["scale"]
     res = {
         "metric": job["metric"],
         "value": round(value, 1),
-        "unit": job["unit"],
+        "unit": unit,
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
@@ -610,19 +857,11 @@ def main():
         "dtype": job.get("dtype", "bf16"),
         "data": "synthetic (seeded N(0,1) bf16, page table drawn per workloads/)",
         "config": dict(job["config"], parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
-        "roofline": {"bound": dom.bound, "achieved": round(achieved, 1), "peak": peak,
-                     "unit": unit, "frac": round(achieved / peak, 4), "peak_kind": kind,
-                     "traffic": traffic, "traffic_source": (f"profiles/{dom.profile}"
-                                                            if traffic is not None else None),
-                     "kernel": dom.kernel, "kernel_build": build_digest,
-                     "kernel_us_mean": round(dom_ms * 1e3, 2),
-                     "kernel_us_min": round(min(kms) * 1e3, 2),
-                     "kernel_us_p10": round(deciles[0] * 1e3, 2),
-                     "kernel_us_median": round(statistics.median(kms) * 1e3, 2),
-                     "kernel_us_p90": round(deciles[-1] * 1e3, 2),
-                     "timed_by": ("library stage events around the kernel" if dom.kernel_ms
-                                  else "CUDA events around the call") + ", second timed pass of K steps",
-                     "call_us_mean": round(call_ms * 1e3, 2)},
+        "roofline": roofline_of(parts, _build),
+        "hot": dict(spread(hot), value=round(num / (statistics.median(hot) * 1e-3) / scale, 1)),
+        "cold": dict(spread(cold), value=round(num / (statistics.median(cold) * 1e-3) / scale, 1),
+                     flush=f"write of {2 * l2_bytes >> 20} MiB (2x L2) before each step, "
+                           "outside its events"),
         "parts_us": {pt.label: round(sum(pt.ms) / len(pt.ms) * 1e3, 2) for pt in parts},
         "kernels_us": {f"{pt.label}.{name}": round(sum(v) / len(v) * 1e3, 2)
                        for pt in parts for name, v in pt.stage_ms.items()},
@@ -647,6 +886,22 @@ def main():
             one = cpu_baseline(job["workload"], budget_s=3.0, threads=1)
             res["cpu_baseline"]["single_thread"] = {"value": one["value"], "unit": one["unit"],
                                                     "sample": one["sample"]}
+    del job, parts
+    gc.collect()
+    torch.cuda.empty_cache()
+
+    # ---- the other workloads (the benchmark spec's five configurations first, then the extended
+    # ones), each hot and cold, on rank 0 of a single-GPU run
+    if world == 1 and args.configs:
+        res["configs"] = {}
+        for cfg in args.configs:
+            if cfg == args.config:
+                continue
+            if time.time() - t_begin > args.time_budget:
+                res["configs"][str(cfg)] = {"skipped": f"bench time budget of {args.time_budget} s spent"}
+                continue
+            res["configs"][str(cfg)] = measure_config(cfg, dev, args, stream, flush, bsr, _build)
+    res["bench_wall_s"] = round(time.time() - t_begin, 1)
     if rank == 0:
         print(json.dumps(res))
     if world > 1:

@@ -50,3 +50,72 @@ def test_traffic_needs_the_matching_build(tmp_path, monkeypatch):
     assert bench.traffic_from_profile("k.md", "abcdef0123456789") == 123456.0
     assert bench.traffic_from_profile("k.md", "0000000000000000") is None
     assert bench.traffic_from_profile("missing.md", "abcdef0123456789") is None
+
+
+class _FakeNvml:
+    """Stands in for libnvidia-ml: a clock and a clock-event reason mask per call."""
+
+    def __init__(self, clocks, reasons):
+        self.clocks, self.reasons = iter(clocks), iter(reasons)
+
+    def nvmlDeviceGetClockInfo(self, h, kind, out):
+        out._obj.value = next(self.clocks)
+        return 0
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h, out):
+        out._obj.value = next(self.reasons)
+        return 0
+
+
+def test_nvml_clock_record_and_reasons():
+    c = bench.NvmlClocks.__new__(bench.NvmlClocks)
+    c.period, c.samples, c.max_mhz, c.h = 0.0005, [], 2070.0, None
+    c.lib = _FakeNvml([2070, 1965, 2070, 2070], [0x0, 0x4, 0x8 | 0x40, 0x1])
+    c._reasons_fn = c.lib.nvmlDeviceGetCurrentClocksEventReasons
+    clock = iter([1.0, 2.0, 3.0, 4.0])
+    real = bench.time.time
+    bench.time.time = lambda: next(clock)
+    try:
+        for _ in range(4):
+            c._sample()
+    finally:
+        bench.time.time = real
+    c.t0, c.t1 = 1.5, 3.5
+    r = c.summary()
+    assert r["samples"] == 2 and r["sm_mhz_min"] == 1965 and r["sm_max_mhz"] == 2070
+    assert r["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap"]
+    c.t0, c.t1 = 10.0, 11.0
+    assert c.summary()["samples"] == 0
+
+
+def test_spread_of_timings():
+    r = bench.spread([1.0, 2.0, 3.0, 4.0, 5.0])
+    assert r["us_median"] == 3000.0 and r["us_mean"] == 3000.0
+    assert r["us_p10"] == 1400.0 and r["us_p90"] == 4600.0
+    assert bench.spread([0.5])["us_p90"] == 500.0
+
+
+def test_e2e_plans_the_next_step_while_the_gpu_runs():
+    """Pipelined e2e: each step launches its copies and kernel, plans the next step's
+    table on the host, then waits for its own result; every step has its copies."""
+    log = []
+    stream = types.SimpleNamespace(synchronize=lambda: log.append("sync"))
+    job = {"e2e": (lambda: log.append("plan"), lambda: log.append("launch")),
+           "e2e_bytes": lambda: (100, 50), "numerator": 1e9, "scale": 1e9, "unit": "GB/s"}
+    r = bench.e2e_run(job, steps=1, warmup=1, stream=stream)
+    n = r["steps"]
+    piped = log[3:3 + 1 + 3 * n]     # after the warm-up's plan, launch, sync
+    assert piped[0] == "plan" and piped[1:] == ["launch", "plan", "sync"] * n
+    assert log[3 + 1 + 3 * n:] == ["plan", "launch", "sync"] * n
+    assert r["h2d_bytes_per_step"] == 100 and r["d2h_bytes_per_step"] == 50
+
+
+def test_cascade_split_evens_out_the_levels():
+    """The prefix level's SM share grows with its FLOPs and shrinks as the suffix's bytes
+    grow, and always leaves both levels at least 8 SMs."""
+    a = bench.cascade_prefix_sms(152, 34.4e9, 578e6)
+    assert 8 <= a <= 144
+    assert bench.cascade_prefix_sms(152, 2 * 34.4e9, 578e6) > a
+    assert bench.cascade_prefix_sms(152, 34.4e9, 2 * 578e6) < a
+    assert bench.cascade_prefix_sms(152, 1e3, 1e12) == 8
+    assert bench.cascade_prefix_sms(152, 1e15, 1e3) == 144

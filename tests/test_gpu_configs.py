@@ -58,6 +58,40 @@ def test_cascade_small_equals_flat(level_dtype):
     assert_lse_close(l.cpu().numpy(), rl, "cascade")
 
 
+def test_cascade_levels_side_by_side():
+    """The prefix level planned on a share of the SMs (bsr_schedule_create) and run on a
+    second stream while the suffix level runs on the other SMs, then merged: the result
+    equals flat attention over prefix + suffix, and each schedule kept to its SMs."""
+    c = wl.config4(small=True)
+    dev = "cuda:0"
+    n = torch.cuda.get_device_properties(0).multi_processor_count
+    sp = plan(c.prefix, bsr.bsr_schedule_create(n // 3))
+    ss = plan(c.suffix, bsr.bsr_schedule_create(n - n // 3))
+    assert sp.info()["num_sms"] == n // 3 and ss.info()["num_sms"] == n - n // 3
+    assert sp.info()["prefill_ctas"] <= n // 3
+    assert ss.info()["decode_ctas"] <= n - n // 3
+    q = c.suffix.q.to(dev)
+    pk, pv = c.prefix.k_pages.to(dev), c.prefix.v_pages.to(dev)
+    sk, sv = c.suffix.k_pages.to(dev), c.suffix.v_pages.to(dev)
+    side = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    fork, join = torch.cuda.Event(), torch.cuda.Event()
+    fork.record(main)
+    side.wait_event(fork)
+    op, lp = bsr.bsr_attn_run(sp, q, pk, pv, sm_scale=c.prefix.sm_scale, out_dtype=torch.float32,
+                              stream=side)
+    join.record(side)
+    os_, ls = bsr.bsr_attn_run(ss, q, sk, sv, sm_scale=c.suffix.sm_scale,
+                               out_dtype=torch.float32)
+    main.wait_event(join)
+    o, l = bsr.bsr_merge_states(op, lp, os_, ls)
+    torch.cuda.synchronize()
+    assert bsr.bsr_last_device_error(sp) == 0 and bsr.bsr_last_device_error(ss) == 0
+    ro, rl = oracle_full(wl.flat_cascade(c))
+    assert_out_close(o.float().cpu().numpy(), ro, False, "cascade side by side")
+    assert_lse_close(l.cpu().numpy(), rl, "cascade side by side")
+
+
 def test_cascade_full_size_sampled():
     c = wl.config4()
     o, l = run_cascade(c, torch.float32)
