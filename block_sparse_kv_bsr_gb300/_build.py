@@ -50,9 +50,12 @@ def _digest() -> str:
 
 
 # Sources that determine a kernel family's machine code (for matching a profile to a build).
-DECODE_KERNEL_SOURCES = ("bsr_decode.cuh", "bsr_decode_d128.cu", "bsr_internal.h", "ptx.cuh")
-PREFILL_KERNEL_SOURCES = ("bsr_prefill.cu", "bsr_internal.h", "ptx.cuh", "umma.cuh")
-DECODE_KV8_KERNEL_SOURCES = ("bsr_decode_kv8.cu", "bsr_decode.cuh", "bsr_internal.h", "ptx.cuh")
+DECODE_KERNEL_SOURCES = ("bsr_decode.cuh", "bsr_decode_d128.cu", "bsr_internal.h", "ptx.cuh",
+                         "bsr_launch.cuh")
+PREFILL_KERNEL_SOURCES = ("bsr_prefill.cu", "bsr_internal.h", "ptx.cuh", "umma.cuh",
+                          "bsr_launch.cuh")
+DECODE_KV8_KERNEL_SOURCES = ("bsr_decode_kv8.cu", "bsr_decode.cuh", "bsr_internal.h", "ptx.cuh",
+                             "bsr_launch.cuh")
 
 
 _COMMENT = re.compile(rb"//[^\n]*|/\*.*?\*/", re.S)

@@ -44,6 +44,7 @@
 #include <cstdint>
 
 #include "bsr_internal.h"
+#include "bsr_launch.cuh"
 #include "ptx.cuh"
 
 namespace bsr {
@@ -221,6 +222,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   constexpr int NT = C::kNTiles;
   constexpr int KH = KS / 2;            // k-steps in the first half of the head dim
   extern __shared__ uint8_t smem_raw[];
+  // launched as a programmatic dependent: let the next grid start its set-up, and touch
+  // no global memory before the previous grid has completed
+  pdl_trigger();
+  pdl_wait();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;

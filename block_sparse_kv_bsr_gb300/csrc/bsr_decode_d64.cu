@@ -25,8 +25,8 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
     if (e != cudaSuccess) return e;
     opted_in[dev].store(true, std::memory_order_release);
   }
-  kern<<<grid, kDecodeWarps * 32, smem, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  const cudaError_t le = launch_pdl(kern, grid, kDecodeWarps * 32, smem, stream, tk, tv, p);
+  return le != cudaSuccess ? le : cudaGetLastError();
 }
 }  // namespace
 

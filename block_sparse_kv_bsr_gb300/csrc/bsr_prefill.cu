@@ -55,6 +55,7 @@
 #include <cstdint>
 
 #include "bsr_internal.h"
+#include "bsr_launch.cuh"
 #include "bsr_schedule.h"
 #include "ptx.cuh"
 #include "umma.cuh"
@@ -248,6 +249,9 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = Smem;
   extern __shared__ uint8_t smem_raw[];
+  // launched as a programmatic dependent (see bsr_launch.cuh)
+  pdl_trigger();
+  pdl_wait();
   const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bar0 = base + L::kBars;
@@ -845,6 +849,9 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
 // chunks are loaded before the weights are known, so the loads overlap.
 constexpr int kMergeWarps = 8;
 __global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(const PrefillMergeParams p) {
+  // launched as a programmatic dependent of the prefill kernel, whose partial states it reads
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int kCtasPerUnit = kUnitRows / kMergeWarps;
   const int unit = blockIdx.x / kCtasPerUnit;
@@ -923,8 +930,8 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
     if (e != cudaSuccess) return e;
     opted_in[dev].store(true, std::memory_order_release);
   }
-  kern<<<grid, threads_of<ROPE>(), smem, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  const cudaError_t le = launch_pdl(kern, grid, threads_of<ROPE>(), smem, stream, tq, tk, tv, p);
+  return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 }  // namespace
@@ -942,8 +949,8 @@ cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& 
 cudaError_t launch_prefill_merge(const PrefillMergeParams& p, cudaStream_t stream) {
   const int64_t grid = int64_t(p.n_units) * (kUnitRows / kMergeWarps);
   if (grid <= 0) return cudaSuccess;
-  bsr_prefill_merge_kernel<<<int(grid), kMergeWarps * 32, 0, stream>>>(p);
-  return cudaGetLastError();
+  const cudaError_t le = launch_pdl(bsr_prefill_merge_kernel, int(grid), kMergeWarps * 32, 0, stream, p);
+  return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 }  // namespace bsr
