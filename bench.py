@@ -66,9 +66,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--small", action="store_true", help="small case (profiling, smoke)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10],
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11],
                     help="workload; 3 (skewed block-sparse decode) is the headline")
-    ap.add_argument("--configs", default="1,2,4,5,6,7,8,9,10",
+    ap.add_argument("--configs", default="1,2,4,5,6,7,8,9,10,11",
                     help="further workloads measured after the headline (comma list; '' for none)")
     ap.add_argument("--time-budget", type=float, default=240.0,
                     help="seconds after which further workloads are skipped (and listed as such)")
@@ -352,15 +352,17 @@ def attention_flops(w) -> int:
     return total * w.num_qo_heads * 4 * w.head_dim
 
 
-def cascade_prefix_sms(num_sms: int, prefix_flops: float, suffix_bytes: float) -> int:
+def cascade_prefix_sms(num_sms: int, prefix_flops: float, suffix_bytes: float,
+                       prefix_levels: int = 1) -> int:
     """SMs for a cascade's tensor-core prefix level when it runs beside the HBM-bound
     suffix level on the other SMs: the split that evens out the two levels' times, from
-    per-SM rates measured on GB300 (the prefill kernel ~5.3 TFLOP/s per SM; the decode
-    kernel streams ~55 GB/s per SM, ~6.3 TB/s at most over the whole GPU)."""
+    rates measured on GB300 with the levels side by side (the prefill kernel ~5.2 TFLOP/s
+    per SM plus ~12 us per prefix level for merging its split ranges; the decode kernel
+    streams ~58 GB/s per SM, ~6.3 TB/s at most over the whole GPU)."""
     best = (float("inf"), num_sms // 2)
     for s1 in range(8, num_sms - 7):
-        t = max(prefix_flops / (s1 * 5.3e12),
-                suffix_bytes / min((num_sms - s1) * 55e9, 6.3e12))
+        t = max(prefix_flops / (s1 * 5.2e12) + 12e-6 * prefix_levels,
+                suffix_bytes / min((num_sms - s1) * 58e9, 6.3e12))
         if t < best[0]:
             best = (t, s1)
     return best[1]
@@ -431,20 +433,21 @@ def build_job(cfg: int, dev, small: bool):
         job["e2e"] = (lambda: plan(w, s), e2e_launch)
         job["e2e_bytes"] = lambda: (q.numel() * 2 + int(s.info()["upload_bytes"]),
                                     out.numel() * 2 + lse.numel() * 4)
-    elif cfg == 6:
-        w = wl.config6(small)
+    elif cfg in (6, 11):
+        w = wl.config6(small) if cfg == 6 else wl.config11(small)
         q = w.q.to(dev)
         k, v = w.k_codes.to(dev), w.v_codes.to(dev)
         out = torch.empty_like(q)
         lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
         s = plan(w)
         run = lambda: bsr.bsr_attn_run_kv8(s, q, k, v, k_scale=w.k_scale, v_scale=w.v_scale,
-                                           sm_scale=w.sm_scale, causal=w.causal, out=out, lse=lse)
+                                           sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+                                           causal=w.causal, out=out, lse=lse)
         alg = wl.algorithmic_bytes(w)
         job["parts"] = [Part("decode", run, "bsr_decode_kv8_kernel", "hbm", alg, "B",
                              launches=s.info()["kernels_per_run"], sched=s, stage="decode",
                              family="decode_kv8",
-                             profile=None if small else "bsr_decode_kv8_skewed_b128.md")]
+                             profile=None if small or cfg == 11 else "bsr_decode_kv8_skewed_b128.md")]
         job["schedules"] = [s]
         job["dtype"] = "f16 MMA on E4M3 codes, fp32 accumulate"
         job.update(workload=w, metric=METRIC, unit="GB/s", numerator=alg, scale=1e9,
@@ -452,7 +455,8 @@ def build_job(cfg: int, dev, small: bool):
                            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
                            "page_size": w.page_size, "active_kv_tokens": w.active_tokens,
                            "kv_cache": "E4M3 codes + per-pool scales (q, out bf16)",
-                           "algorithmic_bytes": alg, "drop": "25% of non-final pages",
+                           "algorithmic_bytes": alg, "rope_theta": w.rope_theta,
+                           "drop": "25% of non-final pages" if cfg == 6 else "none",
                            "l2": "inputs larger than L2, no flush"})
         q_host = w.q.pin_memory()
         out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -462,7 +466,8 @@ def build_job(cfg: int, dev, small: bool):
         def e2e_launch():
             q_dev.copy_(q_host, non_blocking=True)
             bsr.bsr_attn_run_kv8(s, q_dev, k, v, k_scale=w.k_scale, v_scale=w.v_scale,
-                                 sm_scale=w.sm_scale, causal=w.causal, out=out, lse=lse)
+                                 sm_scale=w.sm_scale, rope_theta=w.rope_theta, causal=w.causal,
+                                 out=out, lse=lse)
             out_host.copy_(out, non_blocking=True)
             lse_host.copy_(lse, non_blocking=True)
 
@@ -529,38 +534,63 @@ def build_job(cfg: int, dev, small: bool):
     elif cfg == 9:
         c = wl.config9(small)
         q = c.levels[0].q.to(dev)
-        parts, scheds, alg = [], [], 0
         st = q.shape[0] * q.shape[1] * (q.shape[2] + 1) * 4          # one fp32 state
-        outs = []
+        n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        # levels on the tensor-core kernel run one after the other on a second stream and
+        # an SM share, beside the decode level on the other SMs (as for the cascade above)
+        is_pre = [plan(w).info()["num_prefill_items"] > 0 for w in c.levels]
+        kvb = [w.active_tokens * 2 * w.num_kv_heads * w.head_dim * 2 for w in c.levels]
+        s_pre = cascade_prefix_sms(
+            n_sms, sum(attention_flops(w) for w, pr in zip(c.levels, is_pre) if pr),
+            sum(kv + q.numel() * 2 + st for kv, pr in zip(kvb, is_pre) if not pr),
+            prefix_levels=sum(is_pre))
+        side = torch.cuda.Stream(dev)
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+        parts, scheds, outs, alg = [], [], [], 0
         for i, w in enumerate(c.levels):
             k, v = w.k_pages.to(dev), w.v_pages.to(dev)
             o_i = torch.empty(q.shape, dtype=torch.float32, device=dev)
             l_i = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-            s = plan(w)
-            pre = s.info()["num_prefill_items"] > 0
-            kv = w.active_tokens * 2 * w.num_kv_heads * w.head_dim * 2
-            fn = (lambda s=s, k=k, v=v, w=w, o_i=o_i, l_i=l_i:
-                  bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, out=o_i, lse=l_i))
+            pre = is_pre[i]
+            s = plan(w, bsr.bsr_schedule_create(s_pre if pre else n_sms - s_pre))
+            first_pre = pre and not any(is_pre[:i])
+
+            def fn(s=s, k=k, v=v, w=w, o_i=o_i, l_i=l_i, pre=pre, first_pre=first_pre):
+                if pre and first_pre:
+                    fork.record(torch.cuda.current_stream())
+                    side.wait_event(fork)
+                bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, out=o_i, lse=l_i,
+                                 stream=side if pre else None)
+
             parts.append(Part(f"level{i + 1}", fn,
                               "bsr_prefill_kernel<0>" if pre else "bsr_decode_kernel<128,0,0,0>",
                               "tensor" if pre else "hbm",
-                              attention_flops(w) if pre else kv + q.numel() * 2 + st,
+                              attention_flops(w) if pre else kvb[i] + q.numel() * 2 + st,
                               "FLOP" if pre else "B", launches=s.info()["kernels_per_run"],
                               sched=s, stage="prefill" if pre else "decode",
                               family="prefill" if pre else "decode"))
             scheds.append(s)
             outs.append((o_i, l_i))
-            alg += kv
+            alg += kvb[i]
         acc_o = torch.empty(q.shape, dtype=torch.float32, device=dev)
         acc_l = torch.empty(q.shape[:2], dtype=torch.float32, device=dev)
-        parts.append(Part("merge12", lambda: bsr.bsr_merge_states(outs[0][0], outs[0][1],
-                                                                  outs[1][0], outs[1][1],
-                                                                  o_out=acc_o, lse_out=acc_l),
-                          "merge_states_kernel<128,1>", "hbm", 3 * st, "B"))
-        parts.append(Part("merge123", lambda: bsr.bsr_merge_states(acc_o, acc_l, outs[2][0],
-                                                                   outs[2][1], o_out=acc_o,
-                                                                   lse_out=acc_l),
-                          "merge_states_kernel<128,1>", "hbm", 3 * st, "B"))
+        # the two shared levels merge on the second stream; the result joins the last level
+        pair_stream = side if is_pre[0] and is_pre[1] else None
+
+        def merge12():
+            bsr.bsr_merge_states(outs[0][0], outs[0][1], outs[1][0], outs[1][1], o_out=acc_o,
+                                 lse_out=acc_l, stream=pair_stream)
+            if pair_stream is not None:
+                join.record(side)
+
+        def merge123():
+            if pair_stream is not None:
+                torch.cuda.current_stream().wait_event(join)
+            bsr.bsr_merge_states(acc_o, acc_l, outs[2][0], outs[2][1], o_out=acc_o,
+                                 lse_out=acc_l)
+
+        parts.append(Part("merge12", merge12, "merge_states_kernel<128,1>", "hbm", 3 * st, "B"))
+        parts.append(Part("merge123", merge123, "merge_states_kernel<128,1>", "hbm", 3 * st, "B"))
         job["parts"] = parts
         job["schedules"] = scheds
         alg += q.numel() * 2 + st
@@ -570,8 +600,10 @@ def build_job(cfg: int, dev, small: bool):
                            "levels": [{"segments": w.batch, "tokens": w.active_tokens,
                                        "page_size": w.page_size} for w in c.levels],
                            "algorithmic_bytes": alg,
-                           "composition": "system prefix + group prefixes (tensor cores) + "
-                                          "suffixes (decode), LSE-merged level by level"})
+                           "composition": "system prefix + group prefixes (tensor cores, one "
+                                          "after the other on a second stream) beside the "
+                                          "suffixes (decode), LSE-merged level by level",
+                           "sm_split": {"prefix_levels": s_pre, "decode_level": n_sms - s_pre}})
     elif cfg == 5:
         w = wl.config5(small)
         q, k, v = w.q.to(dev), w.k_pages.to(dev), w.v_pages.to(dev)
@@ -880,7 +912,7 @@ def main():
                        "imbalance": round(max(info["decode_imbalance"], info["prefill_imbalance"]), 4)}
     # the oracle on the host cores, for the decode workloads (a pass takes well under a
     # second there); on the tiny and the Llama-8B-shaped ones also on one thread
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.config in (1, 2, 3, 6, 7, 8, 10):
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.config in (1, 2, 3, 6, 7, 8, 10, 11):
         res["cpu_baseline"] = cpu_baseline(job["workload"])
         if args.config in (1, 2):
             one = cpu_baseline(job["workload"], budget_s=3.0, threads=1)
@@ -935,7 +967,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     import workloads as wl
-    w = wl.by_name(args.config if args.config in (1, 2, 3, 6, 7, 8, 10) else 3, args.small)
+    w = wl.by_name(args.config if args.config in (1, 2, 3, 6, 7, 8, 10, 11) else 3, args.small)
     t_pass = 0.0
     for _ in range(max(args.warmup, 1)):
         t = time.perf_counter()

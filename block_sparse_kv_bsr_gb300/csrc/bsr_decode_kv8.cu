@@ -54,7 +54,13 @@ constexpr int kStage8 = 2 * kTile8;
 constexpr int kStages8 = BSR_DECODE_STAGES_KV8;
 constexpr size_t kSmem8 = size_t(kDecodeWarps) * kStages8 * kStage8 +
                           size_t(kDecodeWarps) * kStages8 * 8 + 1024;
-static_assert(kSmem8 <= 232448, "FP8 decode stages exceed the shared memory of one SM");
+// RoPE: one table row per stage (the angles of the stage's first key, pair order:
+// D / 4 float4 (cos f, cos f+1, sin f, sin f+1)) beside the ring, and the CTA's 16
+// offset rows t < 16 (times the operand scale)
+constexpr int kRowBytes8 = kD8 / 4 * 16;
+constexpr size_t kSmem8Rope = kSmem8 + size_t(kDecodeWarps) * kStages8 * kRowBytes8 +
+                              size_t(kStageTokens) * kRowBytes8;
+static_assert(kSmem8Rope <= 232448, "FP8 decode stages exceed the shared memory of one SM");
 
 // Byte offset of (token t, 16-byte chunk c of 8) in a [16 rows][128 B] tile with
 // the TMA 128-byte swizzle.
@@ -75,7 +81,22 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return ptx::pack_f16(ptx::bf16_lo(v), ptx::bf16_hi(v));
 }
 
-template <bool R16, bool WIN>
+__device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t v) {
+  float2 r;
+  asm("{\n\t.reg .f16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+      "cvt.f32.f16 %0, lo;\n\tcvt.f32.f16 %1, hi;\n\t}" : "=f"(r.x), "=f"(r.y) : "r"(v));
+  return r;
+}
+
+// RoPE on a pair of frequencies (f, f + 1): x are dims f, f + 1, y their rotate-half
+// partners; (c, s) the angles' cosines and sines.  x <- x c - y s, y <- y c + x s.
+__device__ __forceinline__ void rotate2(float2& x, float2& y, float2 c, float2 s) {
+  const float2 u = ptx::fsub2(ptx::fmul2(x, c), ptx::fmul2(y, s));
+  y = ptx::ffma2(y, c, ptx::fmul2(x, s));
+  x = u;
+}
+
+template <bool R16, bool WIN, bool ROPE>
 __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     bsr_decode_kv8_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
@@ -84,14 +105,34 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   constexpr int KB = D / 16;            // 16-dim blocks
   constexpr int NT = D / 8;             // n-tiles of the output
   extern __shared__ uint8_t smem_raw[];
+  // launched as a programmatic dependent (see bsr_launch.cuh)
+  pdl_trigger();
+  pdl_wait();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
+  uint8_t* const base_ptr = smem_raw + (base - ptx::smem_u32(smem_raw));
+  // RoPE: this warp's per-stage table rows, then the CTA's offset rows
+  const uint32_t grows = base + uint32_t(kDecodeWarps * kStages8 * (kStage8 + 8) +
+                                         warp * kStages8 * kRowBytes8);
+  const uint8_t* const grows_ptr = base_ptr + (grows - base);
+  uint8_t* const frows_ptr =
+      base_ptr + kDecodeWarps * kStages8 * (kStage8 + 8) + kDecodeWarps * kStages8 * kRowBytes8;
+  if constexpr (ROPE) {
+    const float4* src = reinterpret_cast<const float4*>(p.rope);
+    for (int i = threadIdx.x; i < kStageTokens * (kD8 / 4); i += kDecodeWarps * 32) {
+      const float4 v = __ldg(src + i);
+      reinterpret_cast<float4*>(frows_ptr)[i] =
+          make_float4(v.x * kRopeOperandScale, v.y * kRopeOperandScale, v.z * kRopeOperandScale,
+                      v.w * kRopeOperandScale);
+    }
+    __syncthreads();
+  }
   const int gw = blockIdx.x * kDecodeWarps + warp;
   if (gw >= p.num_warps) return;
   const int it_begin = __ldg(p.warp_ptr + gw), it_end = __ldg(p.warp_ptr + gw + 1);
   if (it_begin >= it_end) return;
 
-  const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   const uint32_t ring = base + uint32_t(warp * kStages8 * kStage8);
   const uint32_t bars = base + uint32_t(kDecodeWarps * kStages8 * kStage8 + warp * kStages8 * 8);
   if (lane == 0) {
@@ -108,13 +149,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   // Up to kStages8 stages ahead of the consumer; page ids of the next 32 stages
   // of the current unit sit one per lane in `win`.
   int p_it = it_begin, p_st = 0, p_nst = 0, win = 0, win_next = 0, win_base = 0;
+  int wpos = 0, wpos_next = 0;   // RoPE with page positions: the stages' first-key positions
   uint32_t p_seq = 0;
   DecodeItem pi;
+  const uint64_t pol_rope = ptx::policy_evict_normal();
   auto load_window = [&](const DecodeItem& it, int ws) -> int {
     const int s = ws + lane;
     if (s < stages_of(it))
       return __ldg(p.indices + it.page_base + ((it.tok0 + kStageTokens * s) >> log2P));
     return 0;
+  };
+  auto load_pos_window = [&](const DecodeItem& it, int ws) -> int {
+    const int s = ws + lane;
+    if (!ROPE || p.page_pos == nullptr || s >= stages_of(it)) return 0;
+    const int tok = it.tok0 + kStageTokens * s;
+    return __ldg(p.page_pos + it.page_base + (tok >> log2P)) + (tok & (p.P - 1));
   };
   auto producer_seek = [&]() {
     while (p_it < it_end) {
@@ -127,18 +176,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       win_base = 0;
       win = load_window(pi, 0);
       win_next = load_window(pi, 32);
+      if constexpr (ROPE) {
+        wpos = load_pos_window(pi, 0);
+        wpos_next = load_pos_window(pi, 32);
+      }
     }
   };
   auto producer_issue = [&]() {
     if (p_it >= it_end) return;
     const int slot = int(p_seq % kStages8);
     const int page = __shfl_sync(0xffffffffu, win, p_st - win_base);
+    const int spos = ROPE ? __shfl_sync(0xffffffffu, wpos, p_st - win_base) : 0;
     if (lane == 0) {
       const uint32_t bar = bars + 8 * slot;
       const uint32_t dk = ring + uint32_t(slot * kStage8), dv = dk + kTile8;
       const int tok = pi.tok0 + kStageTokens * p_st;
       const int row = (page * p.Hk + pi.kvh) * p.P + (tok & (p.P - 1));
-      ptx::mbar_arrive_expect_tx(bar, kStage8);
+      ptx::mbar_arrive_expect_tx(bar, kStage8 + (ROPE ? kRowBytes8 : 0));
+      if constexpr (ROPE) {
+        // the table row of the stage's first key: its index, or its logical position
+        const int rpos = min(p.page_pos ? spos : tok, p.rope_max_pos);
+        ptx::bulk_load(grows + uint32_t(slot * kRowBytes8),
+                       reinterpret_cast<const float4*>(p.rope) + size_t(rpos) * (kD8 / 4),
+                       kRowBytes8, bar, pol_rope);
+      }
       if (p.nhd) {   // token row page * P + slot, the head as the map's outer coordinate
         const int trow = page * p.P + (tok & (p.P - 1));
         ptx::tma_load_3d(dk, &tm_k, bar, 0, trow, pi.kvh, pol);
@@ -158,6 +219,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
       win_base += 32;
       win = win_next;
       win_next = load_window(pi, win_base + 32);
+      if constexpr (ROPE) {
+        wpos = wpos_next;
+        wpos_next = load_pos_window(pi, win_base + 32);
+      }
     }
   };
   producer_seek();
@@ -175,6 +240,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
   uint32_t c_seq = 0;
   bool failed = false;
+  float rmag = 0.f;   // RoPE: largest rotated q / k magnitude of a valid row or key
 #pragma unroll 1
   for (int c_it = it_begin; c_it < it_end; ++c_it) {
     const DecodeItem ci = load_item(p.items, c_it);
@@ -195,7 +261,42 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     // [kb][0] = row g4 dims 4t, 4t+1; [kb][NR/2] = row g4 dims 4t+2, 4t+3;
     // with R16 [kb][1] / [kb][3] the same for row g4 + 8.
     uint32_t qh[KB][NR];
-    {
+    if constexpr (ROPE) {
+      // rotate q at its (logical) position in fp32, then fp16 x 2^-4; dims 4t..4t+3 of
+      // block kb (< KB / 2) pair with the same dims of block kb + KB / 2
+      const int qsh = p.qshift != nullptr ? __ldg(p.qshift + ci.req) : 0;
+#pragma unroll
+      for (int rr = 0; rr < (R16 ? 2 : 1); ++rr) {
+        const int R = rr == 0 ? rA : rB;
+        const bool valid = rr == 0 ? vA : vB;
+        const uint16_t* qr =
+            p.q + (size_t(ci.q_row0 + R / group) * p.Hq + ci.kvh * group + R % group) * D;
+        const int pos = min(max(ci.qpos0 + R / group + qsh, 0), p.rope_max_pos);
+        const float4* tab = reinterpret_cast<const float4*>(p.rope) + size_t(pos) * (D / 4) + 2 * t4;
+        const int lo = rr == 0 ? 0 : 1, hi = rr == 0 ? NR / 2 : 3;
+#pragma unroll
+        for (int kb = 0; kb < KB / 2; ++kb) {
+          const int d0 = 16 * kb + 4 * t4;
+          const uint2 a = valid ? __ldg(reinterpret_cast<const uint2*>(qr + d0)) : make_uint2(0u, 0u);
+          const uint2 b = valid ? __ldg(reinterpret_cast<const uint2*>(qr + d0 + D / 2))
+                                : make_uint2(0u, 0u);
+          const float4 t01 = __ldg(tab + 8 * kb), t23 = __ldg(tab + 8 * kb + 1);
+          float2 x01 = make_float2(ptx::bf16_lo(a.x), ptx::bf16_hi(a.x));
+          float2 x23 = make_float2(ptx::bf16_lo(a.y), ptx::bf16_hi(a.y));
+          float2 y01 = make_float2(ptx::bf16_lo(b.x), ptx::bf16_hi(b.x));
+          float2 y23 = make_float2(ptx::bf16_lo(b.y), ptx::bf16_hi(b.y));
+          const float2 sc = make_float2(kRopeOperandScale, kRopeOperandScale);
+          rotate2(x01, y01, ptx::fmul2(make_float2(t01.x, t01.y), sc), ptx::fmul2(make_float2(t01.z, t01.w), sc));
+          rotate2(x23, y23, ptx::fmul2(make_float2(t23.x, t23.y), sc), ptx::fmul2(make_float2(t23.z, t23.w), sc));
+          rmag = ptx::fmax3(rmag, fmaxf(fabsf(x01.x), fabsf(x01.y)), fmaxf(fabsf(x23.x), fabsf(x23.y)));
+          rmag = ptx::fmax3(rmag, fmaxf(fabsf(y01.x), fabsf(y01.y)), fmaxf(fabsf(y23.x), fabsf(y23.y)));
+          qh[kb][lo] = ptx::pack_f16(x01.x, x01.y);
+          qh[kb][hi] = ptx::pack_f16(x23.x, x23.y);
+          qh[kb + KB / 2][lo] = ptx::pack_f16(y01.x, y01.y);
+          qh[kb + KB / 2][hi] = ptx::pack_f16(y23.x, y23.y);
+        }
+      }
+    } else {
       const uint16_t* qa =
           p.q + (size_t(ci.q_row0 + rA / group) * p.Hq + ci.kvh * group + rA % group) * D;
       const uint16_t* qb =
@@ -266,6 +367,66 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int r = 0; r < 4; ++r) sacc[s][n][r] = 0.f;
+      if constexpr (ROPE) {
+        // keys are rotated in registers: codes -> fp16 -> fp32, angle of key tok + t =
+        // angle of tok (the stage's table row) (+) angle of t (offset row), then fp16 x
+        // 2^-4.  A thread holds keys g4 (n-tile 0) and 8 + g4 (n-tile 1), dims 4 t4 ..
+        // 4 t4 + 3 of each block: block kb pairs with block kb + KB / 2.
+        const float4* fo[2] = {reinterpret_cast<const float4*>(frows_ptr + g4 * kRowBytes8) + 2 * t4,
+                               reinterpret_cast<const float4*>(frows_ptr + (g4 + 8) * kRowBytes8) + 2 * t4};
+#pragma unroll
+        for (int pr = 0; pr < KB / 4; ++pr) {
+          uint32_t kl[NS][4], kh[NS][4];
+#pragma unroll
+          for (int s = 0; s < NS; ++s) {
+            ptx::ldsm_x4(kl[s], kt[s] + tile8_off(k_tok, 2 * pr + k_cb));
+            ptx::ldsm_x4(kh[s], kt[s] + tile8_off(k_tok, 2 * pr + KB / 2 + k_cb));
+          }
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int kb = 2 * pr + h;
+            const uint32_t a0 = qh[kb][0], a2 = qh[kb][NR / 2];
+            const uint32_t a1 = R16 ? qh[kb][1] : 0u, a3 = R16 ? qh[kb][NR - 1] : 0u;
+            const int kb2 = kb + KB / 2;
+            const uint32_t b0 = qh[kb2][0], b2 = qh[kb2][NR / 2];
+            const uint32_t b1 = R16 ? qh[kb2][1] : 0u, b3 = R16 ? qh[kb2][NR - 1] : 0u;
+#pragma unroll
+            for (int s = 0; s < NS; ++s) {
+              const float4* gr = reinterpret_cast<const float4*>(
+                                     grows_ptr + int((c_seq + uint32_t(s)) % kStages8) * kRowBytes8) +
+                                 2 * t4;
+              const float4 g01 = gr[8 * kb], g23 = gr[8 * kb + 1];
+#pragma unroll
+              for (int n = 0; n < 2; ++n) {
+                const float4 o01 = fo[n][8 * kb], o23 = fo[n][8 * kb + 1];
+                // cos / sin of (tok + t) omega for the four frequencies, times 2^-4
+                const float2 cg01 = make_float2(g01.x, g01.y), sg01 = make_float2(g01.z, g01.w);
+                const float2 cg23 = make_float2(g23.x, g23.y), sg23 = make_float2(g23.z, g23.w);
+                const float2 co01 = make_float2(o01.x, o01.y), so01 = make_float2(o01.z, o01.w);
+                const float2 co23 = make_float2(o23.x, o23.y), so23 = make_float2(o23.z, o23.w);
+                const float2 c01 = ptx::fsub2(ptx::fmul2(cg01, co01), ptx::fmul2(sg01, so01));
+                const float2 s01 = ptx::ffma2(sg01, co01, ptx::fmul2(cg01, so01));
+                const float2 c23 = ptx::fsub2(ptx::fmul2(cg23, co23), ptx::fmul2(sg23, so23));
+                const float2 s23 = ptx::ffma2(sg23, co23, ptx::fmul2(cg23, so23));
+                const uint32_t lo = kl[s][2 * n + h], hi = kh[s][2 * n + h];
+                float2 x01 = f16x2_to_f32x2(e4m3x2_to_f16x2(lo)), x23 = f16x2_to_f32x2(e4m3x2_to_f16x2(lo >> 16));
+                float2 y01 = f16x2_to_f32x2(e4m3x2_to_f16x2(hi)), y23 = f16x2_to_f32x2(e4m3x2_to_f16x2(hi >> 16));
+                rotate2(x01, y01, c01, s01);
+                rotate2(x23, y23, c23, s23);
+                if (8 * n + g4 < nvalid[s]) {
+                  rmag = ptx::fmax3(rmag, fmaxf(fabsf(x01.x), fabsf(x01.y)), fmaxf(fabsf(x23.x), fabsf(x23.y)));
+                  rmag = ptx::fmax3(rmag, fmaxf(fabsf(y01.x), fabsf(y01.y)), fmaxf(fabsf(y23.x), fabsf(y23.y)));
+                }
+                float* acc = sacc[s][n];
+                ptx::mma_f16(acc[0], acc[1], acc[2], acc[3], a0, a1, a2, a3, ptx::pack_f16(x01.x, x01.y),
+                             ptx::pack_f16(x23.x, x23.y));
+                ptx::mma_f16(acc[0], acc[1], acc[2], acc[3], b0, b1, b2, b3, ptx::pack_f16(y01.x, y01.y),
+                             ptx::pack_f16(y23.x, y23.y));
+              }
+            }
+          }
+        }
+      } else {
 #pragma unroll
       for (int pr = 0; pr < KB / 2; ++pr) {
         uint32_t kr[NS][4];
@@ -288,6 +449,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
           }
         }
       }
+      }
 
       // ---------------- mask + online softmax (log2 domain; k_scale is in scale_log2)
       float xa[NS][4], xb[NS][4];
@@ -296,7 +458,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
         const bool full = (nvalid[s] == kStageTokens) &&
                           (!p.causal || tok[s] + kStageTokens - 1 <= qpos_min) &&
                           (!WIN || tok[s] >= wlo_max);
-        const float sc = p.scale_log2;
+        // with RoPE q and k are both scaled by 2^-4
+        const float sc = ROPE ? p.scale_log2 * (1.f / (kRopeOperandScale * kRopeOperandScale))
+                              : p.scale_log2;
         const int k0 = tok[s] + 2 * t4;
         const int kidx[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
         const float sa[4] = {sacc[s][0][0], sacc[s][0][1], sacc[s][1][0], sacc[s][1][1]};
@@ -494,6 +658,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     }
   }
 
+  if (ROPE && __any_sync(0xffffffffu, rmag > kRopeOperandMax) && lane == 0)
+    atomicOr(p.error, kStatusOperandRange);
   if (failed) {
     if (lane == 0) atomicOr(p.error, 1);
     // let the copies this warp still has in flight land before the CTA exits
@@ -505,33 +671,40 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
 constexpr int kMaxDevices = 64;
 
-template <bool R16, bool WIN>
+template <bool R16, bool WIN, bool ROPE>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
                        int grid, cudaStream_t stream) {
-  auto kern = bsr_decode_kv8_kernel<R16, WIN>;
+  auto kern = bsr_decode_kv8_kernel<R16, WIN, ROPE>;
+  constexpr size_t smem = ROPE ? kSmem8Rope : kSmem8;
   static std::atomic<bool> opted_in[kMaxDevices];   // zero-initialized: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   if (!opted_in[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem8));
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
     if (e != cudaSuccess) return e;
     opted_in[dev].store(true, std::memory_order_release);
   }
-  kern<<<grid, kDecodeWarps * 32, kSmem8, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  const cudaError_t le = launch_pdl(kern, grid, kDecodeWarps * 32, smem, stream, tk, tv, p);
+  return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode_kv8(bool r16, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_decode_kv8(bool rope, bool r16, const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, int grid, cudaStream_t stream) {
   const bool win = p.window_left > 0;
-  if (r16) return win ? launch_one<true, true>(tk, tv, p, grid, stream)
-                      : launch_one<true, false>(tk, tv, p, grid, stream);
-  return win ? launch_one<false, true>(tk, tv, p, grid, stream)
-             : launch_one<false, false>(tk, tv, p, grid, stream);
+  if (rope) {
+    if (r16) return win ? launch_one<true, true, true>(tk, tv, p, grid, stream)
+                        : launch_one<true, false, true>(tk, tv, p, grid, stream);
+    return win ? launch_one<false, true, true>(tk, tv, p, grid, stream)
+               : launch_one<false, false, true>(tk, tv, p, grid, stream);
+  }
+  if (r16) return win ? launch_one<true, true, false>(tk, tv, p, grid, stream)
+                      : launch_one<true, false, false>(tk, tv, p, grid, stream);
+  return win ? launch_one<false, true, false>(tk, tv, p, grid, stream)
+             : launch_one<false, false, false>(tk, tv, p, grid, stream);
 }
 
 }  // namespace bsr

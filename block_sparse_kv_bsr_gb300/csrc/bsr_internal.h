@@ -56,7 +56,9 @@ struct DecodeParams {
   float* part_o;                  // [num_partials, kMaxDecodeRows, D] normalized partial outputs
   float* part_lse;                // [num_partials, kMaxDecodeRows] partial LSE (log2 domain)
   const int32_t* indices;         // [nnz] page ids
-  const float2* rope;             // [rope rows, 4, D / 8] (cos, sin) in fragment order, or null
+  const float2* rope;             // RoPE cos/sin table, or null: the bf16 kernel's fragment order
+                                  // [rows, 4, D / 8] (cos, sin); the FP8 kernel's pair order
+                                  // [rows, D / 4] float4 (cos f, cos f+1, sin f, sin f+1)
   const int32_t* page_pos;        // RoPE: logical position of each page entry's first key, or null
   const int32_t* qshift;          // RoPE with page_pos: logical minus cached end per request
   const uint16_t* q;              // bf16 [sum_qo, Hq, D]

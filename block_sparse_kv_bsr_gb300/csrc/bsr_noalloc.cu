@@ -309,7 +309,7 @@ int noalloc_impl(const void* q, const void* k_pages, const void* v_pages, const 
   const int grid = (units + kDecodeWarps - 1) / kDecodeWarps;
   const bool r16 = group > 8;
   const cudaError_t e =
-      kv8 ? bsr::launch_decode_kv8(r16, tk, tv, p, grid, stream)
+      kv8 ? bsr::launch_decode_kv8(false, r16, tk, tv, p, grid, stream)
           : head_dim == 128 ? bsr::launch_decode_d128(false, r16, smallp, tk, tv, p, grid, stream)
                             : bsr::launch_decode_d64(false, r16, smallp, tk, tv, p, grid, stream);
   if (e != cudaSuccess) {

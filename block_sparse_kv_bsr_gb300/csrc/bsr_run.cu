@@ -395,9 +395,8 @@ extern "C" int bsr_attn_run_kv8(bsr_schedule_t s, const void* q, const void* k_p
   if (out_dtype != BSR_DTYPE_BF16 && out_dtype != BSR_DTYPE_F32) return BSR_ERR_INVALID_ARGUMENT;
   if (rope_theta != s->rope_theta || causal != s->causal) return BSR_ERR_SCHEDULE_MISMATCH;
   // the FP8 path covers the decode kernel's work: D = 128, pages of at least 16
-  // keys, no RoPE, every request on the decode kernel
-  if (s->D != 128 || s->P < bsr::kStageTokens || s->rope_rows > 0 || s->n_pitems > 0)
-    return BSR_ERR_UNSUPPORTED;
+  // keys, every request on the decode kernel (RoPE included)
+  if (s->D != 128 || s->P < bsr::kStageTokens || s->n_pitems > 0) return BSR_ERR_UNSUPPORTED;
   if (s->n_items == 0) return BSR_OK;
   if (q == nullptr || out == nullptr || k_pages == nullptr || v_pages == nullptr)
     return BSR_ERR_INVALID_ARGUMENT;
@@ -436,7 +435,11 @@ extern "C" int bsr_attn_run_kv8(bsr_schedule_t s, const void* q, const void* k_p
   p.part_o = s->dev<float>(s->off_part_o);
   p.part_lse = s->dev<float>(s->off_part_lse);
   p.indices = s->dev<const int32_t>(s->off_indices);
-  p.rope = nullptr;
+  // the FP8 kernel reads the cos/sin table in pair order
+  const bool rope = s->rope_rows > 0;
+  p.rope = rope ? reinterpret_cast<const float2*>(s->d_rope + s->rope_bytes) : nullptr;
+  p.page_pos = rope && s->has_page_pos ? s->dev<const int32_t>(s->off_page_pos) : nullptr;
+  p.qshift = rope && s->has_page_pos ? s->dev<const int32_t>(s->off_qshift) : nullptr;
   p.q = static_cast<const uint16_t*>(q);
   p.k_pages = k_pages;
   p.v_pages = v_pages;
@@ -452,12 +455,12 @@ extern "C" int bsr_attn_run_kv8(bsr_schedule_t s, const void* q, const void* k_p
   p.causal = s->causal;
   p.out_f32 = out_dtype == BSR_DTYPE_F32;
   p.num_warps = s->dec_warps;
-  p.rope_max_pos = 0;
+  p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
   p.window_left = s->window_left;
   p.nhd = s->kv_layout == BSR_KV_NHD;
   p.wait_limit_ns = 1000000000ull;
   t_mark(0, 0);
-  const cudaError_t e = bsr::launch_decode_kv8(s->max_rows > 8, s->tm_k8, s->tm_v8, p,
+  const cudaError_t e = bsr::launch_decode_kv8(rope, s->max_rows > 8, s->tm_k8, s->tm_v8, p,
                                                s->dec_ctas, stream);
   t_mark(0, 1);
   if (e != cudaSuccess) {

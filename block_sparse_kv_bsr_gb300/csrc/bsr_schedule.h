@@ -98,7 +98,7 @@ cudaError_t launch_decode_d64(bool rope, bool r16, bool smallp, const CUtensorMa
 cudaError_t launch_decode_d128(bool rope, bool r16, bool smallp, const CUtensorMap& tk,
                                const CUtensorMap& tv, const DecodeParams& p, int grid,
                                cudaStream_t stream);
-cudaError_t launch_decode_kv8(bool r16, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_decode_kv8(bool rope, bool r16, const CUtensorMap& tk, const CUtensorMap& tv,
                               const DecodeParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillParams& p, int grid,

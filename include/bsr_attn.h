@@ -173,10 +173,14 @@ int bsr_attn_run(bsr_schedule_t schedule, const void* q, const void* k_pages, co
  * k_scale * code and v_scale * code (per-pool scales, finite and > 0; codes
  * S.1111.111 are NaN).  Dequantisation is fused into the page gather: the
  * codes are converted to fp16 in registers (exact) right before the MMAs.
+ * With rope_theta > 0 (planned so) the keys are rotated in registers after
+ * that conversion, RoPE and dequantisation fused into one kernel ("JIT 컴파일은
+ * …" names both): the rotated q and k enter Q K^T as fp16 x 2^-4, as on the
+ * bf16 path, at the positions the plan gives (page_pos included).
  * Everything else (q bf16, out, lse, alignment, ownership, stream semantics)
- * is as for bsr_attn_run.  Covered: head_dim 128, page_size >= 16, no RoPE,
- * every request on the decode kernel (info.num_prefill_items == 0); other
- * schedules return BSR_ERR_UNSUPPORTED.
+ * is as for bsr_attn_run.  Covered: head_dim 128, page_size >= 16, every
+ * request on the decode kernel (info.num_prefill_items == 0); other schedules
+ * return BSR_ERR_UNSUPPORTED.
  */
 int bsr_attn_run_kv8(bsr_schedule_t schedule, const void* q, const void* k_pages,
                      const void* v_pages, float k_scale, float v_scale, float sm_scale,

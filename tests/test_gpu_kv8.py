@@ -43,7 +43,7 @@ def oracle_kv8(w: wl.Paged, rows=None, heads=None):
                                 num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
                                 head_dim=w.head_dim, page_size=w.page_size,
                                 sm_scale=w.sm_scale, rope_theta=w.rope_theta, causal=w.causal,
-                                rows=rows, heads=heads)
+                                page_pos=w.page_pos, rows=rows, heads=heads)
 
 
 def check_full_kv8(w, out, lse):
@@ -98,7 +98,6 @@ def test_kv8_unsupported_schedules_are_refused():
     dev = "cuda:0"
     cases = [
         wl.make_paged("kv8d64", 73, [100, 200], Hq=8, Hk=2, D=64, P=16),          # head_dim 64
-        wl.make_paged("kv8rope", 74, [100, 200], Hq=32, Hk=8, D=128, P=16, rope_theta=1e4),
         wl.make_paged("kv8pf", 75, [700], Hq=32, Hk=8, D=128, P=16, qo_lens=[300],
                       causal=True),                                                # prefill class
         wl.make_paged("kv8p8", 76, [100, 200], Hq=32, Hk=8, D=128, P=8),            # P < 16
@@ -110,3 +109,56 @@ def test_kv8_unsupported_schedules_are_refused():
             bsr.bsr_attn_run_kv8(s, w.q.to(dev), w.k_codes.to(dev), w.v_codes.to(dev),
                                  k_scale=w.k_scale, v_scale=w.v_scale, sm_scale=w.sm_scale,
                                  rope_theta=w.rope_theta, causal=w.causal)
+
+
+# ---------------------------------------------------------------- FP8 cache with RoPE
+
+def test_kv8_rope_llama8b_small():
+    w = wl.config11(small=True)
+    out, lse, _ = run_kv8(w)
+    check_full_kv8(w, out, lse)
+
+
+def test_kv8_rope_llama8b_full_size_sampled():
+    w = wl.config11()
+    out, lse, _ = run_kv8(w)
+    rows, heads = sample_rows(w, 1536)
+    ro, rl = oracle_kv8(w, rows, heads)
+    assert_out_close(out.float().cpu().numpy()[rows, heads], ro, True, w.name)
+    assert_lse_close(lse.cpu().numpy()[rows, heads], rl, w.name)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
+def test_kv8_rope_short_keys_and_causal_rows(out_dtype):
+    """Rows that see a handful of keys (the rotated operands' rounding does not average
+    out), several query rows per request, a 16-row group: the plain bars."""
+    w = wl.with_kv8(wl.make_paged("kv8ropeshort", 81, [5, 17, 40, 300, 2100], Hq=32, Hk=2,
+                                  D=128, P=16, qo_lens=[1, 3, 1, 2, 1], causal=True,
+                                  rope_theta=1e4), 811)
+    out, lse, _ = run_kv8(w, out_dtype)
+    check_full_kv8(w, out, lse)
+
+
+@pytest.mark.parametrize("P", [16, 64])
+def test_kv8_rope_at_logical_positions(P):
+    """Dropped blocks keep the logical positions of the kept ones (page_pos)."""
+    w = wl.with_kv8(wl.make_paged(f"kv8ropepos{P}", 82 + P, [900, 3000, 40], Hq=32, Hk=8, D=128,
+                                  P=P, drop=0.25, rope_theta=5e5), 821 + P)
+    assert w.page_pos is not None
+    out, lse, _ = run_kv8(w)
+    check_full_kv8(w, out, lse)
+
+
+def test_kv8_rope_query_beyond_operand_range_sets_status():
+    """A rotated query element of magnitude 2^20 or more does not fit its fp16 operand:
+    status bit 1."""
+    dev = "cuda:0"
+    w = wl.with_kv8(wl.make_paged("kv8roperange", 83, [300, 200], Hq=32, Hk=8, D=128, P=16,
+                                  rope_theta=1e4), 831)
+    q = w.q.clone()
+    q[0, 0, 3] = 3.0e6
+    s = plan(w)
+    bsr.bsr_attn_run_kv8(s, q.to(dev), w.k_codes.to(dev), w.v_codes.to(dev), k_scale=w.k_scale,
+                         v_scale=w.v_scale, sm_scale=w.sm_scale, rope_theta=w.rope_theta)
+    torch.cuda.synchronize()
+    assert bsr.bsr_last_device_error(s) & 2

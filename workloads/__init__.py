@@ -486,12 +486,17 @@ def config6(small: bool = False) -> Paged:
     return with_kv8(config3(small), 1006)
 
 
+def config11(small: bool = False) -> Paged:
+    """The Llama-3-8B-shaped decode with RoPE over an FP8 (E4M3) KV cache."""
+    return with_kv8(config2(small), 1011)
+
+
 def by_name(cfg: int, small: bool = False):
     return {1: lambda: config1(), 2: lambda: config2(small), 3: lambda: config3(small),
             4: lambda: config4(small), 5: lambda: config5(small),
             6: lambda: config6(small), 7: lambda: config7(small),
             8: lambda: config8(small), 9: lambda: config9(small),
-            10: lambda: config10(small)}[cfg]()
+            10: lambda: config10(small), 11: lambda: config11(small)}[cfg]()
 
 
 def flat_cascade(c: Cascade) -> Paged:
