@@ -41,7 +41,7 @@ def draw(i: int):
     causal = multi and r.random() < 0.7
     rope = r.choice([0.0, 0.0, 1e4, 5e5]) if P >= 16 else 0.0
     drop = r.choice([0.0, 0.0, 0.25])
-    kv8 = D == 128 and P >= 16 and rope == 0.0 and not multi and r.random() < 0.3
+    kv8 = D == 128 and P >= 16 and not multi and r.random() < 0.3
     nhd = r.random() < 0.3
     window = r.choice([0, 0, 0, r.randint(1, 300)])
     return dict(D=D, Hk=Hk, Hq=Hk * group, P=P, lens=lens, qo=qo, causal=causal, rope=rope,
@@ -69,7 +69,8 @@ def test_random_batch(i):
     if c["kv8"]:
         out, lse = bsr.bsr_attn_run_kv8(s, q, w.k_codes.to(dev), w.v_codes.to(dev),
                                         k_scale=w.k_scale, v_scale=w.v_scale,
-                                        sm_scale=w.sm_scale, causal=w.causal)
+                                        sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+                                        causal=w.causal)
     else:
         out, lse = bsr.bsr_attn_run(s, q, w.k_pages.to(dev), w.v_pages.to(dev),
                                     sm_scale=w.sm_scale, rope_theta=w.rope_theta,
