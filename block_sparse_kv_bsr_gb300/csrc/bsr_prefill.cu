@@ -32,8 +32,11 @@
 //              as soon as the previous unit's last Q K^T has read them, and a FIFO
 //              ring of 32 KB stages with the K and V tiles of every key tile in
 //              turn (K(j), V(j), K(j+1), ...), gathered box by box from `indices`
-//              (inactive blocks are absent, "Block-Sparse 포맷"), 128B-swizzled;
-//              lane b fetches box b's page id one key tile ahead.
+//              (inactive blocks are absent, "Block-Sparse 포맷") into one row-group
+//              layout, 128B-swizzled: one box per page-sized piece with both column
+//              blocks (a 4 KB box for 16-token pages where per-block boxes would be
+//              2 KB: the copy engine's cost is mostly per box).  Lane b fetches box
+//              b's page id two key tiles ahead.
 //   warp 17    allocates TMEM and issues the MMAs: S_i = Q_i K^T (M 128, N 128,
 //              K-major operands from shared memory) and O_i += P_i V (P from
 //              TMEM, V MN-major from shared memory), i = 0, 1.
@@ -53,6 +56,7 @@
 #include <atomic>
 #include <climits>
 #include <cstdint>
+#include <type_traits>
 
 #include "bsr_internal.h"
 #include "bsr_launch.cuh"
@@ -206,14 +210,18 @@ __device__ __forceinline__ Angles load_angles(const float4* rope, int pos, int c
   return an;
 }
 
-// Rotate dimensions 8 ch .. 8 ch + 7 of row r of a [2 column blocks][128 rows][128 B]
-// 128B-swizzled bf16 tile together with their rotate-half partners 64 further (the same
-// bytes of the other column block), two frequencies per packed instruction, and write
-// both back in place as fp16.  The angles are already times the operand scale.
-// Returns the largest magnitude written.
+// Rotate dimensions 8 ch .. 8 ch + 7 of row r of a 128B-swizzled bf16 tile together
+// with their rotate-half partners 64 further (the same bytes of the other column
+// block), two frequencies per packed instruction, and write both back in place as
+// fp16.  A query tile is [2 column blocks][128 rows][128 B]; a key tile (GROUPED) is
+// [16 row groups][2 column blocks][8 rows][128 B].  The angles are already times the
+// operand scale.  Returns the largest magnitude written.
+template <bool GROUPED>
 __device__ __forceinline__ float rotate_row_chunk(uint32_t tile, int r, int ch, const Angles& an) {
-  const uint32_t lo = tile + uint32_t(r) * 128u + (uint32_t(ch ^ (r & 7)) << 4);
-  const uint32_t hi = lo + kHalfBytes;
+  const uint32_t swz = uint32_t(ch ^ (r & 7)) << 4;
+  const uint32_t lo = GROUPED ? tile + uint32_t(r >> 3) * 2048u + uint32_t(r & 7) * 128u + swz
+                              : tile + uint32_t(r) * 128u + swz;
+  const uint32_t hi = lo + (GROUPED ? 1024u : uint32_t(kHalfBytes));
   uint32_t a[4], b[4];
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(lo));
@@ -304,7 +312,7 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
     // ------------------------------------------------------------ TMA producer
     // The whole warp runs the loop: lane 0 waits on the ring and posts the byte
     // counts, lane b gathers box b of a paged key tile, and each lane fetches its
-    // box's page id one tile ahead, so no page-table load is on the issue path.
+    // box's page id two tiles ahead, so no page-table load is on the issue path.
     // K/V tiles are re-read by the other row units of the same (request, kv head),
     // which run concurrently on other SMs: keep them in L2 at normal priority.
     // Query tiles are read once.
@@ -343,11 +351,13 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
       return lane < nsub ? __ldg(p.indices + it.page_base + ((it.tok0 + kTileN * j + (lane << lr)) >> lp))
                          : 0;
     };
-    // gather the paged boxes of key tile j into stage c (lane b: box b).  K: with boxes
-    // of 128 rows one copy lands both column blocks ([block][128 rows]); smaller boxes
-    // go one per column block.  V: one copy per box in the row-group layout.
-    auto issue_paged = [&](bool is_v, uint32_t cc, const DecodeItem& it, int j, int nsub,
-                           int page) {
+    // gather the paged boxes of key tile j into the stage of ring position cc (lane b:
+    // box b).  K and V tiles alike land in the row-group layout, one copy per box.
+    int last_pos[kStages];
+#pragma unroll
+    for (int sl = 0; sl < kStages; ++sl) last_pos[sl] = -1;
+    auto issue_paged = [&](uint32_t cc, const CUtensorMap* tm, const DecodeItem& it, int j,
+                           int nsub, int page) {
       if (lane == 0) ptx::mbar_arrive_expect_tx(FULL(cc), uint32_t(nsub) * 2u * box_bytes);
       __syncwarp();
       if (lane < nsub) {
@@ -356,50 +366,52 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
         // with the head as the map's outer coordinate
         const int row = p.nhd ? page * p.P + (key & (p.P - 1))
                               : (page * p.Hk + it.kvh) * p.P + (key & (p.P - 1));
-        const uint32_t vdst = STAGE(cc) + uint32_t(lane) * 2u * box_bytes;
-        if (is_v) {
-          if (p.nhd) ptx::tma_load_5d(vdst, &tm_v, FULL(cc), 0, 0, 0, row >> 3, it.kvh, pol);
-          else ptx::tma_load_4d(vdst, &tm_v, FULL(cc), 0, 0, 0, row >> 3, pol);
-        } else if (p.box_rows == kTileN) {
-          if (p.nhd) ptx::tma_load_4d(STAGE(cc), &tm_k, FULL(cc), 0, row, 0, it.kvh, pol);
-          else ptx::tma_load_3d(STAGE(cc), &tm_k, FULL(cc), 0, row, 0, pol);
-        } else {
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t kdst = STAGE(cc) + h * kHalfBytes + uint32_t(lane) * box_bytes;
-            if (p.nhd) ptx::tma_load_4d(kdst, &tm_k, FULL(cc), 0, h, row, it.kvh, pol);
-            else ptx::tma_load_3d(kdst, &tm_k, FULL(cc), 0, h, row, pol);
-          }
-        }
+        const uint32_t dst = STAGE(cc) + uint32_t(lane) * 2u * box_bytes;
+        if (p.nhd) ptx::tma_load_5d(dst, tm, FULL(cc), 0, 0, 0, row >> 3, it.kvh, pol);
+        else ptx::tma_load_4d(dst, tm, FULL(cc), 0, 0, 0, row >> 3, pol);
       }
+      last_pos[cc % kStages] = int(cc);
+    };
+    // K(j) sits at ring position base + 2 j and V(j) at base + 2 j + 1, issued in
+    // that order (issuing K(j + 1) ahead of V(j) measured slower)
+    auto issue = [&](uint32_t cc, const CUtensorMap* tm, const DecodeItem& it, int j, int nsub,
+                     int page) {
+      if (cc >= kStages && !ring_wait(EMPTY(cc), PHASE(cc) ^ 1u)) return false;
+      issue_paged(cc, tm, it, j, nsub, page);
+      return true;
     };
     for (int u = u_begin; u < u_end && ok; ++u) {
       const DecodeItem it = p.items[u];
       const int nt = ntiles_of(it);
-      int nsub_next = nt > 0 ? boxes_of(it, 0) : 0;
-      int page_next = nt > 0 ? page_of(it, 0, nsub_next) : 0;
+      if (nt == 0) continue;
+      const uint32_t c0 = c;
+      int nsub0 = boxes_of(it, 0), page0 = page_of(it, 0, nsub0);
+      int nsub1 = nt > 1 ? boxes_of(it, 1) : 0, page1 = nt > 1 ? page_of(it, 1, nsub1) : 0;
+      if (!issue(c0, &tm_k, it, 0, nsub0, page0) || !load_q(0, nq0, it) ||
+          (it.nrows > kTileM && !load_q(1, nq1, it))) { ok = false; break; }
       for (int j = 0; j < nt; ++j) {
-        const int nsub = nsub_next, page = page_next;
-        if (j + 1 < nt) {
-          nsub_next = boxes_of(it, j + 1);
-          page_next = page_of(it, j + 1, nsub_next);
+        int nsub2 = 0, page2 = 0;
+        if (j + 2 < nt) {
+          nsub2 = boxes_of(it, j + 2);
+          page2 = page_of(it, j + 2, nsub2);
         }
-        // K(j)
-        if (c >= kStages && !ring_wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
-        issue_paged(false, c, it, j, nsub, page);
-        ++c;
-        if (j == 0) {
-          if (!load_q(0, nq0, it) || (it.nrows > kTileM && !load_q(1, nq1, it))) { ok = false; break; }
+        if (j > 0 && !issue(c0 + 2u * uint32_t(j), &tm_k, it, j, nsub0, page0)) {
+          ok = false;
+          break;
         }
-        // V(j)
-        if (c >= kStages && !ring_wait(EMPTY(c), PHASE(c) ^ 1u)) { ok = false; break; }
-        issue_paged(true, c, it, j, nsub, page);
-        ++c;
+        if (!issue(c0 + 2u * uint32_t(j) + 1u, &tm_v, it, j, nsub0, page0)) { ok = false; break; }
+        nsub0 = nsub1, page0 = page1, nsub1 = nsub2, page1 = page2;
       }
+      c = c0 + 2u * uint32_t(nt);
     }
-    // on abort, let the copies still in flight land before shared memory is released
+    // on abort, let the copies still in flight land before shared memory is released:
+    // a slot's earlier positions completed before the slot was reissued, so its latest
+    // issued position is the only one that can be outstanding
     if (!ok && lane == 0) {
-      for (uint32_t k = c > kStages ? c - kStages : 0; k < c; ++k)
-        ptx::mbar_wait_bounded(FULL(k), PHASE(k), 50000000ull);
+      for (int sl = 0; sl < kStages; ++sl)
+        if (last_pos[sl] >= 0)
+          ptx::mbar_wait_bounded(FULL(uint32_t(last_pos[sl])), PHASE(uint32_t(last_pos[sl])),
+                                 50000000ull);
       if (nq0 > 0) ptx::mbar_wait_bounded(BAR(L::kQFull), (nq0 - 1) & 1u, 50000000ull);
       if (nq1 > 0) ptx::mbar_wait_bounded(BAR(L::kQFull + 1), (nq1 - 1) & 1u, 50000000ull);
     }
@@ -417,7 +429,9 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
       // 256 KB, so the field never carries).
       const uint64_t dq0 = umma::sdesc_sw128(Q_S(0), 16, 1024);
       const uint64_t dq1 = umma::sdesc_sw128(Q_S(1), 16, 1024);
-      const uint64_t dk = umma::sdesc_sw128(STAGE(0), 16, 1024);            // K-major stage 0
+      // K (K-major) by row groups like V: 8-key groups 2 KB apart (SBO), the second
+      // 64-column block of a group 1 KB in
+      const uint64_t dk = umma::sdesc_sw128(STAGE(0), 16, 2048);
       // V (MN-major) by row groups: column blocks 1 KB apart (LBO), 8-key groups 2 KB
       // apart (SBO), a 16-key step 4 KB
       const uint64_t dv = umma::sdesc_sw128(STAGE(0), 1024, 2048);
@@ -427,8 +441,9 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
         const uint64_t kd = dk + stage_field(kc), qd = i == 0 ? dq0 : dq1;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint64_t off = uint64_t(((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4);
-          umma::mma_f16_ss(S_T(i), qd + off, kd + off, idesc_qk, k > 0);
+          const uint64_t qoff = uint64_t(((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4);
+          const uint64_t koff = uint64_t(((k >> 2) * 1024 + (k & 3) * 32) >> 4);
+          umma::mma_f16_ss(S_T(i), qd + qoff, kd + koff, idesc_qk, k > 0);
         }
         umma::commit(BAR(L::kSFull + i));
       };
@@ -546,8 +561,8 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
       return b;
     };
     // rows 8 blk + t of a tile at `tile`: compose base (+) offset off(t), rotate in place
-    auto rotate_rows = [&](uint32_t tile, const Angles& b, int first_off, int step_div,
-                           int valid_rows) {
+    auto rotate_rows = [&](auto grouped, uint32_t tile, const Angles& b, int first_off,
+                           int step_div, int valid_rows) {
 #pragma unroll 1
       for (int t = 0; t < 8; ++t) {
         const int r = 8 * blk + t;
@@ -562,7 +577,7 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
           an.c[e] = ptx::fsub2(ptx::fmul2(b.c[e], ct), ptx::fmul2(b.s[e], st));
           an.s[e] = ptx::ffma2(b.s[e], ct, ptx::fmul2(b.c[e], st));
         }
-        const float m = rotate_row_chunk(tile, r, ch, an);
+        const float m = rotate_row_chunk<decltype(grouped)::value>(tile, r, ch, an);
         if (r < valid_rows) mag = fmaxf(mag, m);
       }
     };
@@ -579,7 +594,7 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
       if (!wt.warp_wait(BAR(L::kQFull + i), nq[i] & 1u)) return false;
       ++nq[i];
       const int R0 = it.row0 + kTileM * i + 8 * blk;
-      rotate_rows(Q_S(i), b, R0 % p.group, p.group, it.nrows - kTileM * i);
+      rotate_rows(std::false_type{}, Q_S(i), b, R0 % p.group, p.group, it.nrows - kTileM * i);
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(L::kQRot + i));
@@ -598,7 +613,7 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
         const int nkeys = min(kTileN, it.tok1 - it.tok0 - kTileN * j);
         if (!wt.warp_wait(FULL(kc), PHASE(kc))) { ok = false; break; }
         const Angles bnext = key_base(it, j + 1);
-        rotate_rows(STAGE(kc), bk, t0, 1, nkeys);
+        rotate_rows(std::true_type{}, STAGE(kc), bk, t0, 1, nkeys);
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(L::kReady + int(kc % kStages)));

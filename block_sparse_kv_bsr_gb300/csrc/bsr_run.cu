@@ -58,24 +58,7 @@ bool encode(CUtensorMap* tm, CUtensorMapDataType dt, cuuint32_t rank, const void
   return r == CUDA_SUCCESS;
 }
 
-// Prefill K tiles of fewer than 128 rows: one 64-column block of R rows per box,
-// landing [R rows][128 B] (D = 128).
-bool encode_pool(CUtensorMap* tm, const void* base, const PoolGeom& g, int box_rows) {
-  constexpr auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (!g.nhd) {
-    const cuuint64_t dims[3] = {64, 2, cuuint64_t(g.rows)};
-    const cuuint64_t strides[2] = {128, 256};
-    const cuuint32_t box[3] = {64, 1, cuuint32_t(box_rows)};
-    return encode(tm, BF, 3, base, dims, strides, box);
-  }
-  const cuuint64_t dims[4] = {64, 2, cuuint64_t(g.tok_rows()), cuuint64_t(g.Hk)};
-  const cuuint64_t strides[3] = {128, cuuint64_t(g.Hk) * 256, 256};
-  const cuuint32_t box[4] = {64, 1, cuuint32_t(box_rows), 1};
-  return encode(tm, BF, 4, base, dims, strides, box);
-}
-
-// Tensor map over a page pool for the decode kernel's 16-key stages (and the
-// prefill kernel's whole 128-row K tiles).  D = 128: the two 64-column blocks are
+// Tensor map over a page pool for the decode kernel's 16-key stages.  D = 128: the two 64-column blocks are
 // an outer dimension (stride 128 B), so one box {64, rows, 2} lands the tile as
 // [column block][rows][128 B], 128B-swizzled: one copy where two would do (a TMA
 // copy's cost is mostly per box: ~26 B/clk per SM with 4 KB boxes against ~20
@@ -124,7 +107,7 @@ bool encode_pool_e4m3(CUtensorMap* tm, const void* base, const PoolGeom& g) {
   return encode(tm, U8, 3, base, dims, strides, box);
 }
 
-// Tensor map over a D = 128 page pool for the prefill kernel's V tiles: a box {64
+// Tensor map over a D = 128 page pool for the prefill kernel's K and V tiles: a box {64
 // cols, 8 rows, 2 column blocks, box_rows / 8 row groups} lands as [row group]
 // [column block][8 rows][128 B], 128B-swizzled, so the boxes of a 128-key tile
 // stack into one uniform layout (8-row groups 2 KB apart, the column blocks of a
@@ -274,12 +257,8 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     const int box_rows = s->P < bsr::kPrefillKeyTile ? s->P : bsr::kPrefillKeyTile;
     if (s->tm_pk_ptr != k_pages || s->tm_pv_ptr != v_pages) {
       const PoolGeom pgeom{rows, s->Hk, s->kv_layout == BSR_KV_NHD};
-      // K: a whole 128-key tile in one box when a page holds it, else one box per
-      // column block and page; V: one box per page-sized piece (row-group layout)
-      const bool k_whole = box_rows == bsr::kPrefillKeyTile;
-      if (rows <= 0 ||
-          !(k_whole ? encode_pool_stage(&s->tm_pk, k_pages, pgeom, s->D, box_rows)
-                    : encode_pool(&s->tm_pk, k_pages, pgeom, box_rows)) ||
+      // K and V alike: one box per page-sized piece of a tile (row-group layout)
+      if (rows <= 0 || !encode_pool_groups(&s->tm_pk, k_pages, pgeom, box_rows) ||
           !encode_pool_groups(&s->tm_pv, v_pages, pgeom, box_rows)) {
         s->tm_pk_ptr = s->tm_pv_ptr = nullptr;
         return BSR_ERR_CUDA;
