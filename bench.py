@@ -11,6 +11,8 @@ value     = algorithmic bytes (active K+V, q, out, lse, page table) / device tim
             (K steps, CUDA events at the ends of the region only).
 hot, cold = the same steps timed one by one: back to back, and after a write of twice the
             L2 before each step (outside its events), so that every step starts cold.
+graph     = (single-call decode workloads) K steps captured in one CUDA graph and replayed:
+            the device time per step without the host's per-call launch cost.
 e2e       = the same bytes / time of the call a user makes with HOST buffers: per step the
             plan of the page table (on the host, overlapping the previous step's kernel as
             a serving loop would), H2D of q and the plan, run, D2H of out and lse, and the
@@ -30,7 +32,8 @@ configs   = after the headline, the other workloads (--configs), each with hot a
 4: shared-prefix cascade, 5: chunked prefill with append, reported in TFLOP/s, 6: the
 skewed decode over an FP8 (E4M3) KV cache, 7: sliding-window decode over long histories,
 8: the skewed decode with RoPE at the kept blocks' logical positions, 9: a three-level
-cascade of shared prefixes, 10: the skewed decode over token-major (NHD) pages);
+cascade of shared prefixes, 10: the skewed decode over token-major (NHD) pages, 11: the
+Llama-3-8B-shaped decode with RoPE over an FP8 cache);
 the default is the skewed decode above.  --impl reference times the oracle (the only
 reference this method has here) on the same workload, each step one pass over the batch
 or, when K passes would take more than ~90 s, over every k-th request.  Under torchrun each
@@ -402,6 +405,7 @@ def build_job(cfg: int, dev, small: bool):
                              launches=s.info()["kernels_per_run"], sched=s, stage="decode",
                              family="decode", profile=None if small else prof)]
         job["schedules"] = [s]
+        job["graphable"] = True
         job.update(workload=w, metric=METRIC, unit="GB/s", numerator=alg, scale=1e9,
                    config={"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads,
                            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
@@ -451,6 +455,7 @@ def build_job(cfg: int, dev, small: bool):
                              "bsr_decode_kv8_skewed_b128.md" if cfg == 6 else
                              "bsr_decode_kv8_rope_llama8b_b64.md")]
         job["schedules"] = [s]
+        job["graphable"] = True
         job["dtype"] = "f16 MMA on E4M3 codes, fp32 accumulate"
         job.update(workload=w, metric=METRIC, unit="GB/s", numerator=alg, scale=1e9,
                    config={"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads,
@@ -652,6 +657,37 @@ def timed_steps(step, steps, stream, flush=None):
     return [a.elapsed_time(b) for a, b in evs]
 
 
+def graph_steps(step, steps):
+    """Device time per step (ms) of `steps` steps captured in one CUDA graph: the
+    launches are queued without the host's per-call cost, as a serving loop that
+    replays a captured step issues them.  One replay warms up; one more is timed with
+    CUDA events around it on the replaying stream."""
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(steps):
+            step()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(side):
+        g.replay()
+        a.record(side)
+        g.replay()
+        b.record(side)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    del g
+    return ms
+
+
+def graph_result(job, step, steps):
+    ms = graph_steps(step, steps)
+    return {"us_per_step": round(ms * 1e3, 2),
+            "value": round(job["numerator"] / (ms * 1e-3) / job["scale"], 1),
+            "note": f"{steps} steps captured in one CUDA graph, replayed (no host launch cost)"}
+
+
 def kernel_pass(parts, steps, stream, bsr):
     """K more steps with CUDA events around each library call and the library's own
     stage events around each kernel of a bsr_attn_run call (records that sit between
@@ -797,6 +833,8 @@ def measure_config(cfg, dev, args, stream, flush, bsr, _build):
            "kernels_us": {f"{pt.label}.{name}": round(sum(v) / len(v) * 1e3, 2)
                           for pt in parts for name, v in pt.stage_ms.items()},
            "config": job["config"]}
+    if job.get("graphable"):
+        res["graph"] = graph_result(job, step, args.steps)
     if "e2e" in job:
         res["e2e"] = e2e_run(job, args.steps, args.warmup, stream)
     if cfg in (1, 2) and not args.no_cpu_baseline:
@@ -871,6 +909,8 @@ def main():
     hot = timed_steps(step, args.steps, stream)
     cold = timed_steps(step, args.steps, stream, flush)
 
+    graph = graph_result(job, step, args.steps) if job.get("graphable") else None
+
     # ---- end to end through the public API with host buffers
     e2e = e2e_run(job, args.steps, args.warmup, stream) if "e2e" in job else None
 
@@ -903,6 +943,8 @@ def main():
         "gpu_launches_note": "kernels launched in the whole-job timed region (region 1)",
         "clocks": clocks.summary(),
     }
+    if graph is not None:
+        res["graph"] = graph
     if e2e is not None:
         res["e2e"] = e2e
     info = job["schedules"][-1].info()

@@ -118,8 +118,9 @@ __device__ __forceinline__ float4 rot_compose(float4 a, float4 b) {
 // this).  Rows are taken four at a time; the chunk maxima and sums are
 // computed lane-parallel over chunks, and the weighted sum of partial outputs
 // (each lane owns D/32 columns) is accumulated in chunk order, so the result
-// does not depend on which warp merges.  Loads of four chunks are issued
-// together to keep the merge off the kernel's tail.
+// does not depend on which warp merges.  The merge sits on the kernel's tail, so
+// its loads are issued as early as possible: the chunk LSEs and the first four
+// chunks' partial rows in one go, then four chunks at a time.
 template <int D>
 __device__ __forceinline__ void merge_range(const DecodeParams& p, const DecodeItem& ci, int lane) {
   constexpr int CPL = D / 32;
@@ -127,69 +128,101 @@ __device__ __forceinline__ void merge_range(const DecodeParams& p, const DecodeI
   const int nck = ci.nchunks, group = p.group;
   const float* lse_base = p.part_lse + size_t(ci.first_slot) * kMaxDecodeRows;
   const float* o_base = p.part_o + size_t(ci.first_slot) * kMaxDecodeRows * D;
+  // lane's CPL columns of the partial row of chunk k, row r (0 where `on` is false)
+  auto load_o = [&](int k, int r, bool on, float (&v)[CPL]) {
+    const size_t sl = size_t(k) * kMaxDecodeRows + r;
+    if constexpr (CPL == 4) {
+      const float4 t = on ? __ldcg(reinterpret_cast<const float4*>(o_base + sl * D) + lane)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+      v[0] = t.x; v[1 % CPL] = t.y; v[2 % CPL] = t.z; v[3 % CPL] = t.w;
+    } else {
+      const float2 t = on ? __ldcg(reinterpret_cast<const float2*>(o_base + sl * D) + lane)
+                          : make_float2(0.f, 0.f);
+      v[0] = t.x; v[1 % CPL] = t.y;
+    }
+  };
 #pragma unroll 1
   for (int r0 = 0; r0 < ci.nrows; r0 += 4) {
     const int nr = min(4, ci.nrows - r0);
-    float M[4], S[4], L2[4];
+    // The chunk LSEs (lane k holds chunk k) and the first four chunks' partial rows are
+    // requested together: for ranges of up to four chunks the merge waits on memory once.
+    float v0[4][4][CPL];
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) { M[rr] = -INFINITY; S[rr] = 0.f; }
-    // chunk maxima (lane k holds chunk k, k + 32, ...)
+    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) load_o(kk, r0 + rr, kk < nck && rr < nr, v0[kk][rr]);
+    float lk[4], M[4], S[4], L2[4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      lk[rr] = lane < nck && rr < nr ? __ldcg(lse_base + size_t(lane) * kMaxDecodeRows + r0 + rr)
+                                     : -INFINITY;
+      M[rr] = lk[rr];
+    }
+    // chunks 32, 33, ... (long ranges only) are read again where they are needed
 #pragma unroll 1
-    for (int k = lane; k < nck; k += 32) {
+    for (int k = lane + 32; k < nck; k += 32) {
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr)
         if (rr < nr) M[rr] = fmaxf(M[rr], __ldcg(lse_base + size_t(k) * kMaxDecodeRows + r0 + rr));
     }
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr)
+    for (int rr = 0; rr < 4; ++rr) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) M[rr] = fmaxf(M[rr], __shfl_xor_sync(0xffffffffu, M[rr], o));
+      S[rr] = M[rr] != -INFINITY && lk[rr] != -INFINITY ? ptx::ex2(lk[rr] - M[rr]) : 0.f;
+    }
 #pragma unroll 1
-    for (int k = lane; k < nck; k += 32) {
+    for (int k = lane + 32; k < nck; k += 32) {
 #pragma unroll
       for (int rr = 0; rr < 4; ++rr)
         if (rr < nr && M[rr] != -INFINITY)
           S[rr] += ptx::ex2(__ldcg(lse_base + size_t(k) * kMaxDecodeRows + r0 + rr) - M[rr]);
     }
+    float wk[4];   // this lane's chunk weight exp2(lse_k - L)
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) S[rr] += __shfl_xor_sync(0xffffffffu, S[rr], o);
       L2[rr] = M[rr] == -INFINITY ? -INFINITY : M[rr] + ptx::lg2(S[rr]);
+      wk[rr] = L2[rr] == -INFINITY || lk[rr] == -INFINITY ? 0.f : ptx::ex2(lk[rr] - L2[rr]);
     }
+    // weight of chunk k, row rr: from lane k for the first 32 chunks, else from memory
+    auto weight = [&](int k, int rr) {
+      if (k < 32) return __shfl_sync(0xffffffffu, wk[rr], k);
+      if (rr >= nr || L2[rr] == -INFINITY) return 0.f;
+      const float l = __ldcg(lse_base + size_t(k) * kMaxDecodeRows + r0 + rr);
+      return l == -INFINITY ? 0.f : ptx::ex2(l - L2[rr]);
+    };
     float acc[4][CPL];
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr)
+    for (int rr = 0; rr < 4; ++rr) {
 #pragma unroll
       for (int c = 0; c < CPL; ++c) acc[rr][c] = 0.f;
-#pragma unroll 1
-    for (int k0 = 0; k0 < nck; k0 += 4) {
-      float w[4][4], v[4][4][CPL];
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
+      for (int kk = 0; kk < 4; ++kk) {
+        const float wt = weight(kk, rr);
+        if (wt != 0.f) {   // an empty chunk's row (weight 0) is not read into the sum
 #pragma unroll
-        for (int rr = 0; rr < 4; ++rr) {
-          const int k = k0 + kk;
-          const bool on = k < nck && rr < nr && L2[rr] != -INFINITY;
-          const size_t sl = size_t(k) * kMaxDecodeRows + r0 + rr;
-          w[kk][rr] = on ? __ldcg(lse_base + sl) : -INFINITY;
-          if constexpr (CPL == 4) {
-            const float4 t = on ? __ldcg(reinterpret_cast<const float4*>(o_base + sl * D) + lane)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            v[kk][rr][0] = t.x; v[kk][rr][1] = t.y; v[kk][rr][2 % CPL] = t.z; v[kk][rr][3 % CPL] = t.w;
-          } else {
-            const float2 t = on ? __ldcg(reinterpret_cast<const float2*>(o_base + sl * D) + lane)
-                                : make_float2(0.f, 0.f);
-            v[kk][rr][0] = t.x; v[kk][rr][1 % CPL] = t.y;
-          }
+          for (int c = 0; c < CPL; ++c) acc[rr][c] += wt * v0[kk][rr][c];
         }
+      }
+    }
+#pragma unroll 1
+    for (int k0 = 4; k0 < nck; k0 += 4) {
+      float v[4][4][CPL];
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) load_o(k0 + kk, r0 + rr, k0 + kk < nck && rr < nr, v[kk][rr]);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr) {
-          const float wt = w[kk][rr] == -INFINITY ? 0.f : ptx::ex2(w[kk][rr] - L2[rr]);
+          const float wt = k0 + kk < nck ? weight(k0 + kk, rr) : 0.f;
+          if (wt != 0.f) {
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) acc[rr][c] += wt * v[kk][rr][c];
+            for (int c = 0; c < CPL; ++c) acc[rr][c] += wt * v[kk][rr][c];
+          }
         }
     }
 #pragma unroll
@@ -222,10 +255,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   constexpr int NT = C::kNTiles;
   constexpr int KH = KS / 2;            // k-steps in the first half of the head dim
   extern __shared__ uint8_t smem_raw[];
-  // launched as a programmatic dependent: let the next grid start its set-up, and touch
-  // no global memory before the previous grid has completed
+  // launched as a programmatic dependent: let the next grid start its set-up.  q, the
+  // pages and every output may be another grid's, so they wait until the previous grid
+  // has completed; a plan's work list, page table and tables came with its host copy
+  // and are read before that wait (the set-up below overlaps the previous grid's tail)
   pdl_trigger();
-  pdl_wait();
+  const bool early = p.plan_uploaded != 0;
+  if (!early) pdl_wait();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -256,6 +292,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
       for (int s = 0; s < C::kStages; ++s) ptx::mbar_init(bars + 8 * s, 1);
       ptx::fence_barrier_init();
+      ptx::prefetch_tensormap(&tm_k);
+      ptx::prefetch_tensormap(&tm_v);
     }
     __syncwarp();
   }
@@ -359,8 +397,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     }
   };
 
+  if (!SMALLP) producer_seek();
+  if (early) pdl_wait();
   if (!SMALLP) {
-    producer_seek();
 #pragma unroll 1
     for (int i = 0; i < C::kStages; ++i) producer_issue();
   }

@@ -105,9 +105,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   constexpr int KB = D / 16;            // 16-dim blocks
   constexpr int NT = D / 8;             // n-tiles of the output
   extern __shared__ uint8_t smem_raw[];
-  // launched as a programmatic dependent (see bsr_launch.cuh)
+  // launched as a programmatic dependent (see bsr_launch.cuh); a plan's work list, page
+  // table and tables are read before the wait, as in bsr_decode_kernel
   pdl_trigger();
-  pdl_wait();
+  const bool early = p.plan_uploaded != 0;
+  if (!early) pdl_wait();
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -139,6 +141,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 #pragma unroll
     for (int s = 0; s < kStages8; ++s) ptx::mbar_init(bars + 8 * s, 1);
     ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tm_k);
+    ptx::prefetch_tensormap(&tm_v);
   }
   __syncwarp();
   const uint64_t pol = ptx::policy_evict_first();
@@ -226,6 +230,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     }
   };
   producer_seek();
+  if (early) pdl_wait();
 #pragma unroll 1
   for (int i = 0; i < kStages8; ++i) producer_issue();
 

@@ -74,6 +74,9 @@ struct DecodeParams {
   int32_t rope_max_pos;           // last row of the cos/sin table
   int32_t window_left;            // sliding window: keys >= position - window_left + 1 (0: none)
   int32_t nhd;                    // page pools token-major [pages, P, Hk, D] (else [pages, Hk, P, D])
+  int32_t plan_uploaded;          // 1: items, warp_ptr, indices, page_pos and rope were written
+                                  // by a host copy before the launch, so the kernel may read
+                                  // them before the previous grid on the stream completes
   uint64_t wait_limit_ns;         // bound on every barrier wait
 };
 

@@ -4,9 +4,12 @@
 // overlaps the previous kernel's tail instead of following it.  Every kernel
 // launched here executes pdl_wait() -- which returns once the previous grid has
 // completed and its memory operations are visible -- before its first access to
-// global memory, so no data a previous kernel writes is read early, and none it
-// reads is overwritten early.  Launched after a copy, or after a kernel launched
-// the ordinary way, it simply starts when that work is done.
+// global memory that another kernel may write (q, the pages, outputs, partial
+// states, counters, the status word), so no such data is read early and none a
+// previous kernel reads is overwritten early.  Only what a plan's host copy wrote
+// before the launch (work lists, page table, RoPE tables) may be read before the
+// wait.  Launched after a copy, or after a kernel launched the ordinary way, a
+// kernel simply starts when that work is done.
 #pragma once
 
 #include <cuda_runtime.h>

@@ -36,9 +36,17 @@ constexpr int64_t kUnitOverhead = 48;
 // Shortest piece a key range is cut into (keys): below this the partial
 // write and merge cost more than the balance gains.
 constexpr int64_t kMinPiece = 64;
+// The same for a batch too small to give every warp of the GPU kMinWarpWork.
+// Such a batch is latency-bound: its longest range's chain of dependent stages
+// sets the time, and a warp takes ~0.6 us per 16-key stage even with the data
+// landed, against ~4 us for a split range's partial write, arrival and merge.
+// Cutting a 255-key range into four pieces instead of two took a 4-request
+// decode from ~10 to ~7.5 us; applied to full batches the shorter pieces only
+// add merges (1.3 % on the skewed 128-request decode), so they stay at kMinPiece.
+constexpr int64_t kMinPieceSmall = 32;
 // Least work (key-equivalents) worth a warp of its own: small batches use
 // fewer warps instead of many tiny pieces.
-constexpr int64_t kMinWarpWork = 128;
+constexpr int64_t kMinWarpWork = 64;
 // Prefill: packed rows from which a request takes the tensor-core kernel, the
 // per-unit overhead (Q load, pipeline fill, epilogue) in keys, the shortest
 // key piece and the least work per CTA.
@@ -149,7 +157,8 @@ int64_t cut_ranges(const CutInput& in, int64_t T, Emit&& emit) {
 // is a pure function of its inputs.  `align` is a power of two (a page or a
 // key tile).
 void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align, int64_t overhead,
-             int64_t min_piece, int64_t min_worker_work, WorkList* out, int64_t* k_hint = nullptr) {
+             int64_t min_piece, int64_t min_worker_work, WorkList* out, int64_t* k_hint = nullptr,
+             int64_t min_piece_small = 0) {
   // Working arrays live across calls (per thread), so a plan per decode step reuses
   // their memory instead of faulting in fresh pages.
   struct Scratch {
@@ -203,6 +212,8 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
   const int workers =
       units.empty() ? 0
                     : int(std::max<int64_t>(1, std::min<int64_t>(max_workers, (total + min_worker_work - 1) / min_worker_work)));
+  // a batch that leaves workers idle may be cut finer (min_piece_small, when given)
+  if (min_piece_small > 0 && workers < max_workers) min_piece = min_piece_small;
   const CutInput in{kb.data(), ke.data(), n, overhead, ~(align - 1), min_piece, max_workers, workers};
   std::vector<int32_t>& pieces_of_unit = sc.pieces_of_unit;
   pieces_of_unit.assign(n, 0);
@@ -572,7 +583,7 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   // consecutive plans of a serving loop are alike: start from the last budget step
   thread_local int64_t dec_k = -1;
   balance(dunits, int64_t(num_sms) * kDecodeWarps, std::max<int64_t>(page_size, kStageTokens),
-          kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec, &dec_k);
+          kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec, &dec_k, kMinPieceSmall);
   balance_gangs(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillKeyTile),
                 kPrefillOverhead, kPrefillMinPiece, kPrefillMinCtaWork, &hp->pre);
   hp->pmerge.clear();

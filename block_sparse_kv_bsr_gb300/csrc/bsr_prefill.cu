@@ -257,9 +257,10 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
                        const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
   using L = Smem;
   extern __shared__ uint8_t smem_raw[];
-  // launched as a programmatic dependent (see bsr_launch.cuh)
+  // launched as a programmatic dependent (see bsr_launch.cuh): the set-up below --
+  // barriers, TMEM, the plan's CTA ranges (written by the plan's host copy) -- overlaps
+  // the previous grid's tail; everything after it waits for that grid
   pdl_trigger();
-  pdl_wait();
   const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t bar0 = base + L::kBars;
@@ -294,6 +295,9 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
     for (int i = 0; i < 2; ++i) ptx::mbar_init(BAR(L::kQRot + i), kRotWarps);
     asm volatile("st.shared.u32 [%0], %1;" ::"r"(abort_addr), "r"(0u));
     ptx::fence_barrier_init();
+    ptx::prefetch_tensormap(&tm_q);
+    ptx::prefetch_tensormap(&tm_k);
+    ptx::prefetch_tensormap(&tm_v);
   }
   if (warp == kMmaWarp) {
     umma::tmem_alloc(base + L::kTmemSlot, kTmemCols);
@@ -302,6 +306,7 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
   umma::fence_before_sync();
   __syncthreads();
   umma::fence_after_sync();
+  pdl_wait();
   uint32_t tmem;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(tmem) : "r"(base + L::kTmemSlot));
   auto S_T = [&](int i) { return tmem + 128u * uint32_t(i); };

@@ -232,6 +232,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
     p.window_left = s->window_left;
     p.nhd = s->kv_layout == BSR_KV_NHD;
+    p.plan_uploaded = 1;   // the work list and page table came with the plan's copy
     p.wait_limit_ns = wait_limit_ns;
     const bool r16 = s->max_rows > 8;
     t_mark(0, 0);
@@ -437,6 +438,7 @@ extern "C" int bsr_attn_run_kv8(bsr_schedule_t s, const void* q, const void* k_p
   p.rope_max_pos = rope ? s->rope_rows - 1 : 0;
   p.window_left = s->window_left;
   p.nhd = s->kv_layout == BSR_KV_NHD;
+  p.plan_uploaded = 1;   // the work list and page table came with the plan's copy
   p.wait_limit_ns = 1000000000ull;
   t_mark(0, 0);
   const cudaError_t e = bsr::launch_decode_kv8(rope, s->max_rows > 8, s->tm_k8, s->tm_v8, p,

@@ -23,6 +23,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Fetch a tensor map (a __grid_constant__ kernel parameter) into the TMA unit's cache
+// ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const void* tm) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
 // Make barrier initialisation visible to the async (TMA) proxy.
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
