@@ -117,6 +117,8 @@ struct PrefillParams {
   int32_t window_left;            // sliding window (0: none)
   int32_t nhd;                    // page pools token-major (else head-major)
   int32_t box_rows;               // rows per K/V box of the prefill tensor maps: min(P, 128)
+  int32_t head_dim;               // 64 or 128 (a D = 64 head runs the 128-wide tile program
+                                  // with its upper 64 dimensions zero)
   uint64_t wait_limit_ns;
 };
 
@@ -129,6 +131,7 @@ struct PrefillMergeParams {
   void* out;
   float* lse;
   int32_t n_units, Hq, group, out_f32;
+  int32_t head_dim;               // 64 or 128
 };
 
 }  // namespace bsr

@@ -541,10 +541,11 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
 
   // ---------------------------------------------------------------- units
   // A request goes to the tensor-core prefill kernel when its packed rows fill
-  // at least half of a 128-row query tile and the layout suits it (head_dim
-  // 128, pages of at least 16 keys, a head group that divides the 128-row
-  // tile, so that a tile is whole queries); the others use the decode
-  // kernel's 16-row groups.  Prefill units hold up to two query tiles (256 rows).
+  // at least half of a 128-row query tile and the layout suits it (pages of at
+  // least 16 keys, a head group that divides the 128-row tile, so that a tile is
+  // whole queries; head_dim 64 runs the 128-wide tile program with its upper 64
+  // dimensions zero); the others use the decode kernel's 16-row groups.  Prefill
+  // units hold up to two query tiles (256 rows).
   std::vector<Unit>& dunits = hp->dunits;
   std::vector<Unit>& punits = hp->punits;
   dunits.clear();
@@ -553,7 +554,7 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   for (int32_t b = 0; b < batch; ++b) {
     const int32_t rows = qo_len[b] * group;
     const int32_t qpos0 = kv_len[b] - qo_len[b];
-    const bool prefill = head_dim == 128 && page_size >= kStageTokens && rows >= kPrefillMinRows &&
+    const bool prefill = page_size >= kStageTokens && rows >= kPrefillMinRows &&
                          bsr::kPrefillKeyTile % group == 0;
     const int32_t step = prefill ? bsr::kPrefillRows : kMaxDecodeRows;
     for (int32_t h = 0; h < num_kv_heads; ++h)

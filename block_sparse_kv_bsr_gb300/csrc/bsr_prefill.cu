@@ -67,7 +67,7 @@
 namespace bsr {
 namespace {
 
-constexpr int D = 128;
+constexpr int D = 128;                      // width of the tile program (head_dim 64 runs it with zeros above)
 constexpr int kTileM = 128;                 // rows per query tile (TMEM lanes)
 constexpr int kUnitRows = kPrefillRows;     // two query tiles
 constexpr int kTileN = kPrefillKeyTile;     // keys per key tile
@@ -161,7 +161,7 @@ __device__ __forceinline__ size_t out_row(const DecodeItem& it, int R, int group
 __device__ __forceinline__ void store_row_chunk(const PrefillParams& p, size_t orow, int c,
                                                 const float (&v)[32]) {
   if (p.out_f32) {
-    float* dst = static_cast<float*>(p.out) + orow * D + 32 * c;
+    float* dst = static_cast<float*>(p.out) + orow * size_t(p.head_dim) + 32 * c;
     if (p.out_v8) {
 #pragma unroll
       for (int i = 0; i < 4; ++i)
@@ -175,7 +175,7 @@ __device__ __forceinline__ void store_row_chunk(const PrefillParams& p, size_t o
         reinterpret_cast<float4*>(dst)[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
     }
   } else {
-    uint16_t* dst = static_cast<uint16_t*>(p.out) + orow * D + 32 * c;
+    uint16_t* dst = static_cast<uint16_t*>(p.out) + orow * size_t(p.head_dim) + 32 * c;
     uint32_t w[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) w[i] = ptx::pack_bf16(v[2 * i], v[2 * i + 1]);
@@ -197,9 +197,10 @@ struct Angles {
   float2 c[4], s[4];
 };
 
-// Angles of chunk ch at table row `pos` (four float4 of the pair-order table).
-__device__ __forceinline__ Angles load_angles(const float4* rope, int pos, int ch) {
-  const float4* row = rope + size_t(pos) * (D / 4) + 4 * ch;
+// Angles of chunk ch at table row `pos` (four float4 of the pair-order table, whose
+// rows hold head_dim / 4 float4).
+__device__ __forceinline__ Angles load_angles(const float4* rope, int pos, int ch, int row_f4) {
+  const float4* row = rope + size_t(pos) * row_f4 + 4 * ch;
   Angles an;
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -211,17 +212,19 @@ __device__ __forceinline__ Angles load_angles(const float4* rope, int pos, int c
 }
 
 // Rotate dimensions 8 ch .. 8 ch + 7 of row r of a 128B-swizzled bf16 tile together
-// with their rotate-half partners 64 further (the same bytes of the other column
-// block), two frequencies per packed instruction, and write both back in place as
-// fp16.  A query tile is [2 column blocks][128 rows][128 B]; a key tile (GROUPED) is
-// [16 row groups][2 column blocks][8 rows][128 B].  The angles are already times the
-// operand scale.  Returns the largest magnitude written.
-template <bool GROUPED>
+// with their rotate-half partners, two frequencies per packed instruction, and write
+// both back in place as fp16.  With head_dim 128 the partners are 64 further (the same
+// bytes of the other column block); with 64 (D64, ch < 4) they are 32 further, chunk
+// ch + 4 of the same 128-byte row.  A query tile is [2 column blocks][128 rows][128 B];
+// a key tile (GROUPED) is [16 row groups][2 column blocks][8 rows][128 B].  The angles
+// are already times the operand scale.  Returns the largest magnitude written.
+template <bool GROUPED, bool D64>
 __device__ __forceinline__ float rotate_row_chunk(uint32_t tile, int r, int ch, const Angles& an) {
-  const uint32_t swz = uint32_t(ch ^ (r & 7)) << 4;
-  const uint32_t lo = GROUPED ? tile + uint32_t(r >> 3) * 2048u + uint32_t(r & 7) * 128u + swz
-                              : tile + uint32_t(r) * 128u + swz;
-  const uint32_t hi = lo + (GROUPED ? 1024u : uint32_t(kHalfBytes));
+  const uint32_t rowb = GROUPED ? tile + uint32_t(r >> 3) * 2048u + uint32_t(r & 7) * 128u
+                                : tile + uint32_t(r) * 128u;
+  const uint32_t lo = rowb + (uint32_t(ch ^ (r & 7)) << 4);
+  const uint32_t hi = D64 ? rowb + (uint32_t((ch + 4) ^ (r & 7)) << 4)
+                          : lo + (GROUPED ? 1024u : uint32_t(kHalfBytes));
   uint32_t a[4], b[4];
   asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]) : "r"(lo));
@@ -250,7 +253,9 @@ __device__ __forceinline__ float rotate_row_chunk(uint32_t tile, int r, int ch, 
 // One CTA per SM.  Each of the 4 SM sub-partitions holds a quarter of the register
 // file (16K registers) and up to 6 of the 22 warps of the RoPE variant, so 80
 // registers per thread is its ceiling (96 for the 18 warps without RoPE).
-template <bool ROPE, bool WIN>
+// D64: head_dim 64 with RoPE (its rotation pairs lie 32 apart); head_dim 64 without
+// RoPE needs nothing of its own beyond the run-time output width.
+template <bool ROPE, bool WIN, bool D64>
 __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96)
     bsr_prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                        const __grid_constant__ CUtensorMap tm_k,
@@ -536,10 +541,14 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
     // covers one row's eight chunks, so its shared-memory accesses hit distinct banks.
     const int rt = tid - 32 * kRotWarp0;
     const int ch = rt & 7, blk = rt >> 3;
+    // head_dim 64: 32 rotation pairs per row, chunks 0-3 with 4-7 (threads of chunks
+    // 4-7 have nothing to rotate and load no angles)
+    const bool rot_on = !D64 || ch < 4;
+    constexpr int row_f4 = D64 ? 16 : D / 4;
     const uint32_t ttab = base + L::kRopeT;
-    for (int i = rt; i < 16 * (D / 4); i += kRotThreads) {
-      const int t = i / (D / 4), fp = i % (D / 4);   // offset, frequency pair
-      const float4 v = __ldg(p.rope + size_t(t) * (D / 4) + fp);
+    for (int i = rt; i < 16 * row_f4; i += kRotThreads) {
+      const int t = i / row_f4, fp = i % row_f4;   // offset, frequency pair
+      const float4 v = __ldg(p.rope + size_t(t) * row_f4 + fp);
       const uint32_t dst = ttab + uint32_t(((t * 4 + (fp & 3)) * 8 + (fp >> 2)) * 16);
       asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst),
                    "f"(v.x * kRopeOperandScale), "f"(v.y * kRopeOperandScale),
@@ -556,18 +565,19 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
     auto key_base = [&](const DecodeItem& it, int j) {
       Angles b{};
       const int nkeys = min(kTileN, it.tok1 - it.tok0 - kTileN * j);
-      if (j < ntiles_of(it) && 16 * g < nkeys) {
+      if (rot_on && j < ntiles_of(it) && 16 * g < nkeys) {
         const int kg = it.tok0 + kTileN * j + 16 * g;
         const int bpos = p.page_pos != nullptr
                              ? __ldg(p.page_pos + it.page_base + (kg >> lp)) + (kg & (p.P - 1))
                              : kg;
-        b = load_angles(p.rope, min(bpos, p.rope_max_pos), ch);
+        b = load_angles(p.rope, min(bpos, p.rope_max_pos), ch, row_f4);
       }
       return b;
     };
     // rows 8 blk + t of a tile at `tile`: compose base (+) offset off(t), rotate in place
     auto rotate_rows = [&](auto grouped, uint32_t tile, const Angles& b, int first_off,
                            int step_div, int valid_rows) {
+      if (!rot_on) return;
 #pragma unroll 1
       for (int t = 0; t < 8; ++t) {
         const int r = 8 * blk + t;
@@ -582,7 +592,7 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
           an.c[e] = ptx::fsub2(ptx::fmul2(b.c[e], ct), ptx::fmul2(b.s[e], st));
           an.s[e] = ptx::ffma2(b.s[e], ct, ptx::fmul2(b.c[e], st));
         }
-        const float m = rotate_row_chunk<decltype(grouped)::value>(tile, r, ch, an);
+        const float m = rotate_row_chunk<decltype(grouped)::value, D64>(tile, r, ch, an);
         if (r < valid_rows) mag = fmaxf(mag, m);
       }
     };
@@ -593,7 +603,7 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
       const int qsh = p.qshift != nullptr ? __ldg(p.qshift + it.req) : 0;
       const int R0 = it.row0 + kTileM * i + 8 * blk;
       const int pos = min(max(it.qpos0 + R0 / p.group + qsh, 0), p.rope_max_pos);
-      return load_angles(p.rope, pos, ch);
+      return rot_on ? load_angles(p.rope, pos, ch, row_f4) : Angles{};
     };
     auto rotate_q = [&](const DecodeItem& it, int i, const Angles& b) -> bool {
       if (!wt.warp_wait(BAR(L::kQFull + i), nq[i] & 1u)) return false;
@@ -810,15 +820,18 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
         l += lother;
       }
       // ---- epilogue: this half's 64 columns of O row t / l (an empty unit writes 0 /
-      // -inf); a split range writes its fp32 partial state instead
+      // -inf); a split range writes its fp32 partial state instead.  With head_dim 64
+      // only the first half's columns are real (the second half's are zero padding).
       const size_t orow = out_row(it, R, group, p.Hq);
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse2 = l > 0.f ? m_used + ptx::lg2(l) : -INFINITY;
       constexpr float kLn2 = 0.69314718055994530942f;
-      float* part_row = p.part_o + (size_t(it.slot < 0 ? 0 : it.slot) * kUnitRows + prow) * D;
+      float* part_row =
+          p.part_o + (size_t(it.slot < 0 ? 0 : it.slot) * kUnitRows + prow) * size_t(p.head_dim);
 #pragma unroll 1
       for (int c2 = 0; c2 < 2; ++c2) {
         const int c4 = 2 * half + c2;      // 32-column chunk of the row
+        if (32 * c4 >= p.head_dim) break;
         float v[32];
         if (nt > 0) {
           umma::tmem_ld32(o_t + 32 * c2, v);
@@ -862,7 +875,8 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
 }
 
 // ---------------------------------------------------------------- split-range merge
-// One warp per packed row of a split unit: lane l owns columns 4l .. 4l + 3.
+// One warp per packed row of a split unit: lane l owns columns 4l .. 4l + 3 (with
+// head_dim 64 lanes 16-31 own none).
 // The partial states (fp32, log2-domain lse) are combined in key order:
 //   lse = M + log2(sum_k 2^(lse_k - M)),  o = sum_k 2^(lse_k - lse) o_k.
 // Lane k holds lse_k (chunks in groups of 32); the partial rows of up to eight
@@ -881,14 +895,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(con
   if (prow >= it.nrows) return;
   const int n = it.nchunks;
   const float* lse_k = p.part_lse + size_t(it.first_slot) * kUnitRows + prow;
-  const float* po = p.part_o + (size_t(it.first_slot) * kUnitRows + prow) * D + 4 * lane;
-  constexpr size_t kSlotStride = size_t(kUnitRows) * D;
+  const size_t hd = size_t(p.head_dim);
+  const bool cols = 4 * lane < p.head_dim;
+  const float* po = p.part_o + (size_t(it.first_slot) * kUnitRows + prow) * hd + 4 * lane;
+  const size_t kSlotStride = size_t(kUnitRows) * hd;
   // the first chunks' partial rows, before anything depends on the lse values
   float4 x[8];
 #pragma unroll
   for (int u = 0; u < 8; ++u)
-    x[u] = u < n ? __ldcg(reinterpret_cast<const float4*>(po + size_t(u) * kSlotStride))
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    x[u] = cols && u < n ? __ldcg(reinterpret_cast<const float4*>(po + size_t(u) * kSlotStride))
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
   // chunk lse values: lane k holds chunk k (and k + 32, ... for longer splits: read
   // again there); one load round trip before the weights when n <= 32
   const float l0 = lane < n ? __ldcg(lse_k + size_t(lane) * kUnitRows) : -INFINITY;
@@ -912,8 +928,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(con
         if (kb + j >= 8) {   // chunks past the first eight: load this group now
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            x[u] = j + u < m ? __ldcg(reinterpret_cast<const float4*>(po + size_t(kb + j + u) * kSlotStride))
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            x[u] = cols && j + u < m
+                       ? __ldcg(reinterpret_cast<const float4*>(po + size_t(kb + j + u) * kSlotStride))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -926,19 +943,21 @@ __global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(con
     }
   }
   const size_t orow = out_row(it, it.row0 + prow, p.group, p.Hq);
-  if (p.out_f32) {
-    reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * D)[lane] = acc;
-  } else {
-    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * D)[lane] =
-        make_uint2(ptx::pack_bf16(acc.x, acc.y), ptx::pack_bf16(acc.z, acc.w));
+  if (cols) {
+    if (p.out_f32) {
+      reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * hd)[lane] = acc;
+    } else {
+      reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * hd)[lane] =
+          make_uint2(ptx::pack_bf16(acc.x, acc.y), ptx::pack_bf16(acc.z, acc.w));
+    }
   }
   if (lane == 0 && p.lse != nullptr) p.lse[orow] = lt * 0.69314718055994530942f;
 }
 
-template <bool ROPE, bool WIN>
+template <bool ROPE, bool WIN, bool D64>
 cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                        const PrefillParams& p, int grid, cudaStream_t stream) {
-  auto kern = bsr_prefill_kernel<ROPE, WIN>;
+  auto kern = bsr_prefill_kernel<ROPE, WIN, D64>;
   constexpr size_t smem = Smem::kDynBytes;
   static std::atomic<bool> opted_in[64];   // zero-initialized: false
   int dev = 0;
@@ -959,11 +978,15 @@ cudaError_t launch_one(const CUtensorMap& tq, const CUtensorMap& tk, const CUten
 cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillParams& p, int grid,
                            cudaStream_t stream) {
-  if (p.window_left > 0)
-    return rope ? launch_one<true, true>(tq, tk, tv, p, grid, stream)
-                : launch_one<false, true>(tq, tk, tv, p, grid, stream);
-  return rope ? launch_one<true, false>(tq, tk, tv, p, grid, stream)
-              : launch_one<false, false>(tq, tk, tv, p, grid, stream);
+  const bool d64 = p.head_dim == 64;
+  if (p.window_left > 0) {
+    if (!rope) return launch_one<false, true, false>(tq, tk, tv, p, grid, stream);
+    return d64 ? launch_one<true, true, true>(tq, tk, tv, p, grid, stream)
+               : launch_one<true, true, false>(tq, tk, tv, p, grid, stream);
+  }
+  if (!rope) return launch_one<false, false, false>(tq, tk, tv, p, grid, stream);
+  return d64 ? launch_one<true, false, true>(tq, tk, tv, p, grid, stream)
+             : launch_one<true, false, false>(tq, tk, tv, p, grid, stream);
 }
 
 cudaError_t launch_prefill_merge(const PrefillMergeParams& p, cudaStream_t stream) {

@@ -107,39 +107,46 @@ bool encode_pool_e4m3(CUtensorMap* tm, const void* base, const PoolGeom& g) {
   return encode(tm, U8, 3, base, dims, strides, box);
 }
 
-// Tensor map over a D = 128 page pool for the prefill kernel's K and V tiles: a box {64
-// cols, 8 rows, 2 column blocks, box_rows / 8 row groups} lands as [row group]
+// Tensor map over a D = 64 or 128 page pool for the prefill kernel's K and V tiles: a
+// box {64 cols, 8 rows, 2 column blocks, box_rows / 8 row groups} lands as [row group]
 // [column block][8 rows][128 B], 128B-swizzled, so the boxes of a 128-key tile
 // stack into one uniform layout (8-row groups 2 KB apart, the column blocks of a
 // group 1 KB apart) whatever the page size: one box per page-sized piece.
-// Rows (token rows with NHD) must be a multiple of 8.
-bool encode_pool_groups(CUtensorMap* tm, const void* base, const PoolGeom& g, int box_rows) {
+// Rows (token rows with NHD) must be a multiple of 8.  A D = 64 pool has one column
+// block: the box still spans two and the second lands as zeros, so a D = 64 head runs
+// the 128-wide tile program with its upper 64 dimensions zero.
+bool encode_pool_groups(CUtensorMap* tm, const void* base, const PoolGeom& g, int box_rows,
+                        int D) {
   constexpr auto BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  if (box_rows % 8 != 0) return false;
+  if (box_rows % 8 != 0 || (D != 64 && D != 128)) return false;
+  const cuuint64_t hs = cuuint64_t(D) * 2;   // bytes of one head row
+  const cuuint64_t blocks = cuuint64_t(D / 64);
   if (!g.nhd) {
     if (g.rows % 8 != 0) return false;
-    const cuuint64_t dims[4] = {64, 8, 2, cuuint64_t(g.rows / 8)};
-    const cuuint64_t strides[3] = {256, 128, 2048};
+    const cuuint64_t dims[4] = {64, 8, blocks, cuuint64_t(g.rows / 8)};
+    const cuuint64_t strides[3] = {hs, 128, 8 * hs};
     const cuuint32_t box[4] = {64, 8, 2, cuuint32_t(box_rows / 8)};
     return encode(tm, BF, 4, base, dims, strides, box);
   }
   if (g.tok_rows() % 8 != 0) return false;
-  const cuuint64_t rs = cuuint64_t(g.Hk) * 256;   // token row stride
-  const cuuint64_t dims[5] = {64, 8, 2, cuuint64_t(g.tok_rows() / 8), cuuint64_t(g.Hk)};
-  const cuuint64_t strides[4] = {rs, 128, 8 * rs, 256};
+  const cuuint64_t rs = cuuint64_t(g.Hk) * hs;   // token row stride
+  const cuuint64_t dims[5] = {64, 8, blocks, cuuint64_t(g.tok_rows() / 8), cuuint64_t(g.Hk)};
+  const cuuint64_t strides[4] = {rs, 128, 8 * rs, hs};
   const cuuint32_t box[5] = {64, 8, 2, cuuint32_t(box_rows / 8), 1};
   return encode(tm, BF, 5, base, dims, strides, box);
 }
 
-// Tensor map over q [rows, Hq, D = 128] (bf16) for the
-// prefill kernel's query tiles: rank 4 {64 cols, 2 column blocks, Hq heads,
-// rows}; one box is one 64-column block of `group` heads x 128 / group
-// queries -- the 128 packed rows of a query tile, 128B-swizzled.
-bool encode_q(CUtensorMap* tm, const void* base, int64_t rows, int Hq, int group) {
+// Tensor map over q [rows, Hq, D] (bf16, D = 64 or 128) for the prefill kernel's
+// query tiles: rank 4 {64 cols, D / 64 column blocks, Hq heads, rows}; one box is one
+// 64-column block of `group` heads x 128 / group queries -- the 128 packed rows of a
+// query tile, 128B-swizzled.  The kernel loads two column blocks; with D = 64 the
+// second starts past the tensor and lands as zeros.
+bool encode_q(CUtensorMap* tm, const void* base, int64_t rows, int Hq, int group, int D) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
-  cuuint64_t dims[4] = {64, 2, cuuint64_t(Hq), cuuint64_t(rows)};
-  cuuint64_t strides[3] = {128, 256, cuuint64_t(Hq) * 256};
+  const cuuint64_t hs = cuuint64_t(D) * 2;   // bytes of one head row
+  cuuint64_t dims[4] = {64, cuuint64_t(D / 64), cuuint64_t(Hq), cuuint64_t(rows)};
+  cuuint64_t strides[3] = {128, hs, cuuint64_t(Hq) * hs};
   cuuint32_t box[4] = {64, 1, cuuint32_t(group), cuuint32_t(bsr::kPrefillKeyTile / group)};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
@@ -248,7 +255,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
   if (s->n_pitems > 0) {
     // query tiles come straight from q (with RoPE the kernel rotates them in shared memory)
     if (s->tm_q_ptr != q) {
-      if (!encode_q(&s->tm_q, q, s->sum_qo, s->Hq, s->group)) {
+      if (!encode_q(&s->tm_q, q, s->sum_qo, s->Hq, s->group, s->D)) {
         s->tm_q_ptr = nullptr;
         return BSR_ERR_CUDA;
       }
@@ -259,8 +266,8 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     if (s->tm_pk_ptr != k_pages || s->tm_pv_ptr != v_pages) {
       const PoolGeom pgeom{rows, s->Hk, s->kv_layout == BSR_KV_NHD};
       // K and V alike: one box per page-sized piece of a tile (row-group layout)
-      if (rows <= 0 || !encode_pool_groups(&s->tm_pk, k_pages, pgeom, box_rows) ||
-          !encode_pool_groups(&s->tm_pv, v_pages, pgeom, box_rows)) {
+      if (rows <= 0 || !encode_pool_groups(&s->tm_pk, k_pages, pgeom, box_rows, s->D) ||
+          !encode_pool_groups(&s->tm_pv, v_pages, pgeom, box_rows, s->D)) {
         s->tm_pk_ptr = s->tm_pv_ptr = nullptr;
         return BSR_ERR_CUDA;
       }
@@ -292,6 +299,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.num_ctas = s->pre_ctas;
     p.window_left = s->window_left;
     p.nhd = s->kv_layout == BSR_KV_NHD;
+    p.head_dim = s->D;
     p.wait_limit_ns = wait_limit_ns;
     t_mark(1, 0);
     cudaError_t e =
@@ -308,6 +316,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
       m.Hq = s->Hq;
       m.group = s->group;
       m.out_f32 = p.out_f32;
+      m.head_dim = s->D;
       t_mark(2, 0);
       e = bsr::launch_prefill_merge(m, stream);
       t_mark(2, 1);

@@ -103,6 +103,46 @@ def test_prefill_one_tile_units_between_two_tile_units(rope):
     check_full(w, out, lse)
 
 
+@pytest.mark.parametrize("causal,P,rope", [(False, 16, 0.0), (True, 16, 1e4), (True, 32, 5e5),
+                                            (True, 256, 0.0)])
+def test_prefill_head_dim_64(causal, P, rope):
+    """head_dim 64 on the tensor-core kernel: the 128-wide tile program with the upper
+    64 dimensions of q, k and v landing as zeros, RoPE pairs 32 apart."""
+    w = wl.make_paged(f"pf64_{P}", 90 + P, [700, 333, 1300], Hq=16, Hk=4, D=64, P=P,
+                      qo_lens=[37, 16, 300], causal=causal, rope_theta=rope)
+    out, lse, s = run(w)
+    assert s.info()["num_prefill_items"] > 0
+    e_out, e_lse = check_full(w, out, lse)
+    print(f"head_dim 64 causal={causal} P={P} rope={rope}: out {e_out:.3e}, lse {e_lse:.3e}")
+
+
+@pytest.mark.parametrize("rope", [0.0, 1e4])
+def test_prefill_head_dim_64_split_ranges_and_nhd(rope):
+    """head_dim 64: key ranges split over CTAs and merged (fp32 out), and token-major
+    (NHD) pages, against the oracle."""
+    w = wl.make_paged("pf64split", 95, [20000], Hq=32, Hk=8, D=64, P=16, qo_lens=[64],
+                      causal=True, rope_theta=rope)
+    out, lse, s = run(w, out_dtype=torch.float32)
+    assert s.info()["num_prefill_items"] > s.info()["num_split_streams"] > 0
+    check_full(w, out, lse)
+    n = wl.to_nhd(wl.make_paged("pf64nhd", 96, [500, 900], Hq=16, Hk=4, D=64, P=16,
+                                qo_lens=[200, 129], causal=True, rope_theta=rope))
+    out, lse, s = run(n)
+    assert s.info()["num_prefill_items"] > 0
+    check_full(n, out, lse)
+
+
+def test_prefill_head_dim_64_fresh_prompt():
+    """A head_dim 64 prompt with no history: its first rows see a handful of keys.
+    Plain bars, with RoPE."""
+    w = wl.make_paged("pf64fresh", 97, [256, 300], Hq=16, Hk=4, D=64, P=16,
+                      qo_lens=[256, 300], causal=True, rope_theta=1e4)
+    out, lse, s = run(w)
+    assert s.info()["num_prefill_items"] > 0 and s.info()["num_decode_items"] == 0
+    e_out, e_lse = check_full(w, out, lse)
+    print(f"head_dim 64 fresh prompt: out {e_out:.3e}, lse {e_lse:.3e}")
+
+
 def test_prefill_v_beyond_fp16_range_sets_status():
     """P and V enter P.V as fp16: a V value beyond 65504 on the tensor-core path sets
     status bit 1 instead of passing silently; planning again clears the word."""

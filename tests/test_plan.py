@@ -25,7 +25,7 @@ def plan_of(w: wl.Paged, num_sms=152):
 def is_prefill(w: wl.Paged, b: int) -> bool:
     g = w.num_qo_heads // w.num_kv_heads
     rows = int(w.qo_indptr[b + 1] - w.qo_indptr[b]) * g
-    return w.head_dim == 128 and w.page_size >= 16 and rows >= 64 and 128 % g == 0
+    return w.page_size >= 16 and rows >= 64 and 128 % g == 0
 
 
 def check_coverage(w: wl.Paged, units: np.ndarray):
