@@ -384,6 +384,7 @@ def build_job(cfg: int, dev, small: bool):
                                  num_pages=w.num_pages, qo_indptr=w.qo_indptr, causal=w.causal,
                                  rope_theta=w.rope_theta, window_left=w.window_left,
                                  page_pos=w.page_pos, kv_layout=w.kv_layout,
+                                 kv_dtype="e4m3" if w.k_codes is not None else "bf16",
                                  schedule=schedule, stream=stream)
 
     job = {"parts": [], "schedules": []}

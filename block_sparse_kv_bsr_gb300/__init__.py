@@ -62,7 +62,7 @@ class _Info(ctypes.Structure):
         ("upload_bytes", ctypes.c_int64),
         ("decode_imbalance", ctypes.c_double), ("prefill_imbalance", ctypes.c_double),
         ("kernels_per_run", ctypes.c_int32), ("window_left", ctypes.c_int32),
-        ("kv_layout", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("kv_layout", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
     ]
 
 
@@ -80,13 +80,15 @@ def load(path: str | None = None):
     lib.bsr_attn_plan.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
                                   ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
-                                  ctypes.c_int32, ctypes.c_float, _vp, ctypes.POINTER(_vp)]
+                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _vp,
+                                  ctypes.POINTER(_vp)]
     lib.bsr_attn_plan_host.restype = ctypes.c_int
     lib.bsr_attn_plan_host.argtypes = [_vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
                                        ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
-                                       ctypes.c_int32, ctypes.c_float, ctypes.c_int32,
-                                       ctypes.POINTER(_Info), _vp, ctypes.c_int64]
+                                       ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
+                                       ctypes.c_int32, ctypes.POINTER(_Info), _vp,
+                                       ctypes.c_int64]
     lib.bsr_attn_run_kv8.restype = ctypes.c_int
     lib.bsr_attn_run_kv8.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                      ctypes.c_float, ctypes.c_float, ctypes.c_int32, _vp,
@@ -152,6 +154,13 @@ def _layout(kv_layout: str) -> int:
     if kv_layout not in ("HND", "NHD"):
         raise ValueError("kv_layout must be 'HND' or 'NHD'")
     return BSR_KV_NHD if kv_layout == "NHD" else BSR_KV_HND
+
+
+def _kv_dtype(kv_dtype: str) -> int:
+    """Cache element type: "bf16" (bsr_attn_run) or "e4m3" (bsr_attn_run_kv8)."""
+    if kv_dtype not in ("bf16", "e4m3"):
+        raise ValueError("kv_dtype must be 'bf16' or 'e4m3'")
+    return 1 if kv_dtype == "e4m3" else 0
 
 
 def _check(code: int, where: str):
@@ -243,16 +252,18 @@ def _plan_args(indptr, indices, last_page_len, qo_indptr):
 def bsr_attn_plan(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_heads: int,
                   head_dim: int, page_size: int, num_pages: int, qo_indptr=None,
                   causal: bool = False, rope_theta: float = 0.0, window_left: int = 0,
-                  page_pos=None, kv_layout: str = "HND", stream=None,
+                  page_pos=None, kv_layout: str = "HND", kv_dtype: str = "bf16", stream=None,
                   schedule: Schedule | None = None) -> Schedule:
-    """Plan one batch from HOST page-table arrays; returns (or re-plans) a Schedule."""
+    """Plan one batch from HOST page-table arrays; returns (or re-plans) a Schedule.
+    kv_dtype: "bf16" for bsr_attn_run, "e4m3" for bsr_attn_run_kv8."""
     lib = load()
     keep, (ip, ix, lp, qi), batch = _plan_args(indptr, indices, last_page_len, qo_indptr)
     handle = _vp(schedule.handle if schedule is not None else None)
     pp = (None, None) if page_pos is None else _host_i32_addr(page_pos)
     code = lib.bsr_attn_plan(ip, ix, lp, batch, num_qo_heads, num_kv_heads, head_dim, page_size,
                              qi, int(num_pages), int(bool(causal)), int(window_left), pp[1],
-                             _layout(kv_layout), float(rope_theta), _stream_ptr(stream),
+                             _layout(kv_layout), _kv_dtype(kv_dtype), float(rope_theta),
+                             _stream_ptr(stream),
                              ctypes.byref(handle))
     del keep
     _check(code, "bsr_attn_plan")
@@ -265,14 +276,15 @@ def bsr_attn_plan(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_h
 def bsr_attn_plan_host(indptr, indices, last_page_len, *, num_qo_heads: int, num_kv_heads: int,
                        head_dim: int, page_size: int, num_pages: int, num_sms: int,
                        qo_indptr=None, causal: bool = False, rope_theta: float = 0.0,
-                       window_left: int = 0, page_pos=None, kv_layout: str = "HND"):
+                       window_left: int = 0, page_pos=None, kv_layout: str = "HND",
+                       kv_dtype: str = "bf16"):
     """Host-only planning for `num_sms` SMs: returns (info dict, units int32 [n, 8])."""
     lib = load()
     keep, (ip, ix, lp, qi), batch = _plan_args(indptr, indices, last_page_len, qo_indptr)
     pp = (None, None) if page_pos is None else _host_i32_addr(page_pos)
     args = [ip, ix, lp, batch, num_qo_heads, num_kv_heads, head_dim, page_size, qi,
             int(num_pages), int(bool(causal)), int(window_left), pp[1],
-            _layout(kv_layout), float(rope_theta), int(num_sms)]
+            _layout(kv_layout), _kv_dtype(kv_dtype), float(rope_theta), int(num_sms)]
     info = _Info()
     n = lib.bsr_attn_plan_host(*args, ctypes.byref(info), None, 0)
     if n < 0:

@@ -52,15 +52,18 @@ constexpr int kD8 = 128;                                      // head dim (bytes
 constexpr int kTile8 = kStageTokens * kD8;                    // one K (or V) stage: 2 KB
 constexpr int kStage8 = 2 * kTile8;
 constexpr int kStages8 = BSR_DECODE_STAGES_KV8;
-constexpr size_t kSmem8 = size_t(kDecodeWarps) * kStages8 * kStage8 +
-                          size_t(kDecodeWarps) * kStages8 * 8 + 1024;
 // RoPE: one table row per stage (the angles of the stage's first key, pair order:
 // D / 4 float4 (cos f, cos f+1, sin f, sin f+1)) beside the ring, and the CTA's 16
 // offset rows t < 16 (times the operand scale)
 constexpr int kRowBytes8 = kD8 / 4 * 16;
-constexpr size_t kSmem8Rope = kSmem8 + size_t(kDecodeWarps) * kStages8 * kRowBytes8 +
-                              size_t(kStageTokens) * kRowBytes8;
-static_assert(kSmem8Rope <= 232448, "FP8 decode stages exceed the shared memory of one SM");
+// dynamic shared memory of a CTA: the warps' rings and barriers (+ RoPE rows)
+constexpr size_t smem8(bool rope) {
+  const size_t w = size_t(decode_kv8_warps(rope));
+  return w * kStages8 * kStage8 + w * kStages8 * 8 + 1024 +
+         (rope ? w * kStages8 * kRowBytes8 + size_t(kStageTokens) * kRowBytes8 : 0);
+}
+static_assert(smem8(false) <= 232448 && smem8(true) <= 232448,
+              "FP8 decode stages exceed the shared memory of one SM");
 
 // Byte offset of (token t, 16-byte chunk c of 8) in a [16 rows][128 B] tile with
 // the TMA 128-byte swizzle.
@@ -97,7 +100,7 @@ __device__ __forceinline__ void rotate2(float2& x, float2& y, float2 c, float2 s
 }
 
 template <bool R16, bool WIN, bool ROPE>
-__global__ void __launch_bounds__(kDecodeWarps * 32, 1)
+__global__ void __launch_bounds__(decode_kv8_warps(ROPE) * 32, 1)
     bsr_decode_kv8_kernel(const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const DecodeParams p) {
   constexpr int D = kD8;
@@ -115,14 +118,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   const uint32_t base = (ptx::smem_u32(smem_raw) + 1023u) & ~1023u;
   uint8_t* const base_ptr = smem_raw + (base - ptx::smem_u32(smem_raw));
   // RoPE: this warp's per-stage table rows, then the CTA's offset rows
-  const uint32_t grows = base + uint32_t(kDecodeWarps * kStages8 * (kStage8 + 8) +
+  constexpr int W = decode_kv8_warps(ROPE);   // warps of this CTA
+  const uint32_t grows = base + uint32_t(W * kStages8 * (kStage8 + 8) +
                                          warp * kStages8 * kRowBytes8);
   const uint8_t* const grows_ptr = base_ptr + (grows - base);
   uint8_t* const frows_ptr =
-      base_ptr + kDecodeWarps * kStages8 * (kStage8 + 8) + kDecodeWarps * kStages8 * kRowBytes8;
+      base_ptr + W * kStages8 * (kStage8 + 8) + W * kStages8 * kRowBytes8;
   if constexpr (ROPE) {
     const float4* src = reinterpret_cast<const float4*>(p.rope);
-    for (int i = threadIdx.x; i < kStageTokens * (kD8 / 4); i += kDecodeWarps * 32) {
+    for (int i = threadIdx.x; i < kStageTokens * (kD8 / 4); i += W * 32) {
       const float4 v = __ldg(src + i);
       reinterpret_cast<float4*>(frows_ptr)[i] =
           make_float4(v.x * kRopeOperandScale, v.y * kRopeOperandScale, v.z * kRopeOperandScale,
@@ -130,13 +134,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     }
     __syncthreads();
   }
-  const int gw = blockIdx.x * kDecodeWarps + warp;
+  const int gw = blockIdx.x * W + warp;
   if (gw >= p.num_warps) return;
   const int it_begin = __ldg(p.warp_ptr + gw), it_end = __ldg(p.warp_ptr + gw + 1);
   if (it_begin >= it_end) return;
 
   const uint32_t ring = base + uint32_t(warp * kStages8 * kStage8);
-  const uint32_t bars = base + uint32_t(kDecodeWarps * kStages8 * kStage8 + warp * kStages8 * 8);
+  const uint32_t bars = base + uint32_t(W * kStages8 * kStage8 + warp * kStages8 * 8);
   if (lane == 0) {
 #pragma unroll
     for (int s = 0; s < kStages8; ++s) ptx::mbar_init(bars + 8 * s, 1);
@@ -678,9 +682,12 @@ constexpr int kMaxDevices = 64;
 
 template <bool R16, bool WIN, bool ROPE>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                       int grid, cudaStream_t stream) {
+                       cudaStream_t stream) {
   auto kern = bsr_decode_kv8_kernel<R16, WIN, ROPE>;
-  constexpr size_t smem = ROPE ? kSmem8Rope : kSmem8;
+  constexpr int W = decode_kv8_warps(ROPE);
+  constexpr size_t smem = smem8(ROPE);
+  const int grid = (p.num_warps + W - 1) / W;
+  if (grid <= 0) return cudaSuccess;
   static std::atomic<bool> opted_in[kMaxDevices];   // zero-initialized: false
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -691,25 +698,25 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Decod
     if (e != cudaSuccess) return e;
     opted_in[dev].store(true, std::memory_order_release);
   }
-  const cudaError_t le = launch_pdl(kern, grid, kDecodeWarps * 32, smem, stream, tk, tv, p);
+  const cudaError_t le = launch_pdl(kern, grid, W * 32, smem, stream, tk, tv, p);
   return le != cudaSuccess ? le : cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode_kv8(bool rope, bool r16, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const DecodeParams& p, int grid, cudaStream_t stream) {
+                              const DecodeParams& p, cudaStream_t stream) {
   const bool win = p.window_left > 0;
   if (rope) {
-    if (r16) return win ? launch_one<true, true, true>(tk, tv, p, grid, stream)
-                        : launch_one<true, false, true>(tk, tv, p, grid, stream);
-    return win ? launch_one<false, true, true>(tk, tv, p, grid, stream)
-               : launch_one<false, false, true>(tk, tv, p, grid, stream);
+    if (r16) return win ? launch_one<true, true, true>(tk, tv, p, stream)
+                        : launch_one<true, false, true>(tk, tv, p, stream);
+    return win ? launch_one<false, true, true>(tk, tv, p, stream)
+               : launch_one<false, false, true>(tk, tv, p, stream);
   }
-  if (r16) return win ? launch_one<true, true, false>(tk, tv, p, grid, stream)
-                      : launch_one<true, false, false>(tk, tv, p, grid, stream);
-  return win ? launch_one<false, true, false>(tk, tv, p, grid, stream)
-             : launch_one<false, false, false>(tk, tv, p, grid, stream);
+  if (r16) return win ? launch_one<true, true, false>(tk, tv, p, stream)
+                      : launch_one<true, false, false>(tk, tv, p, stream);
+  return win ? launch_one<false, true, false>(tk, tv, p, stream)
+             : launch_one<false, false, false>(tk, tv, p, stream);
 }
 
 }  // namespace bsr

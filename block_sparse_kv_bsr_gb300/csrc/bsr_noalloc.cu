@@ -252,7 +252,8 @@ int noalloc_impl(const void* q, const void* k_pages, const void* v_pages, const 
   // Equal split per (request, kv head): enough units to cover every warp slot of the
   // persistent grid, never more than the scratch holds.
   const int64_t pairs = int64_t(batch) * num_kv_heads;
-  const int64_t want = int64_t(sms) * kDecodeWarps;
+  // (the FP8 kernel keeps decode_kv8_warps(false) warps per SM, the bf16 one kDecodeWarps)
+  const int64_t want = int64_t(sms) * (kv8 ? bsr::decode_kv8_warps(false) : kDecodeWarps);
   int64_t splits = (want + pairs - 1) / pairs;
   if (splits > kMaxSplits) splits = kMaxSplits;
   if (splits * pairs > kMaxUnits) splits = kMaxUnits / pairs;
@@ -309,7 +310,7 @@ int noalloc_impl(const void* q, const void* k_pages, const void* v_pages, const 
   const int grid = (units + kDecodeWarps - 1) / kDecodeWarps;
   const bool r16 = group > 8;
   const cudaError_t e =
-      kv8 ? bsr::launch_decode_kv8(false, r16, tk, tv, p, grid, stream)
+      kv8 ? bsr::launch_decode_kv8(false, r16, tk, tv, p, stream)
           : head_dim == 128 ? bsr::launch_decode_d128(false, r16, smallp, tk, tv, p, grid, stream)
                             : bsr::launch_decode_d64(false, r16, smallp, tk, tv, p, grid, stream);
   if (e != cudaSuccess) {

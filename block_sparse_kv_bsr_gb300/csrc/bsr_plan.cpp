@@ -56,6 +56,10 @@ constexpr int64_t kPrefillMinPiece = 512;
 constexpr int64_t kPrefillMinCtaWork = 1024;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+// warps per SM that the decode kernel of a cache type keeps
+int decode_warps_per_sm(int32_t kv_dtype, bool rope) {
+  return kv_dtype == BSR_KV_DTYPE_E4M3 ? bsr::decode_kv8_warps(rope) : kDecodeWarps;
+}
 bool is_pow2(int64_t x) { return x > 0 && (x & (x - 1)) == 0; }
 
 // A (request, kv head, row group) range of keys before chunking.
@@ -441,6 +445,7 @@ struct HostPlan {
   int64_t sum_qo = 0, active = 0;
   int32_t max_len = 0, max_rows = 0;
   WorkList dec;   // split-KV decode kernel, workers = warps
+  int32_t dec_warps_per_cta = 0;   // warps of one decode CTA (one CTA per SM)
   WorkList pre;   // tensor-core prefill kernel, workers = CTAs
   std::vector<DecodeItem> pmerge;   // one entry per prefill unit whose key range was split
   // per-page positions: logical minus cached end of each request, and one past the
@@ -456,7 +461,7 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
                    int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                    int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
                    int32_t causal, int32_t window_left, const int32_t* page_pos,
-                   float rope_theta, int num_sms, HostPlan* hp) {
+                   float rope_theta, int num_sms, int dec_warps_per_sm, HostPlan* hp) {
   if (indptr == nullptr || batch < 0 || num_pages_in_pool < 0 || num_sms <= 0)
     return BSR_ERR_INVALID_ARGUMENT;
   if (batch > 0 && last_page_len == nullptr) return BSR_ERR_INVALID_ARGUMENT;
@@ -583,7 +588,7 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   }
   // consecutive plans of a serving loop are alike: start from the last budget step
   thread_local int64_t dec_k = -1;
-  balance(dunits, int64_t(num_sms) * kDecodeWarps, std::max<int64_t>(page_size, kStageTokens),
+  balance(dunits, int64_t(num_sms) * dec_warps_per_sm, std::max<int64_t>(page_size, kStageTokens),
           kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec, &dec_k, kMinPieceSmall);
   balance_gangs(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillKeyTile),
                 kPrefillOverhead, kPrefillMinPiece, kPrefillMinCtaWork, &hp->pre);
@@ -591,6 +596,7 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   for (const DecodeItem& it : hp->pre.items)
     if (it.slot >= 0 && it.slot == it.first_slot) hp->pmerge.push_back(it);
 
+  hp->dec_warps_per_cta = dec_warps_per_sm;
   hp->group = group;
   hp->sum_qo = sum_qo;
   hp->active = active;
@@ -606,8 +612,10 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
                              int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                              const int32_t* qo_indptr, int32_t num_pages_in_pool, int32_t causal,
                              int32_t window_left, const int32_t* page_pos, int32_t kv_layout,
-                             float rope_theta, void* stream_v, bsr_schedule_t* schedule) {
+                             int32_t kv_dtype, float rope_theta, void* stream_v,
+                             bsr_schedule_t* schedule) {
   if (kv_layout != BSR_KV_HND && kv_layout != BSR_KV_NHD) return BSR_ERR_INVALID_ARGUMENT;
+  if (kv_dtype != BSR_KV_DTYPE_BF16 && kv_dtype != BSR_KV_DTYPE_E4M3) return BSR_ERR_INVALID_ARGUMENT;
   if (schedule == nullptr) return BSR_ERR_INVALID_ARGUMENT;
   const cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   const bool rope = rope_theta > 0.f;
@@ -621,7 +629,8 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   thread_local HostPlan hp;   // reused: its vectors keep their memory between plans
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
-                                window_left, page_pos, rope_theta, num_sms, &hp);
+                                window_left, page_pos, rope_theta, num_sms,
+                                decode_warps_per_sm(kv_dtype, rope), &hp);
   if (rc != BSR_OK) return rc;
   const int64_t nnz = indptr[batch];
 
@@ -768,6 +777,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->causal = causal;
   s->window_left = window_left;
   s->kv_layout = kv_layout;
+  s->kv_dtype = kv_dtype;
   s->tm_k_ptr = s->tm_v_ptr = nullptr;      // the maps depend on the layout
   s->tm_k8_ptr = s->tm_v8_ptr = nullptr;
   s->rope_theta = rope_theta;
@@ -780,7 +790,8 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->n_partials = hp.dec.n_partials;
   s->n_split = hp.dec.n_split;
   s->dec_warps = hp.dec.workers;
-  s->dec_ctas = (hp.dec.workers + kDecodeWarps - 1) / kDecodeWarps;
+  s->dec_ctas = (hp.dec.workers + hp.dec_warps_per_cta - 1) / hp.dec_warps_per_cta;
+  s->dec_warps_per_cta = hp.dec_warps_per_cta;
   s->dec_imbalance = hp.dec.imbalance;
   s->n_pitems = int32_t(hp.pre.items.size());
   s->n_ppartials = hp.pre.n_partials;
@@ -852,6 +863,7 @@ extern "C" int bsr_schedule_get_info(bsr_schedule_t s, bsr_schedule_info_t* info
   info->causal = s->causal;
   info->window_left = s->window_left;
   info->kv_layout = s->kv_layout;
+  info->kv_dtype = s->kv_dtype;
   info->rope_theta = s->rope_theta;
   info->sum_qo = s->sum_qo;
   info->active_tokens = s->active_tokens;
@@ -860,7 +872,7 @@ extern "C" int bsr_schedule_get_info(bsr_schedule_t s, bsr_schedule_info_t* info
   info->num_split_streams = s->n_split + s->n_psplit;
   info->num_partials = s->n_partials + s->n_ppartials;
   info->decode_ctas = s->dec_ctas;
-  info->decode_warps_per_cta = kDecodeWarps;
+  info->decode_warps_per_cta = s->dec_warps_per_cta;
   info->prefill_ctas = s->pre_ctas;
   info->num_sms = s->num_sms;
   info->workspace_bytes = int64_t(s->ws_used);
@@ -878,13 +890,16 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
                                   int32_t page_size, const int32_t* qo_indptr,
                                   int32_t num_pages_in_pool, int32_t causal,
                                   int32_t window_left, const int32_t* page_pos,
-                                  int32_t kv_layout, float rope_theta, int32_t num_sms,
-                                  bsr_schedule_info_t* info, int32_t* units, int64_t max_units) {
+                                  int32_t kv_layout, int32_t kv_dtype, float rope_theta,
+                                  int32_t num_sms, bsr_schedule_info_t* info, int32_t* units,
+                                  int64_t max_units) {
   if (kv_layout != BSR_KV_HND && kv_layout != BSR_KV_NHD) return BSR_ERR_INVALID_ARGUMENT;
+  if (kv_dtype != BSR_KV_DTYPE_BF16 && kv_dtype != BSR_KV_DTYPE_E4M3) return BSR_ERR_INVALID_ARGUMENT;
   thread_local HostPlan hp;   // reused: its vectors keep their memory between plans
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
-                                window_left, page_pos, rope_theta, num_sms, &hp);
+                                window_left, page_pos, rope_theta, num_sms,
+                                decode_warps_per_sm(kv_dtype, rope_theta > 0.f), &hp);
   if (rc != BSR_OK) return rc;
   if (info != nullptr) {
     std::memset(info, 0, sizeof(*info));
@@ -896,6 +911,7 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
     info->causal = causal;
     info->window_left = window_left;
     info->kv_layout = kv_layout;
+    info->kv_dtype = kv_dtype;
     info->rope_theta = rope_theta;
     info->sum_qo = hp.sum_qo;
     info->active_tokens = hp.active;
@@ -903,8 +919,8 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
     info->num_prefill_items = int32_t(hp.pre.items.size());
     info->num_split_streams = hp.dec.n_split + hp.pre.n_split;
     info->num_partials = hp.dec.n_partials + hp.pre.n_partials;
-    info->decode_ctas = (hp.dec.workers + kDecodeWarps - 1) / kDecodeWarps;
-    info->decode_warps_per_cta = kDecodeWarps;
+    info->decode_ctas = (hp.dec.workers + hp.dec_warps_per_cta - 1) / hp.dec_warps_per_cta;
+    info->decode_warps_per_cta = hp.dec_warps_per_cta;
     info->prefill_ctas = hp.pre.workers;
     info->num_sms = num_sms;
     info->decode_imbalance = hp.dec.imbalance;

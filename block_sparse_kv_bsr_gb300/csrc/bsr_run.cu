@@ -167,6 +167,7 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
   if (!(sm_scale > 0.f) || !std::isfinite(sm_scale)) return BSR_ERR_INVALID_ARGUMENT;
   if (out_dtype != BSR_DTYPE_BF16 && out_dtype != BSR_DTYPE_F32) return BSR_ERR_INVALID_ARGUMENT;
   if (rope_theta != s->rope_theta || causal != s->causal) return BSR_ERR_SCHEDULE_MISMATCH;
+  if (s->kv_dtype != BSR_KV_DTYPE_BF16) return BSR_ERR_SCHEDULE_MISMATCH;   // planned for FP8
   if (s->n_items == 0 && s->n_pitems == 0) return BSR_OK;
   if (q == nullptr || out == nullptr || k_pages == nullptr || v_pages == nullptr)
     return BSR_ERR_INVALID_ARGUMENT;
@@ -383,6 +384,7 @@ extern "C" int bsr_attn_run_kv8(bsr_schedule_t s, const void* q, const void* k_p
     return BSR_ERR_INVALID_ARGUMENT;
   if (out_dtype != BSR_DTYPE_BF16 && out_dtype != BSR_DTYPE_F32) return BSR_ERR_INVALID_ARGUMENT;
   if (rope_theta != s->rope_theta || causal != s->causal) return BSR_ERR_SCHEDULE_MISMATCH;
+  if (s->kv_dtype != BSR_KV_DTYPE_E4M3) return BSR_ERR_SCHEDULE_MISMATCH;   // planned for bf16
   // the FP8 path covers the decode kernel's work: D = 128, pages of at least 16
   // keys, every request on the decode kernel (RoPE included)
   if (s->D != 128 || s->P < bsr::kStageTokens || s->n_pitems > 0) return BSR_ERR_UNSUPPORTED;
@@ -450,8 +452,7 @@ extern "C" int bsr_attn_run_kv8(bsr_schedule_t s, const void* q, const void* k_p
   p.plan_uploaded = 1;   // the work list and page table came with the plan's copy
   p.wait_limit_ns = 1000000000ull;
   t_mark(0, 0);
-  const cudaError_t e = bsr::launch_decode_kv8(rope, s->max_rows > 8, s->tm_k8, s->tm_v8, p,
-                                               s->dec_ctas, stream);
+  const cudaError_t e = bsr::launch_decode_kv8(rope, s->max_rows > 8, s->tm_k8, s->tm_v8, p, stream);
   t_mark(0, 1);
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -23,6 +23,7 @@ struct bsr_schedule {
   int32_t rope_rows = 0;       // rows of the cos/sin table (0 without RoPE)
   int32_t window_left = 0;     // sliding window (0: none)
   int32_t kv_layout = 0;       // BSR_KV_HND or BSR_KV_NHD
+  int32_t kv_dtype = 0;        // BSR_KV_DTYPE_BF16 or BSR_KV_DTYPE_E4M3 (sets the decode warps)
   // per-page logical positions for RoPE (uploaded with the image when given)
   bool has_page_pos = false;
   size_t off_page_pos = 0, off_qshift = 0;
@@ -30,6 +31,7 @@ struct bsr_schedule {
 
   // decode plan
   int32_t n_items = 0, n_partials = 0, n_split = 0, dec_warps = 0, dec_ctas = 0;
+  int32_t dec_warps_per_cta = 0;   // warps one decode CTA runs (one CTA per SM)
   double dec_imbalance = 0.0;
   // prefill plan (tensor-core kernel)
   int32_t n_pitems = 0, n_ppartials = 0, n_psplit = 0, pre_ctas = 0;
@@ -98,8 +100,9 @@ cudaError_t launch_decode_d64(bool rope, bool r16, bool smallp, const CUtensorMa
 cudaError_t launch_decode_d128(bool rope, bool r16, bool smallp, const CUtensorMap& tk,
                                const CUtensorMap& tv, const DecodeParams& p, int grid,
                                cudaStream_t stream);
+// the grid is one CTA of decode_kv8_warps(rope) warps per p.num_warps of them
 cudaError_t launch_decode_kv8(bool rope, bool r16, const CUtensorMap& tk, const CUtensorMap& tv,
-                              const DecodeParams& p, int grid, cudaStream_t stream);
+                              const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const PrefillParams& p, int grid,
                            cudaStream_t stream);

@@ -69,7 +69,7 @@ enum {
 enum { BSR_DTYPE_BF16 = 0, BSR_DTYPE_F32 = 1 };
 /* page pool layouts: head-major [pages, Hk, P, D] or token-major [pages, P, Hk, D] */
 enum { BSR_KV_HND = 0, BSR_KV_NHD = 1 };
-/* element type of a KV cache (bsr_attn_decode_noalloc_ex) */
+/* element type of a KV cache (bsr_attn_plan, bsr_attn_decode_noalloc_ex) */
 enum { BSR_KV_DTYPE_BF16 = 0, BSR_KV_DTYPE_E4M3 = 1 };
 
 typedef struct bsr_schedule* bsr_schedule_t;
@@ -119,6 +119,12 @@ typedef struct bsr_schedule* bsr_schedule_t;
  * token's heads contiguous, the token-major layout some serving engines keep).
  * Every run of the schedule reads k_pages / v_pages in that layout.
  *
+ * kv_dtype: BSR_KV_DTYPE_BF16 (the schedule runs with bsr_attn_run) or
+ * BSR_KV_DTYPE_E4M3 (with bsr_attn_run_kv8).  The decode work is balanced over
+ * the warps the cache's decode kernel keeps per SM -- 12 for an FP8 cache without
+ * RoPE (its stages are half the bytes, so more warps hide the latency), 8
+ * otherwise; a run of the other type returns BSR_ERR_SCHEDULE_MISMATCH.
+ *
  * *schedule must be NULL (a new schedule is created) or a schedule returned
  * by an earlier plan or by bsr_schedule_create, which is then (re-)planned in
  * place: its device workspace is reused when large enough.  Re-planning is ordered on `stream` after work
@@ -130,7 +136,8 @@ int bsr_attn_plan(const int32_t* indptr, const int32_t* indices, const int32_t* 
                   int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                   int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
                   int32_t causal, int32_t window_left, const int32_t* page_pos,
-                  int32_t kv_layout, float rope_theta, void* stream, bsr_schedule_t* schedule);
+                  int32_t kv_layout, int32_t kv_dtype, float rope_theta, void* stream,
+                  bsr_schedule_t* schedule);
 
 /*
  * bsr_schedule_create — an empty schedule, bound to the current CUDA device,
@@ -154,7 +161,8 @@ int bsr_schedule_create(int32_t sm_budget, bsr_schedule_t* schedule);
  * read; out (out_dtype: BSR_DTYPE_BF16 or BSR_DTYPE_F32) and lse (fp32, may
  * be NULL) are written.  All are caller-owned device buffers; no buffer may
  * alias another.  sm_scale must be finite and > 0.  rope_theta and causal
- * must equal the values given to plan (else BSR_ERR_SCHEDULE_MISMATCH).
+ * must equal the values given to plan, which was for BSR_KV_DTYPE_BF16 (else
+ * BSR_ERR_SCHEDULE_MISMATCH).
  * q, k_pages, v_pages and out must be 16-byte aligned (else
  * BSR_ERR_INVALID_ARGUMENT).
  * The call allocates nothing, never synchronizes the host, and is
@@ -177,8 +185,9 @@ int bsr_attn_run(bsr_schedule_t schedule, const void* q, const void* k_pages, co
  * that conversion, RoPE and dequantisation fused into one kernel ("JIT 컴파일은
  * …" names both): the rotated q and k enter Q K^T as fp16 x 2^-4, as on the
  * bf16 path, at the positions the plan gives (page_pos included).
- * Everything else (q bf16, out, lse, alignment, ownership, stream semantics)
- * is as for bsr_attn_run.  Covered: head_dim 128, page_size >= 16, every
+ * The schedule must be planned with kv_dtype BSR_KV_DTYPE_E4M3 (else
+ * BSR_ERR_SCHEDULE_MISMATCH).  Everything else (q bf16, out, lse, alignment,
+ * ownership, stream semantics) is as for bsr_attn_run.  Covered: head_dim 128, page_size >= 16, every
  * request on the decode kernel (info.num_prefill_items == 0); other schedules
  * return BSR_ERR_UNSUPPORTED.
  */
@@ -249,7 +258,7 @@ typedef struct bsr_schedule_info {
                                  split-range merge; 0 when there is no work) */
   int32_t window_left;        /* sliding window given to plan (0: none) */
   int32_t kv_layout;          /* BSR_KV_HND or BSR_KV_NHD */
-  int32_t reserved;
+  int32_t kv_dtype;           /* BSR_KV_DTYPE_BF16 or BSR_KV_DTYPE_E4M3 (as planned) */
 } bsr_schedule_info_t;
 
 int bsr_schedule_get_info(bsr_schedule_t schedule, bsr_schedule_info_t* info);
@@ -289,8 +298,8 @@ int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
                        int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                        const int32_t* qo_indptr, int32_t num_pages_in_pool, int32_t causal,
                        int32_t window_left, const int32_t* page_pos, int32_t kv_layout,
-                       float rope_theta, int32_t num_sms, bsr_schedule_info_t* info,
-                       int32_t* units, int64_t max_units);
+                       int32_t kv_dtype, float rope_theta, int32_t num_sms,
+                       bsr_schedule_info_t* info, int32_t* units, int64_t max_units);
 
 /*
  * bsr_attn_decode_noalloc — decode attention that allocates nothing.

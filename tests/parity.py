@@ -34,6 +34,7 @@ def plan(w: wl.Paged, schedule=None):
                              qo_indptr=w.qo_indptr, causal=w.causal, rope_theta=w.rope_theta,
                              window_left=w.window_left, page_pos=w.page_pos,
                              kv_layout=w.kv_layout,
+                             kv_dtype="e4m3" if w.k_codes is not None else "bf16",
                              schedule=schedule)
 
 

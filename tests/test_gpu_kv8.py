@@ -94,6 +94,26 @@ def test_kv8_causal_multi_query_rows():
     check_full_kv8(w, out, lse)
 
 
+def test_schedule_planned_for_the_other_cache_type_is_refused():
+    """bsr_attn_run_kv8 needs a schedule planned with kv_dtype "e4m3" (its decode work is
+    spread over the FP8 kernel's warps), bsr_attn_run one planned for "bf16"."""
+    dev = "cuda:0"
+    w = wl.with_kv8(wl.make_paged("kv8mis", 74, [100, 200], Hq=32, Hk=8, D=128, P=16), 704)
+    kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+              page_size=w.page_size, num_pages=w.num_pages)
+    s16 = bsr.bsr_attn_plan(w.indptr, w.indices, w.last_page_len, kv_dtype="bf16", **kw)
+    with pytest.raises(bsr.BsrError) as e:
+        bsr.bsr_attn_run_kv8(s16, w.q.to(dev), w.k_codes.to(dev), w.v_codes.to(dev),
+                             k_scale=w.k_scale, v_scale=w.v_scale, sm_scale=w.sm_scale)
+    assert e.value.code == -7
+    s8 = bsr.bsr_attn_plan(w.indptr, w.indices, w.last_page_len, kv_dtype="e4m3", **kw)
+    assert s8.info()["decode_warps_per_cta"] == 12
+    with pytest.raises(bsr.BsrError) as e:
+        bsr.bsr_attn_run(s8, w.q.to(dev), w.k_pages.to(dev), w.v_pages.to(dev),
+                         sm_scale=w.sm_scale)
+    assert e.value.code == -7
+
+
 def test_kv8_unsupported_schedules_are_refused():
     dev = "cuda:0"
     cases = [

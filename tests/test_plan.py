@@ -111,6 +111,26 @@ def test_skewed_batch_is_balanced():
     assert info["num_split_streams"] >= 13 * 8     # every long (request, head) range is cut
 
 
+@pytest.mark.parametrize("rope,warps", [(0.0, 12), (5e5, 8)])
+def test_fp8_cache_plans_for_its_kernel_warps(rope, warps):
+    """An FP8 (E4M3) schedule spreads the decode work over the FP8 kernel's warps per SM
+    (12 without RoPE, 8 with), still covering every key once and balanced; bf16 keeps 8."""
+    w = wl.config3(small=False)
+    w.rope_theta = rope
+    kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+              page_size=w.page_size, num_pages=w.num_pages, num_sms=152, rope_theta=rope)
+    info, units = bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len,
+                                         kv_dtype="e4m3", **kw)
+    check_coverage(w, units)
+    assert info["kv_dtype"] == 1 and info["decode_warps_per_cta"] == warps
+    assert info["decode_ctas"] == 152 and units[:, 7].max() < 152 * warps
+    assert info["decode_imbalance"] < 1.05
+    info16, _ = bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len, **kw)
+    assert info16["kv_dtype"] == 0 and info16["decode_warps_per_cta"] == 8
+    with pytest.raises(ValueError):
+        bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len, kv_dtype="fp8", **kw)
+
+
 def test_uniform_batch_is_balanced():
     w = wl.config2(small=False)
     info, units = plan_of(w, num_sms=152)
