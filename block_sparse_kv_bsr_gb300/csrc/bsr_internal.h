@@ -29,12 +29,6 @@ constexpr int kMaxDecodeRows = 16;
 #define BSR_DECODE_STAGES_D64 6
 #endif
 constexpr int kDecodeWarps = BSR_DECODE_WARPS;
-// Warps per CTA (one CTA per SM) of the FP8 (E4M3) decode kernel.  Without RoPE a
-// 16-key stage is half the bf16 kernel's bytes and each warp's chain of conversions
-// and MMAs is latency-bound, so 12 warps (a 170-register cap; 4 stages each) keep
-// more stages in flight: 88 against 97.5 us on the skewed batch (10 warps measured
-// 100 us).  With RoPE (253 registers) 12 warps spill heavily, so it keeps 8.
-__host__ __device__ constexpr int decode_kv8_warps(bool rope) { return rope ? kDecodeWarps : 12; }
 
 // One decode work unit: rows [row0, row0 + nrows) of the packed rows of
 // (request req, kv head kvh) against keys [tok0, tok1).  Packed row R is

@@ -93,6 +93,13 @@ struct bsr_schedule {
 };
 
 namespace bsr {
+// Warps per CTA (one CTA per SM) of the FP8 (E4M3) decode kernel.  Without RoPE a
+// 16-key stage is half the bf16 kernel's bytes and each warp's chain of conversions
+// and MMAs is latency-bound, so 12 warps (a 170-register cap; 4 stages each) keep
+// more stages in flight: 88 against 97.5 us on the skewed batch (10 warps measured
+// 100 us).  With RoPE (253 registers) 12 warps spill heavily, so it keeps 8.
+__host__ __device__ constexpr int decode_kv8_warps(bool rope) { return rope ? kDecodeWarps : 12; }
+
 // Kernel launchers (one translation unit per head dim).
 cudaError_t launch_decode_d64(bool rope, bool r16, bool smallp, const CUtensorMap& tk,
                               const CUtensorMap& tv, const DecodeParams& p, int grid,
