@@ -967,7 +967,7 @@ def main():
     gc.collect()
     torch.cuda.empty_cache()
 
-    # ---- the other workloads (the benchmark spec's five configurations first, then the extended
+    # ---- the other workloads (the five headline configurations first, then the extended
     # ones), each hot and cold, on rank 0 of a single-GPU run
     if world == 1 and args.configs:
         res["configs"] = {}
