@@ -17,10 +17,12 @@ e2e       = the same bytes / time of the call a user makes with HOST buffers: pe
             plan of the page table (on the host, overlapping the previous step's kernel as
             a serving loop would), H2D of q and the plan, run, D2H of out and lse, and the
             host's wait for them; the serialised form is reported beside it.
-roofline  = the dominant kernel's algorithmic bytes (or FLOPs) / its mean CUDA-event
-            duration, against the measured HBM copy bandwidth (or bf16 dense peak); also
-            its p10 / median / p90 over the timed calls and the DRAM traffic from the
-            committed ncu summary of the same build.
+roofline  = the dominant kernel's algorithmic bytes (or FLOPs) / its mean launch duration,
+            against the measured HBM copy bandwidth (or bf16 dense peak).  A step of one
+            kernel launch is timed as K back-to-back steps with CUDA events at their ends
+            only; steps of several kernels by the library's stage events around each
+            kernel (which also give p10 / median / p90 per call for every workload).  The
+            DRAM traffic comes from the committed ncu summary of the same build.
 cpu_baseline = the fp64 oracle on this host's cores over whole passes for ~10 s (decode
             workloads; configs 1 and 2 add a one-thread figure).
 clocks    = SM clock and clock-event reasons polled through NVML every ~0.5 ms during the
@@ -641,6 +643,19 @@ def build_job(cfg: int, dev, small: bool):
     return job
 
 
+def region_steps(step, steps, stream):
+    """Device time per step (ms) of `steps` back-to-back steps, CUDA events at the ends."""
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / steps
+
+
 def timed_steps(step, steps, stream, flush=None):
     """Device time (ms) of each of `steps` steps, CUDA events around each on `stream`.
     With `flush` (an int32 tensor over twice the L2), every step is preceded, outside
@@ -728,15 +743,23 @@ def spread(ms):
             "us_p10": round(dec[0] * 1e3, 2), "us_p90": round(dec[-1] * 1e3, 2)}
 
 
-def roofline_of(parts, _build):
+def roofline_of(parts, _build, whole_ms=None, whole_by=None):
     """Roofline of the call that takes the most time in a step (among the attention
-    kernels' calls): its algorithmic bytes or FLOPs over its kernel's mean duration."""
+    kernels' calls): its algorithmic bytes or FLOPs over its kernel's mean duration.
+    When a step is one call launching one kernel, `whole_ms` -- the per-step time of K
+    back-to-back steps timed with events only at their ends (or replayed from a CUDA
+    graph) -- is that kernel's mean launch duration, without the event records the
+    per-kernel pass inserts between launches (a few us each); the per-kernel figures are
+    reported beside it."""
     peak_hbm, hbm_kind = peaks()
     peak_tensor, tensor_kind = tensor_peak()
     dom = max([pt for pt in parts if pt.family is not None] or parts, key=lambda pt: sum(pt.ms))
     call_ms = sum(dom.ms) / len(dom.ms)
     kms = dom.kernel_ms if dom.kernel_ms else dom.ms
     dom_ms = sum(kms) / len(kms)
+    one_kernel = whole_ms is not None and len(parts) == 1 and dom.launches == 1
+    if one_kernel:
+        dom_ms = whole_ms
     sources = {"decode": _build.DECODE_KERNEL_SOURCES,
                "decode_kv8": _build.DECODE_KV8_KERNEL_SOURCES,
                "prefill": _build.PREFILL_KERNEL_SOURCES}.get(dom.family)
@@ -756,8 +779,11 @@ def roofline_of(parts, _build):
             "kernel_us_mean": sp["us_mean"], "kernel_us_min": round(min(kms) * 1e3, 2),
             "kernel_us_p10": sp["us_p10"], "kernel_us_median": sp["us_median"],
             "kernel_us_p90": sp["us_p90"],
-            "timed_by": ("library stage events around the kernel" if dom.kernel_ms
+            "kernel_us_launch": round(dom_ms * 1e3, 2),
+            "timed_by": whole_by if one_kernel else
+                        ("library stage events around the kernel" if dom.kernel_ms
                          else "CUDA events around the call") + ", a separate timed pass of K steps",
+            "kernel_us_by": "library stage events around each kernel, a separate pass of K steps",
             "call_us_mean": round(call_ms * 1e3, 2)}
 
 
@@ -821,6 +847,7 @@ def measure_config(cfg, dev, args, stream, flush, bsr, _build):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    region_ms = region_steps(step, args.steps, stream)
     hot = timed_steps(step, args.steps, stream)
     cold = timed_steps(step, args.steps, stream, flush)
     kernel_pass(parts, args.steps, stream, bsr)
@@ -830,7 +857,12 @@ def measure_config(cfg, dev, args, stream, flush, bsr, _build):
     res = {"workload": job["config"]["workload"], "metric": job["metric"], "unit": unit,
            "hot": dict(spread(hot), value=round(num / (statistics.median(hot) * 1e-3) / scale, 1)),
            "cold": dict(spread(cold), value=round(num / (statistics.median(cold) * 1e-3) / scale, 1)),
-           "roofline": roofline_of(parts, _build),
+           "region": {"us_per_step": round(region_ms * 1e3, 2),
+                      "value": round(num / (region_ms * 1e-3) / scale, 1),
+                      "note": "K back-to-back steps, CUDA events at their ends only"},
+           "roofline": roofline_of(parts, _build, whole_ms=region_ms,
+                                   whole_by="K back-to-back steps of one kernel launch each, "
+                                            "CUDA events at their ends only"),
            "kernels_us": {f"{pt.label}.{name}": round(sum(v) / len(v) * 1e3, 2)
                           for pt in parts for name, v in pt.stage_ms.items()},
            "config": job["config"]}
@@ -932,7 +964,9 @@ def main():
         "dtype": job.get("dtype", "bf16"),
         "data": "synthetic (seeded N(0,1) bf16, page table drawn per workloads/)",
         "config": dict(job["config"], parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
-        "roofline": roofline_of(parts, _build),
+        "roofline": roofline_of(parts, _build, whole_ms=ms_step,
+                                whole_by="region 1: CUDA events at the ends of K back-to-back "
+                                         "steps of one kernel launch each"),
         "hot": dict(spread(hot), value=round(num / (statistics.median(hot) * 1e-3) / scale, 1)),
         "cold": dict(spread(cold), value=round(num / (statistics.median(cold) * 1e-3) / scale, 1),
                      flush=f"write of {2 * l2_bytes >> 20} MiB (2x L2) before each step, "
