@@ -132,6 +132,18 @@ def test_prefill_head_dim_64_split_ranges_and_nhd(rope):
     check_full(n, out, lse)
 
 
+@pytest.mark.parametrize("rope", [0.0, 1e4])
+def test_prefill_head_dim_64_sliding_window(rope):
+    """head_dim 64 with a 150-key sliding window (the windowed kernel variants, RoPE pairs
+    32 apart included): units start at the page holding their oldest visible key."""
+    w = wl.make_paged("pf64win", 98, [900, 400], Hq=16, Hk=4, D=64, P=16,
+                      qo_lens=[200, 100], causal=True, rope_theta=rope)
+    w.window_left = 150
+    out, lse, s = run(w)
+    assert s.info()["num_prefill_items"] > 0 and s.info()["window_left"] == 150
+    check_full(w, out, lse)
+
+
 def test_prefill_head_dim_64_fresh_prompt():
     """A head_dim 64 prompt with no history: its first rows see a handful of keys.
     Plain bars, with RoPE."""
