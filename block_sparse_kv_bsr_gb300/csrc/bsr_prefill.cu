@@ -875,83 +875,70 @@ __global__ void __launch_bounds__(threads_of<ROPE>()) __maxnreg__(ROPE ? 80 : 96
 }
 
 // ---------------------------------------------------------------- split-range merge
-// One warp per packed row of a split unit: lane l owns columns 4l .. 4l + 3 (with
-// head_dim 64 lanes 16-31 own none).
+// One thread per 16-byte column chunk (4 columns) of a packed row of a split unit.
 // The partial states (fp32, log2-domain lse) are combined in key order:
-//   lse = M + log2(sum_k 2^(lse_k - M)),  o = sum_k 2^(lse_k - lse) o_k.
-// Lane k holds lse_k (chunks in groups of 32); the partial rows of up to eight
-// chunks are loaded before the weights are known, so the loads overlap.
-constexpr int kMergeWarps = 8;
-__global__ void __launch_bounds__(kMergeWarps * 32) bsr_prefill_merge_kernel(const PrefillMergeParams p) {
+//   lse = M + log2(sum_k 2^(lse_k - M)),  o = sum_k 2^(lse_k - M) o_k / sum_k 2^(lse_k - M).
+// Every thread of a row reads the row's few chunk lse values itself (one broadcast load
+// per warp) and the partial columns of the first kMergeAhead chunks before the weights
+// are known, so a split of up to that many chunks waits on memory once; no shuffles.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeAhead = 4;
+__global__ void __launch_bounds__(kMergeThreads) bsr_prefill_merge_kernel(const PrefillMergeParams p) {
   // launched as a programmatic dependent of the prefill kernel, whose partial states it reads
   pdl_trigger();
   pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int kCtasPerUnit = kUnitRows / kMergeWarps;
-  const int unit = blockIdx.x / kCtasPerUnit;
-  const int prow = (blockIdx.x % kCtasPerUnit) * kMergeWarps + warp;
+  const int cpr = p.head_dim / 4;                       // 16-byte chunks per row
+  const int64_t gid = int64_t(blockIdx.x) * kMergeThreads + threadIdx.x;
+  const int64_t grow = gid / cpr;                       // unit * kUnitRows + packed row
+  const int ch = int(gid - grow * cpr);
+  const int unit = int(grow / kUnitRows), prow = int(grow % kUnitRows);
   if (unit >= p.n_units) return;
   const DecodeItem it = p.units[unit];
   if (prow >= it.nrows) return;
   const int n = it.nchunks;
-  const float* lse_k = p.part_lse + size_t(it.first_slot) * kUnitRows + prow;
   const size_t hd = size_t(p.head_dim);
-  const bool cols = 4 * lane < p.head_dim;
-  const float* po = p.part_o + (size_t(it.first_slot) * kUnitRows + prow) * hd + 4 * lane;
-  const size_t kSlotStride = size_t(kUnitRows) * hd;
-  // the first chunks' partial rows, before anything depends on the lse values
-  float4 x[8];
+  const float* lse_k = p.part_lse + size_t(it.first_slot) * kUnitRows + prow;
+  const float* po = p.part_o + (size_t(it.first_slot) * kUnitRows + prow) * hd + 4 * ch;
+  const size_t slot_stride = size_t(kUnitRows) * hd;
+  float lk[kMergeAhead];
+  float4 x[kMergeAhead];
 #pragma unroll
-  for (int u = 0; u < 8; ++u)
-    x[u] = cols && u < n ? __ldcg(reinterpret_cast<const float4*>(po + size_t(u) * kSlotStride))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-  // chunk lse values: lane k holds chunk k (and k + 32, ... for longer splits: read
-  // again there); one load round trip before the weights when n <= 32
-  const float l0 = lane < n ? __ldcg(lse_k + size_t(lane) * kUnitRows) : -INFINITY;
-  float M = l0;
-  for (int k = lane + 32; k < n; k += 32) M = fmaxf(M, __ldcg(lse_k + size_t(k) * kUnitRows));
+  for (int k = 0; k < kMergeAhead; ++k) {
+    lk[k] = k < n ? __ldg(lse_k + size_t(k) * kUnitRows) : -INFINITY;
+    x[k] = k < n ? __ldcg(reinterpret_cast<const float4*>(po + size_t(k) * slot_stride))
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float M = -INFINITY;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float lt = -INFINITY;
+  for (int k = 0; k < kMergeAhead; ++k) M = fmaxf(M, lk[k]);
+  for (int k = kMergeAhead; k < n; ++k) M = fmaxf(M, __ldg(lse_k + size_t(k) * kUnitRows));
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lt = -INFINITY;
   if (M != -INFINITY) {
-    float sum = lane < n ? ptx::ex2(l0 - M) : 0.f;
-    for (int k = lane + 32; k < n; k += 32) sum += ptx::ex2(__ldcg(lse_k + size_t(k) * kUnitRows) - M);
+    float sum = 0.f;
+    auto add = [&](float l, const float4& v) {
+      const float wk = l == -INFINITY ? 0.f : ptx::ex2(l - M);
+      sum += wk;
+      acc.x += wk * v.x; acc.y += wk * v.y; acc.z += wk * v.z; acc.w += wk * v.w;
+    };
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    for (int k = 0; k < kMergeAhead; ++k)
+      if (k < n) add(lk[k], x[k]);
+    for (int k = kMergeAhead; k < n; ++k)
+      add(__ldg(lse_k + size_t(k) * kUnitRows),
+          __ldcg(reinterpret_cast<const float4*>(po + size_t(k) * slot_stride)));
+    const float inv = 1.f / sum;
+    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
     lt = M + ptx::lg2(sum);
-    for (int kb = 0; kb < n; kb += 32) {
-      const int m = min(32, n - kb);
-      const float lk = kb == 0 ? l0 : (lane < m ? __ldcg(lse_k + size_t(kb + lane) * kUnitRows) : 0.f);
-      const float wl = lane < m ? ptx::ex2(lk - lt) : 0.f;
-      for (int j = 0; j < m; j += 8) {
-        if (kb + j >= 8) {   // chunks past the first eight: load this group now
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            x[u] = cols && j + u < m
-                       ? __ldcg(reinterpret_cast<const float4*>(po + size_t(kb + j + u) * kSlotStride))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float w = __shfl_sync(0xffffffffu, wl, (j + u) & 31);
-          if (j + u < m) {
-            acc.x += w * x[u].x; acc.y += w * x[u].y; acc.z += w * x[u].z; acc.w += w * x[u].w;
-          }
-        }
-      }
-    }
   }
   const size_t orow = out_row(it, it.row0 + prow, p.group, p.Hq);
-  if (cols) {
-    if (p.out_f32) {
-      reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * hd)[lane] = acc;
-    } else {
-      reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * hd)[lane] =
-          make_uint2(ptx::pack_bf16(acc.x, acc.y), ptx::pack_bf16(acc.z, acc.w));
-    }
+  if (p.out_f32) {
+    reinterpret_cast<float4*>(static_cast<float*>(p.out) + orow * hd)[ch] = acc;
+  } else {
+    reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + orow * hd)[ch] =
+        make_uint2(ptx::pack_bf16(acc.x, acc.y), ptx::pack_bf16(acc.z, acc.w));
   }
-  if (lane == 0 && p.lse != nullptr) p.lse[orow] = lt * 0.69314718055994530942f;
+  if (ch == 0 && p.lse != nullptr) p.lse[orow] = lt * 0.69314718055994530942f;
 }
 
 template <bool ROPE, bool WIN, bool D64>
@@ -990,9 +977,10 @@ cudaError_t launch_prefill(bool rope, const CUtensorMap& tq, const CUtensorMap& 
 }
 
 cudaError_t launch_prefill_merge(const PrefillMergeParams& p, cudaStream_t stream) {
-  const int64_t grid = int64_t(p.n_units) * (kUnitRows / kMergeWarps);
+  const int64_t threads = int64_t(p.n_units) * kUnitRows * (p.head_dim / 4);
+  const int64_t grid = (threads + kMergeThreads - 1) / kMergeThreads;
   if (grid <= 0) return cudaSuccess;
-  const cudaError_t le = launch_pdl(bsr_prefill_merge_kernel, int(grid), kMergeWarps * 32, 0, stream, p);
+  const cudaError_t le = launch_pdl(bsr_prefill_merge_kernel, int(grid), kMergeThreads, 0, stream, p);
   return le != cudaSuccess ? le : cudaGetLastError();
 }
 
