@@ -247,7 +247,7 @@ typedef struct bsr_schedule_info {
   int32_t num_prefill_items;  /* work units of the tensor-core prefill kernel */
   int32_t num_split_streams;  /* (request, kv head, row group) ranges cut into >1 chunk */
   int32_t num_partials;       /* partial states written before merging */
-  int32_t decode_ctas, decode_warps_per_cta;
+  int32_t decode_ctas, decode_warps_per_cta;  /* one decode CTA per SM; its warps follow kv_dtype */
   int32_t prefill_ctas;
   int32_t num_sms;
   int64_t workspace_bytes;    /* device workspace of the schedule */
@@ -283,12 +283,14 @@ int bsr_schedule_stage_times(bsr_schedule_t schedule, int32_t call, float* ms);
 
 /*
  * bsr_attn_plan_host — the host half of bsr_attn_plan, for a given SM count,
- * touching no GPU: validates the table exactly like bsr_attn_plan and returns
- * the number of decode work units (or a negative BSR_ERR_* code).  If `info`
- * is non-NULL it is filled as bsr_schedule_get_info would (without the
- * workspace size); if `units` is non-NULL (capacity max_units rows) each unit
- * is written as int32[8]: request, kv head, first packed row, packed rows,
- * first key, end key, partial slot (-1 = unsplit), warp.  Packed row R of
+ * touching no GPU: validates the table exactly like bsr_attn_plan (kv_dtype
+ * included, which sets the decode warps per SM) and returns the number of work
+ * units, decode and prefill (or a negative BSR_ERR_* code).  If `info` is non-NULL
+ * it is filled as bsr_schedule_get_info would (without the workspace size); if
+ * `units` is non-NULL (capacity max_units rows) each unit is written as
+ * int32[8]: request, kv head, first packed row, packed rows, first key, end key,
+ * partial slot (-1 = unsplit), then the decode warp that runs it, or -1 - CTA for
+ * a unit of the tensor-core prefill kernel.  Packed row R of
  * (request, kv head) is query R / (Hq/Hk), qo head kv_head * (Hq/Hk) +
  * R % (Hq/Hk).  All arrays are host arrays owned by the caller.  Use it to
  * inspect or test a schedule (coverage of every key, balance) without a device.
