@@ -17,7 +17,7 @@ from . import _build
 
 __all__ = [
     "BsrError", "load", "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run",
-    "bsr_attn_run_kv8", "bsr_merge_states", "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info",
+    "bsr_attn_run_kv8", "bsr_attn_run_host", "bsr_merge_states", "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info",
     "bsr_last_device_error", "bsr_status_string", "bsr_attn_decode_noalloc", "Schedule",
     "bsr_attn_decode_noalloc_kv8", "bsr_attn_decode_noalloc_ex",
     "bsr_schedule_set_stage_timing", "bsr_schedule_stage_times", "STAGES", "EXPORTED_SYMBOLS",
@@ -29,7 +29,8 @@ BSR_DTYPE_BF16 = 0
 BSR_DTYPE_F32 = 1
 
 EXPORTED_SYMBOLS = (
-    "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run", "bsr_attn_run_kv8", "bsr_merge_states",
+    "bsr_attn_plan", "bsr_attn_plan_host", "bsr_attn_run", "bsr_attn_run_kv8",
+    "bsr_attn_run_host", "bsr_merge_states",
     "bsr_append_kv", "bsr_schedule_destroy", "bsr_schedule_get_info", "bsr_last_device_error",
     "bsr_status_string", "bsr_attn_decode_noalloc", "bsr_attn_decode_noalloc_kv8",
     "bsr_attn_decode_noalloc_ex",
@@ -96,6 +97,10 @@ def load(path: str | None = None):
     lib.bsr_attn_run.restype = ctypes.c_int
     lib.bsr_attn_run.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                  ctypes.c_int32, _vp, ctypes.c_int32, _vp, _vp]
+    lib.bsr_attn_run_host.restype = ctypes.c_int
+    lib.bsr_attn_run_host.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
+                                      ctypes.c_float, ctypes.c_float, ctypes.c_int32, _vp,
+                                      ctypes.c_int32, _vp, _vp]
     lib.bsr_merge_states.restype = ctypes.c_int
     lib.bsr_merge_states.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int64, ctypes.c_int32,
                                      ctypes.c_int32, ctypes.c_int32, _vp, _vp, _vp]
@@ -317,6 +322,43 @@ def bsr_attn_run(schedule: Schedule, q, k_pages, v_pages, *, sm_scale: float,
                             float(sm_scale), float(rope_theta), int(bool(causal)), _dptr(out), dt,
                             _dptr(lse), _vp(_stream_ptr(stream)))
     _check(code, "bsr_attn_run")
+    return out, lse
+
+
+def _host_ptr(t):
+    if t is None:
+        return None
+    if t.is_cuda:
+        raise ValueError("expected a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def bsr_attn_run_host(schedule: Schedule, q, k_pages, v_pages, *, sm_scale: float,
+                      rope_theta: float = 0.0, causal: bool = False, k_scale: float = 1.0,
+                      v_scale: float = 1.0, out=None, lse=None, out_dtype=None,
+                      want_lse: bool = True, stream=None):
+    """One step with HOST q / out / lse (pinned memory keeps the copies asynchronous):
+    the upload, the run and the read-back are queued on `stream`; the host tensors hold
+    the result once the stream has completed.  ``k_pages``/``v_pages`` are the device
+    pools (bf16, or E4M3 codes with k_scale / v_scale for a schedule planned "e4m3")."""
+    import torch
+    lib = load()
+    if q.dtype != torch.bfloat16:
+        raise ValueError("q must be bf16")
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype or torch.bfloat16, pin_memory=True)
+    if lse is None and want_lse:
+        lse = torch.empty(q.shape[:2], dtype=torch.float32, pin_memory=True)
+    if out.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("out must be bf16 or fp32")
+    dt = BSR_DTYPE_F32 if out.dtype == torch.float32 else BSR_DTYPE_BF16
+    code = lib.bsr_attn_run_host(_vp(schedule.handle), _host_ptr(q), _dptr(k_pages),
+                                 _dptr(v_pages), float(k_scale), float(v_scale), float(sm_scale),
+                                 float(rope_theta), int(bool(causal)), _host_ptr(out), dt,
+                                 _host_ptr(lse), _vp(_stream_ptr(stream)))
+    _check(code, "bsr_attn_run_host")
     return out, lse
 
 

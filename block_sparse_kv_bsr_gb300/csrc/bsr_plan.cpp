@@ -847,6 +847,7 @@ extern "C" void bsr_schedule_destroy(bsr_schedule_t s) {
   for (cudaEvent_t e : s->t_ev) cudaEventDestroy(e);
   if (s->h_stage) cudaFreeHost(s->h_stage);
   if (s->d_rope) cudaFree(s->d_rope);
+  if (s->d_io) cudaFree(s->d_io);
   std::free(s->h_rope);
   cudaGetLastError();
   delete s;

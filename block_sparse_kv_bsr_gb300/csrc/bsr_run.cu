@@ -330,6 +330,65 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
   return BSR_OK;
 }
 
+extern "C" int bsr_attn_run_host(bsr_schedule_t s, const void* q_host, const void* k_pages,
+                                 const void* v_pages, float k_scale, float v_scale,
+                                 float sm_scale, float rope_theta, int32_t causal, void* out_host,
+                                 int32_t out_dtype, float* lse_host, void* stream_v) {
+  if (s == nullptr || s->d_ws == nullptr) return BSR_ERR_INVALID_ARGUMENT;
+  if (out_dtype != BSR_DTYPE_BF16 && out_dtype != BSR_DTYPE_F32) return BSR_ERR_INVALID_ARGUMENT;
+  const cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  const size_t n = size_t(s->sum_qo) * size_t(s->Hq) * size_t(s->D);   // q / out elements
+  if (n == 0) return s->kv_dtype == BSR_KV_DTYPE_E4M3
+                         ? bsr_attn_run_kv8(s, nullptr, k_pages, v_pages, k_scale, v_scale, sm_scale,
+                                            rope_theta, causal, nullptr, out_dtype, nullptr, stream_v)
+                         : bsr_attn_run(s, nullptr, k_pages, v_pages, sm_scale, rope_theta, causal,
+                                        nullptr, out_dtype, nullptr, stream_v);
+  if (q_host == nullptr || out_host == nullptr) return BSR_ERR_INVALID_ARGUMENT;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != s->device) return BSR_ERR_SCHEDULE_MISMATCH;
+  // staging: q (bf16), out (room for fp32), lse, each 256-byte aligned
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t rows = size_t(s->sum_qo) * size_t(s->Hq);
+  const size_t q_bytes = n * 2, out_bytes = n * (out_dtype == BSR_DTYPE_F32 ? 4 : 2);
+  const size_t need = up(q_bytes) + up(n * 4) + up(rows * 4);
+  if (s->io_cap < need) {
+    if (s->d_io != nullptr) {
+      if (cudaFree(s->d_io) != cudaSuccess) {   // synchronizes: no copy can still use it
+        cudaGetLastError();
+        return BSR_ERR_CUDA;
+      }
+      s->d_io = nullptr;
+      s->io_cap = 0;
+    }
+    if (cudaMalloc(reinterpret_cast<void**>(&s->d_io), need) != cudaSuccess) {
+      cudaGetLastError();
+      return BSR_ERR_OUT_OF_MEMORY;
+    }
+    s->io_cap = need;
+  }
+  uint8_t* dq = s->d_io;
+  uint8_t* dout = dq + up(q_bytes);
+  float* dlse = reinterpret_cast<float*>(dout + up(n * 4));
+  if (cudaMemcpyAsync(dq, q_host, q_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return BSR_ERR_CUDA;
+  }
+  const int rc = s->kv_dtype == BSR_KV_DTYPE_E4M3
+                     ? bsr_attn_run_kv8(s, dq, k_pages, v_pages, k_scale, v_scale, sm_scale,
+                                        rope_theta, causal, dout, out_dtype,
+                                        lse_host != nullptr ? dlse : nullptr, stream_v)
+                     : bsr_attn_run(s, dq, k_pages, v_pages, sm_scale, rope_theta, causal, dout,
+                                    out_dtype, lse_host != nullptr ? dlse : nullptr, stream_v);
+  if (rc != BSR_OK) return rc;
+  if (cudaMemcpyAsync(out_host, dout, out_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      (lse_host != nullptr &&
+       cudaMemcpyAsync(lse_host, dlse, rows * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess)) {
+    cudaGetLastError();
+    return BSR_ERR_CUDA;
+  }
+  return BSR_OK;
+}
+
 extern "C" int bsr_schedule_set_stage_timing(bsr_schedule_t s, int32_t max_calls) {
   if (s == nullptr || max_calls < 0 || max_calls > (1 << 16)) return BSR_ERR_INVALID_ARGUMENT;
   if (s->device >= 0 && cudaSetDevice(s->device) != cudaSuccess) return BSR_ERR_CUDA;

@@ -54,6 +54,11 @@ struct bsr_schedule {
   CUtensorMap tm_q;
   const void* tm_q_ptr = nullptr;
 
+  // device staging of bsr_attn_run_host (q in, out and lse back), allocated on its
+  // first call and when a larger batch needs more, kept until destroy
+  uint8_t* d_io = nullptr;
+  size_t io_cap = 0;
+
   // pinned staging buffer for the single host-to-device upload
   uint8_t* h_stage = nullptr;
   size_t stage_cap = 0;

@@ -197,6 +197,26 @@ int bsr_attn_run_kv8(bsr_schedule_t schedule, const void* q, const void* k_pages
                      void* stream);
 
 /*
+ * bsr_attn_run_host — one decode or prefill step with HOST buffers: q_host (bf16
+ * [sum_qo, Hq, D]) is copied to the device, the schedule runs (bsr_attn_run, or
+ * bsr_attn_run_kv8 with k_scale / v_scale for a schedule planned for
+ * BSR_KV_DTYPE_E4M3; the scales are not used otherwise), and out (out_dtype) and lse
+ * (fp32, may be NULL) are copied back into out_host / lse_host -- all ordered on
+ * `stream`, so the host buffers hold the result once the stream has completed (the
+ * call itself does not wait).  With pinned host memory the copies are asynchronous;
+ * pageable memory works, but then the copies hold the host.  The device staging for
+ * q, out and lse belongs to the schedule: allocated by the first call (or when a
+ * larger plan needs more; the old one is freed, which waits for the device) and kept
+ * until bsr_schedule_destroy -- the only allocation on a run path, so a caller that
+ * must not allocate later makes one call while warming up.  The page pools are device
+ * buffers, as for bsr_attn_run; the other rules and error codes are the same.
+ */
+int bsr_attn_run_host(bsr_schedule_t schedule, const void* q_host, const void* k_pages,
+                      const void* v_pages, float k_scale, float v_scale, float sm_scale,
+                      float rope_theta, int32_t causal, void* out_host, int32_t out_dtype,
+                      float* lse_host, void* stream);
+
+/*
  * bsr_merge_states — combine two attention states over disjoint key sets
  * (split chunks, or the shared-prefix and suffix levels of a cascade;
  * "Block-Sparse 포맷", composition of a stored-once prefix with suffixes):

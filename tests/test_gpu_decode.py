@@ -135,6 +135,35 @@ def test_cuda_graph_capture_replays_identically():
     assert torch.equal(bits_t(out), bits_t(ref_out)) and torch.equal(lse, ref_lse)
 
 
+@pytest.mark.parametrize("cfg", ["decode", "prefill"])
+def test_run_with_host_buffers_matches_the_device_run(cfg):
+    """bsr_attn_run_host (host q in, host out / lse back, one call) gives the bits of
+    bsr_attn_run on the same schedule, for a decode and a prefill batch."""
+    if cfg == "decode":
+        w = wl.config2(small=True)
+    else:
+        w = wl.make_paged("hostpf", 58, [700, 333], Hq=32, Hk=8, D=128, P=16, qo_lens=[100, 64],
+                          causal=True, rope_theta=1e4)
+    q, k, v = device_tensors(w)
+    s = plan(w)
+    out, lse = bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+                                causal=w.causal)
+    q_host = w.q.pin_memory()
+    out_h, lse_h = bsr.bsr_attn_run_host(s, q_host, k, v, sm_scale=w.sm_scale,
+                                         rope_theta=w.rope_theta, causal=w.causal)
+    torch.cuda.synchronize()
+    assert not out_h.is_cuda and out_h.is_pinned()
+    assert torch.equal(bits_t(out_h), bits_t(out.cpu())) and torch.equal(lse_h, lse.cpu())
+    # fp32 output, no lse, and pageable host memory
+    out_f, lse_f = bsr.bsr_attn_run_host(s, w.q.clone(), k, v, sm_scale=w.sm_scale,
+                                         rope_theta=w.rope_theta, causal=w.causal,
+                                         out=torch.empty(w.q.shape, dtype=torch.float32),
+                                         want_lse=False)
+    torch.cuda.synchronize()
+    assert lse_f is None
+    check_full(w, out_f, lse.cpu())
+
+
 def test_mismatched_run_arguments_are_rejected():
     w = wl.config2(small=True)
     q, k, v = device_tensors(w)

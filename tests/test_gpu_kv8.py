@@ -94,6 +94,24 @@ def test_kv8_causal_multi_query_rows():
     check_full_kv8(w, out, lse)
 
 
+def test_kv8_run_with_host_buffers_matches_the_device_run():
+    """bsr_attn_run_host on a schedule planned for E4M3 runs the FP8 kernel with the given
+    scales and returns the bits of bsr_attn_run_kv8."""
+    dev = "cuda:0"
+    w = wl.config11(small=True)
+    s = plan(w)
+    k, v = w.k_codes.to(dev), w.v_codes.to(dev)
+    out, lse = bsr.bsr_attn_run_kv8(s, w.q.to(dev), k, v, k_scale=w.k_scale, v_scale=w.v_scale,
+                                    sm_scale=w.sm_scale, rope_theta=w.rope_theta,
+                                    causal=w.causal)
+    out_h, lse_h = bsr.bsr_attn_run_host(s, w.q.pin_memory(), k, v, k_scale=w.k_scale,
+                                         v_scale=w.v_scale, sm_scale=w.sm_scale,
+                                         rope_theta=w.rope_theta, causal=w.causal)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.view(torch.int16), out.cpu().view(torch.int16))
+    assert torch.equal(lse_h, lse.cpu())
+
+
 def test_schedule_planned_for_the_other_cache_type_is_refused():
     """bsr_attn_run_kv8 needs a schedule planned with kv_dtype "e4m3" (its decode work is
     spread over the FP8 kernel's warps), bsr_attn_run one planned for "bf16"."""
