@@ -55,7 +55,7 @@ DECODE_KERNEL_SOURCES = ("bsr_decode.cuh", "bsr_decode_d128.cu", "bsr_internal.h
 PREFILL_KERNEL_SOURCES = ("bsr_prefill.cu", "bsr_internal.h", "ptx.cuh", "umma.cuh",
                           "bsr_launch.cuh")
 DECODE_KV8_KERNEL_SOURCES = ("bsr_decode_kv8.cu", "bsr_decode.cuh", "bsr_internal.h", "ptx.cuh",
-                             "bsr_launch.cuh", "bsr_schedule.h")
+                             "bsr_launch.cuh", "bsr_launchers.h")
 
 
 _COMMENT = re.compile(rb"//[^\n]*|/\*.*?\*/", re.S)

@@ -39,7 +39,7 @@
 #include <type_traits>
 
 #include "bsr_decode.cuh"
-#include "bsr_schedule.h"
+#include "bsr_launchers.h"
 
 #ifndef BSR_DECODE_STAGES_KV8
 #define BSR_DECODE_STAGES_KV8 4
