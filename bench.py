@@ -803,13 +803,12 @@ def e2e_run(job, steps, warmup, stream):
         stream.synchronize()
     gc.collect()
     n = max(3, min(5 * steps, 100))
-    import torch
-    done = torch.cuda.Event()
+    done = None
     plan()
     t0 = time.perf_counter()
     for _ in range(n):
         launch()
-        done.record(stream)      # this step's out / lse are on the host once it completes
+        done = stream.record_event(done)   # this step's out / lse are on the host then
         plan()                   # the next step's table, while the GPU runs this one
         done.synchronize()       # (the next table's upload, queued behind, need not be waited for)
     stream.synchronize()

@@ -99,14 +99,19 @@ def test_e2e_plans_the_next_step_while_the_gpu_runs():
     """Pipelined e2e: each step launches its copies and kernel, plans the next step's
     table on the host, then waits for its own result; every step has its copies."""
     log = []
-    stream = types.SimpleNamespace(synchronize=lambda: log.append("sync"))
+    result_ready = types.SimpleNamespace(synchronize=lambda: log.append("wait result"))
+    stream = types.SimpleNamespace(synchronize=lambda: log.append("sync"),
+                                   record_event=lambda ev=None: result_ready)
     job = {"e2e": (lambda: log.append("plan"), lambda: log.append("launch")),
            "e2e_bytes": lambda: (100, 50), "numerator": 1e9, "scale": 1e9, "unit": "GB/s"}
     r = bench.e2e_run(job, steps=1, warmup=1, stream=stream)
     n = r["steps"]
-    piped = log[3:3 + 1 + 3 * n]     # after the warm-up's plan, launch, sync
-    assert piped[0] == "plan" and piped[1:] == ["launch", "plan", "sync"] * n
-    assert log[3 + 1 + 3 * n:] == ["plan", "launch", "sync"] * n
+    piped = log[3:3 + 1 + 3 * n + 1]     # after the warm-up's plan, launch, sync
+    # each step waits for its own read-back (an event behind it), not for the next
+    # step's plan upload; the stream is drained once at the end
+    assert piped[0] == "plan" and piped[1:-1] == ["launch", "plan", "wait result"] * n
+    assert piped[-1] == "sync"
+    assert log[3 + 1 + 3 * n + 1:] == ["plan", "launch", "sync"] * n
     assert r["h2d_bytes_per_step"] == 100 and r["d2h_bytes_per_step"] == 50
 
 
