@@ -572,7 +572,8 @@ def build_job(cfg: int, dev, small: bool):
                               attention_flops(w) if pre else kvb[i] + q.numel() * 2 + st,
                               "FLOP" if pre else "B", launches=s.info()["kernels_per_run"],
                               sched=s, stage="prefill" if pre else "decode",
-                              family="prefill" if pre else "decode"))
+                              family="prefill" if pre else "decode",
+                              profile=None if small or pre else "bsr_decode_cascade3_suffix.md"))
             scheds.append(s)
             outs.append((o_i, l_i))
             alg += kvb[i]
