@@ -30,9 +30,16 @@ using bsr::kMaxDecodeRows;
 using bsr::kStageTokens;
 
 constexpr size_t kAlign = 256;
-// Cost of one work unit beyond its keys (q load, epilogue, partial write),
-// in key-equivalents; used only to weigh units against each other.
-constexpr int64_t kUnitOverhead = 48;
+// Cost of one decode work unit beyond its keys (q load, epilogue), in key-equivalents,
+// and the extra cost of each piece of a split range (its partial write, arrival and
+// its share of the merge); used only to weigh units against each other.  A fit of the
+// decode kernel's per-warp busy times (clock stamps of every warp of the skewed
+// 128-request batch over 16 launches, against the keys, pieces and split pieces each
+// warp was given) put them at ~33 and ~69 key-equivalents.  The split surcharge stays
+// at 16: at the fitted value a uniform batch (512 equal ranges over 1216 warps) is cut
+// into fewer pieces than it has warps, 3-4 % slower; at 16 its cut is unchanged.
+constexpr int64_t kUnitOverhead = 32;
+constexpr int64_t kSplitOverhead = 16;
 // Shortest piece a key range is cut into (keys): below this the partial
 // write and merge cost more than the balance gains.
 constexpr int64_t kMinPiece = 64;
@@ -111,6 +118,7 @@ struct CutInput {
   size_t n;
   int64_t overhead, align_mask, min_piece, max_workers;   // align_mask: ~(align - 1)
   int workers;
+  int64_t split_overhead;   // extra cost of every piece of a range that is cut
 };
 
 // Cut with budget T: ranges are laid end to end and each worker takes pieces until
@@ -128,12 +136,13 @@ int64_t cut_ranges(const CutInput& in, int64_t T, Emit&& emit) {
     int64_t pos = in.kb[oi];
     for (;;) {   // until the piece ending at kend is placed (an empty range still needs one)
       const int64_t rest = kend - pos;
-      if (rest + in.overhead <= room) {
+      const int64_t last_cost = rest + in.overhead + (pos != in.kb[oi] ? in.split_overhead : 0);
+      if (last_cost <= room) {
         emit(oi, pos, kend, w);
-        room -= rest + in.overhead;
+        room -= last_cost;
         break;
       }
-      int64_t take = (room - in.overhead) & in.align_mask;
+      int64_t take = (room - in.overhead - in.split_overhead) & in.align_mask;
       if (rest - take < in.min_piece) take = (rest - in.min_piece) & in.align_mask;
       if (take >= in.min_piece) {
         emit(oi, pos, pos + take, w);
@@ -162,7 +171,7 @@ int64_t cut_ranges(const CutInput& in, int64_t T, Emit&& emit) {
 // key tile).
 void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align, int64_t overhead,
              int64_t min_piece, int64_t min_worker_work, WorkList* out, int64_t* k_hint = nullptr,
-             int64_t min_piece_small = 0) {
+             int64_t min_piece_small = 0, int64_t split_overhead = 0) {
   // Working arrays live across calls (per thread), so a plan per decode step reuses
   // their memory instead of faulting in fresh pages.
   struct Scratch {
@@ -218,7 +227,8 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
                     : int(std::max<int64_t>(1, std::min<int64_t>(max_workers, (total + min_worker_work - 1) / min_worker_work)));
   // a batch that leaves workers idle may be cut finer (min_piece_small, when given)
   if (min_piece_small > 0 && workers < max_workers) min_piece = min_piece_small;
-  const CutInput in{kb.data(), ke.data(), n, overhead, ~(align - 1), min_piece, max_workers, workers};
+  const CutInput in{kb.data(), ke.data(), n, overhead, ~(align - 1), min_piece, max_workers, workers,
+                    split_overhead};
   std::vector<int32_t>& pieces_of_unit = sc.pieces_of_unit;
   pieces_of_unit.assign(n, 0);
   int64_t T = 0;
@@ -308,7 +318,7 @@ void balance(const std::vector<Unit>& units, int64_t max_workers, int64_t align,
       it.page_base = u.page_base;
       it.q_row0 = u.q_row0;
       it.qpos0 = u.qpos0;
-      load[w] += tok1 - tok0 + overhead;
+      load[w] += tok1 - tok0 + overhead + (it.nchunks > 1 ? split_overhead : 0);
     });
     while (cur < workers) out->ptr[++cur] = idx;
   }
@@ -589,7 +599,8 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   // consecutive plans of a serving loop are alike: start from the last budget step
   thread_local int64_t dec_k = -1;
   balance(dunits, int64_t(num_sms) * dec_warps_per_sm, std::max<int64_t>(page_size, kStageTokens),
-          kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec, &dec_k, kMinPieceSmall);
+          kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec, &dec_k, kMinPieceSmall,
+          kSplitOverhead);
   balance_gangs(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillKeyTile),
                 kPrefillOverhead, kPrefillMinPiece, kPrefillMinCtaWork, &hp->pre);
   hp->pmerge.clear();
