@@ -66,11 +66,17 @@ struct DecodeCfg {
   static constexpr int kRopeOffStride = kRopeRowBytes + 64;
   static constexpr size_t kRingBytes = size_t(kDecodeWarps) * kStages * kStageBytes;
   static constexpr size_t kBarBytes = size_t(kDecodeWarps) * kStages * 8;
-  static constexpr size_t kSmemBytes = kRingBytes + kBarBytes + 1024;
+  // per warp: the item ids of the run-time units it has taken, by position (a ring: the
+  // producer runs at most kStages stages, so at most kStages units, ahead)
+  static constexpr int kTakenRing = 8;
+  static constexpr size_t kTakenBytes = size_t(kDecodeWarps) * kTakenRing * 4;
+  static constexpr size_t kSmemBytes = kRingBytes + kBarBytes + kTakenBytes + 1024;
   static constexpr size_t kSmemBytesRope = kSmemBytes +
                                            size_t(kDecodeWarps) * kStages * kRopeRowBytes +
                                            size_t(kStageTokens) * kRopeOffStride;
-  static_assert(kBarBytes % 16 == 0, "stage-row copies need 16-byte aligned destinations");
+  static_assert((kBarBytes + kTakenBytes) % 16 == 0,
+                "stage-row copies need 16-byte aligned destinations");
+  static_assert(kTakenRing > kStages && (kTakenRing & (kTakenRing - 1)) == 0, "taken-unit ring");
   static_assert(kSmemBytesRope <= 232448, "decode stages exceed the shared memory of one SM");
 };
 
@@ -268,12 +274,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   uint8_t* const base_ptr = smem_raw + (base - ptx::smem_u32(smem_raw));
   const uint32_t ring = base + uint32_t(warp * C::kStages * C::kStageBytes);
   const uint32_t bars = base + uint32_t(C::kRingBytes + warp * C::kStages * 8);
-  // RoPE: this warp's per-stage table rows, then the CTA's offset rows t < 16
-  const uint32_t grows =
-      base + uint32_t(C::kRingBytes + C::kBarBytes + warp * C::kStages * C::kRopeRowBytes);
+  // this warp's taken run-time units, then with RoPE its per-stage table rows, then the
+  // CTA's offset rows t < 16
+  volatile int* const taken =
+      reinterpret_cast<volatile int*>(base_ptr + C::kRingBytes + C::kBarBytes) + warp * C::kTakenRing;
+  const size_t rope_off = C::kRingBytes + C::kBarBytes + C::kTakenBytes;
+  const uint32_t grows = base + uint32_t(rope_off + warp * C::kStages * C::kRopeRowBytes);
   uint8_t* const goff_ptr = base_ptr + (grows - base);
   uint8_t* const frows_ptr =
-      base_ptr + C::kRingBytes + C::kBarBytes + size_t(kDecodeWarps) * C::kStages * C::kRopeRowBytes;
+      base_ptr + rope_off + size_t(kDecodeWarps) * C::kStages * C::kRopeRowBytes;
   if constexpr (ROPE) {
     const float4* src = reinterpret_cast<const float4*>(p.rope);
     for (int i = threadIdx.x; i < kStageTokens * C::kRopeRowF4; i += kDecodeWarps * 32) {
@@ -286,7 +295,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   const int gw = blockIdx.x * kDecodeWarps + warp;
   if (gw >= p.num_warps) return;
   const int it_begin = __ldg(p.warp_ptr + gw), it_end = __ldg(p.warp_ptr + gw + 1);
-  if (it_begin >= it_end) return;
+  // positions 0 .. nstat - 1 of this warp's sequence are its planned items; after them
+  // come run-time units taken from the shared queue until it is empty (dyn)
+  const bool dyn = !SMALLP && p.n_dyn > 0;
+  const int nstat = it_end - it_begin;
+  if (nstat <= 0 && !dyn) return;
+  if (dyn && lane < C::kTakenRing) taken[lane] = p.dyn_begin;   // always a valid item id
+  __syncwarp();
   if (!SMALLP) {
     if (lane == 0) {
 #pragma unroll
@@ -306,7 +321,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   // The producer runs up to kStages stages ahead of the consumer.  Page ids of
   // the next 32 stages of the current unit sit one per lane in `win`; the next
   // window is requested before it is needed.
-  int p_it = it_begin, p_st = 0, p_nst = 0, win = 0, win_next = 0, win_base = 0;
+  // p_end: the first position with no item (known for a warp without run-time units;
+  // otherwise found when the queue is empty); p_have: pi is the unit at position p_q
+  int p_q = 0, p_end = dyn ? INT_MAX : nstat, p_st = 0, p_nst = 0;
+  int win = 0, win_next = 0, win_base = 0;
+  bool p_have = false, may_take = !early, took_last = false;
   // with RoPE and per-page positions: each stage's logical position, same windows
   int wpos = 0, wpos_next = 0;
   uint32_t p_seq = 0;
@@ -323,14 +342,49 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     const int tok = it.tok0 + kStageTokens * s;
     return __ldg(p.page_pos + it.page_base + (tok >> log2P)) + (tok & (p.P - 1));
   };
-  auto producer_seek = [&]() {
-    while (p_it < it_end) {
-      pi = load_item(p.items, p_it);
-      p_nst = stages_of(pi);
-      if (p_nst > 0) break;
-      ++p_it;
+  // item id at position q (a run-time unit's was recorded when the producer took it)
+  auto item_at = [&](int q) { return q < nstat ? it_begin + q : taken[q & (C::kTakenRing - 1)]; };
+  // this warp has found the queue empty: the last planned warp to do so empties the
+  // counters for the next launch (every taker of this launch has finished taking)
+  auto done_taking = [&]() {
+    took_last = true;
+    if (lane == 0 && atomicAdd(p.dyn_ctr + 1, 1) == p.num_warps - 1) {
+      atomicExch(p.dyn_ctr, 0);
+      atomicExch(p.dyn_ctr + 1, 0);
     }
-    if (p_it < it_end) {
+  };
+  // take the next run-time unit for position q; false when the queue is empty
+  auto take = [&](int q) -> bool {
+    int d = 0;
+    if (lane == 0) d = atomicAdd(p.dyn_ctr, 1);
+    d = __shfl_sync(0xffffffffu, d, 0);
+    if (d >= p.n_dyn) {
+      done_taking();
+      return false;
+    }
+    if (lane == 0) taken[q & (C::kTakenRing - 1)] = p.dyn_begin + d;
+    __syncwarp();
+    return true;
+  };
+  auto producer_seek = [&]() {
+    p_have = false;
+    while (p_q < p_end) {
+      if (p_q >= nstat) {
+        if (!may_take) return;   // run-time units wait for the grid-dependency wait
+        if (!take(p_q)) {
+          p_end = p_q;
+          return;
+        }
+      }
+      pi = load_item(p.items, item_at(p_q));
+      p_nst = stages_of(pi);
+      if (p_nst > 0) {
+        p_have = true;
+        break;
+      }
+      ++p_q;
+    }
+    if (p_have) {
       win_base = 0;
       win = load_window(pi, 0);
       win_next = load_window(pi, 32);
@@ -341,7 +395,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     }
   };
   auto producer_issue = [&]() {
-    if (p_it >= it_end) return;
+    if (!p_have) return;
     const int slot = int(p_seq % C::kStages);
     const int page = __shfl_sync(0xffffffffu, win, p_st - win_base);
     const int spos = ROPE ? __shfl_sync(0xffffffffu, wpos, p_st - win_base) : 0;
@@ -383,7 +437,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
     ++p_seq;
     ++p_st;
     if (p_st == p_nst) {
-      ++p_it;
+      ++p_q;
       p_st = 0;
       producer_seek();
     } else if (p_st - win_base == 32) {
@@ -399,6 +453,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
   if (!SMALLP) producer_seek();
   if (early) pdl_wait();
+  if (!may_take) {
+    may_take = true;
+    if (!SMALLP && !p_have) producer_seek();
+  }
   if (!SMALLP) {
 #pragma unroll 1
     for (int i = 0; i < C::kStages; ++i) producer_issue();
@@ -415,8 +473,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
   uint32_t c_seq = 0;
   bool failed = false;
 #pragma unroll 1
-  for (int c_it = it_begin; c_it < it_end; ++c_it) {
-    const DecodeItem ci = load_item(p.items, c_it);
+  for (int c_q = 0; c_q < p_end; ++c_q) {
+    // the producer has placed position c_q (or found the end) before the consumer
+    // gets here: it moves past a unit as soon as it has issued its last stage
+    const DecodeItem ci = load_item(p.items, item_at(c_q));
     const int nst = stages_of(ci);
     const int group = p.group;
     const int rA = ci.row0 + g4, rB = ci.row0 + g4 + 8;
@@ -780,6 +840,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, 1)
 
   if (failed) {
     if (lane == 0) atomicOr(p.error, 1);
+    if (dyn && !took_last) done_taking();   // the queue's count of finished warps stays exact
     // let the copies this warp still has in flight land before the CTA exits
 #pragma unroll 1
     for (uint32_t s = c_seq; s < p_seq; ++s)

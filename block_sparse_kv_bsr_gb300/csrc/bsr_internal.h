@@ -77,6 +77,13 @@ struct DecodeParams {
   int32_t plan_uploaded;          // 1: items, warp_ptr, indices, page_pos and rope were written
                                   // by a host copy before the launch, so the kernel may read
                                   // them before the previous grid on the stream completes
+  // Units taken at run time: items [dyn_begin, dyn_begin + n_dyn) (whole short ranges,
+  // longest first) go to whichever warp has finished its own list, one at a time, so
+  // that warps which ran slow take fewer.  dyn_ctr[0] is the next one to take,
+  // dyn_ctr[1] the warps that found the queue empty; both are 0 between launches (the
+  // plan uploads zeros, the last warp of a launch resets them).  n_dyn = 0: none.
+  int32_t n_dyn, dyn_begin;
+  int32_t* dyn_ctr;
   uint64_t wait_limit_ns;         // bound on every barrier wait
 };
 

@@ -54,6 +54,20 @@ constexpr int64_t kMinPieceSmall = 32;
 // Least work (key-equivalents) worth a warp of its own: small batches use
 // fewer warps instead of many tiny pieces.
 constexpr int64_t kMinWarpWork = 64;
+// Run-time units: the shortest whole ranges, up to this share of a decode batch's cost,
+// each at most a quarter of a warp's mean share, are left out of the static cut and taken at
+// run time by warps that have finished their own lists (longest first), so the spread
+// of finishing times that a static cut cannot foresee (SMs that stream slower, units
+// that cost more than planned) is filled instead of waited for.  Only for skewed
+// batches (some range is at least kDynSkew warps' mean share: the long ranges are cut
+// over many warps anyway and the short ones are the natural fill) with enough work to
+// keep every warp busy, pages of 16 keys or more, a bf16 cache and no RoPE.  Measured
+// on GB300: the skewed 128-request decode 3.5 % faster (NHD pages 4 %); with RoPE at
+// logical positions 9 % slower and on a cascade's suffix level (no range longer than a
+// warp's share) 3.4 % slower, hence the conditions.
+constexpr double kDynShare = 0.15;
+constexpr int64_t kDynMinWarpWork = 256;
+constexpr int64_t kDynSkew = 4;
 // Prefill: packed rows from which a request takes the tensor-core kernel, the
 // per-unit overhead (Q load, pipeline fill, epilogue) in keys, the shortest
 // key piece and the least work per CTA.
@@ -109,6 +123,9 @@ struct WorkList {
   std::vector<int32_t> ptr;          // [workers + 1]
   int32_t n_partials = 0, n_split = 0, workers = 0;
   double imbalance = 1.0;
+  // decode only: items [dyn_begin, dyn_begin + n_dyn), after every worker's list, are
+  // taken at run time by whichever worker is free (longest first)
+  int32_t n_dyn = 0, dyn_begin = 0;
 };
 
 // The ranges to cut, longest first, and the limits of the cut.
@@ -464,14 +481,17 @@ struct HostPlan {
   int64_t max_pos_end = 0;
   // working arrays, kept with the plan so that re-planning reuses their memory
   std::vector<int32_t> kv_len, qo_len, q_row0;
-  std::vector<Unit> dunits, punits;
+  std::vector<Unit> dunits, punits, dyn_units;
+  std::vector<int32_t> dyn_idx;
+  std::vector<uint8_t> dyn_mark;
 };
 
 int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t* last_page_len,
                    int32_t batch, int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
                    int32_t page_size, const int32_t* qo_indptr, int32_t num_pages_in_pool,
                    int32_t causal, int32_t window_left, const int32_t* page_pos,
-                   float rope_theta, int num_sms, int dec_warps_per_sm, HostPlan* hp) {
+                   float rope_theta, int num_sms, int dec_warps_per_sm, bool allow_dyn,
+                   HostPlan* hp) {
   if (indptr == nullptr || batch < 0 || num_pages_in_pool < 0 || num_sms <= 0)
     return BSR_ERR_INVALID_ARGUMENT;
   if (batch > 0 && last_page_len == nullptr) return BSR_ERR_INVALID_ARGUMENT;
@@ -598,9 +618,91 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
   }
   // consecutive plans of a serving loop are alike: start from the last budget step
   thread_local int64_t dec_k = -1;
-  balance(dunits, int64_t(num_sms) * dec_warps_per_sm, std::max<int64_t>(page_size, kStageTokens),
-          kUnitOverhead, kMinPiece, kMinWarpWork, &hp->dec, &dec_k, kMinPieceSmall,
-          kSplitOverhead);
+  const int64_t dec_workers = int64_t(num_sms) * dec_warps_per_sm;
+  // the run-time pool: the shortest whole ranges up to kDynShare of the cost
+  std::vector<Unit>& dyn = hp->dyn_units;
+  dyn.clear();
+  if (allow_dyn && page_size >= kStageTokens && !(rope_theta > 0.f)) {
+    int64_t total = 0, longest = 0;
+    for (const Unit& u : dunits) {
+      total += u.kend - u.kbegin + kUnitOverhead;
+      longest = std::max<int64_t>(longest, u.kend - u.kbegin);
+    }
+    if (total >= dec_workers * kDynMinWarpWork && longest >= kDynSkew * (total / dec_workers)) {
+      const int64_t max_len = total / dec_workers / 4 - kUnitOverhead;
+      std::vector<int32_t>& idx = hp->dyn_idx;
+      idx.clear();
+      for (size_t i = 0; i < dunits.size(); ++i) {
+        const int64_t len = dunits[i].kend - dunits[i].kbegin;
+        if (len > 0 && len <= max_len) idx.push_back(int32_t(i));
+      }
+      std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
+        return dunits[a].kend - dunits[a].kbegin < dunits[b].kend - dunits[b].kbegin;
+      });
+      const int64_t cap = int64_t(kDynShare * double(total));
+      int64_t pool = 0;
+      std::vector<uint8_t>& in_pool = hp->dyn_mark;
+      in_pool.assign(dunits.size(), 0);
+      for (int32_t i : idx) {
+        const int64_t c = dunits[i].kend - dunits[i].kbegin + kUnitOverhead;
+        if (pool + c > cap) break;
+        pool += c;
+        in_pool[size_t(i)] = 1;
+      }
+      size_t kept = 0;
+      for (size_t i = 0; i < dunits.size(); ++i) {
+        if (in_pool[i]) dyn.push_back(dunits[i]);
+        else dunits[kept++] = dunits[i];
+      }
+      dunits.resize(kept);
+    }
+  }
+  balance(dunits, dec_workers, std::max<int64_t>(page_size, kStageTokens), kUnitOverhead,
+          kMinPiece, kMinWarpWork, &hp->dec, &dec_k, kMinPieceSmall, kSplitOverhead);
+  hp->dec.n_dyn = 0;
+  hp->dec.dyn_begin = int32_t(hp->dec.items.size());
+  if (!dyn.empty()) {
+    // every warp of the grid takes run-time units, including ones without a list
+    WorkList& dl = hp->dec;
+    while (dl.workers < dec_workers) {
+      dl.ptr.push_back(dl.ptr.back());
+      ++dl.workers;
+    }
+    std::stable_sort(dyn.begin(), dyn.end(), [](const Unit& a, const Unit& b) {
+      return a.kend - a.kbegin > b.kend - b.kbegin;
+    });
+    // imbalance: the most planned (static) cost of a warp against the mean cost of all
+    // decode work per warp, run-time units included (below 1: they fill the rest)
+    int64_t mx = 0, all = 0;
+    for (int32_t w = 0; w < dl.workers; ++w) {
+      int64_t l = 0;
+      for (int32_t i = dl.ptr[w]; i < dl.ptr[w + 1]; ++i)
+        l += dl.items[i].tok1 - dl.items[i].tok0 + kUnitOverhead +
+             (dl.items[i].nchunks > 1 ? kSplitOverhead : 0);
+      mx = std::max(mx, l);
+      all += l;
+    }
+    for (const Unit& u : dyn) {
+      DecodeItem it{};
+      it.req = u.req;
+      it.kvh = u.kvh;
+      it.row0 = u.row0;
+      it.nrows = u.nrows;
+      it.tok0 = u.kbegin;
+      it.tok1 = u.kend;
+      it.slot = -1;
+      it.first_slot = -1;
+      it.nchunks = 1;
+      it.page_base = u.page_base;
+      it.q_row0 = u.q_row0;
+      it.qpos0 = u.qpos0;
+      dl.items.push_back(it);
+      all += u.kend - u.kbegin + kUnitOverhead;
+    }
+    dl.n_dyn = int32_t(dyn.size());
+    const double mean = double(all) / dl.workers;
+    dl.imbalance = mean > 0 ? double(mx) / mean : 1.0;
+  }
   balance_gangs(punits, num_sms, std::max<int64_t>(page_size, bsr::kPrefillKeyTile),
                 kPrefillOverhead, kPrefillMinPiece, kPrefillMinCtaWork, &hp->pre);
   hp->pmerge.clear();
@@ -641,7 +743,8 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
                                 window_left, page_pos, rope_theta, num_sms,
-                                decode_warps_per_sm(kv_dtype, rope), &hp);
+                                decode_warps_per_sm(kv_dtype, rope), kv_dtype == BSR_KV_DTYPE_BF16,
+                                &hp);
   if (rc != BSR_OK) return rc;
   const int64_t nnz = indptr[batch];
 
@@ -717,6 +820,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   const size_t off_page_pos = take(with_pos ? size_t(std::max<int64_t>(nnz, 1)) * 4 : 0);
   const size_t off_qshift = take(with_pos ? size_t(std::max(batch, 1)) * 4 : 0);
   const size_t off_error = take(16);
+  const size_t off_dyn_ctr = take(16);   // run-time queue: next unit, warps done (zeros)
   const size_t image_bytes = off;  // everything above is uploaded
   const size_t off_part_o = take(size_t(hp.dec.n_partials) * kMaxDecodeRows * head_dim * 4);
   const size_t off_part_lse = take(size_t(hp.dec.n_partials) * kMaxDecodeRows * 4);
@@ -757,6 +861,7 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   // every region is written below except the split-range counters and the status word
   std::memset(h + off_counters, 0, size_t(std::max(hp.dec.n_partials, 1)) * 4);
   std::memset(h + off_error, 0, 16);
+  std::memset(h + off_dyn_ctr, 0, 16);
   if (nnz > 0) std::memcpy(h + off_indices, indices, size_t(nnz) * 4);
   if (!hp.dec.items.empty())
     std::memcpy(h + off_items, hp.dec.items.data(), hp.dec.items.size() * sizeof(DecodeItem));
@@ -824,6 +929,9 @@ extern "C" int bsr_attn_plan(const int32_t* indptr, const int32_t* indices,
   s->off_items = off_items;
   s->off_warp_ptr = off_warp_ptr;
   s->off_counters = off_counters;
+  s->off_dyn_ctr = off_dyn_ctr;
+  s->n_dyn = hp.dec.n_dyn;
+  s->dyn_begin = hp.dec.dyn_begin;
   s->off_error = off_error;
   s->off_page_pos = with_pos ? off_page_pos : 0;
   s->off_qshift = with_pos ? off_qshift : 0;
@@ -911,7 +1019,8 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
   const int rc = make_host_plan(indptr, indices, last_page_len, batch, num_qo_heads, num_kv_heads,
                                 head_dim, page_size, qo_indptr, num_pages_in_pool, causal,
                                 window_left, page_pos, rope_theta, num_sms,
-                                decode_warps_per_sm(kv_dtype, rope_theta > 0.f), &hp);
+                                decode_warps_per_sm(kv_dtype, rope_theta > 0.f),
+                                kv_dtype == BSR_KV_DTYPE_BF16, &hp);
   if (rc != BSR_OK) return rc;
   if (info != nullptr) {
     std::memset(info, 0, sizeof(*info));
@@ -944,16 +1053,20 @@ extern "C" int bsr_attn_plan_host(const int32_t* indptr, const int32_t* indices,
   if (units != nullptr) {
     if (max_units < n) return BSR_ERR_INVALID_ARGUMENT;
     int64_t i_out = 0;
+    auto put = [&](const DecodeItem& it, int32_t col) {
+      int32_t* u = units + i_out * 8;
+      u[0] = it.req; u[1] = it.kvh; u[2] = it.row0; u[3] = it.nrows;
+      u[4] = it.tok0; u[5] = it.tok1; u[6] = it.slot; u[7] = col;
+      ++i_out;
+    };
     for (int pass = 0; pass < 2; ++pass) {
       const WorkList& wl = pass == 0 ? hp.dec : hp.pre;
       for (int32_t w = 0; w < wl.workers; ++w)
-        for (int32_t i = wl.ptr[w]; i < wl.ptr[w + 1]; ++i, ++i_out) {
-          const DecodeItem& it = wl.items[i];
-          int32_t* u = units + i_out * 8;
-          u[0] = it.req; u[1] = it.kvh; u[2] = it.row0; u[3] = it.nrows;
-          u[4] = it.tok0; u[5] = it.tok1; u[6] = it.slot; u[7] = pass == 0 ? w : -1 - w;
-        }
+        for (int32_t i = wl.ptr[w]; i < wl.ptr[w + 1]; ++i) put(wl.items[i], pass == 0 ? w : -1 - w);
     }
+    // run-time units: column decode warps + their place in the queue
+    for (int32_t k = 0; k < hp.dec.n_dyn; ++k)
+      put(hp.dec.items[size_t(hp.dec.dyn_begin + k)], hp.dec.workers + k);
   }
   return int(n);
 }

@@ -241,6 +241,9 @@ extern "C" int bsr_attn_run(bsr_schedule_t s, const void* q, const void* k_pages
     p.window_left = s->window_left;
     p.nhd = s->kv_layout == BSR_KV_NHD;
     p.plan_uploaded = 1;   // the work list and page table came with the plan's copy
+    p.n_dyn = smallp ? 0 : s->n_dyn;
+    p.dyn_begin = s->dyn_begin;
+    p.dyn_ctr = s->dev<int32_t>(s->off_dyn_ctr);
     p.wait_limit_ns = wait_limit_ns;
     const bool r16 = s->max_rows > 8;
     t_mark(0, 0);

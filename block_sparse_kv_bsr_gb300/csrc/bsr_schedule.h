@@ -32,6 +32,8 @@ struct bsr_schedule {
 
   // decode plan
   int32_t n_items = 0, n_partials = 0, n_split = 0, dec_warps = 0, dec_ctas = 0;
+  int32_t n_dyn = 0, dyn_begin = 0;   // run-time units (decode): count, first item
+  size_t off_dyn_ctr = 0;             // their queue counters in the workspace
   int32_t dec_warps_per_cta = 0;   // warps one decode CTA runs (one CTA per SM)
   double dec_imbalance = 0.0;
   // prefill plan (tensor-core kernel)

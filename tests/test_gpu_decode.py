@@ -112,6 +112,34 @@ def bits_t(x):
     return x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32)
 
 
+def test_run_time_units_match_the_oracle_and_repeat_bit_exact():
+    """A skewed batch large enough that the plan leaves its short ranges to run time
+    (warps take them from a queue once their own list is done): every output matches
+    the oracle, and repeated runs -- each with its own assignment of the queued ranges
+    to warps, the queue reset by the kernel between launches -- give the same bits."""
+    lens = [20000, 23000, 17500, 26000] + [16 + (37 * i) % 280 for i in range(160)]
+    w = wl.make_paged("dynq", 77, lens, Hq=32, Hk=8, D=128, P=16)
+    q, k, v = device_tensors(w)
+    s = plan(w)
+    info = s.info()
+    nwarps = info["decode_ctas"] * info["decode_warps_per_cta"]
+    ip, ix, lp = [np.ascontiguousarray(np.asarray(x).astype(np.int32))
+                  for x in (w.indptr, w.indices, w.last_page_len)]
+    _, units = bsr.bsr_attn_plan_host(ip, ix, lp, num_qo_heads=32, num_kv_heads=8, head_dim=128,
+                                      page_size=16, num_pages=w.num_pages,
+                                      num_sms=info["num_sms"])
+    assert (units[:, 7] >= nwarps).sum() > 500          # the queue is in use
+    outs = []
+    for _ in range(4):
+        out, lse = bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale)
+        torch.cuda.synchronize()
+        outs.append((bits_t(out).clone(), lse.clone()))
+    assert bsr.bsr_last_device_error(s) == 0
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    check_full(w, out, lse)
+
+
 def test_cuda_graph_capture_replays_identically():
     w = wl.config2(small=True)
     q, k, v = device_tensors(w)

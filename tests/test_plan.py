@@ -260,11 +260,51 @@ def test_ranges_are_cut_longest_first_in_unit_order():
                                          head_dim=128, page_size=P, num_pages=int(indptr[-1]),
                                          num_sms=4)
     assert info["num_split_streams"] > 0
-    seen = []
-    for req, kvh, *_ in units.tolist():
+    # ranges the plan leaves to run time (column >= the decode warps) come after every
+    # warp's list, also longest first
+    nwarps = info["decode_ctas"] * info["decode_warps_per_cta"]
+    seen, late = [], set()
+    for req, kvh, _, _, _, _, _, col in units.tolist():
+        if col >= nwarps:
+            late.add((req, kvh))
         if not seen or seen[-1] != (req, kvh):
             assert (req, kvh) not in seen, "a range's pieces are not consecutive"
             seen.append((req, kvh))
     expect = sorted(((b, h) for b in range(len(lens)) for h in range(Hk)),
-                    key=lambda u: (-lens[u[0]], u))
+                    key=lambda u: (u in late, -lens[u[0]], u))
     assert seen == expect
+
+
+def test_skewed_batch_leaves_short_ranges_to_run_time():
+    """On the skewed batch the shortest whole ranges (up to 15 % of the cost, each at most
+    a quarter of a warp's share) are left out of the static cut: they come after every
+    warp's list, unsplit, longest first.  Batches with RoPE, without a range several warps
+    long, or over an FP8 cache keep a fully static plan."""
+    w = wl.config3()
+    kw = dict(num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+              page_size=w.page_size, num_pages=w.num_pages, num_sms=152)
+    info, units = bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len, **kw)
+    check_coverage(w, units)
+    nwarps = info["decode_ctas"] * info["decode_warps_per_cta"]
+    late = units[units[:, 7] >= nwarps]
+    assert len(late) > 0 and (late[:, 6] == -1).all()
+    assert np.array_equal(late[:, 7], nwarps + np.arange(len(late)))       # queue order
+    lens = late[:, 5] - late[:, 4]
+    assert (np.diff(lens) <= 0).all() and lens.min() > 0
+    static = units[units[:, 7] < nwarps]
+    cost = lambda u: (u[:, 5] - u[:, 4] + 32).sum()
+    assert cost(late) <= 0.15 * (cost(late) + cost(static)) + 1
+    assert lens.max() <= (cost(late) + cost(static)) / nwarps / 4
+    # the reported imbalance is the largest static share against the mean of all work
+    assert info["decode_imbalance"] < 1.0
+    for extra in (dict(rope_theta=1e4), dict(kv_dtype="e4m3")):
+        info2, units2 = bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len, **extra, **kw)
+        n2 = info2["decode_ctas"] * info2["decode_warps_per_cta"]
+        assert (units2[:, 7] < n2).all()
+    u2 = wl.config2()
+    info2, units2 = bsr.bsr_attn_plan_host(u2.indptr, u2.indices, u2.last_page_len,
+                                           num_qo_heads=u2.num_qo_heads,
+                                           num_kv_heads=u2.num_kv_heads, head_dim=u2.head_dim,
+                                           page_size=u2.page_size, num_pages=u2.num_pages,
+                                           num_sms=152)
+    assert (units2[:, 7] < info2["decode_ctas"] * info2["decode_warps_per_cta"]).all()
