@@ -272,7 +272,8 @@ typedef struct bsr_schedule_info {
   int32_t num_sms;
   int64_t workspace_bytes;    /* device workspace of the schedule */
   int64_t upload_bytes;       /* bytes of the one host-to-device copy a plan makes */
-  double decode_imbalance;    /* max / mean planned cost over decode warps */
+  double decode_imbalance;    /* max planned cost of a decode warp / mean decode cost per
+                                 warp (run-time units counted in the mean only) */
   double prefill_imbalance;   /* max / mean planned cost over prefill CTAs */
   int32_t kernels_per_run;    /* kernels one bsr_attn_run launches (decode, prefill,
                                  split-range merge; 0 when there is no work) */
@@ -310,7 +311,10 @@ int bsr_schedule_stage_times(bsr_schedule_t schedule, int32_t call, float* ms);
  * `units` is non-NULL (capacity max_units rows) each unit is written as
  * int32[8]: request, kv head, first packed row, packed rows, first key, end key,
  * partial slot (-1 = unsplit), then the decode warp that runs it, or -1 - CTA for
- * a unit of the tensor-core prefill kernel.  Packed row R of
+ * a unit of the tensor-core prefill kernel, or -- for a whole range the plan leaves to
+ * run time (skewed bf16 batches without RoPE: warps that have finished their own lists
+ * take these from a queue, longest first) -- the number of decode warps plus its place
+ * in the queue.  Packed row R of
  * (request, kv head) is query R / (Hq/Hk), qo head kv_head * (Hq/Hk) +
  * R % (Hq/Hk).  All arrays are host arrays owned by the caller.  Use it to
  * inspect or test a schedule (coverage of every key, balance) without a device.
