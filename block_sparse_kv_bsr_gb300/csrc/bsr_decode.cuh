@@ -9,7 +9,11 @@
 //    workgroup that walks its own planned list of work units (request,
 //    kv head, packed-row group, page-aligned key chunk) — the load-balanced
 //    split of long sequences into pieces interleaved with short ones
-//    (section "벤치마크: FlashInfer는 얼마나 빠른가?").
+//    (section "벤치마크: FlashInfer는 얼마나 빠른가?").  For skewed batches the
+//    plan leaves the shortest whole ranges out of those lists: a warp that has
+//    finished its own list takes them one at a time from a shared queue (an
+//    atomic counter; the last warp of a launch resets it), so the warps that
+//    stream faster take more and the kernel does not wait for the slowest list.
 //  * Each warp feeds itself through a private ring of shared-memory stages:
 //    one elected lane issues TMA (cp.async.bulk.tensor) loads of the next
 //    16-token K and V tiles of the unit's pages, straight from the page ids
