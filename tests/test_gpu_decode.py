@@ -140,6 +140,44 @@ def test_run_time_units_match_the_oracle_and_repeat_bit_exact():
     check_full(w, out, lse)
 
 
+def _queued_batch(kind):
+    short = [16 + (37 * i) % 280 for i in range(160)]
+    if kind == "d64":
+        return wl.make_paged("dynq64", 78, [40000, 46000, 35000, 52000] + short * 2,
+                             Hq=16, Hk=4, D=64, P=16)
+    if kind == "nhd":
+        return wl.to_nhd(wl.make_paged("dynqn", 79, [20000, 23000, 17500, 26000] + short,
+                                       Hq=32, Hk=8, D=128, P=16))
+    if kind == "window":
+        return wl.sliding_window_decode("dynqw", 80, [20000, 23000, 17500, 26000] + short + short[:40],
+                                        4096, Hq=32, Hk=8, D=128, P=16)
+    return wl.make_paged("dynq64p", 81, [20000, 23000, 17500, 26000] + short, Hq=32, Hk=8,
+                         D=128, P=64)
+
+
+@pytest.mark.parametrize("kind", ["d64", "nhd", "window", "p64"])
+def test_run_time_units_in_every_kernel_variant(kind):
+    """The run-time unit queue with head_dim 64, token-major pages, a sliding window and
+    64-key pages: the plan queues ranges, results match the oracle and repeat bit-exact."""
+    w = _queued_batch(kind)
+    q, k, v = device_tensors(w)
+    s = plan(w)
+    info = s.info()
+    nwarps = info["decode_ctas"] * info["decode_warps_per_cta"]
+    _, units = bsr.bsr_attn_plan_host(w.indptr, w.indices, w.last_page_len,
+                                      num_qo_heads=w.num_qo_heads, num_kv_heads=w.num_kv_heads,
+                                      head_dim=w.head_dim, page_size=w.page_size,
+                                      num_pages=w.num_pages, num_sms=info["num_sms"],
+                                      window_left=w.window_left, kv_layout=w.kv_layout)
+    assert (units[:, 7] >= nwarps).sum() > 50
+    out1, lse1 = bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, causal=w.causal)
+    out2, lse2 = bsr.bsr_attn_run(s, q, k, v, sm_scale=w.sm_scale, causal=w.causal)
+    torch.cuda.synchronize()
+    assert bsr.bsr_last_device_error(s) == 0
+    assert torch.equal(bits_t(out1), bits_t(out2)) and torch.equal(lse1, lse2)
+    check_full(w, out2, lse2)
+
+
 def test_cuda_graph_capture_replays_identically():
     w = wl.config2(small=True)
     q, k, v = device_tensors(w)
