@@ -481,7 +481,7 @@ struct HostPlan {
   int64_t max_pos_end = 0;
   // working arrays, kept with the plan so that re-planning reuses their memory
   std::vector<int32_t> kv_len, qo_len, q_row0;
-  std::vector<Unit> dunits, punits, dyn_units;
+  std::vector<Unit> dunits, punits, dyn_units, dyn_sorted;
   std::vector<int32_t> dyn_idx;
   std::vector<uint8_t> dyn_mark;
 };
@@ -630,24 +630,40 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
     }
     if (total >= dec_workers * kDynMinWarpWork && longest >= kDynSkew * (total / dec_workers)) {
       const int64_t max_len = total / dec_workers / 4 - kUnitOverhead;
-      std::vector<int32_t>& idx = hp->dyn_idx;
-      idx.clear();
-      for (size_t i = 0; i < dunits.size(); ++i) {
-        const int64_t len = dunits[i].kend - dunits[i].kbegin;
-        if (len > 0 && len <= max_len) idx.push_back(int32_t(i));
-      }
-      std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
-        return dunits[a].kend - dunits[a].kbegin < dunits[b].kend - dunits[b].kbegin;
-      });
       const int64_t cap = int64_t(kDynShare * double(total));
-      int64_t pool = 0;
       std::vector<uint8_t>& in_pool = hp->dyn_mark;
       in_pool.assign(dunits.size(), 0);
-      for (int32_t i : idx) {
-        const int64_t c = dunits[i].kend - dunits[i].kbegin + kUnitOverhead;
-        if (pool + c > cap) break;
-        pool += c;
-        in_pool[size_t(i)] = 1;
+      if (max_len > 0 && max_len <= (int64_t(1) << 22)) {
+        // shortest first, equal lengths in unit order: count by length, find the longest
+        // length taken whole and how many of the next length still fit, then mark
+        std::vector<int32_t>& cnt = hp->dyn_idx;
+        cnt.assign(size_t(max_len) + 1, 0);
+        for (const Unit& u : dunits) {
+          const int64_t len = u.kend - u.kbegin;
+          if (len > 0 && len <= max_len) ++cnt[size_t(len)];
+        }
+        int64_t pool = 0, cut_len = max_len + 1, cut_n = 0;
+        for (int64_t len = 1; len <= max_len; ++len) {
+          const int64_t c = len + kUnitOverhead, n = cnt[size_t(len)];
+          if (n == 0) continue;
+          if (pool + c * n <= cap) {
+            pool += c * n;
+            continue;
+          }
+          cut_len = len;
+          cut_n = (cap - pool) / c;
+          break;
+        }
+        for (size_t i = 0; i < dunits.size(); ++i) {
+          const int64_t len = dunits[i].kend - dunits[i].kbegin;
+          if (len <= 0 || len > max_len || len > cut_len) continue;
+          if (len < cut_len) {
+            in_pool[i] = 1;
+          } else if (cut_n > 0) {
+            in_pool[i] = 1;
+            --cut_n;
+          }
+        }
       }
       size_t kept = 0;
       for (size_t i = 0; i < dunits.size(); ++i) {
@@ -668,9 +684,18 @@ int make_host_plan(const int32_t* indptr, const int32_t* indices, const int32_t*
       dl.ptr.push_back(dl.ptr.back());
       ++dl.workers;
     }
-    std::stable_sort(dyn.begin(), dyn.end(), [](const Unit& a, const Unit& b) {
-      return a.kend - a.kbegin > b.kend - b.kbegin;
-    });
+    // longest first, equal lengths in unit order (a counting sort: every length is at
+    // most a quarter of a warp's share)
+    int64_t lmax = 0;
+    for (const Unit& u : dyn) lmax = std::max<int64_t>(lmax, u.kend - u.kbegin);
+    std::vector<int32_t>& pos = hp->dyn_idx;
+    pos.assign(size_t(lmax) + 2, 0);
+    for (const Unit& u : dyn) ++pos[size_t(lmax - (u.kend - u.kbegin)) + 1];
+    for (size_t k = 1; k < pos.size(); ++k) pos[k] += pos[k - 1];
+    std::vector<Unit>& sorted = hp->dyn_sorted;
+    sorted.resize(dyn.size());
+    for (const Unit& u : dyn) sorted[size_t(pos[size_t(lmax - (u.kend - u.kbegin))]++)] = u;
+    dyn.swap(sorted);
     // imbalance: the most planned (static) cost of a warp against the mean cost of all
     // decode work per warp, run-time units included (below 1: they fill the rest)
     int64_t mx = 0, all = 0;
